@@ -1,0 +1,52 @@
+"""Dense brute-force attention for pinning the oracle (tests only).
+
+Decodes bytes with torch's own bf16 / float8_e4m3fn conversions (not the
+oracle's decoders), gathers each request's K/V rows densely through the block
+table, and applies scipy's softmax / logsumexp to the full score matrix.
+"""
+import numpy as np
+import torch
+from scipy.special import logsumexp, softmax
+
+
+def decode_bf16(u16: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def decode_e4m3(u8: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(u8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def values(h: dict, key: str) -> np.ndarray:
+    a = h[key]
+    return decode_e4m3(a) if a.dtype == np.uint8 else decode_bf16(a)
+
+
+def dense_attention(h: dict, num_q_heads: int, num_kv_heads: int, sm_scale: float, page: int = 64):
+    q = values(h, "q")
+    if h.get("q_scale") is not None:
+        q = q * h["q_scale"].astype(np.float64)[..., None]
+    k = values(h, "k_pages")
+    v = values(h, "v_pages")
+    if h.get("k_scale") is not None:
+        k = k * h["k_scale"].astype(np.float64)[..., None]
+        v = v * h["v_scale"].astype(np.float64)[..., None]
+    B = h["seq_lens"].shape[0]
+    G = num_q_heads // num_kv_heads
+    d = q.shape[-1]
+    out = np.zeros((B, num_q_heads, d))
+    lse = np.full((B, num_q_heads), -np.inf)
+    for b in range(B):
+        n = int(h["seq_lens"][b])
+        if n <= 0:
+            continue
+        pages = h["block_table"][b, : (n + page - 1) // page]
+        kb = k[pages].transpose(1, 0, 2, 3).reshape(num_kv_heads, -1, d)[:, :n]  # [Hkv, n, d]
+        vb = v[pages].transpose(1, 0, 2, 3).reshape(num_kv_heads, -1, d)[:, :n]
+        for j in range(num_q_heads):
+            s = sm_scale * (kb[j // G] @ q[b, j])
+            out[b, j] = softmax(s) @ vb[j // G]
+            lse[b, j] = logsumexp(s)
+    return out, lse
