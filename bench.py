@@ -1,0 +1,406 @@
+"""Benchmark: load-balanced paged-KV decode attention on GB300.
+
+One step = one pass of the hot path over one decode batch: plan (task map) ->
+persistent decode -> combine, on the mixed-length workload (batch 32, KV lengths
+log-uniform 128-32768, 64 q / 8 KV heads, head_dim 128, page 64, bf16, 148
+persistent CTAs).  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference] [--workload NAME]
+
+value: achieved KV GB/s over the whole step (algorithmic KV bytes / step time),
+summed over ranks; us_per_step is the same measurement as time.  L2 (129 MB) is
+flushed by writing a 2 x L2 buffer before every timed step, outside the timed
+events.  N > 1 runs independent replicas (one per GPU, no data-path collective).
+--impl reference times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "decode attention µs/step and KV GB/s (% of GB300 HBM peak) on mixed-length batches"
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, tagged with host time."""
+
+    def __init__(self, uuid: str | None):
+        self.samples = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not inside:  # timed region shorter than the sampling period: nearest samples
+            inside = [s for t, s in self.samples if t0 - 1.0 <= t <= t1 + 1.0]
+            window = "timed+-1s"
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in inside:
+            try:
+                sm.append(float(s[1]))
+                mx.append(float(s[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, s[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm), "window": window}
+
+
+def flush_buffer(device):
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    return torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
+
+
+def kv_bytes(inp):
+    return workloads.kv_bytes(inp["seq_lens"].cpu().numpy(), inp["num_kv_heads"], inp["kv_dtype"])
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def bench_ours(args, device, rank, world):
+    import load_balanced_paged_gb300 as dsa
+
+    name = args.workload
+    w = workloads.WORKLOADS[name]
+    inp = workloads.make_workload(name, device=device, seed=w.seed + rank)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    C = w.ctas or sms
+    m = args.min_tiles
+    B, hq, hkv = w.batch, w.num_q_heads, w.num_kv_heads
+    G = hq // hkv
+    tm = dsa.TaskMap(B, hkv, C, device)
+    po, pl = dsa.partial_buffers(tm.max_descs, G, device)
+    out = torch.empty(B, hq, 128, dtype=torch.bfloat16, device=device)
+    out_lse = torch.empty(B, hq, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    kw = dict(q_scale=inp["q_scale"], k_scale=inp["k_scale"], v_scale=inp["v_scale"])
+
+    def plan():
+        dsa.plan(inp["seq_lens"], hkv, C, m, task_map=tm, stream=stream)
+
+    def decode():
+        dsa.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
+                   inp["sm_scale"], partial_o=po, partial_lse=pl, stream=stream, **kw)
+
+    def combine():
+        dsa.combine(tm, po, pl, hq, out=out, out_lse=out_lse, stream=stream)
+
+    flush = flush_buffer(device)
+    nbytes = kv_bytes(inp)
+
+    def timed(fns, steps, warmup):
+        """Per-step CUDA events around each fn; L2 flushed before each step, untimed."""
+        for _ in range(warmup):
+            flush.fill_(1.0)
+            for f in fns:
+                f()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)] for _ in range(steps)]
+        for k in range(steps):
+            flush.fill_(float(k))
+            ev[k][0].record(stream)
+            for i, f in enumerate(fns):
+                f()
+                ev[k][i + 1].record(stream)
+        stream.synchronize()
+        per = np.array([[ev[k][i].elapsed_time(ev[k][i + 1]) for i in range(len(fns))] for k in range(steps)])
+        return per  # ms, [steps, len(fns)]
+
+    # warm-up + correctness gate of this configuration (status word must be clean)
+    timed([plan, decode, combine], 1, args.warmup)
+    torch.cuda.synchronize()
+    status = dsa.get_status(tm)
+    if status != 0:
+        raise RuntimeError(f"device status {status} on the bench workload")
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.get_device_properties(device).uuid and
+                          "GPU-" + str(torch.cuda.get_device_properties(device).uuid))
+    time.sleep(0.3)
+    t_wall0 = time.time()
+    per = timed([plan, decode, combine], args.steps, 0)
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.stop()
+    clk = clocks.summary(t_wall0, t_wall1)
+
+    step_ms = per.sum(axis=1)
+    total_ms = float(step_ms.sum())
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    t_plan, t_dec, t_comb = (float(x) for x in per.mean(axis=0))
+
+    # static split-KV comparison on the same inputs (decode + its combine)
+    static = {}
+    max_len = int(inp["seq_lens"].max().item())
+    for label, mode, param in (("static_16_splits", 0, 16), ("static_4096_chunk", 1, 4096)):
+        S = dsa.static_num_splits(mode, param, max_len)
+        spo, spl = dsa.partial_buffers(B * hkv * S, G, device)
+        sst = torch.zeros(1, dtype=torch.int32, device=device)
+
+        def sdec(mode=mode, param=param, spo=spo, spl=spl, sst=sst):
+            dsa.static_splitkv(mode, param, max_len, inp["q"], inp["k_pages"], inp["v_pages"],
+                               inp["block_table"], inp["seq_lens"], hkv, inp["sm_scale"], partial_o=spo,
+                               partial_lse=spl, status=sst, stream=stream, **kw)
+
+        def scomb(S=S, spo=spo, spl=spl):
+            dsa.static_combine(S, spo, spl, B, hq, hkv, out=out, out_lse=out_lse, stream=stream)
+
+        sp = timed([sdec, scomb], max(10, min(args.steps, 200)), 3)
+        if dsa.read_status(sst) != 0:
+            raise RuntimeError(f"{label}: device status set")
+        s_ms = float(sp.sum(axis=1).mean())
+        static[label] = {"splits": S, "us_per_step": round(s_ms * 1e3, 2),
+                         "speedup_of_dynamic": round(s_ms / (t_dec + t_comb), 3)}
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    host = {k: inp[k].cpu().pin_memory() for k in ("q", "q_scale", "k_pages", "v_pages", "k_scale", "v_scale",
+                                                   "block_table", "seq_lens") if inp[k] is not None}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(out_lse.shape, dtype=out_lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for k, t in host.items():
+            inp[k].copy_(t, non_blocking=True)
+        plan()
+        decode()
+        combine()
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(out_lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    e1.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    peak, peak_src = measured_peaks()
+    achieved = nbytes / (t_dec * 1e-3) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": round(world * nbytes / (ms_per_step * 1e-3) / 1e9, 2),
+        "unit": "GB/s",
+        "us_per_step": round(ms_per_step * 1e3, 2),
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3",
+        "data": "synthetic (seeded; lengths, page permutation and N(0,1) values drawn as in workloads.py)",
+        "config": {"workload": w.description, "name": name, "batch": B, "num_q_heads": hq, "num_kv_heads": hkv,
+                   "head_dim": 128, "page_size": 64, "persistent_ctas": C, "min_tiles_per_split": m,
+                   "kv_bytes_per_step": nbytes, "l2": "flushed (2 x L2 write) before every timed step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "breakdown_us": {"plan": round(t_plan * 1e3, 2), "decode": round(t_dec * 1e3, 2),
+                         "combine": round(t_comb * 1e3, 2)},
+        "kv_gbs_decode_plus_combine": round(nbytes / ((t_dec + t_comb) * 1e-3) / 1e9, 1),
+        "pct_of_nominal_8tbs": round(100 * nbytes / (ms_per_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 1),
+        "static": static,
+        "roofline": {"bound": "hbm", "kernel": "attn_kernel (persistent decode)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "traffic": None},
+        "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "us_per_step": round(e2e_ms * 1e3, 1), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    return res, inp, nbytes
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+
+def oracle_problem(inp, requests):
+    """Host copy (exact bytes) of the listed requests with their pages renumbered."""
+    import oracle
+
+    def np_bytes(t):
+        t = t.detach().cpu().contiguous()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+    lens = inp["seq_lens"][requests].cpu().numpy()
+    npages = [(int(n) + 63) // 64 for n in lens]
+    idx = torch.cat([inp["block_table"][b, :n] for b, n in zip(requests, npages)]).long()
+    pools = {k: (None if inp[k] is None else np_bytes(inp[k].index_select(0, idx)))
+             for k in ("k_pages", "v_pages", "k_scale", "v_scale")}
+    bt = np.full((len(requests), max(max(npages), 1)), -1, np.int32)
+    off = 0
+    for i, n in enumerate(npages):
+        bt[i, :n] = np.arange(off, off + n)
+        off += n
+    qs = None if inp["q_scale"] is None else np_bytes(inp["q_scale"][requests])
+    return oracle.Problem(np_bytes(inp["q"][requests]), pools["k_pages"], pools["v_pages"], bt, lens,
+                          inp["num_q_heads"], inp["num_kv_heads"], inp["sm_scale"], q_scale=qs,
+                          k_scale=pools["k_scale"], v_scale=pools["v_scale"]), lens
+
+
+def cpu_oracle_rate(inp, budget_s: float, rng_seed: int = 0):
+    """Time the oracle (all host threads) on a bounded sample of requests; returns
+    (GB/s of KV processed, threads, description)."""
+    import oracle
+    lens = inp["seq_lens"].cpu().numpy()
+    rng = np.random.default_rng(rng_seed)
+    order = rng.permutation(len(lens))
+    # calibrate on the shortest request, then take requests until the estimated time fills the budget
+    threads = oracle.default_threads()
+    prob, _ = oracle_problem(inp, [int(np.argmin(lens))])
+    t0 = time.perf_counter()
+    prob.attention()
+    per_token = (time.perf_counter() - t0) / max(int(lens.min()), 1)
+    # the oracle runs one thread per (request, KV head) unit
+    eff = min(threads, inp["num_kv_heads"] * len(lens))
+    chosen, est = [], 0.0
+    for b in order:
+        chosen.append(int(b))
+        est += per_token * lens[b] * inp["num_kv_heads"] / eff
+        if est >= budget_s:
+            break
+    prob, sl = oracle_problem(inp, chosen)
+    t0 = time.perf_counter()
+    prob.attention()
+    dt = time.perf_counter() - t0
+    nbytes = workloads.kv_bytes(sl, inp["num_kv_heads"], inp["kv_dtype"])
+    desc = (f"{len(chosen)} of {len(lens)} requests ({int(sl.sum())} of {int(lens.sum())} tokens), "
+            f"fp64 oracle, {dt:.1f} s")
+    return nbytes / dt / 1e9, threads, desc
+
+
+# ---------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixed", choices=list(workloads.WORKLOADS))
+    ap.add_argument("--min-tiles", type=int, default=4)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        bench_reference(args)
+        return
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    res, inp, nbytes = bench_ours(args, device, rank, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, desc = cpu_oracle_rate(inp, args.cpu_budget)
+        res["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                               "sample": desc}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bench_reference(args):
+    """The fp64 CPU oracle as the reference arm: W + K steps, each a bounded sample."""
+    import oracle
+    name = args.workload
+    w = workloads.WORKLOADS[name]
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    inp = workloads.make_workload(name, device=dev)
+    per_step = max(0.5, 150.0 / (args.steps + args.warmup))
+    rates = []
+    desc = ""
+    for k in range(args.warmup + args.steps):
+        v, cores, desc = cpu_oracle_rate(inp, per_step, rng_seed=k)
+        if k >= args.warmup:
+            rates.append(v)
+    v = float(np.mean(rates))
+    nbytes = kv_bytes(inp)
+    us = nbytes / (v * 1e9) * 1e6
+    res = {"metric": METRIC, "value": round(v, 4), "unit": "GB/s", "us_per_step": round(us, 1),
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded, as in workloads.py)",
+           "config": {"workload": w.description, "name": name},
+           "impl": "reference",
+           "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": oracle.default_threads(),
+                            "kind": "oracle", "sample": f"per step: {desc}"},
+           "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,227 @@
+/*
+ * dsa.h -- C ABI of libdsa: load-balanced, variable-length, paged-KV GQA decode
+ * attention for GB300 (sm_103a), scheduled by a per-step task map.
+ *
+ * The operation (sources are web pages; section names as printed on them):
+ *   HPC-Ops × SGLang blog (news.paixiangai.cn), "Attention：变长 decode 的负载均衡":
+ *     decode attention work grows with each request's live KV length; a static
+ *     split-KV grid over (KV head, request, chunk) either uses a fixed split
+ *     count (long requests make heavy chunks and a tail) or a fixed chunk size
+ *     (the grid reserves splits for the longest request, short ones leave empty
+ *     chunks).
+ *   Same page, "围绕活跃 KV 工作进行调度": an assign kernel builds a global task
+ *     map from the live device-side KV lengths once per decode step (reused by
+ *     every layer): 64-token tiles, total over heads and requests, per-CTA budget
+ *     = total / persistent CTAs, bins filled up to the budget then spilled, with
+ *     a minimum-work floor.  Each resident CTA drains its bin; each descriptor
+ *     covers one or more contiguous KV tiles of one (request, head) and yields a
+ *     partial output with its log-sum-exp; a combine kernel merges the actual
+ *     number of partials per (request, head) under the global softmax.
+ *   Hy3 preview write-up (m.youleyou.com), 2.1.1 "Attention动态调度": the same
+ *     scheme as uniform tiles, greedy bin packing, a task map generated before
+ *     each step, and a combine kernel.
+ *
+ * Conventions for every call:
+ *   - All array arguments are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or synchronises (dsa_get_status and
+ *     dsa_read_status excepted).  Work is enqueued on `stream` (a cudaStream_t;
+ *     NULL = the legacy default stream) and returns before it runs.
+ *   - Shapes: B = batch, Hq = query heads, Hkv = KV heads, G = Hq / Hkv query
+ *     heads per KV head (query head j reads KV head j / G), d = head_dim = 128,
+ *     P = page_size = 64 tokens = the tile.  Unit u = (request b, KV head h),
+ *     u = b * Hkv + h.
+ *   - Layouts (row-major, innermost last):
+ *       q            [B, Hq, d]              bf16, or E4M3 bytes
+ *       q_scale      [B, Hq] fp32            E4M3 Q only: real = e4m3 * scale
+ *       k/v_pages    [num_pages, Hkv, P, d]  bf16, or E4M3 bytes; one
+ *                                            (page, KV head) block is contiguous
+ *       k/v_scale    [num_pages, Hkv, P] fp32  E4M3 K/V only, per token and head
+ *       block_table  [B, max_pages_per_req] int32; token t of request b is slot
+ *                    t % P of page block_table[b][t / P]; entries at or past
+ *                    ceil(seq_lens[b] / P) are never read
+ *       seq_lens     [B] int32, live KV length of each request (0 allowed)
+ *       out          [B, Hq, d] bf16 or fp32;  out_lse [B, Hq] fp32
+ *   - Log-sum-exp values are natural logarithms of sum_t exp(s_t), with
+ *     s_t = sm_scale * q . k_t already scaled; an empty request has lse = -inf
+ *     and output 0.
+ *   - Pointers to q, k/v pages, scales and partials must be 16-byte aligned.
+ *   - Host-side checks fail with DSA_ERR_INVALID_ARG / DSA_ERR_UNSUPPORTED /
+ *     DSA_ERR_BUFFER_TOO_SMALL before anything is launched; a failed launch
+ *     returns DSA_ERR_CUDA.  Bad device-resident input (a negative length, a
+ *     length beyond max_pages_per_req * P, a page id outside [0, num_pages))
+ *     cannot be seen from the host: the kernels set a bit in a device status
+ *     word (DSA_DEV_* below), skip the affected work and never trap.
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *dsa_stream; /* same type as cudaStream_t */
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1,      /* null pointer, bad size, inconsistent shapes */
+    DSA_ERR_UNSUPPORTED = 2,      /* valid but not built: head_dim != 128, P != 64, G > 8, ... */
+    DSA_ERR_BUFFER_TOO_SMALL = 3, /* a caller buffer is smaller than the call needs */
+    DSA_ERR_CUDA = 4,             /* a CUDA runtime/driver call or a launch failed */
+    DSA_ERR_DEVICE_INPUT = 5      /* returned by dsa_get_status when a DSA_DEV_* bit is set */
+} dsa_status;
+
+/* Bits of the device status word (task map meta[3], or the static path's word). */
+#define DSA_DEV_BAD_SEQLEN 1   /* seq_len < 0, > max_pages_per_req * P, or not covered by the grid */
+#define DSA_DEV_BAD_PAGE 2     /* block_table entry outside [0, num_pages) */
+#define DSA_DEV_TIMEOUT 4      /* an in-kernel pipeline wait passed its time limit; work abandoned */
+#define DSA_DEV_BAD_MAP 8      /* task map inconsistent with the decode arguments */
+
+typedef enum { DSA_BF16 = 0, DSA_FP8_E4M3 = 1, DSA_FP32 = 2 } dsa_dtype;
+
+/*
+ * Task map: the per-step schedule ("全局任务映射" in the blog's "围绕活跃 KV
+ * 工作进行调度").  Caller-allocated device buffers; dsa_plan fills them.
+ *   cta_desc_begin [num_ctas + 1]: the descriptors of bin (CTA) i are
+ *       [cta_desc_begin[i], cta_desc_begin[i+1]).
+ *   descs [max_descs * 4]: {u, t0, t1, k}: tiles [t0, t1) (64-token tiles,
+ *       local to unit u), k = index of the descriptor among u's descriptors.
+ *       Descriptor index = partial-output slot.
+ *   unit_partial_begin [num_units], unit_num_partials [num_units]: the slots
+ *       of unit u are [begin, begin + count); count = 0 for an empty unit.
+ *   meta [4]: {T = total tiles, C_eff = bins in use, num_descs, status}.
+ */
+typedef struct {
+    int32_t *cta_desc_begin;
+    int32_t *descs;
+    int32_t *unit_partial_begin;
+    int32_t *unit_num_partials;
+    int32_t *meta;
+    int32_t max_descs; /* capacity of descs, in descriptors */
+    int32_t num_ctas;  /* persistent CTAs = bins */
+    int32_t num_units; /* B * Hkv the map is sized for */
+} dsa_task_map;
+
+/*
+ * Capacity bound for the task map: every bin boundary cuts at most one unit,
+ * so a map never holds more than B*Hkv + num_ctas - 1 descriptors.  Size
+ * descs, partial_o ([max_descs, G, d] fp32) and partial_lse ([max_descs, G]
+ * fp32) from it.  Returns -1 on a non-positive or overflowing argument.
+ */
+int32_t dsa_max_descs(int32_t batch, int32_t num_kv_heads, int32_t num_ctas);
+
+/*
+ * dsa_plan -- the assign step (blog, "围绕活跃 KV 工作进行调度"; Hy3 write-up
+ * 2.1.1 "贪心装桶"), run on the device from device-resident lengths so that it
+ * needs no host synchronisation and can be captured in a CUDA graph.
+ *   n_u = ceil(len_b / tile) for u = b*Hkv + h; T = sum n_u (walked b-major,
+ *   then h, then tile); C_eff = min(num_persistent_ctas, max(1, T /
+ *   min_tiles_per_split)) (0 when T = 0); bin i gets the global tiles
+ *   [floor(i*T/C_eff), floor((i+1)*T/C_eff)), i.e. bins filled up to the
+ *   real-valued budget T/C_eff then spilled; each bin is cut at unit boundaries
+ *   into descriptors.  One CTA; the result is unique and bit-exact.
+ * Arguments: seq_lens [batch] device int32; tile must be 64; min_tiles_per_split
+ * >= 1; map->num_ctas must equal num_persistent_ctas, map->num_units must equal
+ * batch*num_kv_heads, map->max_descs >= dsa_max_descs(...).  B*Hkv <= 16384.
+ * A negative length counts as zero tiles and sets DSA_DEV_BAD_SEQLEN in meta[3];
+ * dsa_plan resets meta[3] for the step.
+ */
+dsa_status dsa_plan(const int32_t *seq_lens, int32_t batch, int32_t num_kv_heads,
+                    int32_t num_persistent_ctas, int32_t tile, int32_t min_tiles_per_split,
+                    const dsa_task_map *map, dsa_stream stream);
+
+/*
+ * dsa_decode -- the persistent attention kernel (blog, "围绕活跃 KV 工作进行调度":
+ * each resident CTA drains its bin; for each descriptor it computes attention
+ * over the descriptor's contiguous tiles and writes a partial output with its
+ * log-sum-exp).  Grid = map->num_ctas CTAs, one per bin.  Each KV tile is read
+ * once and serves all G query heads of its KV head (GQA).
+ *   For descriptor x = {u, t0, t1, k} (b = u / Hkv, h = u % Hkv) and each of the
+ *   G query heads j = h*G + g, over the tokens t in [64*t0, min(64*t1, len_b)):
+ *     s_t = sm_scale * q_j . k_t    (FP8: * q_scale[b][j] * k_scale[t])
+ *     partial_lse[x][g] = ln sum_t exp(s_t)
+ *     partial_o[x][g][:] = sum_t exp(s_t - partial_lse) * v_t  (FP8: * v_scale[t])
+ * Supported: (q_dtype, kv_dtype) = (BF16, BF16) or (FP8_E4M3, FP8_E4M3);
+ * head_dim 128; page_size 64; 1 <= G <= 8.  q_scale is required for FP8 Q,
+ * k_scale/v_scale for FP8 K/V, otherwise ignored.  partial_o holds
+ * [map->max_descs, G, 128] fp32, partial_lse [map->max_descs, G] fp32.
+ * Device input errors set bits in map->meta[3] (see above).
+ */
+dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *q_scale,
+                      const void *k_pages, const void *v_pages, dsa_dtype kv_dtype,
+                      const float *k_scale, const float *v_scale,
+                      const int32_t *block_table, int32_t max_pages_per_req, int32_t num_pages,
+                      const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                      int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
+                      const dsa_task_map *map, float *partial_o, float *partial_lse,
+                      dsa_stream stream);
+
+/*
+ * dsa_combine -- the combine kernel (blog, "围绕活跃 KV 工作进行调度": reads the
+ * actual number of partials of each (request, head) and merges them under the
+ * global softmax normalisation; Hy3 write-up 2.1.1 "Combine Kernel"):
+ *   L = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - L) * o_k
+ * over unit u's slots [unit_partial_begin[u], + unit_num_partials[u]).
+ * out: [B, Hq, 128] in out_dtype (DSA_BF16, round to nearest even, or DSA_FP32);
+ * out_lse: [B, Hq] fp32, may be NULL.  A unit with no partials gives out = 0,
+ * lse = -inf.
+ */
+dsa_status dsa_combine(const dsa_task_map *map, const float *partial_o, const float *partial_lse,
+                       int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                       void *out, dsa_dtype out_dtype, float *out_lse, dsa_stream stream);
+
+/*
+ * Static split-KV, the in-run comparison (blog, "Attention：变长 decode 的负载
+ * 均衡", its two forms).  Grid (S, Hkv, B), one CTA per (split, unit), the same
+ * per-tile engine as dsa_decode.  Unit u with n_u tiles:
+ *   mode 0 (fixed split count, param = S): c = ceil(n_u / S) tiles per split;
+ *   mode 1 (fixed chunk, param = chunk tokens, a multiple of 64):
+ *           c = param / 64, S = ceil(max_seq_len / param), max_seq_len given by
+ *           the host (the static grid must be sized for the longest request).
+ *   split s covers tiles [s*c, min((s+1)*c, n_u)); an empty split writes
+ *   o = 0, lse = -inf.  Slot of (u, s) = u*S + s.
+ * dsa_static_num_splits returns S (or -1 on bad arguments).
+ * partial_o: [B*Hkv*S, G, 128] fp32, partial_lse: [B*Hkv*S, G] fp32.
+ * status: device int32 word for DSA_DEV_* bits (may be NULL); a request longer
+ * than S*param in mode 1 is not covered and sets DSA_DEV_BAD_SEQLEN.
+ */
+int32_t dsa_static_num_splits(int32_t mode, int32_t param, int32_t max_seq_len);
+dsa_status dsa_static_splitkv(int32_t mode, int32_t param, int32_t max_seq_len,
+                              const void *q, dsa_dtype q_dtype, const float *q_scale,
+                              const void *k_pages, const void *v_pages, dsa_dtype kv_dtype,
+                              const float *k_scale, const float *v_scale,
+                              const int32_t *block_table, int32_t max_pages_per_req,
+                              int32_t num_pages, const int32_t *seq_lens, int32_t batch,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t page_size, float sm_scale, float *partial_o,
+                              float *partial_lse, int32_t *status, dsa_stream stream);
+
+/*
+ * Combine for the static grid: merges all S slots of each unit, empty ones
+ * included (they carry lse = -inf).  Same formula and outputs as dsa_combine.
+ */
+dsa_status dsa_static_combine(int32_t num_splits, const float *partial_o, const float *partial_lse,
+                              int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, void *out, dsa_dtype out_dtype, float *out_lse,
+                              dsa_stream stream);
+
+/*
+ * Status readback.  dsa_read_status copies one device status word to
+ * *host_status after synchronising the device; dsa_get_status does the same
+ * for map->meta[3].  Both return DSA_OK when the word is 0,
+ * DSA_ERR_DEVICE_INPUT when any DSA_DEV_* bit is set, DSA_ERR_CUDA if the copy
+ * fails, DSA_ERR_INVALID_ARG for NULL pointers.
+ */
+dsa_status dsa_read_status(const int32_t *device_status, int32_t *host_status);
+dsa_status dsa_get_status(const dsa_task_map *map, int32_t *host_status);
+
+/* Static string naming a dsa_status value. */
+const char *dsa_status_string(dsa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H */

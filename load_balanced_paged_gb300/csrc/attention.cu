@@ -1,0 +1,722 @@
+// Paged-KV GQA decode attention over 64-token tiles, in two schedules:
+//   - persistent (dsa_decode): one CTA per task-map bin drains its descriptors
+//     (HPC-Ops × SGLang blog, section "围绕活跃 KV 工作进行调度");
+//   - static split-KV (dsa_static_splitkv): one CTA per (split, KV head, request)
+//     on a fixed grid (same blog, section "Attention：变长 decode 的负载均衡").
+// Both run the same per-tile engine.
+//
+// Engine (per CTA):
+//   * one producer warp walks the descriptors, reads the page ids of the tiles
+//     from the block table (32 at a time, one per lane) and streams each
+//     (page, KV head) K and V block -- contiguous 16 KB (bf16) / 8 KB (E4M3) --
+//     into a ring of shared-memory stages with TMA (cp.async.bulk.tensor, 128-byte
+//     swizzle), completion counted on mbarriers; E4M3 scales and Q come by bulk copy;
+//   * GROUPS groups of 4 consumer warps take alternate tiles; warp w of a group
+//     owns tokens [16w, 16w+16) of its tile.  One KV tile feeds all G <= 8 query
+//     heads of its KV head (GQA: the KV stream is read once):
+//       S^T[16 tok x 8 heads] = K[16 x 128] . Q^T   (mma.sync m16n8k16 bf16 or
+//                                                    m16n8k32 e4m3, fp32 accumulate)
+//       online softmax in base 2, fp32, per warp and head
+//       O^T[128 x 8] += V^T[128 x 16] . P^T         (P transposed in registers
+//                                                    with movmatrix)
+//     bf16: P is split into a bf16 high part and a bf16 residual, two MMAs, so the
+//     probabilities carry ~16 bits; E4M3: V is converted exactly to f16 in registers
+//     and P (times the per-token V scale) is f16;
+//   * at the end of a descriptor the warps' (m, l, O) are merged in shared memory
+//     and written as a normalised fp32 partial with its natural-log LSE.
+// Every wait is bounded (a few seconds of %globaltimer); on expiry the CTA sets
+// DSA_DEV_TIMEOUT, stops, lets its in-flight copies land and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct KernelParams {
+    const uint8_t *q;
+    const float *q_scale;
+    const float *k_scale;
+    const float *v_scale;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    int32_t max_pages, num_pages, hq, hkv, G, num_units, max_slots;
+    float score_scale;  // sm_scale * log2(e)
+    // persistent schedule
+    const int32_t *cta_desc_begin;
+    const int4 *descs;
+    // static schedule
+    int32_t static_mode, static_tiles, num_splits;
+    float *partial_o;
+    float *partial_lse;
+    int32_t *status;
+};
+
+template <int KV>
+struct Cfg;
+template <>
+struct Cfg<0> {  // bf16 K/V and Q
+    static constexpr int kTileBytes = kTile * kHeadDim * 2;
+    static constexpr int kScaleBytes = 0;
+    static constexpr int kQHeadBytes = kHeadDim * 2;
+};
+template <>
+struct Cfg<1> {  // E4M3 K/V and Q, fp32 scales
+    static constexpr int kTileBytes = kTile * kHeadDim;
+    static constexpr int kScaleBytes = kTile * 4;
+    static constexpr int kQHeadBytes = kHeadDim;
+};
+
+constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
+
+template <int KV, int STAGES, int GROUPS>
+struct Layout {
+    static constexpr int kNcw = GROUPS * 4;  // consumer warps
+    static constexpr int kThreads = (kNcw + 1) * 32;
+    static constexpr int kStageTx = 2 * Cfg<KV>::kTileBytes + 2 * Cfg<KV>::kScaleBytes;
+    static constexpr int kStageBytes = round_up(kStageTx, 1024);
+    static constexpr int kQSlot = kMaxGroup * Cfg<KV>::kQHeadBytes;
+    static constexpr int kQOff = STAGES * kStageBytes;
+    static constexpr int kOStride = 132;  // floats per head row of a warp's O (padding avoids bank conflicts)
+    static constexpr int kWarpFloats = kMaxGroup * kOStride + 2 * kMaxGroup;
+    static constexpr int kMergeOff = kQOff + 2 * kQSlot;
+    static constexpr int kBarOff = kMergeOff + kNcw * kWarpFloats * 4;
+    static constexpr int kNumBars = 2 * STAGES + 6;  // full, empty, qfull x2, qempty x2, merge_full, merge_done
+    static constexpr int kNValidOff = kBarOff + kNumBars * 8;
+    static constexpr int kAbortOff = kNValidOff + STAGES * 4;
+    static constexpr int kBytes = kAbortOff + 16;
+    static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
+    static_assert(STAGES % GROUPS == 0, "each stage must belong to one consumer group");
+    static_assert(kStageBytes % 1024 == 0 && kQOff % 1024 == 0, "swizzled TMA boxes need 1024-byte alignment");
+    static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+struct Desc {
+    int u, t0, t1, slot;
+    bool ok;
+};
+
+template <bool PERSIST>
+__device__ __forceinline__ Desc get_desc(const KernelParams &p, int d_begin, int i, int t0s, int t1s) {
+    Desc x;
+    if (PERSIST) {
+        const int4 v = p.descs[d_begin + i];
+        x.u = v.x;
+        x.t0 = v.y;
+        x.t1 = v.z;
+        x.slot = d_begin + i;
+        x.ok = v.x >= 0 && v.x < p.num_units && v.y >= 0 && v.y <= v.z && x.slot < p.max_slots;
+    } else {
+        x.u = blockIdx.z * p.hkv + blockIdx.y;
+        x.t0 = t0s;
+        x.t1 = t1s;
+        x.slot = x.u * p.num_splits + blockIdx.x;
+        x.ok = true;
+    }
+    return x;
+}
+
+// Bounded wait on an mbarrier phase; gives up (false) when the CTA aborted or the
+// time limit passed (then it records the timeout and raises the abort flag).
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                        int32_t *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                atomicOr(status, DSA_DEV_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Wait used while draining after an abort: ignores the abort flag, still bounded.
+__device__ __noinline__ void drain_phase(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+    }
+}
+
+__device__ __forceinline__ uint32_t tok_mask(int t, int nv) {
+    return (t < nv ? 0x0000FFFFu : 0u) | (t + 1 < nv ? 0xFFFF0000u : 0u);
+}
+
+template <int KV, int STAGES, int GROUPS, bool PERSIST>
+__global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                const KernelParams p) {
+    using L = Layout<KV, STAGES, GROUPS>;
+    using C = Cfg<KV>;
+    constexpr int NCW = L::kNcw;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + L::kBarOff;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto qfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+    auto qempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 + s); };
+    const uint32_t merge_full = bar0 + 8u * (2 * STAGES + 4);
+    const uint32_t merge_done = bar0 + 8u * (2 * STAGES + 5);
+    int *nvalid = reinterpret_cast<int *>(smem + L::kNValidOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbortOff);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.G;
+
+    // ---- this CTA's work
+    int d_begin = 0, d_count = 1, st0 = 0, st1 = 0;
+    if (PERSIST) {
+        d_begin = p.cta_desc_begin[blockIdx.x];
+        d_count = p.cta_desc_begin[blockIdx.x + 1] - d_begin;
+        if (d_count <= 0) return;
+    } else {
+        const int b = blockIdx.z;
+        int len = p.seq_lens[b];
+        if (len < 0) {
+            if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.status, DSA_DEV_BAD_SEQLEN);
+            len = 0;
+        }
+        const int n = len / kTile + (len % kTile != 0);
+        const int c = p.static_mode == 0 ? (n + p.num_splits - 1) / p.num_splits : p.static_tiles;
+        st0 = min(static_cast<int>(blockIdx.x) * c, n);
+        st1 = min(st0 + c, n);
+        if (p.static_mode == 1 && blockIdx.x == p.num_splits - 1 && n > st1 && threadIdx.x == 0)
+            atomicOr(p.status, DSA_DEV_BAD_SEQLEN);  // grid too small for this request
+        if (st0 >= st1) {  // empty split: o = 0, lse = -inf
+            const int slot = (b * p.hkv + blockIdx.y) * p.num_splits + blockIdx.x;
+            for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x)
+                p.partial_o[static_cast<int64_t>(slot) * G * kHeadDim + i] = 0.f;
+            if (threadIdx.x < G) p.partial_lse[static_cast<int64_t>(slot) * G + threadIdx.x] = -INFINITY;
+            return;
+        }
+    }
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 4);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(qfull_bar(s), 1);
+            mbar_init(qempty_bar(s), NCW);
+        }
+        mbar_init(merge_full, NCW);
+        mbar_init(merge_done, NCW);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == NCW) {
+        // =========================== producer warp ===========================
+        if (lane == 0) {
+            prefetch_tmap(&kmap);
+            prefetch_tmap(&vmap);
+        }
+        const uint64_t policy = policy_evict_first();
+        int c = 0;          // tiles issued so far (ring position)
+        int q_issued = -1;  // ring index of the last Q copy issued
+        int qi = 0;         // accepted descriptors so far (Q ring and merge phases)
+        bool aborted = false;
+        for (int i = 0; i < d_count && !aborted; ++i) {
+            const Desc x = get_desc<PERSIST>(p, d_begin, i, st0, st1);
+            if (!x.ok) {
+                if (lane == 0) atomicOr(p.status, DSA_DEV_BAD_MAP);
+                continue;
+            }
+            const int b = x.u / p.hkv, h = x.u - b * p.hkv;
+            const int len = p.seq_lens[b];
+            const bool len_ok = len >= 0 && len <= p.max_pages * kTile;
+            int ab = 0;
+            if (lane == 0) {
+                if (!len_ok) atomicOr(p.status, DSA_DEV_BAD_SEQLEN);
+                if (!wait_phase(qempty_bar(qi & 1), ((qi >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                    ab = 1;
+                } else {
+                    const uint32_t bytes = G * C::kQHeadBytes;
+                    mbar_arrive_expect_tx(qfull_bar(qi & 1), bytes);
+                    const uint8_t *src = p.q + (static_cast<int64_t>(b) * p.hq + h * G) * C::kQHeadBytes;
+                    bulk_load(sbase + L::kQOff + (qi & 1) * L::kQSlot, src, bytes, qfull_bar(qi & 1));
+                    q_issued = qi;
+                }
+            }
+            ++qi;
+            if (__shfl_sync(0xffffffffu, ab, 0)) {
+                aborted = true;
+                break;
+            }
+            for (int base = x.t0; base < x.t1 && !aborted; base += 32) {
+                const int t = base + lane;
+                int page = -1;
+                if (t < x.t1 && t < p.max_pages) page = p.block_table[static_cast<int64_t>(b) * p.max_pages + t];
+                const int ntile = min(32, x.t1 - base);
+                for (int j = 0; j < ntile; ++j) {
+                    const int pg = __shfl_sync(0xffffffffu, page, j);
+                    ab = 0;
+                    if (lane == 0) {
+                        const int tt = base + j;
+                        const int stage = c % STAGES;
+                        if (!wait_phase(empty_bar(stage), ((c / STAGES) & 1) ^ 1, abort_flag, p.status)) {
+                            ab = 1;
+                        } else {
+                            int nv = len_ok ? min(kTile, len - tt * kTile) : 0;
+                            if (nv < 0 || tt >= p.max_pages) nv = 0;
+                            if (nv > 0 && (pg < 0 || pg >= p.num_pages)) {
+                                atomicOr(p.status, DSA_DEV_BAD_PAGE);
+                                nv = 0;
+                            }
+                            nvalid[stage] = nv;
+                            const uint32_t fb = full_bar(stage);
+                            if (nv > 0) {
+                                const uint32_t kdst = sbase + stage * L::kStageBytes;
+                                const uint32_t vdst = kdst + C::kTileBytes;
+                                mbar_arrive_expect_tx(fb, L::kStageTx);
+                                if (KV == 0) {  // two 64-column boxes per 128-wide bf16 row
+                                    tma_load_4d(kdst, &kmap, fb, 0, 0, h, pg, policy);
+                                    tma_load_4d(kdst + C::kTileBytes / 2, &kmap, fb, 64, 0, h, pg, policy);
+                                    tma_load_4d(vdst, &vmap, fb, 0, 0, h, pg, policy);
+                                    tma_load_4d(vdst + C::kTileBytes / 2, &vmap, fb, 64, 0, h, pg, policy);
+                                } else {
+                                    tma_load_4d(kdst, &kmap, fb, 0, 0, h, pg, policy);
+                                    tma_load_4d(vdst, &vmap, fb, 0, 0, h, pg, policy);
+                                    const int64_t srow = (static_cast<int64_t>(pg) * p.hkv + h) * kTile;
+                                    bulk_load(vdst + C::kTileBytes, p.k_scale + srow, C::kScaleBytes, fb);
+                                    bulk_load(vdst + C::kTileBytes + C::kScaleBytes, p.v_scale + srow,
+                                              C::kScaleBytes, fb);
+                                }
+                            } else {
+                                mbar_arrive(fb);
+                            }
+                        }
+                    }
+                    if (__shfl_sync(0xffffffffu, ab, 0)) {
+                        aborted = true;
+                        break;
+                    }
+                    ++c;
+                }
+            }
+        }
+        if (aborted && lane == 0) {
+            // let every copy this CTA started land before the CTA exits
+            for (int cc = max(0, c - STAGES); cc < c; ++cc) drain_phase(full_bar(cc % STAGES), (cc / STAGES) & 1);
+            if (q_issued >= 0) drain_phase(qfull_bar(q_issued & 1), (q_issued >> 1) & 1);
+        }
+        return;
+    }
+
+    // =========================== consumer warps ===========================
+    const int grp = warp / 4, wig = warp & 3;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int tok_base = wig * 16;
+    // per-lane ldmatrix row offsets (row & 7 == lane & 7 for every 8-row block)
+    const int xr = lane & 7;
+    const int k_row = tok_base + xr + ((lane >> 3) & 1) * 8;  // K: matrices (rows 0-7|8-15) x (chunk 0|1)
+    const int k_chunk = lane >> 4;
+    const int v_row = (KV == 0) ? tok_base + xr + (lane >> 4) * 8 : k_row;
+    const int v_chunk = (KV == 0) ? ((lane >> 3) & 1) : (lane >> 4);
+
+    int c_start = 0;  // tiles of this CTA before the current descriptor
+    int qi = -1;      // accepted descriptors so far, minus one (Q ring and merge phases)
+    for (int i = 0; i < d_count; ++i) {
+        const Desc x = get_desc<PERSIST>(p, d_begin, i, st0, st1);
+        if (!x.ok) continue;
+        ++qi;
+        const int b = x.u / p.hkv, h = x.u - b * p.hkv;
+        const int n = x.t1 - x.t0;
+
+        // ---- Q fragments (B operand, n = query head gid), zero past G
+        constexpr int KSTEPS = (KV == 0) ? 8 : 4;
+        uint32_t qf[KSTEPS][2];
+        if (!wait_phase(qfull_bar(qi & 1), (qi >> 1) & 1, abort_flag, p.status)) return;
+        {
+            const uint8_t *qs = smem + L::kQOff + (qi & 1) * L::kQSlot + gid * C::kQHeadBytes;
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                const int off = (KV == 0) ? (32 * ks + 4 * tig) : (32 * ks + 4 * tig);
+                qf[ks][0] = gid < G ? *reinterpret_cast<const uint32_t *>(qs + off) : 0u;
+                qf[ks][1] = gid < G ? *reinterpret_cast<const uint32_t *>(qs + off + 16) : 0u;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qempty_bar(qi & 1));
+
+        // score scale for this thread's heads 2*tig, 2*tig+1 (log2 domain)
+        float qsc0 = p.score_scale, qsc1 = p.score_scale;
+        if (KV == 1) {
+            const int64_t qrow = static_cast<int64_t>(b) * p.hq + h * G;
+            qsc0 *= (2 * tig < G) ? p.q_scale[qrow + 2 * tig] : 0.f;
+            qsc1 *= (2 * tig + 1 < G) ? p.q_scale[qrow + 2 * tig + 1] : 0.f;
+        }
+
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        float vsc = 1.f;  // E4M3: O holds the true output divided by vsc
+        float o[8][4];
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
+
+        bool aborted = false;
+        for (int li = ((grp - c_start) % GROUPS + GROUPS) % GROUPS; li < n; li += GROUPS) {
+            const int c = c_start + li;
+            const int stage = c % STAGES;
+            if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status)) {
+                aborted = true;
+                break;
+            }
+            const int nv = nvalid[stage];
+            if (nv > tok_base) {
+                const uint32_t kbase = sbase + stage * L::kStageBytes;
+                const uint32_t vbase = kbase + C::kTileBytes;
+                // ---- S^T = K . Q^T  (rows: tokens tok_base + gid / + 8; cols: heads 2tig, 2tig+1)
+                float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < KSTEPS; ++ks) {
+                    const int ch = 2 * ks + k_chunk;
+                    uint32_t addr;
+                    if (KV == 0)
+                        addr = kbase + (ch >> 3) * (C::kTileBytes / 2) + k_row * 128 + (((ch & 7) ^ xr) << 4);
+                    else
+                        addr = kbase + k_row * 128 + ((ch ^ xr) << 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(addr, a0, a1, a2, a3);
+                    if (KV == 0) mma_bf16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+                    else mma_e4m3(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+                }
+                const int ta = tok_base + gid, tb = ta + 8;
+                float ksa = 1.f, ksb = 1.f, vsa = 0.f, vsb = 0.f;
+                if (KV == 1) {
+                    const float *ksm = reinterpret_cast<const float *>(smem + stage * L::kStageBytes + 2 * C::kTileBytes);
+                    const float *vsm = ksm + kTile;
+                    ksa = ksm[ta];
+                    ksb = ksm[tb];
+                    vsa = ta < nv ? vsm[ta] : 0.f;
+                    vsb = tb < nv ? vsm[tb] : 0.f;
+                }
+                s[0] *= qsc0 * ksa;
+                s[1] *= qsc1 * ksa;
+                s[2] *= qsc0 * ksb;
+                s[3] *= qsc1 * ksb;
+                const bool partial = nv < tok_base + 16;
+                if (partial) {
+                    if (ta >= nv) s[0] = s[1] = -INFINITY;
+                    if (tb >= nv) s[2] = s[3] = -INFINITY;
+                }
+                // ---- online softmax (base 2), per head, over this warp's tokens
+                float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+                for (int o_ = 4; o_ < 32; o_ <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
+                }
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float r0 = mn0 == -INFINITY ? 0.f : mn0, r1 = mn1 == -INFINITY ? 0.f : mn1;
+                float al0 = ex2(m0 - r0), al1 = ex2(m1 - r1);
+                const float p0 = ex2(s[0] - r0), p1 = ex2(s[1] - r1), p2 = ex2(s[2] - r0), p3 = ex2(s[3] - r1);
+                l0 = l0 * al0 + p0 + p2;
+                l1 = l1 * al1 + p1 + p3;
+                m0 = mn0;
+                m1 = mn1;
+
+                uint32_t b0h, b1h, b0l = 0, b1l = 0;
+                if (KV == 0) {
+                    const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+                    const uint32_t l01 = pack_bf16x2(p0 - bf16lo_to_f32(h01), p1 - bf16hi_to_f32(h01));
+                    const uint32_t l23 = pack_bf16x2(p2 - bf16lo_to_f32(h23), p3 - bf16hi_to_f32(h23));
+                    b0h = movmatrix_trans(h01);
+                    b1h = movmatrix_trans(h23);
+                    b0l = movmatrix_trans(l01);
+                    b1l = movmatrix_trans(l23);
+                } else {
+                    // fold the per-token V scale into P, relative to this warp's largest scale
+                    float vm = fmaxf(vsa, vsb);
+#pragma unroll
+                    for (int o_ = 4; o_ < 32; o_ <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o_));
+                    float inv = 0.f;
+                    if (vm > 0.f) {
+                        const float f = vsc / vm;
+                        al0 *= f;
+                        al1 *= f;
+                        vsc = vm;
+                        inv = 1.f / vm;
+                    }
+                    const float wa = vsa * inv, wb = vsb * inv;
+                    b0h = movmatrix_trans(pack_f16x2(p0 * wa, p1 * wa));
+                    b1h = movmatrix_trans(pack_f16x2(p2 * wb, p3 * wb));
+                }
+#pragma unroll
+                for (int mb = 0; mb < 8; ++mb) {
+                    o[mb][0] *= al0;
+                    o[mb][1] *= al1;
+                    o[mb][2] *= al0;
+                    o[mb][3] *= al1;
+                }
+                // masks for the A (V^T) fragments: tokens (2tig, 2tig+1) and (8+2tig, 9+2tig)
+                const uint32_t mlo = partial ? tok_mask(tok_base + 2 * tig, nv) : 0xFFFFFFFFu;
+                const uint32_t mhi = partial ? tok_mask(tok_base + 8 + 2 * tig, nv) : 0xFFFFFFFFu;
+                // ---- O^T += V^T . P^T
+                if (KV == 0) {
+#pragma unroll
+                    for (int mb = 0; mb < 8; ++mb) {
+                        const int ch = 2 * mb + v_chunk;
+                        const uint32_t addr =
+                            vbase + (ch >> 3) * (C::kTileBytes / 2) + v_row * 128 + (((ch & 7) ^ xr) << 4);
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4_trans(addr, a0, a1, a2, a3);
+                        a0 &= mlo;
+                        a1 &= mlo;
+                        a2 &= mhi;
+                        a3 &= mhi;
+                        mma_bf16(o[mb], a0, a1, a2, a3, b0h, b1h);
+                        mma_bf16(o[mb], a0, a1, a2, a3, b0l, b1l);
+                    }
+                } else {
+#pragma unroll
+                    for (int mp = 0; mp < 4; ++mp) {
+                        const int ch = 2 * mp + v_chunk;
+                        const uint32_t addr = vbase + v_row * 128 + ((ch ^ xr) << 4);
+                        uint32_t x0, x1, x2, x3;
+                        ldsm_x4_trans(addr, x0, x1, x2, x3);
+                        // x0/x1: tokens 0-7 / 8-15 of chunk 2mp; x2/x3: of chunk 2mp+1.
+                        // Each holds, for dims (2gid, 2gid+1) of the chunk, tokens (2tig, 2tig+1).
+                        const uint32_t y0 = prmt(x0, 0, 0x3120), y1 = prmt(x1, 0, 0x3120);
+                        const uint32_t y2 = prmt(x2, 0, 0x3120), y3 = prmt(x3, 0, 0x3120);
+                        uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(y0 & 0xFFFF)) & mlo;
+                        uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(y0 >> 16)) & mlo;
+                        uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(y1 & 0xFFFF)) & mhi;
+                        uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(y1 >> 16)) & mhi;
+                        mma_f16(o[2 * mp], a0, a1, a2, a3, b0h, b1h);
+                        a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(y2 & 0xFFFF)) & mlo;
+                        a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(y2 >> 16)) & mlo;
+                        a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(y3 & 0xFFFF)) & mhi;
+                        a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(y3 >> 16)) & mhi;
+                        mma_f16(o[2 * mp + 1], a0, a1, a2, a3, b0h, b1h);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(stage));
+        }
+        if (aborted) return;
+        c_start += n;
+
+        // ---- merge the consumer warps' (m, l, O) and write the partial
+#pragma unroll
+        for (int o_ = 4; o_ < 32; o_ <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, o_);
+        }
+        if (!wait_phase(merge_done, (qi & 1) ^ 1, abort_flag, p.status)) return;
+        float *W = reinterpret_cast<float *>(smem + L::kMergeOff) + warp * L::kWarpFloats;
+        if (gid == 0) {
+            W[kMaxGroup * L::kOStride + 2 * tig] = m0;
+            W[kMaxGroup * L::kOStride + 2 * tig + 1] = m1;
+            W[kMaxGroup * L::kOStride + kMaxGroup + 2 * tig] = l0;
+            W[kMaxGroup * L::kOStride + kMaxGroup + 2 * tig + 1] = l1;
+        }
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb) {
+            const int d0 = (KV == 0) ? 16 * mb + gid : 16 * mb + 2 * gid;
+            const int d1 = (KV == 0) ? d0 + 8 : d0 + 1;
+            W[(2 * tig) * L::kOStride + d0] = o[mb][0] * vsc;
+            W[(2 * tig + 1) * L::kOStride + d0] = o[mb][1] * vsc;
+            W[(2 * tig) * L::kOStride + d1] = o[mb][2] * vsc;
+            W[(2 * tig + 1) * L::kOStride + d1] = o[mb][3] * vsc;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(merge_full);
+        if (!wait_phase(merge_full, qi & 1, abort_flag, p.status)) return;
+        {
+            const float *M0 = reinterpret_cast<const float *>(smem + L::kMergeOff);
+            for (int idx = warp * 32 + lane; idx < G * 32; idx += NCW * 32) {
+                const int hd = idx >> 5, d4 = (idx & 31) * 4;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) M = fmaxf(M, M0[w * L::kWarpFloats + kMaxGroup * L::kOStride + hd]);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float lse = -INFINITY;
+                if (M != -INFINITY) {
+                    float Lsum = 0.f;
+#pragma unroll
+                    for (int w = 0; w < NCW; ++w) {
+                        const float *Ww = M0 + w * L::kWarpFloats;
+                        const float e = ex2(Ww[kMaxGroup * L::kOStride + hd] - M);
+                        Lsum += e * Ww[kMaxGroup * L::kOStride + kMaxGroup + hd];
+                        const float4 v = *reinterpret_cast<const float4 *>(Ww + hd * L::kOStride + d4);
+                        acc.x += e * v.x;
+                        acc.y += e * v.y;
+                        acc.z += e * v.z;
+                        acc.w += e * v.w;
+                    }
+                    const float inv = 1.f / Lsum;
+                    acc.x *= inv;
+                    acc.y *= inv;
+                    acc.z *= inv;
+                    acc.w *= inv;
+                    lse = (M + lg2(Lsum)) * kLn2;
+                }
+                const int64_t row = static_cast<int64_t>(x.slot) * G + hd;
+                *reinterpret_cast<float4 *>(p.partial_o + row * kHeadDim + d4) = acc;
+                if ((idx & 31) == 0) p.partial_lse[row] = lse;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(merge_done);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 4-D view [num_pages][Hkv][64 tokens][128] of a page pool, box = 64 tokens of one
+// (page, head) x 128 bytes of the row, 128-byte swizzle.
+bool make_pool_map(CUtensorMap *m, const void *pool, int kv, int num_pages, int hkv) {
+    std::memset(m, 0, sizeof(*m));
+    if (num_pages == 0) return true;  // nothing can be loaded
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t es = kv == 0 ? 2 : 1;
+    const cuuint64_t dims[4] = {kHeadDim, kTile, static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(num_pages)};
+    const cuuint64_t strides[3] = {kHeadDim * es, kTile * kHeadDim * es, static_cast<cuuint64_t>(hkv) * kTile * kHeadDim * es};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / es), kTile, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, kv == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+                    const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int KV, int STAGES, int GROUPS, bool PERSIST>
+dsa_status launch(const AttnArgs &a, const KernelParams &kp, dim3 grid, cudaStream_t st) {
+    using L = Layout<KV, STAGES, GROUPS>;
+    CUtensorMap km, vm;
+    if (!make_pool_map(&km, a.k_pages, KV, a.num_pages, a.num_kv_heads) ||
+        !make_pool_map(&vm, a.v_pages, KV, a.num_pages, a.num_kv_heads))
+        return DSA_ERR_CUDA;
+    auto kern = attn_kernel<KV, STAGES, GROUPS, PERSIST>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    kern<<<grid, L::kThreads, L::kAlloc, st>>>(km, vm, kp);
+    return launch_status();
+}
+
+KernelParams base_params(const AttnArgs &a, float *partial_o, float *partial_lse, int32_t *status) {
+    KernelParams kp{};
+    kp.q = static_cast<const uint8_t *>(a.q);
+    kp.q_scale = a.q_scale;
+    kp.k_scale = a.k_scale;
+    kp.v_scale = a.v_scale;
+    kp.block_table = a.block_table;
+    kp.seq_lens = a.seq_lens;
+    kp.max_pages = a.max_pages_per_req;
+    kp.num_pages = a.num_pages;
+    kp.hq = a.num_q_heads;
+    kp.hkv = a.num_kv_heads;
+    kp.G = a.num_q_heads / a.num_kv_heads;
+    kp.num_units = a.batch * a.num_kv_heads;
+    kp.score_scale = a.sm_scale * kLog2e;
+    kp.partial_o = partial_o;
+    kp.partial_lse = partial_lse;
+    kp.status = status;
+    return kp;
+}
+
+// Ring depths: the persistent kernel keeps one CTA per SM with deep rings; the static
+// grid keeps two CTAs per SM with shallow rings (many short-lived CTAs).
+constexpr int kPersistStagesBf16 = 4, kPersistStagesFp8 = 8, kPersistGroups = 2;
+constexpr int kStaticStagesBf16 = 2, kStaticStagesFp8 = 4, kStaticGroups = 1;
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *q_scale, const void *k_pages,
+                                 const void *v_pages, dsa_dtype kv_dtype, const float *k_scale,
+                                 const float *v_scale, const int32_t *block_table, int32_t max_pages_per_req,
+                                 int32_t num_pages, const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
+                                 const dsa_task_map *map, float *partial_o, float *partial_lse,
+                                 dsa_stream stream) {
+    const AttnArgs a{q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale, block_table,
+                     max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                     page_size, sm_scale};
+    dsa_status s = validate_attn(a);
+    if (s != DSA_OK) return s;
+    if (!map || !map->cta_desc_begin || !map->descs || !map->meta || !partial_o || !partial_lse)
+        return DSA_ERR_INVALID_ARG;
+    if (map->num_units != batch * num_kv_heads || map->num_ctas < 1) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(partial_o) || !aligned16(map->descs)) return DSA_ERR_INVALID_ARG;
+    if (batch == 0) return DSA_OK;
+    KernelParams kp = base_params(a, partial_o, partial_lse, map->meta + 3);
+    kp.max_slots = map->max_descs;
+    kp.cta_desc_begin = map->cta_desc_begin;
+    kp.descs = reinterpret_cast<const int4 *>(map->descs);
+    const dim3 grid(map->num_ctas);
+    if (kv_dtype == DSA_BF16)
+        return launch<0, kPersistStagesBf16, kPersistGroups, true>(a, kp, grid, to_cuda(stream));
+    return launch<1, kPersistStagesFp8, kPersistGroups, true>(a, kp, grid, to_cuda(stream));
+}
+
+extern "C" int32_t dsa_static_num_splits(int32_t mode, int32_t param, int32_t max_seq_len) {
+    if (mode == 0) return param >= 1 ? param : -1;
+    if (mode != 1 || param < kTile || param % kTile != 0 || max_seq_len < 0) return -1;
+    const int64_t s = (static_cast<int64_t>(max_seq_len) + param - 1) / param;
+    return s < 1 ? 1 : (s > 65535 ? -1 : static_cast<int32_t>(s));
+}
+
+extern "C" dsa_status dsa_static_splitkv(int32_t mode, int32_t param, int32_t max_seq_len, const void *q,
+                                         dsa_dtype q_dtype, const float *q_scale, const void *k_pages,
+                                         const void *v_pages, dsa_dtype kv_dtype, const float *k_scale,
+                                         const float *v_scale, const int32_t *block_table,
+                                         int32_t max_pages_per_req, int32_t num_pages, const int32_t *seq_lens,
+                                         int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t page_size, float sm_scale, float *partial_o,
+                                         float *partial_lse, int32_t *status, dsa_stream stream) {
+    const AttnArgs a{q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale, block_table,
+                     max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                     page_size, sm_scale};
+    dsa_status s = validate_attn(a);
+    if (s != DSA_OK) return s;
+    const int32_t S = dsa_static_num_splits(mode, param, max_seq_len);
+    if (S < 1 || S > 65535) return DSA_ERR_INVALID_ARG;
+    if (!partial_o || !partial_lse || !status || !aligned16(partial_o)) return DSA_ERR_INVALID_ARG;
+    if (num_kv_heads > 65535 || batch > 65535) return DSA_ERR_UNSUPPORTED;
+    if (batch == 0) return DSA_OK;
+    KernelParams kp = base_params(a, partial_o, partial_lse, status);
+    kp.static_mode = mode;
+    kp.static_tiles = mode == 1 ? param / kTile : 0;
+    kp.num_splits = S;
+    kp.max_slots = batch * num_kv_heads * S;
+    const dim3 grid(S, num_kv_heads, batch);
+    if (kv_dtype == DSA_BF16) return launch<0, kStaticStagesBf16, kStaticGroups, false>(a, kp, grid, to_cuda(stream));
+    return launch<1, kStaticStagesFp8, kStaticGroups, false>(a, kp, grid, to_cuda(stream));
+}

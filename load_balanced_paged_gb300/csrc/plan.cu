@@ -1,0 +1,205 @@
+// The assign step: builds the per-step task map on the device from device-resident
+// KV lengths (HPC-Ops × SGLang blog, section "围绕活跃 KV 工作进行调度"; Hy3 preview
+// write-up, section 2.1.1 "Attention动态调度", "贪心装桶").
+//
+// One CTA of 1024 threads.  Instead of walking tiles one by one, it uses the closed
+// form of the greedy fill: with a real-valued budget T / C_eff, bin i ends where the
+// cumulative tile count first reaches floor((i+1) * T / C_eff), so the bin holding
+// global tile x is floor(((x+1) * C_eff - 1) / T).  Every unit and every descriptor
+// is then placed independently:
+//   1. n_u = ceil(len_b / 64), exclusive scan -> P_u, total T;
+//   2. per unit, the number of bins it touches -> exclusive scan -> first slot;
+//   3. per bin, its first descriptor = first slot of the unit holding its first tile
+//      plus the number of that unit's bins before it;
+//   4. per descriptor (grid-stride), its unit by binary search over first slots,
+//      its bin, and its tile range clipped to the unit.
+#include "common.h"
+
+namespace dsa {
+namespace {
+
+__device__ __forceinline__ int64_t bin_of(int64_t x, int64_t T, int64_t C_eff) {
+    return ((x + 1) * C_eff - 1) / T;
+}
+
+__device__ __forceinline__ int64_t bin_start(int64_t i, int64_t T, int64_t C_eff) {
+    return (i * T) / C_eff;
+}
+
+// First index in a[0, n) with a[i] > x (a nondecreasing).
+__device__ __forceinline__ int upper_bound(const int32_t *a, int n, int64_t x) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if (a[mid] <= x) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// In-place exclusive scan of a[0, n) by the whole block; returns the total.
+__device__ int64_t block_exclusive_scan(int32_t *a, int n, int64_t *warp_tot) {
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5, nw = nt >> 5;
+    const int per = (n + nt - 1) / nt;
+    const int lo = min(n, tid * per), hi = min(n, lo + per);
+    int64_t s = 0;
+    for (int i = lo; i < hi; ++i) s += a[i];
+    int64_t x = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int64_t t = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int64_t y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < nw) warp_tot[lane] = t;
+    }
+    __syncthreads();
+    int64_t run = x - s + (w > 0 ? warp_tot[w - 1] : 0);
+    const int64_t total = warp_tot[nw - 1];
+    for (int i = lo; i < hi; ++i) {
+        int32_t v = a[i];
+        a[i] = static_cast<int32_t>(run);
+        run += v;
+    }
+    __syncthreads();
+    return total;
+}
+
+__global__ void __launch_bounds__(1024, 1)
+plan_kernel(const int32_t *__restrict__ seq_lens, int32_t batch, int32_t num_kv_heads, int32_t num_ctas,
+            int32_t min_tiles, dsa_task_map map) {
+    extern __shared__ int32_t smem[];
+    __shared__ int64_t warp_tot[32];
+    __shared__ int s_status;
+    const int U = batch * num_kv_heads;
+    int32_t *sP = smem;             // [U + 1] first global tile of each unit, then T
+    int32_t *sBeg = smem + U + 1;   // [U + 1] first descriptor of each unit, then num_descs
+    const int tid = threadIdx.x, nt = blockDim.x;
+
+    if (tid == 0) s_status = 0;
+    __syncthreads();
+
+    // 1. tiles per unit (u = b * Hkv + h)
+    for (int u = tid; u < U; u += nt) {
+        int32_t len = seq_lens[u / num_kv_heads];
+        if (len < 0) {
+            atomicOr(&s_status, DSA_DEV_BAD_SEQLEN);
+            len = 0;
+        }
+        sP[u] = len / kTile + (len % kTile != 0);
+    }
+    __syncthreads();
+    int64_t T = block_exclusive_scan(sP, U, warp_tot);
+    bool overflow = T > INT32_MAX;  // cannot index the tiles: schedule nothing
+    if (overflow) T = 0;
+    int64_t C_eff = T / min_tiles;
+    if (C_eff < 1) C_eff = 1;
+    if (C_eff > num_ctas) C_eff = num_ctas;
+    if (T == 0) C_eff = 0;
+    if (tid == 0) {
+        sP[U] = static_cast<int32_t>(T);
+        if (overflow) s_status |= DSA_DEV_BAD_SEQLEN;
+    }
+    __syncthreads();
+
+    // 2. bins touched by each unit
+    for (int u = tid; u < U; u += nt) {
+        const int64_t p = sP[u], n = overflow ? 0 : sP[u + 1] - p;
+        sBeg[u] = n > 0 ? static_cast<int32_t>(bin_of(p + n - 1, T, C_eff) - bin_of(p, T, C_eff) + 1) : 0;
+    }
+    __syncthreads();
+    int64_t nd = block_exclusive_scan(sBeg, U, warp_tot);
+    if (nd > map.max_descs) {  // cannot happen with a map sized by dsa_max_descs
+        if (tid == 0) s_status |= DSA_DEV_BAD_MAP;
+        nd = 0;
+    }
+    if (tid == 0) sBeg[U] = static_cast<int32_t>(nd);
+    __syncthreads();
+    const bool empty_map = nd == 0;
+
+    for (int u = tid; u < U; u += nt) {
+        map.unit_partial_begin[u] = empty_map ? 0 : sBeg[u];
+        map.unit_num_partials[u] = empty_map ? 0 : sBeg[u + 1] - sBeg[u];
+    }
+
+    // 3. first descriptor of every bin
+    for (int i = tid; i <= num_ctas; i += nt) {
+        int32_t b;
+        if (empty_map || i >= C_eff) {
+            b = static_cast<int32_t>(nd);
+        } else {
+            const int64_t x = bin_start(i, T, C_eff);
+            const int v = upper_bound(sP, U, x) - 1;
+            b = static_cast<int32_t>(sBeg[v] + (i - bin_of(sP[v], T, C_eff)));
+        }
+        map.cta_desc_begin[i] = b;
+    }
+
+    // 4. descriptors, grid-stride
+    for (int64_t d = tid; d < nd; d += nt) {
+        const int v = upper_bound(sBeg, U, d) - 1;
+        const int64_t k = d - sBeg[v];
+        const int64_t p = sP[v], n = sP[v + 1] - p;
+        const int64_t i = bin_of(p, T, C_eff) + k;
+        const int64_t g0 = max(bin_start(i, T, C_eff), p);
+        const int64_t g1 = min(bin_start(i + 1, T, C_eff), p + n);
+        int4 desc = make_int4(v, static_cast<int32_t>(g0 - p), static_cast<int32_t>(g1 - p),
+                              static_cast<int32_t>(k));
+        reinterpret_cast<int4 *>(map.descs)[d] = desc;
+    }
+
+    __syncthreads();
+    if (tid == 0) {
+        map.meta[0] = static_cast<int32_t>(T);
+        map.meta[1] = static_cast<int32_t>(C_eff);
+        map.meta[2] = static_cast<int32_t>(nd);
+        map.meta[3] = s_status;
+    }
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" int32_t dsa_max_descs(int32_t batch, int32_t num_kv_heads, int32_t num_ctas) {
+    if (batch < 0 || num_kv_heads < 1 || num_ctas < 1) return -1;
+    int64_t v = static_cast<int64_t>(batch) * num_kv_heads + num_ctas - 1;
+    return v > INT32_MAX ? -1 : static_cast<int32_t>(v);
+}
+
+extern "C" dsa_status dsa_plan(const int32_t *seq_lens, int32_t batch, int32_t num_kv_heads,
+                               int32_t num_persistent_ctas, int32_t tile, int32_t min_tiles_per_split,
+                               const dsa_task_map *map, dsa_stream stream) {
+    if (!map || batch < 0 || num_kv_heads < 1 || num_persistent_ctas < 1 || min_tiles_per_split < 1)
+        return DSA_ERR_INVALID_ARG;
+    if (batch > 0 && !seq_lens) return DSA_ERR_INVALID_ARG;
+    if (!map->cta_desc_begin || !map->descs || !map->meta ||
+        (batch > 0 && (!map->unit_partial_begin || !map->unit_num_partials)))
+        return DSA_ERR_INVALID_ARG;
+    if (tile != kTile) return DSA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(map->descs) & 15u) != 0) return DSA_ERR_INVALID_ARG;
+    const int64_t U = static_cast<int64_t>(batch) * num_kv_heads;
+    if (U > kPlanMaxUnits) return DSA_ERR_UNSUPPORTED;
+    if (map->num_ctas != num_persistent_ctas || map->num_units != U) return DSA_ERR_INVALID_ARG;
+    const int32_t need = dsa_max_descs(batch, num_kv_heads, num_persistent_ctas);
+    if (need < 0) return DSA_ERR_INVALID_ARG;
+    if (map->max_descs < need) return DSA_ERR_BUFFER_TOO_SMALL;
+
+    const size_t smem = sizeof(int32_t) * 2 * static_cast<size_t>(U + 1);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    plan_kernel<<<1, 1024, smem, to_cuda(stream)>>>(seq_lens, batch, num_kv_heads, num_persistent_ctas,
+                                                   min_tiles_per_split, *map);
+    return launch_status();
+}
