@@ -217,6 +217,39 @@ dsa_status dsa_static_combine(int32_t num_splits, const float *partial_o, const 
 dsa_status dsa_read_status(const int32_t *device_status, int32_t *host_status);
 dsa_status dsa_get_status(const dsa_task_map *map, int32_t *host_status);
 
+/*
+ * dsa_decode_step_noalloc -- one whole decode step (dsa_plan, dsa_decode,
+ * dsa_combine with the same arguments and results) that allocates nothing.  The
+ * pages have no counterpart of this call: it exists for callers that cannot
+ * call cudaMalloc -- code running under another framework's memory pool or
+ * allocator hooks, loops that forbid allocation once started, C programs that
+ * own only their inputs and outputs -- and so cannot provide the task map and
+ * partial-output buffers dsa_decode needs between its kernels.
+ *
+ * Scratch: a fixed device array of DSA_NOALLOC_SCRATCH_BYTES inside the
+ * library, present on every GPU that loads it until the process exits.  The
+ * step needs about 16*(B*Hkv + C) + 4*C + 8*B*Hkv bytes of task map plus
+ * (B*Hkv + C - 1) * G * 129 * 4 bytes of partials (C = num_persistent_ctas);
+ * larger steps are rejected with DSA_ERR_BUFFER_TOO_SMALL before anything is
+ * launched.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  Every call reuses the same array, so calls whose work
+ * overlaps on the GPU (other streams, other threads) race on it; calls in one
+ * stream are safe.  Nothing in the array needs clearing between calls.
+ * status: device int32, may be NULL; receives the step's DSA_DEV_* bits.
+ * No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+#define DSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+dsa_status dsa_decode_step_noalloc(const void *q, dsa_dtype q_dtype, const float *q_scale,
+                                   const void *k_pages, const void *v_pages, dsa_dtype kv_dtype,
+                                   const float *k_scale, const float *v_scale,
+                                   const int32_t *block_table, int32_t max_pages_per_req,
+                                   int32_t num_pages, const int32_t *seq_lens, int32_t batch,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t page_size, float sm_scale, int32_t num_persistent_ctas,
+                                   int32_t min_tiles_per_split, void *out, dsa_dtype out_dtype,
+                                   float *out_lse, int32_t *status, dsa_stream stream);
+
 /* Static string naming a dsa_status value. */
 const char *dsa_status_string(dsa_status s);
 

@@ -65,6 +65,8 @@ _lib.dsa_read_status.argtypes = [_vp, ctypes.POINTER(_i32)]
 _lib.dsa_read_status.restype = ctypes.c_int
 _lib.dsa_get_status.argtypes = [_TMP, ctypes.POINTER(_i32)]
 _lib.dsa_get_status.restype = ctypes.c_int
+_lib.dsa_decode_step_noalloc.argtypes = _attn_args + [_i32, _i32, _vp, _i32, _vp, _vp, _vp]
+_lib.dsa_decode_step_noalloc.restype = ctypes.c_int
 _lib.dsa_status_string.argtypes = [ctypes.c_int]
 _lib.dsa_status_string.restype = ctypes.c_char_p
 
@@ -256,3 +258,16 @@ def attention(inp: dict, num_ctas: int, min_tiles_per_split: int = 4, out_dtype=
     out_lse = torch.empty(B, inp["num_q_heads"], dtype=torch.float32, device=po.device)
     out = combine(tm, po, pl, inp["num_q_heads"], out_lse=out_lse, out_dtype=out_dtype, stream=stream)
     return out, out_lse, tm, po, pl
+
+
+def decode_step_noalloc(inp: dict, num_ctas: int, out, out_lse=None, status=None, min_tiles_per_split: int = 4,
+                        stream=None):
+    """dsa_decode_step_noalloc: plan, decode and combine with the library's own fixed device
+    scratch (for callers that cannot allocate device memory); writes out / out_lse / status."""
+    args = _attn_args(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"],
+                      inp["num_kv_heads"], inp["sm_scale"], inp.get("q_scale"), inp.get("k_scale"),
+                      inp.get("v_scale"))
+    rc = _lib.dsa_decode_step_noalloc(*args, num_ctas, min_tiles_per_split, _ptr(out), _dtype_code(out),
+                                      _ptr(out_lse), _ptr(status), _stream(stream))
+    _check(rc, "dsa_decode_step_noalloc")
+    return out
