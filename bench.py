@@ -114,11 +114,11 @@ def bench_ours(args, device, rank, world):
 
     name = args.workload
     w = workloads.WORKLOADS[name]
-    inp = workloads.make_workload(name, device=device, seed=w.seed + rank)
+    inp = workloads.make_workload(name, device=device, seed=w.seed + rank, max_requests=args.requests)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     C = w.ctas or sms
     m = args.min_tiles
-    B, hq, hkv = w.batch, w.num_q_heads, w.num_kv_heads
+    B, hq, hkv = int(inp["seq_lens"].shape[0]), w.num_q_heads, w.num_kv_heads
     G = hq // hkv
     tm = dsa.TaskMap(B, hkv, C, device)
     po, pl = dsa.partial_buffers(tm.max_descs, G, device)
@@ -128,34 +128,62 @@ def bench_ours(args, device, rank, world):
     kw = dict(q_scale=inp["q_scale"], k_scale=inp["k_scale"], v_scale=inp["v_scale"])
 
     def plan():
-        dsa.plan(inp["seq_lens"], hkv, C, m, task_map=tm, stream=stream)
+        dsa.plan(inp["seq_lens"], hkv, C, m, task_map=tm)
 
     def decode():
         dsa.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
-                   inp["sm_scale"], partial_o=po, partial_lse=pl, stream=stream, **kw)
+                   inp["sm_scale"], partial_o=po, partial_lse=pl, **kw)
 
     def combine():
-        dsa.combine(tm, po, pl, hq, out=out, out_lse=out_lse, stream=stream)
+        dsa.combine(tm, po, pl, hq, out=out, out_lse=out_lse)
 
     flush = flush_buffer(device)
     nbytes = kv_bytes(inp)
 
+    def graphs_of(fns):
+        """One CUDA graph per function (each a captured kernel launch)."""
+        gs = []
+        for f in fns:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                f()
+            gs.append(g)
+        torch.cuda.synchronize()
+        return gs
+
     def timed(fns, steps, warmup):
-        """Per-step CUDA events around each fn; L2 flushed before each step, untimed."""
+        """Replays the captured kernels with CUDA events between them; L2 is flushed before
+        each step, outside the events.  Returns ms [steps, len(fns)]."""
         for _ in range(warmup):
-            flush.fill_(1.0)
             for f in fns:
                 f()
+        gs = graphs_of(fns)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)] for _ in range(steps)]
         for k in range(steps):
             flush.fill_(float(k))
             ev[k][0].record(stream)
-            for i, f in enumerate(fns):
-                f()
+            for i, g in enumerate(gs):
+                g.replay()
                 ev[k][i + 1].record(stream)
         stream.synchronize()
         per = np.array([[ev[k][i].elapsed_time(ev[k][i + 1]) for i in range(len(fns))] for k in range(steps)])
-        return per  # ms, [steps, len(fns)]
+        return per
+
+    def timed_whole(fns, steps):
+        """The same kernels captured as ONE graph (a production decode step) timed as a unit."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for f in fns:
+                f()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for k in range(steps):
+            flush.fill_(float(k))
+            ev[k][0].record(stream)
+            g.replay()
+            ev[k][1].record(stream)
+        stream.synchronize()
+        return np.array([ev[k][0].elapsed_time(ev[k][1]) for k in range(steps)])
 
     # warm-up + correctness gate of this configuration (status word must be clean)
     timed([plan, decode, combine], 1, args.warmup)
@@ -171,7 +199,7 @@ def bench_ours(args, device, rank, world):
                           "GPU-" + str(torch.cuda.get_device_properties(device).uuid))
     time.sleep(0.3)
     t_wall0 = time.time()
-    per = timed([plan, decode, combine], args.steps, 0)
+    step_ms = timed_whole([plan, decode, combine], args.steps)
     t_wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
@@ -179,8 +207,8 @@ def bench_ours(args, device, rank, world):
     clocks.stop()
     clk = clocks.summary(t_wall0, t_wall1)
 
-    step_ms = per.sum(axis=1)
     total_ms = float(step_ms.sum())
+    per = timed([plan, decode, combine], max(10, min(args.steps, 500)), 0)
     if world > 1:
         t = torch.tensor([total_ms], device=device)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -199,17 +227,18 @@ def bench_ours(args, device, rank, world):
         def sdec(mode=mode, param=param, spo=spo, spl=spl, sst=sst):
             dsa.static_splitkv(mode, param, max_len, inp["q"], inp["k_pages"], inp["v_pages"],
                                inp["block_table"], inp["seq_lens"], hkv, inp["sm_scale"], partial_o=spo,
-                               partial_lse=spl, status=sst, stream=stream, **kw)
+                               partial_lse=spl, status=sst, **kw)
 
         def scomb(S=S, spo=spo, spl=spl):
-            dsa.static_combine(S, spo, spl, B, hq, hkv, out=out, out_lse=out_lse, stream=stream)
+            dsa.static_combine(S, spo, spl, B, hq, hkv, out=out, out_lse=out_lse)
 
         sp = timed([sdec, scomb], max(10, min(args.steps, 200)), 3)
         if dsa.read_status(sst) != 0:
             raise RuntimeError(f"{label}: device status set")
         s_ms = float(sp.sum(axis=1).mean())
         static[label] = {"splits": S, "us_per_step": round(s_ms * 1e3, 2),
-                         "speedup_of_dynamic": round(s_ms / (t_dec + t_comb), 3)}
+                         "speedup_of_dynamic": round(s_ms / (t_dec + t_comb), 3),
+                         "speedup_of_dynamic_with_plan": round(s_ms / ms_per_step, 3)}
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     host = {k: inp[k].cpu().pin_memory() for k in ("q", "q_scale", "k_pages", "v_pages", "k_scale", "v_scale",
@@ -344,6 +373,7 @@ def main():
     ap.add_argument("--min-tiles", type=int, default=4)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--requests", type=int, default=None, help="keep only the first N requests (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

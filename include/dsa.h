@@ -124,7 +124,8 @@ int32_t dsa_max_descs(int32_t batch, int32_t num_kv_heads, int32_t num_ctas);
  *   into descriptors.  One CTA; the result is unique and bit-exact.
  * Arguments: seq_lens [batch] device int32; tile must be 64; min_tiles_per_split
  * >= 1; map->num_ctas must equal num_persistent_ctas, map->num_units must equal
- * batch*num_kv_heads, map->max_descs >= dsa_max_descs(...).  B*Hkv <= 16384.
+ * batch*num_kv_heads, map->max_descs >= dsa_max_descs(...).  B*Hkv <= 16384 and
+ * num_persistent_ctas <= 16384 (else DSA_ERR_UNSUPPORTED).
  * A negative length counts as zero tiles and sets DSA_DEV_BAD_SEQLEN in meta[3];
  * dsa_plan resets meta[3] for the step.
  */

@@ -93,7 +93,8 @@ struct Layout {
     static constexpr int kNumBars = 2 * STAGES + 6;  // full, empty, qfull x2, qempty x2, merge_full, merge_done
     static constexpr int kNValidOff = kBarOff + kNumBars * 8;
     static constexpr int kAbortOff = kNValidOff + STAGES * 4;
-    static constexpr int kBytes = kAbortOff + 16;
+    static constexpr int kInfoOff = round_up(kAbortOff + 16, 64);  // 2 DescInfo slots, beside the 2 Q slots
+    static constexpr int kBytes = kInfoOff + 2 * 64;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static_assert(STAGES % GROUPS == 0, "each stage must belong to one consumer group");
     static_assert(kStageBytes % 1024 == 0 && kQOff % 1024 == 0, "swizzled TMA boxes need 1024-byte alignment");
@@ -104,6 +105,18 @@ struct Desc {
     int u, t0, t1, slot;
     bool ok;
 };
+
+// What the producer hands the consumers with each descriptor's Q (shared memory).
+struct DescInfo {
+    int end;      // 1: no more descriptors in this CTA
+    int b, h;     // request, KV head
+    int n;        // tiles
+    int slot;     // partial-output slot
+    int c_start;  // ring position of the descriptor's first tile
+    int pad[2];
+    float qscale[kMaxGroup];  // E4M3: q_scale of the G query heads
+};
+static_assert(sizeof(DescInfo) == 64, "DescInfo slot size");
 
 template <bool PERSIST>
 __device__ __forceinline__ Desc get_desc(const KernelParams &p, int d_begin, int i, int t0s, int t1s) {
@@ -144,11 +157,11 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile 
     }
 }
 
-// Wait used while draining after an abort: ignores the abort flag, still bounded.
-__device__ __noinline__ void drain_phase(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
+// Wait used while draining after an abort: ignores the abort flag; gives up at `deadline`
+// (%globaltimer ns), shared by all the drain's waits.
+__device__ __noinline__ void drain_phase(uint32_t bar, uint32_t parity, uint64_t deadline) {
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+        if (globaltimer_ns() > deadline) return;
     }
 }
 
@@ -225,77 +238,159 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
 
     if (warp == NCW) {
         // =========================== producer warp ===========================
+        // The CTA's descriptors are read 32 at a time (one per lane, with their
+        // lengths and Q scales); their tiles form one stream, mapped 32 at a time
+        // onto lanes, whose page ids are fetched one chunk ahead of the chunk whose
+        // TMA copies are being issued.  Lane 0 issues; the warp stays converged.
         if (lane == 0) {
             prefetch_tmap(&kmap);
             prefetch_tmap(&vmap);
         }
         const uint64_t policy = policy_evict_first();
         int c = 0;          // tiles issued so far (ring position)
-        int q_issued = -1;  // ring index of the last Q copy issued
-        int qi = 0;         // accepted descriptors so far (Q ring and merge phases)
+        int qi = 0;         // descriptors handed to the consumers
+        int q_issued = -1;  // hand-off index of the last Q copy issued
         bool aborted = false;
-        for (int i = 0; i < d_count && !aborted; ++i) {
-            const Desc x = get_desc<PERSIST>(p, d_begin, i, st0, st1);
-            if (!x.ok) {
-                if (lane == 0) atomicOr(p.status, DSA_DEV_BAD_MAP);
-                continue;
-            }
-            const int b = x.u / p.hkv, h = x.u - b * p.hkv;
-            const int len = p.seq_lens[b];
-            const bool len_ok = len >= 0 && len <= p.max_pages * kTile;
-            int ab = 0;
-            if (lane == 0) {
-                if (!len_ok) atomicOr(p.status, DSA_DEV_BAD_SEQLEN);
-                if (!wait_phase(qempty_bar(qi & 1), ((qi >> 1) & 1) ^ 1, abort_flag, p.status)) {
-                    ab = 1;
+        for (int wbase = 0; wbase < d_count && !aborted; wbase += 32) {
+            // ---- window: descriptor wbase + lane
+            int wb = 0, wh = 0, wt0 = 0, wn = 0, wslot = 0, wlen = 0;
+            float wqs[kMaxGroup];
+#pragma unroll
+            for (int g = 0; g < kMaxGroup; ++g) wqs[g] = 0.f;
+            if (wbase + lane < d_count) {
+                const Desc x = get_desc<PERSIST>(p, d_begin, wbase + lane, st0, st1);
+                if (x.ok) {
+                    wb = x.u / p.hkv;
+                    wh = x.u - wb * p.hkv;
+                    wt0 = x.t0;
+                    wn = x.t1 - x.t0;
+                    wslot = x.slot;
+                    wlen = p.seq_lens[wb];
+                    if (wlen < 0 || wlen > p.max_pages * kTile) atomicOr(p.status, DSA_DEV_BAD_SEQLEN);
+                    if (KV == 1) {
+                        const float *qs = p.q_scale + static_cast<int64_t>(wb) * p.hq + wh * G;
+#pragma unroll
+                        for (int g = 0; g < kMaxGroup; ++g)
+                            if (g < G) wqs[g] = qs[g];
+                    }
+                    if (wn == 0) {  // no tiles: its partial is empty, the consumers never see it
+                        for (int i = 0; i < G * kHeadDim; ++i)
+                            p.partial_o[static_cast<int64_t>(wslot) * G * kHeadDim + i] = 0.f;
+                        for (int g = 0; g < G; ++g) p.partial_lse[static_cast<int64_t>(wslot) * G + g] = -INFINITY;
+                    }
                 } else {
-                    const uint32_t bytes = G * C::kQHeadBytes;
-                    mbar_arrive_expect_tx(qfull_bar(qi & 1), bytes);
-                    const uint8_t *src = p.q + (static_cast<int64_t>(b) * p.hq + h * G) * C::kQHeadBytes;
-                    bulk_load(sbase + L::kQOff + (qi & 1) * L::kQSlot, src, bytes, qfull_bar(qi & 1));
-                    q_issued = qi;
+                    atomicOr(p.status, DSA_DEV_BAD_MAP);
                 }
             }
-            ++qi;
-            if (__shfl_sync(0xffffffffu, ab, 0)) {
-                aborted = true;
-                break;
+            // stream offset of each descriptor in the window (exclusive scan of tile counts)
+            int incl = wn;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
             }
-            for (int base = x.t0; base < x.t1 && !aborted; base += 32) {
-                const int t = base + lane;
-                int page = -1;
-                if (t < x.t1 && t < p.max_pages) page = p.block_table[static_cast<int64_t>(b) * p.max_pages + t];
-                const int ntile = min(32, x.t1 - base);
-                for (int j = 0; j < ntile; ++j) {
-                    const int pg = __shfl_sync(0xffffffffu, page, j);
-                    ab = 0;
-                    if (lane == 0) {
-                        const int tt = base + j;
-                        const int stage = c % STAGES;
-                        if (!wait_phase(empty_bar(stage), ((c / STAGES) & 1) ^ 1, abort_flag, p.status)) {
+            const int wstart = incl - wn;
+            const int wtotal = __shfl_sync(0xffffffffu, incl, 31);
+
+            // lane -> (descriptor, tile, page) for stream tile s0 + lane
+            auto map_chunk = [&](int s0, int &j, int &t, int &pg) {
+                const int s = s0 + lane;
+                j = 0;
+#pragma unroll
+                for (int step = 16; step > 0; step >>= 1) {
+                    const int v = __shfl_sync(0xffffffffu, wstart, j + step);
+                    if (v <= s) j += step;
+                }
+                t = __shfl_sync(0xffffffffu, wt0, j) + (s - __shfl_sync(0xffffffffu, wstart, j));
+                const int bj = __shfl_sync(0xffffffffu, wb, j);
+                pg = -1;
+                if (s < wtotal && t < p.max_pages) pg = p.block_table[static_cast<int64_t>(bj) * p.max_pages + t];
+            };
+
+            int cj = 0, ct = 0, cpg = -1;
+            if (wtotal > 0) map_chunk(0, cj, ct, cpg);
+            for (int s0 = 0; s0 < wtotal && !aborted; s0 += 32) {
+                int nj = 0, nt = 0, npg = -1;
+                if (s0 + 32 < wtotal) map_chunk(s0 + 32, nj, nt, npg);  // next chunk's page ids in flight
+                const int cnt = min(32, wtotal - s0);
+                // ---- per-lane view of this lane's own tile (stream tile s0 + lane)
+                const int h_l = __shfl_sync(0xffffffffu, wh, cj);
+                const int len_l = __shfl_sync(0xffffffffu, wlen, cj);
+                const int t0_l = __shfl_sync(0xffffffffu, wt0, cj);
+                const bool first_l = lane < cnt && ct == t0_l;
+                int nv_l = 0;
+                if (lane < cnt) {
+                    const bool len_ok = len_l >= 0 && len_l <= p.max_pages * kTile;
+                    nv_l = len_ok ? min(kTile, len_l - ct * kTile) : 0;
+                    if (nv_l < 0 || ct >= p.max_pages) nv_l = 0;
+                    if (nv_l > 0 && (cpg < 0 || cpg >= p.num_pages)) {
+                        atomicOr(p.status, DSA_DEV_BAD_PAGE);
+                        nv_l = 0;
+                    }
+                }
+                const uint32_t starts = __ballot_sync(0xffffffffu, first_l);
+                // ---- runs of at most STAGES tiles, cut where a descriptor starts; in a run
+                //      every lane waits for and fills its own stage, in parallel
+                for (int k = 0; k < cnt && !aborted;) {
+                    int ab = 0;
+                    if ((starts >> k) & 1u) {
+                        // descriptor cj[k] starts here: hand it (info + Q) to the consumers
+                        const int j = __shfl_sync(0xffffffffu, cj, k);
+                        float qs[kMaxGroup];
+#pragma unroll
+                        for (int g = 0; g < kMaxGroup; ++g) qs[g] = __shfl_sync(0xffffffffu, wqs[g], j);
+                        const int b = __shfl_sync(0xffffffffu, wb, j);
+                        const int h = __shfl_sync(0xffffffffu, wh, j);
+                        const int n = __shfl_sync(0xffffffffu, wn, j);
+                        const int slot = __shfl_sync(0xffffffffu, wslot, j);
+                        if (lane == 0) {
+                            if (!wait_phase(qempty_bar(qi & 1), ((qi >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                                ab = 1;
+                            } else {
+                                DescInfo *inf = reinterpret_cast<DescInfo *>(smem + L::kInfoOff) + (qi & 1);
+                                inf->end = 0;
+                                inf->b = b;
+                                inf->h = h;
+                                inf->n = n;
+                                inf->slot = slot;
+                                inf->c_start = c;
+#pragma unroll
+                                for (int g = 0; g < kMaxGroup; ++g) inf->qscale[g] = qs[g];
+                                const uint32_t bytes = G * C::kQHeadBytes;
+                                mbar_arrive_expect_tx(qfull_bar(qi & 1), bytes);
+                                const uint8_t *src = p.q + (static_cast<int64_t>(b) * p.hq + h * G) * C::kQHeadBytes;
+                                bulk_load(sbase + L::kQOff + (qi & 1) * L::kQSlot, src, bytes, qfull_bar(qi & 1));
+                                q_issued = qi;
+                            }
+                        }
+                        ++qi;
+                        ab = __shfl_sync(0xffffffffu, ab, 0);
+                    }
+                    // run [k, e): up to STAGES tiles, no descriptor start after k
+                    const uint32_t later = starts & ~((2u << k) - 1u);
+                    int e = later ? __ffs(later) - 1 : 32;
+                    e = min(e, min(cnt, k + STAGES));
+                    if (!ab && lane >= k && lane < e) {
+                        const int cl = c + (lane - k);
+                        const int stage = cl % STAGES;
+                        if (!wait_phase(empty_bar(stage), ((cl / STAGES) & 1) ^ 1, abort_flag, p.status)) {
                             ab = 1;
                         } else {
-                            int nv = len_ok ? min(kTile, len - tt * kTile) : 0;
-                            if (nv < 0 || tt >= p.max_pages) nv = 0;
-                            if (nv > 0 && (pg < 0 || pg >= p.num_pages)) {
-                                atomicOr(p.status, DSA_DEV_BAD_PAGE);
-                                nv = 0;
-                            }
-                            nvalid[stage] = nv;
+                            nvalid[stage] = nv_l;
                             const uint32_t fb = full_bar(stage);
-                            if (nv > 0) {
+                            if (nv_l > 0) {
                                 const uint32_t kdst = sbase + stage * L::kStageBytes;
                                 const uint32_t vdst = kdst + C::kTileBytes;
                                 mbar_arrive_expect_tx(fb, L::kStageTx);
                                 if (KV == 0) {  // two 64-column boxes per 128-wide bf16 row
-                                    tma_load_4d(kdst, &kmap, fb, 0, 0, h, pg, policy);
-                                    tma_load_4d(kdst + C::kTileBytes / 2, &kmap, fb, 64, 0, h, pg, policy);
-                                    tma_load_4d(vdst, &vmap, fb, 0, 0, h, pg, policy);
-                                    tma_load_4d(vdst + C::kTileBytes / 2, &vmap, fb, 64, 0, h, pg, policy);
+                                    tma_load_4d(kdst, &kmap, fb, 0, 0, h_l, cpg, policy);
+                                    tma_load_4d(kdst + C::kTileBytes / 2, &kmap, fb, 64, 0, h_l, cpg, policy);
+                                    tma_load_4d(vdst, &vmap, fb, 0, 0, h_l, cpg, policy);
+                                    tma_load_4d(vdst + C::kTileBytes / 2, &vmap, fb, 64, 0, h_l, cpg, policy);
                                 } else {
-                                    tma_load_4d(kdst, &kmap, fb, 0, 0, h, pg, policy);
-                                    tma_load_4d(vdst, &vmap, fb, 0, 0, h, pg, policy);
-                                    const int64_t srow = (static_cast<int64_t>(pg) * p.hkv + h) * kTile;
+                                    tma_load_4d(kdst, &kmap, fb, 0, 0, h_l, cpg, policy);
+                                    tma_load_4d(vdst, &vmap, fb, 0, 0, h_l, cpg, policy);
+                                    const int64_t srow = (static_cast<int64_t>(cpg) * p.hkv + h_l) * kTile;
                                     bulk_load(vdst + C::kTileBytes, p.k_scale + srow, C::kScaleBytes, fb);
                                     bulk_load(vdst + C::kTileBytes + C::kScaleBytes, p.v_scale + srow,
                                               C::kScaleBytes, fb);
@@ -305,18 +400,35 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
                             }
                         }
                     }
-                    if (__shfl_sync(0xffffffffu, ab, 0)) {
+                    if (__any_sync(0xffffffffu, ab)) {
                         aborted = true;
+                        // tiles this run did issue are still counted for the drain below
+                        c += e - k;
                         break;
                     }
-                    ++c;
+                    c += e - k;
+                    k = e;
                 }
+                cj = nj;
+                ct = nt;
+                cpg = npg;
+            }
+        }
+        if (!aborted && lane == 0) {
+            // end marker for the consumers
+            if (wait_phase(qempty_bar(qi & 1), ((qi >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                reinterpret_cast<DescInfo *>(smem + L::kInfoOff)[qi & 1].end = 1;
+                mbar_arrive(qfull_bar(qi & 1));
+            } else {
+                aborted = true;
             }
         }
         if (aborted && lane == 0) {
             // let every copy this CTA started land before the CTA exits
-            for (int cc = max(0, c - STAGES); cc < c; ++cc) drain_phase(full_bar(cc % STAGES), (cc / STAGES) & 1);
-            if (q_issued >= 0) drain_phase(qfull_bar(q_issued & 1), (q_issued >> 1) & 1);
+            const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+            for (int cc = max(0, c - STAGES); cc < c; ++cc)
+                drain_phase(full_bar(cc % STAGES), (cc / STAGES) & 1, deadline);
+            if (q_issued >= 0) drain_phase(qfull_bar(q_issued & 1), (q_issued >> 1) & 1, deadline);
         }
         return;
     }
@@ -332,38 +444,32 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
     const int v_row = (KV == 0) ? tok_base + xr + (lane >> 4) * 8 : k_row;
     const int v_chunk = (KV == 0) ? ((lane >> 3) & 1) : (lane >> 4);
 
-    int c_start = 0;  // tiles of this CTA before the current descriptor
-    int qi = -1;      // accepted descriptors so far, minus one (Q ring and merge phases)
-    for (int i = 0; i < d_count; ++i) {
-        const Desc x = get_desc<PERSIST>(p, d_begin, i, st0, st1);
-        if (!x.ok) continue;
-        ++qi;
-        const int b = x.u / p.hkv, h = x.u - b * p.hkv;
-        const int n = x.t1 - x.t0;
+    for (int qi = 0;; ++qi) {
+        // ---- next descriptor from the producer (info + Q in shared memory)
+        if (!wait_phase(qfull_bar(qi & 1), (qi >> 1) & 1, abort_flag, p.status)) return;
+        const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + (qi & 1);
+        if (inf->end) break;
+        const int n = inf->n, slot = inf->slot, c_start = inf->c_start;
+        float qsc0 = p.score_scale, qsc1 = p.score_scale;
+        if (KV == 1) {
+            qsc0 *= inf->qscale[2 * tig];
+            qsc1 *= inf->qscale[2 * tig + 1];
+        }
 
         // ---- Q fragments (B operand, n = query head gid), zero past G
         constexpr int KSTEPS = (KV == 0) ? 8 : 4;
         uint32_t qf[KSTEPS][2];
-        if (!wait_phase(qfull_bar(qi & 1), (qi >> 1) & 1, abort_flag, p.status)) return;
         {
             const uint8_t *qs = smem + L::kQOff + (qi & 1) * L::kQSlot + gid * C::kQHeadBytes;
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
-                const int off = (KV == 0) ? (32 * ks + 4 * tig) : (32 * ks + 4 * tig);
+                const int off = 32 * ks + 4 * tig;
                 qf[ks][0] = gid < G ? *reinterpret_cast<const uint32_t *>(qs + off) : 0u;
                 qf[ks][1] = gid < G ? *reinterpret_cast<const uint32_t *>(qs + off + 16) : 0u;
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(qempty_bar(qi & 1));
-
-        // score scale for this thread's heads 2*tig, 2*tig+1 (log2 domain)
-        float qsc0 = p.score_scale, qsc1 = p.score_scale;
-        if (KV == 1) {
-            const int64_t qrow = static_cast<int64_t>(b) * p.hq + h * G;
-            qsc0 *= (2 * tig < G) ? p.q_scale[qrow + 2 * tig] : 0.f;
-            qsc1 *= (2 * tig + 1 < G) ? p.q_scale[qrow + 2 * tig + 1] : 0.f;
-        }
 
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
         float vsc = 1.f;  // E4M3: O holds the true output divided by vsc
@@ -513,7 +619,6 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
             if (lane == 0) mbar_arrive(empty_bar(stage));
         }
         if (aborted) return;
-        c_start += n;
 
         // ---- merge the consumer warps' (m, l, O) and write the partial
 #pragma unroll
@@ -570,7 +675,7 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
                     acc.w *= inv;
                     lse = (M + lg2(Lsum)) * kLn2;
                 }
-                const int64_t row = static_cast<int64_t>(x.slot) * G + hd;
+                const int64_t row = static_cast<int64_t>(slot) * G + hd;
                 *reinterpret_cast<float4 *>(p.partial_o + row * kHeadDim + d4) = acc;
                 if ((idx & 31) == 0) p.partial_lse[row] = lse;
             }

@@ -13,6 +13,7 @@ constexpr int kHeadDim = 128;  // d
 constexpr int kTile = 64;      // tokens per tile = tokens per page
 constexpr int kMaxGroup = 8;   // query heads per KV head handled in one MMA column block
 constexpr int kPlanMaxUnits = 16384;
+constexpr int kPlanMaxCtas = 16384;
 
 inline cudaStream_t to_cuda(dsa_stream s) { return reinterpret_cast<cudaStream_t>(s); }
 

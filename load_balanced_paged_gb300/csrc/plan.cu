@@ -2,11 +2,11 @@
 // KV lengths (HPC-Ops × SGLang blog, section "围绕活跃 KV 工作进行调度"; Hy3 preview
 // write-up, section 2.1.1 "Attention动态调度", "贪心装桶").
 //
-// One CTA of 1024 threads.  Instead of walking tiles one by one, it uses the closed
-// form of the greedy fill: with a real-valued budget T / C_eff, bin i ends where the
-// cumulative tile count first reaches floor((i+1) * T / C_eff), so the bin holding
-// global tile x is floor(((x+1) * C_eff - 1) / T).  Every unit and every descriptor
-// is then placed independently:
+// One CTA (256 or 1024 threads).  Instead of walking tiles one by one, it uses the
+// closed form of the greedy fill: with a real-valued budget T / C_eff, bin i holds the
+// global tiles [floor(i*T/C_eff), floor((i+1)*T/C_eff)); these starts go to a shared
+// table, and the bin holding a tile is found by binary search in it.  Every unit and
+// every descriptor is then placed independently:
 //   1. n_u = ceil(len_b / 64), exclusive scan -> P_u, total T;
 //   2. per unit, the number of bins it touches -> exclusive scan -> first slot;
 //   3. per bin, its first descriptor = first slot of the unit holding its first tile
@@ -17,14 +17,6 @@
 
 namespace dsa {
 namespace {
-
-__device__ __forceinline__ int64_t bin_of(int64_t x, int64_t T, int64_t C_eff) {
-    return ((x + 1) * C_eff - 1) / T;
-}
-
-__device__ __forceinline__ int64_t bin_start(int64_t i, int64_t T, int64_t C_eff) {
-    return (i * T) / C_eff;
-}
 
 // First index in a[0, n) with a[i] > x (a nondecreasing).
 __device__ __forceinline__ int upper_bound(const int32_t *a, int n, int64_t x) {
@@ -73,15 +65,17 @@ __device__ int64_t block_exclusive_scan(int32_t *a, int n, int64_t *warp_tot) {
     return total;
 }
 
-__global__ void __launch_bounds__(1024, 1)
+template <int NT>
+__global__ void __launch_bounds__(NT, 1)
 plan_kernel(const int32_t *__restrict__ seq_lens, int32_t batch, int32_t num_kv_heads, int32_t num_ctas,
             int32_t min_tiles, dsa_task_map map) {
     extern __shared__ int32_t smem[];
     __shared__ int64_t warp_tot[32];
     __shared__ int s_status;
     const int U = batch * num_kv_heads;
-    int32_t *sP = smem;             // [U + 1] first global tile of each unit, then T
-    int32_t *sBeg = smem + U + 1;   // [U + 1] first descriptor of each unit, then num_descs
+    int32_t *sP = smem;                 // [U + 1] first global tile of each unit, then T
+    int32_t *sBeg = smem + U + 1;       // [U + 1] first descriptor of each unit, then num_descs
+    int32_t *sBin = smem + 2 * (U + 1);  // [num_ctas + 1] first global tile of each bin, then T
     const int tid = threadIdx.x, nt = blockDim.x;
 
     if (tid == 0) s_status = 0;
@@ -108,12 +102,18 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int32_t batch, int32_t num_kv_
         sP[U] = static_cast<int32_t>(T);
         if (overflow) s_status |= DSA_DEV_BAD_SEQLEN;
     }
+    // bin i starts at global tile floor(i * T / C_eff): the cumulative budget, rounded down
+    for (int i = tid; C_eff > 0 && i <= C_eff; i += nt)
+        sBin[i] = static_cast<int32_t>(static_cast<uint64_t>(i) * static_cast<uint64_t>(T) /
+                                       static_cast<uint64_t>(C_eff));
     __syncthreads();
+    // bin holding global tile x: the last bin starting at or before x
+    auto bin_of = [&](int64_t x) -> int64_t { return upper_bound(sBin, static_cast<int>(C_eff), x) - 1; };
 
     // 2. bins touched by each unit
     for (int u = tid; u < U; u += nt) {
         const int64_t p = sP[u], n = overflow ? 0 : sP[u + 1] - p;
-        sBeg[u] = n > 0 ? static_cast<int32_t>(bin_of(p + n - 1, T, C_eff) - bin_of(p, T, C_eff) + 1) : 0;
+        sBeg[u] = n > 0 ? static_cast<int32_t>(bin_of(p + n - 1) - bin_of(p) + 1) : 0;
     }
     __syncthreads();
     int64_t nd = block_exclusive_scan(sBeg, U, warp_tot);
@@ -136,9 +136,8 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int32_t batch, int32_t num_kv_
         if (empty_map || i >= C_eff) {
             b = static_cast<int32_t>(nd);
         } else {
-            const int64_t x = bin_start(i, T, C_eff);
-            const int v = upper_bound(sP, U, x) - 1;
-            b = static_cast<int32_t>(sBeg[v] + (i - bin_of(sP[v], T, C_eff)));
+            const int v = upper_bound(sP, U, sBin[i]) - 1;
+            b = static_cast<int32_t>(sBeg[v] + (i - bin_of(sP[v])));
         }
         map.cta_desc_begin[i] = b;
     }
@@ -148,9 +147,9 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int32_t batch, int32_t num_kv_
         const int v = upper_bound(sBeg, U, d) - 1;
         const int64_t k = d - sBeg[v];
         const int64_t p = sP[v], n = sP[v + 1] - p;
-        const int64_t i = bin_of(p, T, C_eff) + k;
-        const int64_t g0 = max(bin_start(i, T, C_eff), p);
-        const int64_t g1 = min(bin_start(i + 1, T, C_eff), p + n);
+        const int64_t i = bin_of(p) + k;
+        const int64_t g0 = max(static_cast<int64_t>(sBin[i]), p);
+        const int64_t g1 = min(static_cast<int64_t>(sBin[i + 1]), p + n);
         int4 desc = make_int4(v, static_cast<int32_t>(g0 - p), static_cast<int32_t>(g1 - p),
                               static_cast<int32_t>(k));
         reinterpret_cast<int4 *>(map.descs)[d] = desc;
@@ -188,18 +187,24 @@ extern "C" dsa_status dsa_plan(const int32_t *seq_lens, int32_t batch, int32_t n
     if (tile != kTile) return DSA_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(map->descs) & 15u) != 0) return DSA_ERR_INVALID_ARG;
     const int64_t U = static_cast<int64_t>(batch) * num_kv_heads;
-    if (U > kPlanMaxUnits) return DSA_ERR_UNSUPPORTED;
+    if (U > kPlanMaxUnits || num_persistent_ctas > kPlanMaxCtas) return DSA_ERR_UNSUPPORTED;
     if (map->num_ctas != num_persistent_ctas || map->num_units != U) return DSA_ERR_INVALID_ARG;
     const int32_t need = dsa_max_descs(batch, num_kv_heads, num_persistent_ctas);
     if (need < 0) return DSA_ERR_INVALID_ARG;
     if (map->max_descs < need) return DSA_ERR_BUFFER_TOO_SMALL;
 
-    const size_t smem = sizeof(int32_t) * 2 * static_cast<size_t>(U + 1);
+    const size_t smem = sizeof(int32_t) * (2 * static_cast<size_t>(U + 1) + num_persistent_ctas + 1);
+    // small maps: fewer warps make the block-wide scans and barriers cheaper
+    if (U <= 2048 && num_persistent_ctas <= 2048) {
+        plan_kernel<256><<<1, 256, smem, to_cuda(stream)>>>(seq_lens, batch, num_kv_heads, num_persistent_ctas,
+                                                           min_tiles_per_split, *map);
+        return launch_status();
+    }
     if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(plan_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return DSA_ERR_CUDA;
-    plan_kernel<<<1, 1024, smem, to_cuda(stream)>>>(seq_lens, batch, num_kv_heads, num_persistent_ctas,
-                                                   min_tiles_per_split, *map);
+    plan_kernel<1024><<<1, 1024, smem, to_cuda(stream)>>>(seq_lens, batch, num_kv_heads, num_persistent_ctas,
+                                                         min_tiles_per_split, *map);
     return launch_status();
 }

@@ -169,11 +169,14 @@ def make_inputs(lengths, num_q_heads: int, num_kv_heads: int, kv_dtype: str = "b
     return out
 
 
-def make_workload(name: str, device="cpu", seed: int | None = None) -> dict:
+def make_workload(name: str, device="cpu", seed: int | None = None, max_requests: int | None = None) -> dict:
+    """The named workload; max_requests keeps only its first requests (small profiling cases)."""
     w = WORKLOADS[name]
     s = w.seed if seed is None else seed
     rng = np.random.default_rng(s)
     lens = draw_lengths(w.name, w.batch, rng)
+    if max_requests is not None:
+        lens = lens[:max_requests]
     inp = make_inputs(lens, w.num_q_heads, w.num_kv_heads, w.kv_dtype, s, device, rng=rng)
     inp["workload"] = w
     return inp
