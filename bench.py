@@ -8,9 +8,10 @@ persistent CTAs).  Prints ONE JSON line (rank 0).
   python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference] [--workload NAME]
 
 value: achieved KV GB/s over the whole step (algorithmic KV bytes / step time),
-summed over ranks; us_per_step is the same measurement as time.  L2 (129 MB) is
-flushed by writing a 2 x L2 buffer before every timed step, outside the timed
-events.  N > 1 runs independent replicas (one per GPU, no data-path collective).
+summed over ranks; us_per_step is the same measurement as time.  The workloads'
+KV (0.5-9.9 GB) is larger than L2 (126 MB), so steps run back to back without an
+L2 flush; inputs smaller than 2 x L2 get a 2 x L2 write-flush before every step,
+outside the timed events (config.l2 says which).  N > 1 runs independent replicas (one per GPU, no data-path collective).
 --impl reference times the fp64 CPU oracle on the host cores instead.
 """
 from __future__ import annotations
@@ -98,6 +99,31 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "window": window}
 
 
+def profile_traffic(workload: str, nbytes: int):
+    """DRAM traffic per decode launch from the committed ncu summary of this workload's
+    decode kernel (profiles/decode_<workload>[_small].md), scaled by KV bytes when the
+    capture was a smaller case of the same workload; None once the kernel source differs
+    from the one captured."""
+    import hashlib
+    import re
+    src = os.path.join(ROOT, "load_balanced_paged_gb300", "csrc", "attention.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    for suffix in ("", "_small"):
+        path = os.path.join(ROOT, "profiles", f"decode_{workload}{suffix}.md")
+        if not os.path.exists(path):
+            continue
+        text = open(path).read()
+        m_sha = re.search(r"sha256 `([0-9a-f]{64})`", text)
+        m_tr = re.search(r"traffic_bytes_per_launch: (\d+)", text)
+        m_alg = re.search(r"algorithmic_bytes_per_launch: (\d+)", text)
+        if not (m_sha and m_tr and m_alg) or m_sha.group(1) != sha:
+            return None, f"{os.path.basename(path)}: stale or incomplete"
+        tr, alg = int(m_tr.group(1)), int(m_alg.group(1))
+        note = os.path.basename(path) + ("" if alg == nbytes else f", scaled by KV bytes {nbytes}/{alg}")
+        return int(round(tr * nbytes / alg)), note
+    return None, "no committed capture for this workload"
+
+
 def flush_buffer(device):
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     return torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
@@ -105,6 +131,21 @@ def flush_buffer(device):
 
 def kv_bytes(inp):
     return workloads.kv_bytes(inp["seq_lens"].cpu().numpy(), inp["num_kv_heads"], inp["kv_dtype"])
+
+
+def replica_max(value: float, world: int, device) -> float:
+    """Max over ranks (replicas are independent; the only cross-rank step is this timing
+    reduction after the timed region)."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job KV GB/s: the bytes all replicas processed per step over the slowest rank's step."""
+    return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------------- our arm
@@ -137,8 +178,18 @@ def bench_ours(args, device, rank, world):
     def combine():
         dsa.combine(tm, po, pl, hq, out=out, out_lse=out_lse)
 
-    flush = flush_buffer(device)
     nbytes = kv_bytes(inp)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    # Inputs larger than L2 need no flush between steps; a write-flush would leave L2 dirty
+    # and bill the next step for ~L2-size of write-backs.  Small inputs are flushed.
+    do_flush = args.l2 == "flush" or (args.l2 == "auto" and nbytes < 2 * l2)
+    flush = flush_buffer(device) if do_flush else None
+    l2_note = ("flushed (2 x L2 write) before every timed step" if do_flush else
+               f"inputs larger than L2 ({nbytes / 1e6:.0f} MB of KV vs {l2 / 1e6:.0f} MB L2), no flush")
+
+    def flush_l2(k):
+        if flush is not None:
+            flush.fill_(float(k))
 
     def graphs_of(fns):
         """One CUDA graph per function (each a captured kernel launch)."""
@@ -152,22 +203,42 @@ def bench_ours(args, device, rank, world):
         return gs
 
     def timed(fns, steps, warmup):
-        """Replays the captured kernels with CUDA events between them; L2 is flushed before
-        each step, outside the events.  Returns ms [steps, len(fns)]."""
+        """Per-kernel device times: the kernels captured in ONE graph with event-record nodes
+        between them (no launch gaps counted), replayed `steps` times after an L2 flush.
+        Returns ms [steps, len(fns)]."""
         for _ in range(warmup):
             for f in fns:
                 f()
+        try:
+            evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(fns) + 1)]
+        except TypeError:  # torch without external events: one graph per kernel, events between
+            return timed_separate(fns, steps)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            evs[0].record()
+            for i, f in enumerate(fns):
+                f()
+                evs[i + 1].record()
+        torch.cuda.synchronize()
+        per = []
+        for k in range(steps):
+            flush_l2(k)
+            g.replay()
+            stream.synchronize()
+            per.append([evs[i].elapsed_time(evs[i + 1]) for i in range(len(fns))])
+        return np.array(per)
+
+    def timed_separate(fns, steps):
         gs = graphs_of(fns)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)] for _ in range(steps)]
         for k in range(steps):
-            flush.fill_(float(k))
+            flush_l2(k)
             ev[k][0].record(stream)
             for i, g in enumerate(gs):
                 g.replay()
                 ev[k][i + 1].record(stream)
         stream.synchronize()
-        per = np.array([[ev[k][i].elapsed_time(ev[k][i + 1]) for i in range(len(fns))] for k in range(steps)])
-        return per
+        return np.array([[ev[k][i].elapsed_time(ev[k][i + 1]) for i in range(len(fns))] for k in range(steps)])
 
     def timed_whole(fns, steps):
         """The same kernels captured as ONE graph (a production decode step) timed as a unit."""
@@ -178,7 +249,7 @@ def bench_ours(args, device, rank, world):
         torch.cuda.synchronize()
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
         for k in range(steps):
-            flush.fill_(float(k))
+            flush_l2(k)
             ev[k][0].record(stream)
             g.replay()
             ev[k][1].record(stream)
@@ -209,10 +280,7 @@ def bench_ours(args, device, rank, world):
 
     total_ms = float(step_ms.sum())
     per = timed([plan, decode, combine], max(10, min(args.steps, 500)), 0)
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = replica_max(total_ms, world, device)
     ms_per_step = total_ms / args.steps
     t_plan, t_dec, t_comb = (float(x) for x in per.mean(axis=0))
 
@@ -271,9 +339,10 @@ def bench_ours(args, device, rank, world):
 
     peak, peak_src = measured_peaks()
     achieved = nbytes / (t_dec * 1e-3) / 1e9
+    traffic, traffic_src = profile_traffic(name, nbytes)
     res = {
         "metric": METRIC,
-        "value": round(world * nbytes / (ms_per_step * 1e-3) / 1e9, 2),
+        "value": round(aggregate_gbs(nbytes, world, ms_per_step), 2),
         "unit": "GB/s",
         "us_per_step": round(ms_per_step * 1e3, 2),
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -285,7 +354,7 @@ def bench_ours(args, device, rank, world):
         "data": "synthetic (seeded; lengths, page permutation and N(0,1) values drawn as in workloads.py)",
         "config": {"workload": w.description, "name": name, "batch": B, "num_q_heads": hq, "num_kv_heads": hkv,
                    "head_dim": 128, "page_size": 64, "persistent_ctas": C, "min_tiles_per_split": m,
-                   "kv_bytes_per_step": nbytes, "l2": "flushed (2 x L2 write) before every timed step",
+                   "kv_bytes_per_step": nbytes, "l2": l2_note,
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "breakdown_us": {"plan": round(t_plan * 1e3, 2), "decode": round(t_dec * 1e3, 2),
                          "combine": round(t_comb * 1e3, 2)},
@@ -295,7 +364,7 @@ def bench_ours(args, device, rank, world):
         "roofline": {"bound": "hbm", "kernel": "attn_kernel (persistent decode)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "traffic": None},
+                     "algorithmic_bytes": nbytes, "traffic": traffic, "traffic_source": traffic_src},
         "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "us_per_step": round(e2e_ms * 1e3, 1), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
@@ -374,6 +443,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--requests", type=int, default=None, help="keep only the first N requests (profiling)")
+    ap.add_argument("--l2", choices=["auto", "flush", "none"], default="auto",
+                    help="auto: flush L2 between steps only when the KV bytes are below 2 x L2")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -78,6 +78,8 @@ struct Cfg<1> {  // E4M3 K/V and Q, fp32 scales
 
 constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
+constexpr int kQSlots = 2;  // descriptors handed ahead to the consumers (Q + info)
+
 template <int KV, int STAGES, int GROUPS>
 struct Layout {
     static constexpr int kNcw = GROUPS * 4;  // consumer warps
@@ -88,13 +90,14 @@ struct Layout {
     static constexpr int kQOff = STAGES * kStageBytes;
     static constexpr int kOStride = 132;  // floats per head row of a warp's O (padding avoids bank conflicts)
     static constexpr int kWarpFloats = kMaxGroup * kOStride + 2 * kMaxGroup;
-    static constexpr int kMergeOff = kQOff + 2 * kQSlot;
-    static constexpr int kBarOff = kMergeOff + kNcw * kWarpFloats * 4;
-    static constexpr int kNumBars = 2 * STAGES + 6;  // full, empty, qfull x2, qempty x2, merge_full, merge_done
+    static constexpr int kMergeOff = kQOff + kQSlots * kQSlot;
+    static constexpr int kMergeSlot = kNcw * kWarpFloats;  // floats per merge slot (2 slots)
+    static constexpr int kBarOff = kMergeOff + 2 * kMergeSlot * 4;
+    static constexpr int kNumBars = 2 * STAGES + 2 * kQSlots + 4;  // full, empty, qfull, qempty, merge_full x2, merge_done x2
     static constexpr int kNValidOff = kBarOff + kNumBars * 8;
     static constexpr int kAbortOff = kNValidOff + STAGES * 4;
-    static constexpr int kInfoOff = round_up(kAbortOff + 16, 64);  // 2 DescInfo slots, beside the 2 Q slots
-    static constexpr int kBytes = kInfoOff + 2 * 64;
+    static constexpr int kInfoOff = round_up(kAbortOff + 16, 64);  // one DescInfo per Q slot
+    static constexpr int kBytes = kInfoOff + kQSlots * 64;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static_assert(STAGES % GROUPS == 0, "each stage must belong to one consumer group");
     static_assert(kStageBytes % 1024 == 0 && kQOff % 1024 == 0, "swizzled TMA boxes need 1024-byte alignment");
@@ -183,9 +186,9 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto qfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-    auto qempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 + s); };
-    const uint32_t merge_full = bar0 + 8u * (2 * STAGES + 4);
-    const uint32_t merge_done = bar0 + 8u * (2 * STAGES + 5);
+    auto qempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + kQSlots + s); };
+    auto merge_full = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + s); };
+    auto merge_done = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 2 + s); };
     int *nvalid = reinterpret_cast<int *>(smem + L::kNValidOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbortOff);
 
@@ -225,12 +228,14 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 4);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kQSlots; ++s) {
             mbar_init(qfull_bar(s), 1);
             mbar_init(qempty_bar(s), NCW);
         }
-        mbar_init(merge_full, NCW);
-        mbar_init(merge_done, NCW);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(merge_full(s), NCW);
+            mbar_init(merge_done(s), NCW);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -344,10 +349,11 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
                         const int n = __shfl_sync(0xffffffffu, wn, j);
                         const int slot = __shfl_sync(0xffffffffu, wslot, j);
                         if (lane == 0) {
-                            if (!wait_phase(qempty_bar(qi & 1), ((qi >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                            const int qs_ = qi % kQSlots;
+                            if (!wait_phase(qempty_bar(qs_), ((qi / kQSlots) & 1) ^ 1, abort_flag, p.status)) {
                                 ab = 1;
                             } else {
-                                DescInfo *inf = reinterpret_cast<DescInfo *>(smem + L::kInfoOff) + (qi & 1);
+                                DescInfo *inf = reinterpret_cast<DescInfo *>(smem + L::kInfoOff) + qs_;
                                 inf->end = 0;
                                 inf->b = b;
                                 inf->h = h;
@@ -357,9 +363,9 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
 #pragma unroll
                                 for (int g = 0; g < kMaxGroup; ++g) inf->qscale[g] = qs[g];
                                 const uint32_t bytes = G * C::kQHeadBytes;
-                                mbar_arrive_expect_tx(qfull_bar(qi & 1), bytes);
+                                mbar_arrive_expect_tx(qfull_bar(qs_), bytes);
                                 const uint8_t *src = p.q + (static_cast<int64_t>(b) * p.hq + h * G) * C::kQHeadBytes;
-                                bulk_load(sbase + L::kQOff + (qi & 1) * L::kQSlot, src, bytes, qfull_bar(qi & 1));
+                                bulk_load(sbase + L::kQOff + qs_ * L::kQSlot, src, bytes, qfull_bar(qs_));
                                 q_issued = qi;
                             }
                         }
@@ -416,9 +422,9 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
         }
         if (!aborted && lane == 0) {
             // end marker for the consumers
-            if (wait_phase(qempty_bar(qi & 1), ((qi >> 1) & 1) ^ 1, abort_flag, p.status)) {
-                reinterpret_cast<DescInfo *>(smem + L::kInfoOff)[qi & 1].end = 1;
-                mbar_arrive(qfull_bar(qi & 1));
+            if (wait_phase(qempty_bar(qi % kQSlots), ((qi / kQSlots) & 1) ^ 1, abort_flag, p.status)) {
+                reinterpret_cast<DescInfo *>(smem + L::kInfoOff)[qi % kQSlots].end = 1;
+                mbar_arrive(qfull_bar(qi % kQSlots));
             } else {
                 aborted = true;
             }
@@ -428,7 +434,7 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
             const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
             for (int cc = max(0, c - STAGES); cc < c; ++cc)
                 drain_phase(full_bar(cc % STAGES), (cc / STAGES) & 1, deadline);
-            if (q_issued >= 0) drain_phase(qfull_bar(q_issued & 1), (q_issued >> 1) & 1, deadline);
+            if (q_issued >= 0) drain_phase(qfull_bar(q_issued % kQSlots), (q_issued / kQSlots) & 1, deadline);
         }
         return;
     }
@@ -444,10 +450,56 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
     const int v_row = (KV == 0) ? tok_base + xr + (lane >> 4) * 8 : k_row;
     const int v_chunk = (KV == 0) ? ((lane >> 3) & 1) : (lane >> 4);
 
+    // Merge of descriptor d (states deposited in merge slot d & 1 by all consumer warps):
+    // the warps' (m, l, O) combined under one softmax, written as a normalised partial.
+    auto merge_and_write = [&](int d, int pslot) -> bool {
+        const int ms = d & 1;
+        if (!wait_phase(merge_full(ms), (d >> 1) & 1, abort_flag, p.status)) return false;
+        const float *M0 = reinterpret_cast<const float *>(smem + L::kMergeOff) + ms * L::kMergeSlot;
+        for (int idx = warp * 32 + lane; idx < G * 32; idx += NCW * 32) {
+            const int hd = idx >> 5, d4 = (idx & 31) * 4;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < NCW; ++w) M = fmaxf(M, M0[w * L::kWarpFloats + kMaxGroup * L::kOStride + hd]);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float lse = -INFINITY;
+            if (M != -INFINITY) {
+                float Lsum = 0.f;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) {
+                    const float *Ww = M0 + w * L::kWarpFloats;
+                    const float e = ex2(Ww[kMaxGroup * L::kOStride + hd] - M);
+                    Lsum += e * Ww[kMaxGroup * L::kOStride + kMaxGroup + hd];
+                    const float4 v = *reinterpret_cast<const float4 *>(Ww + hd * L::kOStride + d4);
+                    acc.x += e * v.x;
+                    acc.y += e * v.y;
+                    acc.z += e * v.z;
+                    acc.w += e * v.w;
+                }
+                const float inv = 1.f / Lsum;
+                acc.x *= inv;
+                acc.y *= inv;
+                acc.z *= inv;
+                acc.w *= inv;
+                lse = (M + lg2(Lsum)) * kLn2;
+            }
+            const int64_t row = static_cast<int64_t>(pslot) * G + hd;
+            *reinterpret_cast<float4 *>(p.partial_o + row * kHeadDim + d4) = acc;
+            if ((idx & 31) == 0) p.partial_lse[row] = lse;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(merge_done(ms));
+        return true;
+    };
+
+    // The merge of a descriptor runs after the NEXT descriptor's tiles, when every warp
+    // deposited its state long ago: no warp waits for the slowest at each boundary.
+    int pend_d = -1, pend_slot = 0;
     for (int qi = 0;; ++qi) {
         // ---- next descriptor from the producer (info + Q in shared memory)
-        if (!wait_phase(qfull_bar(qi & 1), (qi >> 1) & 1, abort_flag, p.status)) return;
-        const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + (qi & 1);
+        const int qslot = qi % kQSlots;
+        if (!wait_phase(qfull_bar(qslot), (qi / kQSlots) & 1, abort_flag, p.status)) return;
+        const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
         if (inf->end) break;
         const int n = inf->n, slot = inf->slot, c_start = inf->c_start;
         float qsc0 = p.score_scale, qsc1 = p.score_scale;
@@ -460,7 +512,7 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
         constexpr int KSTEPS = (KV == 0) ? 8 : 4;
         uint32_t qf[KSTEPS][2];
         {
-            const uint8_t *qs = smem + L::kQOff + (qi & 1) * L::kQSlot + gid * C::kQHeadBytes;
+            const uint8_t *qs = smem + L::kQOff + qslot * L::kQSlot + gid * C::kQHeadBytes;
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
                 const int off = 32 * ks + 4 * tig;
@@ -469,7 +521,7 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(qempty_bar(qi & 1));
+        if (lane == 0) mbar_arrive(qempty_bar(qslot));
 
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
         float vsc = 1.f;  // E4M3: O holds the true output divided by vsc
@@ -620,14 +672,15 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
         }
         if (aborted) return;
 
-        // ---- merge the consumer warps' (m, l, O) and write the partial
+        // ---- deposit this warp's (m, l, O) in merge slot qi & 1, then merge the previous descriptor
 #pragma unroll
         for (int o_ = 4; o_ < 32; o_ <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
             l1 += __shfl_xor_sync(0xffffffffu, l1, o_);
         }
-        if (!wait_phase(merge_done, (qi & 1) ^ 1, abort_flag, p.status)) return;
-        float *W = reinterpret_cast<float *>(smem + L::kMergeOff) + warp * L::kWarpFloats;
+        const int ms = qi & 1;
+        if (!wait_phase(merge_done(ms), ((qi >> 1) & 1) ^ 1, abort_flag, p.status)) return;
+        float *W = reinterpret_cast<float *>(smem + L::kMergeOff) + ms * L::kMergeSlot + warp * L::kWarpFloats;
         if (gid == 0) {
             W[kMaxGroup * L::kOStride + 2 * tig] = m0;
             W[kMaxGroup * L::kOStride + 2 * tig + 1] = m1;
@@ -644,45 +697,12 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
             W[(2 * tig + 1) * L::kOStride + d1] = o[mb][3] * vsc;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(merge_full);
-        if (!wait_phase(merge_full, qi & 1, abort_flag, p.status)) return;
-        {
-            const float *M0 = reinterpret_cast<const float *>(smem + L::kMergeOff);
-            for (int idx = warp * 32 + lane; idx < G * 32; idx += NCW * 32) {
-                const int hd = idx >> 5, d4 = (idx & 31) * 4;
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < NCW; ++w) M = fmaxf(M, M0[w * L::kWarpFloats + kMaxGroup * L::kOStride + hd]);
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                float lse = -INFINITY;
-                if (M != -INFINITY) {
-                    float Lsum = 0.f;
-#pragma unroll
-                    for (int w = 0; w < NCW; ++w) {
-                        const float *Ww = M0 + w * L::kWarpFloats;
-                        const float e = ex2(Ww[kMaxGroup * L::kOStride + hd] - M);
-                        Lsum += e * Ww[kMaxGroup * L::kOStride + kMaxGroup + hd];
-                        const float4 v = *reinterpret_cast<const float4 *>(Ww + hd * L::kOStride + d4);
-                        acc.x += e * v.x;
-                        acc.y += e * v.y;
-                        acc.z += e * v.z;
-                        acc.w += e * v.w;
-                    }
-                    const float inv = 1.f / Lsum;
-                    acc.x *= inv;
-                    acc.y *= inv;
-                    acc.z *= inv;
-                    acc.w *= inv;
-                    lse = (M + lg2(Lsum)) * kLn2;
-                }
-                const int64_t row = static_cast<int64_t>(slot) * G + hd;
-                *reinterpret_cast<float4 *>(p.partial_o + row * kHeadDim + d4) = acc;
-                if ((idx & 31) == 0) p.partial_lse[row] = lse;
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(merge_done);
+        if (lane == 0) mbar_arrive(merge_full(ms));
+        if (pend_d >= 0 && !merge_and_write(pend_d, pend_slot)) return;
+        pend_d = qi;
+        pend_slot = slot;
     }
+    if (pend_d >= 0) merge_and_write(pend_d, pend_slot);
 }
 
 // ------------------------------------------------------------------ host side
