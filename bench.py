@@ -178,6 +178,13 @@ def bench_ours(args, device, rank, world):
     def combine():
         dsa.combine(tm, po, pl, hq, out=out, out_lse=out_lse)
 
+    counters = tm.unit_counters()
+
+    def decode_fused():
+        dsa.decode_fused(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
+                         inp["sm_scale"], out=out, out_lse=out_lse, partial_o=po, partial_lse=pl,
+                         unit_counters=counters, **kw)
+
     nbytes = kv_bytes(inp)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     # Inputs larger than L2 need no flush between steps; a write-flush would leave L2 dirty
@@ -258,6 +265,7 @@ def bench_ours(args, device, rank, world):
 
     # warm-up + correctness gate of this configuration (status word must be clean)
     timed([plan, decode, combine], 1, args.warmup)
+    timed([plan, decode_fused], 1, args.warmup)
     torch.cuda.synchronize()
     status = dsa.get_status(tm)
     if status != 0:
@@ -279,7 +287,11 @@ def bench_ours(args, device, rank, world):
     clk = clocks.summary(t_wall0, t_wall1)
 
     total_ms = float(step_ms.sum())
-    per = timed([plan, decode, combine], max(10, min(args.steps, 500)), 0)
+    nrep = max(10, min(args.steps, 500))
+    fused_ms = float(timed_whole([plan, decode_fused], nrep).mean())
+    per = timed([plan, decode, combine], nrep, 0)
+    per_f = timed([plan, decode_fused], nrep, 0)
+    t_dec_fused = float(per_f[:, 1].mean())
     total_ms = replica_max(total_ms, world, device)
     ms_per_step = total_ms / args.steps
     t_plan, t_dec, t_comb = (float(x) for x in per.mean(axis=0))
@@ -329,6 +341,9 @@ def bench_ours(args, device, rank, world):
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
+    if dsa.get_status(tm) != 0:
+        raise RuntimeError("device status set on the end-to-end step")
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
@@ -356,12 +371,15 @@ def bench_ours(args, device, rank, world):
                    "head_dim": 128, "page_size": 64, "persistent_ctas": C, "min_tiles_per_split": m,
                    "kv_bytes_per_step": nbytes, "l2": l2_note,
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "step": "dsa_plan -> dsa_decode -> dsa_combine, one CUDA graph, programmatic dependent launch",
         "breakdown_us": {"plan": round(t_plan * 1e3, 2), "decode": round(t_dec * 1e3, 2),
                          "combine": round(t_comb * 1e3, 2)},
-        "kv_gbs_decode_plus_combine": round(nbytes / ((t_dec + t_comb) * 1e-3) / 1e9, 1),
+        "fused_combine": {"us_per_step": round(fused_ms * 1e3, 2),
+                          "decode_fused_us": round(t_dec_fused * 1e3, 2),
+                          "note": "dsa_plan -> dsa_decode_fused (combine inside the persistent kernel)"},
         "pct_of_nominal_8tbs": round(100 * nbytes / (ms_per_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 1),
         "static": static,
-        "roofline": {"bound": "hbm", "kernel": "attn_kernel (persistent decode)",
+        "roofline": {"bound": "hbm", "kernel": "attn_kernel (persistent decode, dsa_decode)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "algorithmic_bytes": nbytes, "traffic": traffic, "traffic_source": traffic_src},

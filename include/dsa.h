@@ -25,7 +25,10 @@
  *   - All array arguments are DEVICE pointers owned by the caller; the library
  *     never allocates, frees or synchronises (dsa_get_status and
  *     dsa_read_status excepted).  Work is enqueued on `stream` (a cudaStream_t;
- *     NULL = the legacy default stream) and returns before it runs.
+ *     NULL = the legacy default stream) and returns before it runs.  Kernels are
+ *     launched with programmatic stream serialization: each may start while the
+ *     previous kernel in the stream finishes, and waits for it (griddepcontrol)
+ *     before reading any global memory.
  *   - Shapes: B = batch, Hq = query heads, Hkv = KV heads, G = Hq / Hkv query
  *     heads per KV head (query head j reads KV head j / G), d = head_dim = 128,
  *     P = page_size = 64 tokens = the tile.  Unit u = (request b, KV head h),
@@ -158,6 +161,36 @@ dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *q_scale,
                       int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
                       const dsa_task_map *map, float *partial_o, float *partial_lse,
                       dsa_stream stream);
+
+/*
+ * dsa_decode_fused -- dsa_decode with the combine step done inside the persistent
+ * kernel: the blog's persistent kernel and combine kernel as one launch, with the
+ * same results as dsa_decode followed by dsa_combine up to rounding order.
+ *   - A unit covered by a single descriptor writes its final output directly.
+ *   - For a unit with several partials, each descriptor's partial is published at
+ *     GPU scope and counted in unit_counters[u]; the CTA whose count completes the
+ *     unit merges all its partials (same formula as dsa_combine) and resets the
+ *     counter to 0.  No CTA waits for another.  A dedicated epilogue warp does this
+ *     off the consumers' path.
+ *   - Units with no tiles get output 0 and LSE -inf.
+ * Extra arguments:
+ *   - unit_counters [B*Hkv] int32: all 0 before the first call.  The kernel leaves
+ *     them 0 after every completed step; after a step that reported
+ *     DSA_DEV_TIMEOUT the caller must zero them again.
+ *   - out [B, Hq, 128] in out_dtype (DSA_BF16 or DSA_FP32), 16-byte aligned.
+ *   - out_lse [B, Hq] fp32, or NULL.
+ * The map's unit_partial_begin and unit_num_partials must be present.  Other
+ * arguments and errors are as for dsa_decode.
+ */
+dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_scale,
+                            const void *k_pages, const void *v_pages, dsa_dtype kv_dtype,
+                            const float *k_scale, const float *v_scale,
+                            const int32_t *block_table, int32_t max_pages_per_req, int32_t num_pages,
+                            const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
+                            const dsa_task_map *map, float *partial_o, float *partial_lse,
+                            int32_t *unit_counters, void *out, dsa_dtype out_dtype, float *out_lse,
+                            dsa_stream stream);
 
 /*
  * dsa_combine -- the combine kernel (blog, "围绕活跃 KV 工作进行调度": reads the

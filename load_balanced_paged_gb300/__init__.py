@@ -53,6 +53,8 @@ _lib.dsa_plan.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, _TMP, _vp]
 _lib.dsa_plan.restype = ctypes.c_int
 _lib.dsa_decode.argtypes = _attn_args + [_TMP, _vp, _vp, _vp]
 _lib.dsa_decode.restype = ctypes.c_int
+_lib.dsa_decode_fused.argtypes = _attn_args + [_TMP, _vp, _vp, _vp, _vp, _i32, _vp, _vp]
+_lib.dsa_decode_fused.restype = ctypes.c_int
 _lib.dsa_combine.argtypes = [_TMP, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]
 _lib.dsa_combine.restype = ctypes.c_int
 _lib.dsa_static_num_splits.argtypes = [_i32, _i32, _i32]
@@ -123,6 +125,14 @@ class TaskMap:
                                     self.unit_partial_begin.data_ptr(), self.unit_num_partials.data_ptr(),
                                     self.meta.data_ptr(), md, num_ctas, units)
 
+    def unit_counters(self) -> torch.Tensor:
+        """Zeroed [B*Hkv] int32 counters for dsa_decode_fused, kept with the map."""
+        c = getattr(self, "_unit_counters", None)
+        if c is None:
+            c = torch.zeros(max(self.num_units, 1), dtype=torch.int32, device=self.meta.device)
+            self._unit_counters = c
+        return c
+
     def host(self) -> dict:
         """Copies of the map (synchronises): the same keys as the oracle's plan."""
         meta = self.meta.cpu().numpy()
@@ -173,6 +183,27 @@ def decode(q, k_pages, v_pages, block_table, seq_lens, task_map: TaskMap, sm_sca
                          _stream(stream))
     _check(rc, "dsa_decode")
     return partial_o, partial_lse
+
+
+def decode_fused(q, k_pages, v_pages, block_table, seq_lens, task_map: TaskMap, sm_scale: float, out=None,
+                 out_lse=None, out_dtype=torch.bfloat16, partial_o=None, partial_lse=None, unit_counters=None,
+                 q_scale=None, k_scale=None, v_scale=None, stream=None):
+    """dsa_decode_fused: decode and combine in one persistent launch.  unit_counters
+    ([B*Hkv] int32, zero) defaults to a buffer kept on the task map."""
+    B, hq, _ = q.shape
+    G = hq // task_map.num_kv_heads
+    if partial_o is None:
+        partial_o, partial_lse = partial_buffers(task_map.max_descs, G, q.device)
+    if unit_counters is None:
+        unit_counters = task_map.unit_counters()
+    if out is None:
+        out = torch.empty(B, hq, HEAD_DIM, dtype=out_dtype, device=q.device)
+    args = _attn_args(q, k_pages, v_pages, block_table, seq_lens, task_map.num_kv_heads, sm_scale,
+                      q_scale, k_scale, v_scale)
+    rc = _lib.dsa_decode_fused(*args, ctypes.byref(task_map.struct), _ptr(partial_o), _ptr(partial_lse),
+                               _ptr(unit_counters), _ptr(out), _dtype_code(out), _ptr(out_lse), _stream(stream))
+    _check(rc, "dsa_decode_fused")
+    return out
 
 
 def combine(task_map: TaskMap, partial_o, partial_lse, num_q_heads: int, out=None, out_lse=None,
@@ -243,6 +274,20 @@ def read_status(status: torch.Tensor) -> int:
 
 def status_string(code: int) -> str:
     return _lib.dsa_status_string(code).decode()
+
+
+def attention_fused(inp: dict, num_ctas: int, min_tiles_per_split: int = 4, out_dtype=torch.bfloat16,
+                    task_map: TaskMap | None = None, stream=None):
+    """One decode step with the combine fused into the persistent kernel: plan, decode_fused.
+    Returns (out, out_lse, task_map)."""
+    tm = plan(inp["seq_lens"], inp["num_kv_heads"], num_ctas, min_tiles_per_split, task_map=task_map,
+              stream=stream)
+    B = inp["seq_lens"].shape[0]
+    out_lse = torch.empty(B, inp["num_q_heads"], dtype=torch.float32, device=inp["q"].device)
+    out = decode_fused(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
+                       inp["sm_scale"], out_lse=out_lse, out_dtype=out_dtype, q_scale=inp.get("q_scale"),
+                       k_scale=inp.get("k_scale"), v_scale=inp.get("v_scale"), stream=stream)
+    return out, out_lse, tm
 
 
 def attention(inp: dict, num_ctas: int, min_tiles_per_split: int = 4, out_dtype=torch.bfloat16,

@@ -59,6 +59,13 @@ struct KernelParams {
     float *partial_o;
     float *partial_lse;
     int32_t *status;
+    // fused combine (dsa_decode_fused)
+    const int32_t *unit_partial_begin;
+    const int32_t *unit_num_partials;
+    int32_t *unit_counters;  // [B * Hkv]: partials of the unit published so far; 0 between steps
+    void *out;               // [B, Hq, 128] bf16 or fp32
+    int32_t out_bf16;
+    float *out_lse;          // [B, Hq] or null
 };
 
 template <int KV>
@@ -78,12 +85,14 @@ struct Cfg<1> {  // E4M3 K/V and Q, fp32 scales
 
 constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
-constexpr int kQSlots = 2;  // descriptors handed ahead to the consumers (Q + info)
+constexpr int kQSlots = 2;   // descriptors handed ahead to the consumers (Q + info)
+constexpr int kEpiRing = 8;  // merged descriptors the epilogue warp may lag behind (fused combine)
 
 template <int KV, int STAGES, int GROUPS>
 struct Layout {
     static constexpr int kNcw = GROUPS * 4;  // consumer warps
-    static constexpr int kThreads = (kNcw + 1) * 32;
+    static constexpr int kThreads = (kNcw + 1) * 32;       // consumers + producer
+    static constexpr int kThreadsFused = (kNcw + 2) * 32;  // + epilogue warp (fused combine)
     static constexpr int kStageTx = 2 * Cfg<KV>::kTileBytes + 2 * Cfg<KV>::kScaleBytes;
     static constexpr int kStageBytes = round_up(kStageTx, 1024);
     static constexpr int kQSlot = kMaxGroup * Cfg<KV>::kQHeadBytes;
@@ -93,11 +102,13 @@ struct Layout {
     static constexpr int kMergeOff = kQOff + kQSlots * kQSlot;
     static constexpr int kMergeSlot = kNcw * kWarpFloats;  // floats per merge slot (2 slots)
     static constexpr int kBarOff = kMergeOff + 2 * kMergeSlot * 4;
-    static constexpr int kNumBars = 2 * STAGES + 2 * kQSlots + 4;  // full, empty, qfull, qempty, merge_full x2, merge_done x2
+    // full, empty, qfull, qempty, merge_full x2, merge_done x2, epi_ready, epi_free
+    static constexpr int kNumBars = 2 * STAGES + 2 * kQSlots + 4 + 2 * kEpiRing;
     static constexpr int kNValidOff = kBarOff + kNumBars * 8;
     static constexpr int kAbortOff = kNValidOff + STAGES * 4;
     static constexpr int kInfoOff = round_up(kAbortOff + 16, 64);  // one DescInfo per Q slot
-    static constexpr int kBytes = kInfoOff + kQSlots * 64;
+    static constexpr int kEpiOff = kInfoOff + kQSlots * 64;  // kEpiRing EpiRecords + descriptor total
+    static constexpr int kBytes = kEpiOff + kEpiRing * 16 + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static_assert(STAGES % GROUPS == 0, "each stage must belong to one consumer group");
     static_assert(kStageBytes % 1024 == 0 && kQOff % 1024 == 0, "swizzled TMA boxes need 1024-byte alignment");
@@ -116,10 +127,16 @@ struct DescInfo {
     int n;        // tiles
     int slot;     // partial-output slot
     int c_start;  // ring position of the descriptor's first tile
-    int pad[2];
+    int np;       // partials of the descriptor's unit (fused combine)
+    int pbeg;     // first partial slot of the unit (fused combine)
     float qscale[kMaxGroup];  // E4M3: q_scale of the G query heads
 };
 static_assert(sizeof(DescInfo) == 64, "DescInfo slot size");
+
+// What the consumers hand the epilogue warp with each merged descriptor (fused combine).
+struct EpiRecord {
+    int b, h, np, pbeg;
+};
 
 template <bool PERSIST>
 __device__ __forceinline__ Desc get_desc(const KernelParams &p, int d_begin, int i, int t0s, int t1s) {
@@ -172,8 +189,94 @@ __device__ __forceinline__ uint32_t tok_mask(int t, int nv) {
     return (t < nv ? 0x0000FFFFu : 0u) | (t + 1 < nv ? 0xFFFF0000u : 0u);
 }
 
-template <int KV, int STAGES, int GROUPS, bool PERSIST>
-__global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
+template <typename T>
+__device__ __forceinline__ void store_out4(void *out, int64_t row, int lane, float4 v, int bf16) {
+    if (bf16) {
+        const uint32_t lo = pack_bf16x2(v.x, v.y), hi = pack_bf16x2(v.z, v.w);
+        reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + row * kHeadDim)[lane] = make_uint2(lo, hi);
+    } else {
+        reinterpret_cast<float4 *>(static_cast<float *>(out) + row * kHeadDim)[lane] = v;
+    }
+}
+
+// Last-arriver merge of a unit's partials by one warp (fused combine): per query head the
+// global softmax over the partials' LSEs; lane = 4 output dims.  The LSEs of up to 32
+// partials are held one per lane, so the per-head maxima and sums are warp reductions, and
+// the G rows of each partial are loaded together.
+__device__ __noinline__ void combine_unit(const KernelParams &p, int lane, int ub, int uh, int unp, int upbeg) {
+    const int G = p.G;
+    float4 acc[kMaxGroup];
+    float Lh[kMaxGroup];
+#pragma unroll
+    for (int hd = 0; hd < kMaxGroup; ++hd) {
+        acc[hd] = make_float4(0.f, 0.f, 0.f, 0.f);
+        Lh[hd] = -INFINITY;
+    }
+    for (int k0 = 0; k0 < unp; k0 += 32) {
+        const int kn = min(32, unp - k0);
+        // this chunk's LSEs: lane k holds partial k0 + k
+        float lk[kMaxGroup];
+#pragma unroll
+        for (int hd = 0; hd < kMaxGroup; ++hd)
+            lk[hd] = (lane < kn && hd < G) ? __ldcg(p.partial_lse + static_cast<int64_t>(upbeg + k0 + lane) * G + hd)
+                                           : -INFINITY;
+        // fold the chunk into the running (L, acc) per head: L' = log(e^L + sum e^lk)
+        float scale[kMaxGroup], wk[kMaxGroup];
+#pragma unroll
+        for (int hd = 0; hd < kMaxGroup; ++hd) {
+            float m = lk[hd];
+#pragma unroll
+            for (int o_ = 1; o_ < 32; o_ <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o_));
+            m = fmaxf(m, Lh[hd]);
+            float e = (lk[hd] == -INFINITY) ? 0.f : exp2f((lk[hd] - m) * kLog2e);
+            float sum = e;
+#pragma unroll
+            for (int o_ = 1; o_ < 32; o_ <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o_);
+            const float eprev = (Lh[hd] == -INFINITY) ? 0.f : exp2f((Lh[hd] - m) * kLog2e);
+            const float tot = sum + eprev;
+            const float Lnew = tot > 0.f ? m + logf(tot) : -INFINITY;
+            scale[hd] = tot > 0.f ? eprev / tot : 0.f;   // weight of what acc already holds
+            wk[hd] = tot > 0.f ? e / tot : 0.f;          // weight of this lane's partial
+            Lh[hd] = Lnew;
+        }
+#pragma unroll
+        for (int hd = 0; hd < kMaxGroup; ++hd) {
+            acc[hd].x *= scale[hd];
+            acc[hd].y *= scale[hd];
+            acc[hd].z *= scale[hd];
+            acc[hd].w *= scale[hd];
+        }
+        for (int k = 0; k < kn; ++k) {
+            const float4 *row = reinterpret_cast<const float4 *>(p.partial_o + static_cast<int64_t>(upbeg + k0 + k) * G * kHeadDim);
+            float4 v[kMaxGroup];
+#pragma unroll
+            for (int hd = 0; hd < kMaxGroup; ++hd)
+                if (hd < G) v[hd] = __ldcg(row + hd * (kHeadDim / 4) + lane);
+#pragma unroll
+            for (int hd = 0; hd < kMaxGroup; ++hd) {
+                if (hd >= G) continue;
+                const float w = __shfl_sync(0xffffffffu, wk[hd], k);
+                acc[hd].x += w * v[hd].x;
+                acc[hd].y += w * v[hd].y;
+                acc[hd].z += w * v[hd].z;
+                acc[hd].w += w * v[hd].w;
+            }
+        }
+    }
+#pragma unroll
+    for (int hd = 0; hd < kMaxGroup; ++hd) {
+        if (hd >= G) continue;
+        const int64_t orow = static_cast<int64_t>(ub) * p.hq + uh * G + hd;
+        store_out4<float>(p.out, orow, lane, acc[hd], p.out_bf16);
+        if (lane == 0 && p.out_lse) p.out_lse[orow] = Lh[hd];
+    }
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+template <int KV, int STAGES, int GROUPS, bool PERSIST, bool FUSE>
+__global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS>::kThreadsFused
+                                       : Layout<KV, STAGES, GROUPS>::kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const KernelParams p) {
     using L = Layout<KV, STAGES, GROUPS>;
@@ -189,17 +292,59 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
     auto qempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + kQSlots + s); };
     auto merge_full = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + s); };
     auto merge_done = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 2 + s); };
+    auto epi_ready = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 4 + s); };
+    auto epi_free = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 4 + kEpiRing + s); };
+    EpiRecord *epi_rec = reinterpret_cast<EpiRecord *>(smem + L::kEpiOff);
+    volatile int *epi_total = reinterpret_cast<volatile int *>(smem + L::kEpiOff + kEpiRing * sizeof(EpiRecord));
     int *nvalid = reinterpret_cast<int *>(smem + L::kNValidOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbortOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G;
 
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 4);
+        }
+        for (int s = 0; s < kQSlots; ++s) {
+            mbar_init(qfull_bar(s), 1);
+            mbar_init(qempty_bar(s), NCW);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(merge_full(s), NCW);
+            mbar_init(merge_done(s), NCW);
+        }
+        for (int s = 0; s < kEpiRing; ++s) {
+            mbar_init(epi_ready(s), NCW);
+            mbar_init(epi_free(s), 1);
+        }
+        *epi_total = -1;
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    grid_launch_dependents();
+    grid_dependency_wait();  // task map, lengths, pages and Q from earlier kernels
+
     // ---- this CTA's work
     int d_begin = 0, d_count = 1, st0 = 0, st1 = 0;
     if (PERSIST) {
         d_begin = p.cta_desc_begin[blockIdx.x];
         d_count = p.cta_desc_begin[blockIdx.x + 1] - d_begin;
+        if (FUSE && warp == NCW + 1) {
+            // units with no tiles have no descriptor: their output is 0 and their LSE -inf
+            for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+                if (p.unit_num_partials[u] != 0) continue;
+                const int b = u / p.hkv, h = u - b * p.hkv;
+                for (int i = lane; i < G * (kHeadDim / 4); i += 32) {
+                    const int64_t orow = static_cast<int64_t>(b) * p.hq + h * G + i / (kHeadDim / 4);
+                    store_out4<float>(p.out, orow, i % (kHeadDim / 4), make_float4(0.f, 0.f, 0.f, 0.f), p.out_bf16);
+                    if (i % (kHeadDim / 4) == 0 && p.out_lse) p.out_lse[orow] = -INFINITY;
+                }
+            }
+        }
         if (d_count <= 0) return;
     } else {
         const int b = blockIdx.z;
@@ -223,24 +368,6 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
         }
     }
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 4);
-        }
-        for (int s = 0; s < kQSlots; ++s) {
-            mbar_init(qfull_bar(s), 1);
-            mbar_init(qempty_bar(s), NCW);
-        }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(merge_full(s), NCW);
-            mbar_init(merge_done(s), NCW);
-        }
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    __syncthreads();
-
     if (warp == NCW) {
         // =========================== producer warp ===========================
         // The CTA's descriptors are read 32 at a time (one per lane, with their
@@ -258,7 +385,7 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
         bool aborted = false;
         for (int wbase = 0; wbase < d_count && !aborted; wbase += 32) {
             // ---- window: descriptor wbase + lane
-            int wb = 0, wh = 0, wt0 = 0, wn = 0, wslot = 0, wlen = 0;
+            int wb = 0, wh = 0, wt0 = 0, wn = 0, wslot = 0, wlen = 0, wnp = 1, wpbeg = 0;
             float wqs[kMaxGroup];
 #pragma unroll
             for (int g = 0; g < kMaxGroup; ++g) wqs[g] = 0.f;
@@ -271,6 +398,10 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
                     wn = x.t1 - x.t0;
                     wslot = x.slot;
                     wlen = p.seq_lens[wb];
+                    if (FUSE) {
+                        wnp = p.unit_num_partials[x.u];
+                        wpbeg = p.unit_partial_begin[x.u];
+                    }
                     if (wlen < 0 || wlen > p.max_pages * kTile) atomicOr(p.status, DSA_DEV_BAD_SEQLEN);
                     if (KV == 1) {
                         const float *qs = p.q_scale + static_cast<int64_t>(wb) * p.hq + wh * G;
@@ -348,6 +479,8 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
                         const int h = __shfl_sync(0xffffffffu, wh, j);
                         const int n = __shfl_sync(0xffffffffu, wn, j);
                         const int slot = __shfl_sync(0xffffffffu, wslot, j);
+                        const int np = __shfl_sync(0xffffffffu, wnp, j);
+                        const int pbeg = __shfl_sync(0xffffffffu, wpbeg, j);
                         if (lane == 0) {
                             const int qs_ = qi % kQSlots;
                             if (!wait_phase(qempty_bar(qs_), ((qi / kQSlots) & 1) ^ 1, abort_flag, p.status)) {
@@ -360,6 +493,8 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
                                 inf->n = n;
                                 inf->slot = slot;
                                 inf->c_start = c;
+                                inf->np = np;
+                                inf->pbeg = pbeg;
 #pragma unroll
                                 for (int g = 0; g < kMaxGroup; ++g) inf->qscale[g] = qs[g];
                                 const uint32_t bytes = G * C::kQHeadBytes;
@@ -420,6 +555,7 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
                 cpg = npg;
             }
         }
+        if (FUSE && lane == 0) *epi_total = qi;  // descriptors handed off (the epilogue's count)
         if (!aborted && lane == 0) {
             // end marker for the consumers
             if (wait_phase(qempty_bar(qi % kQSlots), ((qi / kQSlots) & 1) ^ 1, abort_flag, p.status)) {
@@ -439,6 +575,51 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
         return;
     }
 
+    if (FUSE && warp == NCW + 1) {
+        // =========================== epilogue warp (fused combine) ===========================
+        // Follows the consumers' merges in order.  For a unit with several partials it
+        // publishes the merged partial at gpu scope (the consumers' writes, ordered by the
+        // epi_ready barrier, are covered by this warp's release) and counts it; the warp that
+        // completes the unit's count merges all its partials.  epi_free bounds its lag to
+        // kEpiRing descriptors.
+        for (int d = 0;; ++d) {
+            const int er = d % kEpiRing;
+            bool have = false;
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t it = 0;; ++it) {
+                if (mbar_try_wait(epi_ready(er), (d / kEpiRing) & 1)) {
+                    have = true;
+                    break;
+                }
+                const int tot = *epi_total;
+                if ((tot >= 0 && d >= tot) || *abort_flag) break;
+                if ((it & 31u) == 31u && globaltimer_ns() - t0 > kWaitLimitNs) {
+                    if (lane == 0) atomicOr(p.status, DSA_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+            }
+            if (!have) return;
+            const EpiRecord r = epi_rec[er];
+            if (r.np > 1) {
+                const int u = r.b * p.hkv + r.h;
+                int prev = 0;
+                if (lane == 0) {
+                    fence_acq_rel_gpu();
+                    prev = atomicAdd(p.unit_counters + u, 1);
+                }
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                if (prev == r.np - 1) {  // every partial of the unit is published
+                    fence_acq_rel_gpu();
+                    combine_unit(p, lane, r.b, r.h, r.np, r.pbeg);
+                    if (lane == 0) p.unit_counters[u] = 0;  // ready for the next step
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(epi_free(er));
+        }
+    }
+
     // =========================== consumer warps ===========================
     const int grp = warp / 4, wig = warp & 3;
     const int gid = lane >> 2, tig = lane & 3;
@@ -452,7 +633,7 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
 
     // Merge of descriptor d (states deposited in merge slot d & 1 by all consumer warps):
     // the warps' (m, l, O) combined under one softmax, written as a normalised partial.
-    auto merge_and_write = [&](int d, int pslot) -> bool {
+    auto merge_and_write = [&](int d, int pslot, int ub, int uh, int unp, int upbeg) -> bool {
         const int ms = d & 1;
         if (!wait_phase(merge_full(ms), (d >> 1) & 1, abort_flag, p.status)) return false;
         const float *M0 = reinterpret_cast<const float *>(smem + L::kMergeOff) + ms * L::kMergeSlot;
@@ -483,18 +664,27 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
                 acc.w *= inv;
                 lse = (M + lg2(Lsum)) * kLn2;
             }
+            if (FUSE && unp == 1) {  // the descriptor is the whole unit: final output
+                const int64_t orow = static_cast<int64_t>(ub) * p.hq + uh * G + hd;
+                store_out4<float>(p.out, orow, idx & 31, acc, p.out_bf16);
+                if ((idx & 31) == 0 && p.out_lse) p.out_lse[orow] = lse;
+                continue;
+            }
             const int64_t row = static_cast<int64_t>(pslot) * G + hd;
             *reinterpret_cast<float4 *>(p.partial_o + row * kHeadDim + d4) = acc;
             if ((idx & 31) == 0) p.partial_lse[row] = lse;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(merge_done(ms));
+        if (lane == 0) {
+            mbar_arrive(merge_done(ms));
+            if (FUSE) mbar_arrive(epi_ready(d % kEpiRing));
+        }
         return true;
     };
 
     // The merge of a descriptor runs after the NEXT descriptor's tiles, when every warp
     // deposited its state long ago: no warp waits for the slowest at each boundary.
-    int pend_d = -1, pend_slot = 0;
+    int pend_d = -1, pend_slot = 0, pend_b = 0, pend_h = 0, pend_np = 1, pend_pbeg = 0;
     for (int qi = 0;; ++qi) {
         // ---- next descriptor from the producer (info + Q in shared memory)
         const int qslot = qi % kQSlots;
@@ -502,6 +692,7 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
         const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
         if (inf->end) break;
         const int n = inf->n, slot = inf->slot, c_start = inf->c_start;
+        const int d_b = inf->b, d_h = inf->h, d_np = inf->np, d_pbeg = inf->pbeg;
         float qsc0 = p.score_scale, qsc1 = p.score_scale;
         if (KV == 1) {
             qsc0 *= inf->qscale[2 * tig];
@@ -680,6 +871,11 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
         }
         const int ms = qi & 1;
         if (!wait_phase(merge_done(ms), ((qi >> 1) & 1) ^ 1, abort_flag, p.status)) return;
+        if (FUSE) {
+            const int er = qi % kEpiRing;
+            if (!wait_phase(epi_free(er), ((qi / kEpiRing) & 1) ^ 1, abort_flag, p.status)) return;
+            if (warp == 0 && lane == 0) epi_rec[er] = EpiRecord{d_b, d_h, d_np, d_pbeg};
+        }
         float *W = reinterpret_cast<float *>(smem + L::kMergeOff) + ms * L::kMergeSlot + warp * L::kWarpFloats;
         if (gid == 0) {
             W[kMaxGroup * L::kOStride + 2 * tig] = m0;
@@ -698,11 +894,15 @@ __global__ void __launch_bounds__(Layout<KV, STAGES, GROUPS>::kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(merge_full(ms));
-        if (pend_d >= 0 && !merge_and_write(pend_d, pend_slot)) return;
+        if (pend_d >= 0 && !merge_and_write(pend_d, pend_slot, pend_b, pend_h, pend_np, pend_pbeg)) return;
         pend_d = qi;
         pend_slot = slot;
+        pend_b = d_b;
+        pend_h = d_h;
+        pend_np = d_np;
+        pend_pbeg = d_pbeg;
     }
-    if (pend_d >= 0) merge_and_write(pend_d, pend_slot);
+    if (pend_d >= 0) merge_and_write(pend_d, pend_slot, pend_b, pend_h, pend_np, pend_pbeg);
 }
 
 // ------------------------------------------------------------------ host side
@@ -739,18 +939,17 @@ bool make_pool_map(CUtensorMap *m, const void *pool, int kv, int num_pages, int 
     return r == CUDA_SUCCESS;
 }
 
-template <int KV, int STAGES, int GROUPS, bool PERSIST>
+template <int KV, int STAGES, int GROUPS, bool PERSIST, bool FUSE = false>
 dsa_status launch(const AttnArgs &a, const KernelParams &kp, dim3 grid, cudaStream_t st) {
     using L = Layout<KV, STAGES, GROUPS>;
     CUtensorMap km, vm;
     if (!make_pool_map(&km, a.k_pages, KV, a.num_pages, a.num_kv_heads) ||
         !make_pool_map(&vm, a.v_pages, KV, a.num_pages, a.num_kv_heads))
         return DSA_ERR_CUDA;
-    auto kern = attn_kernel<KV, STAGES, GROUPS, PERSIST>;
+    auto kern = attn_kernel<KV, STAGES, GROUPS, PERSIST, FUSE>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
         return DSA_ERR_CUDA;
-    kern<<<grid, L::kThreads, L::kAlloc, st>>>(km, vm, kp);
-    return launch_status();
+    return launch_pdl(kern, grid, dim3(FUSE ? L::kThreadsFused : L::kThreads), L::kAlloc, st, km, vm, kp);
 }
 
 KernelParams base_params(const AttnArgs &a, float *partial_o, float *partial_lse, int32_t *status) {
@@ -809,6 +1008,42 @@ extern "C" dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *
     if (kv_dtype == DSA_BF16)
         return launch<0, kPersistStagesBf16, kPersistGroups, true>(a, kp, grid, to_cuda(stream));
     return launch<1, kPersistStagesFp8, kPersistGroups, true>(a, kp, grid, to_cuda(stream));
+}
+
+extern "C" dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_scale, const void *k_pages,
+                                       const void *v_pages, dsa_dtype kv_dtype, const float *k_scale,
+                                       const float *v_scale, const int32_t *block_table,
+                                       int32_t max_pages_per_req, int32_t num_pages, const int32_t *seq_lens,
+                                       int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                       int32_t page_size, float sm_scale, const dsa_task_map *map, float *partial_o,
+                                       float *partial_lse, int32_t *unit_counters, void *out, dsa_dtype out_dtype,
+                                       float *out_lse, dsa_stream stream) {
+    const AttnArgs a{q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale, block_table,
+                     max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                     page_size, sm_scale};
+    dsa_status s = validate_attn(a);
+    if (s != DSA_OK) return s;
+    if (out_dtype != DSA_BF16 && out_dtype != DSA_FP32) return DSA_ERR_UNSUPPORTED;
+    if (!map || !map->cta_desc_begin || !map->descs || !map->meta || !partial_o || !partial_lse) return DSA_ERR_INVALID_ARG;
+    if (map->num_units != batch * num_kv_heads || map->num_ctas < 1) return DSA_ERR_INVALID_ARG;
+    if (batch > 0 && (!map->unit_partial_begin || !map->unit_num_partials || !unit_counters || !out))
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(partial_o) || !aligned16(map->descs) || !aligned16(out)) return DSA_ERR_INVALID_ARG;
+    if (batch == 0) return DSA_OK;
+    KernelParams kp = base_params(a, partial_o, partial_lse, map->meta + 3);
+    kp.max_slots = map->max_descs;
+    kp.cta_desc_begin = map->cta_desc_begin;
+    kp.descs = reinterpret_cast<const int4 *>(map->descs);
+    kp.unit_partial_begin = map->unit_partial_begin;
+    kp.unit_num_partials = map->unit_num_partials;
+    kp.unit_counters = unit_counters;
+    kp.out = out;
+    kp.out_bf16 = out_dtype == DSA_BF16;
+    kp.out_lse = out_lse;
+    const dim3 grid(map->num_ctas);
+    if (kv_dtype == DSA_BF16)
+        return launch<0, kPersistStagesBf16, kPersistGroups, true, true>(a, kp, grid, to_cuda(stream));
+    return launch<1, kPersistStagesFp8, kPersistGroups, true, true>(a, kp, grid, to_cuda(stream));
 }
 
 extern "C" int32_t dsa_static_num_splits(int32_t mode, int32_t param, int32_t max_seq_len) {

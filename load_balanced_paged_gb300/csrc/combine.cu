@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 
 #include "common.h"
+#include "ptx.cuh"
 
 namespace dsa {
 namespace {
@@ -40,6 +41,8 @@ __global__ void __launch_bounds__(kMaxGroup * 32)
                    int32_t hkv, int32_t G, OutT *__restrict__ out, float *__restrict__ out_lse) {
     const int u = blockIdx.x;
     const int head = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    grid_launch_dependents();
+    grid_dependency_wait();  // partials from the decode kernel
     if (head >= G) return;
     const int b = u / hkv, h = u - b * hkv;
     const int64_t beg = STATIC ? static_cast<int64_t>(u) * S : unit_begin[u];
@@ -93,12 +96,10 @@ dsa_status launch_combine(const int32_t *ub, const int32_t *uc, int32_t S, const
     if (units == 0) return DSA_OK;
     const int G = hq / hkv;
     if (out_dtype == DSA_BF16)
-        combine_kernel<STATIC, __nv_bfloat16><<<units, kMaxGroup * 32, 0, st>>>(
-            ub, uc, S, po, plse, hq, hkv, G, static_cast<__nv_bfloat16 *>(out), out_lse);
-    else
-        combine_kernel<STATIC, float><<<units, kMaxGroup * 32, 0, st>>>(ub, uc, S, po, plse, hq, hkv, G,
-                                                                         static_cast<float *>(out), out_lse);
-    return launch_status();
+        return launch_pdl(combine_kernel<STATIC, __nv_bfloat16>, dim3(units), dim3(kMaxGroup * 32), 0, st, ub, uc, S,
+                          po, plse, hq, hkv, G, static_cast<__nv_bfloat16 *>(out), out_lse);
+    return launch_pdl(combine_kernel<STATIC, float>, dim3(units), dim3(kMaxGroup * 32), 0, st, ub, uc, S, po, plse,
+                      hq, hkv, G, static_cast<float *>(out), out_lse);
 }
 
 }  // namespace

@@ -14,6 +14,7 @@
 //   4. per descriptor (grid-stride), its unit by binary search over first slots,
 //      its bin, and its tile range clipped to the unit.
 #include "common.h"
+#include "ptx.cuh"
 
 namespace dsa {
 namespace {
@@ -79,6 +80,8 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int32_t batch, int32_t num_kv_
     const int tid = threadIdx.x, nt = blockDim.x;
 
     if (tid == 0) s_status = 0;
+    grid_launch_dependents();
+    grid_dependency_wait();  // lengths (and the map's previous readers) from earlier kernels
     __syncthreads();
 
     // 1. tiles per unit (u = b * Hkv + h)
@@ -195,16 +198,13 @@ extern "C" dsa_status dsa_plan(const int32_t *seq_lens, int32_t batch, int32_t n
 
     const size_t smem = sizeof(int32_t) * (2 * static_cast<size_t>(U + 1) + num_persistent_ctas + 1);
     // small maps: fewer warps make the block-wide scans and barriers cheaper
-    if (U <= 2048 && num_persistent_ctas <= 2048) {
-        plan_kernel<256><<<1, 256, smem, to_cuda(stream)>>>(seq_lens, batch, num_kv_heads, num_persistent_ctas,
-                                                           min_tiles_per_split, *map);
-        return launch_status();
-    }
+    if (U <= 2048 && num_persistent_ctas <= 2048)
+        return launch_pdl(plan_kernel<256>, dim3(1), dim3(256), smem, to_cuda(stream), seq_lens, batch,
+                          num_kv_heads, num_persistent_ctas, min_tiles_per_split, *map);
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(plan_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return DSA_ERR_CUDA;
-    plan_kernel<1024><<<1, 1024, smem, to_cuda(stream)>>>(seq_lens, batch, num_kv_heads, num_persistent_ctas,
-                                                         min_tiles_per_split, *map);
-    return launch_status();
+    return launch_pdl(plan_kernel<1024>, dim3(1), dim3(1024), smem, to_cuda(stream), seq_lens, batch,
+                      num_kv_heads, num_persistent_ctas, min_tiles_per_split, *map);
 }

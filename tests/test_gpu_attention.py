@@ -227,3 +227,55 @@ def test_host_validation(dsa):
         dsa.decode(inp["q"].view(torch.uint8)[..., :128].contiguous(), inp["k_pages"].view(torch.uint8)[..., :128].contiguous(),
                    inp["v_pages"].view(torch.uint8)[..., :128].contiguous(), inp["block_table"], inp["seq_lens"], tm, 0.1)
     assert e.value.code == dsa.ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- fused decode + combine
+
+@pytest.mark.parametrize("lens,hq,hkv,kv", SMALL[:6])
+@pytest.mark.parametrize("C,m", [(3, 1), (None, 4), (300, 1)])
+def test_fused_vs_oracle(dsa, lens, hq, hkv, kv, C, m):
+    inp = make(lens, hq, hkv, kv, seed=len(lens) + 100)
+    C = C or sm_count()
+    out, lse, tm = dsa.attention_fused(inp, C, m)
+    out32, _, _ = dsa.attention_fused(inp, C, m, out_dtype=torch.float32, task_map=tm)
+    torch.cuda.synchronize()
+    assert dsa.get_status(tm) == 0
+    assert (tm.unit_counters() == 0).all()  # every unit's counter returned to zero
+    prob = parity.problem_from_host(workloads.host_view(inp), inp)
+    ref, ref_lse = prob.attention()
+    parity.check_outputs(out.float().cpu().numpy(), out32.cpu().numpy(), ref, kv, "fused")
+    parity.assert_lse_close(lse.cpu().numpy(), ref_lse, "fused lse")
+
+
+def test_fused_matches_separate_combine(dsa):
+    """The fused epilogue and the separate combine kernel merge the same partials."""
+    inp = make([100, 5000, 64, 2000, 129], 64, 8, "bf16", seed=21)
+    sep, sep_lse, _, _, _ = run_dynamic(dsa, inp, 40, 1, out_dtype=torch.float32)
+    fused, fused_lse, _ = dsa.attention_fused(inp, 40, 1, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert (fused - sep).abs().max().item() <= 1e-5
+    fin = torch.isfinite(sep_lse)
+    assert torch.equal(fin, torch.isfinite(fused_lse))
+    assert (fused_lse[fin] - sep_lse[fin]).abs().max().item() <= 1e-5
+
+
+@pytest.mark.parametrize("name", ["mixed", "tail", "fp8"])
+def test_fused_full_size_sampled(dsa, name):
+    w = workloads.WORKLOADS[name]
+    inp = workloads.make_workload(name, device="cuda")
+    C = w.ctas or sm_count()
+    tm = dsa.plan(inp["seq_lens"], w.num_kv_heads, C, 4)
+    kw = dict(q_scale=inp["q_scale"], k_scale=inp["k_scale"], v_scale=inp["v_scale"])
+    outs = []
+    for dt in (torch.bfloat16, torch.float32, torch.float32):  # the last two: a repeated step
+        outs.append(dsa.decode_fused(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"],
+                                     inp["seq_lens"], tm, inp["sm_scale"], out_dtype=dt, **kw))
+    torch.cuda.synchronize()
+    assert dsa.get_status(tm) == 0
+    assert torch.equal(outs[1], outs[2])
+    lens = inp["seq_lens"].cpu().numpy()
+    order = np.argsort(lens, kind="stable")
+    picks = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])})
+    ref, _ = parity.sub_problem(inp, picks).attention()
+    parity.check_outputs(outs[0][picks].float().cpu().numpy(), outs[1][picks].cpu().numpy(), ref, w.kv_dtype,
+                         f"{name} fused sampled")
