@@ -157,7 +157,7 @@ def bench_ours(args, device, rank, world):
     w = workloads.WORKLOADS[name]
     inp = workloads.make_workload(name, device=device, seed=w.seed + rank, max_requests=args.requests)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
-    C = w.ctas or sms
+    C = w.num_ctas(sms)
     m = args.min_tiles
     B, hq, hkv = int(inp["seq_lens"].shape[0]), w.num_q_heads, w.num_kv_heads
     G = hq // hkv

@@ -185,6 +185,14 @@ __device__ __noinline__ void drain_phase(uint32_t bar, uint32_t parity, uint64_t
     }
 }
 
+// E4M3 bytes {V[t][2g], V[t][2g+1], V[t+1][2g], V[t+1][2g+1]} -> f16x2 pairs over tokens
+// (t, t+1) for dims 2g (lo) and 2g+1 (hi).
+__device__ __forceinline__ void cvt_pair(uint32_t x, uint32_t &lo, uint32_t &hi) {
+    const uint32_t y = prmt(x, 0, 0x3120);
+    lo = e4m3x2_to_f16x2(static_cast<uint16_t>(y & 0xFFFF));
+    hi = e4m3x2_to_f16x2(static_cast<uint16_t>(y >> 16));
+}
+
 __device__ __forceinline__ uint32_t tok_mask(int t, int nv) {
     return (t < nv ? 0x0000FFFFu : 0u) | (t + 1 < nv ? 0xFFFF0000u : 0u);
 }
@@ -715,7 +723,8 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS>::kThreadsFus
         if (lane == 0) mbar_arrive(qempty_bar(qslot));
 
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        float vsc = 1.f;  // E4M3: O holds the true output divided by vsc
+        // E4M3: O holds the true output divided by vsc (set by the first scaled tile); bf16: 1
+        float vsc = (KV == 1) ? 0.f : 1.f;
         float o[8][4];
 #pragma unroll
         for (int mb = 0; mb < 8; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
@@ -733,7 +742,8 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS>::kThreadsFus
                 const uint32_t kbase = sbase + stage * L::kStageBytes;
                 const uint32_t vbase = kbase + C::kTileBytes;
                 // ---- S^T = K . Q^T  (rows: tokens tok_base + gid / + 8; cols: heads 2tig, 2tig+1)
-                float s[4] = {0.f, 0.f, 0.f, 0.f};
+                // two independent accumulation chains (even / odd k-steps) halve the MMA latency
+                float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < KSTEPS; ++ks) {
                     const int ch = 2 * ks + k_chunk;
@@ -744,9 +754,12 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS>::kThreadsFus
                         addr = kbase + k_row * 128 + ((ch ^ xr) << 4);
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4(addr, a0, a1, a2, a3);
-                    if (KV == 0) mma_bf16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-                    else mma_e4m3(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+                    float(&acc)[4] = (ks & 1) ? s2 : s;
+                    if (KV == 0) mma_bf16(acc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+                    else mma_e4m3(acc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
                 }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) s[i] += s2[i];
                 const int ta = tok_base + gid, tb = ta + 8;
                 float ksa = 1.f, ksb = 1.f, vsa = 0.f, vsb = 0.f;
                 if (KV == 1) {
@@ -792,18 +805,20 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS>::kThreadsFus
                     b0l = movmatrix_trans(l01);
                     b1l = movmatrix_trans(l23);
                 } else {
-                    // fold the per-token V scale into P, relative to this warp's largest scale
+                    // fold the per-token V scale into P, relative to this warp's largest scale in
+                    // the tile (O holds the output divided by vsc)
                     float vm = fmaxf(vsa, vsb);
 #pragma unroll
                     for (int o_ = 4; o_ < 32; o_ <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o_));
-                    float inv = 0.f;
                     if (vm > 0.f) {
-                        const float f = vsc / vm;
-                        al0 *= f;
-                        al1 *= f;
+                        if (vsc > 0.f) {
+                            const float f = vsc / vm;
+                            al0 *= f;
+                            al1 *= f;
+                        }
                         vsc = vm;
-                        inv = 1.f / vm;
                     }
+                    const float inv = vsc > 0.f ? 1.f / vsc : 0.f;
                     const float wa = vsa * inv, wb = vsb * inv;
                     b0h = movmatrix_trans(pack_f16x2(p0 * wa, p1 * wa));
                     b1h = movmatrix_trans(pack_f16x2(p2 * wb, p3 * wb));
@@ -827,10 +842,12 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS>::kThreadsFus
                             vbase + (ch >> 3) * (C::kTileBytes / 2) + v_row * 128 + (((ch & 7) ^ xr) << 4);
                         uint32_t a0, a1, a2, a3;
                         ldsm_x4_trans(addr, a0, a1, a2, a3);
-                        a0 &= mlo;
-                        a1 &= mlo;
-                        a2 &= mhi;
-                        a3 &= mhi;
+                        if (partial) {
+                            a0 &= mlo;
+                            a1 &= mlo;
+                            a2 &= mhi;
+                            a3 &= mhi;
+                        }
                         mma_bf16(o[mb], a0, a1, a2, a3, b0h, b1h);
                         mma_bf16(o[mb], a0, a1, a2, a3, b0l, b1l);
                     }
@@ -843,17 +860,24 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS>::kThreadsFus
                         ldsm_x4_trans(addr, x0, x1, x2, x3);
                         // x0/x1: tokens 0-7 / 8-15 of chunk 2mp; x2/x3: of chunk 2mp+1.
                         // Each holds, for dims (2gid, 2gid+1) of the chunk, tokens (2tig, 2tig+1).
-                        const uint32_t y0 = prmt(x0, 0, 0x3120), y1 = prmt(x1, 0, 0x3120);
-                        const uint32_t y2 = prmt(x2, 0, 0x3120), y3 = prmt(x3, 0, 0x3120);
-                        uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(y0 & 0xFFFF)) & mlo;
-                        uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(y0 >> 16)) & mlo;
-                        uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(y1 & 0xFFFF)) & mhi;
-                        uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(y1 >> 16)) & mhi;
+                        uint32_t a0, a1, a2, a3;
+                        cvt_pair(x0, a0, a1);
+                        cvt_pair(x1, a2, a3);
+                        if (partial) {
+                            a0 &= mlo;
+                            a1 &= mlo;
+                            a2 &= mhi;
+                            a3 &= mhi;
+                        }
                         mma_f16(o[2 * mp], a0, a1, a2, a3, b0h, b1h);
-                        a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(y2 & 0xFFFF)) & mlo;
-                        a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(y2 >> 16)) & mlo;
-                        a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(y3 & 0xFFFF)) & mhi;
-                        a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(y3 >> 16)) & mhi;
+                        cvt_pair(x2, a0, a1);
+                        cvt_pair(x3, a2, a3);
+                        if (partial) {
+                            a0 &= mlo;
+                            a1 &= mlo;
+                            a2 &= mhi;
+                            a3 &= mhi;
+                        }
                         mma_f16(o[2 * mp + 1], a0, a1, a2, a3, b0h, b1h);
                     }
                 }
@@ -973,10 +997,29 @@ KernelParams base_params(const AttnArgs &a, float *partial_o, float *partial_lse
     return kp;
 }
 
-// Ring depths: the persistent kernel keeps one CTA per SM with deep rings; the static
-// grid keeps two CTAs per SM with shallow rings (many short-lived CTAs).
+// CTA shapes.  One persistent CTA per SM: two consumer groups and a deep ring.  Two CTAs per
+// SM (used by the static grid, and by the persistent kernel when the task map has at least
+// two bins per SM): one consumer group and a shallow ring each, so both fit in shared memory.
 constexpr int kPersistStagesBf16 = 4, kPersistStagesFp8 = 8, kPersistGroups = 2;
-constexpr int kStaticStagesBf16 = 2, kStaticStagesFp8 = 4, kStaticGroups = 1;
+constexpr int kPairStagesBf16 = 2, kPairStagesFp8 = 4, kPairGroups = 1;
+
+int sm_count() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!cached[dev]) cudaDeviceGetAttribute(&cached[dev], cudaDevAttrMultiProcessorCount, dev);
+    return cached[dev];
+}
+
+// Persistent launch: the CTA shape that keeps all of the map's bins resident at once.
+template <int KV, bool FUSE>
+dsa_status launch_persistent(const AttnArgs &a, const KernelParams &kp, int num_ctas, cudaStream_t st) {
+    const int sms = sm_count();
+    const dim3 grid(num_ctas);
+    if (sms > 0 && num_ctas >= 2 * sms)
+        return launch<KV, KV == 0 ? kPairStagesBf16 : kPairStagesFp8, kPairGroups, true, FUSE>(a, kp, grid, st);
+    return launch<KV, KV == 0 ? kPersistStagesBf16 : kPersistStagesFp8, kPersistGroups, true, FUSE>(a, kp, grid, st);
+}
 
 }  // namespace
 }  // namespace dsa
@@ -1004,10 +1047,8 @@ extern "C" dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *
     kp.max_slots = map->max_descs;
     kp.cta_desc_begin = map->cta_desc_begin;
     kp.descs = reinterpret_cast<const int4 *>(map->descs);
-    const dim3 grid(map->num_ctas);
-    if (kv_dtype == DSA_BF16)
-        return launch<0, kPersistStagesBf16, kPersistGroups, true>(a, kp, grid, to_cuda(stream));
-    return launch<1, kPersistStagesFp8, kPersistGroups, true>(a, kp, grid, to_cuda(stream));
+    if (kv_dtype == DSA_BF16) return launch_persistent<0, false>(a, kp, map->num_ctas, to_cuda(stream));
+    return launch_persistent<1, false>(a, kp, map->num_ctas, to_cuda(stream));
 }
 
 extern "C" dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_scale, const void *k_pages,
@@ -1040,10 +1081,8 @@ extern "C" dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const f
     kp.out = out;
     kp.out_bf16 = out_dtype == DSA_BF16;
     kp.out_lse = out_lse;
-    const dim3 grid(map->num_ctas);
-    if (kv_dtype == DSA_BF16)
-        return launch<0, kPersistStagesBf16, kPersistGroups, true, true>(a, kp, grid, to_cuda(stream));
-    return launch<1, kPersistStagesFp8, kPersistGroups, true, true>(a, kp, grid, to_cuda(stream));
+    if (kv_dtype == DSA_BF16) return launch_persistent<0, true>(a, kp, map->num_ctas, to_cuda(stream));
+    return launch_persistent<1, true>(a, kp, map->num_ctas, to_cuda(stream));
 }
 
 extern "C" int32_t dsa_static_num_splits(int32_t mode, int32_t param, int32_t max_seq_len) {
@@ -1077,6 +1116,6 @@ extern "C" dsa_status dsa_static_splitkv(int32_t mode, int32_t param, int32_t ma
     kp.num_splits = S;
     kp.max_slots = batch * num_kv_heads * S;
     const dim3 grid(S, num_kv_heads, batch);
-    if (kv_dtype == DSA_BF16) return launch<0, kStaticStagesBf16, kStaticGroups, false>(a, kp, grid, to_cuda(stream));
-    return launch<1, kStaticStagesFp8, kStaticGroups, false>(a, kp, grid, to_cuda(stream));
+    if (kv_dtype == DSA_BF16) return launch<0, kPairStagesBf16, kPairGroups, false>(a, kp, grid, to_cuda(stream));
+    return launch<1, kPairStagesFp8, kPairGroups, false>(a, kp, grid, to_cuda(stream));
 }

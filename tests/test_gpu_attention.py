@@ -47,11 +47,20 @@ SMALL = [
 ]
 
 
+def resolve_ctas(C):
+    """None: one bin per SM; "2x": two bins per SM (the two-CTAs-per-SM kernel shape)."""
+    if C is None:
+        return sm_count()
+    if C == "2x":
+        return 2 * sm_count()
+    return C
+
+
 @pytest.mark.parametrize("lens,hq,hkv,kv", SMALL)
-@pytest.mark.parametrize("C,m", [(3, 1), (None, 4), (300, 1)])
+@pytest.mark.parametrize("C,m", [(3, 1), (None, 4), (300, 1), ("2x", 4)])
 def test_small_vs_oracle(dsa, lens, hq, hkv, kv, C, m):
     inp = make(lens, hq, hkv, kv, seed=len(lens))
-    C = C or sm_count()
+    C = resolve_ctas(C)
     out, lse, tm, po, pl = run_dynamic(dsa, inp, C, m)
     assert dsa.get_status(tm) == 0
     h = workloads.host_view(inp)
@@ -130,7 +139,7 @@ def test_full_size_workloads_sampled(dsa, name):
     the task map is checked whole."""
     w = workloads.WORKLOADS[name]
     inp = workloads.make_workload(name, device="cuda")
-    C = w.ctas or sm_count()
+    C = w.num_ctas(sm_count())
     out, lse, tm, po, pl = run_dynamic(dsa, inp, C, 4)
     out32 = dsa.combine(tm, po, pl, w.num_q_heads, out_dtype=torch.float32)
     assert dsa.get_status(tm) == 0
@@ -232,10 +241,10 @@ def test_host_validation(dsa):
 # ---------------------------------------------------------------- fused decode + combine
 
 @pytest.mark.parametrize("lens,hq,hkv,kv", SMALL[:6])
-@pytest.mark.parametrize("C,m", [(3, 1), (None, 4), (300, 1)])
+@pytest.mark.parametrize("C,m", [(3, 1), (None, 4), (300, 1), ("2x", 4)])
 def test_fused_vs_oracle(dsa, lens, hq, hkv, kv, C, m):
     inp = make(lens, hq, hkv, kv, seed=len(lens) + 100)
-    C = C or sm_count()
+    C = resolve_ctas(C)
     out, lse, tm = dsa.attention_fused(inp, C, m)
     out32, _, _ = dsa.attention_fused(inp, C, m, out_dtype=torch.float32, task_map=tm)
     torch.cuda.synchronize()
@@ -263,7 +272,7 @@ def test_fused_matches_separate_combine(dsa):
 def test_fused_full_size_sampled(dsa, name):
     w = workloads.WORKLOADS[name]
     inp = workloads.make_workload(name, device="cuda")
-    C = w.ctas or sm_count()
+    C = w.num_ctas(sm_count())
     tm = dsa.plan(inp["seq_lens"], w.num_kv_heads, C, 4)
     kw = dict(q_scale=inp["q_scale"], k_scale=inp["k_scale"], v_scale=inp["v_scale"])
     outs = []

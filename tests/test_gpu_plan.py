@@ -34,7 +34,7 @@ def check_plan(dsa, lens, hkv, C, m):
 @pytest.mark.parametrize("m", [1, 4, 16])
 def test_workload_maps_bit_exact(dsa, name, m):
     w = workloads.WORKLOADS[name]
-    C = w.ctas or sm_count()
+    C = w.num_ctas(sm_count())
     got = check_plan(dsa, w.lengths(), w.num_kv_heads, C, m)
     assert got["meta"][3] == 0
 

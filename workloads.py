@@ -38,8 +38,12 @@ class Workload:
     num_q_heads: int
     num_kv_heads: int
     kv_dtype: str  # "bf16" or "fp8"
-    ctas: int | None  # persistent CTAs; None = the device's SM count
+    ctas: int | None  # persistent CTAs (bins); None = ctas_per_sm x the device's SM count
     seed: int = 0
+    ctas_per_sm: int = 1
+
+    def num_ctas(self, sm_count: int) -> int:
+        return self.ctas or self.ctas_per_sm * sm_count
 
     def lengths(self) -> np.ndarray:
         return draw_lengths(self.name, self.batch, np.random.default_rng(self.seed))
@@ -54,9 +58,9 @@ WORKLOADS = {
     "long": Workload("long", "batch 1, KV length 131072, 64 q / 8 KV heads, bf16",
                      1, 64, 8, "bf16", None),
     "tail": Workload("tail", "batch 128: 127 KV lengths uniform 512-2048 plus one 65536, 64 q / 8 KV heads, bf16",
-                     128, 64, 8, "bf16", None),
+                     128, 64, 8, "bf16", None, ctas_per_sm=2),
     "fp8": Workload("fp8", "batch 64, KV lengths lognormal (mean 68k, cap 192k, min 1k), 64 q / 8 KV heads, FP8-E4M3 Q/K/V",
-                    64, 64, 8, "fp8", None),
+                    64, 64, 8, "fp8", None, ctas_per_sm=2),
 }
 
 # lognormal location chosen so that the mean after clipping to [1024, 196608] is 69632 (68k)
