@@ -61,15 +61,21 @@ __global__ void __launch_bounds__(kMaxGroup * 32)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         L = M + logf(sum);
-#pragma unroll 4
-        for (int k = 0; k < n; ++k) {
-            const int64_t row = (beg + k) * G + head;
-            const float w = exp2f((partial_lse[row] - L) * kLog2e);
-            const float4 v = *reinterpret_cast<const float4 *>(partial_o + row * kHeadDim + lane * 4);
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
+        // 32 partials at a time: lane k holds the weight of partial k0 + k; the rows of the
+        // batch are loaded back to back
+        for (int k0 = 0; k0 < n; k0 += 32) {
+            const int kn = min(32, n - k0);
+            const float w = lane < kn ? exp2f((partial_lse[(beg + k0 + lane) * G + head] - L) * kLog2e) : 0.f;
+#pragma unroll 8
+            for (int j = 0; j < kn; ++j) {
+                const float4 v =
+                    *reinterpret_cast<const float4 *>(partial_o + ((beg + k0 + j) * G + head) * kHeadDim + lane * 4);
+                const float wj = __shfl_sync(0xffffffffu, w, j);
+                acc.x += wj * v.x;
+                acc.y += wj * v.y;
+                acc.z += wj * v.z;
+                acc.w += wj * v.w;
+            }
         }
     }
     const int64_t orow = static_cast<int64_t>(b) * hq + h * G + head;

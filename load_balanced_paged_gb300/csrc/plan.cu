@@ -5,14 +5,14 @@
 // One CTA (256 or 1024 threads).  Instead of walking tiles one by one, it uses the
 // closed form of the greedy fill: with a real-valued budget T / C_eff, bin i holds the
 // global tiles [floor(i*T/C_eff), floor((i+1)*T/C_eff)); these starts go to a shared
-// table, and the bin holding a tile is found by binary search in it.  Every unit and
+// table, and the bin holding a tile is found from an fp32 estimate corrected against it.
+// Every unit and
 // every descriptor is then placed independently:
 //   1. n_u = ceil(len_b / 64), exclusive scan -> P_u, total T;
 //   2. per unit, the number of bins it touches -> exclusive scan -> first slot;
 //   3. per bin, its first descriptor = first slot of the unit holding its first tile
 //      plus the number of that unit's bins before it;
-//   4. per descriptor (grid-stride), its unit by binary search over first slots,
-//      its bin, and its tile range clipped to the unit.
+//   4. per unit, its descriptors: one per bin it touches, tile ranges clipped to the unit.
 #include "common.h"
 #include "ptx.cuh"
 
@@ -105,13 +105,20 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int32_t batch, int32_t num_kv_
         sP[U] = static_cast<int32_t>(T);
         if (overflow) s_status |= DSA_DEV_BAD_SEQLEN;
     }
-    // bin i starts at global tile floor(i * T / C_eff): the cumulative budget, rounded down
-    for (int i = tid; C_eff > 0 && i <= C_eff; i += nt)
-        sBin[i] = static_cast<int32_t>(static_cast<uint64_t>(i) * static_cast<uint64_t>(T) /
-                                       static_cast<uint64_t>(C_eff));
+    // bin i starts at global tile floor(i * T / C_eff): the cumulative budget, rounded down.
+    // With T = q * C_eff + r this is i * q + floor(i * r / C_eff), all in 32 bits.
+    const int32_t Ti = static_cast<int32_t>(T), Ci = static_cast<int32_t>(C_eff);
+    const int32_t q_ = Ci > 0 ? Ti / Ci : 0, r_ = Ci > 0 ? Ti % Ci : 0;
+    for (int i = tid; Ci > 0 && i <= Ci; i += nt) sBin[i] = i * q_ + (i * r_) / Ci;
     __syncthreads();
-    // bin holding global tile x: the last bin starting at or before x
-    auto bin_of = [&](int64_t x) -> int64_t { return upper_bound(sBin, static_cast<int>(C_eff), x) - 1; };
+    // bin holding global tile x: an fp32 estimate of x * C_eff / T, corrected against the table
+    const float ratio = Ci > 0 ? static_cast<float>(Ci) / static_cast<float>(Ti) : 0.f;
+    auto bin_of = [&](int64_t x) -> int64_t {
+        int i = min(Ci - 1, max(0, static_cast<int>((static_cast<float>(x) + 0.5f) * ratio)));
+        while (i > 0 && sBin[i] > x) --i;
+        while (i + 1 < Ci && sBin[i + 1] <= x) ++i;
+        return i;
+    };
 
     // 2. bins touched by each unit
     for (int u = tid; u < U; u += nt) {
@@ -145,17 +152,19 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int32_t batch, int32_t num_kv_
         map.cta_desc_begin[i] = b;
     }
 
-    // 4. descriptors, grid-stride
-    for (int64_t d = tid; d < nd; d += nt) {
-        const int v = upper_bound(sBeg, U, d) - 1;
-        const int64_t k = d - sBeg[v];
-        const int64_t p = sP[v], n = sP[v + 1] - p;
-        const int64_t i = bin_of(p) + k;
-        const int64_t g0 = max(static_cast<int64_t>(sBin[i]), p);
-        const int64_t g1 = min(static_cast<int64_t>(sBin[i + 1]), p + n);
-        int4 desc = make_int4(v, static_cast<int32_t>(g0 - p), static_cast<int32_t>(g1 - p),
-                              static_cast<int32_t>(k));
-        reinterpret_cast<int4 *>(map.descs)[d] = desc;
+    // 4. descriptors: each unit walks the bins it touches, in order
+    for (int u = tid; u < U && !empty_map; u += nt) {
+        const int32_t first = sBeg[u], np = sBeg[u + 1] - first;
+        if (np == 0) continue;
+        const int64_t p = sP[u], n = sP[u + 1] - p;
+        const int64_t b0 = bin_of(p);
+        for (int k = 0; k < np; ++k) {
+            const int64_t i = b0 + k;
+            const int64_t g0 = max(static_cast<int64_t>(sBin[i]), p);
+            const int64_t g1 = min(static_cast<int64_t>(sBin[i + 1]), p + n);
+            reinterpret_cast<int4 *>(map.descs)[first + k] =
+                make_int4(u, static_cast<int32_t>(g0 - p), static_cast<int32_t>(g1 - p), k);
+        }
     }
 
     __syncthreads();

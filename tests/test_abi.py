@@ -21,7 +21,8 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(dsa_\w+)\s*\(", text, flags=re.M)))
 

@@ -79,7 +79,12 @@ def check_invariants(lens, hkv, C, m, tm):
     assert seen == nd
 
 
-@pytest.mark.parametrize("case", json.load(open(GOLDEN))["cases"], ids=lambda c: c["name"])
+def golden_cases():
+    with open(GOLDEN) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", golden_cases(), ids=lambda c: c["name"])
 def test_hand_worked_examples(case):
     tm = oracle.plan(case["seq_lens"], case["num_kv_heads"], case["num_ctas"], TILE,
                      case["min_tiles_per_split"])
