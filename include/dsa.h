@@ -284,6 +284,16 @@ dsa_status dsa_decode_step_noalloc(const void *q, dsa_dtype q_dtype, const float
                                    int32_t min_tiles_per_split, void *out, dsa_dtype out_dtype,
                                    float *out_lse, int32_t *status, dsa_stream stream);
 
+/*
+ * dsa_selftest_wait_timeout -- exercises the bounded wait every kernel of this
+ * library uses (no counterpart on the pages).  One CTA waits on an mbarrier that
+ * nothing ever arrives at; after limit_ns (0 < limit_ns <= 2 s) it sets
+ * DSA_DEV_TIMEOUT in *status and raises the CTA's abort flag, on which a second
+ * waiting warp must leave (it then also sets bit 16).  The kernel returns, and the
+ * context stays usable.  status: device int32, which the caller zeroes first.
+ */
+dsa_status dsa_selftest_wait_timeout(int32_t *status, int64_t limit_ns, dsa_stream stream);
+
 /* Static string naming a dsa_status value. */
 const char *dsa_status_string(dsa_status s);
 

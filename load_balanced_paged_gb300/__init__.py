@@ -69,6 +69,8 @@ _lib.dsa_get_status.argtypes = [_TMP, ctypes.POINTER(_i32)]
 _lib.dsa_get_status.restype = ctypes.c_int
 _lib.dsa_decode_step_noalloc.argtypes = _attn_args + [_i32, _i32, _vp, _i32, _vp, _vp, _vp]
 _lib.dsa_decode_step_noalloc.restype = ctypes.c_int
+_lib.dsa_selftest_wait_timeout.argtypes = [_vp, ctypes.c_int64, _vp]
+_lib.dsa_selftest_wait_timeout.restype = ctypes.c_int
 _lib.dsa_status_string.argtypes = [ctypes.c_int]
 _lib.dsa_status_string.restype = ctypes.c_char_p
 
@@ -270,6 +272,14 @@ def read_status(status: torch.Tensor) -> int:
     if rc not in (OK, ERR_DEVICE_INPUT):
         raise DSAError(rc, "dsa_read_status")
     return v.value
+
+
+def selftest_wait_timeout(limit_ns: int = 10_000_000, stream=None) -> int:
+    """Runs dsa_selftest_wait_timeout and returns the device status word it produced."""
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _check(_lib.dsa_selftest_wait_timeout(_ptr(status), int(limit_ns), _stream(stream)),
+           "dsa_selftest_wait_timeout")
+    return read_status(status)
 
 
 def status_string(code: int) -> str:

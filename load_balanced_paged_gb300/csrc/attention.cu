@@ -161,14 +161,14 @@ __device__ __forceinline__ Desc get_desc(const KernelParams &p, int d_begin, int
 // Bounded wait on an mbarrier phase; gives up (false) when the CTA aborted or the
 // time limit passed (then it records the timeout and raises the abort flag).
 __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                        int32_t *status) {
+                                        int32_t *status, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 atomicOr(status, DSA_DEV_TIMEOUT);
                 *abort_flag = 1;
                 return false;
@@ -929,6 +929,31 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS>::kThreadsFus
     if (pend_d >= 0) merge_and_write(pend_d, pend_slot, pend_b, pend_h, pend_np, pend_pbeg);
 }
 
+// Self-test of the bounded wait: warp 0 waits on an mbarrier that nothing ever arrives at;
+// when its limit passes it records DSA_DEV_TIMEOUT and raises the CTA's abort flag; warp 1
+// waits on a second such barrier and must leave on the abort flag.  *status also gets bit
+// 16 when warp 1 observed the abort.
+__global__ void __launch_bounds__(64, 1) wait_selftest_kernel(int32_t *status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars[0]), 1);
+        mbar_init(smem_u32(&bars[1]), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (lane != 0) return;
+    volatile int *ab = &abort_flag;
+    if (warp == 0) {
+        wait_phase(smem_u32(&bars[0]), 0, ab, status, limit_ns);
+    } else {
+        // a limit far beyond warp 0's: this wait can only end through the abort flag
+        if (!wait_phase(smem_u32(&bars[1]), 0, ab, status, 8 * limit_ns) && *ab) atomicOr(status, 1 << 16);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1083,6 +1108,12 @@ extern "C" dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const f
     kp.out_lse = out_lse;
     if (kv_dtype == DSA_BF16) return launch_persistent<0, true>(a, kp, map->num_ctas, to_cuda(stream));
     return launch_persistent<1, true>(a, kp, map->num_ctas, to_cuda(stream));
+}
+
+extern "C" dsa_status dsa_selftest_wait_timeout(int32_t *status, int64_t limit_ns, dsa_stream stream) {
+    if (!status || limit_ns <= 0 || limit_ns > static_cast<int64_t>(kWaitLimitNs)) return DSA_ERR_INVALID_ARG;
+    wait_selftest_kernel<<<1, 64, 0, to_cuda(stream)>>>(status, static_cast<uint64_t>(limit_ns));
+    return launch_status();
 }
 
 extern "C" int32_t dsa_static_num_splits(int32_t mode, int32_t param, int32_t max_seq_len) {

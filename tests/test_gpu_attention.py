@@ -288,3 +288,28 @@ def test_fused_full_size_sampled(dsa, name):
     ref, _ = parity.sub_problem(inp, picks).attention()
     parity.check_outputs(outs[0][picks].float().cpu().numpy(), outs[1][picks].cpu().numpy(), ref, w.kv_dtype,
                          f"{name} fused sampled")
+
+
+def test_bounded_wait_times_out_and_context_survives(dsa):
+    """A wait on a barrier nothing arrives at ends after its limit with DSA_DEV_TIMEOUT; the
+    other waiting warp leaves on the abort flag; the device keeps working afterwards."""
+    import time
+    t0 = time.time()
+    status = dsa.selftest_wait_timeout(limit_ns=20_000_000)  # 20 ms
+    assert time.time() - t0 < 10
+    assert status & dsa.DEV_TIMEOUT
+    assert status & (1 << 16)
+    inp = make([300, 200], 16, 2, "bf16")
+    _, _, tm, _, _ = run_dynamic(dsa, inp, 4, 1)
+    assert dsa.get_status(tm) == 0
+
+
+def test_batch_zero_is_a_no_op(dsa):
+    inp = make([], 16, 2, "bf16")
+    tm = dsa.plan(inp["seq_lens"], 2, 8)
+    po, pl = dsa.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
+                        inp["sm_scale"])
+    out = dsa.combine(tm, po, pl, 16)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 16, 128)
+    assert tm.host()["meta"].tolist() == [0, 0, 0, 0]

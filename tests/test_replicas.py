@@ -30,7 +30,7 @@ def _rank_main(rank, world, port, results):
 def test_max_over_ranks_and_aggregate():
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     results = mgr.dict()
     mp.spawn(_rank_main, args=(world, port, results), nprocs=world, join=True)
     assert results[0][0] == results[1][0] == 11.0
