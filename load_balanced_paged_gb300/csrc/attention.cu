@@ -88,7 +88,7 @@ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 constexpr int kQSlots = 2;   // descriptors handed ahead to the consumers (Q + info)
 constexpr int kEpiRing = 8;  // merged descriptors the epilogue warp may lag behind (fused combine)
 
-template <int KV, int STAGES, int GROUPS>
+template <int KV, int STAGES, int GROUPS, int MSLOTS = 2>
 struct Layout {
     static constexpr int kNcw = GROUPS * 4;  // consumer warps
     static constexpr int kThreads = (kNcw + 1) * 32;       // consumers + producer
@@ -100,8 +100,9 @@ struct Layout {
     static constexpr int kOStride = 132;  // floats per head row of a warp's O (padding avoids bank conflicts)
     static constexpr int kWarpFloats = kMaxGroup * kOStride + 2 * kMaxGroup;
     static constexpr int kMergeOff = kQOff + kQSlots * kQSlot;
-    static constexpr int kMergeSlot = kNcw * kWarpFloats;  // floats per merge slot (2 slots)
-    static constexpr int kBarOff = kMergeOff + 2 * kMergeSlot * 4;
+    static constexpr int kMergeSlot = kNcw * kWarpFloats;  // floats per merge slot
+    static constexpr int kMergeSlots = MSLOTS;             // 2: lagged merge; 1: merge at once
+    static constexpr int kBarOff = kMergeOff + MSLOTS * kMergeSlot * 4;
     // full, empty, qfull, qempty, merge_full x2, merge_done x2, epi_ready, epi_free
     static constexpr int kNumBars = 2 * STAGES + 2 * kQSlots + 4 + 2 * kEpiRing;
     static constexpr int kNValidOff = kBarOff + kNumBars * 8;
@@ -110,6 +111,11 @@ struct Layout {
     static constexpr int kEpiOff = kInfoOff + kQSlots * 64;  // kEpiRing EpiRecords + descriptor total
     static constexpr int kBytes = kEpiOff + kEpiRing * 16 + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
+    static_assert(MSLOTS == 1 || MSLOTS == 2, "merge slots");
+    // Each stage must be consumed by one group only: a group then meets the phases of its
+    // stages' full barriers in order.  With stages shared by two groups, one group could wait
+    // for phase k+1 while phase k is still pending, pass the parity test early and arrive on
+    // the stage's empty barrier out of turn (an undefined mbarrier use that faults the GPU).
     static_assert(STAGES % GROUPS == 0, "each stage must belong to one consumer group");
     static_assert(kStageBytes % 1024 == 0 && kQOff % 1024 == 0, "swizzled TMA boxes need 1024-byte alignment");
     static_assert(kAlloc <= 227 * 1024, "shared memory budget");
@@ -282,12 +288,12 @@ __device__ __noinline__ void combine_unit(const KernelParams &p, int lane, int u
 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
-template <int KV, int STAGES, int GROUPS, bool PERSIST, bool FUSE>
-__global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS>::kThreadsFused
-                                       : Layout<KV, STAGES, GROUPS>::kThreads, 1)
+template <int KV, int STAGES, int GROUPS, bool PERSIST, bool FUSE, int MSLOTS>
+__global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS>::kThreadsFused
+                                       : Layout<KV, STAGES, GROUPS, MSLOTS>::kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const KernelParams p) {
-    using L = Layout<KV, STAGES, GROUPS>;
+    using L = Layout<KV, STAGES, GROUPS, MSLOTS>;
     using C = Cfg<KV>;
     constexpr int NCW = L::kNcw;
     extern __shared__ uint8_t smem_raw[];
@@ -319,7 +325,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS>::kThreadsFus
             mbar_init(qfull_bar(s), 1);
             mbar_init(qempty_bar(s), NCW);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < MSLOTS; ++s) {
             mbar_init(merge_full(s), NCW);
             mbar_init(merge_done(s), NCW);
         }
@@ -642,8 +648,8 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS>::kThreadsFus
     // Merge of descriptor d (states deposited in merge slot d & 1 by all consumer warps):
     // the warps' (m, l, O) combined under one softmax, written as a normalised partial.
     auto merge_and_write = [&](int d, int pslot, int ub, int uh, int unp, int upbeg) -> bool {
-        const int ms = d & 1;
-        if (!wait_phase(merge_full(ms), (d >> 1) & 1, abort_flag, p.status)) return false;
+        const int ms = d % MSLOTS;
+        if (!wait_phase(merge_full(ms), (d / MSLOTS) & 1, abort_flag, p.status)) return false;
         const float *M0 = reinterpret_cast<const float *>(smem + L::kMergeOff) + ms * L::kMergeSlot;
         for (int idx = warp * 32 + lane; idx < G * 32; idx += NCW * 32) {
             const int hd = idx >> 5, d4 = (idx & 31) * 4;
@@ -893,8 +899,8 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS>::kThreadsFus
             l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
             l1 += __shfl_xor_sync(0xffffffffu, l1, o_);
         }
-        const int ms = qi & 1;
-        if (!wait_phase(merge_done(ms), ((qi >> 1) & 1) ^ 1, abort_flag, p.status)) return;
+        const int ms = qi % MSLOTS;
+        if (!wait_phase(merge_done(ms), ((qi / MSLOTS) & 1) ^ 1, abort_flag, p.status)) return;
         if (FUSE) {
             const int er = qi % kEpiRing;
             if (!wait_phase(epi_free(er), ((qi / kEpiRing) & 1) ^ 1, abort_flag, p.status)) return;
@@ -918,6 +924,10 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS>::kThreadsFus
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(merge_full(ms));
+        if (MSLOTS == 1) {  // one merge slot: merge this descriptor at once
+            if (!merge_and_write(qi, slot, d_b, d_h, d_np, d_pbeg)) return;
+            continue;
+        }
         if (pend_d >= 0 && !merge_and_write(pend_d, pend_slot, pend_b, pend_h, pend_np, pend_pbeg)) return;
         pend_d = qi;
         pend_slot = slot;
@@ -988,14 +998,14 @@ bool make_pool_map(CUtensorMap *m, const void *pool, int kv, int num_pages, int 
     return r == CUDA_SUCCESS;
 }
 
-template <int KV, int STAGES, int GROUPS, bool PERSIST, bool FUSE = false>
+template <int KV, int STAGES, int GROUPS, bool PERSIST, bool FUSE = false, int MSLOTS = 2>
 dsa_status launch(const AttnArgs &a, const KernelParams &kp, dim3 grid, cudaStream_t st) {
-    using L = Layout<KV, STAGES, GROUPS>;
+    using L = Layout<KV, STAGES, GROUPS, MSLOTS>;
     CUtensorMap km, vm;
     if (!make_pool_map(&km, a.k_pages, KV, a.num_pages, a.num_kv_heads) ||
         !make_pool_map(&vm, a.v_pages, KV, a.num_pages, a.num_kv_heads))
         return DSA_ERR_CUDA;
-    auto kern = attn_kernel<KV, STAGES, GROUPS, PERSIST, FUSE>;
+    auto kern = attn_kernel<KV, STAGES, GROUPS, PERSIST, FUSE, MSLOTS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
         return DSA_ERR_CUDA;
     return launch_pdl(kern, grid, dim3(FUSE ? L::kThreadsFused : L::kThreads), L::kAlloc, st, km, vm, kp);
@@ -1025,7 +1035,9 @@ KernelParams base_params(const AttnArgs &a, float *partial_o, float *partial_lse
 // CTA shapes.  One persistent CTA per SM: two consumer groups and a deep ring.  Two CTAs per
 // SM (used by the static grid, and by the persistent kernel when the task map has at least
 // two bins per SM): one consumer group and a shallow ring each, so both fit in shared memory.
-constexpr int kPersistStagesBf16 = 4, kPersistStagesFp8 = 8, kPersistGroups = 2;
+// (A sweep on the GB300 found the lagged two-slot merge with 4 / 8 stages faster than one
+// merge slot with the same or deeper rings.)
+constexpr int kPersistStagesBf16 = 4, kPersistStagesFp8 = 8, kPersistGroups = 2, kPersistMergeSlots = 2;
 constexpr int kPairStagesBf16 = 2, kPairStagesFp8 = 4, kPairGroups = 1;
 
 int sm_count() {
@@ -1043,7 +1055,8 @@ dsa_status launch_persistent(const AttnArgs &a, const KernelParams &kp, int num_
     const dim3 grid(num_ctas);
     if (sms > 0 && num_ctas >= 2 * sms)
         return launch<KV, KV == 0 ? kPairStagesBf16 : kPairStagesFp8, kPairGroups, true, FUSE>(a, kp, grid, st);
-    return launch<KV, KV == 0 ? kPersistStagesBf16 : kPersistStagesFp8, kPersistGroups, true, FUSE>(a, kp, grid, st);
+    return launch<KV, KV == 0 ? kPersistStagesBf16 : kPersistStagesFp8, kPersistGroups, true, FUSE, kPersistMergeSlots>(
+        a, kp, grid, st);
 }
 
 }  // namespace
