@@ -27,7 +27,8 @@ Readings where the pages are silent (each one is the plainest form of the step):
    to the whole head vector of Q and of K after RoPE.  It is orthogonal, so it leaves
    every q·k unchanged.
 5. Quantisation is per (token, head): scale = amax/448 (1 when amax = 0), stored value =
-   E4M3 round-to-nearest-even of y/scale.  A bf16 output is the bf16
+   E4M3 round-to-nearest-even of y/scale, evaluated as (y·448)/amax so that the only
+   rounding before the decision is that of the quotient.  A bf16 output is the bf16
    round-to-nearest-even of y.
 6. The cache slot of token n is ``slot_mapping[n]`` = page·page_size + offset; −1 means
    the token writes no K/V.  K/V scales live at [page, kv_head, offset].
@@ -157,10 +158,14 @@ def quantize_rows(y, dtype: str):
     if dtype == "bf16":
         val, code = round_bf16(y)
         return val, code.astype(np.uint16), None
-    amax = np.max(np.abs(y), axis=-1)
-    scale = np.where(amax > 0, amax / E4M3_MAX, 1.0)
-    val, code = round_e4m3(y / scale[..., None])
-    return val, code.astype(np.uint8), scale
+    amax = np.max(np.abs(y), axis=-1, keepdims=True)
+    pos = amax > 0
+    scale = np.where(pos, amax / E4M3_MAX, 1.0)
+    # y / scale written as (y * 448) / amax: one rounding of the exact quotient, so a value
+    # exactly on a rounding midpoint (common for bf16 inputs) is decided to even
+    v = np.where(pos, y * E4M3_MAX / np.where(pos, amax, 1.0), y)
+    val, code = round_e4m3(v)
+    return val, code.astype(np.uint8), scale[..., 0]
 
 
 def prologue(qkv_u16, num_q_heads: int, num_kv_heads: int, positions, cos_sin, rotary_dim: int,
