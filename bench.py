@@ -320,6 +320,8 @@ def bench_ours(args, device, rank, world):
                          "speedup_of_dynamic": round(s_ms / (t_dec + t_comb), 3),
                          "speedup_of_dynamic_with_plan": round(s_ms / ms_per_step, 3)}
 
+    prologue = bench_prologue(dsa, device, w, B, timed, max(10, min(args.steps, 200)))
+
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     host = {k: inp[k].cpu().pin_memory() for k in ("q", "q_scale", "k_pages", "v_pages", "k_scale", "v_scale",
                                                    "block_table", "seq_lens") if inp[k] is not None}
@@ -379,6 +381,7 @@ def bench_ours(args, device, rank, world):
                           "note": "dsa_plan -> dsa_decode_fused (combine inside the persistent kernel)"},
         "pct_of_nominal_8tbs": round(100 * nbytes / (ms_per_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 1),
         "static": static,
+        "prologue": prologue,
         "roofline": {"bound": "hbm", "kernel": "attn_kernel (persistent decode, dsa_decode)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
@@ -389,6 +392,50 @@ def bench_ours(args, device, rank, world):
         "clocks": clk,
     }
     return res, inp, nbytes
+
+
+def prologue_bytes(n_tokens: int, hq: int, hkv: int, fp8: bool, rot: int = 128) -> int:
+    """Algorithmic bytes of dsa_prologue: per token its qkv row, position, slot and cos/sin
+    row read once; its Q and K/V rows (and FP8 scales) written once."""
+    rd = (hq + 2 * hkv) * 128 * 2 + 4 + 4 + rot * 4
+    wr = (hq + 2 * hkv) * 128 * (1 if fp8 else 2) + ((hq + 2 * hkv) * 4 if fp8 else 0)
+    return n_tokens * (rd + wr)
+
+
+def bench_prologue(dsa, device, w, batch: int, timed, steps: int) -> dict:
+    """dsa_prologue (QK-Norm, RoPE, Hadamard, encoding, cache write) for the decode batch of
+    this workload and for a 16384-token prefill chunk of the same heads and dtypes."""
+    fp8 = w.kv_dtype == "fp8"
+    res = {"chain": "RMSNorm(Q, K) -> RoPE neox, rotary_dim 128 -> Hadamard(Q, K) -> "
+                    + ("E4M3 + per-(token, head) scale" if fp8 else "bf16") + " -> paged cache write"}
+    peak, _ = measured_peaks()
+    for label, n in (("decode_batch", batch), ("prefill_16k", 16384)):
+        num_pages = (n + 63) // 64 + 1
+        pin = workloads.make_prologue_inputs(n, w.num_q_heads, w.num_kv_heads, num_pages, seed=1, device=device,
+                                             skip_fraction=0.0)
+        shape = (num_pages, w.num_kv_heads, 64, 128)
+        dt = torch.uint8 if fp8 else torch.bfloat16
+        kp, vp = torch.zeros(shape, dtype=dt, device=device), torch.zeros(shape, dtype=dt, device=device)
+        ks = torch.zeros(shape[:3], dtype=torch.float32, device=device) if fp8 else None
+        vs = torch.zeros(shape[:3], dtype=torch.float32, device=device) if fp8 else None
+        q = torch.empty(n, w.num_q_heads, 128, dtype=dt, device=device)
+        qs = torch.empty(n, w.num_q_heads, dtype=torch.float32, device=device) if fp8 else None
+        st = torch.zeros(1, dtype=torch.int32, device=device)
+
+        def run(pin=pin, kp=kp, vp=vp, ks=ks, vs=vs, q=q, qs=qs, st=st):
+            dsa.prologue(pin["qkv"], w.num_q_heads, w.num_kv_heads, pin["slot_mapping"], kp, vp, ks, vs,
+                         positions=pin["positions"], cos_sin=pin["cos_sin"], q_norm_weight=pin["q_norm_weight"],
+                         k_norm_weight=pin["k_norm_weight"], hadamard=True, q_dtype=dt, q_out=q, q_scale=qs,
+                         status=st)
+
+        ms = float(timed([run], steps, 3).mean())
+        if dsa.read_status(st) != 0:
+            raise RuntimeError(f"prologue {label}: device status set")
+        nb = prologue_bytes(n, w.num_q_heads, w.num_kv_heads, fp8)
+        gbs = nb / (ms * 1e-3) / 1e9
+        res[label] = {"tokens": n, "us": round(ms * 1e3, 2), "algorithmic_bytes": nb, "GB/s": round(gbs, 1),
+                      "frac_of_hbm_peak": round(gbs / peak, 4)}
+    return res
 
 
 # ---------------------------------------------------------------------------- CPU oracle

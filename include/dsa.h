@@ -78,9 +78,11 @@ typedef enum {
 
 /* Bits of the device status word (task map meta[3], or the static path's word). */
 #define DSA_DEV_BAD_SEQLEN 1   /* seq_len < 0, > max_pages_per_req * P, or not covered by the grid */
-#define DSA_DEV_BAD_PAGE 2     /* block_table entry outside [0, num_pages) */
+#define DSA_DEV_BAD_PAGE 2     /* block_table entry outside [0, num_pages); dsa_prologue: a
+                                  cache slot outside [-1, num_pages * P) */
 #define DSA_DEV_TIMEOUT 4      /* an in-kernel pipeline wait passed its time limit; work abandoned */
 #define DSA_DEV_BAD_MAP 8      /* task map inconsistent with the decode arguments */
+#define DSA_DEV_BAD_POSITION 32 /* dsa_prologue: a position outside [0, max_position) */
 
 typedef enum { DSA_BF16 = 0, DSA_FP8_E4M3 = 1, DSA_FP32 = 2 } dsa_dtype;
 
@@ -250,6 +252,54 @@ dsa_status dsa_static_combine(int32_t num_splits, const float *partial_o, const 
  */
 dsa_status dsa_read_status(const int32_t *device_status, int32_t *host_status);
 dsa_status dsa_get_status(const dsa_task_map *map, int32_t *host_status);
+
+/*
+ * dsa_prologue -- the fused attention prologue that produces this library's inputs
+ * (HPC-Ops × SGLang blog, "融合式 attention 前导": QK-Norm before RoPE, Q in FP8 with
+ * one scale per (token, head) passed to the attention kernel without requantising, K
+ * and V written directly into the paged FP8 cache; Hy3 preview write-up 2.2.1 "Fused
+ * Rope+Norm+[Hadamard]+Quant+Store KV", one kernel, intermediates kept in registers,
+ * quantised online before the cache write; 2.6.1 "Hadamard在线旋转变换", an orthogonal
+ * rotation of Q and K before quantisation).  For every token n and head:
+ *   Q and K heads:  y = RMSNorm(x) = x / sqrt(mean(x^2) + norm_eps) * w   (if w given)
+ *                   y = RoPE(y, positions[n])                           (if rotary_dim)
+ *                   y = H_128 y / sqrt(128)                              (if hadamard)
+ *   V heads:        y = x
+ *   encoding:       FP8: scale = amax(|y|) / 448 (1 if y = 0), byte = E4M3(y / scale),
+ *                   round to nearest even, saturating; BF16: round to nearest even.
+ * Q goes to q_out [n_tokens, Hq, 128] (q_scale [n_tokens, Hq] for FP8); K and V go
+ * to slot s = slot_mapping[n] of the cache, i.e. page s / 64, offset s % 64 of
+ * k_pages / v_pages [num_pages, Hkv, 64, 128] (k/v_scale [num_pages, Hkv, 64] for
+ * FP8), the layout dsa_decode reads.  s = -1 writes nothing for that token.
+ * Arguments:
+ *   qkv            [n_tokens, (Hq + 2 Hkv) * 128] bf16: the QKV projection output,
+ *                  heads in the order Q, K, V.
+ *   positions      [n_tokens] int32, row of cos_sin (needed when rotary_dim > 0).
+ *   cos_sin        [max_position, rotary_dim] fp32: cos(angle i) in column i and
+ *                  sin(angle i) in column rotary_dim/2 + i, i < rotary_dim/2.
+ *   rotary_dim     0 (no RoPE), 16, 32, 64 or 128: dims >= rotary_dim pass through.
+ *   rope_style     DSA_ROPE_NEOX rotates the pairs (i, i + rotary_dim/2);
+ *                  DSA_ROPE_INTERLEAVED the pairs (2i, 2i + 1); pair i uses angle i.
+ *   q_norm_weight, k_norm_weight  [128] fp32, or NULL for no normalisation of that
+ *                  input; norm_eps >= 0.
+ *   hadamard       nonzero: apply the Hadamard rotation to Q and K.
+ *   q_dtype, kv_dtype  DSA_BF16 or DSA_FP8_E4M3 (scales required for FP8).
+ *   status         device int32 or NULL: DSA_DEV_BAD_POSITION for a position outside
+ *                  [0, max_position) (that token's Q and K rows are not written),
+ *                  DSA_DEV_BAD_PAGE for a slot outside [-1, num_pages * 64) (that
+ *                  token's K and V are not written).
+ * head_dim must be 128 and page_size 64.  qkv, q_out, the pages, cos_sin and the
+ * weights must be 16-byte aligned.  Several tokens must not share a slot.
+ */
+typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_INTERLEAVED = 1 } dsa_rope_style;
+dsa_status dsa_prologue(const void *qkv, int32_t n_tokens, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_dim, const int32_t *positions, const float *cos_sin,
+                        int32_t max_position, int32_t rotary_dim, int32_t rope_style,
+                        const float *q_norm_weight, const float *k_norm_weight, float norm_eps,
+                        int32_t hadamard, const int32_t *slot_mapping, void *q_out, dsa_dtype q_dtype,
+                        float *q_scale, void *k_pages, void *v_pages, dsa_dtype kv_dtype,
+                        float *k_scale, float *v_scale, int32_t num_pages, int32_t page_size,
+                        int32_t *status, dsa_stream stream);
 
 /*
  * dsa_decode_step_noalloc -- one whole decode step (dsa_plan, dsa_decode,

@@ -22,7 +22,9 @@ _lib = ctypes.CDLL(LIB_PATH)
 # dsa_status
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_BUFFER_TOO_SMALL, ERR_CUDA, ERR_DEVICE_INPUT = range(6)
 # device status bits
-DEV_BAD_SEQLEN, DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_MAP = 1, 2, 4, 8
+DEV_BAD_SEQLEN, DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_MAP, DEV_BAD_POSITION = 1, 2, 4, 8, 32
+# dsa_rope_style
+ROPE_NEOX, ROPE_INTERLEAVED = 0, 1
 # dsa_dtype
 BF16, FP8_E4M3, FP32 = 0, 1, 2
 
@@ -71,6 +73,9 @@ _lib.dsa_decode_step_noalloc.argtypes = _attn_args + [_i32, _i32, _vp, _i32, _vp
 _lib.dsa_decode_step_noalloc.restype = ctypes.c_int
 _lib.dsa_selftest_wait_timeout.argtypes = [_vp, ctypes.c_int64, _vp]
 _lib.dsa_selftest_wait_timeout.restype = ctypes.c_int
+_lib.dsa_prologue.argtypes = [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _f32, _i32, _vp,
+                              _vp, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp]
+_lib.dsa_prologue.restype = ctypes.c_int
 _lib.dsa_status_string.argtypes = [ctypes.c_int]
 _lib.dsa_status_string.restype = ctypes.c_char_p
 
@@ -255,6 +260,32 @@ def static_combine(num_splits: int, partial_o, partial_lse, batch: int, num_q_he
                                  _stream(stream))
     _check(rc, "dsa_static_combine")
     return out
+
+
+def prologue(qkv, num_q_heads: int, num_kv_heads: int, slot_mapping, k_pages, v_pages, k_scale=None,
+             v_scale=None, positions=None, cos_sin=None, rotary_dim: int | None = None, rope_style: str = "neox",
+             q_norm_weight=None, k_norm_weight=None, eps: float = 1e-6, hadamard: bool = False,
+             q_dtype=torch.bfloat16, q_out=None, q_scale=None, status=None, stream=None):
+    """dsa_prologue: QK-Norm -> RoPE -> [Hadamard] -> Q out (bf16, or E4M3 + per-(token, head)
+    scales) and K/V written into the paged cache at slot_mapping.  Returns (q_out, q_scale)."""
+    n = int(qkv.shape[0])
+    fp8_q = q_dtype in (torch.uint8, torch.float8_e4m3fn, "e4m3")
+    if q_out is None:
+        q_out = torch.empty(n, num_q_heads, HEAD_DIM, dtype=torch.uint8 if fp8_q else torch.bfloat16,
+                            device=qkv.device)
+    if fp8_q and q_scale is None:
+        q_scale = torch.empty(n, num_q_heads, dtype=torch.float32, device=qkv.device)
+    rot = (0 if cos_sin is None else int(cos_sin.shape[1])) if rotary_dim is None else rotary_dim
+    max_pos = 0 if cos_sin is None else int(cos_sin.shape[0])
+    style = {"neox": ROPE_NEOX, "interleaved": ROPE_INTERLEAVED}[rope_style]
+    rc = _lib.dsa_prologue(_ptr(qkv), n, num_q_heads, num_kv_heads, HEAD_DIM, _ptr(positions), _ptr(cos_sin),
+                           max_pos, rot, style, _ptr(q_norm_weight), _ptr(k_norm_weight), float(eps),
+                           int(bool(hadamard)), _ptr(slot_mapping), _ptr(q_out), _dtype_code(q_out),
+                           _ptr(q_scale), _ptr(k_pages), _ptr(v_pages), _dtype_code(k_pages), _ptr(k_scale),
+                           _ptr(v_scale), int(k_pages.shape[0]), int(k_pages.shape[2]), _ptr(status),
+                           _stream(stream))
+    _check(rc, "dsa_prologue")
+    return q_out, q_scale
 
 
 def get_status(task_map: TaskMap) -> int:

@@ -4,6 +4,14 @@
 
 namespace dsa {
 
+int sm_count() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!cached[dev]) cudaDeviceGetAttribute(&cached[dev], cudaDevAttrMultiProcessorCount, dev);
+    return cached[dev];
+}
+
 dsa_status validate_attn(const AttnArgs &a) {
     if (a.batch < 0 || a.num_q_heads < 1 || a.num_kv_heads < 1 || a.num_q_heads % a.num_kv_heads != 0 ||
         a.max_pages_per_req < 0 || a.num_pages < 0)

@@ -1040,14 +1040,6 @@ KernelParams base_params(const AttnArgs &a, float *partial_o, float *partial_lse
 constexpr int kPersistStagesBf16 = 4, kPersistStagesFp8 = 8, kPersistGroups = 2, kPersistMergeSlots = 2;
 constexpr int kPairStagesBf16 = 2, kPairStagesFp8 = 4, kPairGroups = 1;
 
-int sm_count() {
-    static int cached[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (!cached[dev]) cudaDeviceGetAttribute(&cached[dev], cudaDevAttrMultiProcessorCount, dev);
-    return cached[dev];
-}
-
 // Persistent launch: the CTA shape that keeps all of the map's bins resident at once.
 template <int KV, bool FUSE>
 dsa_status launch_persistent(const AttnArgs &a, const KernelParams &kp, int num_ctas, cudaStream_t st) {

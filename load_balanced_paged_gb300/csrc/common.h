@@ -67,4 +67,7 @@ struct AttnArgs {
 
 dsa_status validate_attn(const AttnArgs &a);
 
+// Multiprocessor count of the current device (cached per device; 0 if unknown).
+int sm_count();
+
 }  // namespace dsa

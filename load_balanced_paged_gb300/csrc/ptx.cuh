@@ -167,6 +167,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
     return r;
 }
 
+// Two floats to two E4M3 bytes (hi -> high byte), round to nearest even, saturating at
+// +-448.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));

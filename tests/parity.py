@@ -108,3 +108,60 @@ def sub_problem(inp: dict, requests) -> oracle.Problem:
     return oracle.Problem(np_bytes(inp["q"][requests]), pools["k_pages"], pools["v_pages"], new_bt, lens,
                           inp["num_q_heads"], inp["num_kv_heads"], inp["sm_scale"], q_scale=qs,
                           k_scale=pools["k_scale"], v_scale=pools["v_scale"])
+
+
+# ---------------------------------------------------------------- prologue encodings
+# Bound on the fp32 prologue chain's absolute error, as a fraction of the row's largest
+# |value|: the sum of 128 squares, one reciprocal square root, two products (RMSNorm), two
+# products and a sum (RoPE) and seven butterfly stages (Hadamard) leave a few fp32 ulps of
+# the row's scale; 5e-5 leaves a wide margin and is still far below an E4M3 step (2^-4
+# relative) or a bf16 step (2^-8 relative) for all but the row's tiniest values.
+PROLOGUE_ERR = 5e-5
+
+
+def _e4m3_lut():
+    return np.array([oracle.e4m3_to_double(c) for c in range(256)])
+
+
+def assert_encoded(got_codes, got_scale, y, kind: str, err_abs, what: str = ""):
+    """GPU encodings of the oracle rows y [rows, 128] (fp64, before encoding).
+
+    err_abs [rows] bounds the kernel's fp32 error in y.  A code is accepted when its value
+    lies between the round-to-nearest-even of the two ends of the interval y can have
+    moved in, so a rounding decision is only allowed to differ from the exact one where y
+    sits within that error of a rounding midpoint; the fraction of such differences must
+    stay below 1e-3.  E4M3: the scale must be amax/448 within the same error."""
+    from oracle import prologue as P
+    y = np.asarray(y, np.float64).reshape(-1, 128)
+    E = np.asarray(err_abs, np.float64).reshape(-1, 1)
+    if kind == "bf16":
+        got = P.bf16_to_double(np.asarray(got_codes).view(np.uint16).reshape(-1, 128))
+        lo, hi, exact = P.round_bf16(y - E)[0], P.round_bf16(y + E)[0], P.round_bf16(y)[0]
+    else:
+        got = _e4m3_lut()[np.asarray(got_codes).view(np.uint8).reshape(-1, 128)]
+        amax = np.abs(y).max(axis=1, keepdims=True)
+        s = np.where(amax > 0, amax / 448.0, 1.0)
+        gs = np.asarray(got_scale, np.float64).reshape(-1, 1)
+        s_tol = (E + amax * 2.0 ** -22) / 448.0
+        bad_s = np.abs(gs - s) > s_tol
+        assert not bad_s.any(), f"{what}: {int(bad_s.sum())} scales off (first row {int(np.argmax(bad_s))})"
+        v = np.where(amax > 0, y * 448.0 / np.where(amax > 0, amax, 1.0), y)
+        rel = np.where(amax > 0, E / np.where(amax > 0, amax, 1.0), 0.0) + 2.0 ** -21
+        d = E / s + np.abs(v) * rel
+        lo, hi, exact = P.round_e4m3(v - d)[0], P.round_e4m3(v + d)[0], P.round_e4m3(v)[0]
+    ties = np.zeros(y.shape, bool)
+    if kind != "bf16":
+        # values exactly on an E4M3 rounding midpoint (frequent when y has few significant
+        # bits, e.g. bf16 V rows): the kernel evaluates y / scale as y * (448 / amax), whose
+        # last-bit rounding decides these either way, so both neighbours count as exact
+        tv, _ = P._e4m3_table()
+        mids = (tv[:-1] + tv[1:]) / 2
+        ties = np.isin(np.abs(v), mids)
+    bad = ~((got >= lo) & (got <= hi))
+    if bad.any():
+        r, c = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {int(bad.sum())} codes outside the rounding interval; row {r} dim {c}: "
+                             f"got {got[r, c]!r}, allowed [{lo[r, c]!r}, {hi[r, c]!r}]")
+    flips = float(np.mean((got != exact) & ~ties))
+    assert flips < 1e-3, f"{what}: {flips:.2e} of the codes differ from the exact rounding"
+    return flips

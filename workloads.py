@@ -204,3 +204,50 @@ def host_view(inp: dict) -> dict:
         return t.numpy()
     keys = ("q", "q_scale", "k_pages", "v_pages", "k_scale", "v_scale", "block_table", "seq_lens")
     return {k: np_bytes(inp[k]) for k in keys}
+
+
+def rotary_table(max_position: int, rotary_dim: int, theta: float = 10000.0) -> np.ndarray:
+    """The usual RoPE cos/sin table [max_position, rotary_dim] as fp32: column i <
+    rotary_dim/2 holds cos(p * theta^(-2i/rotary_dim)), column rotary_dim/2 + i its sin.
+    An input of the prologue (a model constant), computed once here in fp64."""
+    inv = theta ** (-np.arange(0, rotary_dim, 2, dtype=np.float64) / rotary_dim)
+    ang = np.arange(max_position, dtype=np.float64)[:, None] * inv[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def make_prologue_inputs(n_tokens: int, num_q_heads: int, num_kv_heads: int, num_pages: int, seed: int = 0,
+                         device="cpu", rotary_dim: int = 128, max_position: int = 8192,
+                         skip_fraction: float = 0.1, outlier_channels: int = 4) -> dict:
+    """Inputs of the fused prologue for n_tokens tokens.
+
+    Draw order: numpy Generator(PCG64(seed)) gives the positions (uniform in
+    [0, max_position)), distinct cache slots in [0, num_pages * 64) with a fraction
+    set to -1 (tokens that write no K/V), and the outlier channels; then
+    torch.Generator(device).manual_seed(seed) gives qkv ~ N(0, 1) with the outlier
+    channels of every Q/K head scaled by 20 (the outliers a Hadamard rotation spreads),
+    cast to bf16, and the Q/K norm weights ~ U(0.5, 1.5) in fp32."""
+    rng = np.random.default_rng(seed)
+    positions = rng.integers(0, max_position, n_tokens).astype(np.int32)
+    slots = rng.choice(num_pages * PAGE, n_tokens, replace=False).astype(np.int32)
+    slots[rng.random(n_tokens) < skip_fraction] = -1
+    chans = rng.choice(HEAD_DIM, outlier_channels, replace=False)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    H = num_q_heads + 2 * num_kv_heads
+    x = torch.randn((n_tokens, H, HEAD_DIM), generator=gen, device=device, dtype=torch.float32)
+    x[:, :num_q_heads + num_kv_heads, torch.as_tensor(chans, device=device)] *= 20.0
+    qw = torch.rand(HEAD_DIM, generator=gen, device=device, dtype=torch.float32) + 0.5
+    kw = torch.rand(HEAD_DIM, generator=gen, device=device, dtype=torch.float32) + 0.5
+    return {
+        "qkv": x.reshape(n_tokens, H * HEAD_DIM).to(torch.bfloat16).contiguous(),
+        "positions": torch.from_numpy(positions).to(device),
+        "slot_mapping": torch.from_numpy(slots).to(device),
+        "cos_sin": torch.from_numpy(rotary_table(max_position, rotary_dim)).to(device),
+        "q_norm_weight": qw,
+        "k_norm_weight": kw,
+        "num_q_heads": num_q_heads,
+        "num_kv_heads": num_kv_heads,
+        "num_pages": num_pages,
+        "rotary_dim": rotary_dim,
+    }
+
