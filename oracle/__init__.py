@@ -64,7 +64,7 @@ def lib():
             common = [_vp, ctypes.c_int32, _f32p, _vp, _vp, ctypes.c_int32, _f32p, _f32p,
                       _i32p, ctypes.c_int32, ctypes.c_int32, _i32p, ctypes.c_int32,
                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                      ctypes.c_double]
+                      ctypes.c_double, ctypes.c_int32]
             L.oracle_attention_span.argtypes = common + [ctypes.c_int32, ctypes.c_int32,
                                                          ctypes.c_int64, ctypes.c_int64, _f64p, _f64p]
             L.oracle_attention_span.restype = ctypes.c_int
@@ -134,10 +134,12 @@ def static_split(mode: int, param: int, tile: int, num_splits: int, n_tiles: int
 
 
 class Problem:
-    """Host copies of one decode step's inputs (exact bytes)."""
+    """Host copies of one decode step's inputs (exact bytes).  q_len > 1: each request
+    has q_len query tokens, q [B, q_len, Hq, d] (q_scale [B, q_len, Hq]), the last q_len
+    positions of the request, each seeing the tokens up to its own position."""
 
     def __init__(self, q, k_pages, v_pages, block_table, seq_lens, num_q_heads, num_kv_heads,
-                 sm_scale, q_scale=None, k_scale=None, v_scale=None, head_dim=128, page_size=64):
+                 sm_scale, q_scale=None, k_scale=None, v_scale=None, head_dim=128, page_size=64, q_len=1):
         self.q_dtype = E4M3 if q.dtype == np.uint8 else BF16
         self.kv_dtype = E4M3 if k_pages.dtype == np.uint8 else BF16
         self.q = np.ascontiguousarray(q)
@@ -156,6 +158,9 @@ class Problem:
         self.head_dim = int(head_dim)
         self.page_size = int(page_size)
         self.sm_scale = float(sm_scale)
+        self.q_len = int(q_len)
+        if self.q.size != self.batch * self.q_len * self.num_q_heads * self.head_dim:
+            raise ValueError("q does not hold B x q_len x Hq x d values")
         if self.q_dtype == E4M3 and self.q_scale is None:
             raise ValueError("FP8 Q needs q_scale")
         if self.kv_dtype == E4M3 and (self.k_scale is None or self.v_scale is None):
@@ -167,17 +172,18 @@ class Problem:
                 _p(self.k_scale, _f32p), _p(self.v_scale, _f32p),
                 _p(self.block_table, _i32p), self.max_pages, self.num_pages,
                 _p(self.seq_lens, _i32p), self.batch, self.num_q_heads, self.num_kv_heads,
-                self.head_dim, self.page_size, self.sm_scale]
+                self.head_dim, self.page_size, self.sm_scale, self.q_len]
 
     @property
     def group(self) -> int:
         return self.num_q_heads // self.num_kv_heads
 
     def attention(self, units=None, n_threads: int = 0):
-        """Unsplit attention.  Returns (out [B, Hq, d], lse [B, Hq]) in fp64; rows of
-        units not listed are left NaN."""
-        out = np.full((self.batch, self.num_q_heads, self.head_dim), np.nan, np.float64)
-        lse = np.full((self.batch, self.num_q_heads), np.nan, np.float64)
+        """Unsplit attention.  Returns (out [B, Hq, d], lse [B, Hq]) in fp64, or [B, q_len,
+        Hq, d] / [B, q_len, Hq] for q_len > 1; rows of units not listed are left NaN."""
+        lead = (self.batch,) if self.q_len == 1 else (self.batch, self.q_len)
+        out = np.full(lead + (self.num_q_heads, self.head_dim), np.nan, np.float64)
+        lse = np.full(lead + (self.num_q_heads,), np.nan, np.float64)
         u = _c(units, np.int32)
         n = 0 if u is None else int(u.shape[0])
         rc = lib().oracle_attention(*self._common(), _p(u, _i32p), n, int(n_threads),
@@ -188,10 +194,11 @@ class Problem:
 
     def span(self, b: int, h: int, tok0: int, tok1: int):
         """Attention of the G query heads on KV head h of request b over tokens
-        [tok0, tok1).  Returns (o [G, d], lse [G])."""
-        G = self.group
-        o = np.zeros((G, self.head_dim), np.float64)
-        lse = np.zeros(G, np.float64)
+        [tok0, tok1) (each query token further limited to its own position).  Returns
+        (o [q_len*G, d], lse [q_len*G]), row i*G + g."""
+        R = self.q_len * self.group
+        o = np.zeros((R, self.head_dim), np.float64)
+        lse = np.zeros(R, np.float64)
         rc = lib().oracle_attention_span(*self._common(), int(b), int(h), int(tok0), int(tok1),
                                          _p(o, _f64p), _p(lse, _f64p))
         if rc != 0:

@@ -230,86 +230,98 @@ typedef struct {
     const float *k_scale; const float *v_scale;
     const int32_t *block_table; int32_t max_pages_per_req; int32_t num_pages;
     const int32_t *seq_lens; int32_t batch; int32_t num_q_heads; int32_t num_kv_heads;
-    int32_t head_dim; int32_t page_size; double sm_scale;
+    int32_t head_dim; int32_t page_size; double sm_scale; int32_t q_len;
 } orc_problem;
 
 /*
  * Exact attention of the G query heads of request b that share KV head h, over
- * the tokens [tok0, tok1) of that request:
- *   s_t = sm_scale * sum_i Q[b, j, i] * K[t, i]          (j = h*G .. h*G+G-1)
- *   o_j = sum_t exp(s_t - M) V[t, :] / sum_t exp(s_t - M), M = max_t s_t
- *   lse_j = M + ln sum_t exp(s_t - M)
- * Token t of request b lives in page block_table[b][t / page_size] at slot
- * t mod page_size; a page holds [Hkv][page_size][d] elements.  FP8 values are
- * decode(byte) * scale: Q scale per (b, q head), K/V scale per (page, KV head,
- * slot).  An empty range gives o = 0, lse = -inf.  Returns nonzero if a page
- * id is out of range.
+ * the tokens [tok0, tok1) of that request, for each of the request's q_len query
+ * tokens.  Query token i (0 <= i < q_len) stands at position len_b - q_len + i
+ * and sees the tokens t <= that position (causal within the draft of a
+ * multi-token verify step; the Hy3 write-up's MTP section, and the GB300
+ * low-latency write-up's verify step of 1 + 5 draft tokens), so its range is
+ * [tok0, min(tok1, len_b - q_len + i + 1)):
+ *   s_t = sm_scale * sum_k Q[b, i, j, k] * K[t, k]          (j = h*G .. h*G+G-1)
+ *   o = sum_t exp(s_t - M) V[t, :] / sum_t exp(s_t - M), M = max_t s_t
+ *   lse = M + ln sum_t exp(s_t - M)
+ * Output row i*G + g.  Token t of request b lives in page block_table[b][t /
+ * page_size] at slot t mod page_size; a page holds [Hkv][page_size][d]
+ * elements.  FP8 values are decode(byte) * scale: Q scale per (b, i, q head),
+ * K/V scale per (page, KV head, slot).  An empty range gives o = 0, lse = -inf.
+ * Returns nonzero if a page id is out of range.
  */
 static int span(const orc_problem *p, int32_t b, int32_t h, int64_t tok0, int64_t tok1,
-                double *out /*[G*d]*/, double *lse /*[G]*/, double *scratch /*[tok1-tok0]*/) {
+                double *out /*[q_len*G*d]*/, double *lse /*[q_len*G]*/, double *scratch /*[tok1-tok0]*/) {
     const int32_t G = p->num_q_heads / p->num_kv_heads;
     const int32_t d = p->head_dim;
     const int32_t P = p->page_size;
-    for (int32_t g = 0; g < G; ++g) {
-        int32_t j = h * G + g;
-        double *o = out + (int64_t)g * d;
-        for (int32_t i = 0; i < d; ++i) o[i] = 0.0;
-        if (tok1 <= tok0) { lse[g] = -INFINITY; continue; }
-        double qs = (p->q_dtype == ORC_E4M3) ? (double)p->q_scale[(int64_t)b * p->num_q_heads + j] : 1.0;
-        int64_t qbase = ((int64_t)b * p->num_q_heads + j) * d;
-        /* scores */
-        double M = -INFINITY;
-        for (int64_t t = tok0; t < tok1; ++t) {
-            int32_t page = p->block_table[(int64_t)b * p->max_pages_per_req + t / P];
-            if (page < 0 || page >= p->num_pages) return 1;
-            int64_t row = ((int64_t)page * p->num_kv_heads + h) * P + (t % P);
-            double ks = (p->kv_dtype == ORC_E4M3) ? (double)p->k_scale[row] : 1.0;
-            double dot = 0.0;
-            for (int32_t i = 0; i < d; ++i)
-                dot += load_elem(p->q, p->q_dtype, qbase + i) * qs *
-                       load_elem(p->k_pages, p->kv_dtype, row * d + i) * ks;
-            double s = p->sm_scale * dot;
-            scratch[t - tok0] = s;
-            if (s > M) M = s;
+    const int64_t len = p->seq_lens[b] > 0 ? p->seq_lens[b] : 0;
+    for (int32_t qi = 0; qi < p->q_len; ++qi) {
+        int64_t end = len - p->q_len + qi + 1;  /* tokens this query token sees */
+        if (end > tok1) end = tok1;
+        for (int32_t g = 0; g < G; ++g) {
+            int32_t j = h * G + g;
+            int64_t r = (int64_t)qi * G + g;
+            double *o = out + r * d;
+            for (int32_t k = 0; k < d; ++k) o[k] = 0.0;
+            if (end <= tok0) { lse[r] = -INFINITY; continue; }
+            int64_t qrow = ((int64_t)b * p->q_len + qi) * p->num_q_heads + j;
+            double qs = (p->q_dtype == ORC_E4M3) ? (double)p->q_scale[qrow] : 1.0;
+            int64_t qbase = qrow * d;
+            /* scores */
+            double M = -INFINITY;
+            for (int64_t t = tok0; t < end; ++t) {
+                int32_t page = p->block_table[(int64_t)b * p->max_pages_per_req + t / P];
+                if (page < 0 || page >= p->num_pages) return 1;
+                int64_t row = ((int64_t)page * p->num_kv_heads + h) * P + (t % P);
+                double ks = (p->kv_dtype == ORC_E4M3) ? (double)p->k_scale[row] : 1.0;
+                double dot = 0.0;
+                for (int32_t k = 0; k < d; ++k)
+                    dot += load_elem(p->q, p->q_dtype, qbase + k) * qs *
+                           load_elem(p->k_pages, p->kv_dtype, row * d + k) * ks;
+                double sc = p->sm_scale * dot;
+                scratch[t - tok0] = sc;
+                if (sc > M) M = sc;
+            }
+            /* softmax-weighted sum of V */
+            double l = 0.0;
+            for (int64_t t = tok0; t < end; ++t) {
+                int32_t page = p->block_table[(int64_t)b * p->max_pages_per_req + t / P];
+                int64_t row = ((int64_t)page * p->num_kv_heads + h) * P + (t % P);
+                double vs = (p->kv_dtype == ORC_E4M3) ? (double)p->v_scale[row] : 1.0;
+                double w = exp(scratch[t - tok0] - M);
+                l += w;
+                for (int32_t k = 0; k < d; ++k)
+                    o[k] += w * load_elem(p->v_pages, p->kv_dtype, row * d + k) * vs;
+            }
+            for (int32_t k = 0; k < d; ++k) o[k] /= l;
+            lse[r] = M + log(l);
         }
-        /* softmax-weighted sum of V */
-        double l = 0.0;
-        for (int64_t t = tok0; t < tok1; ++t) {
-            int32_t page = p->block_table[(int64_t)b * p->max_pages_per_req + t / P];
-            int64_t row = ((int64_t)page * p->num_kv_heads + h) * P + (t % P);
-            double vs = (p->kv_dtype == ORC_E4M3) ? (double)p->v_scale[row] : 1.0;
-            double w = exp(scratch[t - tok0] - M);
-            l += w;
-            for (int32_t i = 0; i < d; ++i)
-                o[i] += w * load_elem(p->v_pages, p->kv_dtype, row * d + i) * vs;
-        }
-        for (int32_t i = 0; i < d; ++i) o[i] /= l;
-        lse[g] = M + log(l);
     }
     return 0;
 }
 
 static int check_problem(const orc_problem *p) {
     if (p->batch < 0 || p->num_kv_heads < 1 || p->num_q_heads < 1 || p->head_dim < 1 ||
-        p->page_size < 1 || p->num_q_heads % p->num_kv_heads != 0)
+        p->page_size < 1 || p->num_q_heads % p->num_kv_heads != 0 || p->q_len < 1)
         return -1;
     if (p->q_dtype != ORC_BF16 && p->q_dtype != ORC_E4M3) return -1;
     if (p->kv_dtype != ORC_BF16 && p->kv_dtype != ORC_E4M3) return -1;
     return 0;
 }
 
-/* One (request, KV head, token range): out [G*d], lse [G]. */
+/* One (request, KV head, token range): out [q_len*G*d], lse [q_len*G] (row i*G + g). */
 int oracle_attention_span(const void *q, int32_t q_dtype, const float *q_scale,
                           const void *k_pages, const void *v_pages, int32_t kv_dtype,
                           const float *k_scale, const float *v_scale,
                           const int32_t *block_table, int32_t max_pages_per_req, int32_t num_pages,
                           const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
                           int32_t num_kv_heads, int32_t head_dim, int32_t page_size, double sm_scale,
-                          int32_t b, int32_t h, int64_t tok0, int64_t tok1,
+                          int32_t q_len, int32_t b, int32_t h, int64_t tok0, int64_t tok1,
                           double *out, double *lse) {
     orc_problem p = {q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale,
                      block_table, max_pages_per_req, num_pages, seq_lens, batch,
-                     num_q_heads, num_kv_heads, head_dim, page_size, sm_scale};
+                     num_q_heads, num_kv_heads, head_dim, page_size, sm_scale, q_len};
     if (check_problem(&p) || b < 0 || b >= batch || h < 0 || h >= num_kv_heads) return -1;
     double *scratch = (double *)malloc(sizeof(double) * (size_t)(tok1 > tok0 ? tok1 - tok0 : 1));
     if (!scratch) return -3;
@@ -332,7 +344,8 @@ static void *attention_worker(void *arg) {
     int64_t cap = 1;
     for (int32_t b = 0; b < p->batch; ++b) if (p->seq_lens[b] > cap) cap = p->seq_lens[b];
     double *scratch = (double *)malloc(sizeof(double) * (size_t)cap);
-    if (!scratch) { job->rc = -3; return NULL; }
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)p->q_len * G * (p->head_dim + 1));
+    if (!scratch || !tmp) { free(scratch); free(tmp); job->rc = -3; return NULL; }
     for (;;) {
         pthread_mutex_lock(job->mu);
         int64_t k = job->next++;
@@ -341,18 +354,27 @@ static void *attention_worker(void *arg) {
         int32_t u = job->units ? job->units[k] : (int32_t)k;
         int32_t b = u / p->num_kv_heads, h = u % p->num_kv_heads;
         int32_t len = p->seq_lens[b] > 0 ? p->seq_lens[b] : 0;
-        int64_t row = (int64_t)b * p->num_q_heads + (int64_t)h * G;
-        if (span(p, b, h, 0, len, job->out + row * p->head_dim, job->out_lse + row, scratch))
-            job->rc = 1;
+        double *o = tmp, *l = tmp + (int64_t)p->q_len * G * p->head_dim;
+        if (span(p, b, h, 0, len, o, l, scratch)) job->rc = 1;
+        for (int32_t qi = 0; qi < p->q_len; ++qi) {  /* to out[b][qi][h*G + g] */
+            int64_t row = ((int64_t)b * p->q_len + qi) * p->num_q_heads + (int64_t)h * G;
+            for (int32_t g = 0; g < G; ++g) {
+                job->out_lse[row + g] = l[qi * G + g];
+                for (int32_t k = 0; k < p->head_dim; ++k)
+                    job->out[(row + g) * p->head_dim + k] = o[((int64_t)qi * G + g) * p->head_dim + k];
+            }
+        }
     }
     free(scratch);
+    free(tmp);
     return NULL;
 }
 
 /*
- * Unsplit attention for every query head of the listed units (u = b*Hkv + h;
- * units == NULL means all B*Hkv units), written at out[b][j][:] and
- * out_lse[b][j].  n_threads <= 0 uses every online core.  Returns nonzero on a
+ * Unsplit attention for every query token and query head of the listed units
+ * (u = b*Hkv + h; units == NULL means all B*Hkv units), written at
+ * out[b][i][j][:] and out_lse[b][i][j] (i < q_len; q_len = 1 is a plain decode
+ * step).  n_threads <= 0 uses every online core.  Returns nonzero on a
  * bad argument or an out-of-range page id.
  */
 int oracle_attention(const void *q, int32_t q_dtype, const float *q_scale,
@@ -361,11 +383,11 @@ int oracle_attention(const void *q, int32_t q_dtype, const float *q_scale,
                      const int32_t *block_table, int32_t max_pages_per_req, int32_t num_pages,
                      const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
                      int32_t num_kv_heads, int32_t head_dim, int32_t page_size, double sm_scale,
-                     const int32_t *units, int64_t n_units, int32_t n_threads,
+                     int32_t q_len, const int32_t *units, int64_t n_units, int32_t n_threads,
                      double *out, double *out_lse) {
     orc_problem p = {q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale,
                      block_table, max_pages_per_req, num_pages, seq_lens, batch,
-                     num_q_heads, num_kv_heads, head_dim, page_size, sm_scale};
+                     num_q_heads, num_kv_heads, head_dim, page_size, sm_scale, q_len};
     if (check_problem(&p)) return -1;
     if (!units) n_units = (int64_t)batch * num_kv_heads;
     if (n_threads <= 0) n_threads = (int32_t)sysconf(_SC_NPROCESSORS_ONLN);

@@ -50,3 +50,42 @@ def dense_attention(h: dict, num_q_heads: int, num_kv_heads: int, sm_scale: floa
             out[b, j] = softmax(s) @ vb[j // G]
             lse[b, j] = logsumexp(s)
     return out, lse
+
+
+def dense_attention_multi(h: dict, num_q_heads: int, num_kv_heads: int, sm_scale: float, q_len: int,
+                          page: int = 64):
+    """q [B, q_len, Hq, d]: query token i of request b (length n) stands at position
+    n - q_len + i and sees the tokens t <= that position; the score matrix of each
+    (request, query head) is masked to that causal pattern before scipy's softmax and
+    logsumexp."""
+    q = values(h, "q").reshape(-1, q_len, num_q_heads, h["q"].shape[-1])
+    if h.get("q_scale") is not None:
+        q = q * h["q_scale"].astype(np.float64).reshape(q.shape[:3])[..., None]
+    k = values(h, "k_pages")
+    v = values(h, "v_pages")
+    if h.get("k_scale") is not None:
+        k = k * h["k_scale"].astype(np.float64)[..., None]
+        v = v * h["v_scale"].astype(np.float64)[..., None]
+    B = h["seq_lens"].shape[0]
+    G = num_q_heads // num_kv_heads
+    d = q.shape[-1]
+    out = np.zeros((B, q_len, num_q_heads, d))
+    lse = np.full((B, q_len, num_q_heads), -np.inf)
+    for b in range(B):
+        n = int(h["seq_lens"][b])
+        if n <= 0:
+            continue
+        pages = h["block_table"][b, : (n + page - 1) // page]
+        kb = k[pages].transpose(1, 0, 2, 3).reshape(num_kv_heads, -1, d)[:, :n]
+        vb = v[pages].transpose(1, 0, 2, 3).reshape(num_kv_heads, -1, d)[:, :n]
+        t = np.arange(n)
+        for i in range(q_len):
+            visible = t <= n - q_len + i
+            if not visible.any():
+                continue
+            for j in range(num_q_heads):
+                s = sm_scale * (kb[j // G] @ q[b, i, j])
+                s = np.where(visible, s, -np.inf)
+                out[b, i, j] = softmax(s) @ vb[j // G]
+                lse[b, i, j] = logsumexp(s)
+    return out, lse

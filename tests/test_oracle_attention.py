@@ -18,8 +18,8 @@ from tests import brute
 HQ, HKV = 8, 2
 
 
-def tiny(lens, kv="bf16", seed=0, hq=HQ, hkv=HKV):
-    inp = workloads.make_inputs(np.array(lens), hq, hkv, kv, seed=seed, device="cpu")
+def tiny(lens, kv="bf16", seed=0, hq=HQ, hkv=HKV, q_len=1):
+    inp = workloads.make_inputs(np.array(lens), hq, hkv, kv, seed=seed, device="cpu", q_len=q_len)
     h = workloads.host_view(inp)
     return inp, h
 
@@ -27,7 +27,8 @@ def tiny(lens, kv="bf16", seed=0, hq=HQ, hkv=HKV):
 def problem(h, inp):
     return oracle.Problem(h["q"], h["k_pages"], h["v_pages"], h["block_table"], h["seq_lens"],
                           inp["num_q_heads"], inp["num_kv_heads"], inp["sm_scale"],
-                          q_scale=h["q_scale"], k_scale=h["k_scale"], v_scale=h["v_scale"])
+                          q_scale=h["q_scale"], k_scale=h["k_scale"], v_scale=h["v_scale"],
+                          q_len=inp.get("q_len", 1))
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
@@ -149,3 +150,57 @@ def test_units_subset_and_threads():
         rows = slice(hk * G, (hk + 1) * G)
         np.testing.assert_array_equal(sub[b, rows], full[b, rows])
     assert np.isnan(sub[0, G:]).all()
+
+
+# ---------------------------------------------------------------- multi-token queries
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("q_len", [2, 3, 6])
+def test_multi_token_matches_causal_brute_force(kv, q_len):
+    lens = [0, 1, 4, 6, 63, 64, 65, 130, 200]
+    inp, h = tiny(lens, kv, seed=5, q_len=q_len)
+    out, lse = problem(h, inp).attention()
+    ref, ref_lse = brute.dense_attention_multi(h, HQ, HKV, inp["sm_scale"], q_len)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+    # query tokens before the request's first token see nothing
+    for b, n in enumerate(lens):
+        for i in range(q_len):
+            if n - q_len + i < 0:
+                assert (out[b, i] == 0).all() and np.isneginf(lse[b, i]).all()
+
+
+@pytest.mark.parametrize("q_len", [2, 5])
+def test_multi_token_row_is_single_token_on_truncated_request(q_len):
+    """Query token i of a request of length n is a one-token decode over the first
+    n - q_len + i + 1 tokens: the same bytes through the q_len = 1 oracle."""
+    lens = [7, 64, 99, 140]
+    inp, h = tiny(lens, "fp8", seed=8, q_len=q_len)
+    out, lse = problem(h, inp).attention()
+    for i in range(q_len):
+        trunc = np.maximum(np.array(lens) - q_len + i + 1, 0).astype(np.int32)
+        one = oracle.Problem(np.ascontiguousarray(h["q"][:, i]), h["k_pages"], h["v_pages"], h["block_table"],
+                             trunc, HQ, HKV, inp["sm_scale"], q_scale=np.ascontiguousarray(h["q_scale"][:, i]),
+                             k_scale=h["k_scale"], v_scale=h["v_scale"])
+        o1, l1 = one.attention()
+        np.testing.assert_allclose(out[:, i], o1, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[:, i], l1, rtol=0, atol=1e-13)
+
+
+def test_multi_token_split_merge():
+    q_len = 4
+    lens = [3, 70, 257]
+    inp, h = tiny(lens, "bf16", seed=9, q_len=q_len)
+    prob = problem(h, inp)
+    out, lse = prob.attention()
+    rng = np.random.default_rng(0)
+    G = HQ // HKV
+    for b, n in enumerate(lens):
+        for hk in range(HKV):
+            cuts = np.unique(np.concatenate([[0, n], rng.integers(0, n + 1, 3)]))
+            parts = [prob.span(b, hk, a, c) for a, c in zip(cuts[:-1], cuts[1:])]
+            o = np.stack([p[0] for p in parts])
+            ls = np.stack([p[1] for p in parts])
+            mo, ml = oracle.merge(o, ls)
+            ref = out[b][:, hk * G:(hk + 1) * G].reshape(q_len * G, -1)
+            np.testing.assert_allclose(mo, ref, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(ml, lse[b][:, hk * G:(hk + 1) * G].reshape(-1), rtol=0, atol=1e-12)

@@ -107,11 +107,13 @@ def _quantize_e4m3(x: torch.Tensor):
 
 def make_inputs(lengths, num_q_heads: int, num_kv_heads: int, kv_dtype: str = "bf16",
                 seed: int = 0, device="cpu", head_dim: int = HEAD_DIM, page_size: int = PAGE,
-                rng: np.random.Generator | None = None, chunk_pages: int = 2048) -> dict:
+                rng: np.random.Generator | None = None, chunk_pages: int = 2048, q_len: int = 1) -> dict:
     """Build one decode step's inputs on `device`.
 
     `rng` continues the numpy stream used for the lengths (draw order above); if
-    None a fresh Generator(seed) is used for the page permutation.
+    None a fresh Generator(seed) is used for the page permutation.  q_len > 1 gives
+    each request q_len query tokens (a multi-token verify step): Q [B, q_len, Hq, d]
+    (Q scale [B, q_len, Hq]), drawn in that order from the same stream.
     """
     lens = np.asarray(lengths, np.int64)
     B = int(lens.shape[0])
@@ -143,9 +145,11 @@ def make_inputs(lengths, num_q_heads: int, num_kv_heads: int, kv_dtype: str = "b
         "page_size": page_size,
         "kv_dtype": kv_dtype,
         "sm_scale": 1.0 / math.sqrt(head_dim),
+        "q_len": q_len,
     }
     # Q
-    qf = torch.randn((B, num_q_heads, head_dim), generator=gen, device=device, dtype=torch.float32)
+    qshape = (B, num_q_heads, head_dim) if q_len == 1 else (B, q_len, num_q_heads, head_dim)
+    qf = torch.randn(qshape, generator=gen, device=device, dtype=torch.float32)
     if fp8:
         out["q"], out["q_scale"] = _quantize_e4m3(qf)
     else:
