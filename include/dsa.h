@@ -195,6 +195,38 @@ dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_sca
                             dsa_stream stream);
 
 /*
+ * dsa_decode_multi -- dsa_decode for q_len query tokens per request (a multi-token
+ * verify step: the Hy3 write-up's MTP section, and the GB300 low-latency write-up's
+ * verify of 1 + 5 draft tokens in one pass).  The task map, the scheduler and the KV
+ * stream are those of dsa_decode: each KV tile is read once and serves all q_len * G
+ * query rows of its unit.  Query token i of request b stands at position
+ * seq_lens[b] - q_len + i and sees the tokens t <= that position (causal within the
+ * draft; rows with no visible token in a descriptor get o = 0, lse = -inf there).
+ *   q        [B, q_len, Hq, 128] bf16 (row i*G + g of unit (b, h) is q[b][i][h*G + g]).
+ *   partial_o [map->max_descs, q_len*G, 128] fp32, partial_lse [map->max_descs, q_len*G].
+ * Supported: BF16 Q and K/V, q_len * G <= 64; q_len = 1 is exactly dsa_decode (all of
+ * its dtypes).  Other arguments and errors are as for dsa_decode.
+ */
+dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q_dtype, const float *q_scale,
+                            const void *k_pages, const void *v_pages, dsa_dtype kv_dtype,
+                            const float *k_scale, const float *v_scale,
+                            const int32_t *block_table, int32_t max_pages_per_req, int32_t num_pages,
+                            const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
+                            const dsa_task_map *map, float *partial_o, float *partial_lse,
+                            dsa_stream stream);
+
+/*
+ * dsa_combine_multi -- dsa_combine over the q_len * G partial rows of each unit:
+ * out [B, q_len, Hq, 128] (out_dtype DSA_BF16 or DSA_FP32), out_lse [B, q_len, Hq] or
+ * NULL.  q_len * G <= 64.  q_len = 1 is dsa_combine.
+ */
+dsa_status dsa_combine_multi(int32_t q_len, const dsa_task_map *map, const float *partial_o,
+                             const float *partial_lse, int32_t batch, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim, void *out, dsa_dtype out_dtype,
+                             float *out_lse, dsa_stream stream);
+
+/*
  * dsa_combine -- the combine kernel (blog, "围绕活跃 KV 工作进行调度": reads the
  * actual number of partials of each (request, head) and merges them under the
  * global softmax normalisation; Hy3 write-up 2.1.1 "Combine Kernel"):

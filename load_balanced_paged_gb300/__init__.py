@@ -59,6 +59,10 @@ _lib.dsa_decode_fused.argtypes = _attn_args + [_TMP, _vp, _vp, _vp, _vp, _i32, _
 _lib.dsa_decode_fused.restype = ctypes.c_int
 _lib.dsa_combine.argtypes = [_TMP, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]
 _lib.dsa_combine.restype = ctypes.c_int
+_lib.dsa_decode_multi.argtypes = [_i32] + _attn_args + [_TMP, _vp, _vp, _vp]
+_lib.dsa_decode_multi.restype = ctypes.c_int
+_lib.dsa_combine_multi.argtypes = [_i32, _TMP, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]
+_lib.dsa_combine_multi.restype = ctypes.c_int
 _lib.dsa_static_num_splits.argtypes = [_i32, _i32, _i32]
 _lib.dsa_static_num_splits.restype = _i32
 _lib.dsa_static_splitkv.argtypes = [_i32, _i32, _i32] + _attn_args + [_vp, _vp, _vp, _vp]
@@ -163,7 +167,7 @@ def plan(seq_lens: torch.Tensor, num_kv_heads: int, num_persistent_ctas: int, mi
 
 
 def _attn_args(q, k_pages, v_pages, block_table, seq_lens, num_kv_heads, sm_scale, q_scale, k_scale, v_scale):
-    batch, hq, d = q.shape
+    batch, hq, d = q.shape[0], q.shape[-2], q.shape[-1]
     num_pages, hkv, page, d2 = k_pages.shape
     if hkv != num_kv_heads:
         raise ValueError("k_pages head count differs from num_kv_heads")
@@ -224,6 +228,49 @@ def combine(task_map: TaskMap, partial_o, partial_lse, num_q_heads: int, out=Non
                           _stream(stream))
     _check(rc, "dsa_combine")
     return out
+
+
+def decode_multi(q_len: int, q, k_pages, v_pages, block_table, seq_lens, task_map: TaskMap, sm_scale: float,
+                 partial_o=None, partial_lse=None, q_scale=None, k_scale=None, v_scale=None, stream=None):
+    """dsa_decode_multi: q [B, q_len, Hq, 128]; partials hold q_len * G rows per descriptor."""
+    R = q_len * (q.shape[-2] // task_map.num_kv_heads)
+    if partial_o is None:
+        partial_o, partial_lse = partial_buffers(task_map.max_descs, R, q.device)
+    args = _attn_args(q, k_pages, v_pages, block_table, seq_lens, task_map.num_kv_heads, sm_scale,
+                      q_scale, k_scale, v_scale)
+    rc = _lib.dsa_decode_multi(q_len, *args, ctypes.byref(task_map.struct), _ptr(partial_o), _ptr(partial_lse),
+                               _stream(stream))
+    _check(rc, "dsa_decode_multi")
+    return partial_o, partial_lse
+
+
+def combine_multi(q_len: int, task_map: TaskMap, partial_o, partial_lse, num_q_heads: int, out=None, out_lse=None,
+                  out_dtype=torch.bfloat16, stream=None):
+    """dsa_combine_multi: out [B, q_len, Hq, 128] (and out_lse [B, q_len, Hq])."""
+    batch = task_map.batch
+    if out is None:
+        out = torch.empty(batch, q_len, num_q_heads, HEAD_DIM, dtype=out_dtype, device=partial_o.device)
+    rc = _lib.dsa_combine_multi(q_len, ctypes.byref(task_map.struct), _ptr(partial_o), _ptr(partial_lse), batch,
+                                num_q_heads, task_map.num_kv_heads, HEAD_DIM, _ptr(out), _dtype_code(out),
+                                _ptr(out_lse), _stream(stream))
+    _check(rc, "dsa_combine_multi")
+    return out
+
+
+def attention_multi(inp: dict, num_ctas: int, min_tiles_per_split: int = 4, out_dtype=torch.bfloat16,
+                    task_map: TaskMap | None = None, stream=None):
+    """One multi-token verify step (inp["q"] [B, q_len, Hq, 128]): plan, decode_multi,
+    combine_multi.  Returns (out, out_lse, task_map, partial_o, partial_lse)."""
+    q_len = int(inp["q_len"])
+    tm = plan(inp["seq_lens"], inp["num_kv_heads"], num_ctas, min_tiles_per_split, task_map=task_map,
+              stream=stream)
+    po, pl = decode_multi(q_len, inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
+                          inp["sm_scale"], q_scale=inp.get("q_scale"), k_scale=inp.get("k_scale"),
+                          v_scale=inp.get("v_scale"), stream=stream)
+    B = inp["seq_lens"].shape[0]
+    out_lse = torch.empty(B, q_len, inp["num_q_heads"], dtype=torch.float32, device=po.device)
+    out = combine_multi(q_len, tm, po, pl, inp["num_q_heads"], out_lse=out_lse, out_dtype=out_dtype, stream=stream)
+    return out, out_lse, tm, po, pl
 
 
 def static_num_splits(mode: int, param: int, max_seq_len: int) -> int:

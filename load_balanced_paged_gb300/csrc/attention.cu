@@ -50,6 +50,7 @@ struct KernelParams {
     const int32_t *block_table;
     const int32_t *seq_lens;
     int32_t max_pages, num_pages, hq, hkv, G, num_units, max_slots;
+    int32_t q_len;      // query tokens per request (1: plain decode; > 1: multi-token verify)
     float score_scale;  // sm_scale * log2(e)
     // persistent schedule
     const int32_t *cta_desc_begin;
@@ -87,36 +88,45 @@ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
 constexpr int kQSlots = 2;   // descriptors handed ahead to the consumers (Q + info)
 constexpr int kEpiRing = 8;  // merged descriptors the epilogue warp may lag behind (fused combine)
+constexpr int kMaxRows = 64; // query rows (query tokens x G) of one unit in a multi-token step
+constexpr int kDescInfoBytes = 80;
 
-template <int KV, int STAGES, int GROUPS, int MSLOTS = 2>
+// QW = 0: one query token per request; the consumer groups take alternate tiles and all
+// warps of the CTA merge at each descriptor end.  QW = 1 or 2: multi-token queries; every
+// consumer warp takes every tile: its token half (32 tokens) for its column set of QW
+// 8-column blocks (query rows), and the two halves of a column set merge pairwise.
+template <int KV, int STAGES, int GROUPS, int MSLOTS = 2, int QW = 0>
 struct Layout {
     static constexpr int kNcw = GROUPS * 4;  // consumer warps
     static constexpr int kThreads = (kNcw + 1) * 32;       // consumers + producer
     static constexpr int kThreadsFused = (kNcw + 2) * 32;  // + epilogue warp (fused combine)
     static constexpr int kStageTx = 2 * Cfg<KV>::kTileBytes + 2 * Cfg<KV>::kScaleBytes;
     static constexpr int kStageBytes = round_up(kStageTx, 1024);
-    static constexpr int kQSlot = kMaxGroup * Cfg<KV>::kQHeadBytes;
+    static constexpr int kQRows = QW ? kMaxRows : kMaxGroup;
+    static constexpr int kQSlot = kQRows * Cfg<KV>::kQHeadBytes;
     static constexpr int kQOff = STAGES * kStageBytes;
     static constexpr int kOStride = 132;  // floats per head row of a warp's O (padding avoids bank conflicts)
     static constexpr int kWarpFloats = kMaxGroup * kOStride + 2 * kMaxGroup;
+    static constexpr int kPairFloats = 8 * QW * kOStride + 2 * 8 * QW;  // one column set's second half
     static constexpr int kMergeOff = kQOff + kQSlots * kQSlot;
-    static constexpr int kMergeSlot = kNcw * kWarpFloats;  // floats per merge slot
-    static constexpr int kMergeSlots = MSLOTS;             // 2: lagged merge; 1: merge at once
+    static constexpr int kMergeSlot = QW ? 4 * kPairFloats : kNcw * kWarpFloats;  // floats per merge slot
+    static constexpr int kMergeBars = QW ? 4 : 2;          // merge_full / merge_done barriers each
     static constexpr int kBarOff = kMergeOff + MSLOTS * kMergeSlot * 4;
-    // full, empty, qfull, qempty, merge_full x2, merge_done x2, epi_ready, epi_free
-    static constexpr int kNumBars = 2 * STAGES + 2 * kQSlots + 4 + 2 * kEpiRing;
+    // full, empty, qfull, qempty, merge_full, merge_done, epi_ready, epi_free
+    static constexpr int kNumBars = 2 * STAGES + 2 * kQSlots + 2 * kMergeBars + 2 * kEpiRing;
     static constexpr int kNValidOff = kBarOff + kNumBars * 8;
     static constexpr int kAbortOff = kNValidOff + STAGES * 4;
     static constexpr int kInfoOff = round_up(kAbortOff + 16, 64);  // one DescInfo per Q slot
-    static constexpr int kEpiOff = kInfoOff + kQSlots * 64;  // kEpiRing EpiRecords + descriptor total
+    static constexpr int kEpiOff = kInfoOff + kQSlots * kDescInfoBytes;  // kEpiRing EpiRecords + descriptor total
     static constexpr int kBytes = kEpiOff + kEpiRing * 16 + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static_assert(MSLOTS == 1 || MSLOTS == 2, "merge slots");
+    static_assert(QW == 0 || (MSLOTS == 1 && GROUPS == 2), "multi-token queries: 8 consumer warps, one merge slot");
     // Each stage must be consumed by one group only: a group then meets the phases of its
     // stages' full barriers in order.  With stages shared by two groups, one group could wait
     // for phase k+1 while phase k is still pending, pass the parity test early and arrive on
     // the stage's empty barrier out of turn (an undefined mbarrier use that faults the GPU).
-    static_assert(STAGES % GROUPS == 0, "each stage must belong to one consumer group");
+    static_assert(QW > 0 || STAGES % GROUPS == 0, "each stage must belong to one consumer group");
     static_assert(kStageBytes % 1024 == 0 && kQOff % 1024 == 0, "swizzled TMA boxes need 1024-byte alignment");
     static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
@@ -135,9 +145,12 @@ struct DescInfo {
     int c_start;  // ring position of the descriptor's first tile
     int np;       // partials of the descriptor's unit (fused combine)
     int pbeg;     // first partial slot of the unit (fused combine)
+    int t0;       // first tile of the descriptor within its unit
+    int len;      // the request's KV length
+    int pad[2];
     float qscale[kMaxGroup];  // E4M3: q_scale of the G query heads
 };
-static_assert(sizeof(DescInfo) == 64, "DescInfo slot size");
+static_assert(sizeof(DescInfo) == kDescInfoBytes, "DescInfo slot size");
 
 // What the consumers hand the epilogue warp with each merged descriptor (fused combine).
 struct EpiRecord {
@@ -288,12 +301,12 @@ __device__ __noinline__ void combine_unit(const KernelParams &p, int lane, int u
 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
-template <int KV, int STAGES, int GROUPS, bool PERSIST, bool FUSE, int MSLOTS>
-__global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS>::kThreadsFused
-                                       : Layout<KV, STAGES, GROUPS, MSLOTS>::kThreads, 1)
+template <int KV, int STAGES, int GROUPS, bool PERSIST, bool FUSE, int MSLOTS, int QW>
+__global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>::kThreadsFused
+                                       : Layout<KV, STAGES, GROUPS, MSLOTS, QW>::kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const KernelParams p) {
-    using L = Layout<KV, STAGES, GROUPS, MSLOTS>;
+    using L = Layout<KV, STAGES, GROUPS, MSLOTS, QW>;
     using C = Cfg<KV>;
     constexpr int NCW = L::kNcw;
     extern __shared__ uint8_t smem_raw[];
@@ -304,10 +317,11 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS>::kTh
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto qfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
     auto qempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + kQSlots + s); };
+    constexpr int MB = L::kMergeBars;
     auto merge_full = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + s); };
-    auto merge_done = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 2 + s); };
-    auto epi_ready = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 4 + s); };
-    auto epi_free = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 4 + kEpiRing + s); };
+    auto merge_done = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + MB + s); };
+    auto epi_ready = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 2 * MB + s); };
+    auto epi_free = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 2 * MB + kEpiRing + s); };
     EpiRecord *epi_rec = reinterpret_cast<EpiRecord *>(smem + L::kEpiOff);
     volatile int *epi_total = reinterpret_cast<volatile int *>(smem + L::kEpiOff + kEpiRing * sizeof(EpiRecord));
     int *nvalid = reinterpret_cast<int *>(smem + L::kNValidOff);
@@ -319,15 +333,22 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS>::kTh
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 4);
+            mbar_init(empty_bar(s), QW ? NCW : 4);  // QW: every consumer warp reads every stage
         }
         for (int s = 0; s < kQSlots; ++s) {
             mbar_init(qfull_bar(s), 1);
             mbar_init(qempty_bar(s), NCW);
         }
-        for (int s = 0; s < MSLOTS; ++s) {
-            mbar_init(merge_full(s), NCW);
-            mbar_init(merge_done(s), NCW);
+        if (QW) {
+            for (int s = 0; s < MB; ++s) {  // per column set: second half deposited / read
+                mbar_init(merge_full(s), 1);
+                mbar_init(merge_done(s), 1);
+            }
+        } else {
+            for (int s = 0; s < MSLOTS; ++s) {
+                mbar_init(merge_full(s), NCW);
+                mbar_init(merge_done(s), NCW);
+            }
         }
         for (int s = 0; s < kEpiRing; ++s) {
             mbar_init(epi_ready(s), NCW);
@@ -424,9 +445,10 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS>::kTh
                             if (g < G) wqs[g] = qs[g];
                     }
                     if (wn == 0) {  // no tiles: its partial is empty, the consumers never see it
-                        for (int i = 0; i < G * kHeadDim; ++i)
-                            p.partial_o[static_cast<int64_t>(wslot) * G * kHeadDim + i] = 0.f;
-                        for (int g = 0; g < G; ++g) p.partial_lse[static_cast<int64_t>(wslot) * G + g] = -INFINITY;
+                        const int R = p.q_len * G;
+                        for (int i = 0; i < R * kHeadDim; ++i)
+                            p.partial_o[static_cast<int64_t>(wslot) * R * kHeadDim + i] = 0.f;
+                        for (int g = 0; g < R; ++g) p.partial_lse[static_cast<int64_t>(wslot) * R + g] = -INFINITY;
                     }
                 } else {
                     atomicOr(p.status, DSA_DEV_BAD_MAP);
@@ -495,6 +517,8 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS>::kTh
                         const int slot = __shfl_sync(0xffffffffu, wslot, j);
                         const int np = __shfl_sync(0xffffffffu, wnp, j);
                         const int pbeg = __shfl_sync(0xffffffffu, wpbeg, j);
+                        const int dt0 = __shfl_sync(0xffffffffu, wt0, j);
+                        const int dlen = __shfl_sync(0xffffffffu, wlen, j);
                         if (lane == 0) {
                             const int qs_ = qi % kQSlots;
                             if (!wait_phase(qempty_bar(qs_), ((qi / kQSlots) & 1) ^ 1, abort_flag, p.status)) {
@@ -509,12 +533,20 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS>::kTh
                                 inf->c_start = c;
                                 inf->np = np;
                                 inf->pbeg = pbeg;
+                                inf->t0 = dt0;
+                                inf->len = dlen;
 #pragma unroll
                                 for (int g = 0; g < kMaxGroup; ++g) inf->qscale[g] = qs[g];
+                                // the G query rows of each of the request's q_len query tokens,
+                                // one after the other (row i*G + g)
                                 const uint32_t bytes = G * C::kQHeadBytes;
-                                mbar_arrive_expect_tx(qfull_bar(qs_), bytes);
-                                const uint8_t *src = p.q + (static_cast<int64_t>(b) * p.hq + h * G) * C::kQHeadBytes;
-                                bulk_load(sbase + L::kQOff + qs_ * L::kQSlot, src, bytes, qfull_bar(qs_));
+                                mbar_arrive_expect_tx(qfull_bar(qs_), bytes * p.q_len);
+                                for (int i = 0; i < p.q_len; ++i) {
+                                    const uint8_t *src =
+                                        p.q + ((static_cast<int64_t>(b) * p.q_len + i) * p.hq + h * G) * C::kQHeadBytes;
+                                    bulk_load(sbase + L::kQOff + qs_ * L::kQSlot + i * bytes, src, bytes,
+                                              qfull_bar(qs_));
+                                }
                                 q_issued = qi;
                             }
                         }
@@ -634,6 +666,273 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS>::kTh
         }
     }
 
+    if constexpr (QW > 0) {
+        // ===================== consumer warps, multi-token queries =====================
+        // Query rows r = i * G + g (query token i, head g); row r of a request of length len
+        // sees the tokens t < len - q_len + i + 1 (causal within the draft).  Warp w takes
+        // tokens [32 (w & 1), +32) of every tile for rows [8 QW (w >> 1), +8 QW): S^T blocks
+        // of 16 tokens x 8 rows, one online softmax per row over its half of the tokens; at
+        // each descriptor end the second half deposits (m, l, O) in shared memory and the
+        // first half merges it into its registers and writes the partial.
+        constexpr int NBW = QW;
+        const int ts = warp & 1, cs = warp >> 1;
+        const int tok_base = 32 * ts;
+        const int cb = 8 * NBW * cs;
+        const int R = p.q_len * G;
+        const bool active = cb < R;
+        const int gid = lane >> 2, tig = lane & 3;
+        const int xr = lane & 7;
+        const int k_row = tok_base + xr + ((lane >> 3) & 1) * 8;
+        const int k_chunk = lane >> 4;
+        const int v_row = tok_base + xr + (lane >> 4) * 8;
+        const int v_chunk = (lane >> 3) & 1;
+        float *pair = reinterpret_cast<float *>(smem + L::kMergeOff) + cs * L::kPairFloats;
+
+        for (int qi = 0;; ++qi) {
+            const int qslot = qi % kQSlots;
+            if (!wait_phase(qfull_bar(qslot), (qi / kQSlots) & 1, abort_flag, p.status)) return;
+            const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
+            if (inf->end) break;
+            const int n = inf->n, slot = inf->slot, c_start = inf->c_start, dt0 = inf->t0, len = inf->len;
+
+            // Q fragments (B operand): row cb + 8 nb + gid, zero past R
+            uint32_t qf[NBW][8][2];
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb) {
+                const int r = cb + 8 * nb + gid;
+                const uint8_t *qs = smem + L::kQOff + qslot * L::kQSlot + r * C::kQHeadBytes;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    qf[nb][ks][0] = r < R ? *reinterpret_cast<const uint32_t *>(qs + 32 * ks + 4 * tig) : 0u;
+                    qf[nb][ks][1] = r < R ? *reinterpret_cast<const uint32_t *>(qs + 32 * ks + 4 * tig + 16) : 0u;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qempty_bar(qslot));
+
+            // causal limit of this lane's two rows per block (rows past R are never stored)
+            int lim[NBW][2];
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = cb + 8 * nb + 2 * tig + e;
+                    lim[nb][e] = len - p.q_len + (r < R ? r / G : 0) + 1;
+                }
+            const int lim_min = len - p.q_len + 1;  // every row sees the tokens below this
+
+            float m[NBW][2], l[NBW][2], o[NBW][8][4];
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb) {
+                m[nb][0] = m[nb][1] = -INFINITY;
+                l[nb][0] = l[nb][1] = 0.f;
+#pragma unroll
+                for (int mb = 0; mb < 8; ++mb) o[nb][mb][0] = o[nb][mb][1] = o[nb][mb][2] = o[nb][mb][3] = 0.f;
+            }
+
+            bool aborted = false;
+            for (int li = 0; li < n; ++li) {
+                const int c = c_start + li;
+                const int stage = c % STAGES;
+                if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status)) {
+                    aborted = true;
+                    break;
+                }
+                const int nv = nvalid[stage];
+                if (active && nv > tok_base) {
+                    const uint32_t kbase = sbase + stage * L::kStageBytes;
+                    const uint32_t vbase = kbase + C::kTileBytes;
+                    const int T0 = (dt0 + li) * kTile + tok_base;  // token of this warp's first row
+                    // ---- S^T = K . Q^T for 2 blocks of 16 tokens x NBW blocks of 8 rows
+                    float sc[2][NBW][4];
+#pragma unroll
+                    for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+                        for (int nb = 0; nb < NBW; ++nb) sc[kt][nb][0] = sc[kt][nb][1] = sc[kt][nb][2] = sc[kt][nb][3] = 0.f;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const int ch = 2 * ks + k_chunk;
+#pragma unroll
+                        for (int kt = 0; kt < 2; ++kt) {
+                            const uint32_t addr =
+                                kbase + (ch >> 3) * (C::kTileBytes / 2) + (k_row + 16 * kt) * 128 + (((ch & 7) ^ xr) << 4);
+                            uint32_t a0, a1, a2, a3;
+                            ldsm_x4(addr, a0, a1, a2, a3);
+#pragma unroll
+                            for (int nb = 0; nb < NBW; ++nb) mma_bf16(sc[kt][nb], a0, a1, a2, a3, qf[nb][ks][0], qf[nb][ks][1]);
+                        }
+                    }
+                    const bool mask = T0 + 32 > lim_min;  // some row of the warp's tokens is past a limit
+#pragma unroll
+                    for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+                        for (int nb = 0; nb < NBW; ++nb) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) sc[kt][nb][e] *= p.score_scale;
+                            if (mask) {
+                                const int ta = T0 + 16 * kt + gid, tb = ta + 8;
+                                if (ta >= lim[nb][0]) sc[kt][nb][0] = -INFINITY;
+                                if (ta >= lim[nb][1]) sc[kt][nb][1] = -INFINITY;
+                                if (tb >= lim[nb][0]) sc[kt][nb][2] = -INFINITY;
+                                if (tb >= lim[nb][1]) sc[kt][nb][3] = -INFINITY;
+                            }
+                        }
+                    // ---- online softmax (base 2) per row over the warp's 32 tokens
+                    uint32_t bh[2][NBW][2], bl[2][NBW][2];
+#pragma unroll
+                    for (int nb = 0; nb < NBW; ++nb) {
+                        float mx0 = fmaxf(fmaxf(sc[0][nb][0], sc[0][nb][2]), fmaxf(sc[1][nb][0], sc[1][nb][2]));
+                        float mx1 = fmaxf(fmaxf(sc[0][nb][1], sc[0][nb][3]), fmaxf(sc[1][nb][1], sc[1][nb][3]));
+#pragma unroll
+                        for (int o_ = 4; o_ < 32; o_ <<= 1) {
+                            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
+                            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
+                        }
+                        const float mn0 = fmaxf(m[nb][0], mx0), mn1 = fmaxf(m[nb][1], mx1);
+                        const float r0 = mn0 == -INFINITY ? 0.f : mn0, r1 = mn1 == -INFINITY ? 0.f : mn1;
+                        const float al0 = ex2(m[nb][0] - r0), al1 = ex2(m[nb][1] - r1);
+                        float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+                        for (int kt = 0; kt < 2; ++kt) {
+                            const float p0 = ex2(sc[kt][nb][0] - r0), p1 = ex2(sc[kt][nb][1] - r1);
+                            const float p2 = ex2(sc[kt][nb][2] - r0), p3 = ex2(sc[kt][nb][3] - r1);
+                            ls0 += p0 + p2;
+                            ls1 += p1 + p3;
+                            const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+                            const uint32_t l01 = pack_bf16x2(p0 - bf16lo_to_f32(h01), p1 - bf16hi_to_f32(h01));
+                            const uint32_t l23 = pack_bf16x2(p2 - bf16lo_to_f32(h23), p3 - bf16hi_to_f32(h23));
+                            bh[kt][nb][0] = movmatrix_trans(h01);
+                            bh[kt][nb][1] = movmatrix_trans(h23);
+                            bl[kt][nb][0] = movmatrix_trans(l01);
+                            bl[kt][nb][1] = movmatrix_trans(l23);
+                        }
+                        l[nb][0] = l[nb][0] * al0 + ls0;
+                        l[nb][1] = l[nb][1] * al1 + ls1;
+                        m[nb][0] = mn0;
+                        m[nb][1] = mn1;
+#pragma unroll
+                        for (int mb = 0; mb < 8; ++mb) {
+                            o[nb][mb][0] *= al0;
+                            o[nb][mb][1] *= al1;
+                            o[nb][mb][2] *= al0;
+                            o[nb][mb][3] *= al1;
+                        }
+                    }
+                    // ---- O^T += V^T . P^T; V rows past the request's length are zeroed
+                    const bool partial = nv < tok_base + 32;
+#pragma unroll
+                    for (int mb = 0; mb < 8; ++mb) {
+                        const int ch = 2 * mb + v_chunk;
+#pragma unroll
+                        for (int kt = 0; kt < 2; ++kt) {
+                            const uint32_t addr =
+                                vbase + (ch >> 3) * (C::kTileBytes / 2) + (v_row + 16 * kt) * 128 + (((ch & 7) ^ xr) << 4);
+                            uint32_t a0, a1, a2, a3;
+                            ldsm_x4_trans(addr, a0, a1, a2, a3);
+                            if (partial) {
+                                const uint32_t mlo = tok_mask(tok_base + 16 * kt + 2 * tig, nv);
+                                const uint32_t mhi = tok_mask(tok_base + 16 * kt + 8 + 2 * tig, nv);
+                                a0 &= mlo;
+                                a1 &= mlo;
+                                a2 &= mhi;
+                                a3 &= mhi;
+                            }
+#pragma unroll
+                            for (int nb = 0; nb < NBW; ++nb) {
+                                mma_bf16(o[nb][mb], a0, a1, a2, a3, bh[kt][nb][0], bh[kt][nb][1]);
+                                mma_bf16(o[nb][mb], a0, a1, a2, a3, bl[kt][nb][0], bl[kt][nb][1]);
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(stage));
+            }
+            if (aborted) return;
+            if (!active) continue;
+
+            // ---- pairwise merge of the two token halves of this column set
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb)
+#pragma unroll
+                for (int o_ = 4; o_ < 32; o_ <<= 1) {
+                    l[nb][0] += __shfl_xor_sync(0xffffffffu, l[nb][0], o_);
+                    l[nb][1] += __shfl_xor_sync(0xffffffffu, l[nb][1], o_);
+                }
+            float *ml = pair + 8 * NBW * L::kOStride;  // m then l of the 8 NBW rows
+            if (ts == 1) {
+                if (!wait_phase(merge_done(cs), (qi & 1) ^ 1, abort_flag, p.status)) return;
+#pragma unroll
+                for (int nb = 0; nb < NBW; ++nb) {
+                    if (gid == 0) {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            ml[8 * nb + 2 * tig + e] = m[nb][e];
+                            ml[8 * NBW + 8 * nb + 2 * tig + e] = l[nb][e];
+                        }
+                    }
+#pragma unroll
+                    for (int mb = 0; mb < 8; ++mb) {
+                        float *w0 = pair + (8 * nb + 2 * tig) * L::kOStride + 16 * mb + gid;
+                        w0[0] = o[nb][mb][0];
+                        w0[L::kOStride] = o[nb][mb][1];
+                        w0[8] = o[nb][mb][2];
+                        w0[L::kOStride + 8] = o[nb][mb][3];
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(merge_full(cs));
+                continue;
+            }
+            if (!wait_phase(merge_full(cs), qi & 1, abort_flag, p.status)) return;
+            float wa[NBW][2], wb[NBW][2], lse[NBW][2];
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float mp = ml[8 * nb + 2 * tig + e], lp = ml[8 * NBW + 8 * nb + 2 * tig + e];
+                    const float M = fmaxf(m[nb][e], mp);
+                    if (M == -INFINITY) {
+                        wa[nb][e] = wb[nb][e] = 0.f;
+                        lse[nb][e] = -INFINITY;
+                    } else {
+                        const float ea = ex2(m[nb][e] - M), eb = ex2(mp - M);
+                        const float Ls = l[nb][e] * ea + lp * eb;
+                        wa[nb][e] = ea / Ls;
+                        wb[nb][e] = eb / Ls;
+                        lse[nb][e] = (M + lg2(Ls)) * kLn2;
+                    }
+                }
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb)
+#pragma unroll
+                for (int mb = 0; mb < 8; ++mb) {
+                    const float *w0 = pair + (8 * nb + 2 * tig) * L::kOStride + 16 * mb + gid;
+                    o[nb][mb][0] = o[nb][mb][0] * wa[nb][0] + w0[0] * wb[nb][0];
+                    o[nb][mb][1] = o[nb][mb][1] * wa[nb][1] + w0[L::kOStride] * wb[nb][1];
+                    o[nb][mb][2] = o[nb][mb][2] * wa[nb][0] + w0[8] * wb[nb][0];
+                    o[nb][mb][3] = o[nb][mb][3] * wa[nb][1] + w0[L::kOStride + 8] * wb[nb][1];
+                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(merge_done(cs));
+            // ---- the partial of rows [cb, cb + 8 NBW) (those below R)
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = cb + 8 * nb + 2 * tig + e;
+                    if (r >= R) continue;
+                    float *dst = p.partial_o + (static_cast<int64_t>(slot) * R + r) * kHeadDim + gid;
+#pragma unroll
+                    for (int mb = 0; mb < 8; ++mb) {
+                        dst[16 * mb] = o[nb][mb][e];
+                        dst[16 * mb + 8] = o[nb][mb][2 + e];
+                    }
+                    if (gid == 0) p.partial_lse[static_cast<int64_t>(slot) * R + r] = lse[nb][e];
+                }
+        }
+        return;
+    } else {
     // =========================== consumer warps ===========================
     const int grp = warp / 4, wig = warp & 3;
     const int gid = lane >> 2, tig = lane & 3;
@@ -937,6 +1236,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS>::kTh
         pend_pbeg = d_pbeg;
     }
     if (pend_d >= 0) merge_and_write(pend_d, pend_slot, pend_b, pend_h, pend_np, pend_pbeg);
+    }  // QW == 0
 }
 
 // Self-test of the bounded wait: warp 0 waits on an mbarrier that nothing ever arrives at;
@@ -998,14 +1298,14 @@ bool make_pool_map(CUtensorMap *m, const void *pool, int kv, int num_pages, int 
     return r == CUDA_SUCCESS;
 }
 
-template <int KV, int STAGES, int GROUPS, bool PERSIST, bool FUSE = false, int MSLOTS = 2>
+template <int KV, int STAGES, int GROUPS, bool PERSIST, bool FUSE = false, int MSLOTS = 2, int QW = 0>
 dsa_status launch(const AttnArgs &a, const KernelParams &kp, dim3 grid, cudaStream_t st) {
-    using L = Layout<KV, STAGES, GROUPS, MSLOTS>;
+    using L = Layout<KV, STAGES, GROUPS, MSLOTS, QW>;
     CUtensorMap km, vm;
     if (!make_pool_map(&km, a.k_pages, KV, a.num_pages, a.num_kv_heads) ||
         !make_pool_map(&vm, a.v_pages, KV, a.num_pages, a.num_kv_heads))
         return DSA_ERR_CUDA;
-    auto kern = attn_kernel<KV, STAGES, GROUPS, PERSIST, FUSE, MSLOTS>;
+    auto kern = attn_kernel<KV, STAGES, GROUPS, PERSIST, FUSE, MSLOTS, QW>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
         return DSA_ERR_CUDA;
     return launch_pdl(kern, grid, dim3(FUSE ? L::kThreadsFused : L::kThreads), L::kAlloc, st, km, vm, kp);
@@ -1025,6 +1325,7 @@ KernelParams base_params(const AttnArgs &a, float *partial_o, float *partial_lse
     kp.hkv = a.num_kv_heads;
     kp.G = a.num_q_heads / a.num_kv_heads;
     kp.num_units = a.batch * a.num_kv_heads;
+    kp.q_len = 1;
     kp.score_scale = a.sm_scale * kLog2e;
     kp.partial_o = partial_o;
     kp.partial_lse = partial_lse;
@@ -1079,6 +1380,41 @@ extern "C" dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *
     kp.descs = reinterpret_cast<const int4 *>(map->descs);
     if (kv_dtype == DSA_BF16) return launch_persistent<0, false>(a, kp, map->num_ctas, to_cuda(stream));
     return launch_persistent<1, false>(a, kp, map->num_ctas, to_cuda(stream));
+}
+
+extern "C" dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q_dtype, const float *q_scale,
+                                       const void *k_pages, const void *v_pages, dsa_dtype kv_dtype,
+                                       const float *k_scale, const float *v_scale, const int32_t *block_table,
+                                       int32_t max_pages_per_req, int32_t num_pages, const int32_t *seq_lens,
+                                       int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                       int32_t page_size, float sm_scale, const dsa_task_map *map, float *partial_o,
+                                       float *partial_lse, dsa_stream stream) {
+    if (q_len == 1)
+        return dsa_decode(q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale, block_table,
+                          max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                          page_size, sm_scale, map, partial_o, partial_lse, stream);
+    const AttnArgs a{q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale, block_table,
+                     max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                     page_size, sm_scale};
+    dsa_status s = validate_attn(a);
+    if (s != DSA_OK) return s;
+    if (q_len < 1) return DSA_ERR_INVALID_ARG;
+    const int R = q_len * (num_q_heads / num_kv_heads);
+    if (R > kMaxRows || kv_dtype != DSA_BF16) return DSA_ERR_UNSUPPORTED;
+    if (!map || !map->cta_desc_begin || !map->descs || !map->meta || !partial_o || !partial_lse)
+        return DSA_ERR_INVALID_ARG;
+    if (map->num_units != batch * num_kv_heads || map->num_ctas < 1) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(partial_o) || !aligned16(map->descs)) return DSA_ERR_INVALID_ARG;
+    if (batch == 0) return DSA_OK;
+    KernelParams kp = base_params(a, partial_o, partial_lse, map->meta + 3);
+    kp.q_len = q_len;
+    kp.max_slots = map->max_descs;
+    kp.cta_desc_begin = map->cta_desc_begin;
+    kp.descs = reinterpret_cast<const int4 *>(map->descs);
+    const dim3 grid(map->num_ctas);
+    if (R <= 32)
+        return launch<0, kPersistStagesBf16, kPersistGroups, true, false, 1, 1>(a, kp, grid, to_cuda(stream));
+    return launch<0, kPersistStagesBf16, kPersistGroups, true, false, 1, 2>(a, kp, grid, to_cuda(stream));
 }
 
 extern "C" dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_scale, const void *k_pages,

@@ -3,8 +3,9 @@
 // 调度": the combine kernel reads the actual number of partials per request and
 // head; Hy3 preview write-up 2.1.1 "Combine Kernel"):
 //   L = ln sum_k exp(lse_k),   out = sum_k exp(lse_k - L) * o_k.
-// One CTA per unit, one warp per query head of the unit, each lane owning 4 of the
-// 128 output dims (float4 loads of the fp32 partials, coalesced per head row).
+// One CTA per unit and block of 8 query rows, one warp per query row of the unit (query
+// token i, head g: row i*G + g; one query token in a plain decode step), each lane owning
+// 4 of the 128 output dims (float4 loads of the fp32 partials, coalesced per row).
 #include <cuda_bf16.h>
 
 #include "common.h"
@@ -38,18 +39,19 @@ template <bool STATIC, typename OutT>
 __global__ void __launch_bounds__(kMaxGroup * 32)
     combine_kernel(const int32_t *__restrict__ unit_begin, const int32_t *__restrict__ unit_count, int32_t S,
                    const float *__restrict__ partial_o, const float *__restrict__ partial_lse, int32_t hq,
-                   int32_t hkv, int32_t G, OutT *__restrict__ out, float *__restrict__ out_lse) {
+                   int32_t hkv, int32_t G, int32_t q_len, OutT *__restrict__ out, float *__restrict__ out_lse) {
     const int u = blockIdx.x;
-    const int head = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.y * kMaxGroup + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     grid_launch_dependents();
     grid_dependency_wait();  // partials from the decode kernel
-    if (head >= G) return;
+    const int R = q_len * G;  // partial rows per slot
+    if (row >= R) return;
     const int b = u / hkv, h = u - b * hkv;
     const int64_t beg = STATIC ? static_cast<int64_t>(u) * S : unit_begin[u];
     const int n = STATIC ? S : unit_count[u];
 
     float M = -INFINITY;
-    for (int k = lane; k < n; k += 32) M = fmaxf(M, partial_lse[(beg + k) * G + head]);
+    for (int k = lane; k < n; k += 32) M = fmaxf(M, partial_lse[(beg + k) * R + row]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
@@ -57,7 +59,7 @@ __global__ void __launch_bounds__(kMaxGroup * 32)
     float L = -INFINITY;
     if (M != -INFINITY) {
         float sum = 0.f;
-        for (int k = lane; k < n; k += 32) sum += exp2f((partial_lse[(beg + k) * G + head] - M) * kLog2e);
+        for (int k = lane; k < n; k += 32) sum += exp2f((partial_lse[(beg + k) * R + row] - M) * kLog2e);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         L = M + logf(sum);
@@ -65,11 +67,11 @@ __global__ void __launch_bounds__(kMaxGroup * 32)
         // batch are loaded back to back
         for (int k0 = 0; k0 < n; k0 += 32) {
             const int kn = min(32, n - k0);
-            const float w = lane < kn ? exp2f((partial_lse[(beg + k0 + lane) * G + head] - L) * kLog2e) : 0.f;
+            const float w = lane < kn ? exp2f((partial_lse[(beg + k0 + lane) * R + row] - L) * kLog2e) : 0.f;
 #pragma unroll 8
             for (int j = 0; j < kn; ++j) {
                 const float4 v =
-                    *reinterpret_cast<const float4 *>(partial_o + ((beg + k0 + j) * G + head) * kHeadDim + lane * 4);
+                    *reinterpret_cast<const float4 *>(partial_o + ((beg + k0 + j) * R + row) * kHeadDim + lane * 4);
                 const float wj = __shfl_sync(0xffffffffu, w, j);
                 acc.x += wj * v.x;
                 acc.y += wj * v.y;
@@ -78,7 +80,8 @@ __global__ void __launch_bounds__(kMaxGroup * 32)
             }
         }
     }
-    const int64_t orow = static_cast<int64_t>(b) * hq + h * G + head;
+    const int qi = row / G, g = row - qi * G;
+    const int64_t orow = (static_cast<int64_t>(b) * q_len + qi) * hq + h * G + g;
     store4<OutT>(out + orow * kHeadDim + lane * 4, acc);
     if (out_lse && lane == 0) out_lse[orow] = L;
 }
@@ -97,15 +100,16 @@ dsa_status validate_combine(int32_t batch, int32_t hq, int32_t hkv, int32_t head
 template <bool STATIC>
 dsa_status launch_combine(const int32_t *ub, const int32_t *uc, int32_t S, const float *po, const float *plse,
                           int32_t batch, int32_t hq, int32_t hkv, void *out, dsa_dtype out_dtype, float *out_lse,
-                          cudaStream_t st) {
+                          cudaStream_t st, int32_t q_len = 1) {
     const int units = batch * hkv;
     if (units == 0) return DSA_OK;
     const int G = hq / hkv;
+    const dim3 grid(units, (q_len * G + kMaxGroup - 1) / kMaxGroup);
     if (out_dtype == DSA_BF16)
-        return launch_pdl(combine_kernel<STATIC, __nv_bfloat16>, dim3(units), dim3(kMaxGroup * 32), 0, st, ub, uc, S,
-                          po, plse, hq, hkv, G, static_cast<__nv_bfloat16 *>(out), out_lse);
-    return launch_pdl(combine_kernel<STATIC, float>, dim3(units), dim3(kMaxGroup * 32), 0, st, ub, uc, S, po, plse,
-                      hq, hkv, G, static_cast<float *>(out), out_lse);
+        return launch_pdl(combine_kernel<STATIC, __nv_bfloat16>, grid, dim3(kMaxGroup * 32), 0, st, ub, uc, S, po,
+                          plse, hq, hkv, G, q_len, static_cast<__nv_bfloat16 *>(out), out_lse);
+    return launch_pdl(combine_kernel<STATIC, float>, grid, dim3(kMaxGroup * 32), 0, st, ub, uc, S, po, plse, hq,
+                      hkv, G, q_len, static_cast<float *>(out), out_lse);
 }
 
 }  // namespace
@@ -122,6 +126,20 @@ extern "C" dsa_status dsa_combine(const dsa_task_map *map, const float *partial_
     if (batch > 0 && (!map->unit_partial_begin || !map->unit_num_partials)) return DSA_ERR_INVALID_ARG;
     return launch_combine<false>(map->unit_partial_begin, map->unit_num_partials, 0, partial_o, partial_lse, batch,
                                  num_q_heads, num_kv_heads, out, out_dtype, out_lse, to_cuda(stream));
+}
+
+extern "C" dsa_status dsa_combine_multi(int32_t q_len, const dsa_task_map *map, const float *partial_o,
+                                        const float *partial_lse, int32_t batch, int32_t num_q_heads,
+                                        int32_t num_kv_heads, int32_t head_dim, void *out, dsa_dtype out_dtype,
+                                        float *out_lse, dsa_stream stream) {
+    dsa_status s = validate_combine(batch, num_q_heads, num_kv_heads, head_dim, partial_o, partial_lse, out, out_dtype);
+    if (s != DSA_OK) return s;
+    if (q_len < 1) return DSA_ERR_INVALID_ARG;
+    if (q_len * (num_q_heads / num_kv_heads) > 64) return DSA_ERR_UNSUPPORTED;
+    if (!map || map->num_units != batch * num_kv_heads) return DSA_ERR_INVALID_ARG;
+    if (batch > 0 && (!map->unit_partial_begin || !map->unit_num_partials)) return DSA_ERR_INVALID_ARG;
+    return launch_combine<false>(map->unit_partial_begin, map->unit_num_partials, 0, partial_o, partial_lse, batch,
+                                 num_q_heads, num_kv_heads, out, out_dtype, out_lse, to_cuda(stream), q_len);
 }
 
 extern "C" dsa_status dsa_static_combine(int32_t num_splits, const float *partial_o, const float *partial_lse,

@@ -148,8 +148,9 @@ __device__ __forceinline__ void rope(const ProParams &p, int l, const float (&cs
     }
 }
 
-// y <- H_128 y / sqrt(128) (Sylvester order).  Dim bits 0-2 (e) and 5-6 (c) are in-lane
-// butterflies; bits 3-4 (l) pair lanes l and l xor 1, l xor 2 of the same row.
+// y <- H_128 y (Sylvester order; the 1/sqrt(128) is left to the caller).  Dim bits 0-2
+// (e) and 5-6 (c) are in-lane butterflies; bits 3-4 (l) pair lanes l and l xor 1, l xor 2
+// of the same row.
 __device__ __forceinline__ void hadamard(int l, float (&y)[4][8]) {
 #pragma unroll
     for (int c = 0; c < 4; ++c)
@@ -184,14 +185,13 @@ __device__ __forceinline__ void hadamard(int l, float (&y)[4][8]) {
                 y[c][e] = fmaf(sgn, y[c][e], o);
             }
     }
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[c][e] *= kInvSqrtHeadDim;
 }
 
-// RMSNorm with weight w over the row (both shuffles taken by every lane).
-__device__ __forceinline__ void rms_norm(const float *w, float eps, int l, float (&y)[4][8]) {
+// RMSNorm with weight w over the row, split into its per-element part y <- y * w and its
+// row-wide factor 1 / sqrt(mean(y^2) + eps), which is returned for the caller to apply
+// once, together with the other row-wide factor of the chain.  Both shuffles are taken by
+// every lane.
+__device__ __forceinline__ float rms_norm_weight(const float *w, float eps, int l, float (&y)[4][8]) {
     float ss = 0.f;
 #pragma unroll
     for (int c = 0; c < 4; ++c)
@@ -204,13 +204,17 @@ __device__ __forceinline__ void rms_norm(const float *w, float eps, int l, float
         const float4 w1 = __ldg(reinterpret_cast<const float4 *>(w + 32 * c + 8 * l + 4));
         const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[c][e] = y[c][e] * inv * wv[e];
+        for (int e = 0; e < 8; ++e) y[c][e] *= wv[e];
     }
+    return inv;
 }
 
-// Encode the row and store it (if `store`): E4M3 with scale = amax / 448 (1 for a zero
-// row), values y * (448 / amax); or bf16.  The amax shuffles are taken by every lane.
-__device__ __forceinline__ void encode_store(int l, const float (&y)[4][8], bool fp8, bool store, void *base,
+// Encode the row z * f and store it (if `store`); f > 0 is the row-wide factor the chain
+// left unapplied (RMSNorm's 1/rms and the Hadamard's 1/sqrt(128)).  E4M3: scale = amax /
+// 448 (1 for a zero row) with values z * (448 / amax(z)), which f does not change, and
+// the stored scale amax(z) * f / 448.  bf16: z * f rounded.  The amax shuffles are taken
+// by every lane.
+__device__ __forceinline__ void encode_store(int l, float (&y)[4][8], float f, bool fp8, bool store, void *base,
                                              int64_t row, float *scale_out) {
     if (fp8) {
         float m = 0.f;
@@ -229,17 +233,17 @@ __device__ __forceinline__ void encode_store(int l, const float (&y)[4][8], bool
             v.y = f32x2_to_e4m3x2(y[c][4] * inv, y[c][5] * inv) | (uint32_t(f32x2_to_e4m3x2(y[c][6] * inv, y[c][7] * inv)) << 16);
             *reinterpret_cast<uint2 *>(dst + 32 * c) = v;
         }
-        if (l == 0) scale_out[row] = amax > 0.f ? amax / kE4m3Max : 1.f;
+        if (l == 0) scale_out[row] = amax > 0.f ? amax * f / kE4m3Max : 1.f;
     } else {
         if (!store) return;
         uint16_t *dst = static_cast<uint16_t *>(base) + row * kHeadDim + 8 * l;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             uint4 v;
-            v.x = pack_bf16x2(y[c][0], y[c][1]);
-            v.y = pack_bf16x2(y[c][2], y[c][3]);
-            v.z = pack_bf16x2(y[c][4], y[c][5]);
-            v.w = pack_bf16x2(y[c][6], y[c][7]);
+            v.x = pack_bf16x2(y[c][0] * f, y[c][1] * f);
+            v.y = pack_bf16x2(y[c][2] * f, y[c][3] * f);
+            v.z = pack_bf16x2(y[c][4] * f, y[c][5] * f);
+            v.w = pack_bf16x2(y[c][6] * f, y[c][7] * f);
             *reinterpret_cast<uint4 *>(dst + 32 * c) = v;
         }
     }
@@ -283,21 +287,26 @@ __global__ void __launch_bounds__(kProWarps * 32, kProCtasPerSm) prologue_kernel
             float y[4][8];
             unpack_row(cur, y);
             if (j < p.hq + p.hkv) {  // Q or K head (uniform over the warp)
+                // RoPE and the Hadamard rotation are linear, so RMSNorm's row factor and the
+                // rotation's 1/sqrt(128) are applied once, at the encoding
                 const bool is_q = j < p.hq;
                 const float *w = is_q ? p.q_norm_w : p.k_norm_w;
-                if (w) rms_norm(w, p.eps, l, y);
+                float f = w ? rms_norm_weight(w, p.eps, l, y) : 1.f;
                 if (p.rope_mode != kRopeNone) rope(p, l, cs, sn, y);
-                if (p.hadamard) hadamard(l, y);
+                if (p.hadamard) {
+                    hadamard(l, y);
+                    f *= kInvSqrtHeadDim;
+                }
                 if (is_q) {
                     const int64_t row = static_cast<int64_t>(n) * p.hq + j;
-                    encode_store(l, y, p.q_fp8, valid && pos_ok, p.q_out, row, p.q_scale);
+                    encode_store(l, y, f, p.q_fp8, valid && pos_ok, p.q_out, row, p.q_scale);
                 } else {
                     const int64_t row = ((slot >> 6) * p.hkv + (j - p.hq)) * kTile + (slot & 63);
-                    encode_store(l, y, p.kv_fp8, valid && pos_ok && slot_ok, p.k_pages, row, p.k_scale);
+                    encode_store(l, y, f, p.kv_fp8, valid && pos_ok && slot_ok, p.k_pages, row, p.k_scale);
                 }
             } else {
                 const int64_t row = ((slot >> 6) * p.hkv + (j - p.hq - p.hkv)) * kTile + (slot & 63);
-                encode_store(l, y, p.kv_fp8, valid && slot_ok, p.v_pages, row, p.v_scale);
+                encode_store(l, y, 1.f, p.kv_fp8, valid && slot_ok, p.v_pages, row, p.v_scale);
             }
         }
     }
