@@ -321,6 +321,7 @@ def bench_ours(args, device, rank, world):
                          "speedup_of_dynamic_with_plan": round(s_ms / ms_per_step, 3)}
 
     prologue = bench_prologue(dsa, device, w, B, timed, max(10, min(args.steps, 200)))
+    multi = bench_multi(dsa, device, inp, w, C, m, timed, max(10, min(args.steps, 200)), nbytes, ms_per_step)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     host = {k: inp[k].cpu().pin_memory() for k in ("q", "q_scale", "k_pages", "v_pages", "k_scale", "v_scale",
@@ -382,6 +383,7 @@ def bench_ours(args, device, rank, world):
         "pct_of_nominal_8tbs": round(100 * nbytes / (ms_per_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 1),
         "static": static,
         "prologue": prologue,
+        "multi_token": multi,
         "roofline": {"bound": "hbm", "kernel": "attn_kernel (persistent decode, dsa_decode)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
@@ -435,6 +437,53 @@ def bench_prologue(dsa, device, w, batch: int, timed, steps: int) -> dict:
         gbs = nb / (ms * 1e-3) / 1e9
         res[label] = {"tokens": n, "us": round(ms * 1e3, 2), "algorithmic_bytes": nb, "GB/s": round(gbs, 1),
                       "frac_of_hbm_peak": round(gbs / peak, 4)}
+    return res
+
+
+def bench_multi(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes: int, single_ms: float) -> dict:
+    """Multi-token verify steps (q_len query tokens per request, causal within the draft) on
+    this workload's KV: plan -> dsa_decode_multi -> dsa_combine_multi in one graph.  The KV
+    stream is read once per step whatever q_len is; `vs_q_len_one_token_steps` compares with
+    q_len separate one-token steps (q_len x the one-token step time)."""
+    if w.kv_dtype != "bf16":
+        return {"note": "multi-token queries are built for bf16 K/V"}
+    B, hq, hkv = int(inp["seq_lens"].shape[0]), w.num_q_heads, w.num_kv_heads
+    G = hq // hkv
+    gen = torch.Generator(device=device)
+    gen.manual_seed(5)
+    peak, _ = measured_peaks()
+    res = {}
+    for q_len in (2, 6):
+        q = torch.randn(B, q_len, hq, 128, generator=gen, device=device).to(torch.bfloat16)
+        tm = dsa.TaskMap(B, hkv, C, device)
+        po, pl = dsa.partial_buffers(tm.max_descs, q_len * G, device)
+        out = torch.empty(B, q_len, hq, 128, dtype=torch.bfloat16, device=device)
+        out_lse = torch.empty(B, q_len, hq, dtype=torch.float32, device=device)
+
+        def plan(tm=tm):
+            dsa.plan(inp["seq_lens"], hkv, C, m, task_map=tm)
+
+        def dec(q=q, q_len=q_len, tm=tm, po=po, pl=pl):
+            dsa.decode_multi(q_len, q, inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
+                             inp["sm_scale"], partial_o=po, partial_lse=pl)
+
+        def comb(q_len=q_len, tm=tm, po=po, pl=pl, out=out, out_lse=out_lse):
+            dsa.combine_multi(q_len, tm, po, pl, hq, out=out, out_lse=out_lse)
+
+        per = timed([plan, dec, comb], steps, 3)
+        if dsa.get_status(tm) != 0:
+            raise RuntimeError(f"multi-token q_len {q_len}: device status set")
+        t_plan, t_dec, t_comb = (float(x) for x in per.mean(axis=0))
+        step = t_plan + t_dec + t_comb
+        gbs = nbytes / (t_dec * 1e-3) / 1e9
+        flops = 4.0 * q_len * G * 128 * (nbytes / 512)  # QK and PV over every (token, KV head)
+        res[f"q_len_{q_len}"] = {
+            "rows_per_unit": q_len * G, "us_per_step": round(step * 1e3, 2),
+            "breakdown_us": {"plan": round(t_plan * 1e3, 2), "decode": round(t_dec * 1e3, 2),
+                             "combine": round(t_comb * 1e3, 2)},
+            "decode_kv_GB/s": round(gbs, 1), "decode_frac_of_hbm_peak": round(gbs / peak, 4),
+            "decode_TFLOP/s": round(flops / (t_dec * 1e-3) / 1e12, 1),
+            "vs_q_len_one_token_steps": round(q_len * single_ms / step, 2)}
     return res
 
 

@@ -92,13 +92,17 @@ constexpr int kMaxRows = 64; // query rows (query tokens x G) of one unit in a m
 constexpr int kDescInfoBytes = 80;
 
 // QW = 0: one query token per request; the consumer groups take alternate tiles and all
-// warps of the CTA merge at each descriptor end.  QW = 1 or 2: multi-token queries; every
-// consumer warp takes every tile: its token half (32 tokens) for its column set of QW
-// 8-column blocks (query rows), and the two halves of a column set merge pairwise.
+// warps of the CTA merge at each descriptor end.  QW = 1 or 2: multi-token queries with
+// mma.sync; every consumer warp takes every tile: its token half (32 tokens) for its
+// column set of QW 8-column blocks (query rows), and the two halves of a column set merge
+// pairwise.  QW = 3: multi-token queries on the 5th-generation tensor cores: S = Q K^T and
+// O = P V accumulate in tensor memory, one softmax thread per query row (4 warps), a warp
+// issuing S (and laying Q out as its operand), a warp issuing P.V.
 template <int KV, int STAGES, int GROUPS, int MSLOTS = 2, int QW = 0>
 struct Layout {
-    static constexpr int kNcw = GROUPS * 4;  // consumer warps
-    static constexpr int kThreads = (kNcw + 1) * 32;       // consumers + producer
+    static constexpr bool kTc = QW == 3;
+    static constexpr int kNcw = GROUPS * 4;  // consumer warps (softmax warps for QW = 3)
+    static constexpr int kThreads = (kNcw + (kTc ? 3 : 1)) * 32;  // consumers + producer (+ MMA, Q warps)
     static constexpr int kThreadsFused = (kNcw + 2) * 32;  // + epilogue warp (fused combine)
     static constexpr int kStageTx = 2 * Cfg<KV>::kTileBytes + 2 * Cfg<KV>::kScaleBytes;
     static constexpr int kStageBytes = round_up(kStageTx, 1024);
@@ -108,20 +112,31 @@ struct Layout {
     static constexpr int kOStride = 132;  // floats per head row of a warp's O (padding avoids bank conflicts)
     static constexpr int kWarpFloats = kMaxGroup * kOStride + 2 * kMaxGroup;
     static constexpr int kPairFloats = 8 * QW * kOStride + 2 * 8 * QW;  // one column set's second half
-    static constexpr int kMergeOff = kQOff + kQSlots * kQSlot;
-    static constexpr int kMergeSlot = QW ? 4 * kPairFloats : kNcw * kWarpFloats;  // floats per merge slot
-    static constexpr int kMergeBars = QW ? 4 : 2;          // merge_full / merge_done barriers each
+    // QW = 3: Q as the MMA's A operand (64 rows x 128, no swizzle, K-major: 8-row x 16-byte
+    // core matrices, 128 B apart along K, 2 KB apart along rows), two buffers; then P (64
+    // rows x 64 tokens, same form, 1 KB between row groups) as bf16 high and low parts, two
+    // buffers of 16 KB.
+    static constexpr int kQcOff = kQOff + kQSlots * kQSlot;
+    static constexpr int kQcBytes = kTc ? 2 * kMaxRows * kHeadDim * 2 : 0;
+    static constexpr int kPOff = kQcOff + kQcBytes;
+    static constexpr int kPBytes = kTc ? 2 * 2 * kMaxRows * kTile * 2 : 0;
+    static constexpr int kMergeOff = kPOff + kPBytes;
+    static constexpr int kMergeSlot = kTc ? 0 : (QW ? 4 * kPairFloats : kNcw * kWarpFloats);  // floats per merge slot
+    static constexpr int kMergeBars = kTc ? 0 : (QW ? 4 : 2);  // merge_full / merge_done barriers each
+    static constexpr int kTcBars = kTc ? 14 : 0;  // s_full, s_free, p_full x2; team1_done, o_free; qc_full, qc_free, p_free x2
     static constexpr int kBarOff = kMergeOff + MSLOTS * kMergeSlot * 4;
-    // full, empty, qfull, qempty, merge_full, merge_done, epi_ready, epi_free
-    static constexpr int kNumBars = 2 * STAGES + 2 * kQSlots + 2 * kMergeBars + 2 * kEpiRing;
+    // full, empty, qfull, qempty, merge_full, merge_done, epi_ready, epi_free, tensor-core barriers
+    static constexpr int kNumBars = 2 * STAGES + 2 * kQSlots + 2 * kMergeBars + 2 * kEpiRing + kTcBars;
     static constexpr int kNValidOff = kBarOff + kNumBars * 8;
-    static constexpr int kAbortOff = kNValidOff + STAGES * 4;
+    static constexpr int kAbortOff = kNValidOff + STAGES * 4;  // abort flag, then the TMEM base address
     static constexpr int kInfoOff = round_up(kAbortOff + 16, 64);  // one DescInfo per Q slot
     static constexpr int kEpiOff = kInfoOff + kQSlots * kDescInfoBytes;  // kEpiRing EpiRecords + descriptor total
-    static constexpr int kBytes = kEpiOff + kEpiRing * 16 + 16;
+    static constexpr int kTeamOff = kEpiOff + kEpiRing * 16 + 16;   // QW = 3: team 1's (m, l, tiles) per row
+    static constexpr int kBytes = kTeamOff + (kTc ? kMaxRows * 12 : 0);
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static_assert(MSLOTS == 1 || MSLOTS == 2, "merge slots");
-    static_assert(QW == 0 || (MSLOTS == 1 && GROUPS == 2), "multi-token queries: 8 consumer warps, one merge slot");
+    static_assert(QW == 0 || (MSLOTS == 1 && GROUPS == 2), "multi-token shapes");
+    static_assert(!kTc || (KV == 0 && kQcOff % 1024 == 0 && kPOff % 1024 == 0), "tensor-core operand buffers");
     // Each stage must be consumed by one group only: a group then meets the phases of its
     // stages' full barriers in order.  With stages shared by two groups, one group could wait
     // for phase k+1 while phase k is still pending, pass the parity test early and arrive on
@@ -322,6 +337,14 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
     auto merge_done = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + MB + s); };
     auto epi_ready = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 2 * MB + s); };
     auto epi_free = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 2 * MB + kEpiRing + s); };
+    const uint32_t tc_bar0 = bar0 + 8u * (2 * STAGES + 2 * kQSlots + 2 * MB + 2 * kEpiRing);
+    auto s_full = [&](int b) { return tc_bar0 + 8u * b; };
+    auto s_free = [&](int b) { return tc_bar0 + 8u * (2 + b); };
+    auto p_full = [&](int b) { return tc_bar0 + 8u * (4 + b); };
+    const uint32_t team1_done = tc_bar0 + 8u * 6, o_free = tc_bar0 + 8u * 7;
+    auto qc_full = [&](int b) { return tc_bar0 + 8u * (8 + b); };
+    auto qc_free = [&](int b) { return tc_bar0 + 8u * (10 + b); };
+    auto p_free = [&](int b) { return tc_bar0 + 8u * (12 + b); };
     EpiRecord *epi_rec = reinterpret_cast<EpiRecord *>(smem + L::kEpiOff);
     volatile int *epi_total = reinterpret_cast<volatile int *>(smem + L::kEpiOff + kEpiRing * sizeof(EpiRecord));
     int *nvalid = reinterpret_cast<int *>(smem + L::kNValidOff);
@@ -333,13 +356,25 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), QW ? NCW : 4);  // QW: every consumer warp reads every stage
+            // QW = 1, 2: every consumer warp reads every stage; QW = 3: the S and PV warps release it
+            mbar_init(empty_bar(s), QW == 3 ? 2 : (QW ? NCW : 4));
         }
         for (int s = 0; s < kQSlots; ++s) {
             mbar_init(qfull_bar(s), 1);
-            mbar_init(qempty_bar(s), NCW);
+            mbar_init(qempty_bar(s), QW == 3 ? NCW + 2 : NCW);  // every warp that reads the hand-off
         }
-        if (QW) {
+        if (QW == 3) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(s_full(b), 1);
+                mbar_init(s_free(b), 4);  // one softmax team per buffer
+                mbar_init(p_full(b), 4);
+                mbar_init(qc_full(b), 1);
+                mbar_init(qc_free(b), 1);
+                mbar_init(p_free(b), 1);
+            }
+            mbar_init(team1_done, 4);
+            mbar_init(o_free, 4);
+        } else if (QW) {
             for (int s = 0; s < MB; ++s) {  // per column set: second half deposited / read
                 mbar_init(merge_full(s), 1);
                 mbar_init(merge_done(s), 1);
@@ -666,7 +701,379 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
         }
     }
 
-    if constexpr (QW > 0) {
+    if constexpr (QW == 3) {
+        // ============ multi-token queries on the 5th-generation tensor cores ============
+        // Rows r = i * G + g (query token i, head g), r < R = q_len * G <= 64.  Per tile:
+        //   S[64 x 64] = Qc . K^T in one of two 64-column TMEM buffers (M = 64: row r sits in
+        //   lane 32 (r / 16) + r % 16, i.e. lanes 0-15 of each warp's 32-lane quarter);
+        //   the softmax thread of row r (lane r % 16 of warp r / 16) masks it (causal within
+        //   the draft, past the length), keeps the running max m, raised lazily (O is
+        //   rescaled only when the max grows by more than 8 in base 2), and writes P =
+        //   2^(s - m) as bf16 high and low parts;
+        //   O[64 x 128] += P_hi . V + P_lo . V in TMEM columns 128-255.
+        // Two warps issue the products: the S warp runs ahead (two S buffers) as stages land,
+        // the PV warp follows the softmax; each releases its half of a ring stage (K, V) when
+        // its products have read it, so the softmax of tile g overlaps the products of its
+        // neighbours and no product waits for an unrelated load.
+        const int R = p.q_len * G;
+        uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kAbortOff + 4);
+        constexpr int kTcThreads = (NCW + 2) * 32;  // softmax warps, S warp, PV warp
+        constexpr uint32_t kQcBuf = kMaxRows * kHeadDim * 2, kPBuf = 2 * kMaxRows * kTile * 2;
+        if (warp == NCW + 1) tmem_alloc(smem_u32(tmem_slot), 512);
+        tc_fence_before();
+        named_bar_sync(1, kTcThreads);
+        tc_fence_after();
+        const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+        constexpr uint32_t kIdS = umma_idesc_bf16(64, 64, 0, 0);   // Q K-major, K K-major
+        constexpr uint32_t kIdO = umma_idesc_bf16(64, 128, 0, 1);  // P K-major, V M/N-major
+        bool failed = false;
+
+        if (warp == NCW + 1) {
+            // ---- S warp: lays each descriptor's Q out as the A operand (zero past R), then
+            //      issues S = Q K^T for its tiles as soon as a stage and an S buffer are ready
+            //      (lane 0 issues, the warp waits together); its commit on the stage's empty
+            //      barrier says the K half is no longer read
+            int g = 0, last_d = -1;
+            for (int d = 0;; ++d) {
+                const int qslot = d % kQSlots;
+                if (!wait_phase(qfull_bar(qslot), (d / kQSlots) & 1, abort_flag, p.status)) {
+                    failed = true;
+                    break;
+                }
+                const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
+                const int end = inf->end, n = inf->n, c_start = inf->c_start;
+                if (!end) {
+                    if (!wait_phase(qc_free(d & 1), ((d >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                        failed = true;
+                        break;
+                    }
+                    const uint8_t *src = smem + L::kQOff + qslot * L::kQSlot;
+                    uint8_t *dst = smem + L::kQcOff + (d & 1) * kQcBuf;
+                    for (int i = lane; i < kMaxRows * 16; i += 32) {  // 16-byte chunk kc of row r
+                        const int r = i >> 4, kc = i & 15;
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (r < R) v = *reinterpret_cast<const uint4 *>(src + r * (kHeadDim * 2) + kc * 16);
+                        *reinterpret_cast<uint4 *>(dst + (r >> 3) * 2048 + kc * 128 + (r & 7) * 16) = v;
+                    }
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qempty_bar(qslot));
+                if (end) break;
+                const uint32_t qa = sbase + L::kQcOff + (d & 1) * kQcBuf;
+                for (int li = 0; li < n; ++li, ++g) {
+                    const int c = c_start + li, stage = c % STAGES, buf = g & 1;
+                    if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status) ||
+                        !wait_phase(s_free(buf), ((g >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                        failed = true;
+                        break;
+                    }
+                    const int nv = nvalid[stage];
+                    if (lane == 0) {
+                        if (nv > 0) {
+                            tc_fence_after();
+                            const uint32_t kb = sbase + stage * L::kStageBytes;
+#pragma unroll
+                            for (int ks = 0; ks < 8; ++ks)
+                                umma_bf16(tmem + 64 * buf, umma_desc(qa + ks * 256, 128, 2048, 0),
+                                          umma_desc(kb + (ks >> 2) * (C::kTileBytes / 2) + (ks & 3) * 32, 16, 1024, 2),
+                                          kIdS, ks > 0);
+                            umma_commit(s_full(buf));
+                            umma_commit(empty_bar(stage));
+                        } else {
+                            mbar_arrive(s_full(buf));
+                            mbar_arrive(empty_bar(stage));
+                        }
+                    }
+                    __syncwarp();
+                }
+                if (failed) break;
+                if (lane == 0) umma_commit(qc_free(d & 1));  // the descriptor's S products have read Qc
+                __syncwarp();
+                last_d = d;
+            }
+            // the last commit lands once every product this warp issued has completed
+            if (!failed && last_d >= 0) wait_phase(qc_free(last_d & 1), (last_d >> 1) & 1, abort_flag, p.status);
+        } else if (warp == NCW + 2) {
+            // ---- PV warp: O += P_hi . V + P_lo . V as soon as the softmax warps hand P over;
+            //      its commit on the stage's empty barrier says the V half is no longer read
+            int g = 0;
+            for (int d = 0;; ++d) {
+                const int qslot = d % kQSlots;
+                if (!wait_phase(qfull_bar(qslot), (d / kQSlots) & 1, abort_flag, p.status)) {
+                    failed = true;
+                    break;
+                }
+                const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
+                const int end = inf->end, n = inf->n, c_start = inf->c_start;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qempty_bar(qslot));
+                if (end) break;
+                bool first_pv[2] = {true, true};  // per softmax team (tile parity): O_t not yet written
+                bool waited_free = false;
+                for (int li = 0; li < n; ++li, ++g) {
+                    const int c = c_start + li, stage = c % STAGES, pb = g & 1;
+                    if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status) ||
+                        !wait_phase(p_full(pb), (g >> 1) & 1, abort_flag, p.status)) {
+                        failed = true;
+                        break;
+                    }
+                    const int nv = nvalid[stage];
+                    if (nv > 0) {
+                        // both O accumulators are free once team 0 merged the previous descriptor
+                        if (!waited_free && !wait_phase(o_free, (d & 1) ^ 1, abort_flag, p.status)) {
+                            failed = true;
+                            break;
+                        }
+                        waited_free = true;
+                        if (lane == 0) {
+                            tc_fence_after();
+                            const uint32_t vb = sbase + stage * L::kStageBytes + C::kTileBytes;
+                            const uint32_t pa = sbase + L::kPOff + pb * kPBuf;
+                            const uint32_t od = tmem + 128 + 128 * pb;
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks) {
+                                const uint64_t bd = umma_desc(vb + ks * 2048, 8192, 1024, 2);
+                                umma_bf16(od, umma_desc(pa + ks * 256, 128, 1024, 0), bd, kIdO, !(first_pv[pb] && ks == 0));
+                                umma_bf16(od, umma_desc(pa + kPBuf / 2 + ks * 256, 128, 1024, 0), bd, kIdO, true);
+                            }
+                            umma_commit(p_free(pb));
+                            umma_commit(empty_bar(stage));
+                        }
+                        first_pv[pb] = false;
+                    } else if (lane == 0) {
+                        // a commit, not an arrive: its phase also means every earlier product is done
+                        umma_commit(p_free(pb));
+                        mbar_arrive(empty_bar(stage));
+                    }
+                    __syncwarp();
+                }
+                if (failed) break;
+            }
+        } else {
+            // ---- softmax warps: two teams of four (team t = warps 4t .. 4t + 3) take the tiles
+            //      of parity t (S[t], P[t], O_t); lane l < 16 of warp w owns row r = 16 (w & 3) + l
+            //      (M = 64 accumulators: lanes 0-15 of each sub-partition).  At each descriptor
+            //      end team 1 publishes its row state and team 0 merges O_0 and O_1 from TMEM.
+            const int team = warp >> 2, sp = warp & 3;
+            const bool own = lane < 16;
+            const int r = 16 * sp + lane;
+            const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
+            const uint32_t o_col = 128 + 128 * team;
+            const int tid = sp * 32 + lane;  // within the team
+            float *team_ml = reinterpret_cast<float *>(smem + L::kTeamOff);  // m[64], l[64], tiles[64]
+            int g = 0;
+            for (int d = 0;; ++d) {
+                const int qslot = d % kQSlots;
+                if (!wait_phase(qfull_bar(qslot), (d / kQSlots) & 1, abort_flag, p.status)) {
+                    failed = true;
+                    break;
+                }
+                const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
+                const int end = inf->end, n = inf->n, slot = inf->slot, c_start = inf->c_start;
+                const int dt0 = inf->t0, len = inf->len;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qempty_bar(qslot));
+                if (end) break;
+                const bool valid = own && r < R;
+                const int lim = valid ? len - p.q_len + r / G + 1 : -1;  // visible tokens: t < lim
+                float m = -INFINITY, l = 0.f;
+                int pv_desc = 0, last_g = -1;
+                for (int li = 0; li < n; ++li, ++g) {
+                    if ((g & 1) != team) continue;
+                    const int c = c_start + li, stage = c % STAGES, buf = team;
+                    if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status) ||
+                        !wait_phase(s_full(buf), (g >> 1) & 1, abort_flag, p.status)) {
+                        failed = true;
+                        break;
+                    }
+                    const int nv = nvalid[stage];
+                    tc_fence_after();
+                    float sv[64];
+                    if (nv > 0) {
+                        float a[32];
+                        tmem_ld32(tmem + lane_base + 64 * buf, a);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) sv[j] = a[j];
+                        tmem_ld32(tmem + lane_base + 64 * buf + 32, a);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) sv[32 + j] = a[j];
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(s_free(buf));
+                    // P[buf] and O_team were last used by the P.V of this team's previous tile
+                    if (!wait_phase(p_free(buf), ((g >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                        failed = true;
+                        break;
+                    }
+                    last_g = g;
+                    if (nv == 0) {  // no data in this stage: the PV warp skips its P.V
+                        if (lane == 0) mbar_arrive(p_full(buf));
+                        continue;
+                    }
+                    // ---- running maximum over the row's visible tokens (t < lim, slot < nv)
+                    const int vis = max(0, min(nv, lim - (dt0 + li) * kTile));
+                    float mx = -INFINITY;
+                    if (vis == kTile) {
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, sv[j]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, j < vis ? sv[j] : -INFINITY);
+                    }
+                    const float mnew = fmaxf(m, mx * p.score_scale);
+                    const bool grow = m != -INFINITY && mnew > m + 8.f;
+                    if (__any_sync(0xffffffffu, grow)) {
+                        // rows whose maximum grew: O_team *= 2^(m - mnew) (its last P.V is done)
+                        tc_fence_after();
+                        const float alpha = grow ? ex2(m - mnew) : 1.f;
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            float o[32];
+                            tmem_ld32(tmem + lane_base + o_col + 32 * cc, o);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) o[j] *= alpha;
+                            tmem_st32(tmem + lane_base + o_col + 32 * cc, o);
+                        }
+                        l *= alpha;
+                    }
+                    if (grow || m == -INFINITY) m = mnew;
+                    // ---- P = 2^(s * scale - m) (0 where not visible) as bf16 high part (the top 16
+                    //      bits) and low part (the rest, rounded), row r of P[buf]
+                    const float nm = -m;
+                    uint8_t *pr = smem + L::kPOff + buf * kPBuf + (r >> 3) * 1024 + (r & 7) * 16;
+                    float ls = 0.f;
+#pragma unroll
+                    for (int kc = 0; kc < 8; ++kc) {
+                        uint32_t hw[4], lw[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 8 * kc + 2 * e;
+                            float p0 = ex2(fmaf(sv[j], p.score_scale, nm));
+                            float p1 = ex2(fmaf(sv[j + 1], p.score_scale, nm));
+                            if (vis < kTile) {
+                                p0 = j < vis ? p0 : 0.f;
+                                p1 = j + 1 < vis ? p1 : 0.f;
+                            }
+                            ls += p0 + p1;
+                            const uint32_t h0 = __float_as_uint(p0) & 0xFFFF0000u, h1 = __float_as_uint(p1) & 0xFFFF0000u;
+                            hw[e] = prmt(h0, h1, 0x7632u);
+                            lw[e] = pack_bf16x2(p0 - __uint_as_float(h0), p1 - __uint_as_float(h1));
+                        }
+                        if (own) {
+                            *reinterpret_cast<uint4 *>(pr + kc * 128) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                            *reinterpret_cast<uint4 *>(pr + kPBuf / 2 + kc * 128) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        }
+                    }
+                    l += ls;
+                    // ---- V rows past the request's length are zeroed (stale or NaN slots of the page)
+                    if (nv < kTile) {
+                        uint8_t *vt = smem + stage * L::kStageBytes + C::kTileBytes;
+                        for (int i = tid; i < (kTile - nv) * 16; i += 128) {
+                            const int row = nv + (i >> 4), ch = i & 15;
+                            *reinterpret_cast<uint4 *>(vt + (ch >> 3) * (C::kTileBytes / 2) + row * 128 + (ch & 7) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(p_full(buf));
+                    ++pv_desc;
+                }
+                if (failed) break;
+                // ---- this team's products of the descriptor are done once its last tile's buffer
+                //      phase is (that commit covers every earlier product)
+                if (last_g >= 0) {
+                    if (!wait_phase(p_free(team), (last_g >> 1) & 1, abort_flag, p.status)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                if (team == 1) {
+                    // publish (m, l, has products) once team 0 has read the previous descriptor's
+                    if (!wait_phase(o_free, (d & 1) ^ 1, abort_flag, p.status)) {
+                        failed = true;
+                        break;
+                    }
+                    if (own) {
+                        team_ml[r] = m;
+                        team_ml[kMaxRows + r] = l;
+                        team_ml[2 * kMaxRows + r] = pv_desc > 0 ? 1.f : 0.f;
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(team1_done);
+                    continue;
+                }
+                // ---- team 0: merge (m, l, O_0) with team 1's (m, l, O_1); the partial row is
+                //      O / L with lse = ln(2) (M + log2 L)
+                if (!wait_phase(team1_done, d & 1, abort_flag, p.status)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                const float m1 = own ? team_ml[r] : -INFINITY, l1 = own ? team_ml[kMaxRows + r] : 0.f;
+                const bool has1 = own && team_ml[2 * kMaxRows + r] != 0.f;
+                const bool any1 = __any_sync(0xffffffffu, has1), any0 = pv_desc > 0;
+                const float M = fmaxf(m, has1 ? m1 : -INFINITY);
+                float w0 = 0.f, w1 = 0.f, lse = -INFINITY;
+                if (M != -INFINITY) {
+                    const float e0 = any0 ? ex2(m - M) : 0.f, e1 = has1 ? ex2(m1 - M) : 0.f;
+                    const float Ls = (any0 ? l * e0 : 0.f) + (has1 ? l1 * e1 : 0.f);
+                    if (Ls > 0.f) {
+                        w0 = e0 / Ls;
+                        w1 = e1 / Ls;
+                        lse = (M + lg2(Ls)) * kLn2;
+                    }
+                }
+                float *dst = p.partial_o + (static_cast<int64_t>(slot) * R + r) * kHeadDim;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    float o0[32], o1[32];
+                    if (any0) {
+                        tmem_ld32(tmem + lane_base + 128 + 32 * cc, o0);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o0[j] = 0.f;
+                    }
+                    if (any1) {
+                        tmem_ld32(tmem + lane_base + 256 + 32 * cc, o1);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o1[j] = 0.f;
+                    }
+                    if (valid) {
+                        const float a0 = any0 ? w0 : 0.f, a1 = has1 ? w1 : 0.f;
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4) {
+                            float4 v;
+                            v.x = (a0 != 0.f ? o0[4 * q4] * a0 : 0.f) + (a1 != 0.f ? o1[4 * q4] * a1 : 0.f);
+                            v.y = (a0 != 0.f ? o0[4 * q4 + 1] * a0 : 0.f) + (a1 != 0.f ? o1[4 * q4 + 1] * a1 : 0.f);
+                            v.z = (a0 != 0.f ? o0[4 * q4 + 2] * a0 : 0.f) + (a1 != 0.f ? o1[4 * q4 + 2] * a1 : 0.f);
+                            v.w = (a0 != 0.f ? o0[4 * q4 + 3] * a0 : 0.f) + (a1 != 0.f ? o1[4 * q4 + 3] * a1 : 0.f);
+                            *reinterpret_cast<float4 *>(dst + 32 * cc + 4 * q4) = v;
+                        }
+                    }
+                }
+                if (valid) p.partial_lse[static_cast<int64_t>(slot) * R + r] = lse;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_free);
+            }
+        }
+        (void)failed;
+        // ---- every tensor-core role is done: release the tensor memory
+        tc_fence_before();
+        named_bar_sync(1, kTcThreads);
+        if (warp == NCW + 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem, 512);
+        }
+        return;
+    } else if constexpr (QW > 0) {
         // ===================== consumer warps, multi-token queries =====================
         // Query rows r = i * G + g (query token i, head g); row r of a request of length len
         // sees the tokens t < len - q_len + i + 1 (causal within the draft).  Warp w takes
@@ -1412,9 +1819,7 @@ extern "C" dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q
     kp.cta_desc_begin = map->cta_desc_begin;
     kp.descs = reinterpret_cast<const int4 *>(map->descs);
     const dim3 grid(map->num_ctas);
-    if (R <= 32)
-        return launch<0, kPersistStagesBf16, kPersistGroups, true, false, 1, 1>(a, kp, grid, to_cuda(stream));
-    return launch<0, kPersistStagesBf16, kPersistGroups, true, false, 1, 2>(a, kp, grid, to_cuda(stream));
+    return launch<0, kPersistStagesBf16, 2, true, false, 1, 3>(a, kp, grid, to_cuda(stream));
 }
 
 extern "C" dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_scale, const void *k_pages,
