@@ -203,7 +203,11 @@ dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_sca
  * seq_lens[b] - q_len + i and sees the tokens t <= that position (causal within the
  * draft; rows with no visible token in a descriptor get o = 0, lse = -inf there).
  *   q        [B, q_len, Hq, 128] bf16 (row i*G + g of unit (b, h) is q[b][i][h*G + g]).
- *   partial_o [map->max_descs, q_len*G, 128] fp32, partial_lse [map->max_descs, q_len*G].
+ *   partial_o [2 * map->max_descs, q_len*G, 128] fp32, partial_lse [2 * map->max_descs,
+ *            q_len*G] for q_len > 1: two slots per descriptor, 2x and 2x + 1, each the
+ *            attention over part of the descriptor's tiles (the two softmax teams of the
+ *            kernel); merging them gives the descriptor's attention, and dsa_combine_multi
+ *            does so.  (q_len = 1: [map->max_descs, G, 128] as for dsa_decode.)
  * Supported: BF16 Q and K/V, q_len * G <= 64; q_len = 1 is exactly dsa_decode (all of
  * its dtypes).  Other arguments and errors are as for dsa_decode.
  */

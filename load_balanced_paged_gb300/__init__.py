@@ -232,10 +232,11 @@ def combine(task_map: TaskMap, partial_o, partial_lse, num_q_heads: int, out=Non
 
 def decode_multi(q_len: int, q, k_pages, v_pages, block_table, seq_lens, task_map: TaskMap, sm_scale: float,
                  partial_o=None, partial_lse=None, q_scale=None, k_scale=None, v_scale=None, stream=None):
-    """dsa_decode_multi: q [B, q_len, Hq, 128]; partials hold q_len * G rows per descriptor."""
+    """dsa_decode_multi: q [B, q_len, Hq, 128]; partials hold q_len * G rows per slot, two
+    slots per descriptor when q_len > 1."""
     R = q_len * (q.shape[-2] // task_map.num_kv_heads)
     if partial_o is None:
-        partial_o, partial_lse = partial_buffers(task_map.max_descs, R, q.device)
+        partial_o, partial_lse = partial_buffers(task_map.max_descs * (2 if q_len > 1 else 1), R, q.device)
     args = _attn_args(q, k_pages, v_pages, block_table, seq_lens, task_map.num_kv_heads, sm_scale,
                       q_scale, k_scale, v_scale)
     rc = _lib.dsa_decode_multi(q_len, *args, ctypes.byref(task_map.struct), _ptr(partial_o), _ptr(partial_lse),

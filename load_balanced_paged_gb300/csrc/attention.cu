@@ -51,6 +51,7 @@ struct KernelParams {
     const int32_t *seq_lens;
     int32_t max_pages, num_pages, hq, hkv, G, num_units, max_slots;
     int32_t q_len;      // query tokens per request (1: plain decode; > 1: multi-token verify)
+    int32_t slots_per_desc;  // partial slots per descriptor (2 for the tensor-core multi-token path)
     float score_scale;  // sm_scale * log2(e)
     // persistent schedule
     const int32_t *cta_desc_begin;
@@ -123,7 +124,7 @@ struct Layout {
     static constexpr int kMergeOff = kPOff + kPBytes;
     static constexpr int kMergeSlot = kTc ? 0 : (QW ? 4 * kPairFloats : kNcw * kWarpFloats);  // floats per merge slot
     static constexpr int kMergeBars = kTc ? 0 : (QW ? 4 : 2);  // merge_full / merge_done barriers each
-    static constexpr int kTcBars = kTc ? 14 : 0;  // s_full, s_free, p_full x2; team1_done, o_free; qc_full, qc_free, p_free x2
+    static constexpr int kTcBars = kTc ? 14 : 0;  // s_full, s_free, p_full, o_free, qc_full, qc_free, p_free x2
     static constexpr int kBarOff = kMergeOff + MSLOTS * kMergeSlot * 4;
     // full, empty, qfull, qempty, merge_full, merge_done, epi_ready, epi_free, tensor-core barriers
     static constexpr int kNumBars = 2 * STAGES + 2 * kQSlots + 2 * kMergeBars + 2 * kEpiRing + kTcBars;
@@ -131,8 +132,7 @@ struct Layout {
     static constexpr int kAbortOff = kNValidOff + STAGES * 4;  // abort flag, then the TMEM base address
     static constexpr int kInfoOff = round_up(kAbortOff + 16, 64);  // one DescInfo per Q slot
     static constexpr int kEpiOff = kInfoOff + kQSlots * kDescInfoBytes;  // kEpiRing EpiRecords + descriptor total
-    static constexpr int kTeamOff = kEpiOff + kEpiRing * 16 + 16;   // QW = 3: team 1's (m, l, tiles) per row
-    static constexpr int kBytes = kTeamOff + (kTc ? kMaxRows * 12 : 0);
+    static constexpr int kBytes = kEpiOff + kEpiRing * 16 + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static_assert(MSLOTS == 1 || MSLOTS == 2, "merge slots");
     static_assert(QW == 0 || (MSLOTS == 1 && GROUPS == 2), "multi-token shapes");
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
     auto s_full = [&](int b) { return tc_bar0 + 8u * b; };
     auto s_free = [&](int b) { return tc_bar0 + 8u * (2 + b); };
     auto p_full = [&](int b) { return tc_bar0 + 8u * (4 + b); };
-    const uint32_t team1_done = tc_bar0 + 8u * 6, o_free = tc_bar0 + 8u * 7;
+    auto o_free = [&](int t) { return tc_bar0 + 8u * (6 + t); };
     auto qc_full = [&](int b) { return tc_bar0 + 8u * (8 + b); };
     auto qc_free = [&](int b) { return tc_bar0 + 8u * (10 + b); };
     auto p_free = [&](int b) { return tc_bar0 + 8u * (12 + b); };
@@ -372,8 +372,8 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 mbar_init(qc_free(b), 1);
                 mbar_init(p_free(b), 1);
             }
-            mbar_init(team1_done, 4);
-            mbar_init(o_free, 4);
+            mbar_init(o_free(0), 4);
+            mbar_init(o_free(1), 4);
         } else if (QW) {
             for (int s = 0; s < MB; ++s) {  // per column set: second half deposited / read
                 mbar_init(merge_full(s), 1);
@@ -479,11 +479,12 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         for (int g = 0; g < kMaxGroup; ++g)
                             if (g < G) wqs[g] = qs[g];
                     }
-                    if (wn == 0) {  // no tiles: its partial is empty, the consumers never see it
+                    if (wn == 0) {  // no tiles: its partials are empty, the consumers never see it
                         const int R = p.q_len * G;
-                        for (int i = 0; i < R * kHeadDim; ++i)
-                            p.partial_o[static_cast<int64_t>(wslot) * R * kHeadDim + i] = 0.f;
-                        for (int g = 0; g < R; ++g) p.partial_lse[static_cast<int64_t>(wslot) * R + g] = -INFINITY;
+                        const int64_t s0 = static_cast<int64_t>(wslot) * p.slots_per_desc;
+                        for (int i = 0; i < p.slots_per_desc * R * kHeadDim; ++i)
+                            p.partial_o[s0 * R * kHeadDim + i] = 0.f;
+                        for (int g = 0; g < p.slots_per_desc * R; ++g) p.partial_lse[s0 * R + g] = -INFINITY;
                     }
                 } else {
                     atomicOr(p.status, DSA_DEV_BAD_MAP);
@@ -810,7 +811,6 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 if (lane == 0) mbar_arrive(qempty_bar(qslot));
                 if (end) break;
                 bool first_pv[2] = {true, true};  // per softmax team (tile parity): O_t not yet written
-                bool waited_free = false;
                 for (int li = 0; li < n; ++li, ++g) {
                     const int c = c_start + li, stage = c % STAGES, pb = g & 1;
                     if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status) ||
@@ -820,12 +820,11 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                     }
                     const int nv = nvalid[stage];
                     if (nv > 0) {
-                        // both O accumulators are free once team 0 merged the previous descriptor
-                        if (!waited_free && !wait_phase(o_free, (d & 1) ^ 1, abort_flag, p.status)) {
+                        // O_t is free once team t has read out the previous descriptor's
+                        if (first_pv[pb] && !wait_phase(o_free(pb), (d & 1) ^ 1, abort_flag, p.status)) {
                             failed = true;
                             break;
                         }
-                        waited_free = true;
                         if (lane == 0) {
                             tc_fence_after();
                             const uint32_t vb = sbase + stage * L::kStageBytes + C::kTileBytes;
@@ -854,14 +853,14 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
             // ---- softmax warps: two teams of four (team t = warps 4t .. 4t + 3) take the tiles
             //      of parity t (S[t], P[t], O_t); lane l < 16 of warp w owns row r = 16 (w & 3) + l
             //      (M = 64 accumulators: lanes 0-15 of each sub-partition).  At each descriptor
-            //      end team 1 publishes its row state and team 0 merges O_0 and O_1 from TMEM.
+            //      end each team writes its own partial (slot 2 x descriptor + team); the
+            //      combine merges them with the others.
             const int team = warp >> 2, sp = warp & 3;
             const bool own = lane < 16;
             const int r = 16 * sp + lane;
             const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
             const uint32_t o_col = 128 + 128 * team;
             const int tid = sp * 32 + lane;  // within the team
-            float *team_ml = reinterpret_cast<float *>(smem + L::kTeamOff);  // m[64], l[64], tiles[64]
             int g = 0;
             for (int d = 0;; ++d) {
                 const int qslot = d % kQSlots;
@@ -992,76 +991,30 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                     }
                     tc_fence_after();
                 }
-                if (team == 1) {
-                    // publish (m, l, has products) once team 0 has read the previous descriptor's
-                    if (!wait_phase(o_free, (d & 1) ^ 1, abort_flag, p.status)) {
-                        failed = true;
-                        break;
-                    }
-                    if (own) {
-                        team_ml[r] = m;
-                        team_ml[kMaxRows + r] = l;
-                        team_ml[2 * kMaxRows + r] = pv_desc > 0 ? 1.f : 0.f;
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(team1_done);
-                    continue;
-                }
-                // ---- team 0: merge (m, l, O_0) with team 1's (m, l, O_1); the partial row is
-                //      O / L with lse = ln(2) (M + log2 L)
-                if (!wait_phase(team1_done, d & 1, abort_flag, p.status)) {
-                    failed = true;
-                    break;
-                }
-                tc_fence_after();
-                const float m1 = own ? team_ml[r] : -INFINITY, l1 = own ? team_ml[kMaxRows + r] : 0.f;
-                const bool has1 = own && team_ml[2 * kMaxRows + r] != 0.f;
-                const bool any1 = __any_sync(0xffffffffu, has1), any0 = pv_desc > 0;
-                const float M = fmaxf(m, has1 ? m1 : -INFINITY);
-                float w0 = 0.f, w1 = 0.f, lse = -INFINITY;
-                if (M != -INFINITY) {
-                    const float e0 = any0 ? ex2(m - M) : 0.f, e1 = has1 ? ex2(m1 - M) : 0.f;
-                    const float Ls = (any0 ? l * e0 : 0.f) + (has1 ? l1 * e1 : 0.f);
-                    if (Ls > 0.f) {
-                        w0 = e0 / Ls;
-                        w1 = e1 / Ls;
-                        lse = (M + lg2(Ls)) * kLn2;
-                    }
-                }
-                float *dst = p.partial_o + (static_cast<int64_t>(slot) * R + r) * kHeadDim;
+                // ---- this team's partial (slot 2 x descriptor + team): O_t / l, lse = ln(2) (m + log2 l)
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float lse = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+                float *dst = p.partial_o + ((2 * static_cast<int64_t>(slot) + team) * R + r) * kHeadDim;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    float o0[32], o1[32];
-                    if (any0) {
-                        tmem_ld32(tmem + lane_base + 128 + 32 * cc, o0);
+                    float o[32];
+                    if (pv_desc > 0) {
+                        tmem_ld32(tmem + lane_base + o_col + 32 * cc, o);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o0[j] = 0.f;
-                    }
-                    if (any1) {
-                        tmem_ld32(tmem + lane_base + 256 + 32 * cc, o1);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) o1[j] = 0.f;
+                        for (int j = 0; j < 32; ++j) o[j] = 0.f;
                     }
                     if (valid) {
-                        const float a0 = any0 ? w0 : 0.f, a1 = has1 ? w1 : 0.f;
 #pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4) {
-                            float4 v;
-                            v.x = (a0 != 0.f ? o0[4 * q4] * a0 : 0.f) + (a1 != 0.f ? o1[4 * q4] * a1 : 0.f);
-                            v.y = (a0 != 0.f ? o0[4 * q4 + 1] * a0 : 0.f) + (a1 != 0.f ? o1[4 * q4 + 1] * a1 : 0.f);
-                            v.z = (a0 != 0.f ? o0[4 * q4 + 2] * a0 : 0.f) + (a1 != 0.f ? o1[4 * q4 + 2] * a1 : 0.f);
-                            v.w = (a0 != 0.f ? o0[4 * q4 + 3] * a0 : 0.f) + (a1 != 0.f ? o1[4 * q4 + 3] * a1 : 0.f);
-                            *reinterpret_cast<float4 *>(dst + 32 * cc + 4 * q4) = v;
-                        }
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            *reinterpret_cast<float4 *>(dst + 32 * cc + 4 * q4) =
+                                make_float4(o[4 * q4] * inv, o[4 * q4 + 1] * inv, o[4 * q4 + 2] * inv, o[4 * q4 + 3] * inv);
                     }
                 }
-                if (valid) p.partial_lse[static_cast<int64_t>(slot) * R + r] = lse;
+                if (valid) p.partial_lse[(2 * static_cast<int64_t>(slot) + team) * R + r] = lse;
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(o_free);
+                if (lane == 0) mbar_arrive(o_free(team));
             }
         }
         (void)failed;
@@ -1733,6 +1686,7 @@ KernelParams base_params(const AttnArgs &a, float *partial_o, float *partial_lse
     kp.G = a.num_q_heads / a.num_kv_heads;
     kp.num_units = a.batch * a.num_kv_heads;
     kp.q_len = 1;
+    kp.slots_per_desc = 1;
     kp.score_scale = a.sm_scale * kLog2e;
     kp.partial_o = partial_o;
     kp.partial_lse = partial_lse;
@@ -1815,6 +1769,7 @@ extern "C" dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q
     if (batch == 0) return DSA_OK;
     KernelParams kp = base_params(a, partial_o, partial_lse, map->meta + 3);
     kp.q_len = q_len;
+    kp.slots_per_desc = 2;
     kp.max_slots = map->max_descs;
     kp.cta_desc_begin = map->cta_desc_begin;
     kp.descs = reinterpret_cast<const int4 *>(map->descs);

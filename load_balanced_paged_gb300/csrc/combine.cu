@@ -39,7 +39,8 @@ template <bool STATIC, typename OutT>
 __global__ void __launch_bounds__(kMaxGroup * 32)
     combine_kernel(const int32_t *__restrict__ unit_begin, const int32_t *__restrict__ unit_count, int32_t S,
                    const float *__restrict__ partial_o, const float *__restrict__ partial_lse, int32_t hq,
-                   int32_t hkv, int32_t G, int32_t q_len, OutT *__restrict__ out, float *__restrict__ out_lse) {
+                   int32_t hkv, int32_t G, int32_t q_len, int32_t spd, OutT *__restrict__ out,
+                   float *__restrict__ out_lse) {
     const int u = blockIdx.x;
     const int row = blockIdx.y * kMaxGroup + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     grid_launch_dependents();
@@ -47,8 +48,9 @@ __global__ void __launch_bounds__(kMaxGroup * 32)
     const int R = q_len * G;  // partial rows per slot
     if (row >= R) return;
     const int b = u / hkv, h = u - b * hkv;
-    const int64_t beg = STATIC ? static_cast<int64_t>(u) * S : unit_begin[u];
-    const int n = STATIC ? S : unit_count[u];
+    // spd partial slots per descriptor: the unit's slots are [spd * begin, spd * (begin + count))
+    const int64_t beg = STATIC ? static_cast<int64_t>(u) * S : static_cast<int64_t>(unit_begin[u]) * spd;
+    const int n = STATIC ? S : unit_count[u] * spd;
 
     float M = -INFINITY;
     for (int k = lane; k < n; k += 32) M = fmaxf(M, partial_lse[(beg + k) * R + row]);
@@ -100,16 +102,16 @@ dsa_status validate_combine(int32_t batch, int32_t hq, int32_t hkv, int32_t head
 template <bool STATIC>
 dsa_status launch_combine(const int32_t *ub, const int32_t *uc, int32_t S, const float *po, const float *plse,
                           int32_t batch, int32_t hq, int32_t hkv, void *out, dsa_dtype out_dtype, float *out_lse,
-                          cudaStream_t st, int32_t q_len = 1) {
+                          cudaStream_t st, int32_t q_len = 1, int32_t spd = 1) {
     const int units = batch * hkv;
     if (units == 0) return DSA_OK;
     const int G = hq / hkv;
     const dim3 grid(units, (q_len * G + kMaxGroup - 1) / kMaxGroup);
     if (out_dtype == DSA_BF16)
         return launch_pdl(combine_kernel<STATIC, __nv_bfloat16>, grid, dim3(kMaxGroup * 32), 0, st, ub, uc, S, po,
-                          plse, hq, hkv, G, q_len, static_cast<__nv_bfloat16 *>(out), out_lse);
+                          plse, hq, hkv, G, q_len, spd, static_cast<__nv_bfloat16 *>(out), out_lse);
     return launch_pdl(combine_kernel<STATIC, float>, grid, dim3(kMaxGroup * 32), 0, st, ub, uc, S, po, plse, hq,
-                      hkv, G, q_len, static_cast<float *>(out), out_lse);
+                      hkv, G, q_len, spd, static_cast<float *>(out), out_lse);
 }
 
 }  // namespace
@@ -139,7 +141,8 @@ extern "C" dsa_status dsa_combine_multi(int32_t q_len, const dsa_task_map *map, 
     if (!map || map->num_units != batch * num_kv_heads) return DSA_ERR_INVALID_ARG;
     if (batch > 0 && (!map->unit_partial_begin || !map->unit_num_partials)) return DSA_ERR_INVALID_ARG;
     return launch_combine<false>(map->unit_partial_begin, map->unit_num_partials, 0, partial_o, partial_lse, batch,
-                                 num_q_heads, num_kv_heads, out, out_dtype, out_lse, to_cuda(stream), q_len);
+                                 num_q_heads, num_kv_heads, out, out_dtype, out_lse, to_cuda(stream), q_len,
+                                 q_len > 1 ? 2 : 1);
 }
 
 extern "C" dsa_status dsa_static_combine(int32_t num_splits, const float *partial_o, const float *partial_lse,
