@@ -456,7 +456,7 @@ def bench_multi(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes: 
     for q_len in (2, 6):
         q = torch.randn(B, q_len, hq, 128, generator=gen, device=device).to(torch.bfloat16)
         tm = dsa.TaskMap(B, hkv, C, device)
-        po, pl = dsa.partial_buffers(2 * tm.max_descs, q_len * G, device)
+        po, pl = dsa.partial_buffers(2 * tm.max_descs, q_len * G, device)  # at most 2 slots per descriptor
         out = torch.empty(B, q_len, hq, 128, dtype=torch.bfloat16, device=device)
         out_lse = torch.empty(B, q_len, hq, dtype=torch.float32, device=device)
 

@@ -203,14 +203,16 @@ dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_sca
  * seq_lens[b] - q_len + i and sees the tokens t <= that position (causal within the
  * draft; rows with no visible token in a descriptor get o = 0, lse = -inf there).
  *   q        [B, q_len, Hq, 128] bf16 (row i*G + g of unit (b, h) is q[b][i][h*G + g]).
- *   partial_o [2 * map->max_descs, q_len*G, 128] fp32, partial_lse [2 * map->max_descs,
- *            q_len*G] for q_len > 1: two slots per descriptor, 2x and 2x + 1, each the
- *            attention over part of the descriptor's tiles (the two softmax teams of the
- *            kernel); merging them gives the descriptor's attention, and dsa_combine_multi
- *            does so.  (q_len = 1: [map->max_descs, G, 128] as for dsa_decode.)
+ *   partial_o [S * map->max_descs, q_len*G, 128] fp32, partial_lse [S * map->max_descs,
+ *            q_len*G] with S = dsa_multi_slots_per_desc(q_len, G): 1 up to 16 query rows
+ *            (slot x = descriptor x, the mma.sync kernel), else 2 (slots 2x and 2x + 1,
+ *            each the attention over part of the descriptor's tiles: the two softmax
+ *            teams of the tensor-memory kernel); merging a descriptor's slots gives its
+ *            attention, and dsa_combine_multi does so.
  * Supported: BF16 Q and K/V, q_len * G <= 64; q_len = 1 is exactly dsa_decode (all of
  * its dtypes).  Other arguments and errors are as for dsa_decode.
  */
+int32_t dsa_multi_slots_per_desc(int32_t q_len, int32_t group);
 dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q_dtype, const float *q_scale,
                             const void *k_pages, const void *v_pages, dsa_dtype kv_dtype,
                             const float *k_scale, const float *v_scale,

@@ -59,6 +59,8 @@ _lib.dsa_decode_fused.argtypes = _attn_args + [_TMP, _vp, _vp, _vp, _vp, _i32, _
 _lib.dsa_decode_fused.restype = ctypes.c_int
 _lib.dsa_combine.argtypes = [_TMP, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]
 _lib.dsa_combine.restype = ctypes.c_int
+_lib.dsa_multi_slots_per_desc.argtypes = [_i32, _i32]
+_lib.dsa_multi_slots_per_desc.restype = _i32
 _lib.dsa_decode_multi.argtypes = [_i32] + _attn_args + [_TMP, _vp, _vp, _vp]
 _lib.dsa_decode_multi.restype = ctypes.c_int
 _lib.dsa_combine_multi.argtypes = [_i32, _TMP, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]
@@ -236,7 +238,8 @@ def decode_multi(q_len: int, q, k_pages, v_pages, block_table, seq_lens, task_ma
     slots per descriptor when q_len > 1."""
     R = q_len * (q.shape[-2] // task_map.num_kv_heads)
     if partial_o is None:
-        partial_o, partial_lse = partial_buffers(task_map.max_descs * (2 if q_len > 1 else 1), R, q.device)
+        spd = int(_lib.dsa_multi_slots_per_desc(q_len, q.shape[-2] // task_map.num_kv_heads))
+        partial_o, partial_lse = partial_buffers(task_map.max_descs * spd, R, q.device)
     args = _attn_args(q, k_pages, v_pages, block_table, seq_lens, task_map.num_kv_heads, sm_scale,
                       q_scale, k_scale, v_scale)
     rc = _lib.dsa_decode_multi(q_len, *args, ctypes.byref(task_map.struct), _ptr(partial_o), _ptr(partial_lse),

@@ -1743,6 +1743,11 @@ extern "C" dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *
     return launch_persistent<1, false>(a, kp, map->num_ctas, to_cuda(stream));
 }
 
+extern "C" int32_t dsa_multi_slots_per_desc(int32_t q_len, int32_t group) {
+    if (q_len < 1 || group < 1) return -1;
+    return q_len > 1 && q_len * group > 16 ? 2 : 1;
+}
+
 extern "C" dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q_dtype, const float *q_scale,
                                        const void *k_pages, const void *v_pages, dsa_dtype kv_dtype,
                                        const float *k_scale, const float *v_scale, const int32_t *block_table,
@@ -1769,11 +1774,15 @@ extern "C" dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q
     if (batch == 0) return DSA_OK;
     KernelParams kp = base_params(a, partial_o, partial_lse, map->meta + 3);
     kp.q_len = q_len;
-    kp.slots_per_desc = 2;
+    kp.slots_per_desc = dsa_multi_slots_per_desc(q_len, num_q_heads / num_kv_heads);
     kp.max_slots = map->max_descs;
     kp.cta_desc_begin = map->cta_desc_begin;
     kp.descs = reinterpret_cast<const int4 *>(map->descs);
     const dim3 grid(map->num_ctas);
+    // up to 16 query rows: mma.sync warps (8 warps, 32 tokens x 8 rows each); more rows:
+    // the tensor-memory kernel (measured faster from 24 rows up, slower at 16)
+    if (kp.slots_per_desc == 1)
+        return launch<0, kPersistStagesBf16, kPersistGroups, true, false, 1, 1>(a, kp, grid, to_cuda(stream));
     return launch<0, kPersistStagesBf16, 2, true, false, 1, 3>(a, kp, grid, to_cuda(stream));
 }
 

@@ -142,7 +142,7 @@ extern "C" dsa_status dsa_combine_multi(int32_t q_len, const dsa_task_map *map, 
     if (batch > 0 && (!map->unit_partial_begin || !map->unit_num_partials)) return DSA_ERR_INVALID_ARG;
     return launch_combine<false>(map->unit_partial_begin, map->unit_num_partials, 0, partial_o, partial_lse, batch,
                                  num_q_heads, num_kv_heads, out, out_dtype, out_lse, to_cuda(stream), q_len,
-                                 q_len > 1 ? 2 : 1);
+                                 dsa_multi_slots_per_desc(q_len, num_q_heads / num_kv_heads));
 }
 
 extern "C" dsa_status dsa_static_combine(int32_t num_splits, const float *partial_o, const float *partial_lse,

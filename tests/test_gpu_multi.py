@@ -73,19 +73,20 @@ def test_multi_vs_oracle(dsa, lens, q_len, hq, hkv, C, m):
                 assert (out32[b, i] == 0).all() and torch.isneginf(lse[b, i]).all()
 
 
-@pytest.mark.parametrize("q_len", [3, 6])
+@pytest.mark.parametrize("q_len", [2, 3, 6])
 def test_multi_partials_each_descriptor(dsa, q_len):
     inp = make([40, 129, 1000, 2500], q_len, 64, 8, seed=7)
     _, _, _, tm, po, pl = run(dsa, inp, 37, 1)
     prob = problem(inp)
     h = tm.host()
     R = q_len * 8
+    spd = int(dsa.lib().dsa_multi_slots_per_desc(q_len, 8))
     po, pl = po.cpu().numpy(), pl.cpu().numpy()
     for x, (u, t0, t1, k) in enumerate(h["descs"]):
         b, hk = divmod(int(u), 8)
         o, lse = prob.span(b, hk, 64 * int(t0), min(64 * int(t1), int(inp["seq_lens"][b])))
-        # two slots per descriptor (the kernel's two softmax teams), merged here by the oracle
-        got_o, got_l = oracle.merge(po[2 * x:2 * x + 2, :R], pl[2 * x:2 * x + 2, :R])
+        # slots of the descriptor (two for the tensor-memory kernel's softmax teams), merged by the oracle
+        got_o, got_l = oracle.merge(po[spd * x:spd * x + spd, :R], pl[spd * x:spd * x + spd, :R])
         parity.assert_close(got_o, o, "bf16", f"descriptor {x}", round_ref=False)
         parity.assert_lse_close(got_l, lse, f"descriptor {x}")
 
