@@ -851,13 +851,15 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
             }
         } else {
             // ---- softmax warps: two teams of four (team t = warps 4t .. 4t + 3) take the tiles
-            //      of parity t (S[t], P[t], O_t); lane l < 16 of warp w owns row r = 16 (w & 3) + l
-            //      (M = 64 accumulators: lanes 0-15 of each sub-partition).  At each descriptor
-            //      end each team writes its own partial (slot 2 x descriptor + team); the
-            //      combine merges them with the others.
+            //      of parity t (S[t], P[t], O_t).  Warp w reads the 16 rows 16 (w & 3) .. + 15
+            //      (M = 64 accumulators: lanes 0-15 of each sub-partition) as m16n8 fragments:
+            //      thread (gid = lane / 4, tig = lane % 4) holds rows ra = 16 (w & 3) + gid and
+            //      rb = ra + 8, columns 8 k + 2 tig, + 1; a row's max and sum combine over the
+            //      four threads of its quad.  At each descriptor end each team writes its own
+            //      partial (slot 2 x descriptor + team); the combine merges them with the others.
             const int team = warp >> 2, sp = warp & 3;
-            const bool own = lane < 16;
-            const int r = 16 * sp + lane;
+            const int gid = lane >> 2, tig = lane & 3;
+            const int ra = 16 * sp + gid, rb = ra + 8;
             const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
             const uint32_t o_col = 128 + 128 * team;
             const int tid = sp * 32 + lane;  // within the team
@@ -874,9 +876,9 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qempty_bar(qslot));
                 if (end) break;
-                const bool valid = own && r < R;
-                const int lim = valid ? len - p.q_len + r / G + 1 : -1;  // visible tokens: t < lim
-                float m = -INFINITY, l = 0.f;
+                // visible tokens of each row: t < lim (-1: a row past R)
+                const int lim[2] = {ra < R ? len - p.q_len + ra / G + 1 : -1, rb < R ? len - p.q_len + rb / G + 1 : -1};
+                float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
                 int pv_desc = 0, last_g = -1;
                 for (int li = 0; li < n; ++li, ++g) {
                     if ((g & 1) != team) continue;
@@ -888,15 +890,11 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                     }
                     const int nv = nvalid[stage];
                     tc_fence_after();
-                    float sv[64];
+                    float sv[8][4];  // [column block k][(ra, 2tig), (ra, 2tig+1), (rb, 2tig), (rb, 2tig+1)]
                     if (nv > 0) {
-                        float a[32];
-                        tmem_ld32(tmem + lane_base + 64 * buf, a);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) sv[j] = a[j];
-                        tmem_ld32(tmem + lane_base + 64 * buf + 32, a);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) sv[32 + j] = a[j];
+                        for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + 64 * buf + 8 * k, sv[k]);
+                        tmem_wait_ld();
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -911,61 +909,77 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         if (lane == 0) mbar_arrive(p_full(buf));
                         continue;
                     }
-                    // ---- running maximum over the row's visible tokens (t < lim, slot < nv)
-                    const int vis = max(0, min(nv, lim - (dt0 + li) * kTile));
-                    float mx = -INFINITY;
-                    if (vis == kTile) {
+                    // ---- running maximum over each row's visible tokens (t < lim, slot < nv)
+                    const int tt = (dt0 + li) * kTile;
+                    const int vis[2] = {max(0, min(nv, lim[0] - tt)), max(0, min(nv, lim[1] - tt))};
+                    const bool full = vis[0] == kTile && vis[1] == kTile;
+                    float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-                        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, sv[j]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, j < vis ? sv[j] : -INFINITY);
-                    }
-                    const float mnew = fmaxf(m, mx * p.score_scale);
-                    const bool grow = m != -INFINITY && mnew > m + 8.f;
-                    if (__any_sync(0xffffffffu, grow)) {
-                        // rows whose maximum grew: O_team *= 2^(m - mnew) (its last P.V is done)
-                        tc_fence_after();
-                        const float alpha = grow ? ex2(m - mnew) : 1.f;
-#pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) {
-                            float o[32];
-                            tmem_ld32(tmem + lane_base + o_col + 32 * cc, o);
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) o[j] *= alpha;
-                            tmem_st32(tmem + lane_base + o_col + 32 * cc, o);
-                        }
-                        l *= alpha;
-                    }
-                    if (grow || m == -INFINITY) m = mnew;
-                    // ---- P = 2^(s * scale - m) (0 where not visible) as bf16 high part (the top 16
-                    //      bits) and low part (the rest, rounded), row r of P[buf]
-                    const float nm = -m;
-                    uint8_t *pr = smem + L::kPOff + buf * kPBuf + (r >> 3) * 1024 + (r & 7) * 16;
-                    float ls = 0.f;
-#pragma unroll
-                    for (int kc = 0; kc < 8; ++kc) {
-                        uint32_t hw[4], lw[4];
+                    for (int k = 0; k < 8; ++k)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int j = 8 * kc + 2 * e;
-                            float p0 = ex2(fmaf(sv[j], p.score_scale, nm));
-                            float p1 = ex2(fmaf(sv[j + 1], p.score_scale, nm));
-                            if (vis < kTile) {
-                                p0 = j < vis ? p0 : 0.f;
-                                p1 = j + 1 < vis ? p1 : 0.f;
-                            }
-                            ls += p0 + p1;
-                            const uint32_t h0 = __float_as_uint(p0) & 0xFFFF0000u, h1 = __float_as_uint(p1) & 0xFFFF0000u;
-                            hw[e] = prmt(h0, h1, 0x7632u);
-                            lw[e] = pack_bf16x2(p0 - __uint_as_float(h0), p1 - __uint_as_float(h1));
+                            const int h = e >> 1, j = 8 * k + 2 * tig + (e & 1);
+                            mx[h] = fmaxf(mx[h], (full || j < vis[h]) ? sv[k][e] : -INFINITY);
                         }
-                        if (own) {
-                            *reinterpret_cast<uint4 *>(pr + kc * 128) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                            *reinterpret_cast<uint4 *>(pr + kPBuf / 2 + kc * 128) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                        }
+                    bool grow[2];
+                    float alpha[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+                        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+                        const float mnew = fmaxf(m[h], mx[h] * p.score_scale);
+                        grow[h] = m[h] != -INFINITY && mnew > m[h] + 8.f;
+                        alpha[h] = grow[h] ? ex2(m[h] - mnew) : 1.f;
+                        if (grow[h] || m[h] == -INFINITY) m[h] = mnew;
                     }
-                    l += ls;
+                    if (__any_sync(0xffffffffu, grow[0] || grow[1])) {
+                        // rows whose maximum grew: O_team *= 2^(m_old - m_new) (its last P.V is done)
+                        tc_fence_after();
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            float o[8][4];
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + o_col + 64 * half + 8 * k, o[k]);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                o[k][0] *= alpha[0];
+                                o[k][1] *= alpha[0];
+                                o[k][2] *= alpha[1];
+                                o[k][3] *= alpha[1];
+                                tmem_st16x8(tmem + lane_base + o_col + 64 * half + 8 * k, o[k]);
+                            }
+                            tmem_wait_st();
+                        }
+                        l[0] *= alpha[0];
+                        l[1] *= alpha[1];
+                    }
+                    // ---- P = 2^(s * scale - m) (0 where not visible) as bf16 high part (the top 16
+                    //      bits) and low part (the rest, rounded) into P[buf]: row r, tokens
+                    //      8 k .. 8 k + 7 at (r / 8) * 1024 + k * 128 + (r % 8) * 16
+                    uint8_t *pa_ = smem + L::kPOff + buf * kPBuf + (ra >> 3) * 1024 + (ra & 7) * 16 + 4 * tig;
+                    uint8_t *pb_ = smem + L::kPOff + buf * kPBuf + (rb >> 3) * 1024 + (rb & 7) * 16 + 4 * tig;
+                    const float nm0 = -m[0], nm1 = -m[1];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        float pv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int h = e >> 1, j = 8 * k + 2 * tig + (e & 1);
+                            const float q = ex2(fmaf(sv[k][e], p.score_scale, h ? nm1 : nm0));
+                            pv[e] = (full || j < vis[h]) ? q : 0.f;
+                        }
+                        l[0] += pv[0] + pv[1];
+                        l[1] += pv[2] + pv[3];
+                        const uint32_t h0 = __float_as_uint(pv[0]) & 0xFFFF0000u, h1 = __float_as_uint(pv[1]) & 0xFFFF0000u;
+                        const uint32_t h2 = __float_as_uint(pv[2]) & 0xFFFF0000u, h3 = __float_as_uint(pv[3]) & 0xFFFF0000u;
+                        *reinterpret_cast<uint32_t *>(pa_ + k * 128) = prmt(h0, h1, 0x7632u);
+                        *reinterpret_cast<uint32_t *>(pb_ + k * 128) = prmt(h2, h3, 0x7632u);
+                        *reinterpret_cast<uint32_t *>(pa_ + kPBuf / 2 + k * 128) =
+                            pack_bf16x2(pv[0] - __uint_as_float(h0), pv[1] - __uint_as_float(h1));
+                        *reinterpret_cast<uint32_t *>(pb_ + kPBuf / 2 + k * 128) =
+                            pack_bf16x2(pv[2] - __uint_as_float(h2), pv[3] - __uint_as_float(h3));
+                    }
                     // ---- V rows past the request's length are zeroed (stale or NaN slots of the page)
                     if (nv < kTile) {
                         uint8_t *vt = smem + stage * L::kStageBytes + C::kTileBytes;
@@ -992,26 +1006,39 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                     tc_fence_after();
                 }
                 // ---- this team's partial (slot 2 x descriptor + team): O_t / l, lse = ln(2) (m + log2 l)
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                const float lse = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
-                float *dst = p.partial_o + ((2 * static_cast<int64_t>(slot) + team) * R + r) * kHeadDim;
+                float inv[2], lse[2];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    float o[32];
+                for (int h = 0; h < 2; ++h) {
+                    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+                    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+                    inv[h] = l[h] > 0.f ? 1.f / l[h] : 0.f;
+                    lse[h] = l[h] > 0.f ? (m[h] + lg2(l[h])) * kLn2 : -INFINITY;
+                }
+                const int64_t slot_row = (2 * static_cast<int64_t>(slot) + team) * R;
+                float *dst_a = p.partial_o + (slot_row + ra) * kHeadDim + 2 * tig;
+                float *dst_b = p.partial_o + (slot_row + rb) * kHeadDim + 2 * tig;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float o[8][4];
                     if (pv_desc > 0) {
-                        tmem_ld32(tmem + lane_base + o_col + 32 * cc, o);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + o_col + 64 * half + 8 * k, o[k]);
+                        tmem_wait_ld();
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = 0.f;
+                        for (int k = 0; k < 8; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
                     }
-                    if (valid) {
 #pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4)
-                            *reinterpret_cast<float4 *>(dst + 32 * cc + 4 * q4) =
-                                make_float4(o[4 * q4] * inv, o[4 * q4 + 1] * inv, o[4 * q4 + 2] * inv, o[4 * q4 + 3] * inv);
+                    for (int k = 0; k < 8; ++k) {
+                        const int col = 64 * half + 8 * k;
+                        if (ra < R) *reinterpret_cast<float2 *>(dst_a + col) = make_float2(o[k][0] * inv[0], o[k][1] * inv[0]);
+                        if (rb < R) *reinterpret_cast<float2 *>(dst_b + col) = make_float2(o[k][2] * inv[1], o[k][3] * inv[1]);
                     }
                 }
-                if (valid) p.partial_lse[(2 * static_cast<int64_t>(slot) + team) * R + r] = lse;
+                if (tig == 0) {
+                    if (ra < R) p.partial_lse[slot_row + ra] = lse[0];
+                    if (rb < R) p.partial_lse[slot_row + rb] = lse[1];
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(o_free(team));
