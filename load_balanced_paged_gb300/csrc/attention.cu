@@ -113,18 +113,14 @@ struct Layout {
     static constexpr int kOStride = 132;  // floats per head row of a warp's O (padding avoids bank conflicts)
     static constexpr int kWarpFloats = kMaxGroup * kOStride + 2 * kMaxGroup;
     static constexpr int kPairFloats = 8 * QW * kOStride + 2 * 8 * QW;  // one column set's second half
-    // QW = 3: Q as the MMA's A operand (64 rows x 128, no swizzle, K-major: 8-row x 16-byte
-    // core matrices, 128 B apart along K, 2 KB apart along rows), two buffers; then P (64
-    // rows x 64 tokens, same form, 1 KB between row groups) as bf16 high and low parts, two
-    // buffers of 16 KB.
+    // QW = 3: Q as the MMA's A operand (64 rows x 128, K-major with the 128-byte swizzle, two
+    // 64-column halves of 8 KB, as the TMA lays out a K tile), two buffers.
     static constexpr int kQcOff = kQOff + kQSlots * kQSlot;
     static constexpr int kQcBytes = kTc ? 2 * kMaxRows * kHeadDim * 2 : 0;
-    static constexpr int kPOff = kQcOff + kQcBytes;
-    static constexpr int kPBytes = kTc ? 2 * 2 * kMaxRows * kTile * 2 : 0;
-    static constexpr int kMergeOff = kPOff + kPBytes;
+    static constexpr int kMergeOff = kQcOff + kQcBytes;
     static constexpr int kMergeSlot = kTc ? 0 : (QW ? 4 * kPairFloats : kNcw * kWarpFloats);  // floats per merge slot
     static constexpr int kMergeBars = kTc ? 0 : (QW ? 4 : 2);  // merge_full / merge_done barriers each
-    static constexpr int kTcBars = kTc ? 14 : 0;  // s_full, s_free, p_full, o_free, qc_full, qc_free, p_free x2
+    static constexpr int kTcBars = kTc ? 22 : 0;  // s_full, s_free, p_full x4; o_done, o_free, qc_full, qc_free, qd_full x2
     static constexpr int kBarOff = kMergeOff + MSLOTS * kMergeSlot * 4;
     // full, empty, qfull, qempty, merge_full, merge_done, epi_ready, epi_free, tensor-core barriers
     static constexpr int kNumBars = 2 * STAGES + 2 * kQSlots + 2 * kMergeBars + 2 * kEpiRing + kTcBars;
@@ -136,7 +132,7 @@ struct Layout {
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static_assert(MSLOTS == 1 || MSLOTS == 2, "merge slots");
     static_assert(QW == 0 || (MSLOTS == 1 && GROUPS == 2), "multi-token shapes");
-    static_assert(!kTc || (KV == 0 && kQcOff % 1024 == 0 && kPOff % 1024 == 0), "tensor-core operand buffers");
+    static_assert(!kTc || (KV == 0 && kQcOff % 1024 == 0), "tensor-core operand buffers");
     // Each stage must be consumed by one group only: a group then meets the phases of its
     // stages' full barriers in order.  With stages shared by two groups, one group could wait
     // for phase k+1 while phase k is still pending, pass the parity test early and arrive on
@@ -338,13 +334,14 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
     auto epi_ready = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 2 * MB + s); };
     auto epi_free = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 2 * MB + kEpiRing + s); };
     const uint32_t tc_bar0 = bar0 + 8u * (2 * STAGES + 2 * kQSlots + 2 * MB + 2 * kEpiRing);
-    auto s_full = [&](int b) { return tc_bar0 + 8u * b; };
-    auto s_free = [&](int b) { return tc_bar0 + 8u * (2 + b); };
-    auto p_full = [&](int b) { return tc_bar0 + 8u * (4 + b); };
-    auto o_free = [&](int t) { return tc_bar0 + 8u * (6 + t); };
-    auto qc_full = [&](int b) { return tc_bar0 + 8u * (8 + b); };
-    auto qc_free = [&](int b) { return tc_bar0 + 8u * (10 + b); };
-    auto p_free = [&](int b) { return tc_bar0 + 8u * (12 + b); };
+    auto s_full = [&](int b) { return tc_bar0 + 8u * b; };         // 4 S/P buffers
+    auto s_free = [&](int b) { return tc_bar0 + 8u * (4 + b); };
+    auto p_full = [&](int b) { return tc_bar0 + 8u * (8 + b); };
+    auto o_done = [&](int t) { return tc_bar0 + 8u * (12 + t); };  // 2 softmax teams
+    auto o_free = [&](int t) { return tc_bar0 + 8u * (14 + t); };
+    auto qc_full = [&](int b) { return tc_bar0 + 8u * (16 + b); };
+    auto qc_free = [&](int b) { return tc_bar0 + 8u * (18 + b); };
+    auto qd_full = [&](int b) { return tc_bar0 + 8u * (20 + b); };  // plain Q rows landed
     EpiRecord *epi_rec = reinterpret_cast<EpiRecord *>(smem + L::kEpiOff);
     volatile int *epi_total = reinterpret_cast<volatile int *>(smem + L::kEpiOff + kEpiRing * sizeof(EpiRecord));
     int *nvalid = reinterpret_cast<int *>(smem + L::kNValidOff);
@@ -364,16 +361,18 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
             mbar_init(qempty_bar(s), QW == 3 ? NCW + 2 : NCW);  // every warp that reads the hand-off
         }
         if (QW == 3) {
+            for (int b = 0; b < 4; ++b) {
+                mbar_init(s_full(b), 1);  // S warp
+                mbar_init(s_free(b), 1);  // PV warp: the buffer's P has been read
+                mbar_init(p_full(b), 4);  // the owning softmax team
+            }
             for (int b = 0; b < 2; ++b) {
-                mbar_init(s_full(b), 1);
-                mbar_init(s_free(b), 4);  // one softmax team per buffer
-                mbar_init(p_full(b), 4);
+                mbar_init(o_done(b), 1);
+                mbar_init(o_free(b), 4);
                 mbar_init(qc_full(b), 1);
                 mbar_init(qc_free(b), 1);
-                mbar_init(p_free(b), 1);
+                mbar_init(qd_full(b), 1);
             }
-            mbar_init(o_free(0), 4);
-            mbar_init(o_free(1), 4);
         } else if (QW) {
             for (int s = 0; s < MB; ++s) {  // per column set: second half deposited / read
                 mbar_init(merge_full(s), 1);
@@ -575,15 +574,19 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                                 for (int g = 0; g < kMaxGroup; ++g) inf->qscale[g] = qs[g];
                                 // the G query rows of each of the request's q_len query tokens,
                                 // one after the other (row i*G + g)
-                                const uint32_t bytes = G * C::kQHeadBytes;
-                                mbar_arrive_expect_tx(qfull_bar(qs_), bytes * p.q_len);
-                                for (int i = 0; i < p.q_len; ++i) {
-                                    const uint8_t *src =
-                                        p.q + ((static_cast<int64_t>(b) * p.q_len + i) * p.hq + h * G) * C::kQHeadBytes;
-                                    bulk_load(sbase + L::kQOff + qs_ * L::kQSlot + i * bytes, src, bytes,
-                                              qfull_bar(qs_));
+                                if (QW == 3) {  // the S warp fetches Q itself, a descriptor ahead
+                                    mbar_arrive(qfull_bar(qs_));
+                                } else {
+                                    const uint32_t bytes = G * C::kQHeadBytes;
+                                    mbar_arrive_expect_tx(qfull_bar(qs_), bytes * p.q_len);
+                                    for (int i = 0; i < p.q_len; ++i) {
+                                        const uint8_t *src = p.q + ((static_cast<int64_t>(b) * p.q_len + i) * p.hq + h * G) *
+                                                                       C::kQHeadBytes;
+                                        bulk_load(sbase + L::kQOff + qs_ * L::kQSlot + i * bytes, src, bytes,
+                                                  qfull_bar(qs_));
+                                    }
+                                    q_issued = qi;
                                 }
-                                q_issued = qi;
                             }
                         }
                         ++qi;
@@ -719,7 +722,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
         const int R = p.q_len * G;
         uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kAbortOff + 4);
         constexpr int kTcThreads = (NCW + 2) * 32;  // softmax warps, S warp, PV warp
-        constexpr uint32_t kQcBuf = kMaxRows * kHeadDim * 2, kPBuf = 2 * kMaxRows * kTile * 2;
+        constexpr uint32_t kQcBuf = kMaxRows * kHeadDim * 2;
         if (warp == NCW + 1) tmem_alloc(smem_u32(tmem_slot), 512);
         tc_fence_before();
         named_bar_sync(1, kTcThreads);
@@ -730,10 +733,50 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
         bool failed = false;
 
         if (warp == NCW + 1) {
-            // ---- S warp: lays each descriptor's Q out as the A operand (zero past R), then
+            // ---- S warp: fetches each descriptor's Q rows one descriptor ahead (plain rows
+            //      into one of two buffers), lays them out as the A operand (zero past R), then
             //      issues S = Q K^T for its tiles as soon as a stage and an S buffer are ready
             //      (lane 0 issues, the warp waits together); its commit on the stage's empty
             //      barrier says the K half is no longer read
+            // descriptors of this CTA, 32 at a time: lane j holds the unit of descriptor wbase + j
+            // if the producer hands it over (valid, with tiles), else -1
+            int wbase = 0, wu = -1;
+            auto load_window = [&](int base) {
+                wbase = base;
+                wu = -1;
+                if (base + lane < d_count) {
+                    const int4 v = p.descs[d_begin + base + lane];
+                    if (v.x >= 0 && v.x < p.num_units && v.y >= 0 && v.y < v.z && d_begin + base + lane < p.max_slots)
+                        wu = v.x;
+                }
+            };
+            load_window(0);
+            auto next_desc = [&](int after) {  // the next handed-over descriptor (raw slot) after `after`
+                for (int rel = after - d_begin + 1; rel < d_count;) {
+                    if (rel < wbase || rel >= wbase + 32) load_window(rel & ~31);
+                    const uint32_t m = __ballot_sync(0xffffffffu, wu >= 0) & (~0u << (rel - wbase));
+                    if (m) return d_begin + wbase + __ffs(m) - 1;
+                    rel = wbase + 32;
+                }
+                return -1;
+            };
+            int fetched[2] = {0, 0};  // Q copies issued into each plain buffer (each one waited for)
+            auto fetch_q = [&](int x, int j) {  // x in the current window
+                const int u = __shfl_sync(0xffffffffu, wu, x - d_begin - wbase);
+                if (lane == 0) {
+                    const int b = u / p.hkv, h = u - b * p.hkv;
+                    const uint32_t bytes = G * C::kQHeadBytes;
+                    mbar_arrive_expect_tx(qd_full(j), bytes * p.q_len);
+                    for (int i = 0; i < p.q_len; ++i)
+                        bulk_load(sbase + L::kQOff + j * L::kQSlot + i * bytes,
+                                  p.q + ((static_cast<int64_t>(b) * p.q_len + i) * p.hq + h * G) * C::kQHeadBytes, bytes,
+                                  qd_full(j));
+                }
+                ++fetched[j];
+            };
+            auto land_q = [&](int j) { return wait_phase(qd_full(j), (fetched[j] - 1) & 1, abort_flag, p.status); };
+            int pf_slot = next_desc(d_begin - 1), pf_buf = 0;  // the descriptor whose Q is in flight
+            if (pf_slot >= 0) fetch_q(pf_slot, 0);
             int g = 0, last_d = -1;
             for (int d = 0;; ++d) {
                 const int qslot = d % kQSlots;
@@ -742,30 +785,59 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                     break;
                 }
                 const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
-                const int end = inf->end, n = inf->n, c_start = inf->c_start;
+                const int end = inf->end, n = inf->n, c_start = inf->c_start, xs = inf->slot;
                 if (!end) {
-                    if (!wait_phase(qc_free(d & 1), ((d >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                    // this descriptor's Q: normally the prefetched one; otherwise fetched now
+                    const int qb = pf_buf;
+                    if (pf_slot != xs) {
+                        if (pf_slot >= 0 && !land_q(qb)) {
+                            failed = true;
+                            break;
+                        }
+                        if (xs < d_begin + wbase || xs >= d_begin + wbase + 32) load_window((xs - d_begin) & ~31);
+                        fetch_q(xs, qb);
+                    }
+                    if (!land_q(qb) || !wait_phase(qc_free(d & 1), ((d >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                        pf_slot = -1;  // consumed (or abandoned with the CTA)
                         failed = true;
                         break;
                     }
-                    const uint8_t *src = smem + L::kQOff + qslot * L::kQSlot;
+                    // 128-byte-swizzled K-major operand (as the TMA lays out K): dims 64 b .. 64 b + 63
+                    // of row r at b * 8 KB + r * 128 B, 16-byte chunk c at (c ^ (r % 8)) * 16.  Each
+                    // quarter-warp writes one 128-byte row: no bank conflicts either way.
+                    const uint8_t *src = smem + L::kQOff + qb * L::kQSlot;
                     uint8_t *dst = smem + L::kQcOff + (d & 1) * kQcBuf;
-                    for (int i = lane; i < kMaxRows * 16; i += 32) {  // 16-byte chunk kc of row r
-                        const int r = i >> 4, kc = i & 15;
-                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                        if (r < R) v = *reinterpret_cast<const uint4 *>(src + r * (kHeadDim * 2) + kc * 16);
-                        *reinterpret_cast<uint4 *>(dst + (r >> 3) * 2048 + kc * 128 + (r & 7) * 16) = v;
+#pragma unroll
+                    for (int rd = 0; rd < 4; ++rd) {
+                        uint4 v[8];
+#pragma unroll
+                        for (int it = 0; it < 8; ++it) {  // chunk kc of row r
+                            const int i = lane + 32 * (8 * rd + it), r = i >> 4, kc = i & 15;
+                            v[it] = r < R ? *reinterpret_cast<const uint4 *>(src + r * (kHeadDim * 2) + kc * 16)
+                                          : make_uint4(0u, 0u, 0u, 0u);
+                        }
+#pragma unroll
+                        for (int it = 0; it < 8; ++it) {
+                            const int i = lane + 32 * (8 * rd + it), r = i >> 4, kc = i & 15;
+                            *reinterpret_cast<uint4 *>(dst + (kc >> 3) * 8192 + r * 128 + (((kc & 7) ^ (r & 7)) << 4)) = v[it];
+                        }
                     }
                     fence_proxy_async_smem();
+                    // the next descriptor's Q lands while this one's tiles are worked on
+                    pf_slot = next_desc(xs);
+                    if (pf_slot >= 0) {
+                        pf_buf = qb ^ 1;
+                        fetch_q(pf_slot, pf_buf);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qempty_bar(qslot));
                 if (end) break;
                 const uint32_t qa = sbase + L::kQcOff + (d & 1) * kQcBuf;
                 for (int li = 0; li < n; ++li, ++g) {
-                    const int c = c_start + li, stage = c % STAGES, buf = g & 1;
+                    const int c = c_start + li, stage = c % STAGES, buf = g & 3;
                     if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status) ||
-                        !wait_phase(s_free(buf), ((g >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                        !wait_phase(s_free(buf), ((g >> 2) & 1) ^ 1, abort_flag, p.status)) {
                         failed = true;
                         break;
                     }
@@ -776,7 +848,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                             const uint32_t kb = sbase + stage * L::kStageBytes;
 #pragma unroll
                             for (int ks = 0; ks < 8; ++ks)
-                                umma_bf16(tmem + 64 * buf, umma_desc(qa + ks * 256, 128, 2048, 0),
+                                umma_bf16(tmem + 64 * buf, umma_desc(qa + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, 2),
                                           umma_desc(kb + (ks >> 2) * (C::kTileBytes / 2) + (ks & 3) * 32, 16, 1024, 2),
                                           kIdS, ks > 0);
                             umma_commit(s_full(buf));
@@ -793,8 +865,13 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 __syncwarp();
                 last_d = d;
             }
-            // the last commit lands once every product this warp issued has completed
+            // the last commit lands once every product this warp issued has completed; a Q copy
+            // still in flight lands before the CTA leaves
             if (!failed && last_d >= 0) wait_phase(qc_free(last_d & 1), (last_d >> 1) & 1, abort_flag, p.status);
+            if (pf_slot >= 0) {
+                const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+                drain_phase(qd_full(pf_buf), (fetched[pf_buf] - 1) & 1, deadline);
+            }
         } else if (warp == NCW + 2) {
             // ---- PV warp: O += P_hi . V + P_lo . V as soon as the softmax warps hand P over;
             //      its commit on the stage's empty barrier says the V half is no longer read
@@ -812,38 +889,38 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 if (end) break;
                 bool first_pv[2] = {true, true};  // per softmax team (tile parity): O_t not yet written
                 for (int li = 0; li < n; ++li, ++g) {
-                    const int c = c_start + li, stage = c % STAGES, pb = g & 1;
+                    const int c = c_start + li, stage = c % STAGES, buf = g & 3, t = g & 1;
                     if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status) ||
-                        !wait_phase(p_full(pb), (g >> 1) & 1, abort_flag, p.status)) {
+                        !wait_phase(p_full(buf), (g >> 2) & 1, abort_flag, p.status)) {
                         failed = true;
                         break;
                     }
                     const int nv = nvalid[stage];
                     if (nv > 0) {
                         // O_t is free once team t has read out the previous descriptor's
-                        if (first_pv[pb] && !wait_phase(o_free(pb), (d & 1) ^ 1, abort_flag, p.status)) {
+                        if (first_pv[t] && !wait_phase(o_free(t), (d & 1) ^ 1, abort_flag, p.status)) {
                             failed = true;
                             break;
                         }
                         if (lane == 0) {
                             tc_fence_after();
                             const uint32_t vb = sbase + stage * L::kStageBytes + C::kTileBytes;
-                            const uint32_t pa = sbase + L::kPOff + pb * kPBuf;
-                            const uint32_t od = tmem + 128 + 128 * pb;
+                            const uint32_t pt = tmem + 64 * buf;  // P high part: columns 0-31, low part: 32-63
+                            const uint32_t od = tmem + 256 + 128 * t;
 #pragma unroll
                             for (int ks = 0; ks < 4; ++ks) {
                                 const uint64_t bd = umma_desc(vb + ks * 2048, 8192, 1024, 2);
-                                umma_bf16(od, umma_desc(pa + ks * 256, 128, 1024, 0), bd, kIdO, !(first_pv[pb] && ks == 0));
-                                umma_bf16(od, umma_desc(pa + kPBuf / 2 + ks * 256, 128, 1024, 0), bd, kIdO, true);
+                                umma_bf16_ta(od, pt + 8 * ks, bd, kIdO, !(first_pv[t] && ks == 0));
+                                umma_bf16_ta(od, pt + 32 + 8 * ks, bd, kIdO, true);
                             }
-                            umma_commit(p_free(pb));
-                            umma_commit(empty_bar(stage));
                         }
-                        first_pv[pb] = false;
-                    } else if (lane == 0) {
-                        // a commit, not an arrive: its phase also means every earlier product is done
-                        umma_commit(p_free(pb));
-                        mbar_arrive(empty_bar(stage));
+                        first_pv[t] = false;
+                    }
+                    // commits, not arrives: a phase also means every earlier product is done
+                    if (lane == 0) {
+                        umma_commit(o_done(t));
+                        umma_commit(s_free(buf));
+                        umma_commit(empty_bar(stage));
                     }
                     __syncwarp();
                 }
@@ -851,7 +928,8 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
             }
         } else {
             // ---- softmax warps: two teams of four (team t = warps 4t .. 4t + 3) take the tiles
-            //      of parity t (S[t], P[t], O_t).  Warp w reads the 16 rows 16 (w & 3) .. + 15
+            //      of parity t (S/P buffers t and t + 2 in turn, O_t).  Warp w reads the 16 rows
+            //      16 (w & 3) .. + 15
             //      (M = 64 accumulators: lanes 0-15 of each sub-partition) as m16n8 fragments:
             //      thread (gid = lane / 4, tig = lane % 4) holds rows ra = 16 (w & 3) + gid and
             //      rb = ra + 8, columns 8 k + 2 tig, + 1; a row's max and sum combine over the
@@ -861,7 +939,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
             const int gid = lane >> 2, tig = lane & 3;
             const int ra = 16 * sp + gid, rb = ra + 8;
             const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
-            const uint32_t o_col = 128 + 128 * team;
+            const uint32_t o_col = 256 + 128 * team;
             const int tid = sp * 32 + lane;  // within the team
             int g = 0;
             for (int d = 0;; ++d) {
@@ -882,9 +960,9 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 int pv_desc = 0, last_g = -1;
                 for (int li = 0; li < n; ++li, ++g) {
                     if ((g & 1) != team) continue;
-                    const int c = c_start + li, stage = c % STAGES, buf = team;
+                    const int c = c_start + li, stage = c % STAGES, buf = g & 3;
                     if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status) ||
-                        !wait_phase(s_full(buf), (g >> 1) & 1, abort_flag, p.status)) {
+                        !wait_phase(s_full(buf), (g >> 2) & 1, abort_flag, p.status)) {
                         failed = true;
                         break;
                     }
@@ -896,16 +974,15 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + 64 * buf + 8 * k, sv[k]);
                         tmem_wait_ld();
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(s_free(buf));
-                    // P[buf] and O_team were last used by the P.V of this team's previous tile
-                    if (!wait_phase(p_free(buf), ((g >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                    // O_team was last written by the P.V of this team's previous tile
+                    if (!wait_phase(o_done(team), ((g >> 1) & 1) ^ 1, abort_flag, p.status)) {
                         failed = true;
                         break;
                     }
                     last_g = g;
                     if (nv == 0) {  // no data in this stage: the PV warp skips its P.V
+                        tc_fence_before();
+                        __syncwarp();
                         if (lane == 0) mbar_arrive(p_full(buf));
                         continue;
                     }
@@ -955,10 +1032,9 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         l[1] *= alpha[1];
                     }
                     // ---- P = 2^(s * scale - m) (0 where not visible) as bf16 high part (the top 16
-                    //      bits) and low part (the rest, rounded) into P[buf]: row r, tokens
-                    //      8 k .. 8 k + 7 at (r / 8) * 1024 + k * 128 + (r % 8) * 16
-                    uint8_t *pa_ = smem + L::kPOff + buf * kPBuf + (ra >> 3) * 1024 + (ra & 7) * 16 + 4 * tig;
-                    uint8_t *pb_ = smem + L::kPOff + buf * kPBuf + (rb >> 3) * 1024 + (rb & 7) * 16 + 4 * tig;
+                    //      bits) and low part (the rest, rounded), written over S in the buffer: the
+                    //      P.V's A operand, tokens (2c, 2c + 1) packed in column c (high part:
+                    //      columns 0-31, low part: 32-63)
                     const float nm0 = -m[0], nm1 = -m[1];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
@@ -973,13 +1049,12 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         l[1] += pv[2] + pv[3];
                         const uint32_t h0 = __float_as_uint(pv[0]) & 0xFFFF0000u, h1 = __float_as_uint(pv[1]) & 0xFFFF0000u;
                         const uint32_t h2 = __float_as_uint(pv[2]) & 0xFFFF0000u, h3 = __float_as_uint(pv[3]) & 0xFFFF0000u;
-                        *reinterpret_cast<uint32_t *>(pa_ + k * 128) = prmt(h0, h1, 0x7632u);
-                        *reinterpret_cast<uint32_t *>(pb_ + k * 128) = prmt(h2, h3, 0x7632u);
-                        *reinterpret_cast<uint32_t *>(pa_ + kPBuf / 2 + k * 128) =
-                            pack_bf16x2(pv[0] - __uint_as_float(h0), pv[1] - __uint_as_float(h1));
-                        *reinterpret_cast<uint32_t *>(pb_ + kPBuf / 2 + k * 128) =
-                            pack_bf16x2(pv[2] - __uint_as_float(h2), pv[3] - __uint_as_float(h3));
+                        tmem_st16x4(tmem + lane_base + 64 * buf + 4 * k, prmt(h0, h1, 0x7632u), prmt(h2, h3, 0x7632u));
+                        tmem_st16x4(tmem + lane_base + 64 * buf + 32 + 4 * k,
+                                    pack_bf16x2(pv[0] - __uint_as_float(h0), pv[1] - __uint_as_float(h1)),
+                                    pack_bf16x2(pv[2] - __uint_as_float(h2), pv[3] - __uint_as_float(h3)));
                     }
+                    tmem_wait_st();
                     // ---- V rows past the request's length are zeroed (stale or NaN slots of the page)
                     if (nv < kTile) {
                         uint8_t *vt = smem + stage * L::kStageBytes + C::kTileBytes;
@@ -999,7 +1074,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 // ---- this team's products of the descriptor are done once its last tile's buffer
                 //      phase is (that commit covers every earlier product)
                 if (last_g >= 0) {
-                    if (!wait_phase(p_free(team), (last_g >> 1) & 1, abort_flag, p.status)) {
+                    if (!wait_phase(o_done(team), (last_g >> 1) & 1, abort_flag, p.status)) {
                         failed = true;
                         break;
                     }
@@ -1017,31 +1092,28 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 const int64_t slot_row = (2 * static_cast<int64_t>(slot) + team) * R;
                 float *dst_a = p.partial_o + (slot_row + ra) * kHeadDim + 2 * tig;
                 float *dst_b = p.partial_o + (slot_row + rb) * kHeadDim + 2 * tig;
+                // O_t into registers first, then release it for the next descriptor's products
+                float o[16][4];
+                if (pv_desc > 0) {
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float o[8][4];
-                    if (pv_desc > 0) {
+                    for (int k = 0; k < 16; ++k) tmem_ld16x8(tmem + lane_base + o_col + 8 * k, o[k]);
+                    tmem_wait_ld();
+                } else {
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + o_col + 64 * half + 8 * k, o[k]);
-                        tmem_wait_ld();
-                    } else {
+                    for (int k = 0; k < 16; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_free(team));
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
-                    }
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int col = 64 * half + 8 * k;
-                        if (ra < R) *reinterpret_cast<float2 *>(dst_a + col) = make_float2(o[k][0] * inv[0], o[k][1] * inv[0]);
-                        if (rb < R) *reinterpret_cast<float2 *>(dst_b + col) = make_float2(o[k][2] * inv[1], o[k][3] * inv[1]);
-                    }
+                for (int k = 0; k < 16; ++k) {
+                    if (ra < R) *reinterpret_cast<float2 *>(dst_a + 8 * k) = make_float2(o[k][0] * inv[0], o[k][1] * inv[0]);
+                    if (rb < R) *reinterpret_cast<float2 *>(dst_b + 8 * k) = make_float2(o[k][2] * inv[1], o[k][3] * inv[1]);
                 }
                 if (tig == 0) {
                     if (ra < R) p.partial_lse[slot_row + ra] = lse[0];
                     if (rb < R) p.partial_lse[slot_row + rb] = lse[1];
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(o_free(team));
             }
         }
         (void)failed;
@@ -1728,6 +1800,9 @@ KernelParams base_params(const AttnArgs &a, float *partial_o, float *partial_lse
 // merge slot with the same or deeper rings.)
 constexpr int kPersistStagesBf16 = 4, kPersistStagesFp8 = 8, kPersistGroups = 2, kPersistMergeSlots = 2;
 constexpr int kPairStagesBf16 = 2, kPairStagesFp8 = 4, kPairGroups = 1;
+// The multi-token tensor-memory kernel keeps P in tensor memory, so its shared memory holds a
+// fifth stage (tiles stay in the ring from their load until their P.V, several microseconds).
+constexpr int kTcStages = 5;
 
 // Persistent launch: the CTA shape that keeps all of the map's bins resident at once.
 template <int KV, bool FUSE>
@@ -1810,7 +1885,7 @@ extern "C" dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q
     // the tensor-memory kernel (measured faster from 24 rows up, slower at 16)
     if (kp.slots_per_desc == 1)
         return launch<0, kPersistStagesBf16, kPersistGroups, true, false, 1, 1>(a, kp, grid, to_cuda(stream));
-    return launch<0, kPersistStagesBf16, 2, true, false, 1, 3>(a, kp, grid, to_cuda(stream));
+    return launch<0, kTcStages, 2, true, false, 1, 3>(a, kp, grid, to_cuda(stream));
 }
 
 extern "C" dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_scale, const void *k_pages,

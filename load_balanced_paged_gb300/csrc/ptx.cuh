@@ -111,6 +111,17 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t 
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] . B[smem]; A (M x K bf16) in tensor memory: row r in the lane of an
+// M = 64 accumulator row, K elements packed in pairs per 32-bit column.  Issued by one thread.
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                             bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+        : "memory");
+}
+
 // Arrive (once) on an mbarrier when every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -184,6 +195,12 @@ __device__ __forceinline__ void tmem_st16x8(uint32_t taddr, const float (&v)[4])
     asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
                  "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
                  "r"(__float_as_uint(v[3]))
+                 : "memory");
+}
+
+// 16 TMEM lanes x 4 columns over the warp: thread t writes lanes t/4 and t/4 + 8, column t%4.
+__device__ __forceinline__ void tmem_st16x4(uint32_t taddr, uint32_t lo_lane, uint32_t hi_lane) {
+    asm volatile("tcgen05.st.sync.aligned.16x128b.x1.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(lo_lane), "r"(hi_lane)
                  : "memory");
 }
 
