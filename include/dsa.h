@@ -196,8 +196,9 @@ dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_sca
 
 /*
  * dsa_decode_multi -- dsa_decode for q_len query tokens per request (a multi-token
- * verify step: the Hy3 write-up's MTP section, and the GB300 low-latency write-up's
- * verify of 1 + 5 draft tokens in one pass).  The task map, the scheduler and the KV
+ * verify step: Hy3 preview write-up 2.5 "MTP与异步调度优化"; SGLang Low-Latency Mode:
+ * Kernels and Runtime (paper-daily.com), section 1, a verify of 1 + 5 draft tokens
+ * in one pass).  The task map, the scheduler and the KV
  * stream are those of dsa_decode: each KV tile is read once and serves all q_len * G
  * query rows of its unit.  Query token i of request b stands at position
  * seq_lens[b] - q_len + i and sees the tokens t <= that position (causal within the

@@ -238,8 +238,9 @@ typedef struct {
  * the tokens [tok0, tok1) of that request, for each of the request's q_len query
  * tokens.  Query token i (0 <= i < q_len) stands at position len_b - q_len + i
  * and sees the tokens t <= that position (causal within the draft of a
- * multi-token verify step; the Hy3 write-up's MTP section, and the GB300
- * low-latency write-up's verify step of 1 + 5 draft tokens), so its range is
+ * multi-token verify step: Hy3 preview write-up 2.5 "MTP与异步调度优化"; SGLang
+ * Low-Latency Mode: Kernels and Runtime, section 1, a verify of 1 + 5 draft
+ * tokens), so its range is
  * [tok0, min(tok1, len_b - q_len + i + 1)):
  *   s_t = sm_scale * sum_k Q[b, i, j, k] * K[t, k]          (j = h*G .. h*G+G-1)
  *   o = sum_t exp(s_t - M) V[t, :] / sum_t exp(s_t - M), M = max_t s_t
