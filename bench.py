@@ -321,7 +321,8 @@ def bench_ours(args, device, rank, world):
                          "speedup_of_dynamic_with_plan": round(s_ms / ms_per_step, 3)}
 
     prologue = bench_prologue(dsa, device, w, B, timed, max(10, min(args.steps, 200)))
-    multi = bench_multi(dsa, device, inp, w, C, m, timed, max(10, min(args.steps, 200)), nbytes, ms_per_step)
+    # multi-token steps use one bin per SM: the tensor-memory kernel holds one CTA per SM
+    multi = bench_multi(dsa, device, inp, w, sms, m, timed, max(10, min(args.steps, 200)), nbytes, ms_per_step)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     host = {k: inp[k].cpu().pin_memory() for k in ("q", "q_scale", "k_pages", "v_pages", "k_scale", "v_scale",
@@ -442,7 +443,7 @@ def bench_prologue(dsa, device, w, batch: int, timed, steps: int) -> dict:
 
 def bench_multi(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes: int, single_ms: float) -> dict:
     """Multi-token verify steps (q_len query tokens per request, causal within the draft) on
-    this workload's KV: plan -> dsa_decode_multi -> dsa_combine_multi in one graph.  The KV
+    this workload's KV, C bins: plan -> dsa_decode_multi -> dsa_combine_multi in one graph.  The KV
     stream is read once per step whatever q_len is; `vs_q_len_one_token_steps` compares with
     q_len separate one-token steps (q_len x the one-token step time)."""
     if w.kv_dtype != "bf16":
