@@ -64,7 +64,7 @@ def lib():
             common = [_vp, ctypes.c_int32, _f32p, _vp, _vp, ctypes.c_int32, _f32p, _f32p,
                       _i32p, ctypes.c_int32, ctypes.c_int32, _i32p, ctypes.c_int32,
                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                      ctypes.c_double, ctypes.c_int32]
+                      ctypes.c_double, ctypes.c_int32, ctypes.c_int32]
             L.oracle_attention_span.argtypes = common + [ctypes.c_int32, ctypes.c_int32,
                                                          ctypes.c_int64, ctypes.c_int64, _f64p, _f64p]
             L.oracle_attention_span.restype = ctypes.c_int
@@ -139,7 +139,8 @@ class Problem:
     positions of the request, each seeing the tokens up to its own position."""
 
     def __init__(self, q, k_pages, v_pages, block_table, seq_lens, num_q_heads, num_kv_heads,
-                 sm_scale, q_scale=None, k_scale=None, v_scale=None, head_dim=128, page_size=64, q_len=1):
+                 sm_scale, q_scale=None, k_scale=None, v_scale=None, head_dim=128, page_size=64, q_len=1,
+                 kv_layout=0):
         self.q_dtype = E4M3 if q.dtype == np.uint8 else BF16
         self.kv_dtype = E4M3 if k_pages.dtype == np.uint8 else BF16
         self.q = np.ascontiguousarray(q)
@@ -159,6 +160,7 @@ class Problem:
         self.page_size = int(page_size)
         self.sm_scale = float(sm_scale)
         self.q_len = int(q_len)
+        self.kv_layout = 1 if kv_layout in (1, "NHD") else 0
         if self.q.size != self.batch * self.q_len * self.num_q_heads * self.head_dim:
             raise ValueError("q does not hold B x q_len x Hq x d values")
         if self.q_dtype == E4M3 and self.q_scale is None:
@@ -172,7 +174,7 @@ class Problem:
                 _p(self.k_scale, _f32p), _p(self.v_scale, _f32p),
                 _p(self.block_table, _i32p), self.max_pages, self.num_pages,
                 _p(self.seq_lens, _i32p), self.batch, self.num_q_heads, self.num_kv_heads,
-                self.head_dim, self.page_size, self.sm_scale, self.q_len]
+                self.head_dim, self.page_size, self.sm_scale, self.q_len, self.kv_layout]
 
     @property
     def group(self) -> int:

@@ -231,7 +231,18 @@ typedef struct {
     const int32_t *block_table; int32_t max_pages_per_req; int32_t num_pages;
     const int32_t *seq_lens; int32_t batch; int32_t num_q_heads; int32_t num_kv_heads;
     int32_t head_dim; int32_t page_size; double sm_scale; int32_t q_len;
+    int32_t kv_layout;  /* 0: pages [num_pages][Hkv][P][d] (HND); 1: [num_pages][P][Hkv][d] (NHD) */
 } orc_problem;
+
+/* Element row of (page, KV head, slot) in the K/V pools; the FP8 scales are always laid out
+ * [num_pages][Hkv][P] (scale_row). */
+static int64_t data_row(const orc_problem *p, int64_t page, int32_t h, int64_t slot) {
+    if (p->kv_layout == 1) return (page * p->page_size + slot) * p->num_kv_heads + h;
+    return (page * p->num_kv_heads + h) * p->page_size + slot;
+}
+static int64_t scale_row(const orc_problem *p, int64_t page, int32_t h, int64_t slot) {
+    return (page * p->num_kv_heads + h) * p->page_size + slot;
+}
 
 /*
  * Exact attention of the G query heads of request b that share KV head h, over
@@ -247,7 +258,9 @@ typedef struct {
  *   lse = M + ln sum_t exp(s_t - M)
  * Output row i*G + g.  Token t of request b lives in page block_table[b][t /
  * page_size] at slot t mod page_size; a page holds [Hkv][page_size][d]
- * elements.  FP8 values are decode(byte) * scale: Q scale per (b, i, q head),
+ * elements (kv_layout 0, "HND") or [page_size][Hkv][d] (kv_layout 1, "NHD";
+ * the blog's integration reads the serving runtime's paged KV store without a
+ * layout conversion, and both orders occur there).  FP8 values are decode(byte) * scale: Q scale per (b, i, q head),
  * K/V scale per (page, KV head, slot).  An empty range gives o = 0, lse = -inf.
  * Returns nonzero if a page id is out of range.
  */
@@ -274,8 +287,8 @@ static int span(const orc_problem *p, int32_t b, int32_t h, int64_t tok0, int64_
             for (int64_t t = tok0; t < end; ++t) {
                 int32_t page = p->block_table[(int64_t)b * p->max_pages_per_req + t / P];
                 if (page < 0 || page >= p->num_pages) return 1;
-                int64_t row = ((int64_t)page * p->num_kv_heads + h) * P + (t % P);
-                double ks = (p->kv_dtype == ORC_E4M3) ? (double)p->k_scale[row] : 1.0;
+                int64_t row = data_row(p, page, h, t % P);
+                double ks = (p->kv_dtype == ORC_E4M3) ? (double)p->k_scale[scale_row(p, page, h, t % P)] : 1.0;
                 double dot = 0.0;
                 for (int32_t k = 0; k < d; ++k)
                     dot += load_elem(p->q, p->q_dtype, qbase + k) * qs *
@@ -288,8 +301,8 @@ static int span(const orc_problem *p, int32_t b, int32_t h, int64_t tok0, int64_
             double l = 0.0;
             for (int64_t t = tok0; t < end; ++t) {
                 int32_t page = p->block_table[(int64_t)b * p->max_pages_per_req + t / P];
-                int64_t row = ((int64_t)page * p->num_kv_heads + h) * P + (t % P);
-                double vs = (p->kv_dtype == ORC_E4M3) ? (double)p->v_scale[row] : 1.0;
+                int64_t row = data_row(p, page, h, t % P);
+                double vs = (p->kv_dtype == ORC_E4M3) ? (double)p->v_scale[scale_row(p, page, h, t % P)] : 1.0;
                 double w = exp(scratch[t - tok0] - M);
                 l += w;
                 for (int32_t k = 0; k < d; ++k)
@@ -304,7 +317,8 @@ static int span(const orc_problem *p, int32_t b, int32_t h, int64_t tok0, int64_
 
 static int check_problem(const orc_problem *p) {
     if (p->batch < 0 || p->num_kv_heads < 1 || p->num_q_heads < 1 || p->head_dim < 1 ||
-        p->page_size < 1 || p->num_q_heads % p->num_kv_heads != 0 || p->q_len < 1)
+        p->page_size < 1 || p->num_q_heads % p->num_kv_heads != 0 || p->q_len < 1 ||
+        (p->kv_layout != 0 && p->kv_layout != 1))
         return -1;
     if (p->q_dtype != ORC_BF16 && p->q_dtype != ORC_E4M3) return -1;
     if (p->kv_dtype != ORC_BF16 && p->kv_dtype != ORC_E4M3) return -1;
@@ -318,11 +332,11 @@ int oracle_attention_span(const void *q, int32_t q_dtype, const float *q_scale,
                           const int32_t *block_table, int32_t max_pages_per_req, int32_t num_pages,
                           const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
                           int32_t num_kv_heads, int32_t head_dim, int32_t page_size, double sm_scale,
-                          int32_t q_len, int32_t b, int32_t h, int64_t tok0, int64_t tok1,
+                          int32_t q_len, int32_t kv_layout, int32_t b, int32_t h, int64_t tok0, int64_t tok1,
                           double *out, double *lse) {
     orc_problem p = {q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale,
                      block_table, max_pages_per_req, num_pages, seq_lens, batch,
-                     num_q_heads, num_kv_heads, head_dim, page_size, sm_scale, q_len};
+                     num_q_heads, num_kv_heads, head_dim, page_size, sm_scale, q_len, kv_layout};
     if (check_problem(&p) || b < 0 || b >= batch || h < 0 || h >= num_kv_heads) return -1;
     double *scratch = (double *)malloc(sizeof(double) * (size_t)(tok1 > tok0 ? tok1 - tok0 : 1));
     if (!scratch) return -3;
@@ -384,11 +398,11 @@ int oracle_attention(const void *q, int32_t q_dtype, const float *q_scale,
                      const int32_t *block_table, int32_t max_pages_per_req, int32_t num_pages,
                      const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
                      int32_t num_kv_heads, int32_t head_dim, int32_t page_size, double sm_scale,
-                     int32_t q_len, const int32_t *units, int64_t n_units, int32_t n_threads,
+                     int32_t q_len, int32_t kv_layout, const int32_t *units, int64_t n_units, int32_t n_threads,
                      double *out, double *out_lse) {
     orc_problem p = {q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale,
                      block_table, max_pages_per_req, num_pages, seq_lens, batch,
-                     num_q_heads, num_kv_heads, head_dim, page_size, sm_scale, q_len};
+                     num_q_heads, num_kv_heads, head_dim, page_size, sm_scale, q_len, kv_layout};
     if (check_problem(&p)) return -1;
     if (!units) n_units = (int64_t)batch * num_kv_heads;
     if (n_threads <= 0) n_threads = (int32_t)sysconf(_SC_NPROCESSORS_ONLN);

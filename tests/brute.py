@@ -24,15 +24,25 @@ def values(h: dict, key: str) -> np.ndarray:
     return decode_e4m3(a) if a.dtype == np.uint8 else decode_bf16(a)
 
 
-def dense_attention(h: dict, num_q_heads: int, num_kv_heads: int, sm_scale: float, page: int = 64):
-    q = values(h, "q")
-    if h.get("q_scale") is not None:
-        q = q * h["q_scale"].astype(np.float64)[..., None]
+def hnd_pools(h: dict, layout: str = "HND"):
+    """Decoded K and V pools as [num_pages, Hkv, page, d] (scales applied); an NHD pool
+    [num_pages, page, Hkv, d] is transposed first.  Scales are [num_pages, Hkv, page]."""
     k = values(h, "k_pages")
     v = values(h, "v_pages")
+    if layout == "NHD":
+        k, v = k.transpose(0, 2, 1, 3), v.transpose(0, 2, 1, 3)
     if h.get("k_scale") is not None:
         k = k * h["k_scale"].astype(np.float64)[..., None]
         v = v * h["v_scale"].astype(np.float64)[..., None]
+    return k, v
+
+
+def dense_attention(h: dict, num_q_heads: int, num_kv_heads: int, sm_scale: float, page: int = 64,
+                    layout: str = "HND"):
+    q = values(h, "q")
+    if h.get("q_scale") is not None:
+        q = q * h["q_scale"].astype(np.float64)[..., None]
+    k, v = hnd_pools(h, layout)
     B = h["seq_lens"].shape[0]
     G = num_q_heads // num_kv_heads
     d = q.shape[-1]
@@ -53,7 +63,7 @@ def dense_attention(h: dict, num_q_heads: int, num_kv_heads: int, sm_scale: floa
 
 
 def dense_attention_multi(h: dict, num_q_heads: int, num_kv_heads: int, sm_scale: float, q_len: int,
-                          page: int = 64):
+                          page: int = 64, layout: str = "HND"):
     """q [B, q_len, Hq, d]: query token i of request b (length n) stands at position
     n - q_len + i and sees the tokens t <= that position; the score matrix of each
     (request, query head) is masked to that causal pattern before scipy's softmax and
@@ -61,11 +71,7 @@ def dense_attention_multi(h: dict, num_q_heads: int, num_kv_heads: int, sm_scale
     q = values(h, "q").reshape(-1, q_len, num_q_heads, h["q"].shape[-1])
     if h.get("q_scale") is not None:
         q = q * h["q_scale"].astype(np.float64).reshape(q.shape[:3])[..., None]
-    k = values(h, "k_pages")
-    v = values(h, "v_pages")
-    if h.get("k_scale") is not None:
-        k = k * h["k_scale"].astype(np.float64)[..., None]
-        v = v * h["v_scale"].astype(np.float64)[..., None]
+    k, v = hnd_pools(h, layout)
     B = h["seq_lens"].shape[0]
     G = num_q_heads // num_kv_heads
     d = q.shape[-1]

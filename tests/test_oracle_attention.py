@@ -18,8 +18,9 @@ from tests import brute
 HQ, HKV = 8, 2
 
 
-def tiny(lens, kv="bf16", seed=0, hq=HQ, hkv=HKV, q_len=1):
-    inp = workloads.make_inputs(np.array(lens), hq, hkv, kv, seed=seed, device="cpu", q_len=q_len)
+def tiny(lens, kv="bf16", seed=0, hq=HQ, hkv=HKV, q_len=1, page=64, layout="HND"):
+    inp = workloads.make_inputs(np.array(lens), hq, hkv, kv, seed=seed, device="cpu", q_len=q_len,
+                                page_size=page, kv_layout=layout)
     h = workloads.host_view(inp)
     return inp, h
 
@@ -28,7 +29,7 @@ def problem(h, inp):
     return oracle.Problem(h["q"], h["k_pages"], h["v_pages"], h["block_table"], h["seq_lens"],
                           inp["num_q_heads"], inp["num_kv_heads"], inp["sm_scale"],
                           q_scale=h["q_scale"], k_scale=h["k_scale"], v_scale=h["v_scale"],
-                          q_len=inp.get("q_len", 1))
+                          q_len=inp.get("q_len", 1), page_size=inp["page_size"], kv_layout=inp["kv_layout"])
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
@@ -204,3 +205,67 @@ def test_multi_token_split_merge():
             ref = out[b][:, hk * G:(hk + 1) * G].reshape(q_len * G, -1)
             np.testing.assert_allclose(mo, ref, rtol=0, atol=1e-12)
             np.testing.assert_allclose(ml, lse[b][:, hk * G:(hk + 1) * G].reshape(-1), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- page layouts and sizes
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("page,layout", [(16, "HND"), (32, "NHD"), (64, "NHD"), (16, "NHD")])
+def test_layouts_match_dense_brute_force(kv, page, layout):
+    lens = [0, 1, 15, 16, 17, 63, 64, 65, 130, 333]
+    inp, h = tiny(lens, kv, seed=11, page=page, layout=layout)
+    out, lse = problem(h, inp).attention()
+    ref, ref_lse = brute.dense_attention(h, HQ, HKV, inp["sm_scale"], page=page, layout=layout)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
+def repage(h, lens, page, new_page, layout, rng):
+    """The same tokens moved into pages of new_page tokens (randomly placed) and the
+    given layout: [num_pages, Hkv, P, d] (HND) or [num_pages, P, Hkv, d] (NHD)."""
+    hkv, d = h["k_pages"].shape[1], h["k_pages"].shape[-1]
+    pieces_k, pieces_v, pieces_ks, pieces_vs, rows = [], [], [], [], []
+    for b, n in enumerate(lens):
+        for t0 in range(0, n, new_page):
+            pieces = []
+            for t in range(t0, t0 + new_page):
+                src_page = h["block_table"][b, min(t, max(n - 1, 0)) // page]
+                slot = min(t, max(n - 1, 0)) % page
+                pieces.append((src_page, slot))
+            rows.append((b, t0 // new_page, pieces))
+    order = rng.permutation(len(rows))
+    npages = len(rows)
+    k = np.zeros((npages, hkv, new_page, d), h["k_pages"].dtype)
+    v = np.zeros_like(k)
+    fp8 = h.get("k_scale") is not None
+    ks = np.zeros((npages, hkv, new_page), np.float32) if fp8 else None
+    vs = np.zeros_like(ks) if fp8 else None
+    bt = np.full((len(lens), max(1, max(-(-n // new_page) for n in lens))), -1, np.int32)
+    for dst, i in enumerate(order):
+        b, j, pieces = rows[i]
+        bt[b, j] = dst
+        for s_, (sp, sl) in enumerate(pieces):
+            k[dst, :, s_] = h["k_pages"][sp, :, sl]
+            v[dst, :, s_] = h["v_pages"][sp, :, sl]
+            if fp8:
+                ks[dst, :, s_] = h["k_scale"][sp, :, sl]
+                vs[dst, :, s_] = h["v_scale"][sp, :, sl]
+    if layout == "NHD":
+        k, v = np.ascontiguousarray(k.transpose(0, 2, 1, 3)), np.ascontiguousarray(v.transpose(0, 2, 1, 3))
+    return dict(h, k_pages=k, v_pages=v, k_scale=ks, v_scale=vs, block_table=bt)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_page_size_and_layout_do_not_change_the_result(kv):
+    """The same tokens in 16- or 32-token pages, HND or NHD, give exactly the 64-token HND result."""
+    lens = [1, 40, 64, 100, 257]
+    inp, h = tiny(lens, kv, seed=12)
+    out, lse = problem(h, inp).attention()
+    rng = np.random.default_rng(3)
+    for new_page in (16, 32):
+        for layout in ("HND", "NHD"):
+            h2 = repage(h, lens, 64, new_page, layout, rng)
+            p2 = oracle.Problem(h2["q"], h2["k_pages"], h2["v_pages"], h2["block_table"], h2["seq_lens"], HQ, HKV,
+                                inp["sm_scale"], q_scale=h2["q_scale"], k_scale=h2["k_scale"], v_scale=h2["v_scale"],
+                                page_size=new_page, kv_layout=layout)
+            o2, l2 = p2.attention()
+            assert np.array_equal(o2, out) and np.array_equal(l2, lse), (new_page, layout)

@@ -107,13 +107,16 @@ def _quantize_e4m3(x: torch.Tensor):
 
 def make_inputs(lengths, num_q_heads: int, num_kv_heads: int, kv_dtype: str = "bf16",
                 seed: int = 0, device="cpu", head_dim: int = HEAD_DIM, page_size: int = PAGE,
-                rng: np.random.Generator | None = None, chunk_pages: int = 2048, q_len: int = 1) -> dict:
+                rng: np.random.Generator | None = None, chunk_pages: int = 2048, q_len: int = 1,
+                kv_layout: str = "HND") -> dict:
     """Build one decode step's inputs on `device`.
 
     `rng` continues the numpy stream used for the lengths (draw order above); if
     None a fresh Generator(seed) is used for the page permutation.  q_len > 1 gives
     each request q_len query tokens (a multi-token verify step): Q [B, q_len, Hq, d]
-    (Q scale [B, q_len, Hq]), drawn in that order from the same stream.
+    (Q scale [B, q_len, Hq]), drawn in that order from the same stream.  kv_layout "NHD"
+    stores each page token-major, [num_pages, page, Hkv, d] (the values drawn as for "HND",
+    then transposed); the FP8 scales stay [num_pages, Hkv, page].
     """
     lens = np.asarray(lengths, np.int64)
     B = int(lens.shape[0])
@@ -144,6 +147,7 @@ def make_inputs(lengths, num_q_heads: int, num_kv_heads: int, kv_dtype: str = "b
         "head_dim": head_dim,
         "page_size": page_size,
         "kv_dtype": kv_dtype,
+        "kv_layout": kv_layout,
         "sm_scale": 1.0 / math.sqrt(head_dim),
         "q_len": q_len,
     }
@@ -174,6 +178,9 @@ def make_inputs(lengths, num_q_heads: int, num_kv_heads: int, kv_dtype: str = "b
                 pool[r0:r1] = x.to(torch.bfloat16)
             _fill_normal(shape, gen, device, chunk_pages, put)
             out[name + "_pages"], out[name + "_scale"] = pool, None
+    if kv_layout == "NHD":
+        for name in ("k_pages", "v_pages"):
+            out[name] = out[name].permute(0, 2, 1, 3).contiguous()
     return out
 
 
