@@ -323,6 +323,7 @@ def bench_ours(args, device, rank, world):
     prologue = bench_prologue(dsa, device, w, B, timed, max(10, min(args.steps, 200)))
     # multi-token steps use one bin per SM: the tensor-memory kernel holds one CTA per SM
     multi = bench_multi(dsa, device, inp, w, sms, m, timed, max(10, min(args.steps, 200)), nbytes, ms_per_step)
+    layouts = bench_layouts(dsa, device, inp, w, C, m, timed, max(10, min(args.steps, 200)), nbytes, t_dec)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     host = {k: inp[k].cpu().pin_memory() for k in ("q", "q_scale", "k_pages", "v_pages", "k_scale", "v_scale",
@@ -385,6 +386,7 @@ def bench_ours(args, device, rank, world):
         "static": static,
         "prologue": prologue,
         "multi_token": multi,
+        "page_layouts": layouts,
         "roofline": {"bound": "hbm", "kernel": "attn_kernel (persistent decode, dsa_decode)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
@@ -485,6 +487,36 @@ def bench_multi(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes: 
             "decode_kv_GB/s": round(gbs, 1), "decode_frac_of_hbm_peak": round(gbs / peak, 4),
             "decode_TFLOP/s": round(flops / (t_dec * 1e-3) / 1e12, 1),
             "vs_q_len_one_token_steps": round(q_len * single_ms / step, 2)}
+    return res
+
+
+def bench_layouts(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes: int, base_ms: float) -> dict:
+    """The decode kernel on the same lengths and C bins with the KV held in pages of 16 / 32 /
+    64 tokens, HND or NHD (dsa_decode_ex): a 64-token tile is then loaded as 64 / P boxes."""
+    B, hq, hkv = int(inp["seq_lens"].shape[0]), w.num_q_heads, w.num_kv_heads
+    lens = inp["seq_lens"].cpu().numpy()
+    peak, _ = measured_peaks()
+    tm = dsa.TaskMap(B, hkv, C, device)
+    dsa.plan(inp["seq_lens"], hkv, C, m, task_map=tm)
+    po, pl = dsa.partial_buffers(tm.max_descs, hq // hkv, device)
+    res = {}
+    for page, layout in ((64, "NHD"), (32, "HND"), (32, "NHD"), (16, "HND"), (16, "NHD")):
+        li = workloads.make_inputs(lens, hq, hkv, w.kv_dtype, w.seed, device, page_size=page, kv_layout=layout)
+
+        def dec(li=li, layout=layout):
+            dsa.decode(inp["q"], li["k_pages"], li["v_pages"], li["block_table"], li["seq_lens"], tm,
+                       inp["sm_scale"], partial_o=po, partial_lse=pl, q_scale=inp.get("q_scale"),
+                       k_scale=li.get("k_scale"), v_scale=li.get("v_scale"), kv_layout=layout)
+
+        per = timed([dec], steps, 3)
+        if dsa.get_status(tm) != 0:
+            raise RuntimeError(f"page {page} {layout}: device status set")
+        t = float(per.mean())
+        gbs = nbytes / (t * 1e-3) / 1e9
+        res[f"P{page}_{layout}"] = {"decode_us": round(t * 1e3, 2), "kv_GB/s": round(gbs, 1),
+                                    "frac_of_hbm_peak": round(gbs / peak, 4),
+                                    "time_vs_P64_HND": round(t / base_ms, 3)}
+        del li
     return res
 
 

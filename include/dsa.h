@@ -31,13 +31,17 @@
  *     before reading any global memory.
  *   - Shapes: B = batch, Hq = query heads, Hkv = KV heads, G = Hq / Hkv query
  *     heads per KV head (query head j reads KV head j / G), d = head_dim = 128,
- *     P = page_size = 64 tokens = the tile.  Unit u = (request b, KV head h),
+ *     P = page_size tokens per page: 64 (the tile) everywhere, also 16 or 32
+ *     for the decode and split-KV calls (a 64-token tile then spans 64 / P
+ *     consecutive block-table entries).  Unit u = (request b, KV head h),
  *     u = b * Hkv + h.
  *   - Layouts (row-major, innermost last):
  *       q            [B, Hq, d]              bf16, or E4M3 bytes
  *       q_scale      [B, Hq] fp32            E4M3 Q only: real = e4m3 * scale
  *       k/v_pages    [num_pages, Hkv, P, d]  bf16, or E4M3 bytes; one
  *                                            (page, KV head) block is contiguous
+ *                                            ("HND"; dsa_decode_ex also reads
+ *                                            "NHD" pages [num_pages, P, Hkv, d])
  *       k/v_scale    [num_pages, Hkv, P] fp32  E4M3 K/V only, per token and head
  *       block_table  [B, max_pages_per_req] int32; token t of request b is slot
  *                    t % P of page block_table[b][t / P]; entries at or past
@@ -85,6 +89,11 @@ typedef enum {
 #define DSA_DEV_BAD_POSITION 32 /* dsa_prologue: a position outside [0, max_position) */
 
 typedef enum { DSA_BF16 = 0, DSA_FP8_E4M3 = 1, DSA_FP32 = 2 } dsa_dtype;
+
+/* Order of a K/V page's dimensions: HND = [num_pages, Hkv, P, d] (one (page, head)
+ * block contiguous), NHD = [num_pages, P, Hkv, d] (one token's heads contiguous).
+ * FP8 scales are [num_pages, Hkv, P] in both. */
+typedef enum { DSA_HND = 0, DSA_NHD = 1 } dsa_kv_layout;
 
 /*
  * Task map: the per-step schedule ("全局任务映射" in the blog's "围绕活跃 KV
@@ -150,7 +159,7 @@ dsa_status dsa_plan(const int32_t *seq_lens, int32_t batch, int32_t num_kv_heads
  *     partial_lse[x][g] = ln sum_t exp(s_t)
  *     partial_o[x][g][:] = sum_t exp(s_t - partial_lse) * v_t  (FP8: * v_scale[t])
  * Supported: (q_dtype, kv_dtype) = (BF16, BF16) or (FP8_E4M3, FP8_E4M3);
- * head_dim 128; page_size 64; 1 <= G <= 8.  q_scale is required for FP8 Q,
+ * head_dim 128; page_size 16, 32 or 64; 1 <= G <= 8.  q_scale is required for FP8 Q,
  * k_scale/v_scale for FP8 K/V, otherwise ignored.  partial_o holds
  * [map->max_descs, G, 128] fp32, partial_lse [map->max_descs, G] fp32.
  * Device input errors set bits in map->meta[3] (see above).
@@ -222,6 +231,28 @@ dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q_dtype, con
                             int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
                             const dsa_task_map *map, float *partial_o, float *partial_lse,
                             dsa_stream stream);
+
+/*
+ * dsa_decode_ex -- dsa_decode / dsa_decode_multi with the page layout as an argument
+ * (HPC-Ops × SGLang blog, "从 HPC-Ops kernel 到 SGLang": the attention kernel reads
+ * the serving runtime's own paged KV store, with no layout conversion first).
+ * kv_layout is DSA_HND or DSA_NHD (k/v_pages shaped [num_pages, Hkv, P, d] or
+ * [num_pages, P, Hkv, d]); page_size is 16, 32 or 64 for either.  q_len = 1 is
+ * dsa_decode, q_len > 1 dsa_decode_multi; the results do not depend on the layout
+ * or the page size (the same tokens in another arrangement give the same bits).
+ * A 64-token tile reads 64 / P pages, each with its own block-table entry; only
+ * pages holding a token below the request's length are read.  Errors: a
+ * kv_layout outside dsa_kv_layout gives DSA_ERR_INVALID_ARG, other page sizes
+ * DSA_ERR_UNSUPPORTED; the rest as for dsa_decode.
+ */
+dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void *q, dsa_dtype q_dtype,
+                         const float *q_scale, const void *k_pages, const void *v_pages,
+                         dsa_dtype kv_dtype, const float *k_scale, const float *v_scale,
+                         const int32_t *block_table, int32_t max_pages_per_req, int32_t num_pages,
+                         const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
+                         const dsa_task_map *map, float *partial_o, float *partial_lse,
+                         dsa_stream stream);
 
 /*
  * dsa_combine_multi -- dsa_combine over the q_len * G partial rows of each unit:
@@ -307,9 +338,10 @@ dsa_status dsa_get_status(const dsa_task_map *map, int32_t *host_status);
  *   encoding:       FP8: scale = amax(|y|) / 448 (1 if y = 0), byte = E4M3(y / scale),
  *                   round to nearest even, saturating; BF16: round to nearest even.
  * Q goes to q_out [n_tokens, Hq, 128] (q_scale [n_tokens, Hq] for FP8); K and V go
- * to slot s = slot_mapping[n] of the cache, i.e. page s / 64, offset s % 64 of
- * k_pages / v_pages [num_pages, Hkv, 64, 128] (k/v_scale [num_pages, Hkv, 64] for
- * FP8), the layout dsa_decode reads.  s = -1 writes nothing for that token.
+ * to slot s = slot_mapping[n] of the cache, i.e. page s / P, offset s % P of
+ * k_pages / v_pages, [num_pages, Hkv, P, 128] for kv_layout DSA_HND or
+ * [num_pages, P, Hkv, 128] for DSA_NHD (k/v_scale [num_pages, Hkv, P] for FP8 in
+ * both), the layouts dsa_decode_ex reads.  s = -1 writes nothing for that token.
  * Arguments:
  *   qkv            [n_tokens, (Hq + 2 Hkv) * 128] bf16: the QKV projection output,
  *                  heads in the order Q, K, V.
@@ -325,9 +357,10 @@ dsa_status dsa_get_status(const dsa_task_map *map, int32_t *host_status);
  *   q_dtype, kv_dtype  DSA_BF16 or DSA_FP8_E4M3 (scales required for FP8).
  *   status         device int32 or NULL: DSA_DEV_BAD_POSITION for a position outside
  *                  [0, max_position) (that token's Q and K rows are not written),
- *                  DSA_DEV_BAD_PAGE for a slot outside [-1, num_pages * 64) (that
+ *                  DSA_DEV_BAD_PAGE for a slot outside [-1, num_pages * P) (that
  *                  token's K and V are not written).
- * head_dim must be 128 and page_size 64.  qkv, q_out, the pages, cos_sin and the
+ * head_dim must be 128 and page_size P 16, 32 or 64 (else DSA_ERR_UNSUPPORTED);
+ * kv_layout DSA_HND or DSA_NHD (else DSA_ERR_INVALID_ARG).  qkv, q_out, the pages, cos_sin and the
  * weights must be 16-byte aligned.  Several tokens must not share a slot.
  */
 typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_INTERLEAVED = 1 } dsa_rope_style;
@@ -338,7 +371,7 @@ dsa_status dsa_prologue(const void *qkv, int32_t n_tokens, int32_t num_q_heads, 
                         int32_t hadamard, const int32_t *slot_mapping, void *q_out, dsa_dtype q_dtype,
                         float *q_scale, void *k_pages, void *v_pages, dsa_dtype kv_dtype,
                         float *k_scale, float *v_scale, int32_t num_pages, int32_t page_size,
-                        int32_t *status, dsa_stream stream);
+                        int32_t kv_layout, int32_t *status, dsa_stream stream);
 
 /*
  * dsa_decode_step_noalloc -- one whole decode step (dsa_plan, dsa_decode,

@@ -63,6 +63,8 @@ _lib.dsa_multi_slots_per_desc.argtypes = [_i32, _i32]
 _lib.dsa_multi_slots_per_desc.restype = _i32
 _lib.dsa_decode_multi.argtypes = [_i32] + _attn_args + [_TMP, _vp, _vp, _vp]
 _lib.dsa_decode_multi.restype = ctypes.c_int
+_lib.dsa_decode_ex.argtypes = [_i32, _i32] + _attn_args + [_TMP, _vp, _vp, _vp]
+_lib.dsa_decode_ex.restype = ctypes.c_int
 _lib.dsa_combine_multi.argtypes = [_i32, _TMP, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]
 _lib.dsa_combine_multi.restype = ctypes.c_int
 _lib.dsa_static_num_splits.argtypes = [_i32, _i32, _i32]
@@ -80,7 +82,7 @@ _lib.dsa_decode_step_noalloc.restype = ctypes.c_int
 _lib.dsa_selftest_wait_timeout.argtypes = [_vp, ctypes.c_int64, _vp]
 _lib.dsa_selftest_wait_timeout.restype = ctypes.c_int
 _lib.dsa_prologue.argtypes = [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _f32, _i32, _vp,
-                              _vp, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp]
+                              _vp, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _vp, _vp]
 _lib.dsa_prologue.restype = ctypes.c_int
 _lib.dsa_status_string.argtypes = [ctypes.c_int]
 _lib.dsa_status_string.restype = ctypes.c_char_p
@@ -168,9 +170,16 @@ def plan(seq_lens: torch.Tensor, num_kv_heads: int, num_persistent_ctas: int, mi
     return tm
 
 
-def _attn_args(q, k_pages, v_pages, block_table, seq_lens, num_kv_heads, sm_scale, q_scale, k_scale, v_scale):
+KV_LAYOUTS = {"HND": 0, "NHD": 1}  # dsa_kv_layout
+
+
+def _attn_args(q, k_pages, v_pages, block_table, seq_lens, num_kv_heads, sm_scale, q_scale, k_scale, v_scale,
+               kv_layout="HND"):
     batch, hq, d = q.shape[0], q.shape[-2], q.shape[-1]
-    num_pages, hkv, page, d2 = k_pages.shape
+    if kv_layout == "NHD":  # [num_pages, P, Hkv, d]
+        num_pages, page, hkv, d2 = k_pages.shape
+    else:                   # [num_pages, Hkv, P, d]
+        num_pages, hkv, page, d2 = k_pages.shape
     if hkv != num_kv_heads:
         raise ValueError("k_pages head count differs from num_kv_heads")
     return [_ptr(q), _dtype_code(q), _ptr(q_scale), _ptr(k_pages), _ptr(v_pages), _dtype_code(k_pages),
@@ -185,15 +194,21 @@ def partial_buffers(max_slots: int, group: int, device="cuda"):
 
 
 def decode(q, k_pages, v_pages, block_table, seq_lens, task_map: TaskMap, sm_scale: float,
-           partial_o=None, partial_lse=None, q_scale=None, k_scale=None, v_scale=None, stream=None):
-    """dsa_decode: persistent kernel writing one partial (o, lse) per descriptor."""
+           partial_o=None, partial_lse=None, q_scale=None, k_scale=None, v_scale=None, stream=None,
+           kv_layout="HND"):
+    """dsa_decode (dsa_decode_ex for NHD pages): persistent kernel writing one partial
+    (o, lse) per descriptor."""
     G = q.shape[1] // task_map.num_kv_heads
     if partial_o is None:
         partial_o, partial_lse = partial_buffers(task_map.max_descs, G, q.device)
     args = _attn_args(q, k_pages, v_pages, block_table, seq_lens, task_map.num_kv_heads, sm_scale,
-                      q_scale, k_scale, v_scale)
-    rc = _lib.dsa_decode(*args, ctypes.byref(task_map.struct), _ptr(partial_o), _ptr(partial_lse),
-                         _stream(stream))
+                      q_scale, k_scale, v_scale, kv_layout)
+    if kv_layout == "HND":
+        rc = _lib.dsa_decode(*args, ctypes.byref(task_map.struct), _ptr(partial_o), _ptr(partial_lse),
+                             _stream(stream))
+    else:
+        rc = _lib.dsa_decode_ex(1, KV_LAYOUTS[kv_layout], *args, ctypes.byref(task_map.struct), _ptr(partial_o),
+                                _ptr(partial_lse), _stream(stream))
     _check(rc, "dsa_decode")
     return partial_o, partial_lse
 
@@ -233,7 +248,8 @@ def combine(task_map: TaskMap, partial_o, partial_lse, num_q_heads: int, out=Non
 
 
 def decode_multi(q_len: int, q, k_pages, v_pages, block_table, seq_lens, task_map: TaskMap, sm_scale: float,
-                 partial_o=None, partial_lse=None, q_scale=None, k_scale=None, v_scale=None, stream=None):
+                 partial_o=None, partial_lse=None, q_scale=None, k_scale=None, v_scale=None, stream=None,
+                 kv_layout="HND"):
     """dsa_decode_multi: q [B, q_len, Hq, 128]; partials hold q_len * G rows per slot, two
     slots per descriptor when q_len > 1."""
     R = q_len * (q.shape[-2] // task_map.num_kv_heads)
@@ -241,9 +257,13 @@ def decode_multi(q_len: int, q, k_pages, v_pages, block_table, seq_lens, task_ma
         spd = int(_lib.dsa_multi_slots_per_desc(q_len, q.shape[-2] // task_map.num_kv_heads))
         partial_o, partial_lse = partial_buffers(task_map.max_descs * spd, R, q.device)
     args = _attn_args(q, k_pages, v_pages, block_table, seq_lens, task_map.num_kv_heads, sm_scale,
-                      q_scale, k_scale, v_scale)
-    rc = _lib.dsa_decode_multi(q_len, *args, ctypes.byref(task_map.struct), _ptr(partial_o), _ptr(partial_lse),
-                               _stream(stream))
+                      q_scale, k_scale, v_scale, kv_layout)
+    if kv_layout == "HND":
+        rc = _lib.dsa_decode_multi(q_len, *args, ctypes.byref(task_map.struct), _ptr(partial_o),
+                                   _ptr(partial_lse), _stream(stream))
+    else:
+        rc = _lib.dsa_decode_ex(q_len, KV_LAYOUTS[kv_layout], *args, ctypes.byref(task_map.struct),
+                                _ptr(partial_o), _ptr(partial_lse), _stream(stream))
     _check(rc, "dsa_decode_multi")
     return partial_o, partial_lse
 
@@ -270,7 +290,7 @@ def attention_multi(inp: dict, num_ctas: int, min_tiles_per_split: int = 4, out_
               stream=stream)
     po, pl = decode_multi(q_len, inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
                           inp["sm_scale"], q_scale=inp.get("q_scale"), k_scale=inp.get("k_scale"),
-                          v_scale=inp.get("v_scale"), stream=stream)
+                          v_scale=inp.get("v_scale"), stream=stream, kv_layout=inp.get("kv_layout", "HND"))
     B = inp["seq_lens"].shape[0]
     out_lse = torch.empty(B, q_len, inp["num_q_heads"], dtype=torch.float32, device=po.device)
     out = combine_multi(q_len, tm, po, pl, inp["num_q_heads"], out_lse=out_lse, out_dtype=out_dtype, stream=stream)
@@ -316,9 +336,10 @@ def static_combine(num_splits: int, partial_o, partial_lse, batch: int, num_q_he
 def prologue(qkv, num_q_heads: int, num_kv_heads: int, slot_mapping, k_pages, v_pages, k_scale=None,
              v_scale=None, positions=None, cos_sin=None, rotary_dim: int | None = None, rope_style: str = "neox",
              q_norm_weight=None, k_norm_weight=None, eps: float = 1e-6, hadamard: bool = False,
-             q_dtype=torch.bfloat16, q_out=None, q_scale=None, status=None, stream=None):
+             q_dtype=torch.bfloat16, q_out=None, q_scale=None, status=None, stream=None, kv_layout="HND"):
     """dsa_prologue: QK-Norm -> RoPE -> [Hadamard] -> Q out (bf16, or E4M3 + per-(token, head)
-    scales) and K/V written into the paged cache at slot_mapping.  Returns (q_out, q_scale)."""
+    scales) and K/V written into the paged cache at slot_mapping (pages [num_pages, Hkv, P, 128]
+    for kv_layout "HND", [num_pages, P, Hkv, 128] for "NHD").  Returns (q_out, q_scale)."""
     n = int(qkv.shape[0])
     fp8_q = q_dtype in (torch.uint8, torch.float8_e4m3fn, "e4m3")
     if q_out is None:
@@ -333,8 +354,8 @@ def prologue(qkv, num_q_heads: int, num_kv_heads: int, slot_mapping, k_pages, v_
                            max_pos, rot, style, _ptr(q_norm_weight), _ptr(k_norm_weight), float(eps),
                            int(bool(hadamard)), _ptr(slot_mapping), _ptr(q_out), _dtype_code(q_out),
                            _ptr(q_scale), _ptr(k_pages), _ptr(v_pages), _dtype_code(k_pages), _ptr(k_scale),
-                           _ptr(v_scale), int(k_pages.shape[0]), int(k_pages.shape[2]), _ptr(status),
-                           _stream(stream))
+                           _ptr(v_scale), int(k_pages.shape[0]), int(k_pages.shape[1 if kv_layout == "NHD" else 2]),
+                           KV_LAYOUTS[kv_layout], _ptr(status), _stream(stream))
     _check(rc, "dsa_prologue")
     return q_out, q_scale
 
@@ -390,7 +411,7 @@ def attention(inp: dict, num_ctas: int, min_tiles_per_split: int = 4, out_dtype=
               stream=stream)
     po, pl = decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
                     inp["sm_scale"], q_scale=inp.get("q_scale"), k_scale=inp.get("k_scale"),
-                    v_scale=inp.get("v_scale"), stream=stream)
+                    v_scale=inp.get("v_scale"), stream=stream, kv_layout=inp.get("kv_layout", "HND"))
     B = inp["seq_lens"].shape[0]
     out_lse = torch.empty(B, inp["num_q_heads"], dtype=torch.float32, device=po.device)
     out = combine(tm, po, pl, inp["num_q_heads"], out_lse=out_lse, out_dtype=out_dtype, stream=stream)

@@ -16,7 +16,9 @@ dsa_status validate_attn(const AttnArgs &a) {
     if (a.batch < 0 || a.num_q_heads < 1 || a.num_kv_heads < 1 || a.num_q_heads % a.num_kv_heads != 0 ||
         a.max_pages_per_req < 0 || a.num_pages < 0)
         return DSA_ERR_INVALID_ARG;
-    if (a.head_dim != kHeadDim || a.page_size != kTile) return DSA_ERR_UNSUPPORTED;
+    if (a.head_dim != kHeadDim || !(a.page_size == 16 || a.page_size == 32 || a.page_size == kTile))
+        return DSA_ERR_UNSUPPORTED;
+    if (a.kv_layout != DSA_HND && a.kv_layout != DSA_NHD) return DSA_ERR_INVALID_ARG;
     if (a.num_q_heads / a.num_kv_heads > kMaxGroup) return DSA_ERR_UNSUPPORTED;
     const bool fp8 = a.kv_dtype == DSA_FP8_E4M3;
     if (!((a.q_dtype == DSA_BF16 && a.kv_dtype == DSA_BF16) || (a.q_dtype == DSA_FP8_E4M3 && fp8)))
@@ -31,7 +33,9 @@ dsa_status validate_attn(const AttnArgs &a) {
         if (!a.q_scale || (a.num_pages > 0 && (!a.k_scale || !a.v_scale))) return DSA_ERR_INVALID_ARG;
         if (!aligned16(a.k_scale) || !aligned16(a.v_scale)) return DSA_ERR_INVALID_ARG;
     }
-    if (static_cast<int64_t>(a.batch) * a.max_pages_per_req > INT32_MAX / 2) return DSA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(a.batch) * a.max_pages_per_req > INT32_MAX / 2 ||
+        static_cast<int64_t>(a.max_pages_per_req) * a.page_size > INT32_MAX / 2)
+        return DSA_ERR_UNSUPPORTED;
     return DSA_OK;
 }
 

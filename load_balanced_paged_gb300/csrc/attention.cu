@@ -52,6 +52,8 @@ struct KernelParams {
     int32_t max_pages, num_pages, hq, hkv, G, num_units, max_slots;
     int32_t q_len;      // query tokens per request (1: plain decode; > 1: multi-token verify)
     int32_t slots_per_desc;  // partial slots per descriptor (2 for the tensor-core multi-token path)
+    int32_t page_size;       // tokens per page P (16, 32 or 64); a 64-token tile spans 64 / P pages
+    int32_t nhd;             // pages laid out [num_pages][P][Hkv][d] instead of [num_pages][Hkv][P][d]
     float score_scale;  // sm_scale * log2(e)
     // persistent schedule
     const int32_t *cta_desc_begin;
@@ -91,6 +93,7 @@ constexpr int kQSlots = 2;   // descriptors handed ahead to the consumers (Q + i
 constexpr int kEpiRing = 8;  // merged descriptors the epilogue warp may lag behind (fused combine)
 constexpr int kMaxRows = 64; // query rows (query tokens x G) of one unit in a multi-token step
 constexpr int kDescInfoBytes = 80;
+constexpr int kMaxPagesPerTile = kTile / 16;  // pages of 16 tokens: four per tile
 
 // QW = 0: one query token per request; the consumer groups take alternate tiles and all
 // warps of the CTA merge at each descriptor end.  QW = 1 or 2: multi-token queries with
@@ -471,7 +474,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         wnp = p.unit_num_partials[x.u];
                         wpbeg = p.unit_partial_begin[x.u];
                     }
-                    if (wlen < 0 || wlen > p.max_pages * kTile) atomicOr(p.status, DSA_DEV_BAD_SEQLEN);
+                    if (wlen < 0 || wlen > p.max_pages * p.page_size) atomicOr(p.status, DSA_DEV_BAD_SEQLEN);
                     if (KV == 1) {
                         const float *qs = p.q_scale + static_cast<int64_t>(wb) * p.hq + wh * G;
 #pragma unroll
@@ -500,7 +503,9 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
             const int wtotal = __shfl_sync(0xffffffffu, incl, 31);
 
             // lane -> (descriptor, tile, page) for stream tile s0 + lane
-            auto map_chunk = [&](int s0, int &j, int &t, int &pg) {
+            // a 64-token tile spans ppt pages of P tokens: pages t * ppt .. t * ppt + ppt - 1
+            const int P = p.page_size, ppt = kTile / P;
+            auto map_chunk = [&](int s0, int &j, int &t, int (&pg)[kMaxPagesPerTile]) {
                 const int s = s0 + lane;
                 j = 0;
 #pragma unroll
@@ -510,14 +515,23 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 }
                 t = __shfl_sync(0xffffffffu, wt0, j) + (s - __shfl_sync(0xffffffffu, wstart, j));
                 const int bj = __shfl_sync(0xffffffffu, wb, j);
-                pg = -1;
-                if (s < wtotal && t < p.max_pages) pg = p.block_table[static_cast<int64_t>(bj) * p.max_pages + t];
+#pragma unroll
+                for (int k = 0; k < kMaxPagesPerTile; ++k) {
+                    const int idx = t * ppt + k;
+                    pg[k] = -1;
+                    if (k < ppt && s < wtotal && idx < p.max_pages)
+                        pg[k] = p.block_table[static_cast<int64_t>(bj) * p.max_pages + idx];
+                }
             };
 
-            int cj = 0, ct = 0, cpg = -1;
+            int cj = 0, ct = 0, cpg[kMaxPagesPerTile];
+#pragma unroll
+            for (int k = 0; k < kMaxPagesPerTile; ++k) cpg[k] = -1;
             if (wtotal > 0) map_chunk(0, cj, ct, cpg);
             for (int s0 = 0; s0 < wtotal && !aborted; s0 += 32) {
-                int nj = 0, nt = 0, npg = -1;
+                int nj = 0, nt = 0, npg[kMaxPagesPerTile];
+#pragma unroll
+                for (int k = 0; k < kMaxPagesPerTile; ++k) npg[k] = -1;
                 if (s0 + 32 < wtotal) map_chunk(s0 + 32, nj, nt, npg);  // next chunk's page ids in flight
                 const int cnt = min(32, wtotal - s0);
                 // ---- per-lane view of this lane's own tile (stream tile s0 + lane)
@@ -527,10 +541,15 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 const bool first_l = lane < cnt && ct == t0_l;
                 int nv_l = 0;
                 if (lane < cnt) {
-                    const bool len_ok = len_l >= 0 && len_l <= p.max_pages * kTile;
+                    const bool len_ok = len_l >= 0 && len_l <= p.max_pages * P;
                     nv_l = len_ok ? min(kTile, len_l - ct * kTile) : 0;
-                    if (nv_l < 0 || ct >= p.max_pages) nv_l = 0;
-                    if (nv_l > 0 && (cpg < 0 || cpg >= p.num_pages)) {
+                    if (nv_l < 0 || ct * ppt >= p.max_pages) nv_l = 0;
+                    // the pages holding the tile's valid tokens must be inside the pool
+                    bool bad = false;
+#pragma unroll
+                    for (int k = 0; k < kMaxPagesPerTile; ++k)
+                        if (k * P < nv_l && (cpg[k] < 0 || cpg[k] >= p.num_pages)) bad = true;
+                    if (nv_l > 0 && bad) {
                         atomicOr(p.status, DSA_DEV_BAD_PAGE);
                         nv_l = 0;
                     }
@@ -607,19 +626,28 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                             if (nv_l > 0) {
                                 const uint32_t kdst = sbase + stage * L::kStageBytes;
                                 const uint32_t vdst = kdst + C::kTileBytes;
-                                mbar_arrive_expect_tx(fb, L::kStageTx);
-                                if (KV == 0) {  // two 64-column boxes per 128-wide bf16 row
-                                    tma_load_4d(kdst, &kmap, fb, 0, 0, h_l, cpg, policy);
-                                    tma_load_4d(kdst + C::kTileBytes / 2, &kmap, fb, 64, 0, h_l, cpg, policy);
-                                    tma_load_4d(vdst, &vmap, fb, 0, 0, h_l, cpg, policy);
-                                    tma_load_4d(vdst + C::kTileBytes / 2, &vmap, fb, 64, 0, h_l, cpg, policy);
-                                } else {
-                                    tma_load_4d(kdst, &kmap, fb, 0, 0, h_l, cpg, policy);
-                                    tma_load_4d(vdst, &vmap, fb, 0, 0, h_l, cpg, policy);
-                                    const int64_t srow = (static_cast<int64_t>(cpg) * p.hkv + h_l) * kTile;
-                                    bulk_load(vdst + C::kTileBytes, p.k_scale + srow, C::kScaleBytes, fb);
-                                    bulk_load(vdst + C::kTileBytes + C::kScaleBytes, p.v_scale + srow,
-                                              C::kScaleBytes, fb);
+                                // the pages holding valid tokens, P rows each: box (column, head, slot
+                                // 0, page) lands as P rows of 128 B at row k * P of the tile
+                                const int nsub = (nv_l + P - 1) / P;
+                                mbar_arrive_expect_tx(fb, nsub * (L::kStageTx / ppt));
+#pragma unroll
+                                for (int k = 0; k < kMaxPagesPerTile; ++k) {
+                                    if (k >= nsub) break;
+                                    const int pg = cpg[k], y = p.nhd ? h_l : 0, z = p.nhd ? 0 : h_l;
+                                    const uint32_t ro = static_cast<uint32_t>(k * P) * 128u;
+                                    if (KV == 0) {  // two 64-column boxes per 128-wide bf16 row
+                                        tma_load_4d(kdst + ro, &kmap, fb, 0, y, z, pg, policy);
+                                        tma_load_4d(kdst + C::kTileBytes / 2 + ro, &kmap, fb, 64, y, z, pg, policy);
+                                        tma_load_4d(vdst + ro, &vmap, fb, 0, y, z, pg, policy);
+                                        tma_load_4d(vdst + C::kTileBytes / 2 + ro, &vmap, fb, 64, y, z, pg, policy);
+                                    } else {
+                                        tma_load_4d(kdst + ro, &kmap, fb, 0, y, z, pg, policy);
+                                        tma_load_4d(vdst + ro, &vmap, fb, 0, y, z, pg, policy);
+                                        const int64_t srow = (static_cast<int64_t>(pg) * p.hkv + h_l) * P;
+                                        bulk_load(vdst + C::kTileBytes + 4 * k * P, p.k_scale + srow, 4 * P, fb);
+                                        bulk_load(vdst + C::kTileBytes + C::kScaleBytes + 4 * k * P, p.v_scale + srow,
+                                                  4 * P, fb);
+                                    }
                                 }
                             } else {
                                 mbar_arrive(fb);
@@ -637,7 +665,8 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 }
                 cj = nj;
                 ct = nt;
-                cpg = npg;
+#pragma unroll
+                for (int k = 0; k < kMaxPagesPerTile; ++k) cpg[k] = npg[k];
             }
         }
         if (FUSE && lane == 0) *epi_total = qi;  // descriptors handed off (the epilogue's count)
@@ -1739,17 +1768,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 4-D view [num_pages][Hkv][64 tokens][128] of a page pool, box = 64 tokens of one
-// (page, head) x 128 bytes of the row, 128-byte swizzle.
-bool make_pool_map(CUtensorMap *m, const void *pool, int kv, int num_pages, int hkv) {
+// 4-D view of a page pool with the box = the P tokens of one (page, head) x 128 bytes of the
+// row, 128-byte swizzle.  HND pages [num_pages][Hkv][P][128]: dims (128, P, Hkv, pages),
+// box (128 B, P, 1, 1); NHD pages [num_pages][P][Hkv][128]: dims (128, Hkv, P, pages), box
+// (128 B, 1, P, 1).  Either box lands as P rows of 128 B.
+bool make_pool_map(CUtensorMap *m, const void *pool, int kv, int num_pages, int hkv, int page, bool nhd) {
     std::memset(m, 0, sizeof(*m));
     if (num_pages == 0) return true;  // nothing can be loaded
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t es = kv == 0 ? 2 : 1;
-    const cuuint64_t dims[4] = {kHeadDim, kTile, static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(num_pages)};
-    const cuuint64_t strides[3] = {kHeadDim * es, kTile * kHeadDim * es, static_cast<cuuint64_t>(hkv) * kTile * kHeadDim * es};
-    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / es), kTile, 1, 1};
+    const cuuint64_t row = kHeadDim * es, P = static_cast<cuuint64_t>(page), H = static_cast<cuuint64_t>(hkv);
+    const cuuint64_t dims[4] = {kHeadDim, nhd ? H : P, nhd ? P : H, static_cast<cuuint64_t>(num_pages)};
+    const cuuint64_t strides[3] = {nhd ? row : row, nhd ? H * row : P * row, P * H * row};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / es), nhd ? 1u : static_cast<cuuint32_t>(page),
+                               nhd ? static_cast<cuuint32_t>(page) : 1u, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(m, kv == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
                     const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1761,8 +1794,8 @@ template <int KV, int STAGES, int GROUPS, bool PERSIST, bool FUSE = false, int M
 dsa_status launch(const AttnArgs &a, const KernelParams &kp, dim3 grid, cudaStream_t st) {
     using L = Layout<KV, STAGES, GROUPS, MSLOTS, QW>;
     CUtensorMap km, vm;
-    if (!make_pool_map(&km, a.k_pages, KV, a.num_pages, a.num_kv_heads) ||
-        !make_pool_map(&vm, a.v_pages, KV, a.num_pages, a.num_kv_heads))
+    if (!make_pool_map(&km, a.k_pages, KV, a.num_pages, a.num_kv_heads, a.page_size, a.kv_layout == DSA_NHD) ||
+        !make_pool_map(&vm, a.v_pages, KV, a.num_pages, a.num_kv_heads, a.page_size, a.kv_layout == DSA_NHD))
         return DSA_ERR_CUDA;
     auto kern = attn_kernel<KV, STAGES, GROUPS, PERSIST, FUSE, MSLOTS, QW>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
@@ -1786,6 +1819,8 @@ KernelParams base_params(const AttnArgs &a, float *partial_o, float *partial_lse
     kp.num_units = a.batch * a.num_kv_heads;
     kp.q_len = 1;
     kp.slots_per_desc = 1;
+    kp.page_size = a.page_size;
+    kp.nhd = a.kv_layout == DSA_NHD;
     kp.score_scale = a.sm_scale * kLog2e;
     kp.partial_o = partial_o;
     kp.partial_lse = partial_lse;
@@ -1820,18 +1855,27 @@ dsa_status launch_persistent(const AttnArgs &a, const KernelParams &kp, int num_
 
 using namespace dsa;
 
-extern "C" dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *q_scale, const void *k_pages,
-                                 const void *v_pages, dsa_dtype kv_dtype, const float *k_scale,
-                                 const float *v_scale, const int32_t *block_table, int32_t max_pages_per_req,
-                                 int32_t num_pages, const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
-                                 int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
-                                 const dsa_task_map *map, float *partial_o, float *partial_lse,
-                                 dsa_stream stream) {
+extern "C" int32_t dsa_multi_slots_per_desc(int32_t q_len, int32_t group) {
+    if (q_len < 1 || group < 1) return -1;
+    return q_len > 1 && q_len * group > 16 ? 2 : 1;
+}
+
+extern "C" dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void *q, dsa_dtype q_dtype,
+                                    const float *q_scale, const void *k_pages, const void *v_pages,
+                                    dsa_dtype kv_dtype, const float *k_scale, const float *v_scale,
+                                    const int32_t *block_table, int32_t max_pages_per_req, int32_t num_pages,
+                                    const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
+                                    const dsa_task_map *map, float *partial_o, float *partial_lse,
+                                    dsa_stream stream) {
     const AttnArgs a{q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale, block_table,
                      max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
-                     page_size, sm_scale};
+                     page_size, sm_scale, kv_layout};
     dsa_status s = validate_attn(a);
     if (s != DSA_OK) return s;
+    if (q_len < 1) return DSA_ERR_INVALID_ARG;
+    const int R = q_len * (num_q_heads / num_kv_heads);
+    if (q_len > 1 && (R > kMaxRows || kv_dtype != DSA_BF16)) return DSA_ERR_UNSUPPORTED;
     if (!map || !map->cta_desc_begin || !map->descs || !map->meta || !partial_o || !partial_lse)
         return DSA_ERR_INVALID_ARG;
     if (map->num_units != batch * num_kv_heads || map->num_ctas < 1) return DSA_ERR_INVALID_ARG;
@@ -1841,13 +1885,30 @@ extern "C" dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *
     kp.max_slots = map->max_descs;
     kp.cta_desc_begin = map->cta_desc_begin;
     kp.descs = reinterpret_cast<const int4 *>(map->descs);
-    if (kv_dtype == DSA_BF16) return launch_persistent<0, false>(a, kp, map->num_ctas, to_cuda(stream));
-    return launch_persistent<1, false>(a, kp, map->num_ctas, to_cuda(stream));
+    if (q_len == 1) {
+        if (kv_dtype == DSA_BF16) return launch_persistent<0, false>(a, kp, map->num_ctas, to_cuda(stream));
+        return launch_persistent<1, false>(a, kp, map->num_ctas, to_cuda(stream));
+    }
+    kp.q_len = q_len;
+    kp.slots_per_desc = dsa_multi_slots_per_desc(q_len, num_q_heads / num_kv_heads);
+    const dim3 grid(map->num_ctas);
+    // up to 16 query rows: mma.sync warps (8 warps, 32 tokens x 8 rows each); more rows:
+    // the tensor-memory kernel (measured faster from 24 rows up, slower at 16)
+    if (kp.slots_per_desc == 1)
+        return launch<0, kPersistStagesBf16, kPersistGroups, true, false, 1, 1>(a, kp, grid, to_cuda(stream));
+    return launch<0, kTcStages, 2, true, false, 1, 3>(a, kp, grid, to_cuda(stream));
 }
 
-extern "C" int32_t dsa_multi_slots_per_desc(int32_t q_len, int32_t group) {
-    if (q_len < 1 || group < 1) return -1;
-    return q_len > 1 && q_len * group > 16 ? 2 : 1;
+extern "C" dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *q_scale, const void *k_pages,
+                                 const void *v_pages, dsa_dtype kv_dtype, const float *k_scale,
+                                 const float *v_scale, const int32_t *block_table, int32_t max_pages_per_req,
+                                 int32_t num_pages, const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
+                                 const dsa_task_map *map, float *partial_o, float *partial_lse,
+                                 dsa_stream stream) {
+    return dsa_decode_ex(1, DSA_HND, q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale,
+                         block_table, max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads,
+                         head_dim, page_size, sm_scale, map, partial_o, partial_lse, stream);
 }
 
 extern "C" dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q_dtype, const float *q_scale,
@@ -1857,35 +1918,9 @@ extern "C" dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q
                                        int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                        int32_t page_size, float sm_scale, const dsa_task_map *map, float *partial_o,
                                        float *partial_lse, dsa_stream stream) {
-    if (q_len == 1)
-        return dsa_decode(q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale, block_table,
-                          max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
-                          page_size, sm_scale, map, partial_o, partial_lse, stream);
-    const AttnArgs a{q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale, block_table,
-                     max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
-                     page_size, sm_scale};
-    dsa_status s = validate_attn(a);
-    if (s != DSA_OK) return s;
-    if (q_len < 1) return DSA_ERR_INVALID_ARG;
-    const int R = q_len * (num_q_heads / num_kv_heads);
-    if (R > kMaxRows || kv_dtype != DSA_BF16) return DSA_ERR_UNSUPPORTED;
-    if (!map || !map->cta_desc_begin || !map->descs || !map->meta || !partial_o || !partial_lse)
-        return DSA_ERR_INVALID_ARG;
-    if (map->num_units != batch * num_kv_heads || map->num_ctas < 1) return DSA_ERR_INVALID_ARG;
-    if (!aligned16(partial_o) || !aligned16(map->descs)) return DSA_ERR_INVALID_ARG;
-    if (batch == 0) return DSA_OK;
-    KernelParams kp = base_params(a, partial_o, partial_lse, map->meta + 3);
-    kp.q_len = q_len;
-    kp.slots_per_desc = dsa_multi_slots_per_desc(q_len, num_q_heads / num_kv_heads);
-    kp.max_slots = map->max_descs;
-    kp.cta_desc_begin = map->cta_desc_begin;
-    kp.descs = reinterpret_cast<const int4 *>(map->descs);
-    const dim3 grid(map->num_ctas);
-    // up to 16 query rows: mma.sync warps (8 warps, 32 tokens x 8 rows each); more rows:
-    // the tensor-memory kernel (measured faster from 24 rows up, slower at 16)
-    if (kp.slots_per_desc == 1)
-        return launch<0, kPersistStagesBf16, kPersistGroups, true, false, 1, 1>(a, kp, grid, to_cuda(stream));
-    return launch<0, kTcStages, 2, true, false, 1, 3>(a, kp, grid, to_cuda(stream));
+    return dsa_decode_ex(q_len, DSA_HND, q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale,
+                         block_table, max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads,
+                         head_dim, page_size, sm_scale, map, partial_o, partial_lse, stream);
 }
 
 extern "C" dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_scale, const void *k_pages,

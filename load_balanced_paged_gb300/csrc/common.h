@@ -63,6 +63,7 @@ struct AttnArgs {
     int32_t head_dim;
     int32_t page_size;
     float sm_scale;
+    int32_t kv_layout = DSA_HND;  // dsa_kv_layout
 };
 
 dsa_status validate_attn(const AttnArgs &a);

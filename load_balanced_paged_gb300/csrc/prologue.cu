@@ -44,6 +44,8 @@ struct ProParams {
     int32_t hadamard;
     const int32_t *slots;
     int64_t num_slots;  // num_pages * page_size
+    int32_t page_shift; // log2(page_size): page size 16, 32 or 64
+    int32_t nhd;        // pages [num_pages][P][Hkv][128] instead of [num_pages][Hkv][P][128]
     void *q_out;
     float *q_scale;
     int32_t q_fp8;
@@ -214,8 +216,9 @@ __device__ __forceinline__ float rms_norm_weight(const float *w, float eps, int 
 // 448 (1 for a zero row) with values z * (448 / amax(z)), which f does not change, and
 // the stored scale amax(z) * f / 448.  bf16: z * f rounded.  The amax shuffles are taken
 // by every lane.
+// row: the 128-element row written in base; srow: the scale's index (FP8)
 __device__ __forceinline__ void encode_store(int l, float (&y)[4][8], float f, bool fp8, bool store, void *base,
-                                             int64_t row, float *scale_out) {
+                                             int64_t row, int64_t srow, float *scale_out) {
     if (fp8) {
         float m = 0.f;
 #pragma unroll
@@ -233,7 +236,7 @@ __device__ __forceinline__ void encode_store(int l, float (&y)[4][8], float f, b
             v.y = f32x2_to_e4m3x2(y[c][4] * inv, y[c][5] * inv) | (uint32_t(f32x2_to_e4m3x2(y[c][6] * inv, y[c][7] * inv)) << 16);
             *reinterpret_cast<uint2 *>(dst + 32 * c) = v;
         }
-        if (l == 0) scale_out[row] = amax > 0.f ? amax * f / kE4m3Max : 1.f;
+        if (l == 0) scale_out[srow] = amax > 0.f ? amax * f / kE4m3Max : 1.f;
     } else {
         if (!store) return;
         uint16_t *dst = static_cast<uint16_t *>(base) + row * kHeadDim + 8 * l;
@@ -271,6 +274,11 @@ __global__ void __launch_bounds__(kProWarps * 32, kProCtasPerSm) prologue_kernel
         }
         const int64_t slot = p.slots[n];
         const bool slot_ok = slot >= 0 && slot < p.num_slots;
+        // cache row of KV head h: HND (page * Hkv + h) * P + offset, NHD slot * Hkv + h; the
+        // FP8 scales are [num_pages][Hkv][P] in both
+        const int64_t page = slot >> p.page_shift, off = slot - (page << p.page_shift);
+        auto kv_row = [&](int h) { return p.nhd ? slot * p.hkv + h : ((page * p.hkv + h) << p.page_shift) + off; };
+        auto kv_srow = [&](int h) { return ((page * p.hkv + h) << p.page_shift) + off; };
         if (valid && l == 0 && hb == 0 && p.status) {
             if (!pos_ok) atomicOr(p.status, DSA_DEV_BAD_POSITION);
             if (slot < -1 || slot >= p.num_slots) atomicOr(p.status, DSA_DEV_BAD_PAGE);
@@ -299,14 +307,15 @@ __global__ void __launch_bounds__(kProWarps * 32, kProCtasPerSm) prologue_kernel
                 }
                 if (is_q) {
                     const int64_t row = static_cast<int64_t>(n) * p.hq + j;
-                    encode_store(l, y, f, p.q_fp8, valid && pos_ok, p.q_out, row, p.q_scale);
+                    encode_store(l, y, f, p.q_fp8, valid && pos_ok, p.q_out, row, row, p.q_scale);
                 } else {
-                    const int64_t row = ((slot >> 6) * p.hkv + (j - p.hq)) * kTile + (slot & 63);
-                    encode_store(l, y, f, p.kv_fp8, valid && pos_ok && slot_ok, p.k_pages, row, p.k_scale);
+                    const int h = j - p.hq;
+                    encode_store(l, y, f, p.kv_fp8, valid && pos_ok && slot_ok, p.k_pages, kv_row(h), kv_srow(h),
+                                 p.k_scale);
                 }
             } else {
-                const int64_t row = ((slot >> 6) * p.hkv + (j - p.hq - p.hkv)) * kTile + (slot & 63);
-                encode_store(l, y, 1.f, p.kv_fp8, valid && slot_ok, p.v_pages, row, p.v_scale);
+                const int h = j - p.hq - p.hkv;
+                encode_store(l, y, 1.f, p.kv_fp8, valid && slot_ok, p.v_pages, kv_row(h), kv_srow(h), p.v_scale);
             }
         }
     }
@@ -324,9 +333,11 @@ extern "C" dsa_status dsa_prologue(const void *qkv, int32_t n_tokens, int32_t nu
                                    int32_t hadamard, const int32_t *slot_mapping, void *q_out, dsa_dtype q_dtype,
                                    float *q_scale, void *k_pages, void *v_pages, dsa_dtype kv_dtype,
                                    float *k_scale, float *v_scale, int32_t num_pages, int32_t page_size,
-                                   int32_t *status, dsa_stream stream) {
+                                   int32_t kv_layout, int32_t *status, dsa_stream stream) {
     if (n_tokens < 0 || num_q_heads < 1 || num_kv_heads < 1 || num_pages < 0) return DSA_ERR_INVALID_ARG;
-    if (head_dim != kHeadDim || page_size != kTile) return DSA_ERR_UNSUPPORTED;
+    if (head_dim != kHeadDim || !(page_size == 16 || page_size == 32 || page_size == kTile))
+        return DSA_ERR_UNSUPPORTED;
+    if (kv_layout != DSA_HND && kv_layout != DSA_NHD) return DSA_ERR_INVALID_ARG;
     if (!(rotary_dim == 0 || rotary_dim == 16 || rotary_dim == 32 || rotary_dim == 64 || rotary_dim == 128))
         return DSA_ERR_UNSUPPORTED;
     if (rope_style != DSA_ROPE_NEOX && rope_style != DSA_ROPE_INTERLEAVED) return DSA_ERR_INVALID_ARG;
@@ -374,7 +385,9 @@ extern "C" dsa_status dsa_prologue(const void *qkv, int32_t n_tokens, int32_t nu
     p.eps = norm_eps;
     p.hadamard = hadamard != 0;
     p.slots = slot_mapping;
-    p.num_slots = static_cast<int64_t>(num_pages) * kTile;
+    p.num_slots = static_cast<int64_t>(num_pages) * page_size;
+    p.page_shift = page_size == 16 ? 4 : page_size == 32 ? 5 : 6;
+    p.nhd = kv_layout == DSA_NHD;
     p.q_out = q_out;
     p.q_scale = q_scale;
     p.q_fp8 = q_dtype == DSA_FP8_E4M3;

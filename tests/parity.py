@@ -75,7 +75,9 @@ def assert_lse_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
 def problem_from_host(h: dict, inp: dict) -> oracle.Problem:
     return oracle.Problem(h["q"], h["k_pages"], h["v_pages"], h["block_table"], h["seq_lens"],
                           inp["num_q_heads"], inp["num_kv_heads"], inp["sm_scale"],
-                          q_scale=h["q_scale"], k_scale=h["k_scale"], v_scale=h["v_scale"])
+                          q_scale=h["q_scale"], k_scale=h["k_scale"], v_scale=h["v_scale"],
+                          page_size=inp.get("page_size", 64), q_len=inp.get("q_len", 1),
+                          kv_layout=inp.get("kv_layout", "HND"))
 
 
 def np_bytes(t):

@@ -89,13 +89,33 @@ def test_decode_host_checks(lib):
         return lib.dsa_decode(fake, q_dt, scales, fake, fake, kv_dt, scales, scales, fake, 4, 8, fake,
                               batch, hq, hkv, d, page, sm, ctypes.byref(tm), fake, fake, None)
     assert call(d=64) == 2
-    assert call(page=16) == 2
+    assert call(page=8) == 2               # page sizes 16, 32 and 64 only
+    assert call(page=48) == 2
+    assert call(page=128) == 2
     assert call(hq=63) == 1
     assert call(hq=128, hkv=8) == 2        # G = 16 not built
     assert call(q_dt=0, kv_dt=1) == 2      # mixed dtypes not built
     assert call(q_dt=1, kv_dt=1) == 1      # E4M3 without scales
     assert call(sm=float("nan")) == 1
     assert call(batch=3) == 1              # map sized for another batch
+
+
+def test_decode_ex_host_checks(lib):
+    fake = ctypes.c_void_p(0x10000)
+    tm = TaskMap(fake, fake, fake, fake, fake, 10, 4, 16)
+    i, f, V = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
+    lib.dsa_decode_ex.argtypes = [i, i, V, i, V, V, V, i, V, V, V, i, i, V, i, i, i, i, i, f,
+                                  ctypes.POINTER(TaskMap), V, V, V]
+
+    def call(q_len=1, layout=1, kv_dt=0, hq=64, hkv=8, page=16):
+        return lib.dsa_decode_ex(q_len, layout, fake, 0, None, fake, fake, kv_dt, None, None, fake, 4, 8, fake,
+                                 2, hq, hkv, 128, page, 0.1, ctypes.byref(tm), fake, fake, None)
+    assert call(layout=2) == 1              # not a dsa_kv_layout
+    assert call(layout=-1) == 1
+    assert call(page=8) == 2
+    assert call(q_len=0) == 1
+    assert call(q_len=9) == 2               # 9 x 8 = 72 query rows per unit
+    assert call(q_len=2, kv_dt=1) == 2      # multi-token E4M3 not built
 
 
 def test_status_strings(lib):

@@ -33,31 +33,36 @@ def host_u16(t):
     return t.cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-def empty_cache(num_pages, hkv, kind):
-    shape = (num_pages, hkv, 64, D)
+def empty_cache(num_pages, hkv, kind, page=64, layout="HND"):
+    """num_pages pages of 64 tokens' worth of slots, held in pages of `page` tokens."""
+    num_pages = num_pages * 64 // page
+    shape = (num_pages, page, hkv, D) if layout == "NHD" else (num_pages, hkv, page, D)
     if kind == "bf16":
         kp = torch.full(shape, SENTINEL_BF16, dtype=torch.bfloat16, device="cuda")
         vp = torch.full(shape, SENTINEL_BF16, dtype=torch.bfloat16, device="cuda")
         return kp, vp, None, None
     kp = torch.full(shape, SENTINEL_U8, dtype=torch.uint8, device="cuda")
     vp = torch.full(shape, SENTINEL_U8, dtype=torch.uint8, device="cuda")
-    ks = torch.full(shape[:3], SENTINEL_SCALE, dtype=torch.float32, device="cuda")
-    vs = torch.full(shape[:3], SENTINEL_SCALE, dtype=torch.float32, device="cuda")
+    ks = torch.full((num_pages, hkv, page), SENTINEL_SCALE, dtype=torch.float32, device="cuda")
+    vs = torch.full((num_pages, hkv, page), SENTINEL_SCALE, dtype=torch.float32, device="cuda")
     return kp, vp, ks, vs
 
 
-def run(dsa, n, hq, hkv, q_kind, kv_kind, rot, style, norm, had, seed=0, max_position=4096):
+def run(dsa, n, hq, hkv, q_kind, kv_kind, rot, style, norm, had, seed=0, max_position=4096, page=64,
+        layout="HND"):
     num_pages = math.ceil(n / 64) + 3
     inp = workloads.make_prologue_inputs(n, hq, hkv, num_pages, seed=seed, device="cuda",
                                          rotary_dim=rot or 128, max_position=max_position)
-    kp, vp, ks, vs = empty_cache(num_pages, hkv, kv_kind)
+    inp["page_size"], inp["kv_layout"] = page, layout
+    kp, vp, ks, vs = empty_cache(num_pages, hkv, kv_kind, page, layout)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     q, qs = dsa.prologue(inp["qkv"], hq, hkv, inp["slot_mapping"], kp, vp, ks, vs,
                          positions=inp["positions"] if rot else None,
                          cos_sin=inp["cos_sin"] if rot else None, rotary_dim=rot, rope_style=style,
                          q_norm_weight=inp["q_norm_weight"] if norm else None,
                          k_norm_weight=inp["k_norm_weight"] if norm else None, eps=EPS, hadamard=had,
-                         q_dtype=torch.uint8 if q_kind == "e4m3" else torch.bfloat16, status=status)
+                         q_dtype=torch.uint8 if q_kind == "e4m3" else torch.bfloat16, status=status,
+                         kv_layout=layout)
     torch.cuda.synchronize()
     assert dsa.read_status(status) == 0
     return inp, (q, qs, kp, vp, ks, vs)
@@ -80,12 +85,16 @@ def check(inp, got, q_kind, kv_kind, rot, style, norm, had, what):
 
     assert_encoded(codes(q), None if qs is None else qs.cpu().numpy(), q64, q_kind, err(q64), what + " Q")
     slots = inp["slot_mapping"].cpu().numpy()
-    writes = P.cache_writes(slots, 64)
+    page, nhd = inp.get("page_size", 64), inp.get("kv_layout", "HND") == "NHD"
+    writes = P.cache_writes(slots, page)
     toks = np.array(sorted(writes), dtype=np.int64)
     pages = np.array([writes[t][0] for t in toks], dtype=np.int64)
     offs = np.array([writes[t][1] for t in toks], dtype=np.int64)
-    kc, vc = codes(kp), codes(vp)                         # [pages, hkv, 64, D]
-    gk, gv = kc[pages, :, offs], vc[pages, :, offs]       # [tokens, hkv, D]
+    kc, vc = codes(kp), codes(vp)                         # [pages, hkv, P, D] or [pages, P, hkv, D]
+    if nhd:
+        gk, gv = kc[pages, offs], vc[pages, offs]         # [tokens, hkv, D]
+    else:
+        gk, gv = kc[pages, :, offs], vc[pages, :, offs]
     gks = None if ks is None else ks.cpu().numpy()[pages, :, offs]
     gvs = None if vs is None else vs.cpu().numpy()[pages, :, offs]
     assert_encoded(gk, gks, k64[toks], kv_kind, err(k64[toks]), what + " K")
@@ -94,12 +103,16 @@ def check(inp, got, q_kind, kv_kind, rot, style, norm, had, what):
         x = host_u16(inp["qkv"]).reshape(n, hq + 2 * hkv, D)[toks, hq + hkv:]
         assert np.array_equal(gv, x)
     # slots no token maps to keep their old contents
-    untouched = np.ones(kc.shape[0] * 64, bool)
-    untouched[pages * 64 + offs] = False
+    untouched = np.ones(kc.shape[0] * page, bool)
+    untouched[pages * page + offs] = False
     sent = np.uint16(0x4040) if kv_kind == "bf16" else np.uint8(SENTINEL_U8)
     for c in (kc, vc):
-        rest = c.transpose(0, 2, 1, 3).reshape(-1, hkv, D)[untouched]
+        rest = (c if nhd else c.transpose(0, 2, 1, 3)).reshape(-1, hkv, D)[untouched]
         assert (rest == sent).all()
+    for s_ in (ks, vs):
+        if s_ is not None:
+            rest = s_.cpu().numpy().transpose(0, 2, 1).reshape(-1, hkv)[untouched]
+            assert (rest == SENTINEL_SCALE).all()
     return len(toks)
 
 
@@ -123,6 +136,15 @@ def test_prologue_vs_oracle(dsa, case):
     inp, got = run(dsa, n, hq, hkv, qk, kvk, rot, style, norm, had, seed=n)
     written = check(inp, got, qk, kvk, rot, style, norm, had, str(case))
     assert written > 0
+
+
+@pytest.mark.parametrize("page,layout", [(16, "HND"), (16, "NHD"), (32, "NHD"), (64, "NHD")])
+@pytest.mark.parametrize("kinds", [("e4m3", "e4m3"), ("bf16", "bf16")])
+def test_prologue_page_layouts(dsa, page, layout, kinds):
+    """Cache writes into pages of 16 / 32 / 64 tokens in either layout."""
+    inp, got = run(dsa, 300, 16, 4, kinds[0], kinds[1], 128, "neox", True, True, seed=page, page=page,
+                   layout=layout)
+    check(inp, got, kinds[0], kinds[1], 128, "neox", True, True, f"P {page} {layout}")
 
 
 @pytest.mark.parametrize("kinds", [("e4m3", "e4m3"), ("bf16", "bf16")])
@@ -172,26 +194,32 @@ def test_host_validation(dsa):
         k8, v8, _, _ = empty_cache(1, 1, "e4m3")
         dsa.prologue(inp["qkv"], 8, 1, inp["slot_mapping"], k8, v8, **args)
     assert e.value.code == dsa.ERR_INVALID_ARG
+    with pytest.raises(dsa.DSAError) as e:     # pages of 8 tokens
+        k8, v8, _, _ = empty_cache(1, 1, "bf16", page=8)
+        dsa.prologue(inp["qkv"], 8, 1, inp["slot_mapping"], k8, v8, **args)
+    assert e.value.code == dsa.ERR_UNSUPPORTED
     q, _ = dsa.prologue(inp["qkv"][:0], 8, 1, inp["slot_mapping"][:0], kp, vp, **args)   # no tokens
     assert q.shape[0] == 0
 
 
-def test_prologue_feeds_decode(dsa):
+@pytest.mark.parametrize("page,layout", [(64, "HND"), (16, "NHD"), (32, "HND")])
+def test_prologue_feeds_decode(dsa, page, layout):
     """The prologue writes each request's newest token (Q, and K/V at its cache slot) into
     an FP8 decode step; the step's output matches the oracle on the bytes it read."""
     lens = [17, 64, 200, 1500, 1]
     hq, hkv = 16, 2
-    inp = workloads.make_inputs(lens, hq, hkv, "fp8", seed=21, device="cuda")
+    inp = workloads.make_inputs(lens, hq, hkv, "fp8", seed=21, device="cuda", page_size=page, kv_layout=layout)
     B = len(lens)
     bt = inp["block_table"].cpu().numpy()
     pos = np.array([L - 1 for L in lens], np.int32)
-    slots = np.array([bt[b, p // 64] * 64 + p % 64 for b, p in enumerate(pos)], np.int32)
+    slots = np.array([bt[b, p // page] * page + p % page for b, p in enumerate(pos)], np.int32)
     pro = workloads.make_prologue_inputs(B, hq, hkv, 1, seed=22, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     q, qs = dsa.prologue(pro["qkv"], hq, hkv, torch.from_numpy(slots).cuda(), inp["k_pages"], inp["v_pages"],
                          inp["k_scale"], inp["v_scale"], positions=torch.from_numpy(pos).cuda(),
                          cos_sin=pro["cos_sin"], q_norm_weight=pro["q_norm_weight"],
-                         k_norm_weight=pro["k_norm_weight"], hadamard=True, q_dtype=torch.uint8, status=status)
+                         k_norm_weight=pro["k_norm_weight"], hadamard=True, q_dtype=torch.uint8, status=status,
+                         kv_layout=layout)
     assert dsa.read_status(status) == 0
     inp["q"], inp["q_scale"] = q, qs
     sms = torch.cuda.get_device_properties(0).multi_processor_count
