@@ -226,6 +226,13 @@ __device__ __forceinline__ void cvt_pair(uint32_t x, uint32_t &lo, uint32_t &hi)
     hi = e4m3x2_to_f16x2(static_cast<uint16_t>(y >> 16));
 }
 
+// Byte offset of tile row r (a token) in a bf16 stage laid out [page][half][P rows][128 B]
+// (P = 64: [half][64 rows][128 B]); the second 128-B half of the row is P * 128 bytes on.
+// Pages are 1024-byte aligned in the stage, so the 128-byte swizzle phase is still r & 7.
+__device__ __forceinline__ uint32_t kv_row_off(int r, int P) {
+    return static_cast<uint32_t>(r + (r & -P)) * 128u;
+}
+
 __device__ __forceinline__ uint32_t tok_mask(int t, int nv) {
     return (t < nv ? 0x0000FFFFu : 0u) | (t + 1 < nv ? 0xFFFF0000u : 0u);
 }
@@ -626,23 +633,28 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                             if (nv_l > 0) {
                                 const uint32_t kdst = sbase + stage * L::kStageBytes;
                                 const uint32_t vdst = kdst + C::kTileBytes;
-                                // the pages holding valid tokens, P rows each: box (column, head, slot
-                                // 0, page) lands as P rows of 128 B at row k * P of the tile
+                                // the pages holding valid tokens, one box of P rows each (both 128-B
+                                // halves of a bf16 row: the stage is [page][half][P rows][128 B]);
+                                // the tensor-core kernel's operands want [half][64 rows][128 B],
+                                // so there each half of a page smaller than the tile is its own box
                                 const int nsub = (nv_l + P - 1) / P;
                                 mbar_arrive_expect_tx(fb, nsub * (L::kStageTx / ppt));
 #pragma unroll
                                 for (int k = 0; k < kMaxPagesPerTile; ++k) {
                                     if (k >= nsub) break;
-                                    const int pg = cpg[k], y = p.nhd ? h_l : 0, z = p.nhd ? 0 : h_l;
-                                    const uint32_t ro = static_cast<uint32_t>(k * P) * 128u;
-                                    if (KV == 0) {  // two 64-column boxes per 128-wide bf16 row
-                                        tma_load_4d(kdst + ro, &kmap, fb, 0, y, z, pg, policy);
-                                        tma_load_4d(kdst + C::kTileBytes / 2 + ro, &kmap, fb, 64, y, z, pg, policy);
-                                        tma_load_4d(vdst + ro, &vmap, fb, 0, y, z, pg, policy);
-                                        tma_load_4d(vdst + C::kTileBytes / 2 + ro, &vmap, fb, 64, y, z, pg, policy);
+                                    const int pg = cpg[k];
+                                    if (QW == 3 && P < kTile) {
+                                        const uint32_t ro = static_cast<uint32_t>(k * P) * 128u;
+                                        tma_load_5d(kdst + ro, &kmap, fb, 0, 0, 0, h_l, pg, policy);
+                                        tma_load_5d(kdst + C::kTileBytes / 2 + ro, &kmap, fb, 0, 0, 1, h_l, pg, policy);
+                                        tma_load_5d(vdst + ro, &vmap, fb, 0, 0, 0, h_l, pg, policy);
+                                        tma_load_5d(vdst + C::kTileBytes / 2 + ro, &vmap, fb, 0, 0, 1, h_l, pg, policy);
                                     } else {
-                                        tma_load_4d(kdst + ro, &kmap, fb, 0, y, z, pg, policy);
-                                        tma_load_4d(vdst + ro, &vmap, fb, 0, y, z, pg, policy);
+                                        const uint32_t ro = static_cast<uint32_t>(k * P) * (C::kTileBytes / kTile);
+                                        tma_load_5d(kdst + ro, &kmap, fb, 0, 0, 0, h_l, pg, policy);
+                                        tma_load_5d(vdst + ro, &vmap, fb, 0, 0, 0, h_l, pg, policy);
+                                    }
+                                    if (KV == 1) {
                                         const int64_t srow = (static_cast<int64_t>(pg) * p.hkv + h_l) * P;
                                         bulk_load(vdst + C::kTileBytes + 4 * k * P, p.k_scale + srow, 4 * P, fb);
                                         bulk_load(vdst + C::kTileBytes + C::kScaleBytes + 4 * k * P, p.v_scale + srow,
@@ -1174,6 +1186,10 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
         const int k_chunk = lane >> 4;
         const int v_row = tok_base + xr + (lane >> 4) * 8;
         const int v_chunk = (lane >> 3) & 1;
+        // byte offsets of this lane's rows in the stage ([page][half][P rows][128 B])
+        const uint32_t half_off = static_cast<uint32_t>(p.page_size) * 128u;
+        const uint32_t k_off[2] = {kv_row_off(k_row, p.page_size), kv_row_off(k_row + 16, p.page_size)};
+        const uint32_t v_off[2] = {kv_row_off(v_row, p.page_size), kv_row_off(v_row + 16, p.page_size)};
         float *pair = reinterpret_cast<float *>(smem + L::kMergeOff) + cs * L::kPairFloats;
 
         for (int qi = 0;; ++qi) {
@@ -1242,8 +1258,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         const int ch = 2 * ks + k_chunk;
 #pragma unroll
                         for (int kt = 0; kt < 2; ++kt) {
-                            const uint32_t addr =
-                                kbase + (ch >> 3) * (C::kTileBytes / 2) + (k_row + 16 * kt) * 128 + (((ch & 7) ^ xr) << 4);
+                            const uint32_t addr = kbase + (ch >> 3) * half_off + k_off[kt] + (((ch & 7) ^ xr) << 4);
                             uint32_t a0, a1, a2, a3;
                             ldsm_x4(addr, a0, a1, a2, a3);
 #pragma unroll
@@ -1313,8 +1328,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         const int ch = 2 * mb + v_chunk;
 #pragma unroll
                         for (int kt = 0; kt < 2; ++kt) {
-                            const uint32_t addr =
-                                vbase + (ch >> 3) * (C::kTileBytes / 2) + (v_row + 16 * kt) * 128 + (((ch & 7) ^ xr) << 4);
+                            const uint32_t addr = vbase + (ch >> 3) * half_off + v_off[kt] + (((ch & 7) ^ xr) << 4);
                             uint32_t a0, a1, a2, a3;
                             ldsm_x4_trans(addr, a0, a1, a2, a3);
                             if (partial) {
@@ -1431,6 +1445,9 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
     const int k_chunk = lane >> 4;
     const int v_row = (KV == 0) ? tok_base + xr + (lane >> 4) * 8 : k_row;
     const int v_chunk = (KV == 0) ? ((lane >> 3) & 1) : (lane >> 4);
+    // bf16 stage [page][half][P rows][128 B]: byte offsets of this lane's rows and of the second half
+    const uint32_t half_off = static_cast<uint32_t>(p.page_size) * 128u;
+    const uint32_t k_off = kv_row_off(k_row, p.page_size), v_off = kv_row_off(v_row, p.page_size);
 
     // Merge of descriptor d (states deposited in merge slot d & 1 by all consumer warps):
     // the warps' (m, l, O) combined under one softmax, written as a normalised partial.
@@ -1542,7 +1559,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                     const int ch = 2 * ks + k_chunk;
                     uint32_t addr;
                     if (KV == 0)
-                        addr = kbase + (ch >> 3) * (C::kTileBytes / 2) + k_row * 128 + (((ch & 7) ^ xr) << 4);
+                        addr = kbase + (ch >> 3) * half_off + k_off + (((ch & 7) ^ xr) << 4);
                     else
                         addr = kbase + k_row * 128 + ((ch ^ xr) << 4);
                     uint32_t a0, a1, a2, a3;
@@ -1631,8 +1648,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
 #pragma unroll
                     for (int mb = 0; mb < 8; ++mb) {
                         const int ch = 2 * mb + v_chunk;
-                        const uint32_t addr =
-                            vbase + (ch >> 3) * (C::kTileBytes / 2) + v_row * 128 + (((ch & 7) ^ xr) << 4);
+                        const uint32_t addr = vbase + (ch >> 3) * half_off + v_off + (((ch & 7) ^ xr) << 4);
                         uint32_t a0, a1, a2, a3;
                         ldsm_x4_trans(addr, a0, a1, a2, a3);
                         if (partial) {
@@ -1768,23 +1784,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 4-D view of a page pool with the box = the P tokens of one (page, head) x 128 bytes of the
-// row, 128-byte swizzle.  HND pages [num_pages][Hkv][P][128]: dims (128, P, Hkv, pages),
-// box (128 B, P, 1, 1); NHD pages [num_pages][P][Hkv][128]: dims (128, Hkv, P, pages), box
-// (128 B, 1, P, 1).  Either box lands as P rows of 128 B.
-bool make_pool_map(CUtensorMap *m, const void *pool, int kv, int num_pages, int hkv, int page, bool nhd) {
+// 5-D view (128-byte piece of a row, token in page, piece, KV head, page) of a page pool,
+// 128-byte swizzle.  A bf16 row is two 128-B pieces, an E4M3 row one.  HND pages
+// [num_pages][Hkv][P][128] and NHD pages [num_pages][P][Hkv][128] differ only in the strides.
+// The box is the P tokens of one (page, head): both pieces (lands as [piece][P rows][128 B]),
+// or one piece when `split` (the tensor-core kernel's per-half operand layout).
+bool make_pool_map(CUtensorMap *m, const void *pool, int kv, int num_pages, int hkv, int page, bool nhd,
+                   bool split) {
     std::memset(m, 0, sizeof(*m));
     if (num_pages == 0) return true;  // nothing can be loaded
     auto fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t es = kv == 0 ? 2 : 1;
+    const cuuint64_t es = kv == 0 ? 2 : 1, pieces = kv == 0 ? 2 : 1;
     const cuuint64_t row = kHeadDim * es, P = static_cast<cuuint64_t>(page), H = static_cast<cuuint64_t>(hkv);
-    const cuuint64_t dims[4] = {kHeadDim, nhd ? H : P, nhd ? P : H, static_cast<cuuint64_t>(num_pages)};
-    const cuuint64_t strides[3] = {nhd ? row : row, nhd ? H * row : P * row, P * H * row};
-    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / es), nhd ? 1u : static_cast<cuuint32_t>(page),
-                               nhd ? static_cast<cuuint32_t>(page) : 1u, 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = fn(m, kv == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+    const cuuint64_t dims[5] = {128 / es, P, pieces, H, static_cast<cuuint64_t>(num_pages)};
+    const cuuint64_t strides[4] = {nhd ? H * row : row, 128, nhd ? row : P * row, P * H * row};
+    const cuuint32_t box[5] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(page),
+                               split ? 1u : static_cast<cuuint32_t>(pieces), 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, kv == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
                     const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -1794,8 +1812,9 @@ template <int KV, int STAGES, int GROUPS, bool PERSIST, bool FUSE = false, int M
 dsa_status launch(const AttnArgs &a, const KernelParams &kp, dim3 grid, cudaStream_t st) {
     using L = Layout<KV, STAGES, GROUPS, MSLOTS, QW>;
     CUtensorMap km, vm;
-    if (!make_pool_map(&km, a.k_pages, KV, a.num_pages, a.num_kv_heads, a.page_size, a.kv_layout == DSA_NHD) ||
-        !make_pool_map(&vm, a.v_pages, KV, a.num_pages, a.num_kv_heads, a.page_size, a.kv_layout == DSA_NHD))
+    const bool nhd = a.kv_layout == DSA_NHD, split = QW == 3 && a.page_size < kTile;
+    if (!make_pool_map(&km, a.k_pages, KV, a.num_pages, a.num_kv_heads, a.page_size, nhd, split) ||
+        !make_pool_map(&vm, a.v_pages, KV, a.num_pages, a.num_kv_heads, a.page_size, nhd, split))
         return DSA_ERR_CUDA;
     auto kern = attn_kernel<KV, STAGES, GROUPS, PERSIST, FUSE, MSLOTS, QW>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
