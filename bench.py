@@ -319,6 +319,18 @@ def bench_ours(args, device, rank, world):
         static[label] = {"splits": S, "us_per_step": round(s_ms * 1e3, 2),
                          "speedup_of_dynamic": round(s_ms / (t_dec + t_comb), 3),
                          "speedup_of_dynamic_with_plan": round(s_ms / ms_per_step, 3)}
+        # how evenly the static grid's CTAs finish (one untimed launch with per-CTA timestamps)
+        st_times = torch.zeros(B * hkv * S, 2, dtype=torch.int64, device=device)
+        dsa.static_splitkv(mode, param, max_len, inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"],
+                           inp["seq_lens"], hkv, inp["sm_scale"], partial_o=spo, partial_lse=spl, status=sst,
+                           cta_times=st_times, **kw)
+        static[label]["balance"] = cta_balance(st_times)
+
+    # the same for the persistent kernel's bins
+    dyn_times = torch.zeros(C, 2, dtype=torch.int64, device=device)
+    dsa.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
+               inp["sm_scale"], partial_o=po, partial_lse=pl, cta_times=dyn_times, **kw)
+    balance = cta_balance(dyn_times)
 
     prologue = bench_prologue(dsa, device, w, B, timed, max(10, min(args.steps, 200)))
     # multi-token steps use one bin per SM: the tensor-memory kernel holds one CTA per SM
@@ -387,6 +399,7 @@ def bench_ours(args, device, rank, world):
         "prologue": prologue,
         "multi_token": multi,
         "page_layouts": layouts,
+        "balance": balance,
         "roofline": {"bound": "hbm", "kernel": "attn_kernel (persistent decode, dsa_decode)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
@@ -490,6 +503,21 @@ def bench_multi(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes: 
     return res
 
 
+def cta_balance(times: torch.Tensor) -> dict:
+    """Per-CTA [start, end] timer readings (ns) of one launch: the span from the first start
+    to the last end, and the idle tail = (last end - median end) / span, the share of the
+    launch during which at least half of the CTAs had already finished."""
+    t = times.cpu().numpy().astype(np.int64)
+    t = t[t[:, 1] > 0]
+    if t.size == 0:
+        return {}
+    start, end = t[:, 0], t[:, 1]
+    span = float(end.max() - start.min())
+    return {"ctas": int(t.shape[0]), "span_us": round(span / 1e3, 2),
+            "idle_tail": round(float(end.max() - np.median(end)) / span, 4) if span > 0 else 0.0,
+            "end_spread_us": round(float(end.max() - end.min()) / 1e3, 2)}
+
+
 def bench_layouts(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes: int, base_ms: float) -> dict:
     """The decode kernel on the same lengths and C bins with the KV held in pages of 16 / 32 /
     64 tokens, HND or NHD (dsa_decode_ex): a 64-token tile is then loaded as 64 / P boxes."""
@@ -546,18 +574,18 @@ def oracle_problem(inp, requests):
                           k_scale=pools["k_scale"], v_scale=pools["v_scale"]), lens
 
 
-def cpu_oracle_rate(inp, budget_s: float, rng_seed: int = 0):
-    """Time the oracle (all host threads) on a bounded sample of requests; returns
-    (GB/s of KV processed, threads, description)."""
+def cpu_oracle_rate(inp, budget_s: float, rng_seed: int = 0, threads: int = 0):
+    """Time the oracle (all host threads, or `threads`) on a bounded sample of requests;
+    returns (GB/s of KV processed, threads, description)."""
     import oracle
     lens = inp["seq_lens"].cpu().numpy()
     rng = np.random.default_rng(rng_seed)
     order = rng.permutation(len(lens))
     # calibrate on the shortest request, then take requests until the estimated time fills the budget
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     prob, _ = oracle_problem(inp, [int(np.argmin(lens))])
     t0 = time.perf_counter()
-    prob.attention()
+    prob.attention(n_threads=threads)
     per_token = (time.perf_counter() - t0) / max(int(lens.min()), 1)
     # the oracle runs one thread per (request, KV head) unit
     eff = min(threads, inp["num_kv_heads"] * len(lens))
@@ -569,7 +597,7 @@ def cpu_oracle_rate(inp, budget_s: float, rng_seed: int = 0):
             break
     prob, sl = oracle_problem(inp, chosen)
     t0 = time.perf_counter()
-    prob.attention()
+    prob.attention(n_threads=threads)
     dt = time.perf_counter() - t0
     nbytes = workloads.kv_bytes(sl, inp["num_kv_heads"], inp["kv_dtype"])
     desc = (f"{len(chosen)} of {len(lens)} requests ({int(sl.sum())} of {int(lens.sum())} tokens), "
@@ -613,8 +641,9 @@ def main():
     res, inp, nbytes = bench_ours(args, device, rank, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, desc = cpu_oracle_rate(inp, args.cpu_budget)
+        v1, _, desc1 = cpu_oracle_rate(inp, args.cpu_budget / 3, threads=1)
         res["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                               "sample": desc}
+                               "sample": desc, "one_thread": {"value": round(v1, 4), "sample": desc1}}
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

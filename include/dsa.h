@@ -241,7 +241,11 @@ dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q_dtype, con
  * dsa_decode, q_len > 1 dsa_decode_multi; the results do not depend on the layout
  * or the page size (the same tokens in another arrangement give the same bits).
  * A 64-token tile reads 64 / P pages, each with its own block-table entry; only
- * pages holding a token below the request's length are read.  Errors: a
+ * pages holding a token below the request's length are read.
+ * cta_times: NULL, or device uint64 [map->num_ctas][2]: CTA i writes the global
+ * timer (%globaltimer, ns) when it starts work (after the previous kernel in the
+ * stream has finished) to [i][0], and the time its last warp finished to [i][1]
+ * (a diagnostic of how evenly the bins finish; costs one barrier per CTA).  Errors: a
  * kv_layout outside dsa_kv_layout gives DSA_ERR_INVALID_ARG, other page sizes
  * DSA_ERR_UNSUPPORTED; the rest as for dsa_decode.
  */
@@ -252,7 +256,7 @@ dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void *q, dsa_dt
                          const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
                          int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
                          const dsa_task_map *map, float *partial_o, float *partial_lse,
-                         dsa_stream stream);
+                         uint64_t *cta_times, dsa_stream stream);
 
 /*
  * dsa_combine_multi -- dsa_combine over the q_len * G partial rows of each unit:
@@ -290,8 +294,11 @@ dsa_status dsa_combine(const dsa_task_map *map, const float *partial_o, const fl
  *   o = 0, lse = -inf.  Slot of (u, s) = u*S + s.
  * dsa_static_num_splits returns S (or -1 on bad arguments).
  * partial_o: [B*Hkv*S, G, 128] fp32, partial_lse: [B*Hkv*S, G] fp32.
- * status: device int32 word for DSA_DEV_* bits (may be NULL); a request longer
+ * status: device int32 word for DSA_DEV_* bits (required); a request longer
  * than S*param in mode 1 is not covered and sets DSA_DEV_BAD_SEQLEN.
+ * cta_times: NULL, or device uint64 [S*Hkv*B][2] that receives each CTA's start
+ * and end of work (%globaltimer ns; CTA (s, h, b) at index s + S*(h + Hkv*b)),
+ * as for dsa_decode_ex.
  */
 int32_t dsa_static_num_splits(int32_t mode, int32_t param, int32_t max_seq_len);
 dsa_status dsa_static_splitkv(int32_t mode, int32_t param, int32_t max_seq_len,
@@ -302,7 +309,8 @@ dsa_status dsa_static_splitkv(int32_t mode, int32_t param, int32_t max_seq_len,
                               int32_t num_pages, const int32_t *seq_lens, int32_t batch,
                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                               int32_t page_size, float sm_scale, float *partial_o,
-                              float *partial_lse, int32_t *status, dsa_stream stream);
+                              float *partial_lse, int32_t *status, uint64_t *cta_times,
+                              dsa_stream stream);
 
 /*
  * Combine for the static grid: merges all S slots of each unit, empty ones

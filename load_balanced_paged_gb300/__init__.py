@@ -63,13 +63,13 @@ _lib.dsa_multi_slots_per_desc.argtypes = [_i32, _i32]
 _lib.dsa_multi_slots_per_desc.restype = _i32
 _lib.dsa_decode_multi.argtypes = [_i32] + _attn_args + [_TMP, _vp, _vp, _vp]
 _lib.dsa_decode_multi.restype = ctypes.c_int
-_lib.dsa_decode_ex.argtypes = [_i32, _i32] + _attn_args + [_TMP, _vp, _vp, _vp]
+_lib.dsa_decode_ex.argtypes = [_i32, _i32] + _attn_args + [_TMP, _vp, _vp, _vp, _vp]
 _lib.dsa_decode_ex.restype = ctypes.c_int
 _lib.dsa_combine_multi.argtypes = [_i32, _TMP, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]
 _lib.dsa_combine_multi.restype = ctypes.c_int
 _lib.dsa_static_num_splits.argtypes = [_i32, _i32, _i32]
 _lib.dsa_static_num_splits.restype = _i32
-_lib.dsa_static_splitkv.argtypes = [_i32, _i32, _i32] + _attn_args + [_vp, _vp, _vp, _vp]
+_lib.dsa_static_splitkv.argtypes = [_i32, _i32, _i32] + _attn_args + [_vp, _vp, _vp, _vp, _vp]
 _lib.dsa_static_splitkv.restype = ctypes.c_int
 _lib.dsa_static_combine.argtypes = [_i32, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]
 _lib.dsa_static_combine.restype = ctypes.c_int
@@ -195,20 +195,20 @@ def partial_buffers(max_slots: int, group: int, device="cuda"):
 
 def decode(q, k_pages, v_pages, block_table, seq_lens, task_map: TaskMap, sm_scale: float,
            partial_o=None, partial_lse=None, q_scale=None, k_scale=None, v_scale=None, stream=None,
-           kv_layout="HND"):
-    """dsa_decode (dsa_decode_ex for NHD pages): persistent kernel writing one partial
-    (o, lse) per descriptor."""
+           kv_layout="HND", cta_times=None):
+    """dsa_decode (dsa_decode_ex for NHD pages or per-CTA timestamps, cta_times uint64-sized
+    [num_ctas, 2]): persistent kernel writing one partial (o, lse) per descriptor."""
     G = q.shape[1] // task_map.num_kv_heads
     if partial_o is None:
         partial_o, partial_lse = partial_buffers(task_map.max_descs, G, q.device)
     args = _attn_args(q, k_pages, v_pages, block_table, seq_lens, task_map.num_kv_heads, sm_scale,
                       q_scale, k_scale, v_scale, kv_layout)
-    if kv_layout == "HND":
+    if kv_layout == "HND" and cta_times is None:
         rc = _lib.dsa_decode(*args, ctypes.byref(task_map.struct), _ptr(partial_o), _ptr(partial_lse),
                              _stream(stream))
     else:
         rc = _lib.dsa_decode_ex(1, KV_LAYOUTS[kv_layout], *args, ctypes.byref(task_map.struct), _ptr(partial_o),
-                                _ptr(partial_lse), _stream(stream))
+                                _ptr(partial_lse), _ptr(cta_times), _stream(stream))
     _check(rc, "dsa_decode")
     return partial_o, partial_lse
 
@@ -263,7 +263,7 @@ def decode_multi(q_len: int, q, k_pages, v_pages, block_table, seq_lens, task_ma
                                    _ptr(partial_lse), _stream(stream))
     else:
         rc = _lib.dsa_decode_ex(q_len, KV_LAYOUTS[kv_layout], *args, ctypes.byref(task_map.struct),
-                                _ptr(partial_o), _ptr(partial_lse), _stream(stream))
+                                _ptr(partial_o), _ptr(partial_lse), None, _stream(stream))
     _check(rc, "dsa_decode_multi")
     return partial_o, partial_lse
 
@@ -303,7 +303,7 @@ def static_num_splits(mode: int, param: int, max_seq_len: int) -> int:
 
 def static_splitkv(mode: int, param: int, max_seq_len: int, q, k_pages, v_pages, block_table, seq_lens,
                    num_kv_heads: int, sm_scale: float, partial_o=None, partial_lse=None, status=None,
-                   q_scale=None, k_scale=None, v_scale=None, stream=None):
+                   q_scale=None, k_scale=None, v_scale=None, stream=None, cta_times=None):
     """dsa_static_splitkv: the fixed-grid comparison (mode 0: param splits; mode 1: param-token chunks)."""
     S = static_num_splits(mode, param, max_seq_len)
     if S < 1:
@@ -317,7 +317,7 @@ def static_splitkv(mode: int, param: int, max_seq_len: int, q, k_pages, v_pages,
     args = _attn_args(q, k_pages, v_pages, block_table, seq_lens, num_kv_heads, sm_scale, q_scale, k_scale,
                       v_scale)
     rc = _lib.dsa_static_splitkv(mode, param, max_seq_len, *args, _ptr(partial_o), _ptr(partial_lse),
-                                 _ptr(status), _stream(stream))
+                                 _ptr(status), _ptr(cta_times), _stream(stream))
     _check(rc, "dsa_static_splitkv")
     return partial_o, partial_lse, S, status
 

@@ -70,6 +70,15 @@ struct KernelParams {
     void *out;               // [B, Hq, 128] bf16 or fp32
     int32_t out_bf16;
     float *out_lse;          // [B, Hq] or null
+    uint64_t *cta_times;     // null, or [CTAs][2]: %globaltimer ns when a CTA starts work and ends
+};
+
+// Stamps the end of a CTA's work: every warp raises the CTA's end time as it leaves.
+struct EndStamp {
+    uint64_t *at;
+    __device__ ~EndStamp() {
+        if (at && (threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned long long *>(at), globaltimer_ns());
+    }
 };
 
 template <int KV>
@@ -89,7 +98,6 @@ struct Cfg<1> {  // E4M3 K/V and Q, fp32 scales
 
 constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
-constexpr int kQSlots = 2;   // descriptors handed ahead to the consumers (Q + info)
 constexpr int kEpiRing = 8;  // merged descriptors the epilogue warp may lag behind (fused combine)
 constexpr int kMaxRows = 64; // query rows (query tokens x G) of one unit in a multi-token step
 constexpr int kDescInfoBytes = 80;
@@ -104,6 +112,9 @@ constexpr int kMaxPagesPerTile = kTile / 16;  // pages of 16 tokens: four per ti
 // issuing S (and laying Q out as its operand), a warp issuing P.V.
 template <int KV, int STAGES, int GROUPS, int MSLOTS = 2, int QW = 0>
 struct Layout {
+    // descriptors handed ahead to the consumers (Q + info): with one query token a slot is
+    // small, and more of them let the producer run ahead through runs of short descriptors
+    static constexpr int kQSlots = QW == 0 ? 4 : 2;
     static constexpr bool kTc = QW == 3;
     static constexpr int kNcw = GROUPS * 4;  // consumer warps (softmax warps for QW = 3)
     static constexpr int kThreads = (kNcw + (kTc ? 3 : 1)) * 32;  // consumers + producer (+ MMA, Q warps)
@@ -330,6 +341,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
     using L = Layout<KV, STAGES, GROUPS, MSLOTS, QW>;
     using C = Cfg<KV>;
     constexpr int NCW = L::kNcw;
+    constexpr int kQSlots = L::kQSlots;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -406,6 +418,13 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
 
     grid_launch_dependents();
     grid_dependency_wait();  // task map, lengths, pages and Q from earlier kernels
+    EndStamp end_stamp{nullptr};
+    if (p.cta_times) {  // uniform over the CTA
+        uint64_t *t = p.cta_times + 2 * (blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+        if (threadIdx.x == 0) t[0] = t[1] = globaltimer_ns();
+        __syncthreads();
+        end_stamp.at = t + 1;
+    }
 
     // ---- this CTA's work
     int d_begin = 0, d_count = 1, st0 = 0, st1 = 0;
@@ -622,12 +641,30 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                     const uint32_t later = starts & ~((2u << k) - 1u);
                     int e = later ? __ffs(later) - 1 : 32;
                     e = min(e, min(cnt, k + STAGES));
-                    if (!ab && lane >= k && lane < e) {
-                        const int cl = c + (lane - k);
-                        const int stage = cl % STAGES;
-                        if (!wait_phase(empty_bar(stage), ((cl / STAGES) & 1) ^ 1, abort_flag, p.status)) {
-                            ab = 1;
-                        } else {
+                    // The run's lanes poll their stages together, in one converged loop, and
+                    // each issues the moment its stage is free: lanes spinning on their own
+                    // barriers in divergent loops starved one another (stages sat free for
+                    // ~0.4 us before their lane noticed).
+                    bool pend = !ab && lane >= k && lane < e;
+                    const int cl = c + (lane - k);
+                    const int stage = pend ? cl % STAGES : 0;
+                    const uint32_t epar = ((cl / STAGES) & 1) ^ 1;
+                    const uint64_t wt0 = globaltimer_ns();
+                    for (uint32_t it = 1; __any_sync(0xffffffffu, pend); ++it) {
+                        if (pend && (it & 31u) == 0) {  // bounded wait
+                            if (*abort_flag) {
+                                ab = 1;
+                                pend = false;
+                            } else if (globaltimer_ns() - wt0 > kWaitLimitNs) {
+                                atomicOr(p.status, DSA_DEV_TIMEOUT);
+                                *abort_flag = 1;
+                                ab = 1;
+                                pend = false;
+                            }
+                        }
+                        if (!pend || !mbar_test_wait(empty_bar(stage), epar)) continue;
+                        pend = false;
+                        {
                             nvalid[stage] = nv_l;
                             const uint32_t fb = full_bar(stage);
                             if (nv_l > 0) {
@@ -1543,6 +1580,13 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
         for (int li = ((grp - c_start) % GROUPS + GROUPS) % GROUPS; li < n; li += GROUPS) {
             const int c = c_start + li;
             const int stage = c % STAGES;
+            // the merge still owed for the previous descriptor is done while this tile's data
+            // is in flight (and every warp has deposited), so it never delays a landed tile
+            if (MSLOTS == 2 && pend_d >= 0 && !mbar_test_wait(full_bar(stage), (c / STAGES) & 1) &&
+                mbar_test_wait(merge_full(pend_d % MSLOTS), (pend_d / MSLOTS) & 1)) {
+                if (!merge_and_write(pend_d, pend_slot, pend_b, pend_h, pend_np, pend_pbeg)) return;
+                pend_d = -1;
+            }
             if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status)) {
                 aborted = true;
                 break;
@@ -1886,7 +1930,7 @@ extern "C" dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void
                                     const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
                                     int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
                                     const dsa_task_map *map, float *partial_o, float *partial_lse,
-                                    dsa_stream stream) {
+                                    uint64_t *cta_times, dsa_stream stream) {
     const AttnArgs a{q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale, block_table,
                      max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
                      page_size, sm_scale, kv_layout};
@@ -1904,6 +1948,7 @@ extern "C" dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void
     kp.max_slots = map->max_descs;
     kp.cta_desc_begin = map->cta_desc_begin;
     kp.descs = reinterpret_cast<const int4 *>(map->descs);
+    kp.cta_times = cta_times;
     if (q_len == 1) {
         if (kv_dtype == DSA_BF16) return launch_persistent<0, false>(a, kp, map->num_ctas, to_cuda(stream));
         return launch_persistent<1, false>(a, kp, map->num_ctas, to_cuda(stream));
@@ -1927,7 +1972,7 @@ extern "C" dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *
                                  dsa_stream stream) {
     return dsa_decode_ex(1, DSA_HND, q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale,
                          block_table, max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads,
-                         head_dim, page_size, sm_scale, map, partial_o, partial_lse, stream);
+                         head_dim, page_size, sm_scale, map, partial_o, partial_lse, nullptr, stream);
 }
 
 extern "C" dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q_dtype, const float *q_scale,
@@ -1939,7 +1984,7 @@ extern "C" dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q
                                        float *partial_lse, dsa_stream stream) {
     return dsa_decode_ex(q_len, DSA_HND, q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale,
                          block_table, max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads,
-                         head_dim, page_size, sm_scale, map, partial_o, partial_lse, stream);
+                         head_dim, page_size, sm_scale, map, partial_o, partial_lse, nullptr, stream);
 }
 
 extern "C" dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_scale, const void *k_pages,
@@ -1996,7 +2041,8 @@ extern "C" dsa_status dsa_static_splitkv(int32_t mode, int32_t param, int32_t ma
                                          int32_t max_pages_per_req, int32_t num_pages, const int32_t *seq_lens,
                                          int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t page_size, float sm_scale, float *partial_o,
-                                         float *partial_lse, int32_t *status, dsa_stream stream) {
+                                         float *partial_lse, int32_t *status, uint64_t *cta_times,
+                                         dsa_stream stream) {
     const AttnArgs a{q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale, block_table,
                      max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
                      page_size, sm_scale};
@@ -2012,6 +2058,7 @@ extern "C" dsa_status dsa_static_splitkv(int32_t mode, int32_t param, int32_t ma
     kp.static_tiles = mode == 1 ? param / kTile : 0;
     kp.num_splits = S;
     kp.max_slots = batch * num_kv_heads * S;
+    kp.cta_times = cta_times;
     const dim3 grid(S, num_kv_heads, batch);
     if (kv_dtype == DSA_BF16) return launch<0, kPairStagesBf16, kPairGroups, false>(a, kp, grid, to_cuda(stream));
     return launch<1, kPairStagesFp8, kPairGroups, false>(a, kp, grid, to_cuda(stream));

@@ -105,11 +105,11 @@ def test_decode_ex_host_checks(lib):
     tm = TaskMap(fake, fake, fake, fake, fake, 10, 4, 16)
     i, f, V = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
     lib.dsa_decode_ex.argtypes = [i, i, V, i, V, V, V, i, V, V, V, i, i, V, i, i, i, i, i, f,
-                                  ctypes.POINTER(TaskMap), V, V, V]
+                                  ctypes.POINTER(TaskMap), V, V, V, V]
 
     def call(q_len=1, layout=1, kv_dt=0, hq=64, hkv=8, page=16):
         return lib.dsa_decode_ex(q_len, layout, fake, 0, None, fake, fake, kv_dt, None, None, fake, 4, 8, fake,
-                                 2, hq, hkv, 128, page, 0.1, ctypes.byref(tm), fake, fake, None)
+                                 2, hq, hkv, 128, page, 0.1, ctypes.byref(tm), fake, fake, None, None)
     assert call(layout=2) == 1              # not a dsa_kv_layout
     assert call(layout=-1) == 1
     assert call(page=8) == 2

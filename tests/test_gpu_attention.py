@@ -313,3 +313,41 @@ def test_batch_zero_is_a_no_op(dsa):
     torch.cuda.synchronize()
     assert out.shape == (0, 16, 128)
     assert tm.host()["meta"].tolist() == [0, 0, 0, 0]
+
+
+# ---------------------------------------------------------------- per-CTA timestamps
+
+@pytest.mark.parametrize("C", [None, "2x", 7])
+def test_cta_times_leave_results_unchanged(dsa, C):
+    """dsa_decode_ex with a timestamp buffer: every CTA reports start <= end, and the
+    partials are bit-identical to a launch without timestamps."""
+    inp = make([1, 63, 700, 3000, 129], 64, 8, "bf16", seed=9)
+    C = resolve_ctas(C)
+    tm = dsa.plan(inp["seq_lens"], 8, C, 1)
+    po0, pl0 = dsa.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
+                          inp["sm_scale"])
+    times = torch.zeros(C, 2, dtype=torch.int64, device="cuda")
+    po1, pl1 = dsa.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
+                          inp["sm_scale"], cta_times=times)
+    torch.cuda.synchronize()
+    assert dsa.get_status(tm) == 0
+    nd = len(tm.host()["descs"])
+    assert torch.equal(po0[:nd], po1[:nd]) and torch.equal(pl0[:nd], pl1[:nd])
+    t = times.cpu().numpy()
+    assert (t[:, 0] > 0).all() and (t[:, 1] >= t[:, 0]).all()
+    assert (t[:, 1] - t[:, 0]).max() < 10 ** 9  # under a second
+
+
+def test_static_cta_times(dsa):
+    lens = [1, 63, 700, 3000]
+    inp = make(lens, 16, 2, "fp8", seed=10)
+    S = dsa.static_num_splits(0, 4, max(lens))
+    times = torch.zeros(len(lens) * 2 * S, 2, dtype=torch.int64, device="cuda")
+    po, pl, S, status = dsa.static_splitkv(0, 4, max(lens), inp["q"], inp["k_pages"], inp["v_pages"],
+                                           inp["block_table"], inp["seq_lens"], 2, inp["sm_scale"],
+                                           q_scale=inp["q_scale"], k_scale=inp["k_scale"], v_scale=inp["v_scale"],
+                                           cta_times=times)
+    torch.cuda.synchronize()
+    assert dsa.read_status(status) == 0
+    t = times.cpu().numpy()
+    assert (t[:, 0] > 0).all() and (t[:, 1] >= t[:, 0]).all()
