@@ -581,12 +581,25 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                     }
                 }
                 const uint32_t starts = __ballot_sync(0xffffffffu, first_l);
-                // ---- runs of at most STAGES tiles, cut where a descriptor starts; in a run
-                //      every lane waits for and fills its own stage, in parallel
-                for (int k = 0; k < cnt && !aborted;) {
-                    int ab = 0;
-                    if ((starts >> k) & 1u) {
-                        // descriptor cj[k] starts here: hand it (info + Q) to the consumers
+                // ---- one converged loop over the chunk.  Lane l issues its tile the moment
+                //      its ring stage is free, once the tile STAGES positions earlier has been
+                //      issued (so the parity it tests names exactly the release it needs);
+                //      descriptors starting in the chunk are handed to the consumers in order,
+                //      each as soon as a hand-off slot is free.  Nothing waits in a divergent
+                //      loop: lanes spinning on their own barriers starved one another.
+                bool pend = lane < cnt;
+                uint32_t todo = starts;  // descriptor starts not yet handed off
+                const int cl = c + lane;
+                const int stage = cl % STAGES;
+                const uint32_t epar = ((cl / STAGES) & 1) ^ 1;
+                uint64_t idle_t0 = globaltimer_ns();  // last progress
+                for (uint32_t it = 1;; ++it) {
+                    const uint32_t done = __ballot_sync(0xffffffffu, !pend);
+                    if (done == 0xffffffffu && todo == 0) break;
+                    bool progress = false;
+                    if (todo) {
+                        // next descriptor to hand off starts at chunk lane k
+                        const int k = __ffs(todo) - 1;
                         const int j = __shfl_sync(0xffffffffu, cj, k);
                         float qs[kMaxGroup];
 #pragma unroll
@@ -599,119 +612,114 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         const int pbeg = __shfl_sync(0xffffffffu, wpbeg, j);
                         const int dt0 = __shfl_sync(0xffffffffu, wt0, j);
                         const int dlen = __shfl_sync(0xffffffffu, wlen, j);
-                        if (lane == 0) {
-                            const int qs_ = qi % kQSlots;
-                            if (!wait_phase(qempty_bar(qs_), ((qi / kQSlots) & 1) ^ 1, abort_flag, p.status)) {
-                                ab = 1;
-                            } else {
-                                DescInfo *inf = reinterpret_cast<DescInfo *>(smem + L::kInfoOff) + qs_;
-                                inf->end = 0;
-                                inf->b = b;
-                                inf->h = h;
-                                inf->n = n;
-                                inf->slot = slot;
-                                inf->c_start = c;
-                                inf->np = np;
-                                inf->pbeg = pbeg;
-                                inf->t0 = dt0;
-                                inf->len = dlen;
+                        const int qs_ = qi % kQSlots;
+                        int ok = 0;
+                        if (lane == 0 && mbar_test_wait(qempty_bar(qs_), ((qi / kQSlots) & 1) ^ 1)) {
+                            ok = 1;
+                            const int c_desc = c + k;  // ring position of the descriptor's first tile
+                            DescInfo *inf = reinterpret_cast<DescInfo *>(smem + L::kInfoOff) + qs_;
+                            inf->end = 0;
+                            inf->b = b;
+                            inf->h = h;
+                            inf->n = n;
+                            inf->slot = slot;
+                            inf->c_start = c_desc;
+                            inf->np = np;
+                            inf->pbeg = pbeg;
+                            inf->t0 = dt0;
+                            inf->len = dlen;
 #pragma unroll
-                                for (int g = 0; g < kMaxGroup; ++g) inf->qscale[g] = qs[g];
-                                // the G query rows of each of the request's q_len query tokens,
-                                // one after the other (row i*G + g)
-                                if (QW == 3) {  // the S warp fetches Q itself, a descriptor ahead
-                                    mbar_arrive(qfull_bar(qs_));
-                                } else {
-                                    const uint32_t bytes = G * C::kQHeadBytes;
-                                    mbar_arrive_expect_tx(qfull_bar(qs_), bytes * p.q_len);
-                                    for (int i = 0; i < p.q_len; ++i) {
-                                        const uint8_t *src = p.q + ((static_cast<int64_t>(b) * p.q_len + i) * p.hq + h * G) *
-                                                                       C::kQHeadBytes;
-                                        bulk_load(sbase + L::kQOff + qs_ * L::kQSlot + i * bytes, src, bytes,
-                                                  qfull_bar(qs_));
-                                    }
-                                    q_issued = qi;
+                            for (int g = 0; g < kMaxGroup; ++g) inf->qscale[g] = qs[g];
+                            // the G query rows of each of the request's q_len query tokens,
+                            // one after the other (row i*G + g)
+                            if (QW == 3) {  // the S warp fetches Q itself, a descriptor ahead
+                                mbar_arrive(qfull_bar(qs_));
+                            } else {
+                                const uint32_t bytes = G * C::kQHeadBytes;
+                                mbar_arrive_expect_tx(qfull_bar(qs_), bytes * p.q_len);
+                                for (int i = 0; i < p.q_len; ++i) {
+                                    const uint8_t *src = p.q + ((static_cast<int64_t>(b) * p.q_len + i) * p.hq + h * G) *
+                                                                   C::kQHeadBytes;
+                                    bulk_load(sbase + L::kQOff + qs_ * L::kQSlot + i * bytes, src, bytes,
+                                              qfull_bar(qs_));
                                 }
+                                q_issued = qi;
                             }
                         }
-                        ++qi;
-                        ab = __shfl_sync(0xffffffffu, ab, 0);
+                        if (__shfl_sync(0xffffffffu, ok, 0)) {
+                            ++qi;
+                            todo &= todo - 1;
+                            progress = true;
+                        }
                     }
-                    // run [k, e): up to STAGES tiles, no descriptor start after k
-                    const uint32_t later = starts & ~((2u << k) - 1u);
-                    int e = later ? __ffs(later) - 1 : 32;
-                    e = min(e, min(cnt, k + STAGES));
-                    // The run's lanes poll their stages together, in one converged loop, and
-                    // each issues the moment its stage is free: lanes spinning on their own
-                    // barriers in divergent loops starved one another (stages sat free for
-                    // ~0.4 us before their lane noticed).
-                    bool pend = !ab && lane >= k && lane < e;
-                    const int cl = c + (lane - k);
-                    const int stage = pend ? cl % STAGES : 0;
-                    const uint32_t epar = ((cl / STAGES) & 1) ^ 1;
-                    const uint64_t wt0 = globaltimer_ns();
-                    for (uint32_t it = 1; __any_sync(0xffffffffu, pend); ++it) {
-                        if (pend && (it & 31u) == 0) {  // bounded wait
+                    // a lane may test its stage once the tile STAGES positions earlier is issued
+                    const bool ready = pend && (lane < STAGES || ((done >> (lane - STAGES)) & 1u));
+                    if (ready && mbar_test_wait(empty_bar(stage), epar)) {
+                        pend = false;
+                        nvalid[stage] = nv_l;
+                        const uint32_t fb = full_bar(stage);
+                        if (nv_l > 0) {
+                            const uint32_t kdst = sbase + stage * L::kStageBytes;
+                            const uint32_t vdst = kdst + C::kTileBytes;
+                            // the pages holding valid tokens, one box of P rows each (both 128-B
+                            // halves of a bf16 row: the stage is [page][half][P rows][128 B]);
+                            // the tensor-core kernel's operands want [half][64 rows][128 B],
+                            // so there each half of a page smaller than the tile is its own box
+                            const int nsub = (nv_l + P - 1) / P;
+                            mbar_arrive_expect_tx(fb, nsub * (L::kStageTx / ppt));
+#pragma unroll
+                            for (int k = 0; k < kMaxPagesPerTile; ++k) {
+                                if (k >= nsub) break;
+                                const int pg = cpg[k];
+                                if (QW == 3 && P < kTile) {
+                                    const uint32_t ro = static_cast<uint32_t>(k * P) * 128u;
+                                    tma_load_5d(kdst + ro, &kmap, fb, 0, 0, 0, h_l, pg, policy);
+                                    tma_load_5d(kdst + C::kTileBytes / 2 + ro, &kmap, fb, 0, 0, 1, h_l, pg, policy);
+                                    tma_load_5d(vdst + ro, &vmap, fb, 0, 0, 0, h_l, pg, policy);
+                                    tma_load_5d(vdst + C::kTileBytes / 2 + ro, &vmap, fb, 0, 0, 1, h_l, pg, policy);
+                                } else {
+                                    const uint32_t ro = static_cast<uint32_t>(k * P) * (C::kTileBytes / kTile);
+                                    tma_load_5d(kdst + ro, &kmap, fb, 0, 0, 0, h_l, pg, policy);
+                                    tma_load_5d(vdst + ro, &vmap, fb, 0, 0, 0, h_l, pg, policy);
+                                }
+                                if (KV == 1) {
+                                    const int64_t srow = (static_cast<int64_t>(pg) * p.hkv + h_l) * P;
+                                    bulk_load(vdst + C::kTileBytes + 4 * k * P, p.k_scale + srow, 4 * P, fb);
+                                    bulk_load(vdst + C::kTileBytes + C::kScaleBytes + 4 * k * P, p.v_scale + srow,
+                                              4 * P, fb);
+                                }
+                            }
+                        } else {
+                            mbar_arrive(fb);
+                        }
+                    }
+                    if (__any_sync(0xffffffffu, ready && !pend)) progress = true;
+                    if (progress) {
+                        idle_t0 = globaltimer_ns();
+                    } else if ((it & 31u) == 0) {  // bounded wait
+                        int ab = 0;
+                        if (lane == 0) {
                             if (*abort_flag) {
                                 ab = 1;
-                                pend = false;
-                            } else if (globaltimer_ns() - wt0 > kWaitLimitNs) {
+                            } else if (globaltimer_ns() - idle_t0 > kWaitLimitNs) {
                                 atomicOr(p.status, DSA_DEV_TIMEOUT);
                                 *abort_flag = 1;
                                 ab = 1;
-                                pend = false;
                             }
                         }
-                        if (!pend || !mbar_test_wait(empty_bar(stage), epar)) continue;
-                        pend = false;
-                        {
-                            nvalid[stage] = nv_l;
-                            const uint32_t fb = full_bar(stage);
-                            if (nv_l > 0) {
-                                const uint32_t kdst = sbase + stage * L::kStageBytes;
-                                const uint32_t vdst = kdst + C::kTileBytes;
-                                // the pages holding valid tokens, one box of P rows each (both 128-B
-                                // halves of a bf16 row: the stage is [page][half][P rows][128 B]);
-                                // the tensor-core kernel's operands want [half][64 rows][128 B],
-                                // so there each half of a page smaller than the tile is its own box
-                                const int nsub = (nv_l + P - 1) / P;
-                                mbar_arrive_expect_tx(fb, nsub * (L::kStageTx / ppt));
-#pragma unroll
-                                for (int k = 0; k < kMaxPagesPerTile; ++k) {
-                                    if (k >= nsub) break;
-                                    const int pg = cpg[k];
-                                    if (QW == 3 && P < kTile) {
-                                        const uint32_t ro = static_cast<uint32_t>(k * P) * 128u;
-                                        tma_load_5d(kdst + ro, &kmap, fb, 0, 0, 0, h_l, pg, policy);
-                                        tma_load_5d(kdst + C::kTileBytes / 2 + ro, &kmap, fb, 0, 0, 1, h_l, pg, policy);
-                                        tma_load_5d(vdst + ro, &vmap, fb, 0, 0, 0, h_l, pg, policy);
-                                        tma_load_5d(vdst + C::kTileBytes / 2 + ro, &vmap, fb, 0, 0, 1, h_l, pg, policy);
-                                    } else {
-                                        const uint32_t ro = static_cast<uint32_t>(k * P) * (C::kTileBytes / kTile);
-                                        tma_load_5d(kdst + ro, &kmap, fb, 0, 0, 0, h_l, pg, policy);
-                                        tma_load_5d(vdst + ro, &vmap, fb, 0, 0, 0, h_l, pg, policy);
-                                    }
-                                    if (KV == 1) {
-                                        const int64_t srow = (static_cast<int64_t>(pg) * p.hkv + h_l) * P;
-                                        bulk_load(vdst + C::kTileBytes + 4 * k * P, p.k_scale + srow, 4 * P, fb);
-                                        bulk_load(vdst + C::kTileBytes + C::kScaleBytes + 4 * k * P, p.v_scale + srow,
-                                                  4 * P, fb);
-                                    }
-                                }
-                            } else {
-                                mbar_arrive(fb);
-                            }
+                        if (__shfl_sync(0xffffffffu, ab, 0)) {
+                            aborted = true;
+                            break;
                         }
                     }
-                    if (__any_sync(0xffffffffu, ab)) {
-                        aborted = true;
-                        // tiles this run did issue are still counted for the drain below
-                        c += e - k;
-                        break;
-                    }
-                    c += e - k;
-                    k = e;
                 }
+                if (aborted) {
+                    // tiles up to the last one issued are counted for the drain below
+                    const uint32_t done = __ballot_sync(0xffffffffu, !pend && lane < cnt);
+                    c += done ? 32 - __clz(done) : 0;
+                    break;
+                }
+                c += cnt;
                 cj = nj;
                 ct = nt;
 #pragma unroll
