@@ -606,7 +606,9 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                     const uint32_t done = __ballot_sync(0xffffffffu, !pend);
                     if (done == 0xffffffffu && todo == 0) break;
                     bool progress = false;
-                    if (todo) {
+                    int hand = 0;  // a hand-off slot is free for the next descriptor
+                    if (todo && lane == 0) hand = mbar_test_wait(qempty_bar(qi % kQSlots), ((qi / kQSlots) & 1) ^ 1);
+                    if (__shfl_sync(0xffffffffu, hand, 0)) {
                         // next descriptor to hand off starts at chunk lane k
                         const int k = __ffs(todo) - 1;
                         const int j = __shfl_sync(0xffffffffu, cj, k);
@@ -622,9 +624,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         const int dt0 = __shfl_sync(0xffffffffu, wt0, j);
                         const int dlen = __shfl_sync(0xffffffffu, wlen, j);
                         const int qs_ = qi % kQSlots;
-                        int ok = 0;
-                        if (lane == 0 && mbar_test_wait(qempty_bar(qs_), ((qi / kQSlots) & 1) ^ 1)) {
-                            ok = 1;
+                        if (lane == 0) {
                             const int c_desc = c + k;  // ring position of the descriptor's first tile
                             DescInfo *inf = reinterpret_cast<DescInfo *>(smem + L::kInfoOff) + qs_;
                             inf->end = 0;
@@ -655,11 +655,9 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                                 q_issued = qi;
                             }
                         }
-                        if (__shfl_sync(0xffffffffu, ok, 0)) {
-                            ++qi;
-                            todo &= todo - 1;
-                            progress = true;
-                        }
+                        ++qi;
+                        todo &= todo - 1;
+                        progress = true;
                     }
                     // a lane may test its stage once the tile STAGES positions earlier is issued
                     const bool ready = pend && (lane < STAGES || ((done >> (lane - STAGES)) & 1u));
@@ -674,28 +672,39 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                             // halves of a bf16 row: the stage is [page][half][P rows][128 B]);
                             // the tensor-core kernel's operands want [half][64 rows][128 B],
                             // so there each half of a page smaller than the tile is its own box
-                            const int nsub = (nv_l + P - 1) / P;
-                            mbar_arrive_expect_tx(fb, nsub * (L::kStageTx / ppt));
-#pragma unroll
-                            for (int k = 0; k < kMaxPagesPerTile; ++k) {
-                                if (k >= nsub) break;
-                                const int pg = cpg[k];
-                                if (QW == 3 && P < kTile) {
-                                    const uint32_t ro = static_cast<uint32_t>(k * P) * 128u;
-                                    tma_load_5d(kdst + ro, &kmap, fb, 0, 0, 0, h_l, pg, policy);
-                                    tma_load_5d(kdst + C::kTileBytes / 2 + ro, &kmap, fb, 0, 0, 1, h_l, pg, policy);
-                                    tma_load_5d(vdst + ro, &vmap, fb, 0, 0, 0, h_l, pg, policy);
-                                    tma_load_5d(vdst + C::kTileBytes / 2 + ro, &vmap, fb, 0, 0, 1, h_l, pg, policy);
-                                } else {
-                                    const uint32_t ro = static_cast<uint32_t>(k * P) * (C::kTileBytes / kTile);
-                                    tma_load_5d(kdst + ro, &kmap, fb, 0, 0, 0, h_l, pg, policy);
-                                    tma_load_5d(vdst + ro, &vmap, fb, 0, 0, 0, h_l, pg, policy);
-                                }
+                            if (P == kTile) {  // one page per tile: the common case, no loop
+                                mbar_arrive_expect_tx(fb, L::kStageTx);
+                                tma_load_5d(kdst, &kmap, fb, 0, 0, 0, h_l, cpg[0], policy);
+                                tma_load_5d(vdst, &vmap, fb, 0, 0, 0, h_l, cpg[0], policy);
                                 if (KV == 1) {
-                                    const int64_t srow = (static_cast<int64_t>(pg) * p.hkv + h_l) * P;
-                                    bulk_load(vdst + C::kTileBytes + 4 * k * P, p.k_scale + srow, 4 * P, fb);
-                                    bulk_load(vdst + C::kTileBytes + C::kScaleBytes + 4 * k * P, p.v_scale + srow,
-                                              4 * P, fb);
+                                    const int64_t srow = (static_cast<int64_t>(cpg[0]) * p.hkv + h_l) * kTile;
+                                    bulk_load(vdst + C::kTileBytes, p.k_scale + srow, C::kScaleBytes, fb);
+                                    bulk_load(vdst + C::kTileBytes + C::kScaleBytes, p.v_scale + srow, C::kScaleBytes, fb);
+                                }
+                            } else {
+                                const int nsub = (nv_l + P - 1) / P;
+                                mbar_arrive_expect_tx(fb, nsub * (L::kStageTx / ppt));
+#pragma unroll
+                                for (int k = 0; k < kMaxPagesPerTile; ++k) {
+                                    if (k >= nsub) break;
+                                    const int pg = cpg[k];
+                                    if (QW == 3 && P < kTile) {
+                                        const uint32_t ro = static_cast<uint32_t>(k * P) * 128u;
+                                        tma_load_5d(kdst + ro, &kmap, fb, 0, 0, 0, h_l, pg, policy);
+                                        tma_load_5d(kdst + C::kTileBytes / 2 + ro, &kmap, fb, 0, 0, 1, h_l, pg, policy);
+                                        tma_load_5d(vdst + ro, &vmap, fb, 0, 0, 0, h_l, pg, policy);
+                                        tma_load_5d(vdst + C::kTileBytes / 2 + ro, &vmap, fb, 0, 0, 1, h_l, pg, policy);
+                                    } else {
+                                        const uint32_t ro = static_cast<uint32_t>(k * P) * (C::kTileBytes / kTile);
+                                        tma_load_5d(kdst + ro, &kmap, fb, 0, 0, 0, h_l, pg, policy);
+                                        tma_load_5d(vdst + ro, &vmap, fb, 0, 0, 0, h_l, pg, policy);
+                                    }
+                                    if (KV == 1) {
+                                        const int64_t srow = (static_cast<int64_t>(pg) * p.hkv + h_l) * P;
+                                        bulk_load(vdst + C::kTileBytes + 4 * k * P, p.k_scale + srow, 4 * P, fb);
+                                        bulk_load(vdst + C::kTileBytes + C::kScaleBytes + 4 * k * P, p.v_scale + srow,
+                                                  4 * P, fb);
+                                    }
                                 }
                             }
                         } else {
