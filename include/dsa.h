@@ -214,11 +214,11 @@ dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_sca
  * draft; rows with no visible token in a descriptor get o = 0, lse = -inf there).
  *   q        [B, q_len, Hq, 128] bf16 (row i*G + g of unit (b, h) is q[b][i][h*G + g]).
  *   partial_o [S * map->max_descs, q_len*G, 128] fp32, partial_lse [S * map->max_descs,
- *            q_len*G] with S = dsa_multi_slots_per_desc(q_len, G): 1 up to 16 query rows
- *            (slot x = descriptor x, the mma.sync kernel), else 2 (slots 2x and 2x + 1,
- *            each the attention over part of the descriptor's tiles: the two softmax
- *            teams of the tensor-memory kernel); merging a descriptor's slots gives its
- *            attention, and dsa_combine_multi does so.
+ *            q_len*G] with S = dsa_multi_slots_per_desc(q_len, G): 2 for q_len > 1
+ *            (slots 2x and 2x + 1, each the attention over part of the descriptor's
+ *            tiles: the two softmax teams of the tensor-memory kernel), 1 for q_len = 1;
+ *            merging a descriptor's slots gives its attention, and dsa_combine_multi
+ *            does so.
  * Supported: BF16 Q and K/V, q_len * G <= 64; q_len = 1 is exactly dsa_decode (all of
  * its dtypes).  Other arguments and errors are as for dsa_decode.
  */

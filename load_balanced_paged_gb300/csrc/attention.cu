@@ -104,12 +104,11 @@ constexpr int kDescInfoBytes = 80;
 constexpr int kMaxPagesPerTile = kTile / 16;  // pages of 16 tokens: four per tile
 
 // QW = 0: one query token per request; the consumer groups take alternate tiles and all
-// warps of the CTA merge at each descriptor end.  QW = 1 or 2: multi-token queries with
-// mma.sync; every consumer warp takes every tile: its token half (32 tokens) for its
-// column set of QW 8-column blocks (query rows), and the two halves of a column set merge
-// pairwise.  QW = 3: multi-token queries on the 5th-generation tensor cores: S = Q K^T and
-// O = P V accumulate in tensor memory, one softmax thread per query row (4 warps), a warp
-// issuing S (and laying Q out as its operand), a warp issuing P.V.
+// warps of the CTA merge at each descriptor end.  QW = 3: multi-token queries on the
+// 5th-generation tensor cores: S = Q K^T and O = P V accumulate in tensor memory, two
+// teams of four softmax warps, a warp issuing S (and laying Q out as its operand), a warp
+// issuing P.V.  (An mma.sync kernel for up to 16 query rows per unit measured 214-221 us on
+// the mixed lengths against 191-195 us for the tensor-memory kernel at 2-16 rows: removed.)
 template <int KV, int STAGES, int GROUPS, int MSLOTS = 2, int QW = 0>
 struct Layout {
     // descriptors handed ahead to the consumers (Q + info): with one query token a slot is
@@ -126,14 +125,13 @@ struct Layout {
     static constexpr int kQOff = STAGES * kStageBytes;
     static constexpr int kOStride = 132;  // floats per head row of a warp's O (padding avoids bank conflicts)
     static constexpr int kWarpFloats = kMaxGroup * kOStride + 2 * kMaxGroup;
-    static constexpr int kPairFloats = 8 * QW * kOStride + 2 * 8 * QW;  // one column set's second half
     // QW = 3: Q as the MMA's A operand (64 rows x 128, K-major with the 128-byte swizzle, two
     // 64-column halves of 8 KB, as the TMA lays out a K tile), two buffers.
     static constexpr int kQcOff = kQOff + kQSlots * kQSlot;
     static constexpr int kQcBytes = kTc ? 2 * kMaxRows * kHeadDim * 2 : 0;
     static constexpr int kMergeOff = kQcOff + kQcBytes;
-    static constexpr int kMergeSlot = kTc ? 0 : (QW ? 4 * kPairFloats : kNcw * kWarpFloats);  // floats per merge slot
-    static constexpr int kMergeBars = kTc ? 0 : (QW ? 4 : 2);  // merge_full / merge_done barriers each
+    static constexpr int kMergeSlot = kTc ? 0 : kNcw * kWarpFloats;  // floats per merge slot
+    static constexpr int kMergeBars = kTc ? 0 : 2;  // merge_full / merge_done barriers each
     static constexpr int kTcBars = kTc ? 22 : 0;  // s_full, s_free, p_full x4; o_done, o_free, qc_full, qc_free, qd_full x2
     static constexpr int kBarOff = kMergeOff + MSLOTS * kMergeSlot * 4;
     // full, empty, qfull, qempty, merge_full, merge_done, epi_ready, epi_free, tensor-core barriers
@@ -385,7 +383,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             // QW = 1, 2: every consumer warp reads every stage; QW = 3: the S and PV warps release it
-            mbar_init(empty_bar(s), QW == 3 ? 2 : (QW ? NCW : 4));
+            mbar_init(empty_bar(s), QW == 3 ? 2 : 4);
         }
         for (int s = 0; s < kQSlots; ++s) {
             mbar_init(qfull_bar(s), 1);
@@ -403,11 +401,6 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 mbar_init(qc_full(b), 1);
                 mbar_init(qc_free(b), 1);
                 mbar_init(qd_full(b), 1);
-            }
-        } else if (QW) {
-            for (int s = 0; s < MB; ++s) {  // per column set: second half deposited / read
-                mbar_init(merge_full(s), 1);
-                mbar_init(merge_done(s), 1);
             }
         } else {
             for (int s = 0; s < MSLOTS; ++s) {
@@ -1229,274 +1222,6 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
             tmem_dealloc(tmem, 512);
         }
         return;
-    } else if constexpr (QW > 0) {
-        // ===================== consumer warps, multi-token queries =====================
-        // Query rows r = i * G + g (query token i, head g); row r of a request of length len
-        // sees the tokens t < len - q_len + i + 1 (causal within the draft).  Warp w takes
-        // tokens [32 (w & 1), +32) of every tile for rows [8 QW (w >> 1), +8 QW): S^T blocks
-        // of 16 tokens x 8 rows, one online softmax per row over its half of the tokens; at
-        // each descriptor end the second half deposits (m, l, O) in shared memory and the
-        // first half merges it into its registers and writes the partial.
-        constexpr int NBW = QW;
-        const int ts = warp & 1, cs = warp >> 1;
-        const int tok_base = 32 * ts;
-        const int cb = 8 * NBW * cs;
-        const int R = p.q_len * G;
-        const bool active = cb < R;
-        const int gid = lane >> 2, tig = lane & 3;
-        const int xr = lane & 7;
-        const int k_row = tok_base + xr + ((lane >> 3) & 1) * 8;
-        const int k_chunk = lane >> 4;
-        const int v_row = tok_base + xr + (lane >> 4) * 8;
-        const int v_chunk = (lane >> 3) & 1;
-        // byte offsets of this lane's rows in the stage ([page][half][P rows][128 B])
-        const uint32_t half_off = static_cast<uint32_t>(p.page_size) * 128u;
-        const uint32_t k_off[2] = {kv_row_off(k_row, p.page_size), kv_row_off(k_row + 16, p.page_size)};
-        const uint32_t v_off[2] = {kv_row_off(v_row, p.page_size), kv_row_off(v_row + 16, p.page_size)};
-        float *pair = reinterpret_cast<float *>(smem + L::kMergeOff) + cs * L::kPairFloats;
-
-        for (int qi = 0;; ++qi) {
-            const int qslot = qi % kQSlots;
-            if (!wait_phase(qfull_bar(qslot), (qi / kQSlots) & 1, abort_flag, p.status)) return;
-            const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
-            if (inf->end) break;
-            const int n = inf->n, slot = inf->slot, c_start = inf->c_start, dt0 = inf->t0, len = inf->len;
-
-            // Q fragments (B operand): row cb + 8 nb + gid, zero past R
-            uint32_t qf[NBW][8][2];
-#pragma unroll
-            for (int nb = 0; nb < NBW; ++nb) {
-                const int r = cb + 8 * nb + gid;
-                const uint8_t *qs = smem + L::kQOff + qslot * L::kQSlot + r * C::kQHeadBytes;
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    qf[nb][ks][0] = r < R ? *reinterpret_cast<const uint32_t *>(qs + 32 * ks + 4 * tig) : 0u;
-                    qf[nb][ks][1] = r < R ? *reinterpret_cast<const uint32_t *>(qs + 32 * ks + 4 * tig + 16) : 0u;
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(qempty_bar(qslot));
-
-            // causal limit of this lane's two rows per block (rows past R are never stored)
-            int lim[NBW][2];
-#pragma unroll
-            for (int nb = 0; nb < NBW; ++nb)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int r = cb + 8 * nb + 2 * tig + e;
-                    lim[nb][e] = len - p.q_len + (r < R ? r / G : 0) + 1;
-                }
-            const int lim_min = len - p.q_len + 1;  // every row sees the tokens below this
-
-            float m[NBW][2], l[NBW][2], o[NBW][8][4];
-#pragma unroll
-            for (int nb = 0; nb < NBW; ++nb) {
-                m[nb][0] = m[nb][1] = -INFINITY;
-                l[nb][0] = l[nb][1] = 0.f;
-#pragma unroll
-                for (int mb = 0; mb < 8; ++mb) o[nb][mb][0] = o[nb][mb][1] = o[nb][mb][2] = o[nb][mb][3] = 0.f;
-            }
-
-            bool aborted = false;
-            for (int li = 0; li < n; ++li) {
-                const int c = c_start + li;
-                const int stage = c % STAGES;
-                if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status)) {
-                    aborted = true;
-                    break;
-                }
-                const int nv = nvalid[stage];
-                if (active && nv > tok_base) {
-                    const uint32_t kbase = sbase + stage * L::kStageBytes;
-                    const uint32_t vbase = kbase + C::kTileBytes;
-                    const int T0 = (dt0 + li) * kTile + tok_base;  // token of this warp's first row
-                    // ---- S^T = K . Q^T for 2 blocks of 16 tokens x NBW blocks of 8 rows
-                    float sc[2][NBW][4];
-#pragma unroll
-                    for (int kt = 0; kt < 2; ++kt)
-#pragma unroll
-                        for (int nb = 0; nb < NBW; ++nb) sc[kt][nb][0] = sc[kt][nb][1] = sc[kt][nb][2] = sc[kt][nb][3] = 0.f;
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const int ch = 2 * ks + k_chunk;
-#pragma unroll
-                        for (int kt = 0; kt < 2; ++kt) {
-                            const uint32_t addr = kbase + (ch >> 3) * half_off + k_off[kt] + (((ch & 7) ^ xr) << 4);
-                            uint32_t a0, a1, a2, a3;
-                            ldsm_x4(addr, a0, a1, a2, a3);
-#pragma unroll
-                            for (int nb = 0; nb < NBW; ++nb) mma_bf16(sc[kt][nb], a0, a1, a2, a3, qf[nb][ks][0], qf[nb][ks][1]);
-                        }
-                    }
-                    const bool mask = T0 + 32 > lim_min;  // some row of the warp's tokens is past a limit
-#pragma unroll
-                    for (int kt = 0; kt < 2; ++kt)
-#pragma unroll
-                        for (int nb = 0; nb < NBW; ++nb) {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) sc[kt][nb][e] *= p.score_scale;
-                            if (mask) {
-                                const int ta = T0 + 16 * kt + gid, tb = ta + 8;
-                                if (ta >= lim[nb][0]) sc[kt][nb][0] = -INFINITY;
-                                if (ta >= lim[nb][1]) sc[kt][nb][1] = -INFINITY;
-                                if (tb >= lim[nb][0]) sc[kt][nb][2] = -INFINITY;
-                                if (tb >= lim[nb][1]) sc[kt][nb][3] = -INFINITY;
-                            }
-                        }
-                    // ---- online softmax (base 2) per row over the warp's 32 tokens
-                    uint32_t bh[2][NBW][2], bl[2][NBW][2];
-#pragma unroll
-                    for (int nb = 0; nb < NBW; ++nb) {
-                        float mx0 = fmaxf(fmaxf(sc[0][nb][0], sc[0][nb][2]), fmaxf(sc[1][nb][0], sc[1][nb][2]));
-                        float mx1 = fmaxf(fmaxf(sc[0][nb][1], sc[0][nb][3]), fmaxf(sc[1][nb][1], sc[1][nb][3]));
-#pragma unroll
-                        for (int o_ = 4; o_ < 32; o_ <<= 1) {
-                            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
-                            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
-                        }
-                        const float mn0 = fmaxf(m[nb][0], mx0), mn1 = fmaxf(m[nb][1], mx1);
-                        const float r0 = mn0 == -INFINITY ? 0.f : mn0, r1 = mn1 == -INFINITY ? 0.f : mn1;
-                        const float al0 = ex2(m[nb][0] - r0), al1 = ex2(m[nb][1] - r1);
-                        float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-                        for (int kt = 0; kt < 2; ++kt) {
-                            const float p0 = ex2(sc[kt][nb][0] - r0), p1 = ex2(sc[kt][nb][1] - r1);
-                            const float p2 = ex2(sc[kt][nb][2] - r0), p3 = ex2(sc[kt][nb][3] - r1);
-                            ls0 += p0 + p2;
-                            ls1 += p1 + p3;
-                            const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-                            const uint32_t l01 = pack_bf16x2(p0 - bf16lo_to_f32(h01), p1 - bf16hi_to_f32(h01));
-                            const uint32_t l23 = pack_bf16x2(p2 - bf16lo_to_f32(h23), p3 - bf16hi_to_f32(h23));
-                            bh[kt][nb][0] = movmatrix_trans(h01);
-                            bh[kt][nb][1] = movmatrix_trans(h23);
-                            bl[kt][nb][0] = movmatrix_trans(l01);
-                            bl[kt][nb][1] = movmatrix_trans(l23);
-                        }
-                        l[nb][0] = l[nb][0] * al0 + ls0;
-                        l[nb][1] = l[nb][1] * al1 + ls1;
-                        m[nb][0] = mn0;
-                        m[nb][1] = mn1;
-#pragma unroll
-                        for (int mb = 0; mb < 8; ++mb) {
-                            o[nb][mb][0] *= al0;
-                            o[nb][mb][1] *= al1;
-                            o[nb][mb][2] *= al0;
-                            o[nb][mb][3] *= al1;
-                        }
-                    }
-                    // ---- O^T += V^T . P^T; V rows past the request's length are zeroed
-                    const bool partial = nv < tok_base + 32;
-#pragma unroll
-                    for (int mb = 0; mb < 8; ++mb) {
-                        const int ch = 2 * mb + v_chunk;
-#pragma unroll
-                        for (int kt = 0; kt < 2; ++kt) {
-                            const uint32_t addr = vbase + (ch >> 3) * half_off + v_off[kt] + (((ch & 7) ^ xr) << 4);
-                            uint32_t a0, a1, a2, a3;
-                            ldsm_x4_trans(addr, a0, a1, a2, a3);
-                            if (partial) {
-                                const uint32_t mlo = tok_mask(tok_base + 16 * kt + 2 * tig, nv);
-                                const uint32_t mhi = tok_mask(tok_base + 16 * kt + 8 + 2 * tig, nv);
-                                a0 &= mlo;
-                                a1 &= mlo;
-                                a2 &= mhi;
-                                a3 &= mhi;
-                            }
-#pragma unroll
-                            for (int nb = 0; nb < NBW; ++nb) {
-                                mma_bf16(o[nb][mb], a0, a1, a2, a3, bh[kt][nb][0], bh[kt][nb][1]);
-                                mma_bf16(o[nb][mb], a0, a1, a2, a3, bl[kt][nb][0], bl[kt][nb][1]);
-                            }
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(stage));
-            }
-            if (aborted) return;
-            if (!active) continue;
-
-            // ---- pairwise merge of the two token halves of this column set
-#pragma unroll
-            for (int nb = 0; nb < NBW; ++nb)
-#pragma unroll
-                for (int o_ = 4; o_ < 32; o_ <<= 1) {
-                    l[nb][0] += __shfl_xor_sync(0xffffffffu, l[nb][0], o_);
-                    l[nb][1] += __shfl_xor_sync(0xffffffffu, l[nb][1], o_);
-                }
-            float *ml = pair + 8 * NBW * L::kOStride;  // m then l of the 8 NBW rows
-            if (ts == 1) {
-                if (!wait_phase(merge_done(cs), (qi & 1) ^ 1, abort_flag, p.status)) return;
-#pragma unroll
-                for (int nb = 0; nb < NBW; ++nb) {
-                    if (gid == 0) {
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            ml[8 * nb + 2 * tig + e] = m[nb][e];
-                            ml[8 * NBW + 8 * nb + 2 * tig + e] = l[nb][e];
-                        }
-                    }
-#pragma unroll
-                    for (int mb = 0; mb < 8; ++mb) {
-                        float *w0 = pair + (8 * nb + 2 * tig) * L::kOStride + 16 * mb + gid;
-                        w0[0] = o[nb][mb][0];
-                        w0[L::kOStride] = o[nb][mb][1];
-                        w0[8] = o[nb][mb][2];
-                        w0[L::kOStride + 8] = o[nb][mb][3];
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(merge_full(cs));
-                continue;
-            }
-            if (!wait_phase(merge_full(cs), qi & 1, abort_flag, p.status)) return;
-            float wa[NBW][2], wb[NBW][2], lse[NBW][2];
-#pragma unroll
-            for (int nb = 0; nb < NBW; ++nb)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float mp = ml[8 * nb + 2 * tig + e], lp = ml[8 * NBW + 8 * nb + 2 * tig + e];
-                    const float M = fmaxf(m[nb][e], mp);
-                    if (M == -INFINITY) {
-                        wa[nb][e] = wb[nb][e] = 0.f;
-                        lse[nb][e] = -INFINITY;
-                    } else {
-                        const float ea = ex2(m[nb][e] - M), eb = ex2(mp - M);
-                        const float Ls = l[nb][e] * ea + lp * eb;
-                        wa[nb][e] = ea / Ls;
-                        wb[nb][e] = eb / Ls;
-                        lse[nb][e] = (M + lg2(Ls)) * kLn2;
-                    }
-                }
-#pragma unroll
-            for (int nb = 0; nb < NBW; ++nb)
-#pragma unroll
-                for (int mb = 0; mb < 8; ++mb) {
-                    const float *w0 = pair + (8 * nb + 2 * tig) * L::kOStride + 16 * mb + gid;
-                    o[nb][mb][0] = o[nb][mb][0] * wa[nb][0] + w0[0] * wb[nb][0];
-                    o[nb][mb][1] = o[nb][mb][1] * wa[nb][1] + w0[L::kOStride] * wb[nb][1];
-                    o[nb][mb][2] = o[nb][mb][2] * wa[nb][0] + w0[8] * wb[nb][0];
-                    o[nb][mb][3] = o[nb][mb][3] * wa[nb][1] + w0[L::kOStride + 8] * wb[nb][1];
-                }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(merge_done(cs));
-            // ---- the partial of rows [cb, cb + 8 NBW) (those below R)
-#pragma unroll
-            for (int nb = 0; nb < NBW; ++nb)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int r = cb + 8 * nb + 2 * tig + e;
-                    if (r >= R) continue;
-                    float *dst = p.partial_o + (static_cast<int64_t>(slot) * R + r) * kHeadDim + gid;
-#pragma unroll
-                    for (int mb = 0; mb < 8; ++mb) {
-                        dst[16 * mb] = o[nb][mb][e];
-                        dst[16 * mb + 8] = o[nb][mb][2 + e];
-                    }
-                    if (gid == 0) p.partial_lse[static_cast<int64_t>(slot) * R + r] = lse[nb][e];
-                }
-        }
-        return;
     } else {
     // =========================== consumer warps ===========================
     const int grp = warp / 4, wig = warp & 3;
@@ -1946,7 +1671,7 @@ using namespace dsa;
 
 extern "C" int32_t dsa_multi_slots_per_desc(int32_t q_len, int32_t group) {
     if (q_len < 1 || group < 1) return -1;
-    return q_len > 1 && q_len * group > 16 ? 2 : 1;
+    return q_len > 1 ? 2 : 1;
 }
 
 extern "C" dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void *q, dsa_dtype q_dtype,
@@ -1981,12 +1706,8 @@ extern "C" dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void
     }
     kp.q_len = q_len;
     kp.slots_per_desc = dsa_multi_slots_per_desc(q_len, num_q_heads / num_kv_heads);
-    const dim3 grid(map->num_ctas);
-    // up to 16 query rows: mma.sync warps (8 warps, 32 tokens x 8 rows each); more rows:
-    // the tensor-memory kernel (measured faster from 24 rows up, slower at 16)
-    if (kp.slots_per_desc == 1)
-        return launch<0, kPersistStagesBf16, kPersistGroups, true, false, 1, 1>(a, kp, grid, to_cuda(stream));
-    return launch<0, kTcStages, 2, true, false, 1, 3>(a, kp, grid, to_cuda(stream));
+    // the tensor-memory kernel, for any number of query rows up to 64
+    return launch<0, kTcStages, 2, true, false, 1, 3>(a, kp, dim3(map->num_ctas), to_cuda(stream));
 }
 
 extern "C" dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *q_scale, const void *k_pages,
