@@ -1038,6 +1038,61 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
             const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
             const uint32_t o_col = 256 + 128 * team;
             const int tid = sp * 32 + lane;  // within the team
+            // The descriptor end of a team (its partial, slot 2 x descriptor + team), deferred
+            // until the team has handed over the P of its first tile of the next descriptor: a
+            // descriptor's first tile never rescales O, so it need not wait for the previous
+            // descriptor's last P.V, and the team computes it while that P.V completes.
+            auto team_epilogue = [&](int slot, float (&m)[2], float (&l)[2], int pv_desc, int last_g) -> bool {
+                // ---- this team's products of the descriptor are done once its last tile's buffer
+                //      phase is (that commit covers every earlier product)
+                if (last_g >= 0) {
+                    if (!wait_phase(o_done(team), (last_g >> 1) & 1, abort_flag, p.status)) return false;
+                    tc_fence_after();
+                }
+                // ---- this team's partial (slot 2 x descriptor + team): O_t / l, lse = ln(2) (m + log2 l)
+                float inv[2], lse[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+                    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+                    inv[h] = l[h] > 0.f ? 1.f / l[h] : 0.f;
+                    lse[h] = l[h] > 0.f ? (m[h] + lg2(l[h])) * kLn2 : -INFINITY;
+                }
+                const int64_t slot_row = (2 * static_cast<int64_t>(slot) + team) * R;
+                float *dst_a = p.partial_o + (slot_row + ra) * kHeadDim + 2 * tig;
+                float *dst_b = p.partial_o + (slot_row + rb) * kHeadDim + 2 * tig;
+                // O_t into registers first, then release it for the next descriptor's products
+                float o[16][4];
+                if (pv_desc > 0) {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) tmem_ld16x8(tmem + lane_base + o_col + 8 * k, o[k]);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_free(team));
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    if (ra < R) *reinterpret_cast<float2 *>(dst_a + 8 * k) = make_float2(o[k][0] * inv[0], o[k][1] * inv[0]);
+                    if (rb < R) *reinterpret_cast<float2 *>(dst_b + 8 * k) = make_float2(o[k][2] * inv[1], o[k][3] * inv[1]);
+                }
+                if (tig == 0) {
+                    if (ra < R) p.partial_lse[slot_row + ra] = lse[0];
+                    if (rb < R) p.partial_lse[slot_row + rb] = lse[1];
+                }
+                return true;
+            };
+            bool ep_pending = false;
+            int ep_slot = 0, ep_pv = 0, ep_last_g = -1;
+            float ep_m[2] = {0.f, 0.f}, ep_l[2] = {0.f, 0.f};
+            auto flush_epilogue = [&]() -> bool {
+                if (!ep_pending) return true;
+                ep_pending = false;
+                return team_epilogue(ep_slot, ep_m, ep_l, ep_pv, ep_last_g);
+            };
             int g = 0;
             for (int d = 0;; ++d) {
                 const int qslot = d % kQSlots;
@@ -1050,7 +1105,10 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 const int dt0 = inf->t0, len = inf->len;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qempty_bar(qslot));
-                if (end) break;
+                if (end) {
+                    if (!flush_epilogue()) failed = true;
+                    break;
+                }
                 // visible tokens of each row: t < lim (-1: a row past R)
                 const int lim[2] = {ra < R ? len - p.q_len + ra / G + 1 : -1, rb < R ? len - p.q_len + rb / G + 1 : -1};
                 float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
@@ -1071,8 +1129,9 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + 64 * buf + 8 * k, sv[k]);
                         tmem_wait_ld();
                     }
-                    // O_team was last written by the P.V of this team's previous tile
-                    if (!wait_phase(o_done(team), ((g >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                    // O_team was last written by the P.V of this team's previous tile (a rescale
+                    // reads it); the first tile of a descriptor starts from m = -inf and never does
+                    if (last_g >= 0 && !wait_phase(o_done(team), ((g >> 1) & 1) ^ 1, abort_flag, p.status)) {
                         failed = true;
                         break;
                     }
@@ -1081,6 +1140,10 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(p_full(buf));
+                        if (!flush_epilogue()) {
+                            failed = true;
+                            break;
+                        }
                         continue;
                     }
                     // ---- running maximum over each row's visible tokens (t < lim, slot < nv)
@@ -1166,51 +1229,24 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                     __syncwarp();
                     if (lane == 0) mbar_arrive(p_full(buf));
                     ++pv_desc;
-                }
-                if (failed) break;
-                // ---- this team's products of the descriptor are done once its last tile's buffer
-                //      phase is (that commit covers every earlier product)
-                if (last_g >= 0) {
-                    if (!wait_phase(o_done(team), (last_g >> 1) & 1, abort_flag, p.status)) {
+                    // the previous descriptor's end, now that this tile's P is handed over
+                    if (!flush_epilogue()) {
                         failed = true;
                         break;
                     }
-                    tc_fence_after();
                 }
-                // ---- this team's partial (slot 2 x descriptor + team): O_t / l, lse = ln(2) (m + log2 l)
-                float inv[2], lse[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
-                    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
-                    inv[h] = l[h] > 0.f ? 1.f / l[h] : 0.f;
-                    lse[h] = l[h] > 0.f ? (m[h] + lg2(l[h])) * kLn2 : -INFINITY;
+                if (failed) break;
+                // ---- a team without tiles here still owes the previous descriptor's end; this
+                //      descriptor's end waits for the next descriptor's first tile
+                if (!flush_epilogue()) {
+                    failed = true;
+                    break;
                 }
-                const int64_t slot_row = (2 * static_cast<int64_t>(slot) + team) * R;
-                float *dst_a = p.partial_o + (slot_row + ra) * kHeadDim + 2 * tig;
-                float *dst_b = p.partial_o + (slot_row + rb) * kHeadDim + 2 * tig;
-                // O_t into registers first, then release it for the next descriptor's products
-                float o[16][4];
-                if (pv_desc > 0) {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) tmem_ld16x8(tmem + lane_base + o_col + 8 * k, o[k]);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(o_free(team));
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    if (ra < R) *reinterpret_cast<float2 *>(dst_a + 8 * k) = make_float2(o[k][0] * inv[0], o[k][1] * inv[0]);
-                    if (rb < R) *reinterpret_cast<float2 *>(dst_b + 8 * k) = make_float2(o[k][2] * inv[1], o[k][3] * inv[1]);
-                }
-                if (tig == 0) {
-                    if (ra < R) p.partial_lse[slot_row + ra] = lse[0];
-                    if (rb < R) p.partial_lse[slot_row + rb] = lse[1];
-                }
+                ep_pending = true;
+                ep_slot = slot;
+                ep_pv = pv_desc;
+                ep_last_g = last_g;
+                ep_m[0] = m[0], ep_m[1] = m[1], ep_l[0] = l[0], ep_l[1] = l[1];
             }
         }
         (void)failed;
