@@ -1172,7 +1172,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                     if (__any_sync(0xffffffffu, grow[0] || grow[1])) {
                         // rows whose maximum grew: O_team *= 2^(m_old - m_new) (its last P.V is done)
                         tc_fence_after();
-#pragma unroll
+#pragma unroll 1  // rare: kept small for the instruction cache
                         for (int half = 0; half < 2; ++half) {
                             float o[8][4];
 #pragma unroll
