@@ -460,9 +460,9 @@ def bench_multi(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes: 
     """Multi-token verify steps (q_len query tokens per request, causal within the draft) on
     this workload's KV, C bins: plan -> dsa_decode_multi -> dsa_combine_multi in one graph.  The KV
     stream is read once per step whatever q_len is; `vs_q_len_one_token_steps` compares with
-    q_len separate one-token steps (q_len x the one-token step time)."""
-    if w.kv_dtype != "bf16":
-        return {"note": "multi-token queries are built for bf16 K/V"}
+    q_len separate one-token steps (q_len x the one-token step time).  bf16 K/V runs on the
+    tensor-memory kernel, E4M3 K/V (with E4M3 Q and per-row Q scales) on the mma.sync one."""
+    fp8 = w.kv_dtype == "fp8"
     B, hq, hkv = int(inp["seq_lens"].shape[0]), w.num_q_heads, w.num_kv_heads
     G = hq // hkv
     gen = torch.Generator(device=device)
@@ -470,7 +470,8 @@ def bench_multi(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes: 
     peak, _ = measured_peaks()
     res = {}
     for q_len in (2, 6):
-        q = torch.randn(B, q_len, hq, 128, generator=gen, device=device).to(torch.bfloat16)
+        qf = torch.randn(B, q_len, hq, 128, generator=gen, device=device)
+        q, qs = workloads._quantize_e4m3(qf) if fp8 else (qf.to(torch.bfloat16), None)
         tm = dsa.TaskMap(B, hkv, C, device)
         po, pl = dsa.partial_buffers(2 * tm.max_descs, q_len * G, device)  # at most 2 slots per descriptor
         out = torch.empty(B, q_len, hq, 128, dtype=torch.bfloat16, device=device)
@@ -479,9 +480,10 @@ def bench_multi(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes: 
         def plan(tm=tm):
             dsa.plan(inp["seq_lens"], hkv, C, m, task_map=tm)
 
-        def dec(q=q, q_len=q_len, tm=tm, po=po, pl=pl):
+        def dec(q=q, qs=qs, q_len=q_len, tm=tm, po=po, pl=pl):
             dsa.decode_multi(q_len, q, inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
-                             inp["sm_scale"], partial_o=po, partial_lse=pl)
+                             inp["sm_scale"], partial_o=po, partial_lse=pl, q_scale=qs, k_scale=inp["k_scale"],
+                             v_scale=inp["v_scale"])
 
         def comb(q_len=q_len, tm=tm, po=po, pl=pl, out=out, out_lse=out_lse):
             dsa.combine_multi(q_len, tm, po, pl, hq, out=out, out_lse=out_lse)
@@ -492,7 +494,8 @@ def bench_multi(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes: 
         t_plan, t_dec, t_comb = (float(x) for x in per.mean(axis=0))
         step = t_plan + t_dec + t_comb
         gbs = nbytes / (t_dec * 1e-3) / 1e9
-        flops = 4.0 * q_len * G * 128 * (nbytes / 512)  # QK and PV over every (token, KV head)
+        # QK and PV over every (token, KV head): 512 B of bf16 K/V, 264 B of E4M3 K/V + scales
+        flops = 4.0 * q_len * G * 128 * (nbytes / (264 if fp8 else 512))
         res[f"q_len_{q_len}"] = {
             "rows_per_unit": q_len * G, "us_per_step": round(step * 1e3, 2),
             "breakdown_us": {"plan": round(t_plan * 1e3, 2), "decode": round(t_dec * 1e3, 2),

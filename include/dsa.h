@@ -212,15 +212,18 @@ dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_sca
  * query rows of its unit.  Query token i of request b stands at position
  * seq_lens[b] - q_len + i and sees the tokens t <= that position (causal within the
  * draft; rows with no visible token in a descriptor get o = 0, lse = -inf there).
- *   q        [B, q_len, Hq, 128] bf16 (row i*G + g of unit (b, h) is q[b][i][h*G + g]).
+ *   q        [B, q_len, Hq, 128] bf16 or E4M3 (row i*G + g of unit (b, h) is
+ *            q[b][i][h*G + g]); E4M3: q_scale [B, q_len, Hq] fp32, K/V and their
+ *            scales as for dsa_decode.
  *   partial_o [S * map->max_descs, q_len*G, 128] fp32, partial_lse [S * map->max_descs,
  *            q_len*G] with S = dsa_multi_slots_per_desc(q_len, G): 2 for q_len > 1
  *            (slots 2x and 2x + 1, each the attention over part of the descriptor's
- *            tiles: the two softmax teams of the tensor-memory kernel), 1 for q_len = 1;
+ *            tokens: for bf16 K/V the two softmax teams of the tensor-memory kernel, for
+ *            E4M3 K/V the two 32-token halves of every tile), 1 for q_len = 1;
  *            merging a descriptor's slots gives its attention, and dsa_combine_multi
  *            does so.
- * Supported: BF16 Q and K/V, q_len * G <= 64; q_len = 1 is exactly dsa_decode (all of
- * its dtypes).  Other arguments and errors are as for dsa_decode.
+ * Supported: the dtypes of dsa_decode (BF16, or E4M3 Q and K/V), q_len * G <= 64;
+ * q_len = 1 is exactly dsa_decode.  Other arguments and errors are as for dsa_decode.
  */
 int32_t dsa_multi_slots_per_desc(int32_t q_len, int32_t group);
 dsa_status dsa_decode_multi(int32_t q_len, const void *q, dsa_dtype q_dtype, const float *q_scale,

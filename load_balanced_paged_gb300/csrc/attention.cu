@@ -107,31 +107,39 @@ constexpr int kMaxPagesPerTile = kTile / 16;  // pages of 16 tokens: four per ti
 // warps of the CTA merge at each descriptor end.  QW = 3: multi-token queries on the
 // 5th-generation tensor cores: S = Q K^T and O = P V accumulate in tensor memory, two
 // teams of four softmax warps, a warp issuing S (and laying Q out as its operand), a warp
-// issuing P.V.  (An mma.sync kernel for up to 16 query rows per unit measured 214-221 us on
-// the mixed lengths against 191-195 us for the tensor-memory kernel at 2-16 rows: removed.)
+// issuing P.V.  (An mma.sync kernel for up to 16 query rows per unit of bf16 K/V measured
+// 214-221 us on the mixed lengths against 191-195 us for the tensor-memory kernel at 2-16
+// rows: bf16 K/V always takes the tensor-memory kernel.)  QW = 1 or 2: multi-token queries
+// over E4M3 K/V with mma.sync (E4M3 products for S, f16 for P.V): every consumer warp takes
+// every tile, its token half for its set of QW 8-row blocks, and the two token halves are
+// the descriptor's two partial slots.  QW = 4: E4M3 K/V with up to 16 rows, the one-token
+// shape (groups on alternate tiles, 16 tokens per warp) over two 8-row blocks; each group
+// merges its warps into its own partial slot.
 template <int KV, int STAGES, int GROUPS, int MSLOTS = 2, int QW = 0>
 struct Layout {
     // descriptors handed ahead to the consumers (Q + info): with one query token a slot is
     // small, and more of them let the producer run ahead through runs of short descriptors
-    static constexpr int kQSlots = QW == 0 ? 4 : 2;
+    static constexpr int kQSlots = (QW == 0 || QW == 4) ? 4 : 2;
     static constexpr bool kTc = QW == 3;
     static constexpr int kNcw = GROUPS * 4;  // consumer warps (softmax warps for QW = 3)
     static constexpr int kThreads = (kNcw + (kTc ? 3 : 1)) * 32;  // consumers + producer (+ MMA, Q warps)
     static constexpr int kThreadsFused = (kNcw + 2) * 32;  // + epilogue warp (fused combine)
     static constexpr int kStageTx = 2 * Cfg<KV>::kTileBytes + 2 * Cfg<KV>::kScaleBytes;
     static constexpr int kStageBytes = round_up(kStageTx, 1024);
-    static constexpr int kQRows = QW ? kMaxRows : kMaxGroup;
+    static constexpr int kQRows = QW == 0 ? kMaxGroup : (QW == 4 ? 16 : kMaxRows);
     static constexpr int kQSlot = kQRows * Cfg<KV>::kQHeadBytes;
     static constexpr int kQOff = STAGES * kStageBytes;
     static constexpr int kOStride = 132;  // floats per head row of a warp's O (padding avoids bank conflicts)
-    static constexpr int kWarpFloats = kMaxGroup * kOStride + 2 * kMaxGroup;
+    static constexpr int kWarpRows = QW == 4 ? 16 : kMaxGroup;  // rows of a warp's merge deposit
+    static constexpr int kWarpFloats = kWarpRows * kOStride + 2 * kWarpRows;
     // QW = 3: Q as the MMA's A operand (64 rows x 128, K-major with the 128-byte swizzle, two
     // 64-column halves of 8 KB, as the TMA lays out a K tile), two buffers.
     static constexpr int kQcOff = kQOff + kQSlots * kQSlot;
     static constexpr int kQcBytes = kTc ? 2 * kMaxRows * kHeadDim * 2 : 0;
     static constexpr int kMergeOff = kQcOff + kQcBytes;
-    static constexpr int kMergeSlot = kTc ? 0 : kNcw * kWarpFloats;  // floats per merge slot
-    static constexpr int kMergeBars = kTc ? 0 : 2;  // merge_full / merge_done barriers each
+    static constexpr bool kMerge = QW == 0 || QW == 4;  // warps merge their states in shared memory
+    static constexpr int kMergeSlot = kMerge ? kNcw * kWarpFloats : 0;  // floats per merge slot
+    static constexpr int kMergeBars = kMerge ? 2 : 0;  // merge_full / merge_done barriers each (QW = 4: per group)
     static constexpr int kTcBars = kTc ? 22 : 0;  // s_full, s_free, p_full x4; o_done, o_free, qc_full, qc_free, qd_full x2
     static constexpr int kBarOff = kMergeOff + MSLOTS * kMergeSlot * 4;
     // full, empty, qfull, qempty, merge_full, merge_done, epi_ready, epi_free, tensor-core barriers
@@ -149,7 +157,7 @@ struct Layout {
     // stages' full barriers in order.  With stages shared by two groups, one group could wait
     // for phase k+1 while phase k is still pending, pass the parity test early and arrive on
     // the stage's empty barrier out of turn (an undefined mbarrier use that faults the GPU).
-    static_assert(QW > 0 || STAGES % GROUPS == 0, "each stage must belong to one consumer group");
+    static_assert(!(QW == 0 || QW == 4) || STAGES % GROUPS == 0, "each stage must belong to one consumer group");
     static_assert(kStageBytes % 1024 == 0 && kQOff % 1024 == 0, "swizzled TMA boxes need 1024-byte alignment");
     static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
@@ -383,7 +391,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             // QW = 1, 2: every consumer warp reads every stage; QW = 3: the S and PV warps release it
-            mbar_init(empty_bar(s), QW == 3 ? 2 : 4);
+            mbar_init(empty_bar(s), QW == 3 ? 2 : ((QW == 1 || QW == 2) ? NCW : 4));
         }
         for (int s = 0; s < kQSlots; ++s) {
             mbar_init(qfull_bar(s), 1);
@@ -402,7 +410,12 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 mbar_init(qc_free(b), 1);
                 mbar_init(qd_full(b), 1);
             }
-        } else {
+        } else if (QW == 4) {
+            for (int s = 0; s < 2; ++s) {  // one pair per consumer group
+                mbar_init(merge_full(s), 4);
+                mbar_init(merge_done(s), 4);
+            }
+        } else if (QW == 0) {
             for (int s = 0; s < MSLOTS; ++s) {
                 mbar_init(merge_full(s), NCW);
                 mbar_init(merge_done(s), NCW);
@@ -1258,6 +1271,505 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
             tmem_dealloc(tmem, 512);
         }
         return;
+    } else if constexpr (QW == 1 || QW == 2) {
+        // ============== multi-token queries over E4M3 K/V (mma.sync, 8 warps) ==============
+        // Rows r = i * G + g (query token i, head g), r < R = q_len * G; row r of a request
+        // of length len sees the tokens t < len - q_len + i + 1.  Warp w takes the tokens
+        // [32 (w & 1), +32) of every tile for the rows [8 QW (w >> 1), +8 QW): S^T blocks of
+        // 16 tokens x 8 rows (E4M3 products, k = 32), one online softmax per row over the
+        // warp's token half, and O^T += V^T . P^T with V widened to f16 (exact) and the
+        // per-token V scale folded into an f16 P.  The two token halves are the descriptor's
+        // two partial slots (2 x descriptor + half), as the two softmax teams of the
+        // tensor-memory kernel are: no merge inside the CTA.
+        constexpr int NBW = QW;
+        const int ts = warp & 1, cs = warp >> 1;
+        const int tok_base = 32 * ts;
+        const int cb = 8 * NBW * cs;
+        const int R = p.q_len * G;
+        const bool active = cb < R;
+        const int gid = lane >> 2, tig = lane & 3;
+        const int xr = lane & 7;
+        // ldmatrix rows of this lane (K and V alike: [64 rows][128 B], 128-byte swizzle):
+        // matrices (tokens 0-7 | 8-15) x (16-byte chunk 2s | 2s + 1)
+        const int k_row = tok_base + xr + ((lane >> 3) & 1) * 8;
+        const int k_chunk = lane >> 4;
+
+        for (int qi = 0;; ++qi) {
+            const int qslot = qi % kQSlots;
+            if (!wait_phase(qfull_bar(qslot), (qi / kQSlots) & 1, abort_flag, p.status)) return;
+            const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
+            if (inf->end) break;
+            const int n = inf->n, slot = inf->slot, c_start = inf->c_start, dt0 = inf->t0, len = inf->len;
+            const int d_b = inf->b, d_h = inf->h;
+
+            // Q fragments (B operand, n = row cb + 8 nb + gid), zero past R
+            uint32_t qf[NBW][4][2];
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb) {
+                const int r = cb + 8 * nb + gid;
+                const uint8_t *qs = smem + L::kQOff + qslot * L::kQSlot + r * C::kQHeadBytes;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    qf[nb][ks][0] = r < R ? *reinterpret_cast<const uint32_t *>(qs + 32 * ks + 4 * tig) : 0u;
+                    qf[nb][ks][1] = r < R ? *reinterpret_cast<const uint32_t *>(qs + 32 * ks + 4 * tig + 16) : 0u;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qempty_bar(qslot));
+
+            // this lane's two rows per block (S^T columns 2 tig, 2 tig + 1): score factor
+            // (softmax scale x q_scale) and causal limit; rows past R get 0 and are never stored
+            float qsc[NBW][2];
+            int lim[NBW][2];
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = cb + 8 * nb + 2 * tig + e;
+                    const int i = r < R ? r / G : 0;
+                    qsc[nb][e] = r < R ? p.score_scale *
+                                             p.q_scale[(static_cast<int64_t>(d_b) * p.q_len + i) * p.hq + d_h * G + (r - i * G)]
+                                       : 0.f;
+                    lim[nb][e] = len - p.q_len + i + 1;
+                }
+            const int lim_min = len - p.q_len + 1;  // every row sees the tokens below this
+
+            float m[NBW][2], l[NBW][2], o[NBW][8][4];
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb) {
+                m[nb][0] = m[nb][1] = -INFINITY;
+                l[nb][0] = l[nb][1] = 0.f;
+#pragma unroll
+                for (int mb = 0; mb < 8; ++mb) o[nb][mb][0] = o[nb][mb][1] = o[nb][mb][2] = o[nb][mb][3] = 0.f;
+            }
+            float vsc = 0.f;  // O holds the true output divided by vsc (set by the first scaled tile)
+
+            bool aborted = false;
+            for (int li = 0; li < n; ++li) {
+                const int c = c_start + li;
+                const int stage = c % STAGES;
+                if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status)) {
+                    aborted = true;
+                    break;
+                }
+                const int nv = nvalid[stage];
+                if (active && nv > tok_base) {
+                    const uint32_t kbase = sbase + stage * L::kStageBytes;
+                    const uint32_t vbase = kbase + C::kTileBytes;
+                    const float *ksm = reinterpret_cast<const float *>(smem + stage * L::kStageBytes + 2 * C::kTileBytes);
+                    const float *vsm = ksm + kTile;
+                    const int T0 = (dt0 + li) * kTile + tok_base;  // token of this warp's first row
+                    // ---- S^T = K . Q^T for 2 blocks of 16 tokens x NBW blocks of 8 rows
+                    float sc[2][NBW][4];
+#pragma unroll
+                    for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+                        for (int nb = 0; nb < NBW; ++nb) sc[kt][nb][0] = sc[kt][nb][1] = sc[kt][nb][2] = sc[kt][nb][3] = 0.f;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const int ch = 2 * ks + k_chunk;
+#pragma unroll
+                        for (int kt = 0; kt < 2; ++kt) {
+                            uint32_t a0, a1, a2, a3;
+                            ldsm_x4(kbase + (k_row + 16 * kt) * 128 + ((ch ^ xr) << 4), a0, a1, a2, a3);
+#pragma unroll
+                            for (int nb = 0; nb < NBW; ++nb) mma_e4m3(sc[kt][nb], a0, a1, a2, a3, qf[nb][ks][0], qf[nb][ks][1]);
+                        }
+                    }
+                    // per-token scales; tokens past the tile's valid rows get none (their
+                    // shared memory may hold anything) and are masked below
+                    float ks_[2][2], vs_[2][2];
+#pragma unroll
+                    for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int t = tok_base + 16 * kt + 8 * hh + gid;
+                            ks_[kt][hh] = t < nv ? ksm[t] : 0.f;
+                            vs_[kt][hh] = t < nv ? vsm[t] : 0.f;
+                        }
+                    const bool mask = T0 + 32 > lim_min;  // some row of the warp's tokens is past a limit
+#pragma unroll
+                    for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+                        for (int nb = 0; nb < NBW; ++nb) {
+                            sc[kt][nb][0] *= qsc[nb][0] * ks_[kt][0];
+                            sc[kt][nb][1] *= qsc[nb][1] * ks_[kt][0];
+                            sc[kt][nb][2] *= qsc[nb][0] * ks_[kt][1];
+                            sc[kt][nb][3] *= qsc[nb][1] * ks_[kt][1];
+                            if (mask) {
+                                const int ta = T0 + 16 * kt + gid, tb = ta + 8;
+                                if (ta >= lim[nb][0]) sc[kt][nb][0] = -INFINITY;
+                                if (ta >= lim[nb][1]) sc[kt][nb][1] = -INFINITY;
+                                if (tb >= lim[nb][0]) sc[kt][nb][2] = -INFINITY;
+                                if (tb >= lim[nb][1]) sc[kt][nb][3] = -INFINITY;
+                            }
+                        }
+                    // ---- the V scale folded into P, relative to the warp's largest scale in
+                    //      the tile (O is rescaled when that reference changes)
+                    float vm = fmaxf(fmaxf(vs_[0][0], vs_[0][1]), fmaxf(vs_[1][0], vs_[1][1]));
+#pragma unroll
+                    for (int o_ = 4; o_ < 32; o_ <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o_));
+                    float vf = 1.f;  // old reference / new reference
+                    if (vm > 0.f) {
+                        if (vsc > 0.f) vf = vsc / vm;
+                        vsc = vm;
+                    }
+                    const float vinv = vsc > 0.f ? 1.f / vsc : 0.f;
+                    // ---- online softmax (base 2) per row over the warp's 32 tokens
+                    uint32_t bh[2][NBW][2];
+#pragma unroll
+                    for (int nb = 0; nb < NBW; ++nb) {
+                        float mx0 = fmaxf(fmaxf(sc[0][nb][0], sc[0][nb][2]), fmaxf(sc[1][nb][0], sc[1][nb][2]));
+                        float mx1 = fmaxf(fmaxf(sc[0][nb][1], sc[0][nb][3]), fmaxf(sc[1][nb][1], sc[1][nb][3]));
+#pragma unroll
+                        for (int o_ = 4; o_ < 32; o_ <<= 1) {
+                            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
+                            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
+                        }
+                        const float mn0 = fmaxf(m[nb][0], mx0), mn1 = fmaxf(m[nb][1], mx1);
+                        const float r0 = mn0 == -INFINITY ? 0.f : mn0, r1 = mn1 == -INFINITY ? 0.f : mn1;
+                        const float al0 = ex2(m[nb][0] - r0), al1 = ex2(m[nb][1] - r1);
+                        float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+                        for (int kt = 0; kt < 2; ++kt) {
+                            const float p0 = ex2(sc[kt][nb][0] - r0), p1 = ex2(sc[kt][nb][1] - r1);
+                            const float p2 = ex2(sc[kt][nb][2] - r0), p3 = ex2(sc[kt][nb][3] - r1);
+                            ls0 += p0 + p2;
+                            ls1 += p1 + p3;
+                            const float wa = vs_[kt][0] * vinv, wb = vs_[kt][1] * vinv;
+                            bh[kt][nb][0] = movmatrix_trans(pack_f16x2(p0 * wa, p1 * wa));
+                            bh[kt][nb][1] = movmatrix_trans(pack_f16x2(p2 * wb, p3 * wb));
+                        }
+                        l[nb][0] = l[nb][0] * al0 + ls0;
+                        l[nb][1] = l[nb][1] * al1 + ls1;
+                        m[nb][0] = mn0;
+                        m[nb][1] = mn1;
+                        const float f0 = al0 * vf, f1 = al1 * vf;
+#pragma unroll
+                        for (int mb = 0; mb < 8; ++mb) {
+                            o[nb][mb][0] *= f0;
+                            o[nb][mb][1] *= f1;
+                            o[nb][mb][2] *= f0;
+                            o[nb][mb][3] *= f1;
+                        }
+                    }
+                    // ---- O^T += V^T . P^T; V rows past the tile's valid tokens are zeroed
+                    const bool partial = nv < tok_base + 32;
+#pragma unroll
+                    for (int kt = 0; kt < 2; ++kt) {
+                        const uint32_t mlo = partial ? tok_mask(tok_base + 16 * kt + 2 * tig, nv) : 0xFFFFFFFFu;
+                        const uint32_t mhi = partial ? tok_mask(tok_base + 16 * kt + 8 + 2 * tig, nv) : 0xFFFFFFFFu;
+#pragma unroll
+                        for (int mp = 0; mp < 4; ++mp) {
+                            const int ch = 2 * mp + k_chunk;
+                            uint32_t x0, x1, x2, x3;
+                            ldsm_x4_trans(vbase + (k_row + 16 * kt) * 128 + ((ch ^ xr) << 4), x0, x1, x2, x3);
+                            // x0 / x1: tokens 0-7 / 8-15 of chunk 2 mp; x2 / x3: of chunk 2 mp + 1;
+                            // each holds, for dims (2 gid, 2 gid + 1) of its chunk, tokens (2 tig, 2 tig + 1)
+                            uint32_t a0, a1, a2, a3;
+                            cvt_pair(x0, a0, a1);
+                            cvt_pair(x1, a2, a3);
+                            a0 &= mlo;
+                            a1 &= mlo;
+                            a2 &= mhi;
+                            a3 &= mhi;
+#pragma unroll
+                            for (int nb = 0; nb < NBW; ++nb) mma_f16(o[nb][2 * mp], a0, a1, a2, a3, bh[kt][nb][0], bh[kt][nb][1]);
+                            cvt_pair(x2, a0, a1);
+                            cvt_pair(x3, a2, a3);
+                            a0 &= mlo;
+                            a1 &= mlo;
+                            a2 &= mhi;
+                            a3 &= mhi;
+#pragma unroll
+                            for (int nb = 0; nb < NBW; ++nb)
+                                mma_f16(o[nb][2 * mp + 1], a0, a1, a2, a3, bh[kt][nb][0], bh[kt][nb][1]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(stage));
+            }
+            if (aborted) return;
+            if (!active) continue;
+
+            // ---- this warp's partial: rows [cb, cb + 8 NBW) below R of slot 2 x descriptor + ts
+            const int64_t slot_row = (2 * static_cast<int64_t>(slot) + ts) * R;
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float lt = l[nb][e];
+#pragma unroll
+                    for (int o_ = 4; o_ < 32; o_ <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o_);
+                    const int r = cb + 8 * nb + 2 * tig + e;
+                    if (r >= R) continue;
+                    const float w = lt > 0.f ? vsc / lt : 0.f;
+                    float *dst = p.partial_o + (slot_row + r) * kHeadDim + 2 * gid;
+#pragma unroll
+                    for (int mb = 0; mb < 8; ++mb)
+                        *reinterpret_cast<float2 *>(dst + 16 * mb) = make_float2(o[nb][mb][e] * w, o[nb][mb][2 + e] * w);
+                    if (gid == 0) p.partial_lse[slot_row + r] = lt > 0.f ? (m[nb][e] + lg2(lt)) * kLn2 : -INFINITY;
+                }
+        }
+        return;
+    } else if constexpr (QW == 4) {
+        // ======= multi-token queries over E4M3 K/V, up to 16 rows per unit (mma.sync) =======
+        // The one-token kernel's shape with two 8-row column blocks: the two consumer groups
+        // take alternate tiles (a stage belongs to one group), warp wig of a group takes the
+        // tokens [16 wig, +16) of its tiles for all rows r = i * G + g < R = q_len * G <= 16
+        // (row r of a request of length len sees the tokens t < len - q_len + i + 1).  At a
+        // descriptor end the four warps of a group merge their (m, l, O) in shared memory into
+        // the group's partial, slot 2 x descriptor + group.
+        constexpr int NBW = 2;
+        const int grp = warp / 4, wig = warp & 3;
+        const int gid = lane >> 2, tig = lane & 3;
+        const int tok_base = wig * 16;
+        const int R = p.q_len * G;
+        const int xr = lane & 7;
+        const int k_row = tok_base + xr + ((lane >> 3) & 1) * 8;  // matrices (tokens 0-7 | 8-15) x (chunk 2s | 2s + 1)
+        const int k_chunk = lane >> 4;
+        float *W = reinterpret_cast<float *>(smem + L::kMergeOff) + warp * L::kWarpFloats;
+        const float *WG = reinterpret_cast<const float *>(smem + L::kMergeOff) + 4 * grp * L::kWarpFloats;
+        constexpr int kMl = 16 * L::kOStride;  // m of the 16 rows, then l
+
+        for (int qi = 0;; ++qi) {
+            const int qslot = qi % kQSlots;
+            if (!wait_phase(qfull_bar(qslot), (qi / kQSlots) & 1, abort_flag, p.status)) return;
+            const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
+            if (inf->end) break;
+            const int n = inf->n, slot = inf->slot, c_start = inf->c_start, dt0 = inf->t0, len = inf->len;
+            const int d_b = inf->b, d_h = inf->h;
+
+            // Q fragments (B operand, n = row 8 nb + gid), zero past R
+            uint32_t qf[NBW][4][2];
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb) {
+                const int r = 8 * nb + gid;
+                const uint8_t *qs = smem + L::kQOff + qslot * L::kQSlot + r * C::kQHeadBytes;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    qf[nb][ks][0] = r < R ? *reinterpret_cast<const uint32_t *>(qs + 32 * ks + 4 * tig) : 0u;
+                    qf[nb][ks][1] = r < R ? *reinterpret_cast<const uint32_t *>(qs + 32 * ks + 4 * tig + 16) : 0u;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qempty_bar(qslot));
+
+            // this lane's rows 8 nb + 2 tig + e: score factor (softmax scale x q_scale) and
+            // causal limit; rows past R get 0 and are never stored
+            float qsc[NBW][2];
+            int lim[NBW][2];
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = 8 * nb + 2 * tig + e;
+                    const int i = r < R ? r / G : 0;
+                    qsc[nb][e] = r < R ? p.score_scale *
+                                             p.q_scale[(static_cast<int64_t>(d_b) * p.q_len + i) * p.hq + d_h * G + (r - i * G)]
+                                       : 0.f;
+                    lim[nb][e] = len - p.q_len + i + 1;
+                }
+            const int lim_min = len - p.q_len + 1;  // every row sees the tokens below this
+
+            float m[NBW][2], l[NBW][2], o[NBW][8][4];
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb) {
+                m[nb][0] = m[nb][1] = -INFINITY;
+                l[nb][0] = l[nb][1] = 0.f;
+#pragma unroll
+                for (int mb = 0; mb < 8; ++mb) o[nb][mb][0] = o[nb][mb][1] = o[nb][mb][2] = o[nb][mb][3] = 0.f;
+            }
+            float vsc = 0.f;  // O holds the true output divided by vsc (set by the first scaled tile)
+
+            bool aborted = false;
+            for (int li = ((grp - c_start) % GROUPS + GROUPS) % GROUPS; li < n; li += GROUPS) {
+                const int c = c_start + li;
+                const int stage = c % STAGES;
+                if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status)) {
+                    aborted = true;
+                    break;
+                }
+                const int nv = nvalid[stage];
+                if (nv > tok_base) {
+                    const uint32_t kbase = sbase + stage * L::kStageBytes;
+                    const uint32_t vbase = kbase + C::kTileBytes;
+                    const float *ksm = reinterpret_cast<const float *>(smem + stage * L::kStageBytes + 2 * C::kTileBytes);
+                    const float *vsm = ksm + kTile;
+                    // ---- S^T = K . Q^T  (rows: tokens tok_base + gid / + 8; columns: rows 8 nb + 2 tig, + 1)
+                    float sc[NBW][4];
+#pragma unroll
+                    for (int nb = 0; nb < NBW; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const int ch = 2 * ks + k_chunk;
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(kbase + k_row * 128 + ((ch ^ xr) << 4), a0, a1, a2, a3);
+#pragma unroll
+                        for (int nb = 0; nb < NBW; ++nb) mma_e4m3(sc[nb], a0, a1, a2, a3, qf[nb][ks][0], qf[nb][ks][1]);
+                    }
+                    // per-token scales; tokens past the tile's valid rows get none (their shared
+                    // memory may hold anything) and are masked below
+                    const int ta = tok_base + gid, tb = ta + 8;
+                    const float ksa = ta < nv ? ksm[ta] : 0.f, ksb = tb < nv ? ksm[tb] : 0.f;
+                    const float vsa = ta < nv ? vsm[ta] : 0.f, vsb = tb < nv ? vsm[tb] : 0.f;
+                    const int T0 = (dt0 + li) * kTile + tok_base;  // token of this warp's first row
+                    const bool mask = T0 + 16 > lim_min;  // some row of the warp's tokens is past a limit
+#pragma unroll
+                    for (int nb = 0; nb < NBW; ++nb) {
+                        sc[nb][0] *= qsc[nb][0] * ksa;
+                        sc[nb][1] *= qsc[nb][1] * ksa;
+                        sc[nb][2] *= qsc[nb][0] * ksb;
+                        sc[nb][3] *= qsc[nb][1] * ksb;
+                        if (mask) {
+                            if (T0 + gid >= lim[nb][0]) sc[nb][0] = -INFINITY;
+                            if (T0 + gid >= lim[nb][1]) sc[nb][1] = -INFINITY;
+                            if (T0 + gid + 8 >= lim[nb][0]) sc[nb][2] = -INFINITY;
+                            if (T0 + gid + 8 >= lim[nb][1]) sc[nb][3] = -INFINITY;
+                        }
+                    }
+                    // ---- the V scale folded into P, relative to the warp's largest scale in
+                    //      the tile (O is rescaled when that reference changes)
+                    float vm = fmaxf(vsa, vsb);
+#pragma unroll
+                    for (int o_ = 4; o_ < 32; o_ <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o_));
+                    float vf = 1.f;
+                    if (vm > 0.f) {
+                        if (vsc > 0.f) vf = vsc / vm;
+                        vsc = vm;
+                    }
+                    const float vinv = vsc > 0.f ? 1.f / vsc : 0.f;
+                    const float wa = vsa * vinv, wb = vsb * vinv;
+                    // ---- online softmax (base 2) per row over the warp's 16 tokens
+                    uint32_t bh[NBW][2];
+#pragma unroll
+                    for (int nb = 0; nb < NBW; ++nb) {
+                        float mx0 = fmaxf(sc[nb][0], sc[nb][2]), mx1 = fmaxf(sc[nb][1], sc[nb][3]);
+#pragma unroll
+                        for (int o_ = 4; o_ < 32; o_ <<= 1) {
+                            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
+                            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
+                        }
+                        const float mn0 = fmaxf(m[nb][0], mx0), mn1 = fmaxf(m[nb][1], mx1);
+                        const float r0 = mn0 == -INFINITY ? 0.f : mn0, r1 = mn1 == -INFINITY ? 0.f : mn1;
+                        const float al0 = ex2(m[nb][0] - r0), al1 = ex2(m[nb][1] - r1);
+                        const float p0 = ex2(sc[nb][0] - r0), p1 = ex2(sc[nb][1] - r1);
+                        const float p2 = ex2(sc[nb][2] - r0), p3 = ex2(sc[nb][3] - r1);
+                        l[nb][0] = l[nb][0] * al0 + p0 + p2;
+                        l[nb][1] = l[nb][1] * al1 + p1 + p3;
+                        m[nb][0] = mn0;
+                        m[nb][1] = mn1;
+                        bh[nb][0] = movmatrix_trans(pack_f16x2(p0 * wa, p1 * wa));
+                        bh[nb][1] = movmatrix_trans(pack_f16x2(p2 * wb, p3 * wb));
+                        const float f0 = al0 * vf, f1 = al1 * vf;
+#pragma unroll
+                        for (int mb = 0; mb < 8; ++mb) {
+                            o[nb][mb][0] *= f0;
+                            o[nb][mb][1] *= f1;
+                            o[nb][mb][2] *= f0;
+                            o[nb][mb][3] *= f1;
+                        }
+                    }
+                    // ---- O^T += V^T . P^T (V widened to f16); V rows past the valid tokens are zeroed
+                    const bool partial = nv < tok_base + 16;
+                    const uint32_t mlo = partial ? tok_mask(tok_base + 2 * tig, nv) : 0xFFFFFFFFu;
+                    const uint32_t mhi = partial ? tok_mask(tok_base + 8 + 2 * tig, nv) : 0xFFFFFFFFu;
+#pragma unroll
+                    for (int mp = 0; mp < 4; ++mp) {
+                        const int ch = 2 * mp + k_chunk;
+                        uint32_t x0, x1, x2, x3;
+                        ldsm_x4_trans(vbase + k_row * 128 + ((ch ^ xr) << 4), x0, x1, x2, x3);
+                        // x0 / x1: tokens 0-7 / 8-15 of chunk 2 mp; x2 / x3: of chunk 2 mp + 1;
+                        // each holds, for dims (2 gid, 2 gid + 1) of its chunk, tokens (2 tig, 2 tig + 1)
+                        uint32_t a0, a1, a2, a3;
+                        cvt_pair(x0, a0, a1);
+                        cvt_pair(x1, a2, a3);
+                        a0 &= mlo;
+                        a1 &= mlo;
+                        a2 &= mhi;
+                        a3 &= mhi;
+#pragma unroll
+                        for (int nb = 0; nb < NBW; ++nb) mma_f16(o[nb][2 * mp], a0, a1, a2, a3, bh[nb][0], bh[nb][1]);
+                        cvt_pair(x2, a0, a1);
+                        cvt_pair(x3, a2, a3);
+                        a0 &= mlo;
+                        a1 &= mlo;
+                        a2 &= mhi;
+                        a3 &= mhi;
+#pragma unroll
+                        for (int nb = 0; nb < NBW; ++nb) mma_f16(o[nb][2 * mp + 1], a0, a1, a2, a3, bh[nb][0], bh[nb][1]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(stage));
+            }
+            if (aborted) return;
+
+            // ---- deposit this warp's (m, l, O x vsc) for the group's merge
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+#pragma unroll
+                    for (int o_ = 4; o_ < 32; o_ <<= 1) l[nb][e] += __shfl_xor_sync(0xffffffffu, l[nb][e], o_);
+            if (!wait_phase(merge_done(grp), (qi & 1) ^ 1, abort_flag, p.status)) return;
+#pragma unroll
+            for (int nb = 0; nb < NBW; ++nb) {
+                const int r0 = 8 * nb + 2 * tig;
+                if (gid == 0) {
+                    W[kMl + r0] = m[nb][0];
+                    W[kMl + r0 + 1] = m[nb][1];
+                    W[kMl + 16 + r0] = l[nb][0];
+                    W[kMl + 16 + r0 + 1] = l[nb][1];
+                }
+#pragma unroll
+                for (int mb = 0; mb < 8; ++mb) {
+                    const int d0 = 16 * mb + 2 * gid;
+                    *reinterpret_cast<float2 *>(W + r0 * L::kOStride + d0) = make_float2(o[nb][mb][0] * vsc, o[nb][mb][2] * vsc);
+                    *reinterpret_cast<float2 *>(W + (r0 + 1) * L::kOStride + d0) =
+                        make_float2(o[nb][mb][1] * vsc, o[nb][mb][3] * vsc);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(merge_full(grp));
+            if (!wait_phase(merge_full(grp), qi & 1, abort_flag, p.status)) return;
+            // ---- merge of the group's four warps: the partial of rows below R, slot 2 x descriptor + group
+            const int64_t slot_row = (2 * static_cast<int64_t>(slot) + grp) * R;
+            for (int idx = wig * 32 + lane; idx < R * 32; idx += 128) {
+                const int hd = idx >> 5, d4 = (idx & 31) * 4;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) M = fmaxf(M, WG[w * L::kWarpFloats + kMl + hd]);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float lse = -INFINITY;
+                if (M != -INFINITY) {
+                    float Lsum = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const float *Ww = WG + w * L::kWarpFloats;
+                        const float e = ex2(Ww[kMl + hd] - M);
+                        Lsum += e * Ww[kMl + 16 + hd];
+                        const float4 v = *reinterpret_cast<const float4 *>(Ww + hd * L::kOStride + d4);
+                        acc.x += e * v.x;
+                        acc.y += e * v.y;
+                        acc.z += e * v.z;
+                        acc.w += e * v.w;
+                    }
+                    const float inv = 1.f / Lsum;
+                    acc.x *= inv;
+                    acc.y *= inv;
+                    acc.z *= inv;
+                    acc.w *= inv;
+                    lse = (M + lg2(Lsum)) * kLn2;
+                }
+                *reinterpret_cast<float4 *>(p.partial_o + (slot_row + hd) * kHeadDim + d4) = acc;
+                if ((idx & 31) == 0) p.partial_lse[slot_row + hd] = lse;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(merge_done(grp));
+        }
+        return;
     } else {
     // =========================== consumer warps ===========================
     const int grp = warp / 4, wig = warp & 3;
@@ -1688,6 +2200,8 @@ constexpr int kPairStagesBf16 = 2, kPairStagesFp8 = 4, kPairGroups = 1;
 // The multi-token tensor-memory kernel keeps P in tensor memory, so its shared memory holds a
 // fifth stage (tiles stay in the ring from their load until their P.V, several microseconds).
 constexpr int kTcStages = 5;
+// The E4M3 multi-token kernel: every warp reads every stage, 8 stages of 17 KB.
+constexpr int kMultiStagesFp8 = 8;
 
 // Persistent launch: the CTA shape that keeps all of the map's bins resident at once.
 template <int KV, bool FUSE>
@@ -1725,7 +2239,7 @@ extern "C" dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void
     if (s != DSA_OK) return s;
     if (q_len < 1) return DSA_ERR_INVALID_ARG;
     const int R = q_len * (num_q_heads / num_kv_heads);
-    if (q_len > 1 && (R > kMaxRows || kv_dtype != DSA_BF16)) return DSA_ERR_UNSUPPORTED;
+    if (q_len > 1 && R > kMaxRows) return DSA_ERR_UNSUPPORTED;
     if (!map || !map->cta_desc_begin || !map->descs || !map->meta || !partial_o || !partial_lse)
         return DSA_ERR_INVALID_ARG;
     if (map->num_units != batch * num_kv_heads || map->num_ctas < 1) return DSA_ERR_INVALID_ARG;
@@ -1742,8 +2256,17 @@ extern "C" dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void
     }
     kp.q_len = q_len;
     kp.slots_per_desc = dsa_multi_slots_per_desc(q_len, num_q_heads / num_kv_heads);
-    // the tensor-memory kernel, for any number of query rows up to 64
-    return launch<0, kTcStages, 2, true, false, 1, 3>(a, kp, dim3(map->num_ctas), to_cuda(stream));
+    const dim3 grid(map->num_ctas);
+    // E4M3 K/V: mma.sync warps; up to 16 rows the groups take alternate tiles (16 tokens x
+    // all rows per warp), beyond that every warp takes a token half of every tile for one
+    // 8-row block (up to 32 rows) or two (up to 64)
+    if (kv_dtype == DSA_FP8_E4M3) {
+        if (R <= 16) return launch<1, kMultiStagesFp8, 2, true, false, 1, 4>(a, kp, grid, to_cuda(stream));
+        if (R <= 32) return launch<1, kMultiStagesFp8, 2, true, false, 1, 1>(a, kp, grid, to_cuda(stream));
+        return launch<1, kMultiStagesFp8, 2, true, false, 1, 2>(a, kp, grid, to_cuda(stream));
+    }
+    // bf16 K/V: the tensor-memory kernel, for any number of query rows up to 64
+    return launch<0, kTcStages, 2, true, false, 1, 3>(a, kp, grid, to_cuda(stream));
 }
 
 extern "C" dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *q_scale, const void *k_pages,

@@ -109,7 +109,8 @@ def sub_problem(inp: dict, requests) -> oracle.Problem:
     qs = None if inp["q_scale"] is None else np_bytes(inp["q_scale"][requests])
     return oracle.Problem(np_bytes(inp["q"][requests]), pools["k_pages"], pools["v_pages"], new_bt, lens,
                           inp["num_q_heads"], inp["num_kv_heads"], inp["sm_scale"], q_scale=qs,
-                          k_scale=pools["k_scale"], v_scale=pools["v_scale"])
+                          k_scale=pools["k_scale"], v_scale=pools["v_scale"], page_size=P,
+                          q_len=inp.get("q_len", 1), kv_layout=inp.get("kv_layout", "HND"))
 
 
 # ---------------------------------------------------------------- prologue encodings

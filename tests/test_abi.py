@@ -115,7 +115,7 @@ def test_decode_ex_host_checks(lib):
     assert call(page=8) == 2
     assert call(q_len=0) == 1
     assert call(q_len=9) == 2               # 9 x 8 = 72 query rows per unit
-    assert call(q_len=2, kv_dt=1) == 2      # multi-token E4M3 not built
+    assert call(q_len=2, kv_dt=1) == 2      # bf16 Q over E4M3 K/V not built
 
 
 def test_status_strings(lib):

@@ -43,7 +43,7 @@ def draw_case(seed):
     page = int(rng.choice([16, 32, 64]))
     layout = str(rng.choice(["HND", "NHD"]))
     q_len = int(rng.choice([1, 1, 2, 3, 6])) if G * 6 <= 64 else 1
-    kv = "bf16" if q_len > 1 else str(rng.choice(["bf16", "fp8"]))
+    kv = str(rng.choice(["bf16", "fp8"]))
     C = int(rng.choice([1, 3, 17, 148, 300]))
     m = int(rng.choice([1, 2, 4, 16]))
     return dict(lens=lens, hkv=hkv, hq=G * hkv, page=page, layout=layout, q_len=q_len, kv=kv, C=C, m=m)

@@ -135,16 +135,17 @@ def test_bad_sub_page_is_flagged(dsa, layout):
 
 @pytest.mark.parametrize("page,layout", [(16, "NHD"), (32, "HND"), (64, "NHD")])
 @pytest.mark.parametrize("q_len,hq,hkv", [(2, 64, 8), (6, 64, 8), (3, 16, 4)])
-def test_multi_token_layouts(dsa, page, layout, q_len, hq, hkv):
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_multi_token_layouts(dsa, page, layout, q_len, hq, hkv, kv):
     lens = [1, 40, 64, 129, 1000, 3000]
-    inp = make(lens, hq, hkv, "bf16", page, layout, seed=q_len, q_len=q_len)
+    inp = make(lens, hq, hkv, kv, page, layout, seed=q_len, q_len=q_len)
     out32, lse, tm, po, pl = dsa.attention_multi(inp, 37, min_tiles_per_split=1, out_dtype=torch.float32)
     out16 = dsa.combine_multi(q_len, tm, po, pl, hq, out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
     assert dsa.get_status(tm) == 0
     ref, ref_lse = oracle_of(inp).attention()
-    what = f"q_len {q_len} P {page} {layout}"
-    parity.check_outputs(out16.float().cpu().numpy(), out32.cpu().numpy(), ref, "bf16", what)
+    what = f"{kv} q_len {q_len} P {page} {layout}"
+    parity.check_outputs(out16.float().cpu().numpy(), out32.cpu().numpy(), ref, kv, what)
     parity.assert_lse_close(lse.cpu().numpy(), ref_lse, what)
 
 

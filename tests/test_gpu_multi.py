@@ -2,8 +2,9 @@
 
 q_len query tokens per request, each seeing the KV tokens up to its own position (the
 last q_len positions of the request).  Outputs, LSEs and every descriptor's partial
-rows are compared with the oracle (parity.check_outputs: the stated bf16-KV tolerance on
-the fp32 output, and the bf16 output equal to its round-to-nearest-even).
+rows are compared with the oracle (parity.check_outputs: the stated tolerance of the KV
+dtype on the fp32 output, and the bf16 output equal to its round-to-nearest-even).  bf16
+K/V runs on the tensor-memory kernel, E4M3 K/V on the mma.sync kernel.
 """
 import numpy as np
 import pytest
@@ -26,14 +27,12 @@ def sm_count():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-def make(lens, q_len, hq=64, hkv=8, seed=0):
-    return workloads.make_inputs(np.asarray(lens), hq, hkv, "bf16", seed=seed, device="cuda", q_len=q_len)
+def make(lens, q_len, hq=64, hkv=8, seed=0, kv="bf16"):
+    return workloads.make_inputs(np.asarray(lens), hq, hkv, kv, seed=seed, device="cuda", q_len=q_len)
 
 
 def problem(inp):
-    h = workloads.host_view(inp)
-    return oracle.Problem(h["q"], h["k_pages"], h["v_pages"], h["block_table"], h["seq_lens"],
-                          inp["num_q_heads"], inp["num_kv_heads"], inp["sm_scale"], q_len=inp["q_len"])
+    return parity.problem_from_host(workloads.host_view(inp), inp)
 
 
 def run(dsa, inp, C, m=4):
@@ -58,13 +57,14 @@ CASES = [
 
 @pytest.mark.parametrize("lens,q_len,hq,hkv", CASES)
 @pytest.mark.parametrize("C,m", [(3, 1), (None, 4), (300, 1)])
-def test_multi_vs_oracle(dsa, lens, q_len, hq, hkv, C, m):
-    inp = make(lens, q_len, hq, hkv, seed=q_len + len(lens))
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_multi_vs_oracle(dsa, lens, q_len, hq, hkv, C, m, kv):
+    inp = make(lens, q_len, hq, hkv, seed=q_len + len(lens), kv=kv)
     C = sm_count() if C is None else C
     out16, out32, lse, tm, po, pl = run(dsa, inp, C, m)
     ref, ref_lse = problem(inp).attention()
-    what = f"q_len {q_len} lens {lens} C {C}"
-    parity.check_outputs(out16.float().cpu().numpy(), out32.cpu().numpy(), ref, "bf16", what)
+    what = f"{kv} q_len {q_len} lens {lens} C {C}"
+    parity.check_outputs(out16.float().cpu().numpy(), out32.cpu().numpy(), ref, kv, what)
     parity.assert_lse_close(lse.cpu().numpy(), ref_lse, what)
     # query tokens before the request's first token see nothing: exactly zero, lse -inf
     for b, n in enumerate(lens):
@@ -74,8 +74,9 @@ def test_multi_vs_oracle(dsa, lens, q_len, hq, hkv, C, m):
 
 
 @pytest.mark.parametrize("q_len", [2, 3, 6])
-def test_multi_partials_each_descriptor(dsa, q_len):
-    inp = make([40, 129, 1000, 2500], q_len, 64, 8, seed=7)
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_multi_partials_each_descriptor(dsa, q_len, kv):
+    inp = make([40, 129, 1000, 2500], q_len, 64, 8, seed=7, kv=kv)
     _, _, _, tm, po, pl = run(dsa, inp, 37, 1)
     prob = problem(inp)
     h = tm.host()
@@ -85,9 +86,9 @@ def test_multi_partials_each_descriptor(dsa, q_len):
     for x, (u, t0, t1, k) in enumerate(h["descs"]):
         b, hk = divmod(int(u), 8)
         o, lse = prob.span(b, hk, 64 * int(t0), min(64 * int(t1), int(inp["seq_lens"][b])))
-        # slots of the descriptor (two for the tensor-memory kernel's softmax teams), merged by the oracle
+        # slots of the descriptor (two: softmax teams, or token halves for E4M3), merged by the oracle
         got_o, got_l = oracle.merge(po[spd * x:spd * x + spd, :R], pl[spd * x:spd * x + spd, :R])
-        parity.assert_close(got_o, o, "bf16", f"descriptor {x}", round_ref=False)
+        parity.assert_close(got_o, o, kv, f"descriptor {x}", round_ref=False)
         parity.assert_lse_close(got_l, lse, f"descriptor {x}")
 
 
@@ -108,17 +109,42 @@ def test_multi_full_size_sampled(dsa):
     parity.assert_lse_close(lse[pick].cpu().numpy(), ref_lse[pick], "mixed, q_len 6")
 
 
-def test_multi_masked_tail_garbage_is_ignored(dsa):
-    inp = make([70, 200], 4, 16, 2, seed=3)
+def test_multi_full_size_fp8_sampled(dsa):
+    """The FP8 workload's lengths (64 requests, mean 68k tokens) with 2 query tokens per
+    request, one bin per SM; the shortest, median and longest requests checked."""
+    w = workloads.WORKLOADS["fp8"]
+    rng = np.random.default_rng(w.seed)
+    lens = workloads.draw_lengths(w.name, w.batch, rng)
+    inp = workloads.make_inputs(lens, w.num_q_heads, w.num_kv_heads, "fp8", w.seed, "cuda", rng=rng, q_len=2)
+    out16, out32, lse, tm, po, pl = run(dsa, inp, sm_count(), 4)
+    order = np.argsort(lens, kind="stable")
+    picks = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])})
+    ref, ref_lse = parity.sub_problem(inp, picks).attention()
+    parity.check_outputs(out16[picks].float().cpu().numpy(), out32[picks].cpu().numpy(), ref, "fp8",
+                         "fp8, q_len 2")
+    parity.assert_lse_close(lse[picks].cpu().numpy(), ref_lse, "fp8, q_len 2")
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_multi_masked_tail_garbage_is_ignored(dsa, kv):
+    """Rows of the last page past the request's length hold NaN (bf16 NaN; E4M3 code 0x7F
+    and NaN scales): no output may see them."""
+    inp = make([70, 200], 4, 16, 2, seed=3, kv=kv)
     bt = inp["block_table"].cpu().numpy()
     for b, n in enumerate([70, 200]):
         last = bt[b, (n - 1) // 64]
-        inp["v_pages"][last, :, n % 64:] = float("nan")
-        inp["k_pages"][last, :, n % 64:] = float("nan")
+        if kv == "bf16":
+            inp["v_pages"][last, :, n % 64:] = float("nan")
+            inp["k_pages"][last, :, n % 64:] = float("nan")
+        else:
+            inp["v_pages"][last, :, n % 64:] = 0x7F
+            inp["k_pages"][last, :, n % 64:] = 0x7F
+            inp["k_scale"][last, :, n % 64:] = float("nan")
+            inp["v_scale"][last, :, n % 64:] = float("nan")
     out16, out32, lse, *_ = run(dsa, inp, 5, 1)
     assert torch.isfinite(out32).all()
     ref, _ = problem(inp).attention()
-    parity.check_outputs(out16.float().cpu().numpy(), out32.cpu().numpy(), ref, "bf16", "NaN tail")
+    parity.check_outputs(out16.float().cpu().numpy(), out32.cpu().numpy(), ref, kv, "NaN tail")
 
 
 def test_multi_one_token_is_decode(dsa):
@@ -137,9 +163,9 @@ def test_multi_rejects_unsupported(dsa):
         dsa.decode_multi(9, inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
                          inp["sm_scale"])
     assert e.value.code == dsa.ERR_UNSUPPORTED
-    f8 = workloads.make_inputs(np.array([100, 200]), 64, 8, "fp8", device="cuda", q_len=2)
+    f8 = workloads.make_inputs(np.array([100, 200]), 64, 8, "fp8", device="cuda", q_len=9)
     tm = dsa.plan(f8["seq_lens"], 8, 4)
     with pytest.raises(dsa.DSAError) as e:
-        dsa.decode_multi(2, f8["q"], f8["k_pages"], f8["v_pages"], f8["block_table"], f8["seq_lens"], tm,
+        dsa.decode_multi(9, f8["q"], f8["k_pages"], f8["v_pages"], f8["block_table"], f8["seq_lens"], tm,
                          f8["sm_scale"], q_scale=f8["q_scale"], k_scale=f8["k_scale"], v_scale=f8["v_scale"])
     assert e.value.code == dsa.ERR_UNSUPPORTED
