@@ -1342,7 +1342,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
 #pragma unroll
                 for (int mb = 0; mb < 8; ++mb) o[nb][mb][0] = o[nb][mb][1] = o[nb][mb][2] = o[nb][mb][3] = 0.f;
             }
-            float vsc = 0.f;  // O holds the true output divided by vsc (set by the first scaled tile)
+            float vsc = 0.f, vinv = 0.f;  // O holds the true output divided by vsc; vinv = 1 / vsc
 
             bool aborted = false;
             for (int li = 0; li < n; ++li) {
@@ -1404,53 +1404,67 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                                 if (tb >= lim[nb][1]) sc[kt][nb][3] = -INFINITY;
                             }
                         }
-                    // ---- the V scale folded into P, relative to the warp's largest scale in
-                    //      the tile (O is rescaled when that reference changes)
-                    float vm = fmaxf(fmaxf(vs_[0][0], vs_[0][1]), fmaxf(vs_[1][0], vs_[1][1]));
+                    // ---- lazy references, so that rescaling O is rare: the V scale reference vsc is
+                    //      the largest V scale seen (P carries vs / vsc <= 1), and a row's reference
+                    //      m moves only when the row's maximum passes it by more than 8 (P <= 2^8,
+                    //      well inside f16); the warp reduces maxima only when some lane sees growth
+                    float lmx[NBW][2];
+                    bool grow = fmaxf(fmaxf(vs_[0][0], vs_[0][1]), fmaxf(vs_[1][0], vs_[1][1])) > vsc;
 #pragma unroll
-                    for (int o_ = 4; o_ < 32; o_ <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o_));
-                    float vf = 1.f;  // old reference / new reference
-                    if (vm > 0.f) {
-                        if (vsc > 0.f) vf = vsc / vm;
-                        vsc = vm;
+                    for (int nb = 0; nb < NBW; ++nb) {
+                        lmx[nb][0] = fmaxf(fmaxf(sc[0][nb][0], sc[0][nb][2]), fmaxf(sc[1][nb][0], sc[1][nb][2]));
+                        lmx[nb][1] = fmaxf(fmaxf(sc[0][nb][1], sc[0][nb][3]), fmaxf(sc[1][nb][1], sc[1][nb][3]));
+                        grow |= lmx[nb][0] > m[nb][0] + 8.f || lmx[nb][1] > m[nb][1] + 8.f;
                     }
-                    const float vinv = vsc > 0.f ? 1.f / vsc : 0.f;
-                    // ---- online softmax (base 2) per row over the warp's 32 tokens
+                    if (__any_sync(0xffffffffu, grow)) {
+                        float vm = fmaxf(fmaxf(vs_[0][0], vs_[0][1]), fmaxf(vs_[1][0], vs_[1][1]));
+#pragma unroll
+                        for (int o_ = 4; o_ < 32; o_ <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o_));
+                        float vf = 1.f;  // old reference / new reference
+                        if (vm > vsc) {
+                            if (vsc > 0.f) vf = vsc / vm;
+                            vsc = vm;
+                            vinv = 1.f / vm;
+                        }
+#pragma unroll
+                        for (int nb = 0; nb < NBW; ++nb) {
+                            float f[2];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                float mx = lmx[nb][e];
+#pragma unroll
+                                for (int o_ = 4; o_ < 32; o_ <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o_));
+                                float alpha = 1.f;
+                                if (mx > m[nb][e] + 8.f) {  // from m = -inf: alpha = 0 (nothing accumulated yet)
+                                    alpha = ex2(m[nb][e] - mx);
+                                    m[nb][e] = mx;
+                                }
+                                l[nb][e] *= alpha;
+                                f[e] = alpha * vf;
+                            }
+#pragma unroll
+                            for (int mb = 0; mb < 8; ++mb) {
+                                o[nb][mb][0] *= f[0];
+                                o[nb][mb][1] *= f[1];
+                                o[nb][mb][2] *= f[0];
+                                o[nb][mb][3] *= f[1];
+                            }
+                        }
+                    }
+                    // ---- P = 2^(s - m) (a row still at m = -inf has seen no visible token: P = 0)
                     uint32_t bh[2][NBW][2];
 #pragma unroll
                     for (int nb = 0; nb < NBW; ++nb) {
-                        float mx0 = fmaxf(fmaxf(sc[0][nb][0], sc[0][nb][2]), fmaxf(sc[1][nb][0], sc[1][nb][2]));
-                        float mx1 = fmaxf(fmaxf(sc[0][nb][1], sc[0][nb][3]), fmaxf(sc[1][nb][1], sc[1][nb][3]));
-#pragma unroll
-                        for (int o_ = 4; o_ < 32; o_ <<= 1) {
-                            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
-                            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
-                        }
-                        const float mn0 = fmaxf(m[nb][0], mx0), mn1 = fmaxf(m[nb][1], mx1);
-                        const float r0 = mn0 == -INFINITY ? 0.f : mn0, r1 = mn1 == -INFINITY ? 0.f : mn1;
-                        const float al0 = ex2(m[nb][0] - r0), al1 = ex2(m[nb][1] - r1);
-                        float ls0 = 0.f, ls1 = 0.f;
+                        const float r0 = m[nb][0] == -INFINITY ? 0.f : m[nb][0], r1 = m[nb][1] == -INFINITY ? 0.f : m[nb][1];
 #pragma unroll
                         for (int kt = 0; kt < 2; ++kt) {
                             const float p0 = ex2(sc[kt][nb][0] - r0), p1 = ex2(sc[kt][nb][1] - r1);
                             const float p2 = ex2(sc[kt][nb][2] - r0), p3 = ex2(sc[kt][nb][3] - r1);
-                            ls0 += p0 + p2;
-                            ls1 += p1 + p3;
+                            l[nb][0] += p0 + p2;
+                            l[nb][1] += p1 + p3;
                             const float wa = vs_[kt][0] * vinv, wb = vs_[kt][1] * vinv;
                             bh[kt][nb][0] = movmatrix_trans(pack_f16x2(p0 * wa, p1 * wa));
                             bh[kt][nb][1] = movmatrix_trans(pack_f16x2(p2 * wb, p3 * wb));
-                        }
-                        l[nb][0] = l[nb][0] * al0 + ls0;
-                        l[nb][1] = l[nb][1] * al1 + ls1;
-                        m[nb][0] = mn0;
-                        m[nb][1] = mn1;
-                        const float f0 = al0 * vf, f1 = al1 * vf;
-#pragma unroll
-                        for (int mb = 0; mb < 8; ++mb) {
-                            o[nb][mb][0] *= f0;
-                            o[nb][mb][1] *= f1;
-                            o[nb][mb][2] *= f0;
-                            o[nb][mb][3] *= f1;
                         }
                     }
                     // ---- O^T += V^T . P^T; V rows past the tile's valid tokens are zeroed
@@ -1469,18 +1483,22 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                             uint32_t a0, a1, a2, a3;
                             cvt_pair(x0, a0, a1);
                             cvt_pair(x1, a2, a3);
-                            a0 &= mlo;
-                            a1 &= mlo;
-                            a2 &= mhi;
-                            a3 &= mhi;
+                            if (partial) {
+                                a0 &= mlo;
+                                a1 &= mlo;
+                                a2 &= mhi;
+                                a3 &= mhi;
+                            }
 #pragma unroll
                             for (int nb = 0; nb < NBW; ++nb) mma_f16(o[nb][2 * mp], a0, a1, a2, a3, bh[kt][nb][0], bh[kt][nb][1]);
                             cvt_pair(x2, a0, a1);
                             cvt_pair(x3, a2, a3);
-                            a0 &= mlo;
-                            a1 &= mlo;
-                            a2 &= mhi;
-                            a3 &= mhi;
+                            if (partial) {
+                                a0 &= mlo;
+                                a1 &= mlo;
+                                a2 &= mhi;
+                                a3 &= mhi;
+                            }
 #pragma unroll
                             for (int nb = 0; nb < NBW; ++nb)
                                 mma_f16(o[nb][2 * mp + 1], a0, a1, a2, a3, bh[kt][nb][0], bh[kt][nb][1]);
@@ -1581,7 +1599,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
 #pragma unroll
                 for (int mb = 0; mb < 8; ++mb) o[nb][mb][0] = o[nb][mb][1] = o[nb][mb][2] = o[nb][mb][3] = 0.f;
             }
-            float vsc = 0.f;  // O holds the true output divided by vsc (set by the first scaled tile)
+            float vsc = 0.f, vinv = 0.f;  // O holds the true output divided by vsc; vinv = 1 / vsc
 
             bool aborted = false;
             for (int li = ((grp - c_start) % GROUPS + GROUPS) % GROUPS; li < n; li += GROUPS) {
@@ -1629,47 +1647,61 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                             if (T0 + gid + 8 >= lim[nb][1]) sc[nb][3] = -INFINITY;
                         }
                     }
-                    // ---- the V scale folded into P, relative to the warp's largest scale in
-                    //      the tile (O is rescaled when that reference changes)
-                    float vm = fmaxf(vsa, vsb);
+                    // ---- lazy references, so that rescaling O is rare: the V scale reference vsc is
+                    //      the largest V scale seen (P carries vs / vsc <= 1), and a row's reference
+                    //      m moves only when the row's maximum passes it by more than 8 (P <= 2^8,
+                    //      well inside f16); the warp reduces maxima only when some lane sees growth
+                    bool grow = fmaxf(vsa, vsb) > vsc;
 #pragma unroll
-                    for (int o_ = 4; o_ < 32; o_ <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o_));
-                    float vf = 1.f;
-                    if (vm > 0.f) {
-                        if (vsc > 0.f) vf = vsc / vm;
-                        vsc = vm;
+                    for (int nb = 0; nb < NBW; ++nb)
+                        grow |= fmaxf(sc[nb][0], sc[nb][2]) > m[nb][0] + 8.f || fmaxf(sc[nb][1], sc[nb][3]) > m[nb][1] + 8.f;
+                    if (__any_sync(0xffffffffu, grow)) {
+                        float vm = fmaxf(vsa, vsb);
+#pragma unroll
+                        for (int o_ = 4; o_ < 32; o_ <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o_));
+                        float vf = 1.f;
+                        if (vm > vsc) {
+                            if (vsc > 0.f) vf = vsc / vm;
+                            vsc = vm;
+                            vinv = 1.f / vm;
+                        }
+#pragma unroll
+                        for (int nb = 0; nb < NBW; ++nb) {
+                            float mx[2] = {fmaxf(sc[nb][0], sc[nb][2]), fmaxf(sc[nb][1], sc[nb][3])};
+                            float f[2];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+#pragma unroll
+                                for (int o_ = 4; o_ < 32; o_ <<= 1) mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], o_));
+                                float alpha = 1.f;
+                                if (mx[e] > m[nb][e] + 8.f) {  // from m = -inf: alpha = 0 (nothing accumulated yet)
+                                    alpha = ex2(m[nb][e] - mx[e]);
+                                    m[nb][e] = mx[e];
+                                }
+                                l[nb][e] *= alpha;
+                                f[e] = alpha * vf;
+                            }
+#pragma unroll
+                            for (int mb = 0; mb < 8; ++mb) {
+                                o[nb][mb][0] *= f[0];
+                                o[nb][mb][1] *= f[1];
+                                o[nb][mb][2] *= f[0];
+                                o[nb][mb][3] *= f[1];
+                            }
+                        }
                     }
-                    const float vinv = vsc > 0.f ? 1.f / vsc : 0.f;
+                    // ---- P = 2^(s - m) (a row still at m = -inf has seen no visible token: P = 0)
                     const float wa = vsa * vinv, wb = vsb * vinv;
-                    // ---- online softmax (base 2) per row over the warp's 16 tokens
                     uint32_t bh[NBW][2];
 #pragma unroll
                     for (int nb = 0; nb < NBW; ++nb) {
-                        float mx0 = fmaxf(sc[nb][0], sc[nb][2]), mx1 = fmaxf(sc[nb][1], sc[nb][3]);
-#pragma unroll
-                        for (int o_ = 4; o_ < 32; o_ <<= 1) {
-                            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
-                            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
-                        }
-                        const float mn0 = fmaxf(m[nb][0], mx0), mn1 = fmaxf(m[nb][1], mx1);
-                        const float r0 = mn0 == -INFINITY ? 0.f : mn0, r1 = mn1 == -INFINITY ? 0.f : mn1;
-                        const float al0 = ex2(m[nb][0] - r0), al1 = ex2(m[nb][1] - r1);
+                        const float r0 = m[nb][0] == -INFINITY ? 0.f : m[nb][0], r1 = m[nb][1] == -INFINITY ? 0.f : m[nb][1];
                         const float p0 = ex2(sc[nb][0] - r0), p1 = ex2(sc[nb][1] - r1);
                         const float p2 = ex2(sc[nb][2] - r0), p3 = ex2(sc[nb][3] - r1);
-                        l[nb][0] = l[nb][0] * al0 + p0 + p2;
-                        l[nb][1] = l[nb][1] * al1 + p1 + p3;
-                        m[nb][0] = mn0;
-                        m[nb][1] = mn1;
+                        l[nb][0] += p0 + p2;
+                        l[nb][1] += p1 + p3;
                         bh[nb][0] = movmatrix_trans(pack_f16x2(p0 * wa, p1 * wa));
                         bh[nb][1] = movmatrix_trans(pack_f16x2(p2 * wb, p3 * wb));
-                        const float f0 = al0 * vf, f1 = al1 * vf;
-#pragma unroll
-                        for (int mb = 0; mb < 8; ++mb) {
-                            o[nb][mb][0] *= f0;
-                            o[nb][mb][1] *= f1;
-                            o[nb][mb][2] *= f0;
-                            o[nb][mb][3] *= f1;
-                        }
                     }
                     // ---- O^T += V^T . P^T (V widened to f16); V rows past the valid tokens are zeroed
                     const bool partial = nv < tok_base + 16;
@@ -1685,18 +1717,22 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         uint32_t a0, a1, a2, a3;
                         cvt_pair(x0, a0, a1);
                         cvt_pair(x1, a2, a3);
-                        a0 &= mlo;
-                        a1 &= mlo;
-                        a2 &= mhi;
-                        a3 &= mhi;
+                        if (partial) {
+                            a0 &= mlo;
+                            a1 &= mlo;
+                            a2 &= mhi;
+                            a3 &= mhi;
+                        }
 #pragma unroll
                         for (int nb = 0; nb < NBW; ++nb) mma_f16(o[nb][2 * mp], a0, a1, a2, a3, bh[nb][0], bh[nb][1]);
                         cvt_pair(x2, a0, a1);
                         cvt_pair(x3, a2, a3);
-                        a0 &= mlo;
-                        a1 &= mlo;
-                        a2 &= mhi;
-                        a3 &= mhi;
+                        if (partial) {
+                            a0 &= mlo;
+                            a1 &= mlo;
+                            a2 &= mhi;
+                            a3 &= mhi;
+                        }
 #pragma unroll
                         for (int nb = 0; nb < NBW; ++nb) mma_f16(o[nb][2 * mp + 1], a0, a1, a2, a3, bh[nb][0], bh[nb][1]);
                     }
