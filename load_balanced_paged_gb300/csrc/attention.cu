@@ -1906,7 +1906,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
 
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
         // E4M3: O holds the true output divided by vsc (set by the first scaled tile); bf16: 1
-        float vsc = (KV == 1) ? 0.f : 1.f;
+        float vsc = (KV == 1) ? 0.f : 1.f, vinv = 0.f;  // vinv = 1 / vsc (E4M3)
         float o[8][4];
 #pragma unroll
         for (int mb = 0; mb < 8; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
@@ -1968,24 +1968,72 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                     if (ta >= nv) s[0] = s[1] = -INFINITY;
                     if (tb >= nv) s[2] = s[3] = -INFINITY;
                 }
-                // ---- online softmax (base 2), per head, over this warp's tokens
-                float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
-#pragma unroll
-                for (int o_ = 4; o_ < 32; o_ <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
-                }
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float r0 = mn0 == -INFINITY ? 0.f : mn0, r1 = mn1 == -INFINITY ? 0.f : mn1;
-                float al0 = ex2(m0 - r0), al1 = ex2(m1 - r1);
-                const float p0 = ex2(s[0] - r0), p1 = ex2(s[1] - r1), p2 = ex2(s[2] - r0), p3 = ex2(s[3] - r1);
-                l0 = l0 * al0 + p0 + p2;
-                l1 = l1 * al1 + p1 + p3;
-                m0 = mn0;
-                m1 = mn1;
-
                 uint32_t b0h, b1h, b0l = 0, b1l = 0;
-                if (KV == 0) {
+                if constexpr (KV == 1) {
+                    // ---- lazy references, so that rescaling O is rare: the V scale reference vsc
+                    //      is the largest V scale seen (P carries vs / vsc <= 1), and a head's
+                    //      reference m moves only when its maximum passes it by more than 8 (P <=
+                    //      2^8, well inside f16); the warp reduces maxima only when a lane sees growth
+                    const bool grow = fmaxf(vsa, vsb) > vsc || fmaxf(s[0], s[2]) > m0 + 8.f || fmaxf(s[1], s[3]) > m1 + 8.f;
+                    if (__any_sync(0xffffffffu, grow)) {
+                        float vm = fmaxf(vsa, vsb), mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+                        for (int o_ = 4; o_ < 32; o_ <<= 1) {
+                            vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o_));
+                            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
+                            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
+                        }
+                        float vf = 1.f;
+                        if (vm > vsc) {
+                            if (vsc > 0.f) vf = vsc / vm;
+                            vsc = vm;
+                            vinv = 1.f / vm;
+                        }
+                        float al0 = 1.f, al1 = 1.f;  // from m = -inf: 0 (nothing accumulated yet)
+                        if (mx0 > m0 + 8.f) {
+                            al0 = ex2(m0 - mx0);
+                            m0 = mx0;
+                        }
+                        if (mx1 > m1 + 8.f) {
+                            al1 = ex2(m1 - mx1);
+                            m1 = mx1;
+                        }
+                        l0 *= al0;
+                        l1 *= al1;
+                        al0 *= vf;
+                        al1 *= vf;
+#pragma unroll
+                        for (int mb = 0; mb < 8; ++mb) {
+                            o[mb][0] *= al0;
+                            o[mb][1] *= al1;
+                            o[mb][2] *= al0;
+                            o[mb][3] *= al1;
+                        }
+                    }
+                    // P = 2^(s - m) (a head still at m = -inf has seen no valid token: P = 0)
+                    const float r0 = m0 == -INFINITY ? 0.f : m0, r1 = m1 == -INFINITY ? 0.f : m1;
+                    const float p0 = ex2(s[0] - r0), p1 = ex2(s[1] - r1), p2 = ex2(s[2] - r0), p3 = ex2(s[3] - r1);
+                    l0 += p0 + p2;
+                    l1 += p1 + p3;
+                    const float wa = vsa * vinv, wb = vsb * vinv;
+                    b0h = movmatrix_trans(pack_f16x2(p0 * wa, p1 * wa));
+                    b1h = movmatrix_trans(pack_f16x2(p2 * wb, p3 * wb));
+                } else {
+                    // ---- online softmax (base 2), per head, over this warp's tokens
+                    float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+                    for (int o_ = 4; o_ < 32; o_ <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
+                    }
+                    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                    const float r0 = mn0 == -INFINITY ? 0.f : mn0, r1 = mn1 == -INFINITY ? 0.f : mn1;
+                    const float al0 = ex2(m0 - r0), al1 = ex2(m1 - r1);
+                    const float p0 = ex2(s[0] - r0), p1 = ex2(s[1] - r1), p2 = ex2(s[2] - r0), p3 = ex2(s[3] - r1);
+                    l0 = l0 * al0 + p0 + p2;
+                    l1 = l1 * al1 + p1 + p3;
+                    m0 = mn0;
+                    m1 = mn1;
                     const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
                     const uint32_t l01 = pack_bf16x2(p0 - bf16lo_to_f32(h01), p1 - bf16hi_to_f32(h01));
                     const uint32_t l23 = pack_bf16x2(p2 - bf16lo_to_f32(h23), p3 - bf16hi_to_f32(h23));
@@ -1993,31 +2041,13 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                     b1h = movmatrix_trans(h23);
                     b0l = movmatrix_trans(l01);
                     b1l = movmatrix_trans(l23);
-                } else {
-                    // fold the per-token V scale into P, relative to this warp's largest scale in
-                    // the tile (O holds the output divided by vsc)
-                    float vm = fmaxf(vsa, vsb);
 #pragma unroll
-                    for (int o_ = 4; o_ < 32; o_ <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o_));
-                    if (vm > 0.f) {
-                        if (vsc > 0.f) {
-                            const float f = vsc / vm;
-                            al0 *= f;
-                            al1 *= f;
-                        }
-                        vsc = vm;
+                    for (int mb = 0; mb < 8; ++mb) {
+                        o[mb][0] *= al0;
+                        o[mb][1] *= al1;
+                        o[mb][2] *= al0;
+                        o[mb][3] *= al1;
                     }
-                    const float inv = vsc > 0.f ? 1.f / vsc : 0.f;
-                    const float wa = vsa * inv, wb = vsb * inv;
-                    b0h = movmatrix_trans(pack_f16x2(p0 * wa, p1 * wa));
-                    b1h = movmatrix_trans(pack_f16x2(p2 * wb, p3 * wb));
-                }
-#pragma unroll
-                for (int mb = 0; mb < 8; ++mb) {
-                    o[mb][0] *= al0;
-                    o[mb][1] *= al1;
-                    o[mb][2] *= al0;
-                    o[mb][3] *= al1;
                 }
                 // masks for the A (V^T) fragments: tokens (2tig, 2tig+1) and (8+2tig, 9+2tig)
                 const uint32_t mlo = partial ? tok_mask(tok_base + 2 * tig, nv) : 0xFFFFFFFFu;
