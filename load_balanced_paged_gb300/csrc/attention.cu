@@ -125,7 +125,10 @@ struct Layout {
     static constexpr int kThreads = (kNcw + (kTc ? 3 : 1)) * 32;  // consumers + producer (+ MMA, Q warps)
     static constexpr int kThreadsFused = (kNcw + 2) * 32;  // + epilogue warp (fused combine)
     static constexpr int kStageTx = 2 * Cfg<KV>::kTileBytes + 2 * Cfg<KV>::kScaleBytes;
-    static constexpr int kStageBytes = round_up(kStageTx, 1024);
+    // QW = 3 with E4M3: each stage also holds its V widened to f16 ([half][64 rows][128 B],
+    // 128-byte swizzle: the P.V operand layout of a bf16 V tile)
+    static constexpr int kVcOff = round_up(kStageTx, 1024);
+    static constexpr int kStageBytes = kVcOff + (kTc && KV == 1 ? kTile * kHeadDim * 2 : 0);
     static constexpr int kQRows = QW == 0 ? kMaxGroup : (QW == 4 ? 16 : kMaxRows);
     static constexpr int kQSlot = kQRows * Cfg<KV>::kQHeadBytes;
     static constexpr int kQOff = STAGES * kStageBytes;
@@ -135,7 +138,7 @@ struct Layout {
     // QW = 3: Q as the MMA's A operand (64 rows x 128, K-major with the 128-byte swizzle, two
     // 64-column halves of 8 KB, as the TMA lays out a K tile), two buffers.
     static constexpr int kQcOff = kQOff + kQSlots * kQSlot;
-    static constexpr int kQcBytes = kTc ? 2 * kMaxRows * kHeadDim * 2 : 0;
+    static constexpr int kQcBytes = kTc ? 2 * kMaxRows * Cfg<KV>::kQHeadBytes : 0;
     static constexpr int kMergeOff = kQcOff + kQcBytes;
     static constexpr bool kMerge = QW == 0 || QW == 4;  // warps merge their states in shared memory
     static constexpr int kMergeSlot = kMerge ? kNcw * kWarpFloats : 0;  // floats per merge slot
@@ -152,7 +155,7 @@ struct Layout {
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static_assert(MSLOTS == 1 || MSLOTS == 2, "merge slots");
     static_assert(QW == 0 || (MSLOTS == 1 && GROUPS == 2), "multi-token shapes");
-    static_assert(!kTc || (KV == 0 && kQcOff % 1024 == 0), "tensor-core operand buffers");
+    static_assert(!kTc || kQcOff % 1024 == 0, "tensor-core operand buffers");
     // Each stage must be consumed by one group only: a group then meets the phases of its
     // stages' full barriers in order.  With stages shared by two groups, one group could wait
     // for phase k+1 while phase k is still pending, pass the parity test early and arrive on
@@ -694,7 +697,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                                 for (int k = 0; k < kMaxPagesPerTile; ++k) {
                                     if (k >= nsub) break;
                                     const int pg = cpg[k];
-                                    if (QW == 3 && P < kTile) {
+                                    if (QW == 3 && KV == 0 && P < kTile) {
                                         const uint32_t ro = static_cast<uint32_t>(k * P) * 128u;
                                         tma_load_5d(kdst + ro, &kmap, fb, 0, 0, 0, h_l, pg, policy);
                                         tma_load_5d(kdst + C::kTileBytes / 2 + ro, &kmap, fb, 0, 0, 1, h_l, pg, policy);
@@ -832,14 +835,16 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
         const int R = p.q_len * G;
         uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kAbortOff + 4);
         constexpr int kTcThreads = (NCW + 2) * 32;  // softmax warps, S warp, PV warp
-        constexpr uint32_t kQcBuf = kMaxRows * kHeadDim * 2;
+        constexpr uint32_t kQcBuf = kMaxRows * C::kQHeadBytes;
         if (warp == NCW + 1) tmem_alloc(smem_u32(tmem_slot), 512);
         tc_fence_before();
         named_bar_sync(1, kTcThreads);
         tc_fence_after();
         const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
-        constexpr uint32_t kIdS = umma_idesc_bf16(64, 64, 0, 0);   // Q K-major, K K-major
-        constexpr uint32_t kIdO = umma_idesc_bf16(64, 128, 0, 1);  // P K-major, V M/N-major
+        // Q K-major, K K-major (bf16, or E4M3 with kind::f8f6f4); P K-major, V M/N-major
+        // (bf16, or f16 for E4M3 K/V: V widened exactly, P carrying the V scale)
+        constexpr uint32_t kIdS = KV == 0 ? umma_idesc_bf16(64, 64, 0, 0) : umma_idesc_fmt0(64, 64, 0, 0);
+        constexpr uint32_t kIdO = KV == 0 ? umma_idesc_bf16(64, 128, 0, 1) : umma_idesc_fmt0(64, 128, 0, 1);
         bool failed = false;
 
         if (warp == NCW + 1) {
@@ -912,11 +917,12 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         failed = true;
                         break;
                     }
+                    const uint8_t *src = smem + L::kQOff + qb * L::kQSlot;
+                    uint8_t *dst = smem + L::kQcOff + (d & 1) * kQcBuf;
+                    if constexpr (KV == 0) {
                     // 128-byte-swizzled K-major operand (as the TMA lays out K): dims 64 b .. 64 b + 63
                     // of row r at b * 8 KB + r * 128 B, 16-byte chunk c at (c ^ (r % 8)) * 16.  Each
                     // quarter-warp writes one 128-byte row: no bank conflicts either way.
-                    const uint8_t *src = smem + L::kQOff + qb * L::kQSlot;
-                    uint8_t *dst = smem + L::kQcOff + (d & 1) * kQcBuf;
 #pragma unroll
                     for (int rd = 0; rd < 4; ++rd) {
                         uint4 v[8];
@@ -931,6 +937,24 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                             const int i = lane + 32 * (8 * rd + it), r = i >> 4, kc = i & 15;
                             *reinterpret_cast<uint4 *>(dst + (kc >> 3) * 8192 + r * 128 + (((kc & 7) ^ (r & 7)) << 4)) = v[it];
                         }
+                    }
+                    } else {
+                    // E4M3: a row is one 128-byte swizzle row (r * 128 B, chunk c at (c ^ (r % 8)) * 16)
+#pragma unroll
+                    for (int rd = 0; rd < 2; ++rd) {
+                        uint4 v[8];
+#pragma unroll
+                        for (int it = 0; it < 8; ++it) {  // chunk kc of row r
+                            const int i = lane + 32 * (8 * rd + it), r = i >> 3, kc = i & 7;
+                            v[it] = r < R ? *reinterpret_cast<const uint4 *>(src + r * kHeadDim + kc * 16)
+                                          : make_uint4(0u, 0u, 0u, 0u);
+                        }
+#pragma unroll
+                        for (int it = 0; it < 8; ++it) {
+                            const int i = lane + 32 * (8 * rd + it), r = i >> 3, kc = i & 7;
+                            *reinterpret_cast<uint4 *>(dst + r * 128 + ((kc ^ (r & 7)) << 4)) = v[it];
+                        }
+                    }
                     }
                     fence_proxy_async_smem();
                     // the next descriptor's Q lands while this one's tiles are worked on
@@ -956,11 +980,18 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         if (nv > 0) {
                             tc_fence_after();
                             const uint32_t kb = sbase + stage * L::kStageBytes;
+                            if constexpr (KV == 0) {
 #pragma unroll
-                            for (int ks = 0; ks < 8; ++ks)
-                                umma_bf16(tmem + 64 * buf, umma_desc(qa + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, 2),
-                                          umma_desc(kb + (ks >> 2) * (C::kTileBytes / 2) + (ks & 3) * 32, 16, 1024, 2),
-                                          kIdS, ks > 0);
+                                for (int ks = 0; ks < 8; ++ks)
+                                    umma_bf16(tmem + 64 * buf, umma_desc(qa + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, 2),
+                                              umma_desc(kb + (ks >> 2) * (C::kTileBytes / 2) + (ks & 3) * 32, 16, 1024, 2),
+                                              kIdS, ks > 0);
+                            } else {  // E4M3: 32 dims (32 bytes) per product
+#pragma unroll
+                                for (int ks = 0; ks < 4; ++ks)
+                                    umma_e4m3(tmem + 64 * buf, umma_desc(qa + ks * 32, 16, 1024, 2),
+                                              umma_desc(kb + ks * 32, 16, 1024, 2), kIdS, ks > 0);
+                            }
                             umma_commit(s_full(buf));
                             umma_commit(empty_bar(stage));
                         } else {
@@ -1014,14 +1045,16 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         }
                         if (lane == 0) {
                             tc_fence_after();
-                            const uint32_t vb = sbase + stage * L::kStageBytes + C::kTileBytes;
-                            const uint32_t pt = tmem + 64 * buf;  // P high part: columns 0-31, low part: 32-63
+                            // bf16: V as loaded, P high part in columns 0-31, low part in 32-63;
+                            // E4M3: V widened to f16 by the softmax team, P (f16) in columns 0-31
+                            const uint32_t vb = sbase + stage * L::kStageBytes + (KV == 0 ? C::kTileBytes : L::kVcOff);
+                            const uint32_t pt = tmem + 64 * buf;
                             const uint32_t od = tmem + 256 + 128 * t;
 #pragma unroll
                             for (int ks = 0; ks < 4; ++ks) {
                                 const uint64_t bd = umma_desc(vb + ks * 2048, 8192, 1024, 2);
                                 umma_bf16_ta(od, pt + 8 * ks, bd, kIdO, !(first_pv[t] && ks == 0));
-                                umma_bf16_ta(od, pt + 32 + 8 * ks, bd, kIdO, true);
+                                if (KV == 0) umma_bf16_ta(od, pt + 32 + 8 * ks, bd, kIdO, true);
                             }
                         }
                         first_pv[t] = false;
@@ -1055,6 +1088,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
             // until the team has handed over the P of its first tile of the next descriptor: a
             // descriptor's first tile never rescales O, so it need not wait for the previous
             // descriptor's last P.V, and the team computes it while that P.V completes.
+            float ep_vref = 1.f;  // E4M3: the V scale reference of the deferred descriptor end
             auto team_epilogue = [&](int slot, float (&m)[2], float (&l)[2], int pv_desc, int last_g) -> bool {
                 // ---- this team's products of the descriptor are done once its last tile's buffer
                 //      phase is (that commit covers every earlier product)
@@ -1068,7 +1102,10 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 for (int h = 0; h < 2; ++h) {
                     l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
                     l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
-                    inv[h] = l[h] > 0.f ? 1.f / l[h] : 0.f;
+                    if constexpr (KV == 0)
+                        inv[h] = l[h] > 0.f ? 1.f / l[h] : 0.f;
+                    else
+                        inv[h] = l[h] > 0.f ? ep_vref / l[h] : 0.f;
                     lse[h] = l[h] > 0.f ? (m[h] + lg2(l[h])) * kLn2 : -INFINITY;
                 }
                 const int64_t slot_row = (2 * static_cast<int64_t>(slot) + team) * R;
@@ -1116,6 +1153,8 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
                 const int end = inf->end, n = inf->n, slot = inf->slot, c_start = inf->c_start;
                 const int dt0 = inf->t0, len = inf->len;
+                int d_b = 0, d_h = 0;
+                if constexpr (KV == 1) d_b = inf->b, d_h = inf->h;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qempty_bar(qslot));
                 if (end) {
@@ -1125,6 +1164,19 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 // visible tokens of each row: t < lim (-1: a row past R)
                 const int lim[2] = {ra < R ? len - p.q_len + ra / G + 1 : -1, rb < R ? len - p.q_len + rb / G + 1 : -1};
                 float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+                // E4M3: score factor per row (softmax scale x the row's q_scale), the V scale
+                // reference (the largest V scale seen, O holds the output divided by it) and its inverse
+                float qsc[2] = {p.score_scale, p.score_scale}, vref = 1.f, vinv = 1.f;
+                if constexpr (KV == 1) {
+                    const int rr[2] = {ra, rb};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        if (rr[h] < R) {
+                            const int i = rr[h] / G;
+                            qsc[h] *= p.q_scale[(static_cast<int64_t>(d_b) * p.q_len + i) * p.hq + d_h * G + rr[h] - i * G];
+                        }
+                    vref = vinv = 0.f;
+                }
                 int pv_desc = 0, last_g = -1;
                 for (int li = 0; li < n; ++li, ++g) {
                     if ((g & 1) != team) continue;
@@ -1159,6 +1211,43 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         }
                         continue;
                     }
+                    // ---- E4M3: S times the K scale of its column; P's factor per column, the V
+                    //      scale over the reference, which moves only when a larger scale appears
+                    //      (O is then rescaled with the maxima below); columns past nv get 0
+                    float vw[8][2];
+                    float vf = 1.f;
+                    if constexpr (KV == 1) {
+                        const float *ksm = reinterpret_cast<const float *>(smem + stage * L::kStageBytes + 2 * C::kTileBytes);
+                        const float *vsm = ksm + kTile;
+                        float vmax = 0.f;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int j = 8 * k + 2 * tig;
+                            const float2 kk = *reinterpret_cast<const float2 *>(ksm + j);
+                            const float2 vv = *reinterpret_cast<const float2 *>(vsm + j);
+                            sv[k][0] *= kk.x;
+                            sv[k][1] *= kk.y;
+                            sv[k][2] *= kk.x;
+                            sv[k][3] *= kk.y;
+                            vw[k][0] = j < nv ? vv.x : 0.f;
+                            vw[k][1] = j + 1 < nv ? vv.y : 0.f;
+                            vmax = fmaxf(vmax, fmaxf(vw[k][0], vw[k][1]));
+                        }
+                        if (__any_sync(0xffffffffu, vmax > vref)) {  // the quad's four lanes cover the 64 columns
+                            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
+                            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+                            if (vmax > vref) {
+                                if (vref > 0.f) vf = vref / vmax;  // from 0: nothing accumulated yet
+                                vref = vmax;
+                                vinv = 1.f / vmax;
+                            }
+                        }
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            vw[k][0] *= vinv;
+                            vw[k][1] *= vinv;
+                        }
+                    }
                     // ---- running maximum over each row's visible tokens (t < lim, slot < nv)
                     const int tt = (dt0 + li) * kTile;
                     const int vis[2] = {max(0, min(nv, lim[0] - tt)), max(0, min(nv, lim[1] - tt))};
@@ -1177,13 +1266,14 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                     for (int h = 0; h < 2; ++h) {
                         mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
                         mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-                        const float mnew = fmaxf(m[h], mx[h] * p.score_scale);
+                        const float mnew = fmaxf(m[h], mx[h] * (KV == 0 ? p.score_scale : qsc[h]));
                         grow[h] = m[h] != -INFINITY && mnew > m[h] + 8.f;
                         alpha[h] = grow[h] ? ex2(m[h] - mnew) : 1.f;
                         if (grow[h] || m[h] == -INFINITY) m[h] = mnew;
                     }
-                    if (__any_sync(0xffffffffu, grow[0] || grow[1])) {
-                        // rows whose maximum grew: O_team *= 2^(m_old - m_new) (its last P.V is done)
+                    if (__any_sync(0xffffffffu, grow[0] || grow[1] || (KV == 1 && vf != 1.f))) {
+                        // rows whose maximum grew: O_team *= 2^(m_old - m_new) (its last P.V is done);
+                        // E4M3: all rows also by the V scale reference's change
                         tc_fence_after();
 #pragma unroll 1  // rare: kept small for the instruction cache
                         for (int half = 0; half < 2; ++half) {
@@ -1193,10 +1283,17 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                             tmem_wait_ld();
 #pragma unroll
                             for (int k = 0; k < 8; ++k) {
-                                o[k][0] *= alpha[0];
-                                o[k][1] *= alpha[0];
-                                o[k][2] *= alpha[1];
-                                o[k][3] *= alpha[1];
+                                if constexpr (KV == 0) {
+                                    o[k][0] *= alpha[0];
+                                    o[k][1] *= alpha[0];
+                                    o[k][2] *= alpha[1];
+                                    o[k][3] *= alpha[1];
+                                } else {
+                                    o[k][0] *= alpha[0] * vf;
+                                    o[k][1] *= alpha[0] * vf;
+                                    o[k][2] *= alpha[1] * vf;
+                                    o[k][3] *= alpha[1] * vf;
+                                }
                                 tmem_st16x8(tmem + lane_base + o_col + 64 * half + 8 * k, o[k]);
                             }
                             tmem_wait_st();
@@ -1215,26 +1312,60 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int h = e >> 1, j = 8 * k + 2 * tig + (e & 1);
-                            const float q = ex2(fmaf(sv[k][e], p.score_scale, h ? nm1 : nm0));
+                            const float q = ex2(fmaf(sv[k][e], KV == 0 ? p.score_scale : qsc[h], h ? nm1 : nm0));
                             pv[e] = (full || j < vis[h]) ? q : 0.f;
                         }
                         l[0] += pv[0] + pv[1];
                         l[1] += pv[2] + pv[3];
-                        const uint32_t h0 = __float_as_uint(pv[0]) & 0xFFFF0000u, h1 = __float_as_uint(pv[1]) & 0xFFFF0000u;
-                        const uint32_t h2 = __float_as_uint(pv[2]) & 0xFFFF0000u, h3 = __float_as_uint(pv[3]) & 0xFFFF0000u;
-                        tmem_st16x4(tmem + lane_base + 64 * buf + 4 * k, prmt(h0, h1, 0x7632u), prmt(h2, h3, 0x7632u));
-                        tmem_st16x4(tmem + lane_base + 64 * buf + 32 + 4 * k,
-                                    pack_bf16x2(pv[0] - __uint_as_float(h0), pv[1] - __uint_as_float(h1)),
-                                    pack_bf16x2(pv[2] - __uint_as_float(h2), pv[3] - __uint_as_float(h3)));
+                        if constexpr (KV == 0) {
+                            const uint32_t h0 = __float_as_uint(pv[0]) & 0xFFFF0000u, h1 = __float_as_uint(pv[1]) & 0xFFFF0000u;
+                            const uint32_t h2 = __float_as_uint(pv[2]) & 0xFFFF0000u, h3 = __float_as_uint(pv[3]) & 0xFFFF0000u;
+                            tmem_st16x4(tmem + lane_base + 64 * buf + 4 * k, prmt(h0, h1, 0x7632u), prmt(h2, h3, 0x7632u));
+                            tmem_st16x4(tmem + lane_base + 64 * buf + 32 + 4 * k,
+                                        pack_bf16x2(pv[0] - __uint_as_float(h0), pv[1] - __uint_as_float(h1)),
+                                        pack_bf16x2(pv[2] - __uint_as_float(h2), pv[3] - __uint_as_float(h3)));
+                        } else {  // E4M3: P x vs / vref <= 2^8 in f16, one product
+                            tmem_st16x4(tmem + lane_base + 64 * buf + 4 * k, pack_f16x2(pv[0] * vw[k][0], pv[1] * vw[k][1]),
+                                        pack_f16x2(pv[2] * vw[k][0], pv[3] * vw[k][1]));
+                        }
                     }
                     tmem_wait_st();
-                    // ---- V rows past the request's length are zeroed (stale or NaN slots of the page)
-                    if (nv < kTile) {
-                        uint8_t *vt = smem + stage * L::kStageBytes + C::kTileBytes;
-                        for (int i = tid; i < (kTile - nv) * 16; i += 128) {
-                            const int row = nv + (i >> 4), ch = i & 15;
-                            *reinterpret_cast<uint4 *>(vt + (ch >> 3) * (C::kTileBytes / 2) + row * 128 + (ch & 7) * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
+                    if constexpr (KV == 0) {
+                        // ---- V rows past the request's length are zeroed (stale or NaN slots of the page)
+                        if (nv < kTile) {
+                            uint8_t *vt = smem + stage * L::kStageBytes + C::kTileBytes;
+                            for (int i = tid; i < (kTile - nv) * 16; i += 128) {
+                                const int row = nv + (i >> 4), ch = i & 15;
+                                *reinterpret_cast<uint4 *>(vt + (ch >> 3) * (C::kTileBytes / 2) + row * 128 + (ch & 7) * 16) =
+                                    make_uint4(0u, 0u, 0u, 0u);
+                            }
+                        }
+                    } else {
+                        // ---- E4M3: V widened exactly to f16 into the stage's operand area, in the
+                        //      layout of a bf16 V tile ([half][64 rows][128 B], 128-byte swizzle);
+                        //      rows past nv are zero (their slots may hold NaN codes).  Thread work:
+                        //      16-byte chunk c (dims 16 c .. 16 c + 15) of row t in, two chunks out
+                        const uint8_t *vr = smem + stage * L::kStageBytes + C::kTileBytes;
+                        uint8_t *vc = smem + stage * L::kStageBytes + L::kVcOff;
+#pragma unroll
+                        for (int it = 0; it < 4; ++it) {
+                            const int i = tid + 128 * it, t = i >> 3, c = i & 7;
+                            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                            if (t < nv) {
+                                const uint4 x = *reinterpret_cast<const uint4 *>(vr + t * 128 + ((c ^ (t & 7)) << 4));
+                                lo = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(x.x & 0xFFFFu)),
+                                                e4m3x2_to_f16x2(static_cast<uint16_t>(x.x >> 16)),
+                                                e4m3x2_to_f16x2(static_cast<uint16_t>(x.y & 0xFFFFu)),
+                                                e4m3x2_to_f16x2(static_cast<uint16_t>(x.y >> 16)));
+                                hi = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(x.z & 0xFFFFu)),
+                                                e4m3x2_to_f16x2(static_cast<uint16_t>(x.z >> 16)),
+                                                e4m3x2_to_f16x2(static_cast<uint16_t>(x.w & 0xFFFFu)),
+                                                e4m3x2_to_f16x2(static_cast<uint16_t>(x.w >> 16)));
+                            }
+                            uint8_t *row = vc + (c >> 2) * 8192 + t * 128;  // half c / 4, chunks 2 (c % 4), + 1
+                            const int cc = 2 * (c & 3);
+                            *reinterpret_cast<uint4 *>(row + ((cc ^ (t & 7)) << 4)) = lo;
+                            *reinterpret_cast<uint4 *>(row + (((cc + 1) ^ (t & 7)) << 4)) = hi;
                         }
                     }
                     fence_proxy_async_smem();
@@ -1260,6 +1391,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                 ep_pv = pv_desc;
                 ep_last_g = last_g;
                 ep_m[0] = m[0], ep_m[1] = m[1], ep_l[0] = l[0], ep_l[1] = l[1];
+                if constexpr (KV == 1) ep_vref = vref;
             }
         }
         (void)failed;
@@ -2221,7 +2353,7 @@ template <int KV, int STAGES, int GROUPS, bool PERSIST, bool FUSE = false, int M
 dsa_status launch(const AttnArgs &a, const KernelParams &kp, dim3 grid, cudaStream_t st) {
     using L = Layout<KV, STAGES, GROUPS, MSLOTS, QW>;
     CUtensorMap km, vm;
-    const bool nhd = a.kv_layout == DSA_NHD, split = QW == 3 && a.page_size < kTile;
+    const bool nhd = a.kv_layout == DSA_NHD, split = QW == 3 && KV == 0 && a.page_size < kTile;
     if (!make_pool_map(&km, a.k_pages, KV, a.num_pages, a.num_kv_heads, a.page_size, nhd, split) ||
         !make_pool_map(&vm, a.v_pages, KV, a.num_pages, a.num_kv_heads, a.page_size, nhd, split))
         return DSA_ERR_CUDA;
@@ -2328,6 +2460,7 @@ extern "C" dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void
     // 8-row block (up to 32 rows) or two (up to 64)
     if (kv_dtype == DSA_FP8_E4M3) {
         if (R <= 16) return launch<1, kMultiStagesFp8, 2, true, false, 1, 4>(a, kp, grid, to_cuda(stream));
+        if (R > 16) return launch<1, kTcStages, 2, true, false, 1, 3>(a, kp, grid, to_cuda(stream));
         if (R <= 32) return launch<1, kMultiStagesFp8, 2, true, false, 1, 1>(a, kp, grid, to_cuda(stream));
         return launch<1, kMultiStagesFp8, 2, true, false, 1, 2>(a, kp, grid, to_cuda(stream));
     }

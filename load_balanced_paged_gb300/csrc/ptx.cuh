@@ -124,6 +124,22 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n, int a_mn, i
            (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// Instruction descriptors with format code 0 for A and B and an fp32 accumulator: f16 A and
+// B for kind::f16, E4M3 A and B for kind::f8f6f4 (same bit layout as above).
+__host__ __device__ constexpr uint32_t umma_idesc_fmt0(int m, int n, int a_mn, int b_mn) {
+    return (1u << 4) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
+           (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] . B[smem] with E4M3 A and B (K = 32 per instruction); issued by one thread.
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+        : "memory");
+}
+
 // D[tmem] (+)= A[smem] . B[smem]; issued by one thread.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool accumulate) {
     asm volatile(
