@@ -109,12 +109,13 @@ constexpr int kMaxPagesPerTile = kTile / 16;  // pages of 16 tokens: four per ti
 // teams of four softmax warps, a warp issuing S (and laying Q out as its operand), a warp
 // issuing P.V.  (An mma.sync kernel for up to 16 query rows per unit of bf16 K/V measured
 // 214-221 us on the mixed lengths against 191-195 us for the tensor-memory kernel at 2-16
-// rows: bf16 K/V always takes the tensor-memory kernel.)  QW = 1 or 2: multi-token queries
-// over E4M3 K/V with mma.sync (E4M3 products for S, f16 for P.V): every consumer warp takes
-// every tile, its token half for its set of QW 8-row blocks, and the two token halves are
-// the descriptor's two partial slots.  QW = 4: E4M3 K/V with up to 16 rows, the one-token
-// shape (groups on alternate tiles, 16 tokens per warp) over two 8-row blocks; each group
-// merges its warps into its own partial slot.
+// rows: bf16 K/V always takes the tensor-memory kernel.)  E4M3 K/V above 16 rows takes it
+// too (S with E4M3 products, V widened to f16 in shared memory).  QW = 4: E4M3 K/V with up
+// to 16 rows on mma.sync, the one-token shape (groups on alternate tiles, 16 tokens per
+// warp) over two 8-row blocks; each group merges its warps into its own partial slot.
+// (There the tensor-memory kernel, bound by its per-tile chain, measured twice the time; an
+// mma.sync kernel giving each warp a 32-token half of every tile measured 1.1-1.6x the
+// tensor-memory kernel's time at 24-64 rows.)
 template <int KV, int STAGES, int GROUPS, int MSLOTS = 2, int QW = 0>
 struct Layout {
     // descriptors handed ahead to the consumers (Q + info): with one query token a slot is
@@ -393,8 +394,8 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            // QW = 1, 2: every consumer warp reads every stage; QW = 3: the S and PV warps release it
-            mbar_init(empty_bar(s), QW == 3 ? 2 : ((QW == 1 || QW == 2) ? NCW : 4));
+            // one consumer group releases a stage; QW = 3: the S and PV warps
+            mbar_init(empty_bar(s), QW == 3 ? 2 : 4);
         }
         for (int s = 0; s < kQSlots; ++s) {
             mbar_init(qfull_bar(s), 1);
@@ -1403,266 +1404,6 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
             tmem_dealloc(tmem, 512);
         }
         return;
-    } else if constexpr (QW == 1 || QW == 2) {
-        // ============== multi-token queries over E4M3 K/V (mma.sync, 8 warps) ==============
-        // Rows r = i * G + g (query token i, head g), r < R = q_len * G; row r of a request
-        // of length len sees the tokens t < len - q_len + i + 1.  Warp w takes the tokens
-        // [32 (w & 1), +32) of every tile for the rows [8 QW (w >> 1), +8 QW): S^T blocks of
-        // 16 tokens x 8 rows (E4M3 products, k = 32), one online softmax per row over the
-        // warp's token half, and O^T += V^T . P^T with V widened to f16 (exact) and the
-        // per-token V scale folded into an f16 P.  The two token halves are the descriptor's
-        // two partial slots (2 x descriptor + half), as the two softmax teams of the
-        // tensor-memory kernel are: no merge inside the CTA.
-        constexpr int NBW = QW;
-        const int ts = warp & 1, cs = warp >> 1;
-        const int tok_base = 32 * ts;
-        const int cb = 8 * NBW * cs;
-        const int R = p.q_len * G;
-        const bool active = cb < R;
-        const int gid = lane >> 2, tig = lane & 3;
-        const int xr = lane & 7;
-        // ldmatrix rows of this lane (K and V alike: [64 rows][128 B], 128-byte swizzle):
-        // matrices (tokens 0-7 | 8-15) x (16-byte chunk 2s | 2s + 1)
-        const int k_row = tok_base + xr + ((lane >> 3) & 1) * 8;
-        const int k_chunk = lane >> 4;
-
-        for (int qi = 0;; ++qi) {
-            const int qslot = qi % kQSlots;
-            if (!wait_phase(qfull_bar(qslot), (qi / kQSlots) & 1, abort_flag, p.status)) return;
-            const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
-            if (inf->end) break;
-            const int n = inf->n, slot = inf->slot, c_start = inf->c_start, dt0 = inf->t0, len = inf->len;
-            const int d_b = inf->b, d_h = inf->h;
-
-            // Q fragments (B operand, n = row cb + 8 nb + gid), zero past R
-            uint32_t qf[NBW][4][2];
-#pragma unroll
-            for (int nb = 0; nb < NBW; ++nb) {
-                const int r = cb + 8 * nb + gid;
-                const uint8_t *qs = smem + L::kQOff + qslot * L::kQSlot + r * C::kQHeadBytes;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    qf[nb][ks][0] = r < R ? *reinterpret_cast<const uint32_t *>(qs + 32 * ks + 4 * tig) : 0u;
-                    qf[nb][ks][1] = r < R ? *reinterpret_cast<const uint32_t *>(qs + 32 * ks + 4 * tig + 16) : 0u;
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(qempty_bar(qslot));
-
-            // this lane's two rows per block (S^T columns 2 tig, 2 tig + 1): score factor
-            // (softmax scale x q_scale) and causal limit; rows past R get 0 and are never stored
-            float qsc[NBW][2];
-            int lim[NBW][2];
-#pragma unroll
-            for (int nb = 0; nb < NBW; ++nb)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int r = cb + 8 * nb + 2 * tig + e;
-                    const int i = r < R ? r / G : 0;
-                    qsc[nb][e] = r < R ? p.score_scale *
-                                             p.q_scale[(static_cast<int64_t>(d_b) * p.q_len + i) * p.hq + d_h * G + (r - i * G)]
-                                       : 0.f;
-                    lim[nb][e] = len - p.q_len + i + 1;
-                }
-            const int lim_min = len - p.q_len + 1;  // every row sees the tokens below this
-
-            float m[NBW][2], l[NBW][2], o[NBW][8][4];
-#pragma unroll
-            for (int nb = 0; nb < NBW; ++nb) {
-                m[nb][0] = m[nb][1] = -INFINITY;
-                l[nb][0] = l[nb][1] = 0.f;
-#pragma unroll
-                for (int mb = 0; mb < 8; ++mb) o[nb][mb][0] = o[nb][mb][1] = o[nb][mb][2] = o[nb][mb][3] = 0.f;
-            }
-            float vsc = 0.f, vinv = 0.f;  // O holds the true output divided by vsc; vinv = 1 / vsc
-
-            bool aborted = false;
-            for (int li = 0; li < n; ++li) {
-                const int c = c_start + li;
-                const int stage = c % STAGES;
-                if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status)) {
-                    aborted = true;
-                    break;
-                }
-                const int nv = nvalid[stage];
-                if (active && nv > tok_base) {
-                    const uint32_t kbase = sbase + stage * L::kStageBytes;
-                    const uint32_t vbase = kbase + C::kTileBytes;
-                    const float *ksm = reinterpret_cast<const float *>(smem + stage * L::kStageBytes + 2 * C::kTileBytes);
-                    const float *vsm = ksm + kTile;
-                    const int T0 = (dt0 + li) * kTile + tok_base;  // token of this warp's first row
-                    // ---- S^T = K . Q^T for 2 blocks of 16 tokens x NBW blocks of 8 rows
-                    float sc[2][NBW][4];
-#pragma unroll
-                    for (int kt = 0; kt < 2; ++kt)
-#pragma unroll
-                        for (int nb = 0; nb < NBW; ++nb) sc[kt][nb][0] = sc[kt][nb][1] = sc[kt][nb][2] = sc[kt][nb][3] = 0.f;
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const int ch = 2 * ks + k_chunk;
-#pragma unroll
-                        for (int kt = 0; kt < 2; ++kt) {
-                            uint32_t a0, a1, a2, a3;
-                            ldsm_x4(kbase + (k_row + 16 * kt) * 128 + ((ch ^ xr) << 4), a0, a1, a2, a3);
-#pragma unroll
-                            for (int nb = 0; nb < NBW; ++nb) mma_e4m3(sc[kt][nb], a0, a1, a2, a3, qf[nb][ks][0], qf[nb][ks][1]);
-                        }
-                    }
-                    // per-token scales; tokens past the tile's valid rows get none (their
-                    // shared memory may hold anything) and are masked below
-                    float ks_[2][2], vs_[2][2];
-#pragma unroll
-                    for (int kt = 0; kt < 2; ++kt)
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int t = tok_base + 16 * kt + 8 * hh + gid;
-                            ks_[kt][hh] = t < nv ? ksm[t] : 0.f;
-                            vs_[kt][hh] = t < nv ? vsm[t] : 0.f;
-                        }
-                    const bool mask = T0 + 32 > lim_min;  // some row of the warp's tokens is past a limit
-#pragma unroll
-                    for (int kt = 0; kt < 2; ++kt)
-#pragma unroll
-                        for (int nb = 0; nb < NBW; ++nb) {
-                            sc[kt][nb][0] *= qsc[nb][0] * ks_[kt][0];
-                            sc[kt][nb][1] *= qsc[nb][1] * ks_[kt][0];
-                            sc[kt][nb][2] *= qsc[nb][0] * ks_[kt][1];
-                            sc[kt][nb][3] *= qsc[nb][1] * ks_[kt][1];
-                            if (mask) {
-                                const int ta = T0 + 16 * kt + gid, tb = ta + 8;
-                                if (ta >= lim[nb][0]) sc[kt][nb][0] = -INFINITY;
-                                if (ta >= lim[nb][1]) sc[kt][nb][1] = -INFINITY;
-                                if (tb >= lim[nb][0]) sc[kt][nb][2] = -INFINITY;
-                                if (tb >= lim[nb][1]) sc[kt][nb][3] = -INFINITY;
-                            }
-                        }
-                    // ---- lazy references, so that rescaling O is rare: the V scale reference vsc is
-                    //      the largest V scale seen (P carries vs / vsc <= 1), and a row's reference
-                    //      m moves only when the row's maximum passes it by more than 8 (P <= 2^8,
-                    //      well inside f16); the warp reduces maxima only when some lane sees growth
-                    float lmx[NBW][2];
-                    bool grow = fmaxf(fmaxf(vs_[0][0], vs_[0][1]), fmaxf(vs_[1][0], vs_[1][1])) > vsc;
-#pragma unroll
-                    for (int nb = 0; nb < NBW; ++nb) {
-                        lmx[nb][0] = fmaxf(fmaxf(sc[0][nb][0], sc[0][nb][2]), fmaxf(sc[1][nb][0], sc[1][nb][2]));
-                        lmx[nb][1] = fmaxf(fmaxf(sc[0][nb][1], sc[0][nb][3]), fmaxf(sc[1][nb][1], sc[1][nb][3]));
-                        grow |= lmx[nb][0] > m[nb][0] + 8.f || lmx[nb][1] > m[nb][1] + 8.f;
-                    }
-                    if (__any_sync(0xffffffffu, grow)) {
-                        float vm = fmaxf(fmaxf(vs_[0][0], vs_[0][1]), fmaxf(vs_[1][0], vs_[1][1]));
-#pragma unroll
-                        for (int o_ = 4; o_ < 32; o_ <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o_));
-                        float vf = 1.f;  // old reference / new reference
-                        if (vm > vsc) {
-                            if (vsc > 0.f) vf = vsc / vm;
-                            vsc = vm;
-                            vinv = 1.f / vm;
-                        }
-#pragma unroll
-                        for (int nb = 0; nb < NBW; ++nb) {
-                            float f[2];
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                float mx = lmx[nb][e];
-#pragma unroll
-                                for (int o_ = 4; o_ < 32; o_ <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o_));
-                                float alpha = 1.f;
-                                if (mx > m[nb][e] + 8.f) {  // from m = -inf: alpha = 0 (nothing accumulated yet)
-                                    alpha = ex2(m[nb][e] - mx);
-                                    m[nb][e] = mx;
-                                }
-                                l[nb][e] *= alpha;
-                                f[e] = alpha * vf;
-                            }
-#pragma unroll
-                            for (int mb = 0; mb < 8; ++mb) {
-                                o[nb][mb][0] *= f[0];
-                                o[nb][mb][1] *= f[1];
-                                o[nb][mb][2] *= f[0];
-                                o[nb][mb][3] *= f[1];
-                            }
-                        }
-                    }
-                    // ---- P = 2^(s - m) (a row still at m = -inf has seen no visible token: P = 0)
-                    uint32_t bh[2][NBW][2];
-#pragma unroll
-                    for (int nb = 0; nb < NBW; ++nb) {
-                        const float r0 = m[nb][0] == -INFINITY ? 0.f : m[nb][0], r1 = m[nb][1] == -INFINITY ? 0.f : m[nb][1];
-#pragma unroll
-                        for (int kt = 0; kt < 2; ++kt) {
-                            const float p0 = ex2(sc[kt][nb][0] - r0), p1 = ex2(sc[kt][nb][1] - r1);
-                            const float p2 = ex2(sc[kt][nb][2] - r0), p3 = ex2(sc[kt][nb][3] - r1);
-                            l[nb][0] += p0 + p2;
-                            l[nb][1] += p1 + p3;
-                            const float wa = vs_[kt][0] * vinv, wb = vs_[kt][1] * vinv;
-                            bh[kt][nb][0] = movmatrix_trans(pack_f16x2(p0 * wa, p1 * wa));
-                            bh[kt][nb][1] = movmatrix_trans(pack_f16x2(p2 * wb, p3 * wb));
-                        }
-                    }
-                    // ---- O^T += V^T . P^T; V rows past the tile's valid tokens are zeroed
-                    const bool partial = nv < tok_base + 32;
-#pragma unroll
-                    for (int kt = 0; kt < 2; ++kt) {
-                        const uint32_t mlo = partial ? tok_mask(tok_base + 16 * kt + 2 * tig, nv) : 0xFFFFFFFFu;
-                        const uint32_t mhi = partial ? tok_mask(tok_base + 16 * kt + 8 + 2 * tig, nv) : 0xFFFFFFFFu;
-#pragma unroll
-                        for (int mp = 0; mp < 4; ++mp) {
-                            const int ch = 2 * mp + k_chunk;
-                            uint32_t x0, x1, x2, x3;
-                            ldsm_x4_trans(vbase + (k_row + 16 * kt) * 128 + ((ch ^ xr) << 4), x0, x1, x2, x3);
-                            // x0 / x1: tokens 0-7 / 8-15 of chunk 2 mp; x2 / x3: of chunk 2 mp + 1;
-                            // each holds, for dims (2 gid, 2 gid + 1) of its chunk, tokens (2 tig, 2 tig + 1)
-                            uint32_t a0, a1, a2, a3;
-                            cvt_pair(x0, a0, a1);
-                            cvt_pair(x1, a2, a3);
-                            if (partial) {
-                                a0 &= mlo;
-                                a1 &= mlo;
-                                a2 &= mhi;
-                                a3 &= mhi;
-                            }
-#pragma unroll
-                            for (int nb = 0; nb < NBW; ++nb) mma_f16(o[nb][2 * mp], a0, a1, a2, a3, bh[kt][nb][0], bh[kt][nb][1]);
-                            cvt_pair(x2, a0, a1);
-                            cvt_pair(x3, a2, a3);
-                            if (partial) {
-                                a0 &= mlo;
-                                a1 &= mlo;
-                                a2 &= mhi;
-                                a3 &= mhi;
-                            }
-#pragma unroll
-                            for (int nb = 0; nb < NBW; ++nb)
-                                mma_f16(o[nb][2 * mp + 1], a0, a1, a2, a3, bh[kt][nb][0], bh[kt][nb][1]);
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(stage));
-            }
-            if (aborted) return;
-            if (!active) continue;
-
-            // ---- this warp's partial: rows [cb, cb + 8 NBW) below R of slot 2 x descriptor + ts
-            const int64_t slot_row = (2 * static_cast<int64_t>(slot) + ts) * R;
-#pragma unroll
-            for (int nb = 0; nb < NBW; ++nb)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float lt = l[nb][e];
-#pragma unroll
-                    for (int o_ = 4; o_ < 32; o_ <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o_);
-                    const int r = cb + 8 * nb + 2 * tig + e;
-                    if (r >= R) continue;
-                    const float w = lt > 0.f ? vsc / lt : 0.f;
-                    float *dst = p.partial_o + (slot_row + r) * kHeadDim + 2 * gid;
-#pragma unroll
-                    for (int mb = 0; mb < 8; ++mb)
-                        *reinterpret_cast<float2 *>(dst + 16 * mb) = make_float2(o[nb][mb][e] * w, o[nb][mb][2 + e] * w);
-                    if (gid == 0) p.partial_lse[slot_row + r] = lt > 0.f ? (m[nb][e] + lg2(lt)) * kLn2 : -INFINITY;
-                }
-        }
-        return;
     } else if constexpr (QW == 4) {
         // ======= multi-token queries over E4M3 K/V, up to 16 rows per unit (mma.sync) =======
         // The one-token kernel's shape with two 8-row column blocks: the two consumer groups
@@ -2455,14 +2196,11 @@ extern "C" dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void
     kp.q_len = q_len;
     kp.slots_per_desc = dsa_multi_slots_per_desc(q_len, num_q_heads / num_kv_heads);
     const dim3 grid(map->num_ctas);
-    // E4M3 K/V: mma.sync warps; up to 16 rows the groups take alternate tiles (16 tokens x
-    // all rows per warp), beyond that every warp takes a token half of every tile for one
-    // 8-row block (up to 32 rows) or two (up to 64)
+    // E4M3 K/V: up to 16 rows mma.sync warps (the groups take alternate tiles, 16 tokens x all
+    // rows per warp), more rows the tensor-memory kernel
     if (kv_dtype == DSA_FP8_E4M3) {
         if (R <= 16) return launch<1, kMultiStagesFp8, 2, true, false, 1, 4>(a, kp, grid, to_cuda(stream));
-        if (R > 16) return launch<1, kTcStages, 2, true, false, 1, 3>(a, kp, grid, to_cuda(stream));
-        if (R <= 32) return launch<1, kMultiStagesFp8, 2, true, false, 1, 1>(a, kp, grid, to_cuda(stream));
-        return launch<1, kMultiStagesFp8, 2, true, false, 1, 2>(a, kp, grid, to_cuda(stream));
+        return launch<1, kTcStages, 2, true, false, 1, 3>(a, kp, grid, to_cuda(stream));
     }
     // bf16 K/V: the tensor-memory kernel, for any number of query rows up to 64
     return launch<0, kTcStages, 2, true, false, 1, 3>(a, kp, grid, to_cuda(stream));
