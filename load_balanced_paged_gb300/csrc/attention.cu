@@ -1195,14 +1195,23 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + 64 * buf + 8 * k, sv[k]);
                         tmem_wait_ld();
                     }
-                    // O_team was last written by the P.V of this team's previous tile (a rescale
-                    // reads it); the first tile of a descriptor starts from m = -inf and never does
-                    if (last_g >= 0 && !wait_phase(o_done(team), ((g >> 1) & 1) ^ 1, abort_flag, p.status)) {
-                        failed = true;
-                        break;
-                    }
+                    // this team's previous tile of the descriptor (-1: none; the first tile starts
+                    // from m = -inf and never rescales O).  Its P.V is waited for before this tile's
+                    // P is handed over (so the team stays within one phase of o_done, which the
+                    // descriptor end's wait needs), and before a rescale of O, which reads O.  (S of
+                    // this tile was issued after the P.V two team tiles back had released its
+                    // buffer, so until this tile's P is handed over the barrier is at most one
+                    // phase behind the one waited for.)
+                    const int prev_g = last_g;
                     last_g = g;
+                    auto wait_prev_pv = [&]() {
+                        return prev_g < 0 || wait_phase(o_done(team), ((g >> 1) & 1) ^ 1, abort_flag, p.status);
+                    };
                     if (nv == 0) {  // no data in this stage: the PV warp skips its P.V
+                        if (!wait_prev_pv()) {
+                            failed = true;
+                            break;
+                        }
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(p_full(buf));
@@ -1273,8 +1282,12 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                         if (grow[h] || m[h] == -INFINITY) m[h] = mnew;
                     }
                     if (__any_sync(0xffffffffu, grow[0] || grow[1] || (KV == 1 && vf != 1.f))) {
-                        // rows whose maximum grew: O_team *= 2^(m_old - m_new) (its last P.V is done);
-                        // E4M3: all rows also by the V scale reference's change
+                        // rows whose maximum grew: O_team *= 2^(m_old - m_new); E4M3: all rows also
+                        // by the V scale reference's change (after the previous P.V into O_team)
+                        if (!wait_prev_pv()) {
+                            failed = true;
+                            break;
+                        }
                         tc_fence_after();
 #pragma unroll 1  // rare: kept small for the instruction cache
                         for (int half = 0; half < 2; ++half) {
@@ -1368,6 +1381,10 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
                             *reinterpret_cast<uint4 *>(row + ((cc ^ (t & 7)) << 4)) = lo;
                             *reinterpret_cast<uint4 *>(row + (((cc + 1) ^ (t & 7)) << 4)) = hi;
                         }
+                    }
+                    if (!wait_prev_pv()) {
+                        failed = true;
+                        break;
                     }
                     fence_proxy_async_smem();
                     tc_fence_before();
