@@ -105,6 +105,22 @@ def test_repaged_tokens_give_the_same_bits(dsa, page, layout, kv):
         assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("page,layout", [(16, "NHD"), (32, "HND")])
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("q_len", [2, 6])
+def test_multi_token_repaged_tokens_give_the_same_bits(dsa, page, layout, kv, q_len):
+    """Multi-token steps too: the same tokens in other pages give bit-identical partials."""
+    base = make(LENS, 64, 8, kv, 64, "HND", seed=12, q_len=q_len)
+    other = repage(base, page, layout, seed=page + q_len)
+    a = dsa.attention_multi(base, 37, min_tiles_per_split=1, out_dtype=torch.float32)
+    b = dsa.attention_multi(other, 37, min_tiles_per_split=1, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert dsa.get_status(a[2]) == 0 and dsa.get_status(b[2]) == 0
+    nd = 2 * len(a[2].host()["descs"])  # two slots per descriptor
+    for x, y in ((a[0], b[0]), (a[1], b[1]), (a[3][:nd], b[3][:nd]), (a[4][:nd], b[4][:nd])):
+        assert torch.equal(x, y)
+
+
 @pytest.mark.parametrize("layout", ["HND", "NHD"])
 def test_bad_sub_page_is_flagged(dsa, layout):
     lens = [100, 200, 40]
