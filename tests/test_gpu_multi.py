@@ -109,20 +109,22 @@ def test_multi_full_size_sampled(dsa):
     parity.assert_lse_close(lse[pick].cpu().numpy(), ref_lse[pick], "mixed, q_len 6")
 
 
-def test_multi_full_size_fp8_sampled(dsa):
+@pytest.mark.parametrize("q_len", [2, 6])
+def test_multi_full_size_fp8_sampled(dsa, q_len):
     """The FP8 workload's lengths (64 requests, mean 68k tokens) with 2 query tokens per
-    request, one bin per SM; the shortest, median and longest requests checked."""
+    request (16 rows: mma.sync kernel) or 6 (48 rows: tensor-memory kernel), one bin per
+    SM; the shortest, median and longest requests checked."""
     w = workloads.WORKLOADS["fp8"]
     rng = np.random.default_rng(w.seed)
     lens = workloads.draw_lengths(w.name, w.batch, rng)
-    inp = workloads.make_inputs(lens, w.num_q_heads, w.num_kv_heads, "fp8", w.seed, "cuda", rng=rng, q_len=2)
+    inp = workloads.make_inputs(lens, w.num_q_heads, w.num_kv_heads, "fp8", w.seed, "cuda", rng=rng, q_len=q_len)
     out16, out32, lse, tm, po, pl = run(dsa, inp, sm_count(), 4)
     order = np.argsort(lens, kind="stable")
     picks = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])})
     ref, ref_lse = parity.sub_problem(inp, picks).attention()
     parity.check_outputs(out16[picks].float().cpu().numpy(), out32[picks].cpu().numpy(), ref, "fp8",
-                         "fp8, q_len 2")
-    parity.assert_lse_close(lse[picks].cpu().numpy(), ref_lse, "fp8, q_len 2")
+                         f"fp8, q_len {q_len}")
+    parity.assert_lse_close(lse[picks].cpu().numpy(), ref_lse, f"fp8, q_len {q_len}")
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
