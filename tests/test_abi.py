@@ -107,15 +107,19 @@ def test_decode_ex_host_checks(lib):
     lib.dsa_decode_ex.argtypes = [i, i, V, i, V, V, V, i, V, V, V, i, i, V, i, i, i, i, i, f,
                                   ctypes.POINTER(TaskMap), V, V, V, V]
 
-    def call(q_len=1, layout=1, kv_dt=0, hq=64, hkv=8, page=16):
-        return lib.dsa_decode_ex(q_len, layout, fake, 0, None, fake, fake, kv_dt, None, None, fake, 4, 8, fake,
-                                 2, hq, hkv, 128, page, 0.1, ctypes.byref(tm), fake, fake, None, None)
+    def call(q_len=1, layout=1, kv_dt=0, hq=64, hkv=8, page=16, q_dt=0, scales=None):
+        return lib.dsa_decode_ex(q_len, layout, fake, q_dt, scales, fake, fake, kv_dt, scales, scales, fake, 4, 8,
+                                 fake, 2, hq, hkv, 128, page, 0.1, ctypes.byref(tm), fake, fake, None, None)
     assert call(layout=2) == 1              # not a dsa_kv_layout
     assert call(layout=-1) == 1
     assert call(page=8) == 2
     assert call(q_len=0) == 1
     assert call(q_len=9) == 2               # 9 x 8 = 72 query rows per unit
     assert call(q_len=2, kv_dt=1) == 2      # bf16 Q over E4M3 K/V not built
+    assert call(q_len=2, q_dt=1, kv_dt=1) == 1  # E4M3 multi-token without scales
+    misaligned = ctypes.c_void_p(0x10004)
+    assert call(q_len=6, q_dt=1, kv_dt=1, scales=misaligned) == 1  # scale pools must be 16-byte aligned
+    assert call(q_len=9, q_dt=1, kv_dt=1, scales=fake) == 2  # 72 query rows per unit
 
 
 def test_status_strings(lib):
