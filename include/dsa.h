@@ -218,8 +218,9 @@ dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_sca
  *   partial_o [S * map->max_descs, q_len*G, 128] fp32, partial_lse [S * map->max_descs,
  *            q_len*G] with S = dsa_multi_slots_per_desc(q_len, G): 2 for q_len > 1
  *            (slots 2x and 2x + 1, each the attention over part of the descriptor's
- *            tokens: for bf16 K/V the two softmax teams of the tensor-memory kernel, for
- *            E4M3 K/V the two 32-token halves of every tile), 1 for q_len = 1;
+ *            tiles: the two softmax teams of the tensor-memory kernel, or, for E4M3 K/V
+ *            with q_len * G <= 16, the two consumer groups that take alternate tiles),
+ *            1 for q_len = 1;
  *            merging a descriptor's slots gives its attention, and dsa_combine_multi
  *            does so.
  * Supported: the dtypes of dsa_decode (BF16, or E4M3 Q and K/V), q_len * G <= 64;
