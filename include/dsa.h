@@ -399,12 +399,18 @@ dsa_status dsa_prologue(const void *qkv, int32_t n_tokens, int32_t num_q_heads, 
  * step needs about 16*(B*Hkv + C) + 4*C + 8*B*Hkv bytes of task map plus
  * (B*Hkv + C - 1) * G * 129 * 4 bytes of partials (C = num_persistent_ctas);
  * larger steps are rejected with DSA_ERR_BUFFER_TOO_SMALL before anything is
- * launched.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  Every call reuses the same array, so calls whose work
- * overlaps on the GPU (other streams, other threads) race on it; calls in one
- * stream are safe.  Nothing in the array needs clearing between calls.
- * status: device int32, may be NULL; receives the step's DSA_DEV_* bits.
+ * launched, as are all arguments dsa_plan, dsa_decode or dsa_combine would refuse
+ * (out must be 16-byte aligned; B*Hkv and num_persistent_ctas at most 16384): a
+ * step is either refused before any launch or enqueued whole.  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current and keeps it for the life of the process; make that first call
+ * before any stream capture, and do not call this entry point on a device after
+ * cudaDeviceReset (the kept address then names freed memory).  Every call reuses
+ * the same array, so calls whose work overlaps on the GPU (other streams, other
+ * threads) race on it; calls in one stream are safe.  Nothing in the array needs
+ * clearing between calls.
+ * status: device int32, may be NULL; receives the step's DSA_DEV_* bits.  When it
+ * is nonzero, out and out_lse are undefined (the kernels skipped the bad work).
  * No cudaMalloc, cudaFree or allocating library routine is called.
  */
 #define DSA_NOALLOC_SCRATCH_BYTES (8u << 20)

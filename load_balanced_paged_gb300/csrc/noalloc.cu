@@ -61,16 +61,20 @@ extern "C" dsa_status dsa_decode_step_noalloc(
                      page_size, sm_scale};
     dsa_status s = validate_attn(a);
     if (s != DSA_OK) return s;
+    // every check that dsa_plan, dsa_decode and dsa_combine make on these arguments is made
+    // here, before anything is launched: a step is either refused whole or enqueued whole
     if (num_persistent_ctas < 1 || min_tiles_per_split < 1) return DSA_ERR_INVALID_ARG;
     if (out_dtype != DSA_BF16 && out_dtype != DSA_FP32) return DSA_ERR_UNSUPPORTED;
     if (batch > 0 && !out) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(out)) return DSA_ERR_INVALID_ARG;
+    const int64_t units = static_cast<int64_t>(batch) * num_kv_heads;
+    if (units > kPlanMaxUnits || num_persistent_ctas > kPlanMaxCtas) return DSA_ERR_UNSUPPORTED;
     const int32_t md = dsa_max_descs(batch, num_kv_heads, num_persistent_ctas);
     if (md < 0) return DSA_ERR_INVALID_ARG;
-    const int64_t units = static_cast<int64_t>(batch) * num_kv_heads;
     const int64_t G = num_q_heads / num_kv_heads;
     // carve the array: task map, then partial outputs and their LSEs
     const size_t off_begin = 0;
-    const size_t off_descs = align256(off_begin + sizeof(int32_t) * (num_persistent_ctas + 1));
+    const size_t off_descs = align256(off_begin + sizeof(int32_t) * (static_cast<size_t>(num_persistent_ctas) + 1));
     const size_t off_upb = align256(off_descs + sizeof(int32_t) * 4 * static_cast<size_t>(md > 0 ? md : 1));
     const size_t off_unp = align256(off_upb + sizeof(int32_t) * static_cast<size_t>(units > 0 ? units : 1));
     const size_t off_meta = align256(off_unp + sizeof(int32_t) * static_cast<size_t>(units > 0 ? units : 1));

@@ -122,6 +122,27 @@ def test_decode_ex_host_checks(lib):
     assert call(q_len=9, q_dt=1, kv_dt=1, scales=fake) == 2  # 72 query rows per unit
 
 
+def test_noalloc_host_checks(lib):
+    """dsa_decode_step_noalloc refuses, before it touches the device, every argument that one
+    of its three kernels' entry points would refuse, so a step is never half enqueued."""
+    fake = ctypes.c_void_p(0x10000)
+    i, f, V = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
+    lib.dsa_decode_step_noalloc.argtypes = [V, i, V, V, V, i, V, V, V, i, i, V, i, i, i, i, i, f,
+                                            i, i, V, i, V, V, V]
+
+    def call(out=fake, batch=2, ctas=4, floor=4, out_dt=0, hq=64, hkv=8):
+        return lib.dsa_decode_step_noalloc(fake, 0, None, fake, fake, 0, None, None, fake, 4, 8, fake, batch,
+                                           hq, hkv, 128, 64, 0.1, ctas, floor, out, out_dt, None, None, None)
+    assert call(out=ctypes.c_void_p(0x10004)) == 1   # out not 16-byte aligned (dsa_combine's rule)
+    assert call(out=None) == 1
+    assert call(out_dt=1) == 2                         # E4M3 output not built
+    assert call(floor=0) == 1
+    assert call(ctas=0) == 1
+    assert call(batch=0, ctas=2 ** 31 - 1) == 2        # above the plan's CTA limit, no overflow
+    assert call(batch=4096, hkv=8, hq=64) == 2         # 32768 units: above the plan's unit limit
+    assert call(batch=2048, hkv=8, hq=64) == 3         # fits the plan, not the fixed scratch
+
+
 def test_status_strings(lib):
     lib.dsa_status_string.restype = ctypes.c_char_p
     assert lib.dsa_status_string(0) == b"DSA_OK"
