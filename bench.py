@@ -150,55 +150,26 @@ def aggregate_gbs(bytes_per_rank: int, world: int, ms_per_step: float) -> float:
 
 # ---------------------------------------------------------------------------- our arm
 
-def bench_ours(args, device, rank, world):
-    import load_balanced_paged_gb300 as dsa
+def stats_us(ms) -> dict:
+    """Mean, median and 90th percentile of per-replay times (ms in, us out)."""
+    a = np.asarray(ms, dtype=np.float64) * 1e3
+    return {"mean": round(float(a.mean()), 2), "median": round(float(np.median(a)), 2),
+            "p90": round(float(np.percentile(a, 90)), 2), "reps": int(a.size)}
 
-    name = args.workload
-    w = workloads.WORKLOADS[name]
-    inp = workloads.make_workload(name, device=device, seed=w.seed + rank, max_requests=args.requests)
-    sms = torch.cuda.get_device_properties(device).multi_processor_count
-    C = w.num_ctas(sms)
-    m = args.min_tiles
-    B, hq, hkv = int(inp["seq_lens"].shape[0]), w.num_q_heads, w.num_kv_heads
-    G = hq // hkv
-    tm = dsa.TaskMap(B, hkv, C, device)
-    po, pl = dsa.partial_buffers(tm.max_descs, G, device)
-    out = torch.empty(B, hq, 128, dtype=torch.bfloat16, device=device)
-    out_lse = torch.empty(B, hq, dtype=torch.float32, device=device)
-    stream = torch.cuda.current_stream(device)
-    kw = dict(q_scale=inp["q_scale"], k_scale=inp["k_scale"], v_scale=inp["v_scale"])
 
-    def plan():
-        dsa.plan(inp["seq_lens"], hkv, C, m, task_map=tm)
+class Timer:
+    """Device timing of captured kernel sequences on one stream (CUDA events on that stream),
+    with an optional 2 x L2 write-flush before every replay (outside the events)."""
 
-    def decode():
-        dsa.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
-                   inp["sm_scale"], partial_o=po, partial_lse=pl, **kw)
+    def __init__(self, stream, flush):
+        self.stream = stream
+        self.flush = flush
 
-    def combine():
-        dsa.combine(tm, po, pl, hq, out=out, out_lse=out_lse)
+    def flush_l2(self, k):
+        if self.flush is not None:
+            self.flush.fill_(float(k))
 
-    counters = tm.unit_counters()
-
-    def decode_fused():
-        dsa.decode_fused(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
-                         inp["sm_scale"], out=out, out_lse=out_lse, partial_o=po, partial_lse=pl,
-                         unit_counters=counters, **kw)
-
-    nbytes = kv_bytes(inp)
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    # Inputs larger than L2 need no flush between steps; a write-flush would leave L2 dirty
-    # and bill the next step for ~L2-size of write-backs.  Small inputs are flushed.
-    do_flush = args.l2 == "flush" or (args.l2 == "auto" and nbytes < 2 * l2)
-    flush = flush_buffer(device) if do_flush else None
-    l2_note = ("flushed (2 x L2 write) before every timed step" if do_flush else
-               f"inputs larger than L2 ({nbytes / 1e6:.0f} MB of KV vs {l2 / 1e6:.0f} MB L2), no flush")
-
-    def flush_l2(k):
-        if flush is not None:
-            flush.fill_(float(k))
-
-    def graphs_of(fns):
+    def graphs_of(self, fns):
         """One CUDA graph per function (each a captured kernel launch)."""
         gs = []
         for f in fns:
@@ -209,17 +180,17 @@ def bench_ours(args, device, rank, world):
         torch.cuda.synchronize()
         return gs
 
-    def timed(fns, steps, warmup):
+    def per_kernel(self, fns, steps, warmup):
         """Per-kernel device times: the kernels captured in ONE graph with event-record nodes
-        between them (no launch gaps counted), replayed `steps` times after an L2 flush.
-        Returns ms [steps, len(fns)]."""
+        between them (no launch gaps counted), replayed `steps` times.  Returns ms
+        [steps, len(fns)]."""
         for _ in range(warmup):
             for f in fns:
                 f()
         try:
             evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(fns) + 1)]
         except TypeError:  # torch without external events: one graph per kernel, events between
-            return timed_separate(fns, steps)
+            return self._separate(fns, steps)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             evs[0].record()
@@ -229,26 +200,27 @@ def bench_ours(args, device, rank, world):
         torch.cuda.synchronize()
         per = []
         for k in range(steps):
-            flush_l2(k)
+            self.flush_l2(k)
             g.replay()
-            stream.synchronize()
+            self.stream.synchronize()
             per.append([evs[i].elapsed_time(evs[i + 1]) for i in range(len(fns))])
         return np.array(per)
 
-    def timed_separate(fns, steps):
-        gs = graphs_of(fns)
+    def _separate(self, fns, steps):
+        gs = self.graphs_of(fns)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)] for _ in range(steps)]
         for k in range(steps):
-            flush_l2(k)
-            ev[k][0].record(stream)
+            self.flush_l2(k)
+            ev[k][0].record(self.stream)
             for i, g in enumerate(gs):
                 g.replay()
-                ev[k][i + 1].record(stream)
-        stream.synchronize()
+                ev[k][i + 1].record(self.stream)
+        self.stream.synchronize()
         return np.array([[ev[k][i].elapsed_time(ev[k][i + 1]) for i in range(len(fns))] for k in range(steps)])
 
-    def timed_whole(fns, steps):
-        """The same kernels captured as ONE graph (a production decode step) timed as a unit."""
+    def whole(self, fns, steps):
+        """The kernels captured as ONE graph (a production decode step) timed as a unit, each
+        replay between its own pair of events.  Returns ms [steps]."""
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for f in fns:
@@ -256,47 +228,75 @@ def bench_ours(args, device, rank, world):
         torch.cuda.synchronize()
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
         for k in range(steps):
-            flush_l2(k)
-            ev[k][0].record(stream)
+            self.flush_l2(k)
+            ev[k][0].record(self.stream)
             g.replay()
-            ev[k][1].record(stream)
-        stream.synchronize()
+            ev[k][1].record(self.stream)
+        self.stream.synchronize()
         return np.array([ev[k][0].elapsed_time(ev[k][1]) for k in range(steps)])
 
-    # warm-up + correctness gate of this configuration (status word must be clean)
-    timed([plan, decode, combine], 1, args.warmup)
-    timed([plan, decode_fused], 1, args.warmup)
-    torch.cuda.synchronize()
-    status = dsa.get_status(tm)
-    if status != 0:
-        raise RuntimeError(f"device status {status} on the bench workload")
 
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(torch.cuda.get_device_properties(device).uuid and
-                          "GPU-" + str(torch.cuda.get_device_properties(device).uuid))
-    time.sleep(0.3)
-    t_wall0 = time.time()
-    step_ms = timed_whole([plan, decode, combine], args.steps)
-    t_wall1 = time.time()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    clocks.stop()
-    clk = clocks.summary(t_wall0, t_wall1)
+def l2_policy(args, nbytes: int, device):
+    """Inputs larger than L2 need no flush between steps (a write-flush would leave L2 dirty and
+    bill the next step for ~L2-size of write-backs); small inputs are flushed."""
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    do_flush = args.l2 == "flush" or (args.l2 == "auto" and nbytes < 2 * l2)
+    note = ("flushed (2 x L2 write) before every timed step" if do_flush else
+            f"inputs larger than L2 ({nbytes / 1e6:.0f} MB of KV vs {l2 / 1e6:.0f} MB L2), no flush")
+    return do_flush, note
 
-    total_ms = float(step_ms.sum())
-    nrep = max(10, min(args.steps, 500))
-    fused_ms = float(timed_whole([plan, decode_fused], nrep).mean())
-    per = timed([plan, decode, combine], nrep, 0)
-    per_f = timed([plan, decode_fused], nrep, 0)
-    t_dec_fused = float(per_f[:, 1].mean())
-    total_ms = replica_max(total_ms, world, device)
-    ms_per_step = total_ms / args.steps
-    t_plan, t_dec, t_comb = (float(x) for x in per.mean(axis=0))
 
-    # static split-KV comparison on the same inputs (decode + its combine)
+def workload_config(w, B: int, C: int, m: int, nbytes: int, l2_note: str, world: int) -> dict:
+    """The `config` object of a bench line (the reference arm prints the same one)."""
+    return {"workload": w.description, "name": w.name, "batch": B, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": 128, "page_size": 64, "persistent_ctas": C,
+            "min_tiles_per_split": m, "kv_bytes_per_step": nbytes, "l2": l2_note,
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+
+
+class Step:
+    """One decode step of a workload through the binding: plan -> decode -> combine."""
+
+    def __init__(self, dsa, inp, w, C: int, m: int, device):
+        self.dsa, self.inp, self.w, self.C, self.m = dsa, inp, w, C, m
+        self.B, self.hq, self.hkv = int(inp["seq_lens"].shape[0]), w.num_q_heads, w.num_kv_heads
+        self.G = self.hq // self.hkv
+        self.tm = dsa.TaskMap(self.B, self.hkv, C, device)
+        self.po, self.pl = dsa.partial_buffers(self.tm.max_descs, self.G, device)
+        self.out = torch.empty(self.B, self.hq, 128, dtype=torch.bfloat16, device=device)
+        self.out_lse = torch.empty(self.B, self.hq, dtype=torch.float32, device=device)
+        self.kw = dict(q_scale=inp["q_scale"], k_scale=inp["k_scale"], v_scale=inp["v_scale"])
+        self.counters = self.tm.unit_counters()
+
+    def plan(self):
+        self.dsa.plan(self.inp["seq_lens"], self.hkv, self.C, self.m, task_map=self.tm)
+
+    def decode(self, cta_times=None):
+        i = self.inp
+        self.dsa.decode(i["q"], i["k_pages"], i["v_pages"], i["block_table"], i["seq_lens"], self.tm, i["sm_scale"],
+                        partial_o=self.po, partial_lse=self.pl, cta_times=cta_times, **self.kw)
+
+    def combine(self):
+        self.dsa.combine(self.tm, self.po, self.pl, self.hq, out=self.out, out_lse=self.out_lse)
+
+    def decode_fused(self):
+        i = self.inp
+        self.dsa.decode_fused(i["q"], i["k_pages"], i["v_pages"], i["block_table"], i["seq_lens"], self.tm,
+                              i["sm_scale"], out=self.out, out_lse=self.out_lse, partial_o=self.po,
+                              partial_lse=self.pl, unit_counters=self.counters, **self.kw)
+
+    def check(self, what):
+        torch.cuda.synchronize()
+        status = self.dsa.get_status(self.tm)
+        if status != 0:
+            raise RuntimeError(f"device status {status} on {what}")
+
+
+def bench_static(dsa, step: Step, timer: Timer, reps: int, device, t_dec_comb: float, t_step: float) -> dict:
+    """Both static split-KV forms on the step's inputs (decode + its combine), timed the same
+    way, with how evenly each static grid's CTAs finish (one untimed launch with per-CTA
+    timestamps)."""
+    inp, B, hq, hkv, G = step.inp, step.B, step.hq, step.hkv, step.G
     static = {}
     max_len = int(inp["seq_lens"].max().item())
     for label, mode, param in (("static_16_splits", 0, 16), ("static_4096_chunk", 1, 4096)):
@@ -304,44 +304,123 @@ def bench_ours(args, device, rank, world):
         spo, spl = dsa.partial_buffers(B * hkv * S, G, device)
         sst = torch.zeros(1, dtype=torch.int32, device=device)
 
-        def sdec(mode=mode, param=param, spo=spo, spl=spl, sst=sst):
+        def sdec(mode=mode, param=param, spo=spo, spl=spl, sst=sst, cta_times=None):
             dsa.static_splitkv(mode, param, max_len, inp["q"], inp["k_pages"], inp["v_pages"],
                                inp["block_table"], inp["seq_lens"], hkv, inp["sm_scale"], partial_o=spo,
-                               partial_lse=spl, status=sst, **kw)
+                               partial_lse=spl, status=sst, cta_times=cta_times, **step.kw)
 
         def scomb(S=S, spo=spo, spl=spl):
-            dsa.static_combine(S, spo, spl, B, hq, hkv, out=out, out_lse=out_lse)
+            dsa.static_combine(S, spo, spl, B, hq, hkv, out=step.out, out_lse=step.out_lse)
 
-        sp = timed([sdec, scomb], max(10, min(args.steps, 200)), 3)
+        sp = timer.per_kernel([sdec, scomb], reps, 3)
         if dsa.read_status(sst) != 0:
             raise RuntimeError(f"{label}: device status set")
-        s_ms = float(sp.sum(axis=1).mean())
-        static[label] = {"splits": S, "us_per_step": round(s_ms * 1e3, 2),
-                         "speedup_of_dynamic": round(s_ms / (t_dec + t_comb), 3),
-                         "speedup_of_dynamic_with_plan": round(s_ms / ms_per_step, 3)}
-        # how evenly the static grid's CTAs finish (one untimed launch with per-CTA timestamps)
+        tot = sp.sum(axis=1)
+        s_ms = float(tot.mean())
+        static[label] = {"splits": S, "us_per_step": round(s_ms * 1e3, 2), "us": stats_us(tot),
+                         "speedup_of_dynamic": round(s_ms / t_dec_comb, 3),
+                         "speedup_of_dynamic_with_plan": round(s_ms / t_step, 3)}
         st_times = torch.zeros(B * hkv * S, 2, dtype=torch.int64, device=device)
-        dsa.static_splitkv(mode, param, max_len, inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"],
-                           inp["seq_lens"], hkv, inp["sm_scale"], partial_o=spo, partial_lse=spl, status=sst,
-                           cta_times=st_times, **kw)
+        sdec(cta_times=st_times)
         static[label]["balance"] = cta_balance(st_times)
+        del spo, spl
+    return static
 
-    # the same for the persistent kernel's bins
+
+def measure_workload(dsa, device, name: str, args, rank: int, world: int, reps: int, seed_offset: int = 0):
+    """The step of one workload: whole-step replays (mean / median / p90), per-kernel times,
+    both static forms, the persistent bins' balance and the clocks seen meanwhile."""
+    w = workloads.WORKLOADS[name]
+    inp = workloads.make_workload(name, device=device, seed=w.seed + seed_offset, max_requests=args.requests)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    C = w.num_ctas(sms)
+    step = Step(dsa, inp, w, C, args.min_tiles, device)
+    nbytes = kv_bytes(inp)
+    do_flush, l2_note = l2_policy(args, nbytes, device)
+    timer = Timer(torch.cuda.current_stream(device), flush_buffer(device) if do_flush else None)
+    fns = [step.plan, step.decode, step.combine]
+    timer.per_kernel(fns, 1, args.warmup)  # warm-up + correctness gate (status word must be clean)
+    step.check(f"the {name} workload")
+    clocks = ClockSampler(gpu_uuid(device))
+    time.sleep(0.3)
+    t0 = time.time()
+    whole = timer.whole(fns, reps)
+    per = timer.per_kernel(fns, reps, 0)
+    t1 = time.time()
+    clocks.stop()
+    step.check(f"the {name} workload (timed)")
+    t_plan, t_dec, t_comb = (float(x) for x in per.mean(axis=0))
+    t_step = float(whole.mean())
+    static = bench_static(dsa, step, timer, reps, device, t_dec + t_comb, t_step)
     dyn_times = torch.zeros(C, 2, dtype=torch.int64, device=device)
-    dsa.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
-               inp["sm_scale"], partial_o=po, partial_lse=pl, cta_times=dyn_times, **kw)
-    balance = cta_balance(dyn_times)
+    step.decode(cta_times=dyn_times)
+    peak, _ = measured_peaks()
+    dec_gbs = nbytes / (t_dec * 1e-3) / 1e9
+    step_gbs = nbytes / (t_step * 1e-3) / 1e9
+    rec = {"config": workload_config(w, step.B, C, args.min_tiles, nbytes, l2_note, world),
+           "step": "plan -> decode -> combine, one CUDA graph", "step_us": stats_us(whole),
+           "breakdown_us": {k: stats_us(per[:, i]) for i, k in enumerate(("plan", "decode", "combine"))},
+           "decode_GB/s": round(dec_gbs, 1), "decode_frac_of_hbm_peak": round(dec_gbs / peak, 4),
+           "decode_frac_of_hbm_peak_median": round(nbytes / (float(np.median(per[:, 1])) * 1e-3) / 1e9 / peak, 4),
+           "step_GB/s": round(step_gbs, 1), "step_frac_of_hbm_peak": round(step_gbs / peak, 4),
+           "static": static, "balance": cta_balance(dyn_times),
+           "clocks": clocks.summary(t0, t1)}
+    rec["decode_traffic_bytes"], rec["decode_traffic_source"] = profile_traffic(name, nbytes)
+    rec["gate"] = {"decode_ge_70pct_of_peak": rec["decode_frac_of_hbm_peak"] >= 0.70,
+                   "faster_than_both_static_forms": all(v["speedup_of_dynamic"] > 1.0 for v in static.values())}
+    return rec, step, timer, (t_plan, t_dec, t_comb)
 
-    prologue = bench_prologue(dsa, device, w, B, timed, max(10, min(args.steps, 200)))
+
+def gpu_uuid(device):
+    u = torch.cuda.get_device_properties(device).uuid
+    return u and "GPU-" + str(u)
+
+
+def bench_ours(args, device, rank, world):
+    import load_balanced_paged_gb300 as dsa
+
+    name = args.workload
+    reps = max(50, min(args.steps, 500))
+    head, step, timer, (t_plan, t_dec, t_comb) = measure_workload(dsa, device, name, args, rank, world, reps,
+                                                                  seed_offset=rank)
+    w, inp, C, m, B, hq = step.w, step.inp, step.C, step.m, step.B, step.hq
+    nbytes = head["config"]["kv_bytes_per_step"]
+    fns = [step.plan, step.decode, step.combine]
+    timer.per_kernel([step.plan, step.decode_fused], 1, args.warmup)
+    step.check("the fused step")
+
+    # ---- the timed region of the contract: exactly K steps of the captured graph
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(gpu_uuid(device))
+    time.sleep(0.3)
+    t_wall0 = time.time()
+    step_ms = timer.whole(fns, args.steps)
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.stop()
+    clk = clocks.summary(t_wall0, t_wall1)
+    total_ms = replica_max(float(step_ms.sum()), world, device)
+    ms_per_step = total_ms / args.steps
+
+    fused_ms = timer.whole([step.plan, step.decode_fused], reps)
+    per_f = timer.per_kernel([step.plan, step.decode_fused], reps, 0)
+    step.check("the fused step (timed)")
+    nrep = max(10, min(args.steps, 200))
+    prologue = bench_prologue(dsa, device, w, B, timer, nrep)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
     # multi-token steps use one bin per SM: the tensor-memory kernel holds one CTA per SM
-    multi = bench_multi(dsa, device, inp, w, sms, m, timed, max(10, min(args.steps, 200)), nbytes, ms_per_step)
-    layouts = bench_layouts(dsa, device, inp, w, C, m, timed, max(10, min(args.steps, 200)), nbytes, t_dec)
+    multi = bench_multi(dsa, device, inp, w, sms, m, timer, nrep, nbytes, ms_per_step)
+    layouts = bench_layouts(dsa, device, inp, w, C, m, timer, nrep, nbytes, t_dec)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     host = {k: inp[k].cpu().pin_memory() for k in ("q", "q_scale", "k_pages", "v_pages", "k_scale", "v_scale",
                                                    "block_table", "seq_lens") if inp[k] is not None}
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(out_lse.shape, dtype=out_lse.dtype).pin_memory()
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    lse_h = torch.empty(step.out_lse.shape, dtype=step.out_lse.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
     e2e_steps = max(3, min(args.steps, 20))
@@ -349,18 +428,16 @@ def bench_ours(args, device, rank, world):
     def e2e_step():
         for k, t in host.items():
             inp[k].copy_(t, non_blocking=True)
-        plan()
-        decode()
-        combine()
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(out_lse, non_blocking=True)
+        step.plan()
+        step.decode()
+        step.combine()
+        out_h.copy_(step.out, non_blocking=True)
+        lse_h.copy_(step.out_lse, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
-    torch.cuda.synchronize()
-    if dsa.get_status(tm) != 0:
-        raise RuntimeError("device status set on the end-to-end step")
-    torch.cuda.synchronize()
+    step.check("the end-to-end step")
+    stream = timer.stream
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
@@ -368,6 +445,18 @@ def bench_ours(args, device, rank, world):
     e1.record(stream)
     e1.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    # the other four workloads, each measured the same way (the headline stays `name`)
+    others = {}
+    if not args.no_other_workloads:
+        del host, out_h, lse_h
+        for other in workloads.WORKLOADS:
+            if other == name:
+                continue
+            rec, ostep, _, _ = measure_workload(dsa, device, other, args, rank, world, reps, seed_offset=rank)
+            others[other] = rec
+            del ostep
+            torch.cuda.empty_cache()
 
     peak, peak_src = measured_peaks()
     achieved = nbytes / (t_dec * 1e-3) / 1e9
@@ -377,6 +466,7 @@ def bench_ours(args, device, rank, world):
         "value": round(aggregate_gbs(nbytes, world, ms_per_step), 2),
         "unit": "GB/s",
         "us_per_step": round(ms_per_step * 1e3, 2),
+        "us_per_step_stats": stats_us(step_ms),
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True,
@@ -384,22 +474,22 @@ def bench_ours(args, device, rank, world):
         "vs_baseline": None,
         "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3",
         "data": "synthetic (seeded; lengths, page permutation and N(0,1) values drawn as in workloads.py)",
-        "config": {"workload": w.description, "name": name, "batch": B, "num_q_heads": hq, "num_kv_heads": hkv,
-                   "head_dim": 128, "page_size": 64, "persistent_ctas": C, "min_tiles_per_split": m,
-                   "kv_bytes_per_step": nbytes, "l2": l2_note,
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "config": head["config"],
         "step": "dsa_plan -> dsa_decode -> dsa_combine, one CUDA graph, programmatic dependent launch",
         "breakdown_us": {"plan": round(t_plan * 1e3, 2), "decode": round(t_dec * 1e3, 2),
                          "combine": round(t_comb * 1e3, 2)},
-        "fused_combine": {"us_per_step": round(fused_ms * 1e3, 2),
-                          "decode_fused_us": round(t_dec_fused * 1e3, 2),
+        "breakdown_us_stats": head["breakdown_us"],
+        "step_us_stats": head["step_us"],
+        "fused_combine": {"us_per_step": round(float(fused_ms.mean()) * 1e3, 2),
+                          "decode_fused_us": round(float(per_f[:, 1].mean()) * 1e3, 2),
                           "note": "dsa_plan -> dsa_decode_fused (combine inside the persistent kernel)"},
         "pct_of_nominal_8tbs": round(100 * nbytes / (ms_per_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 1),
-        "static": static,
+        "static": head["static"],
         "prologue": prologue,
         "multi_token": multi,
         "page_layouts": layouts,
-        "balance": balance,
+        "balance": head["balance"],
+        "workloads": others,
         "roofline": {"bound": "hbm", "kernel": "attn_kernel (persistent decode, dsa_decode)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
@@ -408,6 +498,7 @@ def bench_ours(args, device, rank, world):
                 "us_per_step": round(e2e_ms * 1e3, 1), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
+        "clocks_headline_workload": head["clocks"],
     }
     return res, inp, nbytes
 
@@ -420,7 +511,7 @@ def prologue_bytes(n_tokens: int, hq: int, hkv: int, fp8: bool, rot: int = 128) 
     return n_tokens * (rd + wr)
 
 
-def bench_prologue(dsa, device, w, batch: int, timed, steps: int) -> dict:
+def bench_prologue(dsa, device, w, batch: int, timer, steps: int) -> dict:
     """dsa_prologue (QK-Norm, RoPE, Hadamard, encoding, cache write) for the decode batch of
     this workload and for a 16384-token prefill chunk of the same heads and dtypes."""
     fp8 = w.kv_dtype == "fp8"
@@ -446,7 +537,7 @@ def bench_prologue(dsa, device, w, batch: int, timed, steps: int) -> dict:
                          k_norm_weight=pin["k_norm_weight"], hadamard=True, q_dtype=dt, q_out=q, q_scale=qs,
                          status=st)
 
-        ms = float(timed([run], steps, 3).mean())
+        ms = float(timer.per_kernel([run], steps, 3).mean())
         if dsa.read_status(st) != 0:
             raise RuntimeError(f"prologue {label}: device status set")
         nb = prologue_bytes(n, w.num_q_heads, w.num_kv_heads, fp8)
@@ -456,7 +547,7 @@ def bench_prologue(dsa, device, w, batch: int, timed, steps: int) -> dict:
     return res
 
 
-def bench_multi(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes: int, single_ms: float) -> dict:
+def bench_multi(dsa, device, inp, w, C: int, m: int, timer, steps: int, nbytes: int, single_ms: float) -> dict:
     """Multi-token verify steps (q_len query tokens per request, causal within the draft) on
     this workload's KV, C bins: plan -> dsa_decode_multi -> dsa_combine_multi in one graph.  The KV
     stream is read once per step whatever q_len is; `vs_q_len_one_token_steps` compares with
@@ -488,7 +579,7 @@ def bench_multi(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes: 
         def comb(q_len=q_len, tm=tm, po=po, pl=pl, out=out, out_lse=out_lse):
             dsa.combine_multi(q_len, tm, po, pl, hq, out=out, out_lse=out_lse)
 
-        per = timed([plan, dec, comb], steps, 3)
+        per = timer.per_kernel([plan, dec, comb], steps, 3)
         if dsa.get_status(tm) != 0:
             raise RuntimeError(f"multi-token q_len {q_len}: device status set")
         t_plan, t_dec, t_comb = (float(x) for x in per.mean(axis=0))
@@ -521,7 +612,7 @@ def cta_balance(times: torch.Tensor) -> dict:
             "end_spread_us": round(float(end.max() - end.min()) / 1e3, 2)}
 
 
-def bench_layouts(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes: int, base_ms: float) -> dict:
+def bench_layouts(dsa, device, inp, w, C: int, m: int, timer, steps: int, nbytes: int, base_ms: float) -> dict:
     """The decode kernel on the same lengths and C bins with the KV held in pages of 16 / 32 /
     64 tokens, HND or NHD (dsa_decode_ex): a 64-token tile is then loaded as 64 / P boxes."""
     B, hq, hkv = int(inp["seq_lens"].shape[0]), w.num_q_heads, w.num_kv_heads
@@ -539,7 +630,7 @@ def bench_layouts(dsa, device, inp, w, C: int, m: int, timed, steps: int, nbytes
                        inp["sm_scale"], partial_o=po, partial_lse=pl, q_scale=inp.get("q_scale"),
                        k_scale=li.get("k_scale"), v_scale=li.get("v_scale"), kv_layout=layout)
 
-        per = timed([dec], steps, 3)
+        per = timer.per_kernel([dec], steps, 3)
         if dsa.get_status(tm) != 0:
             raise RuntimeError(f"page {page} {layout}: device status set")
         t = float(per.mean())
@@ -620,6 +711,8 @@ def main():
     ap.add_argument("--min-tiles", type=int, default=4)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="measure only --workload (the default also measures the other four)")
     ap.add_argument("--requests", type=int, default=None, help="keep only the first N requests (profiling)")
     ap.add_argument("--l2", choices=["auto", "flush", "none"], default="auto",
                     help="auto: flush L2 between steps only when the KV bytes are below 2 x L2")
@@ -646,20 +739,55 @@ def main():
         v, cores, desc = cpu_oracle_rate(inp, args.cpu_budget)
         v1, _, desc1 = cpu_oracle_rate(inp, args.cpu_budget / 3, threads=1)
         res["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                               "sample": desc, "one_thread": {"value": round(v1, 4), "sample": desc1}}
+                               "sample": desc, **host_cpu(),
+                               "one_thread": {"value": round(v1, 4), "sample": desc1}}
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
+def host_cpu() -> dict:
+    """Model string and hardware thread count of the host CPU the oracle runs on."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"cpu_model": model or platform.processor() or platform.machine(),
+            "hardware_concurrency": os.cpu_count(), "cpu_arch": platform.machine()}
+
+
 def bench_reference(args):
-    """The fp64 CPU oracle as the reference arm: W + K steps, each a bounded sample."""
+    """The fp64 CPU oracle as the reference arm: W + K steps, each a bounded sample.  Its
+    `config` is the one our arm prints for the same workload."""
     import oracle
     name = args.workload
     w = workloads.WORKLOADS[name]
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
-    inp = workloads.make_workload(name, device=dev)
+    inp = workloads.make_workload(name, device=dev, max_requests=args.requests)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if dev.type == "cuda":
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        _, l2_note = l2_policy(args, kv_bytes(inp), dev)
+    else:
+        sms, l2_note = 152, "no GPU visible"
+    config = workload_config(w, int(inp["seq_lens"].shape[0]), w.num_ctas(sms), args.min_tiles, kv_bytes(inp),
+                             l2_note, world)
     per_step = max(0.5, 150.0 / (args.steps + args.warmup))
     rates = []
     desc = ""
@@ -674,10 +802,10 @@ def bench_reference(args):
            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (seeded, as in workloads.py)",
-           "config": {"workload": w.description, "name": name},
+           "config": config,
            "impl": "reference",
            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": oracle.default_threads(),
-                            "kind": "oracle", "sample": f"per step: {desc}"},
+                            "kind": "oracle", "sample": f"per step: {desc}", **host_cpu()},
            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
 
