@@ -366,6 +366,10 @@ def measure_workload(dsa, device, name: str, args, rank: int, world: int, reps: 
            "static": static, "balance": cta_balance(dyn_times),
            "clocks": clocks.summary(t0, t1)}
     rec["decode_traffic_bytes"], rec["decode_traffic_source"] = profile_traffic(name, nbytes)
+    if w.kv_dtype == "fp8":
+        # multi-token verify steps over E4M3 K/V (q_len 2: mma.sync kernel; 6: tensor-memory kernel)
+        rec["multi_token"] = bench_multi(dsa, device, inp, w, sms, args.min_tiles, timer, max(10, min(reps, 30)),
+                                         nbytes, t_step)
     rec["gate"] = {"decode_ge_70pct_of_peak": rec["decode_frac_of_hbm_peak"] >= 0.70,
                    "faster_than_both_static_forms": all(v["speedup_of_dynamic"] > 1.0 for v in static.values())}
     return rec, step, timer, (t_plan, t_dec, t_comb)

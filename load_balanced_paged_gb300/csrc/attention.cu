@@ -6,7 +6,8 @@
 // Both run the same per-tile engine.
 //
 // Engine (per CTA):
-//   * one producer warp walks the descriptors, reads the page ids of the tiles
+//   * one producer warp (engine.cuh, shared with the tensor-memory multi-token kernel in
+//     attention_tc.cu) walks the descriptors, reads the page ids of the tiles
 //     from the block table (32 at a time, one per lane) and streams each
 //     (page, KV head) K and V block -- contiguous 16 KB (bf16) / 8 KB (E4M3) --
 //     into a ring of shared-memory stages with TMA (cp.async.bulk.tensor, 128-byte
@@ -34,219 +35,66 @@
 
 #include "common.h"
 #include "ptx.cuh"
+#include "engine.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-
-struct KernelParams {
-    const uint8_t *q;
-    const float *q_scale;
-    const float *k_scale;
-    const float *v_scale;
-    const int32_t *block_table;
-    const int32_t *seq_lens;
-    int32_t max_pages, num_pages, hq, hkv, G, num_units, max_slots;
-    int32_t q_len;      // query tokens per request (1: plain decode; > 1: multi-token verify)
-    int32_t slots_per_desc;  // partial slots per descriptor (2 for the tensor-core multi-token path)
-    int32_t page_size;       // tokens per page P (16, 32 or 64); a 64-token tile spans 64 / P pages
-    int32_t nhd;             // pages laid out [num_pages][P][Hkv][d] instead of [num_pages][Hkv][P][d]
-    float score_scale;  // sm_scale * log2(e)
-    // persistent schedule
-    const int32_t *cta_desc_begin;
-    const int4 *descs;
-    // static schedule
-    int32_t static_mode, static_tiles, num_splits;
-    float *partial_o;
-    float *partial_lse;
-    int32_t *status;
-    // fused combine (dsa_decode_fused)
-    const int32_t *unit_partial_begin;
-    const int32_t *unit_num_partials;
-    int32_t *unit_counters;  // [B * Hkv]: partials of the unit published so far; 0 between steps
-    void *out;               // [B, Hq, 128] bf16 or fp32
-    int32_t out_bf16;
-    float *out_lse;          // [B, Hq] or null
-    uint64_t *cta_times;     // null, or [CTAs][2]: %globaltimer ns when a CTA starts work and ends
-};
-
-// Stamps the end of a CTA's work: every warp raises the CTA's end time as it leaves.
-struct EndStamp {
-    uint64_t *at;
-    __device__ ~EndStamp() {
-        if (at && (threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned long long *>(at), globaltimer_ns());
-    }
-};
-
-template <int KV>
-struct Cfg;
-template <>
-struct Cfg<0> {  // bf16 K/V and Q
-    static constexpr int kTileBytes = kTile * kHeadDim * 2;
-    static constexpr int kScaleBytes = 0;
-    static constexpr int kQHeadBytes = kHeadDim * 2;
-};
-template <>
-struct Cfg<1> {  // E4M3 K/V and Q, fp32 scales
-    static constexpr int kTileBytes = kTile * kHeadDim;
-    static constexpr int kScaleBytes = kTile * 4;
-    static constexpr int kQHeadBytes = kHeadDim;
-};
-
-constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
-
 constexpr int kEpiRing = 8;  // merged descriptors the epilogue warp may lag behind (fused combine)
-constexpr int kMaxRows = 64; // query rows (query tokens x G) of one unit in a multi-token step
-constexpr int kDescInfoBytes = 80;
-constexpr int kMaxPagesPerTile = kTile / 16;  // pages of 16 tokens: four per tile
 
 // QW = 0: one query token per request; the consumer groups take alternate tiles and all
-// warps of the CTA merge at each descriptor end.  QW = 3: multi-token queries on the
-// 5th-generation tensor cores: S = Q K^T and O = P V accumulate in tensor memory, two
-// teams of four softmax warps, a warp issuing S (and laying Q out as its operand), a warp
-// issuing P.V.  (An mma.sync kernel for up to 16 query rows per unit of bf16 K/V measured
-// 214-221 us on the mixed lengths against 191-195 us for the tensor-memory kernel at 2-16
-// rows: bf16 K/V always takes the tensor-memory kernel.)  E4M3 K/V above 16 rows takes it
-// too (S with E4M3 products, V widened to f16 in shared memory).  QW = 4: E4M3 K/V with up
-// to 16 rows on mma.sync, the one-token shape (groups on alternate tiles, 16 tokens per
-// warp) over two 8-row blocks; each group merges its warps into its own partial slot.
-// (There the tensor-memory kernel, bound by its per-tile chain, measured twice the time; an
-// mma.sync kernel giving each warp a 32-token half of every tile measured 1.1-1.6x the
-// tensor-memory kernel's time at 24-64 rows.)
+// warps of the CTA merge at each descriptor end.  QW = 4: multi-token queries over E4M3 K/V
+// with up to 16 query rows per unit on mma.sync, the one-token shape (groups on alternate
+// tiles, 16 tokens per warp) over two 8-row blocks; each group merges its warps into its own
+// partial slot.  (Other multi-token steps run on the tensor-memory kernel, attention_tc.cu:
+// for E4M3 K/V at up to 16 rows it measured twice the time of this one, bound by its per-tile
+// chain; an mma.sync kernel giving each warp a 32-token half of every tile measured 1.1-1.6x
+// the tensor-memory kernel's time at 24-64 rows.)
 template <int KV, int STAGES, int GROUPS, int MSLOTS = 2, int QW = 0>
 struct Layout {
     // descriptors handed ahead to the consumers (Q + info): with one query token a slot is
     // small, and more of them let the producer run ahead through runs of short descriptors
-    static constexpr int kQSlots = (QW == 0 || QW == 4) ? 4 : 2;
-    static constexpr bool kTc = QW == 3;
-    static constexpr int kNcw = GROUPS * 4;  // consumer warps (softmax warps for QW = 3)
-    static constexpr int kThreads = (kNcw + (kTc ? 3 : 1)) * 32;  // consumers + producer (+ MMA, Q warps)
+    static constexpr int kQSlots = 4;
+    static constexpr int kNcw = GROUPS * 4;  // consumer warps
+    static constexpr int kThreads = (kNcw + 1) * 32;  // consumers + producer
     static constexpr int kThreadsFused = (kNcw + 2) * 32;  // + epilogue warp (fused combine)
     static constexpr int kStageTx = 2 * Cfg<KV>::kTileBytes + 2 * Cfg<KV>::kScaleBytes;
-    // QW = 3 with E4M3: each stage also holds its V widened to f16 ([half][64 rows][128 B],
-    // 128-byte swizzle: the P.V operand layout of a bf16 V tile)
-    static constexpr int kVcOff = round_up(kStageTx, 1024);
-    static constexpr int kStageBytes = kVcOff + (kTc && KV == 1 ? kTile * kHeadDim * 2 : 0);
-    static constexpr int kQRows = QW == 0 ? kMaxGroup : (QW == 4 ? 16 : kMaxRows);
+    static constexpr int kStageBytes = round_up(kStageTx, 1024);
+    static constexpr int kQRows = QW == 0 ? kMaxGroup : 16;
     static constexpr int kQSlot = kQRows * Cfg<KV>::kQHeadBytes;
     static constexpr int kQOff = STAGES * kStageBytes;
     static constexpr int kOStride = 132;  // floats per head row of a warp's O (padding avoids bank conflicts)
     static constexpr int kWarpRows = QW == 4 ? 16 : kMaxGroup;  // rows of a warp's merge deposit
     static constexpr int kWarpFloats = kWarpRows * kOStride + 2 * kWarpRows;
-    // QW = 3: Q as the MMA's A operand (64 rows x 128, K-major with the 128-byte swizzle, two
-    // 64-column halves of 8 KB, as the TMA lays out a K tile), two buffers.
-    static constexpr int kQcOff = kQOff + kQSlots * kQSlot;
-    static constexpr int kQcBytes = kTc ? 2 * kMaxRows * Cfg<KV>::kQHeadBytes : 0;
-    static constexpr int kMergeOff = kQcOff + kQcBytes;
-    static constexpr bool kMerge = QW == 0 || QW == 4;  // warps merge their states in shared memory
-    static constexpr int kMergeSlot = kMerge ? kNcw * kWarpFloats : 0;  // floats per merge slot
-    static constexpr int kMergeBars = kMerge ? 2 : 0;  // merge_full / merge_done barriers each (QW = 4: per group)
-    static constexpr int kTcBars = kTc ? 22 : 0;  // s_full, s_free, p_full x4; o_done, o_free, qc_full, qc_free, qd_full x2
+    static constexpr int kMergeOff = kQOff + kQSlots * kQSlot;
+    static constexpr int kMergeSlot = kNcw * kWarpFloats;  // floats per merge slot
+    static constexpr int kMergeBars = 2;  // merge_full / merge_done barriers each (QW = 4: per group)
     static constexpr int kBarOff = kMergeOff + MSLOTS * kMergeSlot * 4;
-    // full, empty, qfull, qempty, merge_full, merge_done, epi_ready, epi_free, tensor-core barriers
-    static constexpr int kNumBars = 2 * STAGES + 2 * kQSlots + 2 * kMergeBars + 2 * kEpiRing + kTcBars;
+    // full, empty, qfull, qempty, merge_full, merge_done, epi_ready, epi_free
+    static constexpr int kNumBars = 2 * STAGES + 2 * kQSlots + 2 * kMergeBars + 2 * kEpiRing;
     static constexpr int kNValidOff = kBarOff + kNumBars * 8;
-    static constexpr int kAbortOff = kNValidOff + STAGES * 4;  // abort flag, then the TMEM base address
+    static constexpr int kAbortOff = kNValidOff + STAGES * 4;  // abort flag
     static constexpr int kInfoOff = round_up(kAbortOff + 16, 64);  // one DescInfo per Q slot
     static constexpr int kEpiOff = kInfoOff + kQSlots * kDescInfoBytes;  // kEpiRing EpiRecords + descriptor total
     static constexpr int kBytes = kEpiOff + kEpiRing * 16 + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static_assert(MSLOTS == 1 || MSLOTS == 2, "merge slots");
+    static_assert(QW == 0 || QW == 4, "kernel shapes");
     static_assert(QW == 0 || (MSLOTS == 1 && GROUPS == 2), "multi-token shapes");
-    static_assert(!kTc || kQcOff % 1024 == 0, "tensor-core operand buffers");
     // Each stage must be consumed by one group only: a group then meets the phases of its
     // stages' full barriers in order.  With stages shared by two groups, one group could wait
     // for phase k+1 while phase k is still pending, pass the parity test early and arrive on
     // the stage's empty barrier out of turn (an undefined mbarrier use that faults the GPU).
-    static_assert(!(QW == 0 || QW == 4) || STAGES % GROUPS == 0, "each stage must belong to one consumer group");
+    static_assert(STAGES % GROUPS == 0, "each stage must belong to one consumer group");
     static_assert(kStageBytes % 1024 == 0 && kQOff % 1024 == 0, "swizzled TMA boxes need 1024-byte alignment");
     static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
-
-struct Desc {
-    int u, t0, t1, slot;
-    bool ok;
-};
-
-// What the producer hands the consumers with each descriptor's Q (shared memory).
-struct DescInfo {
-    int end;      // 1: no more descriptors in this CTA
-    int b, h;     // request, KV head
-    int n;        // tiles
-    int slot;     // partial-output slot
-    int c_start;  // ring position of the descriptor's first tile
-    int np;       // partials of the descriptor's unit (fused combine)
-    int pbeg;     // first partial slot of the unit (fused combine)
-    int t0;       // first tile of the descriptor within its unit
-    int len;      // the request's KV length
-    int pad[2];
-    float qscale[kMaxGroup];  // E4M3: q_scale of the G query heads
-};
-static_assert(sizeof(DescInfo) == kDescInfoBytes, "DescInfo slot size");
 
 // What the consumers hand the epilogue warp with each merged descriptor (fused combine).
 struct EpiRecord {
     int b, h, np, pbeg;
 };
 
-template <bool PERSIST>
-__device__ __forceinline__ Desc get_desc(const KernelParams &p, int d_begin, int i, int t0s, int t1s) {
-    Desc x;
-    if (PERSIST) {
-        const int4 v = p.descs[d_begin + i];
-        x.u = v.x;
-        x.t0 = v.y;
-        x.t1 = v.z;
-        x.slot = d_begin + i;
-        x.ok = v.x >= 0 && v.x < p.num_units && v.y >= 0 && v.y <= v.z && x.slot < p.max_slots;
-    } else {
-        x.u = blockIdx.z * p.hkv + blockIdx.y;
-        x.t0 = t0s;
-        x.t1 = t1s;
-        x.slot = x.u * p.num_splits + blockIdx.x;
-        x.ok = true;
-    }
-    return x;
-}
-
-// Bounded wait on an mbarrier phase; gives up (false) when the CTA aborted or the
-// time limit passed (then it records the timeout and raises the abort flag).
-__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                             int32_t *status, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > limit_ns) {
-                atomicOr(status, DSA_DEV_TIMEOUT);
-                *abort_flag = 1;
-                return false;
-            }
-        }
-    }
-}
-
-// The same with the common case inline: a phase that has already completed costs one
-// non-blocking test, not a call (measured: 11% off the tensor-core multi-token kernel,
-// whose warps meet many completed barriers per tile).
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                           int32_t *status, uint64_t limit_ns = kWaitLimitNs) {
-    if (mbar_test_wait(bar, parity)) return true;
-    return wait_phase_slow(bar, parity, abort_flag, status, limit_ns);
-}
-
-// Wait used while draining after an abort: ignores the abort flag; gives up at `deadline`
-// (%globaltimer ns), shared by all the drain's waits.
-__device__ __noinline__ void drain_phase(uint32_t bar, uint32_t parity, uint64_t deadline) {
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() > deadline) return;
-    }
-}
 
 // E4M3 bytes {V[t][2g], V[t][2g+1], V[t+1][2g], V[t+1][2g+1]} -> f16x2 pairs over tokens
 // (t, t+1) for dims 2g (lo) and 2g+1 (hi).
@@ -374,15 +222,6 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
     auto merge_done = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + MB + s); };
     auto epi_ready = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 2 * MB + s); };
     auto epi_free = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * kQSlots + 2 * MB + kEpiRing + s); };
-    const uint32_t tc_bar0 = bar0 + 8u * (2 * STAGES + 2 * kQSlots + 2 * MB + 2 * kEpiRing);
-    auto s_full = [&](int b) { return tc_bar0 + 8u * b; };         // 4 S/P buffers
-    auto s_free = [&](int b) { return tc_bar0 + 8u * (4 + b); };
-    auto p_full = [&](int b) { return tc_bar0 + 8u * (8 + b); };
-    auto o_done = [&](int t) { return tc_bar0 + 8u * (12 + t); };  // 2 softmax teams
-    auto o_free = [&](int t) { return tc_bar0 + 8u * (14 + t); };
-    auto qc_full = [&](int b) { return tc_bar0 + 8u * (16 + b); };
-    auto qc_free = [&](int b) { return tc_bar0 + 8u * (18 + b); };
-    auto qd_full = [&](int b) { return tc_bar0 + 8u * (20 + b); };  // plain Q rows landed
     EpiRecord *epi_rec = reinterpret_cast<EpiRecord *>(smem + L::kEpiOff);
     volatile int *epi_total = reinterpret_cast<volatile int *>(smem + L::kEpiOff + kEpiRing * sizeof(EpiRecord));
     int *nvalid = reinterpret_cast<int *>(smem + L::kNValidOff);
@@ -394,32 +233,18 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            // one consumer group releases a stage; QW = 3: the S and PV warps
-            mbar_init(empty_bar(s), QW == 3 ? 2 : 4);
+            mbar_init(empty_bar(s), 4);  // one consumer group releases a stage
         }
         for (int s = 0; s < kQSlots; ++s) {
             mbar_init(qfull_bar(s), 1);
-            mbar_init(qempty_bar(s), QW == 3 ? NCW + 2 : NCW);  // every warp that reads the hand-off
+            mbar_init(qempty_bar(s), NCW);  // every warp that reads the hand-off
         }
-        if (QW == 3) {
-            for (int b = 0; b < 4; ++b) {
-                mbar_init(s_full(b), 1);  // S warp
-                mbar_init(s_free(b), 1);  // PV warp: the buffer's P has been read
-                mbar_init(p_full(b), 4);  // the owning softmax team
-            }
-            for (int b = 0; b < 2; ++b) {
-                mbar_init(o_done(b), 1);
-                mbar_init(o_free(b), 4);
-                mbar_init(qc_full(b), 1);
-                mbar_init(qc_free(b), 1);
-                mbar_init(qd_full(b), 1);
-            }
-        } else if (QW == 4) {
+        if (QW == 4) {
             for (int s = 0; s < 2; ++s) {  // one pair per consumer group
                 mbar_init(merge_full(s), 4);
                 mbar_init(merge_done(s), 4);
             }
-        } else if (QW == 0) {
+        } else {
             for (int s = 0; s < MSLOTS; ++s) {
                 mbar_init(merge_full(s), NCW);
                 mbar_init(merge_done(s), NCW);
@@ -486,291 +311,8 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
     }
 
     if (warp == NCW) {
-        // =========================== producer warp ===========================
-        // The CTA's descriptors are read 32 at a time (one per lane, with their
-        // lengths and Q scales); their tiles form one stream, mapped 32 at a time
-        // onto lanes, whose page ids are fetched one chunk ahead of the chunk whose
-        // TMA copies are being issued.  Lane 0 issues; the warp stays converged.
-        if (lane == 0) {
-            prefetch_tmap(&kmap);
-            prefetch_tmap(&vmap);
-        }
-        const uint64_t policy = policy_evict_first();
-        int c = 0;          // tiles issued so far (ring position)
-        int qi = 0;         // descriptors handed to the consumers
-        int q_issued = -1;  // hand-off index of the last Q copy issued
-        bool aborted = false;
-        for (int wbase = 0; wbase < d_count && !aborted; wbase += 32) {
-            // ---- window: descriptor wbase + lane
-            int wb = 0, wh = 0, wt0 = 0, wn = 0, wslot = 0, wlen = 0, wnp = 1, wpbeg = 0;
-            float wqs[kMaxGroup];
-#pragma unroll
-            for (int g = 0; g < kMaxGroup; ++g) wqs[g] = 0.f;
-            if (wbase + lane < d_count) {
-                const Desc x = get_desc<PERSIST>(p, d_begin, wbase + lane, st0, st1);
-                if (x.ok) {
-                    wb = x.u / p.hkv;
-                    wh = x.u - wb * p.hkv;
-                    wt0 = x.t0;
-                    wn = x.t1 - x.t0;
-                    wslot = x.slot;
-                    wlen = p.seq_lens[wb];
-                    if (FUSE) {
-                        wnp = p.unit_num_partials[x.u];
-                        wpbeg = p.unit_partial_begin[x.u];
-                    }
-                    if (wlen < 0 || wlen > p.max_pages * p.page_size) atomicOr(p.status, DSA_DEV_BAD_SEQLEN);
-                    if (KV == 1) {
-                        const float *qs = p.q_scale + static_cast<int64_t>(wb) * p.hq + wh * G;
-#pragma unroll
-                        for (int g = 0; g < kMaxGroup; ++g)
-                            if (g < G) wqs[g] = qs[g];
-                    }
-                    if (wn == 0) {  // no tiles: its partials are empty, the consumers never see it
-                        const int R = p.q_len * G;
-                        const int64_t s0 = static_cast<int64_t>(wslot) * p.slots_per_desc;
-                        for (int i = 0; i < p.slots_per_desc * R * kHeadDim; ++i)
-                            p.partial_o[s0 * R * kHeadDim + i] = 0.f;
-                        for (int g = 0; g < p.slots_per_desc * R; ++g) p.partial_lse[s0 * R + g] = -INFINITY;
-                    }
-                } else {
-                    atomicOr(p.status, DSA_DEV_BAD_MAP);
-                }
-            }
-            // stream offset of each descriptor in the window (exclusive scan of tile counts)
-            int incl = wn;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const int wstart = incl - wn;
-            const int wtotal = __shfl_sync(0xffffffffu, incl, 31);
-
-            // lane -> (descriptor, tile, page) for stream tile s0 + lane
-            // a 64-token tile spans ppt pages of P tokens: pages t * ppt .. t * ppt + ppt - 1
-            const int P = p.page_size, ppt = kTile / P;
-            auto map_chunk = [&](int s0, int &j, int &t, int (&pg)[kMaxPagesPerTile]) {
-                const int s = s0 + lane;
-                j = 0;
-#pragma unroll
-                for (int step = 16; step > 0; step >>= 1) {
-                    const int v = __shfl_sync(0xffffffffu, wstart, j + step);
-                    if (v <= s) j += step;
-                }
-                t = __shfl_sync(0xffffffffu, wt0, j) + (s - __shfl_sync(0xffffffffu, wstart, j));
-                const int bj = __shfl_sync(0xffffffffu, wb, j);
-#pragma unroll
-                for (int k = 0; k < kMaxPagesPerTile; ++k) {
-                    const int idx = t * ppt + k;
-                    pg[k] = -1;
-                    if (k < ppt && s < wtotal && idx < p.max_pages)
-                        pg[k] = p.block_table[static_cast<int64_t>(bj) * p.max_pages + idx];
-                }
-            };
-
-            int cj = 0, ct = 0, cpg[kMaxPagesPerTile];
-#pragma unroll
-            for (int k = 0; k < kMaxPagesPerTile; ++k) cpg[k] = -1;
-            if (wtotal > 0) map_chunk(0, cj, ct, cpg);
-            for (int s0 = 0; s0 < wtotal && !aborted; s0 += 32) {
-                int nj = 0, nt = 0, npg[kMaxPagesPerTile];
-#pragma unroll
-                for (int k = 0; k < kMaxPagesPerTile; ++k) npg[k] = -1;
-                if (s0 + 32 < wtotal) map_chunk(s0 + 32, nj, nt, npg);  // next chunk's page ids in flight
-                const int cnt = min(32, wtotal - s0);
-                // ---- per-lane view of this lane's own tile (stream tile s0 + lane)
-                const int h_l = __shfl_sync(0xffffffffu, wh, cj);
-                const int len_l = __shfl_sync(0xffffffffu, wlen, cj);
-                const int t0_l = __shfl_sync(0xffffffffu, wt0, cj);
-                const bool first_l = lane < cnt && ct == t0_l;
-                int nv_l = 0;
-                if (lane < cnt) {
-                    const bool len_ok = len_l >= 0 && len_l <= p.max_pages * P;
-                    nv_l = len_ok ? min(kTile, len_l - ct * kTile) : 0;
-                    if (nv_l < 0 || ct * ppt >= p.max_pages) nv_l = 0;
-                    // the pages holding the tile's valid tokens must be inside the pool
-                    bool bad = false;
-#pragma unroll
-                    for (int k = 0; k < kMaxPagesPerTile; ++k)
-                        if (k * P < nv_l && (cpg[k] < 0 || cpg[k] >= p.num_pages)) bad = true;
-                    if (nv_l > 0 && bad) {
-                        atomicOr(p.status, DSA_DEV_BAD_PAGE);
-                        nv_l = 0;
-                    }
-                }
-                const uint32_t starts = __ballot_sync(0xffffffffu, first_l);
-                // ---- one converged loop over the chunk.  Lane l issues its tile the moment
-                //      its ring stage is free, once the tile STAGES positions earlier has been
-                //      issued (so the parity it tests names exactly the release it needs);
-                //      descriptors starting in the chunk are handed to the consumers in order,
-                //      each as soon as a hand-off slot is free.  Nothing waits in a divergent
-                //      loop: lanes spinning on their own barriers starved one another.
-                bool pend = lane < cnt;
-                uint32_t todo = starts;  // descriptor starts not yet handed off
-                const int cl = c + lane;
-                const int stage = cl % STAGES;
-                const uint32_t epar = ((cl / STAGES) & 1) ^ 1;
-                uint64_t idle_t0 = globaltimer_ns();  // last progress
-                for (uint32_t it = 1;; ++it) {
-                    const uint32_t done = __ballot_sync(0xffffffffu, !pend);
-                    if (done == 0xffffffffu && todo == 0) break;
-                    bool progress = false;
-                    int hand = 0;  // a hand-off slot is free for the next descriptor
-                    if (todo && lane == 0) hand = mbar_test_wait(qempty_bar(qi % kQSlots), ((qi / kQSlots) & 1) ^ 1);
-                    if (__shfl_sync(0xffffffffu, hand, 0)) {
-                        // next descriptor to hand off starts at chunk lane k
-                        const int k = __ffs(todo) - 1;
-                        const int j = __shfl_sync(0xffffffffu, cj, k);
-                        float qs[kMaxGroup];
-#pragma unroll
-                        for (int g = 0; g < kMaxGroup; ++g) qs[g] = __shfl_sync(0xffffffffu, wqs[g], j);
-                        const int b = __shfl_sync(0xffffffffu, wb, j);
-                        const int h = __shfl_sync(0xffffffffu, wh, j);
-                        const int n = __shfl_sync(0xffffffffu, wn, j);
-                        const int slot = __shfl_sync(0xffffffffu, wslot, j);
-                        const int np = __shfl_sync(0xffffffffu, wnp, j);
-                        const int pbeg = __shfl_sync(0xffffffffu, wpbeg, j);
-                        const int dt0 = __shfl_sync(0xffffffffu, wt0, j);
-                        const int dlen = __shfl_sync(0xffffffffu, wlen, j);
-                        const int qs_ = qi % kQSlots;
-                        if (lane == 0) {
-                            const int c_desc = c + k;  // ring position of the descriptor's first tile
-                            DescInfo *inf = reinterpret_cast<DescInfo *>(smem + L::kInfoOff) + qs_;
-                            inf->end = 0;
-                            inf->b = b;
-                            inf->h = h;
-                            inf->n = n;
-                            inf->slot = slot;
-                            inf->c_start = c_desc;
-                            inf->np = np;
-                            inf->pbeg = pbeg;
-                            inf->t0 = dt0;
-                            inf->len = dlen;
-#pragma unroll
-                            for (int g = 0; g < kMaxGroup; ++g) inf->qscale[g] = qs[g];
-                            // the G query rows of each of the request's q_len query tokens,
-                            // one after the other (row i*G + g)
-                            if (QW == 3) {  // the S warp fetches Q itself, a descriptor ahead
-                                mbar_arrive(qfull_bar(qs_));
-                            } else {
-                                const uint32_t bytes = G * C::kQHeadBytes;
-                                mbar_arrive_expect_tx(qfull_bar(qs_), bytes * p.q_len);
-                                for (int i = 0; i < p.q_len; ++i) {
-                                    const uint8_t *src = p.q + ((static_cast<int64_t>(b) * p.q_len + i) * p.hq + h * G) *
-                                                                   C::kQHeadBytes;
-                                    bulk_load(sbase + L::kQOff + qs_ * L::kQSlot + i * bytes, src, bytes,
-                                              qfull_bar(qs_));
-                                }
-                                q_issued = qi;
-                            }
-                        }
-                        ++qi;
-                        todo &= todo - 1;
-                        progress = true;
-                    }
-                    // a lane may test its stage once the tile STAGES positions earlier is issued
-                    const bool ready = pend && (lane < STAGES || ((done >> (lane - STAGES)) & 1u));
-                    if (ready && mbar_test_wait(empty_bar(stage), epar)) {
-                        pend = false;
-                        nvalid[stage] = nv_l;
-                        const uint32_t fb = full_bar(stage);
-                        if (nv_l > 0) {
-                            const uint32_t kdst = sbase + stage * L::kStageBytes;
-                            const uint32_t vdst = kdst + C::kTileBytes;
-                            // the pages holding valid tokens, one box of P rows each (both 128-B
-                            // halves of a bf16 row: the stage is [page][half][P rows][128 B]);
-                            // the tensor-core kernel's operands want [half][64 rows][128 B],
-                            // so there each half of a page smaller than the tile is its own box
-                            if (P == kTile) {  // one page per tile: the common case, no loop
-                                mbar_arrive_expect_tx(fb, L::kStageTx);
-                                tma_load_5d(kdst, &kmap, fb, 0, 0, 0, h_l, cpg[0], policy);
-                                tma_load_5d(vdst, &vmap, fb, 0, 0, 0, h_l, cpg[0], policy);
-                                if (KV == 1) {
-                                    const int64_t srow = (static_cast<int64_t>(cpg[0]) * p.hkv + h_l) * kTile;
-                                    bulk_load(vdst + C::kTileBytes, p.k_scale + srow, C::kScaleBytes, fb);
-                                    bulk_load(vdst + C::kTileBytes + C::kScaleBytes, p.v_scale + srow, C::kScaleBytes, fb);
-                                }
-                            } else {
-                                const int nsub = (nv_l + P - 1) / P;
-                                mbar_arrive_expect_tx(fb, nsub * (L::kStageTx / ppt));
-#pragma unroll
-                                for (int k = 0; k < kMaxPagesPerTile; ++k) {
-                                    if (k >= nsub) break;
-                                    const int pg = cpg[k];
-                                    if (QW == 3 && KV == 0 && P < kTile) {
-                                        const uint32_t ro = static_cast<uint32_t>(k * P) * 128u;
-                                        tma_load_5d(kdst + ro, &kmap, fb, 0, 0, 0, h_l, pg, policy);
-                                        tma_load_5d(kdst + C::kTileBytes / 2 + ro, &kmap, fb, 0, 0, 1, h_l, pg, policy);
-                                        tma_load_5d(vdst + ro, &vmap, fb, 0, 0, 0, h_l, pg, policy);
-                                        tma_load_5d(vdst + C::kTileBytes / 2 + ro, &vmap, fb, 0, 0, 1, h_l, pg, policy);
-                                    } else {
-                                        const uint32_t ro = static_cast<uint32_t>(k * P) * (C::kTileBytes / kTile);
-                                        tma_load_5d(kdst + ro, &kmap, fb, 0, 0, 0, h_l, pg, policy);
-                                        tma_load_5d(vdst + ro, &vmap, fb, 0, 0, 0, h_l, pg, policy);
-                                    }
-                                    if (KV == 1) {
-                                        const int64_t srow = (static_cast<int64_t>(pg) * p.hkv + h_l) * P;
-                                        bulk_load(vdst + C::kTileBytes + 4 * k * P, p.k_scale + srow, 4 * P, fb);
-                                        bulk_load(vdst + C::kTileBytes + C::kScaleBytes + 4 * k * P, p.v_scale + srow,
-                                                  4 * P, fb);
-                                    }
-                                }
-                            }
-                        } else {
-                            mbar_arrive(fb);
-                        }
-                    }
-                    if (__any_sync(0xffffffffu, ready && !pend)) progress = true;
-                    if (progress) {
-                        idle_t0 = globaltimer_ns();
-                    } else if ((it & 31u) == 0) {  // bounded wait
-                        int ab = 0;
-                        if (lane == 0) {
-                            if (*abort_flag) {
-                                ab = 1;
-                            } else if (globaltimer_ns() - idle_t0 > kWaitLimitNs) {
-                                atomicOr(p.status, DSA_DEV_TIMEOUT);
-                                *abort_flag = 1;
-                                ab = 1;
-                            }
-                        }
-                        if (__shfl_sync(0xffffffffu, ab, 0)) {
-                            aborted = true;
-                            break;
-                        }
-                    }
-                }
-                if (aborted) {
-                    // tiles up to the last one issued are counted for the drain below
-                    const uint32_t done = __ballot_sync(0xffffffffu, !pend && lane < cnt);
-                    c += done ? 32 - __clz(done) : 0;
-                    break;
-                }
-                c += cnt;
-                cj = nj;
-                ct = nt;
-#pragma unroll
-                for (int k = 0; k < kMaxPagesPerTile; ++k) cpg[k] = npg[k];
-            }
-        }
-        if (FUSE && lane == 0) *epi_total = qi;  // descriptors handed off (the epilogue's count)
-        if (!aborted && lane == 0) {
-            // end marker for the consumers
-            if (wait_phase(qempty_bar(qi % kQSlots), ((qi / kQSlots) & 1) ^ 1, abort_flag, p.status)) {
-                reinterpret_cast<DescInfo *>(smem + L::kInfoOff)[qi % kQSlots].end = 1;
-                mbar_arrive(qfull_bar(qi % kQSlots));
-            } else {
-                aborted = true;
-            }
-        }
-        if (aborted && lane == 0) {
-            // let every copy this CTA started land before the CTA exits
-            const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
-            for (int cc = max(0, c - STAGES); cc < c; ++cc)
-                drain_phase(full_bar(cc % STAGES), (cc / STAGES) & 1, deadline);
-            if (q_issued >= 0) drain_phase(qfull_bar(q_issued % kQSlots), (q_issued / kQSlots) & 1, deadline);
-        }
+        producer_warp<KV, STAGES, PERSIST, FUSE, false, L>(&kmap, &vmap, p, smem, sbase, bar0, nvalid, abort_flag,
+                                                           epi_total, d_begin, d_count, st0, st1, lane);
         return;
     }
 
@@ -819,609 +361,7 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
         }
     }
 
-    if constexpr (QW == 3) {
-        // ============ multi-token queries on the 5th-generation tensor cores ============
-        // Rows r = i * G + g (query token i, head g), r < R = q_len * G <= 64.  Per tile:
-        //   S[64 x 64] = Qc . K^T in one of two 64-column TMEM buffers (M = 64: row r sits in
-        //   lane 32 (r / 16) + r % 16, i.e. lanes 0-15 of each warp's 32-lane quarter);
-        //   the softmax thread of row r (lane r % 16 of warp r / 16) masks it (causal within
-        //   the draft, past the length), keeps the running max m, raised lazily (O is
-        //   rescaled only when the max grows by more than 8 in base 2), and writes P =
-        //   2^(s - m) as bf16 high and low parts;
-        //   O[64 x 128] += P_hi . V + P_lo . V in TMEM columns 128-255.
-        // Two warps issue the products: the S warp runs ahead (two S buffers) as stages land,
-        // the PV warp follows the softmax; each releases its half of a ring stage (K, V) when
-        // its products have read it, so the softmax of tile g overlaps the products of its
-        // neighbours and no product waits for an unrelated load.
-        const int R = p.q_len * G;
-        uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kAbortOff + 4);
-        constexpr int kTcThreads = (NCW + 2) * 32;  // softmax warps, S warp, PV warp
-        constexpr uint32_t kQcBuf = kMaxRows * C::kQHeadBytes;
-        if (warp == NCW + 1) tmem_alloc(smem_u32(tmem_slot), 512);
-        tc_fence_before();
-        named_bar_sync(1, kTcThreads);
-        tc_fence_after();
-        const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
-        // Q K-major, K K-major (bf16, or E4M3 with kind::f8f6f4); P K-major, V M/N-major
-        // (bf16, or f16 for E4M3 K/V: V widened exactly, P carrying the V scale)
-        constexpr uint32_t kIdS = KV == 0 ? umma_idesc_bf16(64, 64, 0, 0) : umma_idesc_fmt0(64, 64, 0, 0);
-        constexpr uint32_t kIdO = KV == 0 ? umma_idesc_bf16(64, 128, 0, 1) : umma_idesc_fmt0(64, 128, 0, 1);
-        bool failed = false;
-
-        if (warp == NCW + 1) {
-            // ---- S warp: fetches each descriptor's Q rows one descriptor ahead (plain rows
-            //      into one of two buffers), lays them out as the A operand (zero past R), then
-            //      issues S = Q K^T for its tiles as soon as a stage and an S buffer are ready
-            //      (lane 0 issues, the warp waits together); its commit on the stage's empty
-            //      barrier says the K half is no longer read
-            // descriptors of this CTA, 32 at a time: lane j holds the unit of descriptor wbase + j
-            // if the producer hands it over (valid, with tiles), else -1
-            int wbase = 0, wu = -1;
-            auto load_window = [&](int base) {
-                wbase = base;
-                wu = -1;
-                if (base + lane < d_count) {
-                    const int4 v = p.descs[d_begin + base + lane];
-                    if (v.x >= 0 && v.x < p.num_units && v.y >= 0 && v.y < v.z && d_begin + base + lane < p.max_slots)
-                        wu = v.x;
-                }
-            };
-            load_window(0);
-            auto next_desc = [&](int after) {  // the next handed-over descriptor (raw slot) after `after`
-                for (int rel = after - d_begin + 1; rel < d_count;) {
-                    if (rel < wbase || rel >= wbase + 32) load_window(rel & ~31);
-                    const uint32_t m = __ballot_sync(0xffffffffu, wu >= 0) & (~0u << (rel - wbase));
-                    if (m) return d_begin + wbase + __ffs(m) - 1;
-                    rel = wbase + 32;
-                }
-                return -1;
-            };
-            int fetched[2] = {0, 0};  // Q copies issued into each plain buffer (each one waited for)
-            auto fetch_q = [&](int x, int j) {  // x in the current window
-                const int u = __shfl_sync(0xffffffffu, wu, x - d_begin - wbase);
-                if (lane == 0) {
-                    const int b = u / p.hkv, h = u - b * p.hkv;
-                    const uint32_t bytes = G * C::kQHeadBytes;
-                    mbar_arrive_expect_tx(qd_full(j), bytes * p.q_len);
-                    for (int i = 0; i < p.q_len; ++i)
-                        bulk_load(sbase + L::kQOff + j * L::kQSlot + i * bytes,
-                                  p.q + ((static_cast<int64_t>(b) * p.q_len + i) * p.hq + h * G) * C::kQHeadBytes, bytes,
-                                  qd_full(j));
-                }
-                ++fetched[j];
-            };
-            auto land_q = [&](int j) { return wait_phase(qd_full(j), (fetched[j] - 1) & 1, abort_flag, p.status); };
-            int pf_slot = next_desc(d_begin - 1), pf_buf = 0;  // the descriptor whose Q is in flight
-            if (pf_slot >= 0) fetch_q(pf_slot, 0);
-            int g = 0, last_d = -1;
-            for (int d = 0;; ++d) {
-                const int qslot = d % kQSlots;
-                if (!wait_phase(qfull_bar(qslot), (d / kQSlots) & 1, abort_flag, p.status)) {
-                    failed = true;
-                    break;
-                }
-                const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
-                const int end = inf->end, n = inf->n, c_start = inf->c_start, xs = inf->slot;
-                if (!end) {
-                    // this descriptor's Q: normally the prefetched one; otherwise fetched now
-                    const int qb = pf_buf;
-                    if (pf_slot != xs) {
-                        if (pf_slot >= 0 && !land_q(qb)) {
-                            failed = true;
-                            break;
-                        }
-                        if (xs < d_begin + wbase || xs >= d_begin + wbase + 32) load_window((xs - d_begin) & ~31);
-                        fetch_q(xs, qb);
-                    }
-                    if (!land_q(qb) || !wait_phase(qc_free(d & 1), ((d >> 1) & 1) ^ 1, abort_flag, p.status)) {
-                        pf_slot = -1;  // consumed (or abandoned with the CTA)
-                        failed = true;
-                        break;
-                    }
-                    const uint8_t *src = smem + L::kQOff + qb * L::kQSlot;
-                    uint8_t *dst = smem + L::kQcOff + (d & 1) * kQcBuf;
-                    if constexpr (KV == 0) {
-                    // 128-byte-swizzled K-major operand (as the TMA lays out K): dims 64 b .. 64 b + 63
-                    // of row r at b * 8 KB + r * 128 B, 16-byte chunk c at (c ^ (r % 8)) * 16.  Each
-                    // quarter-warp writes one 128-byte row: no bank conflicts either way.
-#pragma unroll
-                    for (int rd = 0; rd < 4; ++rd) {
-                        uint4 v[8];
-#pragma unroll
-                        for (int it = 0; it < 8; ++it) {  // chunk kc of row r
-                            const int i = lane + 32 * (8 * rd + it), r = i >> 4, kc = i & 15;
-                            v[it] = r < R ? *reinterpret_cast<const uint4 *>(src + r * (kHeadDim * 2) + kc * 16)
-                                          : make_uint4(0u, 0u, 0u, 0u);
-                        }
-#pragma unroll
-                        for (int it = 0; it < 8; ++it) {
-                            const int i = lane + 32 * (8 * rd + it), r = i >> 4, kc = i & 15;
-                            *reinterpret_cast<uint4 *>(dst + (kc >> 3) * 8192 + r * 128 + (((kc & 7) ^ (r & 7)) << 4)) = v[it];
-                        }
-                    }
-                    } else {
-                    // E4M3: a row is one 128-byte swizzle row (r * 128 B, chunk c at (c ^ (r % 8)) * 16)
-#pragma unroll
-                    for (int rd = 0; rd < 2; ++rd) {
-                        uint4 v[8];
-#pragma unroll
-                        for (int it = 0; it < 8; ++it) {  // chunk kc of row r
-                            const int i = lane + 32 * (8 * rd + it), r = i >> 3, kc = i & 7;
-                            v[it] = r < R ? *reinterpret_cast<const uint4 *>(src + r * kHeadDim + kc * 16)
-                                          : make_uint4(0u, 0u, 0u, 0u);
-                        }
-#pragma unroll
-                        for (int it = 0; it < 8; ++it) {
-                            const int i = lane + 32 * (8 * rd + it), r = i >> 3, kc = i & 7;
-                            *reinterpret_cast<uint4 *>(dst + r * 128 + ((kc ^ (r & 7)) << 4)) = v[it];
-                        }
-                    }
-                    }
-                    fence_proxy_async_smem();
-                    // the next descriptor's Q lands while this one's tiles are worked on
-                    pf_slot = next_desc(xs);
-                    if (pf_slot >= 0) {
-                        pf_buf = qb ^ 1;
-                        fetch_q(pf_slot, pf_buf);
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(qempty_bar(qslot));
-                if (end) break;
-                const uint32_t qa = sbase + L::kQcOff + (d & 1) * kQcBuf;
-                for (int li = 0; li < n; ++li, ++g) {
-                    const int c = c_start + li, stage = c % STAGES, buf = g & 3;
-                    if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status) ||
-                        !wait_phase(s_free(buf), ((g >> 2) & 1) ^ 1, abort_flag, p.status)) {
-                        failed = true;
-                        break;
-                    }
-                    const int nv = nvalid[stage];
-                    if (lane == 0) {
-                        if (nv > 0) {
-                            tc_fence_after();
-                            const uint32_t kb = sbase + stage * L::kStageBytes;
-                            if constexpr (KV == 0) {
-#pragma unroll
-                                for (int ks = 0; ks < 8; ++ks)
-                                    umma_bf16(tmem + 64 * buf, umma_desc(qa + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, 2),
-                                              umma_desc(kb + (ks >> 2) * (C::kTileBytes / 2) + (ks & 3) * 32, 16, 1024, 2),
-                                              kIdS, ks > 0);
-                            } else {  // E4M3: 32 dims (32 bytes) per product
-#pragma unroll
-                                for (int ks = 0; ks < 4; ++ks)
-                                    umma_e4m3(tmem + 64 * buf, umma_desc(qa + ks * 32, 16, 1024, 2),
-                                              umma_desc(kb + ks * 32, 16, 1024, 2), kIdS, ks > 0);
-                            }
-                            umma_commit(s_full(buf));
-                            umma_commit(empty_bar(stage));
-                        } else {
-                            mbar_arrive(s_full(buf));
-                            mbar_arrive(empty_bar(stage));
-                        }
-                    }
-                    __syncwarp();
-                }
-                if (failed) break;
-                if (lane == 0) umma_commit(qc_free(d & 1));  // the descriptor's S products have read Qc
-                __syncwarp();
-                last_d = d;
-            }
-            // the last commit lands once every product this warp issued has completed; a Q copy
-            // still in flight lands before the CTA leaves
-            if (!failed && last_d >= 0) wait_phase(qc_free(last_d & 1), (last_d >> 1) & 1, abort_flag, p.status);
-            if (pf_slot >= 0) {
-                const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
-                drain_phase(qd_full(pf_buf), (fetched[pf_buf] - 1) & 1, deadline);
-            }
-        } else if (warp == NCW + 2) {
-            // ---- PV warp: O += P_hi . V + P_lo . V as soon as the softmax warps hand P over;
-            //      its commit on the stage's empty barrier says the V half is no longer read
-            int g = 0;
-            for (int d = 0;; ++d) {
-                const int qslot = d % kQSlots;
-                if (!wait_phase(qfull_bar(qslot), (d / kQSlots) & 1, abort_flag, p.status)) {
-                    failed = true;
-                    break;
-                }
-                const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
-                const int end = inf->end, n = inf->n, c_start = inf->c_start;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(qempty_bar(qslot));
-                if (end) break;
-                bool first_pv[2] = {true, true};  // per softmax team (tile parity): O_t not yet written
-                for (int li = 0; li < n; ++li, ++g) {
-                    const int c = c_start + li, stage = c % STAGES, buf = g & 3, t = g & 1;
-                    if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status) ||
-                        !wait_phase(p_full(buf), (g >> 2) & 1, abort_flag, p.status)) {
-                        failed = true;
-                        break;
-                    }
-                    const int nv = nvalid[stage];
-                    if (nv > 0) {
-                        // O_t is free once team t has read out the previous descriptor's
-                        if (first_pv[t] && !wait_phase(o_free(t), (d & 1) ^ 1, abort_flag, p.status)) {
-                            failed = true;
-                            break;
-                        }
-                        if (lane == 0) {
-                            tc_fence_after();
-                            // bf16: V as loaded, P high part in columns 0-31, low part in 32-63;
-                            // E4M3: V widened to f16 by the softmax team, P (f16) in columns 0-31
-                            const uint32_t vb = sbase + stage * L::kStageBytes + (KV == 0 ? C::kTileBytes : L::kVcOff);
-                            const uint32_t pt = tmem + 64 * buf;
-                            const uint32_t od = tmem + 256 + 128 * t;
-#pragma unroll
-                            for (int ks = 0; ks < 4; ++ks) {
-                                const uint64_t bd = umma_desc(vb + ks * 2048, 8192, 1024, 2);
-                                umma_bf16_ta(od, pt + 8 * ks, bd, kIdO, !(first_pv[t] && ks == 0));
-                                if (KV == 0) umma_bf16_ta(od, pt + 32 + 8 * ks, bd, kIdO, true);
-                            }
-                        }
-                        first_pv[t] = false;
-                    }
-                    // commits, not arrives: a phase also means every earlier product is done
-                    if (lane == 0) {
-                        umma_commit(o_done(t));
-                        umma_commit(s_free(buf));
-                        umma_commit(empty_bar(stage));
-                    }
-                    __syncwarp();
-                }
-                if (failed) break;
-            }
-        } else {
-            // ---- softmax warps: two teams of four (team t = warps 4t .. 4t + 3) take the tiles
-            //      of parity t (S/P buffers t and t + 2 in turn, O_t).  Warp w reads the 16 rows
-            //      16 (w & 3) .. + 15
-            //      (M = 64 accumulators: lanes 0-15 of each sub-partition) as m16n8 fragments:
-            //      thread (gid = lane / 4, tig = lane % 4) holds rows ra = 16 (w & 3) + gid and
-            //      rb = ra + 8, columns 8 k + 2 tig, + 1; a row's max and sum combine over the
-            //      four threads of its quad.  At each descriptor end each team writes its own
-            //      partial (slot 2 x descriptor + team); the combine merges them with the others.
-            const int team = warp >> 2, sp = warp & 3;
-            const int gid = lane >> 2, tig = lane & 3;
-            const int ra = 16 * sp + gid, rb = ra + 8;
-            const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
-            const uint32_t o_col = 256 + 128 * team;
-            const int tid = sp * 32 + lane;  // within the team
-            // The descriptor end of a team (its partial, slot 2 x descriptor + team), deferred
-            // until the team has handed over the P of its first tile of the next descriptor: a
-            // descriptor's first tile never rescales O, so it need not wait for the previous
-            // descriptor's last P.V, and the team computes it while that P.V completes.
-            float ep_vref = 1.f;  // E4M3: the V scale reference of the deferred descriptor end
-            auto team_epilogue = [&](int slot, float (&m)[2], float (&l)[2], int pv_desc, int last_g) -> bool {
-                // ---- this team's products of the descriptor are done once its last tile's buffer
-                //      phase is (that commit covers every earlier product)
-                if (last_g >= 0) {
-                    if (!wait_phase(o_done(team), (last_g >> 1) & 1, abort_flag, p.status)) return false;
-                    tc_fence_after();
-                }
-                // ---- this team's partial (slot 2 x descriptor + team): O_t / l, lse = ln(2) (m + log2 l)
-                float inv[2], lse[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
-                    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
-                    if constexpr (KV == 0)
-                        inv[h] = l[h] > 0.f ? 1.f / l[h] : 0.f;
-                    else
-                        inv[h] = l[h] > 0.f ? ep_vref / l[h] : 0.f;
-                    lse[h] = l[h] > 0.f ? (m[h] + lg2(l[h])) * kLn2 : -INFINITY;
-                }
-                const int64_t slot_row = (2 * static_cast<int64_t>(slot) + team) * R;
-                float *dst_a = p.partial_o + (slot_row + ra) * kHeadDim + 2 * tig;
-                float *dst_b = p.partial_o + (slot_row + rb) * kHeadDim + 2 * tig;
-                // O_t into registers first, then release it for the next descriptor's products
-                float o[16][4];
-                if (pv_desc > 0) {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) tmem_ld16x8(tmem + lane_base + o_col + 8 * k, o[k]);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(o_free(team));
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    if (ra < R) *reinterpret_cast<float2 *>(dst_a + 8 * k) = make_float2(o[k][0] * inv[0], o[k][1] * inv[0]);
-                    if (rb < R) *reinterpret_cast<float2 *>(dst_b + 8 * k) = make_float2(o[k][2] * inv[1], o[k][3] * inv[1]);
-                }
-                if (tig == 0) {
-                    if (ra < R) p.partial_lse[slot_row + ra] = lse[0];
-                    if (rb < R) p.partial_lse[slot_row + rb] = lse[1];
-                }
-                return true;
-            };
-            bool ep_pending = false;
-            int ep_slot = 0, ep_pv = 0, ep_last_g = -1;
-            float ep_m[2] = {0.f, 0.f}, ep_l[2] = {0.f, 0.f};
-            auto flush_epilogue = [&]() -> bool {
-                if (!ep_pending) return true;
-                ep_pending = false;
-                return team_epilogue(ep_slot, ep_m, ep_l, ep_pv, ep_last_g);
-            };
-            int g = 0;
-            for (int d = 0;; ++d) {
-                const int qslot = d % kQSlots;
-                if (!wait_phase(qfull_bar(qslot), (d / kQSlots) & 1, abort_flag, p.status)) {
-                    failed = true;
-                    break;
-                }
-                const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
-                const int end = inf->end, n = inf->n, slot = inf->slot, c_start = inf->c_start;
-                const int dt0 = inf->t0, len = inf->len;
-                int d_b = 0, d_h = 0;
-                if constexpr (KV == 1) d_b = inf->b, d_h = inf->h;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(qempty_bar(qslot));
-                if (end) {
-                    if (!flush_epilogue()) failed = true;
-                    break;
-                }
-                // visible tokens of each row: t < lim (-1: a row past R)
-                const int lim[2] = {ra < R ? len - p.q_len + ra / G + 1 : -1, rb < R ? len - p.q_len + rb / G + 1 : -1};
-                float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-                // E4M3: score factor per row (softmax scale x the row's q_scale), the V scale
-                // reference (the largest V scale seen, O holds the output divided by it) and its inverse
-                float qsc[2] = {p.score_scale, p.score_scale}, vref = 1.f, vinv = 1.f;
-                if constexpr (KV == 1) {
-                    const int rr[2] = {ra, rb};
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        if (rr[h] < R) {
-                            const int i = rr[h] / G;
-                            qsc[h] *= p.q_scale[(static_cast<int64_t>(d_b) * p.q_len + i) * p.hq + d_h * G + rr[h] - i * G];
-                        }
-                    vref = vinv = 0.f;
-                }
-                int pv_desc = 0, last_g = -1;
-                for (int li = 0; li < n; ++li, ++g) {
-                    if ((g & 1) != team) continue;
-                    const int c = c_start + li, stage = c % STAGES, buf = g & 3;
-                    if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status) ||
-                        !wait_phase(s_full(buf), (g >> 2) & 1, abort_flag, p.status)) {
-                        failed = true;
-                        break;
-                    }
-                    const int nv = nvalid[stage];
-                    tc_fence_after();
-                    float sv[8][4];  // [column block k][(ra, 2tig), (ra, 2tig+1), (rb, 2tig), (rb, 2tig+1)]
-                    if (nv > 0) {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + 64 * buf + 8 * k, sv[k]);
-                        tmem_wait_ld();
-                    }
-                    // this team's previous tile of the descriptor (-1: none; the first tile starts
-                    // from m = -inf and never rescales O).  Its P.V is waited for before this tile's
-                    // P is handed over (so the team stays within one phase of o_done, which the
-                    // descriptor end's wait needs), and before a rescale of O, which reads O.  (S of
-                    // this tile was issued after the P.V two team tiles back had released its
-                    // buffer, so until this tile's P is handed over the barrier is at most one
-                    // phase behind the one waited for.)
-                    const int prev_g = last_g;
-                    last_g = g;
-                    auto wait_prev_pv = [&]() {
-                        return prev_g < 0 || wait_phase(o_done(team), ((g >> 1) & 1) ^ 1, abort_flag, p.status);
-                    };
-                    if (nv == 0) {  // no data in this stage: the PV warp skips its P.V
-                        if (!wait_prev_pv()) {
-                            failed = true;
-                            break;
-                        }
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(p_full(buf));
-                        if (!flush_epilogue()) {
-                            failed = true;
-                            break;
-                        }
-                        continue;
-                    }
-                    // ---- E4M3: S times the K scale of its column; P's factor per column, the V
-                    //      scale over the reference, which moves only when a larger scale appears
-                    //      (O is then rescaled with the maxima below); columns past nv get 0
-                    float vw[8][2];
-                    float vf = 1.f;
-                    if constexpr (KV == 1) {
-                        const float *ksm = reinterpret_cast<const float *>(smem + stage * L::kStageBytes + 2 * C::kTileBytes);
-                        const float *vsm = ksm + kTile;
-                        float vmax = 0.f;
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const int j = 8 * k + 2 * tig;
-                            const float2 kk = *reinterpret_cast<const float2 *>(ksm + j);
-                            const float2 vv = *reinterpret_cast<const float2 *>(vsm + j);
-                            sv[k][0] *= kk.x;
-                            sv[k][1] *= kk.y;
-                            sv[k][2] *= kk.x;
-                            sv[k][3] *= kk.y;
-                            vw[k][0] = j < nv ? vv.x : 0.f;
-                            vw[k][1] = j + 1 < nv ? vv.y : 0.f;
-                            vmax = fmaxf(vmax, fmaxf(vw[k][0], vw[k][1]));
-                        }
-                        if (__any_sync(0xffffffffu, vmax > vref)) {  // the quad's four lanes cover the 64 columns
-                            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
-                            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
-                            if (vmax > vref) {
-                                if (vref > 0.f) vf = vref / vmax;  // from 0: nothing accumulated yet
-                                vref = vmax;
-                                vinv = 1.f / vmax;
-                            }
-                        }
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            vw[k][0] *= vinv;
-                            vw[k][1] *= vinv;
-                        }
-                    }
-                    // ---- running maximum over each row's visible tokens (t < lim, slot < nv)
-                    const int tt = (dt0 + li) * kTile;
-                    const int vis[2] = {max(0, min(nv, lim[0] - tt)), max(0, min(nv, lim[1] - tt))};
-                    const bool full = vis[0] == kTile && vis[1] == kTile;
-                    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int h = e >> 1, j = 8 * k + 2 * tig + (e & 1);
-                            mx[h] = fmaxf(mx[h], (full || j < vis[h]) ? sv[k][e] : -INFINITY);
-                        }
-                    bool grow[2];
-                    float alpha[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-                        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-                        const float mnew = fmaxf(m[h], mx[h] * (KV == 0 ? p.score_scale : qsc[h]));
-                        grow[h] = m[h] != -INFINITY && mnew > m[h] + 8.f;
-                        alpha[h] = grow[h] ? ex2(m[h] - mnew) : 1.f;
-                        if (grow[h] || m[h] == -INFINITY) m[h] = mnew;
-                    }
-                    if (__any_sync(0xffffffffu, grow[0] || grow[1] || (KV == 1 && vf != 1.f))) {
-                        // rows whose maximum grew: O_team *= 2^(m_old - m_new); E4M3: all rows also
-                        // by the V scale reference's change (after the previous P.V into O_team)
-                        if (!wait_prev_pv()) {
-                            failed = true;
-                            break;
-                        }
-                        tc_fence_after();
-#pragma unroll 1  // rare: kept small for the instruction cache
-                        for (int half = 0; half < 2; ++half) {
-                            float o[8][4];
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + o_col + 64 * half + 8 * k, o[k]);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                if constexpr (KV == 0) {
-                                    o[k][0] *= alpha[0];
-                                    o[k][1] *= alpha[0];
-                                    o[k][2] *= alpha[1];
-                                    o[k][3] *= alpha[1];
-                                } else {
-                                    o[k][0] *= alpha[0] * vf;
-                                    o[k][1] *= alpha[0] * vf;
-                                    o[k][2] *= alpha[1] * vf;
-                                    o[k][3] *= alpha[1] * vf;
-                                }
-                                tmem_st16x8(tmem + lane_base + o_col + 64 * half + 8 * k, o[k]);
-                            }
-                            tmem_wait_st();
-                        }
-                        l[0] *= alpha[0];
-                        l[1] *= alpha[1];
-                    }
-                    // ---- P = 2^(s * scale - m) (0 where not visible) as bf16 high part (the top 16
-                    //      bits) and low part (the rest, rounded), written over S in the buffer: the
-                    //      P.V's A operand, tokens (2c, 2c + 1) packed in column c (high part:
-                    //      columns 0-31, low part: 32-63)
-                    const float nm0 = -m[0], nm1 = -m[1];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        float pv[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int h = e >> 1, j = 8 * k + 2 * tig + (e & 1);
-                            const float q = ex2(fmaf(sv[k][e], KV == 0 ? p.score_scale : qsc[h], h ? nm1 : nm0));
-                            pv[e] = (full || j < vis[h]) ? q : 0.f;
-                        }
-                        l[0] += pv[0] + pv[1];
-                        l[1] += pv[2] + pv[3];
-                        if constexpr (KV == 0) {
-                            const uint32_t h0 = __float_as_uint(pv[0]) & 0xFFFF0000u, h1 = __float_as_uint(pv[1]) & 0xFFFF0000u;
-                            const uint32_t h2 = __float_as_uint(pv[2]) & 0xFFFF0000u, h3 = __float_as_uint(pv[3]) & 0xFFFF0000u;
-                            tmem_st16x4(tmem + lane_base + 64 * buf + 4 * k, prmt(h0, h1, 0x7632u), prmt(h2, h3, 0x7632u));
-                            tmem_st16x4(tmem + lane_base + 64 * buf + 32 + 4 * k,
-                                        pack_bf16x2(pv[0] - __uint_as_float(h0), pv[1] - __uint_as_float(h1)),
-                                        pack_bf16x2(pv[2] - __uint_as_float(h2), pv[3] - __uint_as_float(h3)));
-                        } else {  // E4M3: P x vs / vref <= 2^8 in f16, one product
-                            tmem_st16x4(tmem + lane_base + 64 * buf + 4 * k, pack_f16x2(pv[0] * vw[k][0], pv[1] * vw[k][1]),
-                                        pack_f16x2(pv[2] * vw[k][0], pv[3] * vw[k][1]));
-                        }
-                    }
-                    tmem_wait_st();
-                    if constexpr (KV == 0) {
-                        // ---- V rows past the request's length are zeroed (stale or NaN slots of the page)
-                        if (nv < kTile) {
-                            uint8_t *vt = smem + stage * L::kStageBytes + C::kTileBytes;
-                            for (int i = tid; i < (kTile - nv) * 16; i += 128) {
-                                const int row = nv + (i >> 4), ch = i & 15;
-                                *reinterpret_cast<uint4 *>(vt + (ch >> 3) * (C::kTileBytes / 2) + row * 128 + (ch & 7) * 16) =
-                                    make_uint4(0u, 0u, 0u, 0u);
-                            }
-                        }
-                    } else {
-                        // ---- E4M3: V widened exactly to f16 into the stage's operand area, in the
-                        //      layout of a bf16 V tile ([half][64 rows][128 B], 128-byte swizzle);
-                        //      rows past nv are zero (their slots may hold NaN codes).  Thread work:
-                        //      16-byte chunk c (dims 16 c .. 16 c + 15) of row t in, two chunks out
-                        const uint8_t *vr = smem + stage * L::kStageBytes + C::kTileBytes;
-                        uint8_t *vc = smem + stage * L::kStageBytes + L::kVcOff;
-#pragma unroll
-                        for (int it = 0; it < 4; ++it) {
-                            const int i = tid + 128 * it, t = i >> 3, c = i & 7;
-                            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-                            if (t < nv) {
-                                const uint4 x = *reinterpret_cast<const uint4 *>(vr + t * 128 + ((c ^ (t & 7)) << 4));
-                                lo = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(x.x & 0xFFFFu)),
-                                                e4m3x2_to_f16x2(static_cast<uint16_t>(x.x >> 16)),
-                                                e4m3x2_to_f16x2(static_cast<uint16_t>(x.y & 0xFFFFu)),
-                                                e4m3x2_to_f16x2(static_cast<uint16_t>(x.y >> 16)));
-                                hi = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(x.z & 0xFFFFu)),
-                                                e4m3x2_to_f16x2(static_cast<uint16_t>(x.z >> 16)),
-                                                e4m3x2_to_f16x2(static_cast<uint16_t>(x.w & 0xFFFFu)),
-                                                e4m3x2_to_f16x2(static_cast<uint16_t>(x.w >> 16)));
-                            }
-                            uint8_t *row = vc + (c >> 2) * 8192 + t * 128;  // half c / 4, chunks 2 (c % 4), + 1
-                            const int cc = 2 * (c & 3);
-                            *reinterpret_cast<uint4 *>(row + ((cc ^ (t & 7)) << 4)) = lo;
-                            *reinterpret_cast<uint4 *>(row + (((cc + 1) ^ (t & 7)) << 4)) = hi;
-                        }
-                    }
-                    if (!wait_prev_pv()) {
-                        failed = true;
-                        break;
-                    }
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(p_full(buf));
-                    ++pv_desc;
-                    // the previous descriptor's end, now that this tile's P is handed over
-                    if (!flush_epilogue()) {
-                        failed = true;
-                        break;
-                    }
-                }
-                if (failed) break;
-                // ---- a team without tiles here still owes the previous descriptor's end; this
-                //      descriptor's end waits for the next descriptor's first tile
-                if (!flush_epilogue()) {
-                    failed = true;
-                    break;
-                }
-                ep_pending = true;
-                ep_slot = slot;
-                ep_pv = pv_desc;
-                ep_last_g = last_g;
-                ep_m[0] = m[0], ep_m[1] = m[1], ep_l[0] = l[0], ep_l[1] = l[1];
-                if constexpr (KV == 1) ep_vref = vref;
-            }
-        }
-        (void)failed;
-        // ---- every tensor-core role is done: release the tensor memory
-        tc_fence_before();
-        named_bar_sync(1, kTcThreads);
-        if (warp == NCW + 1) {
-            tc_fence_after();
-            tmem_dealloc(tmem, 512);
-        }
-        return;
-    } else if constexpr (QW == 4) {
+    if constexpr (QW == 4) {
         // ======= multi-token queries over E4M3 K/V, up to 16 rows per unit (mma.sync) =======
         // The one-token kernel's shape with two 8-row column blocks: the two consumer groups
         // take alternate tiles (a stage belongs to one group), warp wig of a group takes the
@@ -2067,9 +1007,11 @@ __global__ void __launch_bounds__(64, 1) wait_selftest_kernel(int32_t *status, u
     }
 }
 
+}  // namespace
+
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -2107,13 +1049,15 @@ bool make_pool_map(CUtensorMap *m, const void *pool, int kv, int num_pages, int 
     return r == CUDA_SUCCESS;
 }
 
+namespace {
+
 template <int KV, int STAGES, int GROUPS, bool PERSIST, bool FUSE = false, int MSLOTS = 2, int QW = 0>
 dsa_status launch(const AttnArgs &a, const KernelParams &kp, dim3 grid, cudaStream_t st) {
     using L = Layout<KV, STAGES, GROUPS, MSLOTS, QW>;
     CUtensorMap km, vm;
-    const bool nhd = a.kv_layout == DSA_NHD, split = QW == 3 && KV == 0 && a.page_size < kTile;
-    if (!make_pool_map(&km, a.k_pages, KV, a.num_pages, a.num_kv_heads, a.page_size, nhd, split) ||
-        !make_pool_map(&vm, a.v_pages, KV, a.num_pages, a.num_kv_heads, a.page_size, nhd, split))
+    const bool nhd = a.kv_layout == DSA_NHD;
+    if (!make_pool_map(&km, a.k_pages, KV, a.num_pages, a.num_kv_heads, a.page_size, nhd, false) ||
+        !make_pool_map(&vm, a.v_pages, KV, a.num_pages, a.num_kv_heads, a.page_size, nhd, false))
         return DSA_ERR_CUDA;
     auto kern = attn_kernel<KV, STAGES, GROUPS, PERSIST, FUSE, MSLOTS, QW>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
@@ -2153,9 +1097,6 @@ KernelParams base_params(const AttnArgs &a, float *partial_o, float *partial_lse
 // merge slot with the same or deeper rings.)
 constexpr int kPersistStagesBf16 = 4, kPersistStagesFp8 = 8, kPersistGroups = 2, kPersistMergeSlots = 2;
 constexpr int kPairStagesBf16 = 2, kPairStagesFp8 = 4, kPairGroups = 1;
-// The multi-token tensor-memory kernel keeps P in tensor memory, so its shared memory holds a
-// fifth stage (tiles stay in the ring from their load until their P.V, several microseconds).
-constexpr int kTcStages = 5;
 // The E4M3 multi-token kernel: every warp reads every stage, 8 stages of 17 KB.
 constexpr int kMultiStagesFp8 = 8;
 
@@ -2217,10 +1158,10 @@ extern "C" dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void
     // rows per warp), more rows the tensor-memory kernel
     if (kv_dtype == DSA_FP8_E4M3) {
         if (R <= 16) return launch<1, kMultiStagesFp8, 2, true, false, 1, 4>(a, kp, grid, to_cuda(stream));
-        return launch<1, kTcStages, 2, true, false, 1, 3>(a, kp, grid, to_cuda(stream));
+        return launch_tc(a, kp, map->num_ctas, to_cuda(stream));
     }
     // bf16 K/V: the tensor-memory kernel, for any number of query rows up to 64
-    return launch<0, kTcStages, 2, true, false, 1, 3>(a, kp, grid, to_cuda(stream));
+    return launch_tc(a, kp, map->num_ctas, to_cuda(stream));
 }
 
 extern "C" dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *q_scale, const void *k_pages,

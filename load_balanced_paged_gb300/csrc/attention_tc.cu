@@ -1,0 +1,754 @@
+// Multi-token decode (q_len query tokens per request: a verify step of a draft; Hy3 preview
+// write-up 2.5 "MTP与异步调度优化"; SGLang Low-Latency Mode: Kernels and Runtime, section 1) on
+// the 5th-generation tensor cores.  The scheduler, the task map and the producer warp are
+// those of the one-token kernel (engine.cuh: each resident CTA drains its bin of descriptors,
+// HPC-Ops × SGLang blog, "围绕活跃 KV 工作进行调度"); every KV tile serves all q_len x G query
+// rows of its unit.  Only the consumers differ: S = Q K^T and O = P V accumulate in tensor
+// memory (tcgen05.mma, M = 64), two teams of four softmax warps take alternate tiles, one
+// warp issues S (and lays Q out as its operand), one issues P.V.  Each team writes its own
+// partial at a descriptor end (two slots per descriptor).
+#include "engine.cuh"
+
+namespace dsa {
+namespace {
+
+// Shared memory of the tensor-memory kernel.  From the base: STAGES ring stages (K tile, V
+// tile, E4M3 scales; E4M3 also a V tile widened to f16), the plain Q rows of kQSlots
+// descriptors, two Q operand buffers, the barriers, the stages' valid-token counts, the abort
+// flag and tensor-memory address, the descriptor hand-off records.
+template <int KV, int STAGES>
+struct TcLayout {
+    static constexpr int kQSlots = 2;  // descriptors handed ahead to the consumers
+    static constexpr int kNcw = 8;     // softmax warps (two teams of four)
+    static constexpr int kThreads = (kNcw + 3) * 32;  // + producer, S and PV warps
+    static constexpr int kStageTx = 2 * Cfg<KV>::kTileBytes + 2 * Cfg<KV>::kScaleBytes;
+    // E4M3: each stage also holds its V widened to f16 ([half][64 rows][128 B], 128-byte
+    // swizzle: the P.V operand layout of a bf16 V tile)
+    static constexpr int kVcOff = round_up(kStageTx, 1024);
+    static constexpr int kStageBytes = kVcOff + (KV == 1 ? kTile * kHeadDim * 2 : 0);
+    static constexpr int kQSlot = kMaxRows * Cfg<KV>::kQHeadBytes;
+    static constexpr int kQOff = STAGES * kStageBytes;
+    // Q as the MMA's A operand (64 rows x 128, K-major with the 128-byte swizzle, two 64-column
+    // halves of 8 KB for bf16, as the TMA lays out a K tile), two buffers
+    static constexpr int kQcOff = kQOff + kQSlots * kQSlot;
+    static constexpr int kQcBytes = 2 * kMaxRows * Cfg<KV>::kQHeadBytes;
+    static constexpr int kBarOff = kQcOff + kQcBytes;
+    // full, empty, qfull, qempty; s_full, s_free, p_full x4; o_done, o_free, qc_full, qc_free, qd_full x2
+    static constexpr int kTcBars = 22;
+    static constexpr int kNumBars = 2 * STAGES + 2 * kQSlots + kTcBars;
+    static constexpr int kNValidOff = kBarOff + kNumBars * 8;
+    static constexpr int kAbortOff = kNValidOff + STAGES * 4;  // abort flag, then the TMEM base address
+    static constexpr int kInfoOff = round_up(kAbortOff + 16, 64);  // one DescInfo per Q slot
+    static constexpr int kBytes = kInfoOff + kQSlots * kDescInfoBytes;
+    static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
+    static_assert(kQcOff % 1024 == 0, "tensor-core operand buffers");
+    static_assert(kStageBytes % 1024 == 0 && kQOff % 1024 == 0, "swizzled TMA boxes need 1024-byte alignment");
+    static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+template <int KV, int STAGES>
+__global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
+    tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                   const KernelParams p) {
+    using L = TcLayout<KV, STAGES>;
+    using C = Cfg<KV>;
+    constexpr int NCW = L::kNcw;
+    constexpr int kQSlots = L::kQSlots;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + L::kBarOff;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto qfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+    auto qempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + kQSlots + s); };
+    const uint32_t tc_bar0 = bar0 + 8u * (2 * STAGES + 2 * kQSlots);
+    auto s_full = [&](int b) { return tc_bar0 + 8u * b; };         // 4 S/P buffers
+    auto s_free = [&](int b) { return tc_bar0 + 8u * (4 + b); };
+    auto p_full = [&](int b) { return tc_bar0 + 8u * (8 + b); };
+    auto o_done = [&](int t) { return tc_bar0 + 8u * (12 + t); };  // 2 softmax teams
+    auto o_free = [&](int t) { return tc_bar0 + 8u * (14 + t); };
+    auto qc_full = [&](int b) { return tc_bar0 + 8u * (16 + b); };
+    auto qc_free = [&](int b) { return tc_bar0 + 8u * (18 + b); };
+    auto qd_full = [&](int b) { return tc_bar0 + 8u * (20 + b); };  // plain Q rows landed
+    int *nvalid = reinterpret_cast<int *>(smem + L::kNValidOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbortOff);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.G;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 2);  // the S and PV warps each release their half of a stage
+        }
+        for (int s = 0; s < kQSlots; ++s) {
+            mbar_init(qfull_bar(s), 1);
+            mbar_init(qempty_bar(s), NCW + 2);  // every warp that reads the hand-off
+        }
+        for (int b = 0; b < 4; ++b) {
+            mbar_init(s_full(b), 1);  // S warp
+            mbar_init(s_free(b), 1);  // PV warp: the buffer's P has been read
+            mbar_init(p_full(b), 4);  // the owning softmax team
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(o_done(b), 1);
+            mbar_init(o_free(b), 4);
+            mbar_init(qc_full(b), 1);
+            mbar_init(qc_free(b), 1);
+            mbar_init(qd_full(b), 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    grid_launch_dependents();
+    grid_dependency_wait();  // task map, lengths, pages and Q from earlier kernels
+    EndStamp end_stamp{nullptr};
+    if (p.cta_times) {  // uniform over the CTA
+        uint64_t *t = p.cta_times + 2 * blockIdx.x;
+        if (threadIdx.x == 0) t[0] = t[1] = globaltimer_ns();
+        __syncthreads();
+        end_stamp.at = t + 1;
+    }
+    const int d_begin = p.cta_desc_begin[blockIdx.x];
+    const int d_count = p.cta_desc_begin[blockIdx.x + 1] - d_begin;
+    if (d_count <= 0) return;
+
+    if (warp == NCW) {
+        producer_warp<KV, STAGES, true, false, true, L>(&kmap, &vmap, p, smem, sbase, bar0, nvalid, abort_flag,
+                                                        nullptr, d_begin, d_count, 0, 0, lane);
+        return;
+    }
+
+    // ============ multi-token queries on the 5th-generation tensor cores ============
+    // Rows r = i * G + g (query token i, head g), r < R = q_len * G <= 64.  Per tile:
+    //   S[64 x 64] = Qc . K^T in one of two 64-column TMEM buffers (M = 64: row r sits in
+    //   lane 32 (r / 16) + r % 16, i.e. lanes 0-15 of each warp's 32-lane quarter);
+    //   the softmax thread of row r (lane r % 16 of warp r / 16) masks it (causal within
+    //   the draft, past the length), keeps the running max m, raised lazily (O is
+    //   rescaled only when the max grows by more than 8 in base 2), and writes P =
+    //   2^(s - m) as bf16 high and low parts;
+    //   O[64 x 128] += P_hi . V + P_lo . V in TMEM columns 128-255.
+    // Two warps issue the products: the S warp runs ahead (two S buffers) as stages land,
+    // the PV warp follows the softmax; each releases its half of a ring stage (K, V) when
+    // its products have read it, so the softmax of tile g overlaps the products of its
+    // neighbours and no product waits for an unrelated load.
+    const int R = p.q_len * G;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kAbortOff + 4);
+    constexpr int kTcThreads = (NCW + 2) * 32;  // softmax warps, S warp, PV warp
+    constexpr uint32_t kQcBuf = kMaxRows * C::kQHeadBytes;
+    if (warp == NCW + 1) tmem_alloc(smem_u32(tmem_slot), 512);
+    tc_fence_before();
+    named_bar_sync(1, kTcThreads);
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+    // Q K-major, K K-major (bf16, or E4M3 with kind::f8f6f4); P K-major, V M/N-major
+    // (bf16, or f16 for E4M3 K/V: V widened exactly, P carrying the V scale)
+    constexpr uint32_t kIdS = KV == 0 ? umma_idesc_bf16(64, 64, 0, 0) : umma_idesc_fmt0(64, 64, 0, 0);
+    constexpr uint32_t kIdO = KV == 0 ? umma_idesc_bf16(64, 128, 0, 1) : umma_idesc_fmt0(64, 128, 0, 1);
+    bool failed = false;
+
+    if (warp == NCW + 1) {
+        // ---- S warp: fetches each descriptor's Q rows one descriptor ahead (plain rows
+        //      into one of two buffers), lays them out as the A operand (zero past R), then
+        //      issues S = Q K^T for its tiles as soon as a stage and an S buffer are ready
+        //      (lane 0 issues, the warp waits together); its commit on the stage's empty
+        //      barrier says the K half is no longer read
+        // descriptors of this CTA, 32 at a time: lane j holds the unit of descriptor wbase + j
+        // if the producer hands it over (valid, with tiles), else -1
+        int wbase = 0, wu = -1;
+        auto load_window = [&](int base) {
+            wbase = base;
+            wu = -1;
+            if (base + lane < d_count) {
+                const int4 v = p.descs[d_begin + base + lane];
+                if (v.x >= 0 && v.x < p.num_units && v.y >= 0 && v.y < v.z && d_begin + base + lane < p.max_slots)
+                    wu = v.x;
+            }
+        };
+        load_window(0);
+        auto next_desc = [&](int after) {  // the next handed-over descriptor (raw slot) after `after`
+            for (int rel = after - d_begin + 1; rel < d_count;) {
+                if (rel < wbase || rel >= wbase + 32) load_window(rel & ~31);
+                const uint32_t m = __ballot_sync(0xffffffffu, wu >= 0) & (~0u << (rel - wbase));
+                if (m) return d_begin + wbase + __ffs(m) - 1;
+                rel = wbase + 32;
+            }
+            return -1;
+        };
+        int fetched[2] = {0, 0};  // Q copies issued into each plain buffer (each one waited for)
+        auto fetch_q = [&](int x, int j) {  // x in the current window
+            const int u = __shfl_sync(0xffffffffu, wu, x - d_begin - wbase);
+            if (lane == 0) {
+                const int b = u / p.hkv, h = u - b * p.hkv;
+                const uint32_t bytes = G * C::kQHeadBytes;
+                mbar_arrive_expect_tx(qd_full(j), bytes * p.q_len);
+                for (int i = 0; i < p.q_len; ++i)
+                    bulk_load(sbase + L::kQOff + j * L::kQSlot + i * bytes,
+                              p.q + ((static_cast<int64_t>(b) * p.q_len + i) * p.hq + h * G) * C::kQHeadBytes, bytes,
+                              qd_full(j));
+            }
+            ++fetched[j];
+        };
+        auto land_q = [&](int j) { return wait_phase(qd_full(j), (fetched[j] - 1) & 1, abort_flag, p.status); };
+        int pf_slot = next_desc(d_begin - 1), pf_buf = 0;  // the descriptor whose Q is in flight
+        if (pf_slot >= 0) fetch_q(pf_slot, 0);
+        int g = 0, last_d = -1;
+        for (int d = 0;; ++d) {
+            const int qslot = d % kQSlots;
+            if (!wait_phase(qfull_bar(qslot), (d / kQSlots) & 1, abort_flag, p.status)) {
+                failed = true;
+                break;
+            }
+            const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
+            const int end = inf->end, n = inf->n, c_start = inf->c_start, xs = inf->slot;
+            if (!end) {
+                // this descriptor's Q: normally the prefetched one; otherwise fetched now
+                const int qb = pf_buf;
+                if (pf_slot != xs) {
+                    if (pf_slot >= 0 && !land_q(qb)) {
+                        failed = true;
+                        break;
+                    }
+                    if (xs < d_begin + wbase || xs >= d_begin + wbase + 32) load_window((xs - d_begin) & ~31);
+                    fetch_q(xs, qb);
+                }
+                if (!land_q(qb) || !wait_phase(qc_free(d & 1), ((d >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                    pf_slot = -1;  // consumed (or abandoned with the CTA)
+                    failed = true;
+                    break;
+                }
+                const uint8_t *src = smem + L::kQOff + qb * L::kQSlot;
+                uint8_t *dst = smem + L::kQcOff + (d & 1) * kQcBuf;
+                if constexpr (KV == 0) {
+                // 128-byte-swizzled K-major operand (as the TMA lays out K): dims 64 b .. 64 b + 63
+                // of row r at b * 8 KB + r * 128 B, 16-byte chunk c at (c ^ (r % 8)) * 16.  Each
+                // quarter-warp writes one 128-byte row: no bank conflicts either way.
+#pragma unroll
+                for (int rd = 0; rd < 4; ++rd) {
+                    uint4 v[8];
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {  // chunk kc of row r
+                        const int i = lane + 32 * (8 * rd + it), r = i >> 4, kc = i & 15;
+                        v[it] = r < R ? *reinterpret_cast<const uint4 *>(src + r * (kHeadDim * 2) + kc * 16)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int i = lane + 32 * (8 * rd + it), r = i >> 4, kc = i & 15;
+                        *reinterpret_cast<uint4 *>(dst + (kc >> 3) * 8192 + r * 128 + (((kc & 7) ^ (r & 7)) << 4)) = v[it];
+                    }
+                }
+                } else {
+                // E4M3: a row is one 128-byte swizzle row (r * 128 B, chunk c at (c ^ (r % 8)) * 16)
+#pragma unroll
+                for (int rd = 0; rd < 2; ++rd) {
+                    uint4 v[8];
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {  // chunk kc of row r
+                        const int i = lane + 32 * (8 * rd + it), r = i >> 3, kc = i & 7;
+                        v[it] = r < R ? *reinterpret_cast<const uint4 *>(src + r * kHeadDim + kc * 16)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int i = lane + 32 * (8 * rd + it), r = i >> 3, kc = i & 7;
+                        *reinterpret_cast<uint4 *>(dst + r * 128 + ((kc ^ (r & 7)) << 4)) = v[it];
+                    }
+                }
+                }
+                fence_proxy_async_smem();
+                // the next descriptor's Q lands while this one's tiles are worked on
+                pf_slot = next_desc(xs);
+                if (pf_slot >= 0) {
+                    pf_buf = qb ^ 1;
+                    fetch_q(pf_slot, pf_buf);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qempty_bar(qslot));
+            if (end) break;
+            const uint32_t qa = sbase + L::kQcOff + (d & 1) * kQcBuf;
+            for (int li = 0; li < n; ++li, ++g) {
+                const int c = c_start + li, stage = c % STAGES, buf = g & 3;
+                if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status) ||
+                    !wait_phase(s_free(buf), ((g >> 2) & 1) ^ 1, abort_flag, p.status)) {
+                    failed = true;
+                    break;
+                }
+                const int nv = nvalid[stage];
+                if (lane == 0) {
+                    if (nv > 0) {
+                        tc_fence_after();
+                        const uint32_t kb = sbase + stage * L::kStageBytes;
+                        if constexpr (KV == 0) {
+#pragma unroll
+                            for (int ks = 0; ks < 8; ++ks)
+                                umma_bf16(tmem + 64 * buf, umma_desc(qa + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, 2),
+                                          umma_desc(kb + (ks >> 2) * (C::kTileBytes / 2) + (ks & 3) * 32, 16, 1024, 2),
+                                          kIdS, ks > 0);
+                        } else {  // E4M3: 32 dims (32 bytes) per product
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks)
+                                umma_e4m3(tmem + 64 * buf, umma_desc(qa + ks * 32, 16, 1024, 2),
+                                          umma_desc(kb + ks * 32, 16, 1024, 2), kIdS, ks > 0);
+                        }
+                        umma_commit(s_full(buf));
+                        umma_commit(empty_bar(stage));
+                    } else {
+                        mbar_arrive(s_full(buf));
+                        mbar_arrive(empty_bar(stage));
+                    }
+                }
+                __syncwarp();
+            }
+            if (failed) break;
+            if (lane == 0) umma_commit(qc_free(d & 1));  // the descriptor's S products have read Qc
+            __syncwarp();
+            last_d = d;
+        }
+        // the last commit lands once every product this warp issued has completed; a Q copy
+        // still in flight lands before the CTA leaves
+        if (!failed && last_d >= 0) wait_phase(qc_free(last_d & 1), (last_d >> 1) & 1, abort_flag, p.status);
+        if (pf_slot >= 0) {
+            const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+            drain_phase(qd_full(pf_buf), (fetched[pf_buf] - 1) & 1, deadline);
+        }
+    } else if (warp == NCW + 2) {
+        // ---- PV warp: O += P_hi . V + P_lo . V as soon as the softmax warps hand P over;
+        //      its commit on the stage's empty barrier says the V half is no longer read
+        int g = 0;
+        for (int d = 0;; ++d) {
+            const int qslot = d % kQSlots;
+            if (!wait_phase(qfull_bar(qslot), (d / kQSlots) & 1, abort_flag, p.status)) {
+                failed = true;
+                break;
+            }
+            const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
+            const int end = inf->end, n = inf->n, c_start = inf->c_start;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qempty_bar(qslot));
+            if (end) break;
+            bool first_pv[2] = {true, true};  // per softmax team (tile parity): O_t not yet written
+            for (int li = 0; li < n; ++li, ++g) {
+                const int c = c_start + li, stage = c % STAGES, buf = g & 3, t = g & 1;
+                if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status) ||
+                    !wait_phase(p_full(buf), (g >> 2) & 1, abort_flag, p.status)) {
+                    failed = true;
+                    break;
+                }
+                const int nv = nvalid[stage];
+                if (nv > 0) {
+                    // O_t is free once team t has read out the previous descriptor's
+                    if (first_pv[t] && !wait_phase(o_free(t), (d & 1) ^ 1, abort_flag, p.status)) {
+                        failed = true;
+                        break;
+                    }
+                    if (lane == 0) {
+                        tc_fence_after();
+                        // bf16: V as loaded, P high part in columns 0-31, low part in 32-63;
+                        // E4M3: V widened to f16 by the softmax team, P (f16) in columns 0-31
+                        const uint32_t vb = sbase + stage * L::kStageBytes + (KV == 0 ? C::kTileBytes : L::kVcOff);
+                        const uint32_t pt = tmem + 64 * buf;
+                        const uint32_t od = tmem + 256 + 128 * t;
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t bd = umma_desc(vb + ks * 2048, 8192, 1024, 2);
+                            umma_bf16_ta(od, pt + 8 * ks, bd, kIdO, !(first_pv[t] && ks == 0));
+                            if (KV == 0) umma_bf16_ta(od, pt + 32 + 8 * ks, bd, kIdO, true);
+                        }
+                    }
+                    first_pv[t] = false;
+                }
+                // commits, not arrives: a phase also means every earlier product is done
+                if (lane == 0) {
+                    umma_commit(o_done(t));
+                    umma_commit(s_free(buf));
+                    umma_commit(empty_bar(stage));
+                }
+                __syncwarp();
+            }
+            if (failed) break;
+        }
+    } else {
+        // ---- softmax warps: two teams of four (team t = warps 4t .. 4t + 3) take the tiles
+        //      of parity t (S/P buffers t and t + 2 in turn, O_t).  Warp w reads the 16 rows
+        //      16 (w & 3) .. + 15
+        //      (M = 64 accumulators: lanes 0-15 of each sub-partition) as m16n8 fragments:
+        //      thread (gid = lane / 4, tig = lane % 4) holds rows ra = 16 (w & 3) + gid and
+        //      rb = ra + 8, columns 8 k + 2 tig, + 1; a row's max and sum combine over the
+        //      four threads of its quad.  At each descriptor end each team writes its own
+        //      partial (slot 2 x descriptor + team); the combine merges them with the others.
+        const int team = warp >> 2, sp = warp & 3;
+        const int gid = lane >> 2, tig = lane & 3;
+        const int ra = 16 * sp + gid, rb = ra + 8;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
+        const uint32_t o_col = 256 + 128 * team;
+        const int tid = sp * 32 + lane;  // within the team
+        // The descriptor end of a team (its partial, slot 2 x descriptor + team), deferred
+        // until the team has handed over the P of its first tile of the next descriptor: a
+        // descriptor's first tile never rescales O, so it need not wait for the previous
+        // descriptor's last P.V, and the team computes it while that P.V completes.
+        float ep_vref = 1.f;  // E4M3: the V scale reference of the deferred descriptor end
+        auto team_epilogue = [&](int slot, float (&m)[2], float (&l)[2], int pv_desc, int last_g) -> bool {
+            // ---- this team's products of the descriptor are done once its last tile's buffer
+            //      phase is (that commit covers every earlier product)
+            if (last_g >= 0) {
+                if (!wait_phase(o_done(team), (last_g >> 1) & 1, abort_flag, p.status)) return false;
+                tc_fence_after();
+            }
+            // ---- this team's partial (slot 2 x descriptor + team): O_t / l, lse = ln(2) (m + log2 l)
+            float inv[2], lse[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+                l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+                if constexpr (KV == 0)
+                    inv[h] = l[h] > 0.f ? 1.f / l[h] : 0.f;
+                else
+                    inv[h] = l[h] > 0.f ? ep_vref / l[h] : 0.f;
+                lse[h] = l[h] > 0.f ? (m[h] + lg2(l[h])) * kLn2 : -INFINITY;
+            }
+            const int64_t slot_row = (2 * static_cast<int64_t>(slot) + team) * R;
+            float *dst_a = p.partial_o + (slot_row + ra) * kHeadDim + 2 * tig;
+            float *dst_b = p.partial_o + (slot_row + rb) * kHeadDim + 2 * tig;
+            // O_t into registers first, then release it for the next descriptor's products
+            float o[16][4];
+            if (pv_desc > 0) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) tmem_ld16x8(tmem + lane_base + o_col + 8 * k, o[k]);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free(team));
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                if (ra < R) *reinterpret_cast<float2 *>(dst_a + 8 * k) = make_float2(o[k][0] * inv[0], o[k][1] * inv[0]);
+                if (rb < R) *reinterpret_cast<float2 *>(dst_b + 8 * k) = make_float2(o[k][2] * inv[1], o[k][3] * inv[1]);
+            }
+            if (tig == 0) {
+                if (ra < R) p.partial_lse[slot_row + ra] = lse[0];
+                if (rb < R) p.partial_lse[slot_row + rb] = lse[1];
+            }
+            return true;
+        };
+        bool ep_pending = false;
+        int ep_slot = 0, ep_pv = 0, ep_last_g = -1;
+        float ep_m[2] = {0.f, 0.f}, ep_l[2] = {0.f, 0.f};
+        auto flush_epilogue = [&]() -> bool {
+            if (!ep_pending) return true;
+            ep_pending = false;
+            return team_epilogue(ep_slot, ep_m, ep_l, ep_pv, ep_last_g);
+        };
+        int g = 0;
+        for (int d = 0;; ++d) {
+            const int qslot = d % kQSlots;
+            if (!wait_phase(qfull_bar(qslot), (d / kQSlots) & 1, abort_flag, p.status)) {
+                failed = true;
+                break;
+            }
+            const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
+            const int end = inf->end, n = inf->n, slot = inf->slot, c_start = inf->c_start;
+            const int dt0 = inf->t0, len = inf->len;
+            int d_b = 0, d_h = 0;
+            if constexpr (KV == 1) d_b = inf->b, d_h = inf->h;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qempty_bar(qslot));
+            if (end) {
+                if (!flush_epilogue()) failed = true;
+                break;
+            }
+            // visible tokens of each row: t < lim (-1: a row past R)
+            const int lim[2] = {ra < R ? len - p.q_len + ra / G + 1 : -1, rb < R ? len - p.q_len + rb / G + 1 : -1};
+            float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+            // E4M3: score factor per row (softmax scale x the row's q_scale), the V scale
+            // reference (the largest V scale seen, O holds the output divided by it) and its inverse
+            float qsc[2] = {p.score_scale, p.score_scale}, vref = 1.f, vinv = 1.f;
+            if constexpr (KV == 1) {
+                const int rr[2] = {ra, rb};
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    if (rr[h] < R) {
+                        const int i = rr[h] / G;
+                        qsc[h] *= p.q_scale[(static_cast<int64_t>(d_b) * p.q_len + i) * p.hq + d_h * G + rr[h] - i * G];
+                    }
+                vref = vinv = 0.f;
+            }
+            int pv_desc = 0, last_g = -1;
+            for (int li = 0; li < n; ++li, ++g) {
+                if ((g & 1) != team) continue;
+                const int c = c_start + li, stage = c % STAGES, buf = g & 3;
+                if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status) ||
+                    !wait_phase(s_full(buf), (g >> 2) & 1, abort_flag, p.status)) {
+                    failed = true;
+                    break;
+                }
+                const int nv = nvalid[stage];
+                tc_fence_after();
+                float sv[8][4];  // [column block k][(ra, 2tig), (ra, 2tig+1), (rb, 2tig), (rb, 2tig+1)]
+                if (nv > 0) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + 64 * buf + 8 * k, sv[k]);
+                    tmem_wait_ld();
+                }
+                // this team's previous tile of the descriptor (-1: none; the first tile starts
+                // from m = -inf and never rescales O).  Its P.V is waited for before this tile's
+                // P is handed over (so the team stays within one phase of o_done, which the
+                // descriptor end's wait needs), and before a rescale of O, which reads O.  (S of
+                // this tile was issued after the P.V two team tiles back had released its
+                // buffer, so until this tile's P is handed over the barrier is at most one
+                // phase behind the one waited for.)
+                const int prev_g = last_g;
+                last_g = g;
+                auto wait_prev_pv = [&]() {
+                    return prev_g < 0 || wait_phase(o_done(team), ((g >> 1) & 1) ^ 1, abort_flag, p.status);
+                };
+                if (nv == 0) {  // no data in this stage: the PV warp skips its P.V
+                    if (!wait_prev_pv()) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(p_full(buf));
+                    if (!flush_epilogue()) {
+                        failed = true;
+                        break;
+                    }
+                    continue;
+                }
+                // ---- E4M3: S times the K scale of its column; P's factor per column, the V
+                //      scale over the reference, which moves only when a larger scale appears
+                //      (O is then rescaled with the maxima below); columns past nv get 0
+                float vw[8][2];
+                float vf = 1.f;
+                if constexpr (KV == 1) {
+                    const float *ksm = reinterpret_cast<const float *>(smem + stage * L::kStageBytes + 2 * C::kTileBytes);
+                    const float *vsm = ksm + kTile;
+                    float vmax = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int j = 8 * k + 2 * tig;
+                        const float2 kk = *reinterpret_cast<const float2 *>(ksm + j);
+                        const float2 vv = *reinterpret_cast<const float2 *>(vsm + j);
+                        sv[k][0] *= kk.x;
+                        sv[k][1] *= kk.y;
+                        sv[k][2] *= kk.x;
+                        sv[k][3] *= kk.y;
+                        vw[k][0] = j < nv ? vv.x : 0.f;
+                        vw[k][1] = j + 1 < nv ? vv.y : 0.f;
+                        vmax = fmaxf(vmax, fmaxf(vw[k][0], vw[k][1]));
+                    }
+                    if (__any_sync(0xffffffffu, vmax > vref)) {  // the quad's four lanes cover the 64 columns
+                        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
+                        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+                        if (vmax > vref) {
+                            if (vref > 0.f) vf = vref / vmax;  // from 0: nothing accumulated yet
+                            vref = vmax;
+                            vinv = 1.f / vmax;
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        vw[k][0] *= vinv;
+                        vw[k][1] *= vinv;
+                    }
+                }
+                // ---- running maximum over each row's visible tokens (t < lim, slot < nv)
+                const int tt = (dt0 + li) * kTile;
+                const int vis[2] = {max(0, min(nv, lim[0] - tt)), max(0, min(nv, lim[1] - tt))};
+                const bool full = vis[0] == kTile && vis[1] == kTile;
+                float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int h = e >> 1, j = 8 * k + 2 * tig + (e & 1);
+                        mx[h] = fmaxf(mx[h], (full || j < vis[h]) ? sv[k][e] : -INFINITY);
+                    }
+                bool grow[2];
+                float alpha[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+                    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+                    const float mnew = fmaxf(m[h], mx[h] * (KV == 0 ? p.score_scale : qsc[h]));
+                    grow[h] = m[h] != -INFINITY && mnew > m[h] + 8.f;
+                    alpha[h] = grow[h] ? ex2(m[h] - mnew) : 1.f;
+                    if (grow[h] || m[h] == -INFINITY) m[h] = mnew;
+                }
+                if (__any_sync(0xffffffffu, grow[0] || grow[1] || (KV == 1 && vf != 1.f))) {
+                    // rows whose maximum grew: O_team *= 2^(m_old - m_new); E4M3: all rows also
+                    // by the V scale reference's change (after the previous P.V into O_team)
+                    if (!wait_prev_pv()) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1  // rare: kept small for the instruction cache
+                    for (int half = 0; half < 2; ++half) {
+                        float o[8][4];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + o_col + 64 * half + 8 * k, o[k]);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            if constexpr (KV == 0) {
+                                o[k][0] *= alpha[0];
+                                o[k][1] *= alpha[0];
+                                o[k][2] *= alpha[1];
+                                o[k][3] *= alpha[1];
+                            } else {
+                                o[k][0] *= alpha[0] * vf;
+                                o[k][1] *= alpha[0] * vf;
+                                o[k][2] *= alpha[1] * vf;
+                                o[k][3] *= alpha[1] * vf;
+                            }
+                            tmem_st16x8(tmem + lane_base + o_col + 64 * half + 8 * k, o[k]);
+                        }
+                        tmem_wait_st();
+                    }
+                    l[0] *= alpha[0];
+                    l[1] *= alpha[1];
+                }
+                // ---- P = 2^(s * scale - m) (0 where not visible) as bf16 high part (the top 16
+                //      bits) and low part (the rest, rounded), written over S in the buffer: the
+                //      P.V's A operand, tokens (2c, 2c + 1) packed in column c (high part:
+                //      columns 0-31, low part: 32-63)
+                const float nm0 = -m[0], nm1 = -m[1];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    float pv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int h = e >> 1, j = 8 * k + 2 * tig + (e & 1);
+                        const float q = ex2(fmaf(sv[k][e], KV == 0 ? p.score_scale : qsc[h], h ? nm1 : nm0));
+                        pv[e] = (full || j < vis[h]) ? q : 0.f;
+                    }
+                    l[0] += pv[0] + pv[1];
+                    l[1] += pv[2] + pv[3];
+                    if constexpr (KV == 0) {
+                        const uint32_t h0 = __float_as_uint(pv[0]) & 0xFFFF0000u, h1 = __float_as_uint(pv[1]) & 0xFFFF0000u;
+                        const uint32_t h2 = __float_as_uint(pv[2]) & 0xFFFF0000u, h3 = __float_as_uint(pv[3]) & 0xFFFF0000u;
+                        tmem_st16x4(tmem + lane_base + 64 * buf + 4 * k, prmt(h0, h1, 0x7632u), prmt(h2, h3, 0x7632u));
+                        tmem_st16x4(tmem + lane_base + 64 * buf + 32 + 4 * k,
+                                    pack_bf16x2(pv[0] - __uint_as_float(h0), pv[1] - __uint_as_float(h1)),
+                                    pack_bf16x2(pv[2] - __uint_as_float(h2), pv[3] - __uint_as_float(h3)));
+                    } else {  // E4M3: P x vs / vref <= 2^8 in f16, one product
+                        tmem_st16x4(tmem + lane_base + 64 * buf + 4 * k, pack_f16x2(pv[0] * vw[k][0], pv[1] * vw[k][1]),
+                                    pack_f16x2(pv[2] * vw[k][0], pv[3] * vw[k][1]));
+                    }
+                }
+                tmem_wait_st();
+                if constexpr (KV == 0) {
+                    // ---- V rows past the request's length are zeroed (stale or NaN slots of the page)
+                    if (nv < kTile) {
+                        uint8_t *vt = smem + stage * L::kStageBytes + C::kTileBytes;
+                        for (int i = tid; i < (kTile - nv) * 16; i += 128) {
+                            const int row = nv + (i >> 4), ch = i & 15;
+                            *reinterpret_cast<uint4 *>(vt + (ch >> 3) * (C::kTileBytes / 2) + row * 128 + (ch & 7) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                } else {
+                    // ---- E4M3: V widened exactly to f16 into the stage's operand area, in the
+                    //      layout of a bf16 V tile ([half][64 rows][128 B], 128-byte swizzle);
+                    //      rows past nv are zero (their slots may hold NaN codes).  Thread work:
+                    //      16-byte chunk c (dims 16 c .. 16 c + 15) of row t in, two chunks out
+                    const uint8_t *vr = smem + stage * L::kStageBytes + C::kTileBytes;
+                    uint8_t *vc = smem + stage * L::kStageBytes + L::kVcOff;
+#pragma unroll
+                    for (int it = 0; it < 4; ++it) {
+                        const int i = tid + 128 * it, t = i >> 3, c = i & 7;
+                        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                        if (t < nv) {
+                            const uint4 x = *reinterpret_cast<const uint4 *>(vr + t * 128 + ((c ^ (t & 7)) << 4));
+                            lo = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(x.x & 0xFFFFu)),
+                                            e4m3x2_to_f16x2(static_cast<uint16_t>(x.x >> 16)),
+                                            e4m3x2_to_f16x2(static_cast<uint16_t>(x.y & 0xFFFFu)),
+                                            e4m3x2_to_f16x2(static_cast<uint16_t>(x.y >> 16)));
+                            hi = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(x.z & 0xFFFFu)),
+                                            e4m3x2_to_f16x2(static_cast<uint16_t>(x.z >> 16)),
+                                            e4m3x2_to_f16x2(static_cast<uint16_t>(x.w & 0xFFFFu)),
+                                            e4m3x2_to_f16x2(static_cast<uint16_t>(x.w >> 16)));
+                        }
+                        uint8_t *row = vc + (c >> 2) * 8192 + t * 128;  // half c / 4, chunks 2 (c % 4), + 1
+                        const int cc = 2 * (c & 3);
+                        *reinterpret_cast<uint4 *>(row + ((cc ^ (t & 7)) << 4)) = lo;
+                        *reinterpret_cast<uint4 *>(row + (((cc + 1) ^ (t & 7)) << 4)) = hi;
+                    }
+                }
+                if (!wait_prev_pv()) {
+                    failed = true;
+                    break;
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full(buf));
+                ++pv_desc;
+                // the previous descriptor's end, now that this tile's P is handed over
+                if (!flush_epilogue()) {
+                    failed = true;
+                    break;
+                }
+            }
+            if (failed) break;
+            // ---- a team without tiles here still owes the previous descriptor's end; this
+            //      descriptor's end waits for the next descriptor's first tile
+            if (!flush_epilogue()) {
+                failed = true;
+                break;
+            }
+            ep_pending = true;
+            ep_slot = slot;
+            ep_pv = pv_desc;
+            ep_last_g = last_g;
+            ep_m[0] = m[0], ep_m[1] = m[1], ep_l[0] = l[0], ep_l[1] = l[1];
+            if constexpr (KV == 1) ep_vref = vref;
+        }
+    }
+    (void)failed;
+    // ---- every tensor-core role is done: release the tensor memory
+    tc_fence_before();
+    named_bar_sync(1, kTcThreads);
+    if (warp == NCW + 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    return;
+}
+
+}  // namespace
+
+// The tensor-memory kernel needs its stages from the load of a tile until its P.V, several
+// microseconds; P lives in tensor memory, so shared memory holds five stages.
+constexpr int kTcStages = 5;
+
+dsa_status launch_tc(const AttnArgs &a, const KernelParams &kp, int num_ctas, cudaStream_t st) {
+    const bool nhd = a.kv_layout == DSA_NHD;
+    const int kv = a.kv_dtype == DSA_BF16 ? 0 : 1;
+    // bf16 pages smaller than the tile: each 128-byte half of a page is its own box, so that a
+    // stage lands as [half][64 rows][128 B], the operand layout
+    const bool split = kv == 0 && a.page_size < kTile;
+    CUtensorMap km, vm;
+    if (!make_pool_map(&km, a.k_pages, kv, a.num_pages, a.num_kv_heads, a.page_size, nhd, split) ||
+        !make_pool_map(&vm, a.v_pages, kv, a.num_pages, a.num_kv_heads, a.page_size, nhd, split))
+        return DSA_ERR_CUDA;
+    auto go = [&](auto kern, int smem, int threads) -> dsa_status {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return DSA_ERR_CUDA;
+        return launch_pdl(kern, dim3(num_ctas), dim3(threads), smem, st, km, vm, kp);
+    };
+    if (kv == 0)
+        return go(tc_attn_kernel<0, kTcStages>, TcLayout<0, kTcStages>::kAlloc, TcLayout<0, kTcStages>::kThreads);
+    return go(tc_attn_kernel<1, kTcStages>, TcLayout<1, kTcStages>::kAlloc, TcLayout<1, kTcStages>::kThreads);
+}
+
+}  // namespace dsa
