@@ -52,26 +52,45 @@ __global__ void __launch_bounds__(kMaxGroup * 32)
     const int64_t beg = STATIC ? static_cast<int64_t>(u) * S : static_cast<int64_t>(unit_begin[u]) * spd;
     const int n = STATIC ? S : unit_count[u] * spd;
 
-    float M = -INFINITY;
-    for (int k = lane; k < n; k += 32) M = fmaxf(M, partial_lse[(beg + k) * R + row]);
+    // the first kPre partials' rows are loaded together with the LSEs, so the merge of a unit
+    // with few partials waits for one round trip to memory after the lengths, not two
+    constexpr int kPre = 8;
+    float4 pre[kPre];
+#pragma unroll
+    for (int j = 0; j < kPre; ++j)
+        if (j < n) pre[j] = *reinterpret_cast<const float4 *>(partial_o + ((beg + j) * R + row) * kHeadDim + lane * 4);
+    const float lse0 = lane < n ? partial_lse[(beg + lane) * R + row] : -INFINITY;
+    float M = lse0;
+    for (int k = lane + 32; k < n; k += 32) M = fmaxf(M, partial_lse[(beg + k) * R + row]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = -INFINITY;
     if (M != -INFINITY) {
-        float sum = 0.f;
-        for (int k = lane; k < n; k += 32) sum += exp2f((partial_lse[(beg + k) * R + row] - M) * kLog2e);
+        float sum = lane < n ? exp2f((lse0 - M) * kLog2e) : 0.f;
+        for (int k = lane + 32; k < n; k += 32) sum += exp2f((partial_lse[(beg + k) * R + row] - M) * kLog2e);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         L = M + logf(sum);
-        // 32 partials at a time: lane k holds the weight of partial k0 + k; the rows of the
-        // batch are loaded back to back
+        // 32 partials at a time: lane k holds the weight of partial k0 + k
         for (int k0 = 0; k0 < n; k0 += 32) {
             const int kn = min(32, n - k0);
-            const float w = lane < kn ? exp2f((partial_lse[(beg + k0 + lane) * R + row] - L) * kLog2e) : 0.f;
+            const float lk = k0 == 0 ? lse0 : (lane < kn ? partial_lse[(beg + k0 + lane) * R + row] : -INFINITY);
+            const float w = lane < kn ? exp2f((lk - L) * kLog2e) : 0.f;
+            if (k0 == 0) {
+#pragma unroll
+                for (int j = 0; j < kPre; ++j) {
+                    if (j >= kn) break;
+                    const float wj = __shfl_sync(0xffffffffu, w, j);
+                    acc.x += wj * pre[j].x;
+                    acc.y += wj * pre[j].y;
+                    acc.z += wj * pre[j].z;
+                    acc.w += wj * pre[j].w;
+                }
+            }
 #pragma unroll 8
-            for (int j = 0; j < kn; ++j) {
+            for (int j = k0 == 0 ? kPre : 0; j < kn; ++j) {
                 const float4 v =
                     *reinterpret_cast<const float4 *>(partial_o + ((beg + k0 + j) * R + row) * kHeadDim + lane * 4);
                 const float wj = __shfl_sync(0xffffffffu, w, j);

@@ -51,6 +51,27 @@ def test_fuzz_bit_exact(dsa):
         check_plan(dsa, lens, hkv, C, m)
 
 
+@pytest.mark.parametrize("units,ctas", [(256, 1), (257, 600), (1024, 4000), (1025, 152), (2048, 8191),
+                                         (2048, 8192), (2049, 304), (3000, 12288)])
+def test_kernel_shapes_bit_exact(dsa, units, ctas):
+    """Maps at the edges of each plan kernel: one warp (up to 256 units), 4 and 8 warps (1024,
+    2048), the bin table at its shared-memory limit (12287 CTAs), and the block kernel beyond
+    (more units, or more CTAs); lengths with empty requests and negative ones."""
+    rng = np.random.default_rng(units + ctas)
+    for hkv in (1, 8):
+        if units % hkv:
+            continue
+        B = units // hkv
+        lens = np.exp(rng.uniform(0, np.log(300_000), B)).astype(np.int64)
+        lens[rng.random(B) < 0.15] = 0
+        for m in (1, 4):
+            check_plan(dsa, lens, hkv, ctas, m)
+    lens = np.full(units, 100, np.int64)
+    lens[units // 2] = -7
+    got = check_plan(dsa, lens, 1, ctas, 2)
+    assert got["meta"][3] == dsa.DEV_BAD_SEQLEN
+
+
 def test_edge_cases(dsa):
     check_plan(dsa, [0, 0, 0], 2, 5, 4)            # no work
     check_plan(dsa, [1], 1, 1, 1)                  # one tile, one CTA
