@@ -419,6 +419,7 @@ def bench_ours(args, device, rank, world):
     # multi-token steps use one bin per SM: the tensor-memory kernel holds one CTA per SM
     multi = bench_multi(dsa, device, inp, w, sms, m, timer, nrep, nbytes, ms_per_step)
     layouts = bench_layouts(dsa, device, inp, w, C, m, timer, nrep, nbytes, t_dec)
+    chain = bench_chain(dsa, device, inp, w, C, m, timer, nrep)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     host = {k: inp[k].cpu().pin_memory() for k in ("q", "q_scale", "k_pages", "v_pages", "k_scale", "v_scale",
@@ -492,6 +493,7 @@ def bench_ours(args, device, rank, world):
         "prologue": prologue,
         "multi_token": multi,
         "page_layouts": layouts,
+        "layer_chain": chain,
         "balance": head["balance"],
         "workloads": others,
         "roofline": {"bound": "hbm", "kernel": "attn_kernel (persistent decode, dsa_decode)",
@@ -598,6 +600,57 @@ def bench_multi(dsa, device, inp, w, C: int, m: int, timer, steps: int, nbytes: 
             "decode_kv_GB/s": round(gbs, 1), "decode_frac_of_hbm_peak": round(gbs / peak, 4),
             "decode_TFLOP/s": round(flops / (t_dec * 1e-3) / 1e12, 1),
             "vs_q_len_one_token_steps": round(q_len * single_ms / step, 2)}
+    return res
+
+
+def bench_chain(dsa, device, inp, w, C: int, m: int, timer, steps: int, n_layers: int = 4) -> dict:
+    """A step of n_layers layers behind one plan: per layer the fused prologue (Q and the new
+    token of each request into the cache), the decode and the combine, one CUDA graph.  The
+    chained form starts each layer's KV gather (every layer but the first) while its prologue
+    runs (dsa_decode_chained); the plain form waits for the prologue (dsa_decode)."""
+    fp8 = w.kv_dtype == "fp8"
+    B, hq, hkv = int(inp["seq_lens"].shape[0]), w.num_q_heads, w.num_kv_heads
+    lens = inp["seq_lens"].cpu().numpy()
+    pin = workloads.make_prologue_inputs(B, hq, hkv, inp["num_pages"], seed=7, device=device, skip_fraction=0.0,
+                                         max_position=int(lens.max()) + 1)
+    bt = inp["block_table"].cpu().numpy()
+    pos = lens - 1
+    pin["positions"] = torch.from_numpy(pos.astype(np.int32)).to(device)
+    pin["slot_mapping"] = torch.from_numpy(
+        np.array([bt[b, p // 64] * 64 + p % 64 for b, p in enumerate(pos)], np.int32)).to(device)
+    qdt = torch.uint8 if fp8 else torch.bfloat16
+    q = torch.empty(B, hq, 128, dtype=qdt, device=device)
+    qs = torch.empty(B, hq, dtype=torch.float32, device=device) if fp8 else None
+    tm = dsa.TaskMap(B, hkv, C, device)
+    po, pl = dsa.partial_buffers(tm.max_descs, hq // hkv, device)
+    out = torch.empty(B, hq, 128, dtype=torch.bfloat16, device=device)
+    kw = dict(q_scale=qs, k_scale=inp["k_scale"], v_scale=inp["v_scale"])
+
+    def step(chained):
+        dsa.plan(inp["seq_lens"], hkv, C, m, task_map=tm)
+        for layer in range(n_layers):
+            dsa.prologue(pin["qkv"], hq, hkv, pin["slot_mapping"], inp["k_pages"], inp["v_pages"], inp["k_scale"],
+                         inp["v_scale"], positions=pin["positions"], cos_sin=pin["cos_sin"],
+                         q_norm_weight=pin["q_norm_weight"], k_norm_weight=pin["k_norm_weight"], hadamard=True,
+                         q_dtype=qdt, q_out=q, q_scale=qs)
+            args = (q, inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm, inp["sm_scale"])
+            if chained and layer > 0:
+                dsa.decode_chained(1, *args, partial_o=po, partial_lse=pl, **kw)
+            else:
+                dsa.decode(*args, partial_o=po, partial_lse=pl, **kw)
+            dsa.combine(tm, po, pl, hq, out=out)
+
+    res = {"layers": n_layers, "step": "plan, then per layer: dsa_prologue -> decode -> dsa_combine; one CUDA graph"}
+    for label, chained in (("plain", False), ("chained", True)):
+        for _ in range(3):
+            step(chained)
+        torch.cuda.synchronize()
+        if dsa.get_status(tm) != 0:
+            raise RuntimeError(f"layer chain ({label}): device status set")
+        ms = timer.whole([lambda chained=chained: step(chained)], steps)
+        res[f"{label}_us"] = stats_us(ms)
+    res["saved_us_per_chained_layer"] = round((res["plain_us"]["median"] - res["chained_us"]["median"]) /
+                                              (n_layers - 1), 2)
     return res
 
 

@@ -263,6 +263,32 @@ dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void *q, dsa_dt
                          uint64_t *cta_times, dsa_stream stream);
 
 /*
+ * dsa_decode_chained -- dsa_decode for one layer of a chain of layers that share one task
+ * map, starting the KV gather before the layer's Q is ready (SGLang Low-Latency Mode: Kernels
+ * and Runtime, section 2, item 1: the next kernel launches early and the attention kernel
+ * begins gathering KV before it waits for the query).  The kernel immediately before this call
+ * in the stream (normally the layer's prologue, dsa_prologue) writes Q (and its scales) and the
+ * newest new_tokens K/V tokens of every request; while it runs, the decode loads the first
+ * ring stages' tiles that hold none of those tokens, and waits for it before anything else.
+ * Caller's guarantee: the task map, seq_lens, block_table and every other K/V token of this
+ * layer were written by kernels that completed before that preceding kernel started -- e.g.
+ * the map was built before the previous layer's decode (every layer of a step but the first),
+ * the cache's older tokens by earlier steps.  Under that guarantee the results are those of
+ * dsa_decode, bit for bit.  The next kernel in the stream is released only after this one has
+ * waited for its predecessor, so the guarantee carries from layer to layer.
+ * One query token per request, pages of 64 tokens in HND layout; new_tokens >= 0 (0: every
+ * tile may be loaded early).  Other arguments and errors are as for dsa_decode.
+ */
+dsa_status dsa_decode_chained(int32_t new_tokens, const void *q, dsa_dtype q_dtype, const float *q_scale,
+                              const void *k_pages, const void *v_pages, dsa_dtype kv_dtype,
+                              const float *k_scale, const float *v_scale,
+                              const int32_t *block_table, int32_t max_pages_per_req, int32_t num_pages,
+                              const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
+                              const dsa_task_map *map, float *partial_o, float *partial_lse,
+                              dsa_stream stream);
+
+/*
  * dsa_combine_multi -- dsa_combine over the q_len * G partial rows of each unit:
  * out [B, q_len, Hq, 128] (out_dtype DSA_BF16 or DSA_FP32), out_lse [B, q_len, Hq] or
  * NULL.  q_len * G <= 64.  q_len = 1 is dsa_combine.

@@ -65,6 +65,8 @@ _lib.dsa_decode_multi.argtypes = [_i32] + _attn_args + [_TMP, _vp, _vp, _vp]
 _lib.dsa_decode_multi.restype = ctypes.c_int
 _lib.dsa_decode_ex.argtypes = [_i32, _i32] + _attn_args + [_TMP, _vp, _vp, _vp, _vp]
 _lib.dsa_decode_ex.restype = ctypes.c_int
+_lib.dsa_decode_chained.argtypes = [_i32] + _attn_args + [_TMP, _vp, _vp, _vp]
+_lib.dsa_decode_chained.restype = ctypes.c_int
 _lib.dsa_combine_multi.argtypes = [_i32, _TMP, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]
 _lib.dsa_combine_multi.restype = ctypes.c_int
 _lib.dsa_static_num_splits.argtypes = [_i32, _i32, _i32]
@@ -210,6 +212,21 @@ def decode(q, k_pages, v_pages, block_table, seq_lens, task_map: TaskMap, sm_sca
         rc = _lib.dsa_decode_ex(1, KV_LAYOUTS[kv_layout], *args, ctypes.byref(task_map.struct), _ptr(partial_o),
                                 _ptr(partial_lse), _ptr(cta_times), _stream(stream))
     _check(rc, "dsa_decode")
+    return partial_o, partial_lse
+
+
+def decode_chained(new_tokens: int, q, k_pages, v_pages, block_table, seq_lens, task_map: TaskMap, sm_scale: float,
+                   partial_o=None, partial_lse=None, q_scale=None, k_scale=None, v_scale=None, stream=None):
+    """dsa_decode_chained: dsa_decode that loads the tiles holding none of each request's newest
+    new_tokens tokens while the preceding kernel in the stream (the layer's prologue) runs."""
+    G = q.shape[1] // task_map.num_kv_heads
+    if partial_o is None:
+        partial_o, partial_lse = partial_buffers(task_map.max_descs, G, q.device)
+    args = _attn_args(q, k_pages, v_pages, block_table, seq_lens, task_map.num_kv_heads, sm_scale, q_scale, k_scale,
+                      v_scale)
+    rc = _lib.dsa_decode_chained(int(new_tokens), *args, ctypes.byref(task_map.struct), _ptr(partial_o),
+                                 _ptr(partial_lse), _stream(stream))
+    _check(rc, "dsa_decode_chained")
     return partial_o, partial_lse
 
 

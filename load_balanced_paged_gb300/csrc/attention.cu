@@ -260,8 +260,17 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
     }
     __syncthreads();
 
-    grid_launch_dependents();
-    grid_dependency_wait();  // task map, lengths, pages and Q from earlier kernels
+    // Early KV gather (dsa_decode_chained): the producer warp waits for the preceding kernel
+    // later, after issuing the tiles it may load before that kernel completes.  The next kernel
+    // may start only once this one has waited, so that whatever it reads before its own wait
+    // comes from kernels that have completed.
+    if (p.early == 0) {
+        grid_launch_dependents();
+        grid_dependency_wait();  // task map, lengths, pages and Q from earlier kernels
+    } else if (warp != NCW) {
+        grid_dependency_wait();
+        grid_launch_dependents();
+    }
     EndStamp end_stamp{nullptr};
     if (p.cta_times) {  // uniform over the CTA
         uint64_t *t = p.cta_times + 2 * (blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
@@ -273,8 +282,9 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
     // ---- this CTA's work
     int d_begin = 0, d_count = 1, st0 = 0, st1 = 0;
     if (PERSIST) {
-        d_begin = p.cta_desc_begin[blockIdx.x];
-        d_count = p.cta_desc_begin[blockIdx.x + 1] - d_begin;
+        // (the producer of dsa_decode_chained reads these before its wait)
+        d_begin = early_load<!FUSE && QW == 0>(p.cta_desc_begin + blockIdx.x);
+        d_count = early_load<!FUSE && QW == 0>(p.cta_desc_begin + blockIdx.x + 1) - d_begin;
         if (FUSE && warp == NCW + 1) {
             // units with no tiles have no descriptor: their output is 0 and their LSE -inf
             for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
@@ -311,8 +321,8 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
     }
 
     if (warp == NCW) {
-        producer_warp<KV, STAGES, PERSIST, FUSE, false, L>(&kmap, &vmap, p, smem, sbase, bar0, nvalid, abort_flag,
-                                                           epi_total, d_begin, d_count, st0, st1, lane);
+        producer_warp<KV, STAGES, PERSIST, FUSE, false, L, PERSIST && !FUSE && QW == 0>(
+            &kmap, &vmap, p, smem, sbase, bar0, nvalid, abort_flag, epi_total, d_begin, d_count, st0, st1, lane);
         return;
     }
 
@@ -1121,14 +1131,16 @@ extern "C" int32_t dsa_multi_slots_per_desc(int32_t q_len, int32_t group) {
     return q_len > 1 ? 2 : 1;
 }
 
-extern "C" dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void *q, dsa_dtype q_dtype,
-                                    const float *q_scale, const void *k_pages, const void *v_pages,
-                                    dsa_dtype kv_dtype, const float *k_scale, const float *v_scale,
-                                    const int32_t *block_table, int32_t max_pages_per_req, int32_t num_pages,
-                                    const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
-                                    int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
-                                    const dsa_task_map *map, float *partial_o, float *partial_lse,
-                                    uint64_t *cta_times, dsa_stream stream) {
+namespace {
+
+// dsa_decode_ex, and dsa_decode_chained when new_tokens >= 0 (early KV gather, one query token).
+dsa_status decode_impl(int32_t q_len, int32_t kv_layout, const void *q, dsa_dtype q_dtype, const float *q_scale,
+                       const void *k_pages, const void *v_pages, dsa_dtype kv_dtype, const float *k_scale,
+                       const float *v_scale, const int32_t *block_table, int32_t max_pages_per_req,
+                       int32_t num_pages, const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
+                       const dsa_task_map *map, float *partial_o, float *partial_lse, uint64_t *cta_times,
+                       int32_t new_tokens, dsa_stream stream) {
     const AttnArgs a{q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale, block_table,
                      max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
                      page_size, sm_scale, kv_layout};
@@ -1147,6 +1159,10 @@ extern "C" dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void
     kp.cta_desc_begin = map->cta_desc_begin;
     kp.descs = reinterpret_cast<const int4 *>(map->descs);
     kp.cta_times = cta_times;
+    if (new_tokens >= 0) {
+        kp.early = 1;
+        kp.new_tokens = new_tokens;
+    }
     if (q_len == 1) {
         if (kv_dtype == DSA_BF16) return launch_persistent<0, false>(a, kp, map->num_ctas, to_cuda(stream));
         return launch_persistent<1, false>(a, kp, map->num_ctas, to_cuda(stream));
@@ -1162,6 +1178,35 @@ extern "C" dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void
     }
     // bf16 K/V: the tensor-memory kernel, for any number of query rows up to 64
     return launch_tc(a, kp, map->num_ctas, to_cuda(stream));
+}
+
+}  // namespace
+
+extern "C" dsa_status dsa_decode_ex(int32_t q_len, int32_t kv_layout, const void *q, dsa_dtype q_dtype,
+                                    const float *q_scale, const void *k_pages, const void *v_pages,
+                                    dsa_dtype kv_dtype, const float *k_scale, const float *v_scale,
+                                    const int32_t *block_table, int32_t max_pages_per_req, int32_t num_pages,
+                                    const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t page_size, float sm_scale,
+                                    const dsa_task_map *map, float *partial_o, float *partial_lse,
+                                    uint64_t *cta_times, dsa_stream stream) {
+    return decode_impl(q_len, kv_layout, q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale,
+                       block_table, max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads,
+                       head_dim, page_size, sm_scale, map, partial_o, partial_lse, cta_times, -1, stream);
+}
+
+extern "C" dsa_status dsa_decode_chained(int32_t new_tokens, const void *q, dsa_dtype q_dtype, const float *q_scale,
+                                         const void *k_pages, const void *v_pages, dsa_dtype kv_dtype,
+                                         const float *k_scale, const float *v_scale, const int32_t *block_table,
+                                         int32_t max_pages_per_req, int32_t num_pages, const int32_t *seq_lens,
+                                         int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t page_size, float sm_scale,
+                                         const dsa_task_map *map, float *partial_o, float *partial_lse,
+                                         dsa_stream stream) {
+    if (new_tokens < 0) return DSA_ERR_INVALID_ARG;
+    return decode_impl(1, DSA_HND, q, q_dtype, q_scale, k_pages, v_pages, kv_dtype, k_scale, v_scale, block_table,
+                       max_pages_per_req, num_pages, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                       page_size, sm_scale, map, partial_o, partial_lse, nullptr, new_tokens, stream);
 }
 
 extern "C" dsa_status dsa_decode(const void *q, dsa_dtype q_dtype, const float *q_scale, const void *k_pages,

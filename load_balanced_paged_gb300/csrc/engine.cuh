@@ -47,6 +47,10 @@ struct KernelParams {
     int32_t out_bf16;
     float *out_lse;          // [B, Hq] or null
     uint64_t *cta_times;     // null, or [CTAs][2]: %globaltimer ns when a CTA starts work and ends
+    // early KV gather (dsa_decode_chained): the producer loads the first ring pass of tiles that
+    // hold none of the newest new_tokens tokens of their request before waiting for the
+    // preceding kernel (which writes those tokens and Q)
+    int32_t early, new_tokens;
 };
 
 // Stamps the end of a CTA's work: every warp raises the CTA's end time as it leaves.
@@ -100,11 +104,21 @@ struct DescInfo {
 };
 static_assert(sizeof(DescInfo) == kDescInfoBytes, "DescInfo slot size");
 
-template <bool PERSIST>
+// Loads that a producer with the early KV gather may issue before its grid dependency wait go
+// to L2 (ld.global.cg), past any line this SM cached before the data's writer completed.
+template <bool EARLY, typename T>
+__device__ __forceinline__ T early_load(const T *ptr) {
+    if constexpr (EARLY)
+        return __ldcg(ptr);
+    else
+        return *ptr;
+}
+
+template <bool PERSIST, bool EARLY = false>
 __device__ __forceinline__ Desc get_desc(const KernelParams &p, int d_begin, int i, int t0s, int t1s) {
     Desc x;
     if (PERSIST) {
-        const int4 v = p.descs[d_begin + i];
+        const int4 v = early_load<EARLY>(p.descs + d_begin + i);
         x.u = v.x;
         x.t0 = v.y;
         x.t1 = v.z;
@@ -167,9 +181,10 @@ dsa_status launch_tc(const AttnArgs &a, const KernelParams &kp, int num_ctas, cu
 // kStageTx, kQSlots); from bar0 the barriers are full[STAGES], empty[STAGES], qfull[kQSlots],
 // qempty[kQSlots].  TC: the tensor-memory kernel, whose S warp fetches each descriptor's Q
 // itself and whose operands want each 128-byte half of a page smaller than the tile as its
-// own box.  The whole warp calls this; it returns when the CTA's tiles are all issued (or the
-// CTA aborted and its copies have landed).
-template <int KV, int STAGES, bool PERSIST, bool FUSE, bool TC, class L>
+// own box.  EARLY: the early KV gather is built in (it runs when p.early is set).  The whole
+// warp calls this; it returns when the CTA's tiles are all issued (or the CTA aborted and its
+// copies have landed).
+template <int KV, int STAGES, bool PERSIST, bool FUSE, bool TC, class L, bool EARLY = false>
 __device__ __forceinline__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap, const KernelParams &p,
                                               uint8_t *smem, uint32_t sbase, uint32_t bar0, int *nvalid,
                                               volatile int *abort_flag, volatile int *epi_total, int d_begin,
@@ -195,43 +210,54 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap *kmap, const CUt
     int qi = 0;         // descriptors handed to the consumers
     int q_issued = -1;  // hand-off index of the last Q copy issued
     bool aborted = false;
+    // early KV gather: the kernel's other warps wait for the preceding kernel at once; this warp
+    // first issues the tiles it may (see below), then waits
+    bool waited = !EARLY || p.early == 0;
     for (int wbase = 0; wbase < d_count && !aborted; wbase += 32) {
         // ---- window: descriptor wbase + lane
         int wb = 0, wh = 0, wt0 = 0, wn = 0, wslot = 0, wlen = 0, wnp = 1, wpbeg = 0;
+        bool wok = false;
         float wqs[kMaxGroup];
 #pragma unroll
         for (int g = 0; g < kMaxGroup; ++g) wqs[g] = 0.f;
         if (wbase + lane < d_count) {
-            const Desc x = get_desc<PERSIST>(p, d_begin, wbase + lane, st0, st1);
+            const Desc x = get_desc<PERSIST, EARLY>(p, d_begin, wbase + lane, st0, st1);
             if (x.ok) {
+                wok = true;
                 wb = x.u / p.hkv;
                 wh = x.u - wb * p.hkv;
                 wt0 = x.t0;
                 wn = x.t1 - x.t0;
                 wslot = x.slot;
-                wlen = p.seq_lens[wb];
+                wlen = early_load<EARLY>(p.seq_lens + wb);
                 if (FUSE) {
                     wnp = p.unit_num_partials[x.u];
                     wpbeg = p.unit_partial_begin[x.u];
                 }
                 if (wlen < 0 || wlen > p.max_pages * p.page_size) atomicOr(p.status, DSA_DEV_BAD_SEQLEN);
-                if (KV == 1) {
-                    const float *qs = p.q_scale + static_cast<int64_t>(wb) * p.hq + wh * G;
-#pragma unroll
-                    for (int g = 0; g < kMaxGroup; ++g)
-                        if (g < G) wqs[g] = qs[g];
-                }
-                if (wn == 0) {  // no tiles: its partials are empty, the consumers never see it
-                    const int R = p.q_len * G;
-                    const int64_t s0 = static_cast<int64_t>(wslot) * p.slots_per_desc;
-                    for (int i = 0; i < p.slots_per_desc * R * kHeadDim; ++i)
-                        p.partial_o[s0 * R * kHeadDim + i] = 0.f;
-                    for (int g = 0; g < p.slots_per_desc * R; ++g) p.partial_lse[s0 * R + g] = -INFINITY;
-                }
             } else {
                 atomicOr(p.status, DSA_DEV_BAD_MAP);
             }
         }
+        // what depends on the preceding kernel (Q scales) or may race with its reads (partial
+        // outputs): after the grid dependency wait
+        auto finish_window = [&]() {
+            if (wbase + lane >= d_count) return;
+            if (KV == 1) {
+                const float *qs = p.q_scale + static_cast<int64_t>(wb) * p.hq + wh * G;
+#pragma unroll
+                for (int g = 0; g < kMaxGroup; ++g)
+                    if (g < G) wqs[g] = qs[g];
+            }
+            if (wok && wn == 0) {  // no tiles: its partials are empty, the consumers never see it
+                const int R = p.q_len * G;
+                const int64_t s0 = static_cast<int64_t>(wslot) * p.slots_per_desc;
+                for (int i = 0; i < p.slots_per_desc * R * kHeadDim; ++i)
+                    p.partial_o[s0 * R * kHeadDim + i] = 0.f;
+                for (int g = 0; g < p.slots_per_desc * R; ++g) p.partial_lse[s0 * R + g] = -INFINITY;
+            }
+        };
+        if (waited) finish_window();
         // stream offset of each descriptor in the window (exclusive scan of tile counts)
         int incl = wn;
 #pragma unroll
@@ -260,7 +286,7 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap *kmap, const CUt
                 const int idx = t * ppt + k;
                 pg[k] = -1;
                 if (k < ppt && s < wtotal && idx < p.max_pages)
-                    pg[k] = p.block_table[static_cast<int64_t>(bj) * p.max_pages + idx];
+                    pg[k] = early_load<EARLY>(p.block_table + static_cast<int64_t>(bj) * p.max_pages + idx);
             }
         };
 
@@ -301,11 +327,20 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap *kmap, const CUt
             //      descriptors starting in the chunk are handed to the consumers in order,
             //      each as soon as a hand-off slot is free.  Nothing waits in a divergent
             //      loop: lanes spinning on their own barriers starved one another.
-            bool pend = lane < cnt;
-            uint32_t todo = starts;  // descriptor starts not yet handed off
             const int cl = c + lane;
             const int stage = cl % STAGES;
             const uint32_t epar = ((cl / STAGES) & 1) ^ 1;
+            // Early KV gather (first chunk only): pass 0 issues the first ring pass of the tiles
+            // that hold none of the request's newest new_tokens tokens, with no hand-offs (Q is
+            // the preceding kernel's output); then the warp waits for that kernel.  Pass 1 is
+            // the loop over everything else.
+            const bool early_l = EARLY && !waited && lane < cnt && lane < STAGES && nv_l > 0 &&
+                                 ct * kTile + kTile <= len_l - p.new_tokens;
+            uint32_t todo = 0;  // descriptor starts not yet handed off
+            bool pend = false;
+            for (int pass = (!EARLY || waited) ? 1 : 0; pass < 2; ++pass) {
+            pend = pass == 0 ? early_l : (lane < cnt && !early_l);
+            todo = pass == 0 ? 0u : starts;
             uint64_t idle_t0 = globaltimer_ns();  // last progress
             for (uint32_t it = 1;; ++it) {
                 const uint32_t done = __ballot_sync(0xffffffffu, !pend);
@@ -435,6 +470,14 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap *kmap, const CUt
                         break;
                     }
                 }
+            }
+            if (aborted) break;
+            if (EARLY && pass == 0) {
+                grid_dependency_wait();  // Q, its scales and the newest tokens are in memory now
+                grid_launch_dependents();
+                waited = true;
+                finish_window();
+            }
             }
             if (aborted) {
                 // tiles up to the last one issued are counted for the drain below

@@ -122,6 +122,23 @@ def test_decode_ex_host_checks(lib):
     assert call(q_len=9, q_dt=1, kv_dt=1, scales=fake) == 2  # 72 query rows per unit
 
 
+def test_chained_decode_host_checks(lib):
+    fake = ctypes.c_void_p(0x10000)
+    tm = TaskMap(fake, fake, fake, fake, fake, 10, 4, 16)
+    i, f, V = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
+    lib.dsa_decode_chained.argtypes = [i, V, i, V, V, V, i, V, V, V, i, i, V, i, i, i, i, i, f,
+                                       ctypes.POINTER(TaskMap), V, V, V]
+
+    def call(new_tokens=1, d=128, page=64, hq=64, batch=2):
+        return lib.dsa_decode_chained(new_tokens, fake, 0, None, fake, fake, 0, None, None, fake, 4, 8, fake, batch,
+                                      hq, 8, d, page, 0.1, ctypes.byref(tm), fake, fake, None)
+    assert call(new_tokens=-1) == 1
+    assert call(d=64) == 2
+    assert call(page=8) == 2
+    assert call(hq=63) == 1
+    assert call(batch=3) == 1              # map sized for another batch
+
+
 def test_noalloc_host_checks(lib):
     """dsa_decode_step_noalloc refuses, before it touches the device, every argument that one
     of its three kernels' entry points would refuse, so a step is never half enqueued."""
