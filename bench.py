@@ -99,21 +99,40 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "window": window}
 
 
+# The sources each profiled kernel is built from; a committed capture records their combined
+# digest, and its counters are used only while the sources are unchanged.
+KERNEL_SOURCES = {
+    "decode": ("attention.cu", "engine.cuh", "ptx.cuh", "common.h"),
+    "multi": ("attention_tc.cu", "engine.cuh", "ptx.cuh", "common.h"),
+    "plan": ("plan.cu", "ptx.cuh", "common.h"),
+    "combine": ("combine.cu", "ptx.cuh", "common.h"),
+    "prologue": ("prologue.cu", "ptx.cuh", "common.h"),
+}
+
+
+def sources_digest(kind: str) -> str:
+    """sha256 over the concatenated sources of one kernel family (csrc/, in the listed order)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "load_balanced_paged_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def profile_traffic(workload: str, nbytes: int):
     """DRAM traffic per decode launch from the committed ncu summary of this workload's
     decode kernel (profiles/decode_<workload>[_small].md), scaled by KV bytes when the
-    capture was a smaller case of the same workload; None once the kernel source differs
-    from the one captured."""
-    import hashlib
+    capture was a smaller case of the same workload; None once the kernel's sources differ
+    from the ones captured."""
     import re
-    src = os.path.join(ROOT, "load_balanced_paged_gb300", "csrc", "attention.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    sha = sources_digest("decode")
     for suffix in ("", "_small"):
         path = os.path.join(ROOT, "profiles", f"decode_{workload}{suffix}.md")
         if not os.path.exists(path):
             continue
         text = open(path).read()
-        m_sha = re.search(r"sha256 `([0-9a-f]{64})`", text)
+        m_sha = re.search(r"sources sha256 `([0-9a-f]{64})`", text)
         m_tr = re.search(r"traffic_bytes_per_launch: (\d+)", text)
         m_alg = re.search(r"algorithmic_bytes_per_launch: (\d+)", text)
         if not (m_sha and m_tr and m_alg) or m_sha.group(1) != sha:
