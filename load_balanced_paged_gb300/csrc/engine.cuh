@@ -176,6 +176,14 @@ bool make_pool_map(CUtensorMap *m, const void *pool, int kv, int num_pages, int 
 // The tensor-memory multi-token kernel over a task map's num_ctas bins (attention_tc.cu).
 dsa_status launch_tc(const AttnArgs &a, const KernelParams &kp, int num_ctas, cudaStream_t st);
 
+// attention.cu: the launch parameters every decode call starts from, and its kernels' launchers
+// (the CTA shape is chosen from the bin count and the SM count).
+KernelParams base_params(const AttnArgs &a, float *partial_o, float *partial_lse, int32_t *status);
+dsa_status launch_decode(const AttnArgs &a, const KernelParams &kp, int num_ctas, bool fused, cudaStream_t st);
+dsa_status launch_multi_mma(const AttnArgs &a, const KernelParams &kp, int num_ctas, cudaStream_t st);
+dsa_status launch_static(const AttnArgs &a, const KernelParams &kp, dim3 grid, cudaStream_t st);
+dsa_status launch_wait_selftest(int32_t *status, uint64_t limit_ns, cudaStream_t st);
+
 // ---------------------------------------------------------------------------------------
 // Producer warp.  L supplies the shared-memory layout (kInfoOff, kQOff, kQSlot, kStageBytes,
 // kStageTx, kQSlots); from bar0 the barriers are full[STAGES], empty[STAGES], qfull[kQSlots],
