@@ -312,9 +312,10 @@ class Step:
 
 
 def bench_static(dsa, step: Step, timer: Timer, reps: int, device, t_dec_comb: float, t_step: float) -> dict:
-    """Both static split-KV forms on the step's inputs (decode + its combine), timed the same
-    way, with how evenly each static grid's CTAs finish (one untimed launch with per-CTA
-    timestamps)."""
+    """Both static split-KV forms on the step's inputs (decode + its combine, one CUDA graph
+    replayed like the dynamic step), with how evenly each static grid's CTAs finish (one
+    untimed launch with per-CTA timestamps).  t_dec_comb / t_step: the dynamic decode + combine
+    and plan + decode + combine graphs' median replay times (ms)."""
     inp, B, hq, hkv, G = step.inp, step.B, step.hq, step.hkv, step.G
     static = {}
     max_len = int(inp["seq_lens"].max().item())
@@ -332,11 +333,13 @@ def bench_static(dsa, step: Step, timer: Timer, reps: int, device, t_dec_comb: f
             dsa.static_combine(S, spo, spl, B, hq, hkv, out=step.out, out_lse=step.out_lse)
 
         sp = timer.per_kernel([sdec, scomb], reps, 3)
+        whole = timer.whole([sdec, scomb], reps)
         if dsa.read_status(sst) != 0:
             raise RuntimeError(f"{label}: device status set")
-        tot = sp.sum(axis=1)
-        s_ms = float(tot.mean())
-        static[label] = {"splits": S, "us_per_step": round(s_ms * 1e3, 2), "us": stats_us(tot),
+        s_ms = float(np.median(whole))
+        static[label] = {"splits": S, "us_per_step": round(s_ms * 1e3, 2), "us": stats_us(whole),
+                         "breakdown_us": {"decode": round(float(np.median(sp[:, 0])) * 1e3, 2),
+                                          "combine": round(float(np.median(sp[:, 1])) * 1e3, 2)},
                          "speedup_of_dynamic": round(s_ms / t_dec_comb, 3),
                          "speedup_of_dynamic_with_plan": round(s_ms / t_step, 3)}
         st_times = torch.zeros(B * hkv * S, 2, dtype=torch.int64, device=device)
@@ -364,13 +367,14 @@ def measure_workload(dsa, device, name: str, args, rank: int, world: int, reps: 
     time.sleep(0.3)
     t0 = time.time()
     whole = timer.whole(fns, reps)
+    whole_dc = timer.whole([step.decode, step.combine], reps)  # the map built above serves every replay
     per = timer.per_kernel(fns, reps, 0)
     t1 = time.time()
     clocks.stop()
     step.check(f"the {name} workload (timed)")
     t_plan, t_dec, t_comb = (float(x) for x in per.mean(axis=0))
     t_step = float(whole.mean())
-    static = bench_static(dsa, step, timer, reps, device, t_dec + t_comb, t_step)
+    static = bench_static(dsa, step, timer, reps, device, float(np.median(whole_dc)), float(np.median(whole)))
     dyn_times = torch.zeros(C, 2, dtype=torch.int64, device=device)
     step.decode(cta_times=dyn_times)
     peak, _ = measured_peaks()
@@ -378,6 +382,7 @@ def measure_workload(dsa, device, name: str, args, rank: int, world: int, reps: 
     step_gbs = nbytes / (t_step * 1e-3) / 1e9
     rec = {"config": workload_config(w, step.B, C, args.min_tiles, nbytes, l2_note, world),
            "step": "plan -> decode -> combine, one CUDA graph", "step_us": stats_us(whole),
+           "decode_combine_us": stats_us(whole_dc),
            "breakdown_us": {k: stats_us(per[:, i]) for i, k in enumerate(("plan", "decode", "combine"))},
            "decode_GB/s": round(dec_gbs, 1), "decode_frac_of_hbm_peak": round(dec_gbs / peak, 4),
            "decode_frac_of_hbm_peak_median": round(nbytes / (float(np.median(per[:, 1])) * 1e-3) / 1e9 / peak, 4),
@@ -434,6 +439,9 @@ def bench_ours(args, device, rank, world):
     step.check("the fused step (timed)")
     nrep = max(10, min(args.steps, 200))
     prologue = bench_prologue(dsa, device, w, B, timer, nrep)
+    # the same chain writing an E4M3 cache (the FP8 workload's heads), whatever the headline's dtype
+    wf = workloads.WORKLOADS["fp8"]
+    prologue_e4m3 = prologue if w.kv_dtype == "fp8" else bench_prologue(dsa, device, wf, B, timer, nrep)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     # multi-token steps use one bin per SM: the tensor-memory kernel holds one CTA per SM
     multi = bench_multi(dsa, device, inp, w, sms, m, timer, nrep, nbytes, ms_per_step)
@@ -510,6 +518,7 @@ def bench_ours(args, device, rank, world):
         "pct_of_nominal_8tbs": round(100 * nbytes / (ms_per_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 1),
         "static": head["static"],
         "prologue": prologue,
+        "prologue_e4m3": prologue_e4m3,
         "multi_token": multi,
         "page_layouts": layouts,
         "layer_chain": chain,
