@@ -225,7 +225,10 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                 if constexpr (KV == 0) {
                 // 128-byte-swizzled K-major operand (as the TMA lays out K): dims 64 b .. 64 b + 63
                 // of row r at b * 8 KB + r * 128 B, 16-byte chunk c at (c ^ (r % 8)) * 16.  Each
-                // quarter-warp writes one 128-byte row: no bank conflicts either way.
+                // quarter-warp writes one 128-byte row: no bank conflicts either way.  A negative
+                // softmax scale is moved onto Q (its sign bits flipped, exact), so that the
+                // softmax sees S x |scale| and may take the maximum of the raw scores.
+                const uint32_t qneg = p.score_scale < 0.f ? 0x80008000u : 0u;
 #pragma unroll
                 for (int rd = 0; rd < 4; ++rd) {
                     uint4 v[8];
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                         const int i = lane + 32 * (8 * rd + it), r = i >> 4, kc = i & 15;
                         v[it] = r < R ? *reinterpret_cast<const uint4 *>(src + r * (kHeadDim * 2) + kc * 16)
                                       : make_uint4(0u, 0u, 0u, 0u);
+                        v[it].x ^= qneg, v[it].y ^= qneg, v[it].z ^= qneg, v[it].w ^= qneg;
                     }
 #pragma unroll
                     for (int it = 0; it < 8; ++it) {
@@ -384,6 +388,7 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
         const int team = warp >> 2, sp = warp & 3;
         const int gid = lane >> 2, tig = lane & 3;
         const int ra = 16 * sp + gid, rb = ra + 8;
+        const bool rows = 16 * sp < R;  // the warp holds at least one query row (warp-uniform)
         const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
         const uint32_t o_col = 256 + 128 * team;
         const int tid = sp * 32 + lane;  // within the team
@@ -492,7 +497,7 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                 const int nv = nvalid[stage];
                 tc_fence_after();
                 float sv[8][4];  // [column block k][(ra, 2tig), (ra, 2tig+1), (rb, 2tig), (rb, 2tig+1)]
-                if (nv > 0) {
+                if (nv > 0 && rows) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + 64 * buf + 8 * k, sv[k]);
                     tmem_wait_ld();
@@ -509,6 +514,28 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                 auto wait_prev_pv = [&]() {
                     return prev_g < 0 || wait_phase(o_done(team), ((g >> 1) & 1) ^ 1, abort_flag, p.status);
                 };
+                // O_team rows ra, rb *= fa, fb, after the team's previous P.V into it
+                auto rescale_o = [&](float fa, float fb) -> bool {
+                    if (!wait_prev_pv()) return false;
+                    tc_fence_after();
+#pragma unroll 1  // rare: kept small for the instruction cache
+                    for (int half = 0; half < 2; ++half) {
+                        float o[8][4];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + o_col + 64 * half + 8 * k, o[k]);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            o[k][0] *= fa;
+                            o[k][1] *= fa;
+                            o[k][2] *= fb;
+                            o[k][3] *= fb;
+                            tmem_st16x8(tmem + lane_base + o_col + 64 * half + 8 * k, o[k]);
+                        }
+                        tmem_wait_st();
+                    }
+                    return true;
+                };
                 if (nv == 0) {  // no data in this stage: the PV warp skips its P.V
                     if (!wait_prev_pv()) {
                         failed = true;
@@ -523,28 +550,102 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                     }
                     continue;
                 }
-                // ---- E4M3: S times the K scale of its column; P's factor per column, the V
-                //      scale over the reference, which moves only when a larger scale appears
-                //      (O is then rescaled with the maxima below); columns past nv get 0
-                float vw[8][2];
-                float vf = 1.f;
-                if constexpr (KV == 1) {
+                // A warp whose 16 rows all lie past R (rows 48-63 at q_len 6 and G = 8) has no
+                // softmax to do: its rows of S are zero (Q is zero there), their P lanes keep
+                // those zeros, and its rows of O are never read out.  It still takes its share
+                // of the stage's V work below and hands the buffer over with the team.
+                if constexpr (KV == 0) {
+                    if (rows) {
+                        // ---- running maximum over each row's visible tokens (t < lim, slot < nv)
+                        //      of the raw scores, scaled once: the scale is non-negative here (the
+                        //      S warp negated Q for a negative one)
+                        const float sc = fabsf(p.score_scale);
+                        const int tt = (dt0 + li) * kTile;
+                        const int vis[2] = {max(0, min(nv, lim[0] - tt)), max(0, min(nv, lim[1] - tt))};
+                        const bool full = vis[0] == kTile && vis[1] == kTile;
+                        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int h = e >> 1, j = 8 * k + 2 * tig + (e & 1);
+                                mx[h] = fmaxf(mx[h], (full || j < vis[h]) ? sv[k][e] : -INFINITY);
+                            }
+                        bool grow[2];
+                        float alpha[2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+                            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+                            const float mnew = fmaxf(m[h], mx[h] * sc);  // -inf x 0 = NaN is ignored
+                            grow[h] = m[h] != -INFINITY && mnew > m[h] + 8.f;
+                            alpha[h] = grow[h] ? ex2(m[h] - mnew) : 1.f;
+                            if (grow[h] || m[h] == -INFINITY) m[h] = mnew;
+                        }
+                        if (__any_sync(0xffffffffu, grow[0] || grow[1])) {
+                            if (!rescale_o(alpha[0], alpha[1])) {
+                                failed = true;
+                                break;
+                            }
+                            l[0] *= alpha[0];
+                            l[1] *= alpha[1];
+                        }
+                        // ---- P = 2^(s * scale - m) (0 where not visible) as bf16 high part (the top
+                        //      16 bits) and low part (the rest, rounded), written over S in the
+                        //      buffer: the P.V's A operand, tokens (2c, 2c + 1) packed in column c
+                        //      (high part: columns 0-31, low part: 32-63)
+                        const float nm0 = -m[0], nm1 = -m[1];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            float pv[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int h = e >> 1, j = 8 * k + 2 * tig + (e & 1);
+                                const float q = ex2(fmaf(sv[k][e], sc, h ? nm1 : nm0));
+                                pv[e] = (full || j < vis[h]) ? q : 0.f;
+                            }
+                            l[0] += pv[0] + pv[1];
+                            l[1] += pv[2] + pv[3];
+                            const uint32_t h0 = __float_as_uint(pv[0]) & 0xFFFF0000u, h1 = __float_as_uint(pv[1]) & 0xFFFF0000u;
+                            const uint32_t h2 = __float_as_uint(pv[2]) & 0xFFFF0000u, h3 = __float_as_uint(pv[3]) & 0xFFFF0000u;
+                            tmem_st16x4(tmem + lane_base + 64 * buf + 4 * k, prmt(h0, h1, 0x7632u), prmt(h2, h3, 0x7632u));
+                            tmem_st16x4(tmem + lane_base + 64 * buf + 32 + 4 * k,
+                                        pack_bf16x2(pv[0] - __uint_as_float(h0), pv[1] - __uint_as_float(h1)),
+                                        pack_bf16x2(pv[2] - __uint_as_float(h2), pv[3] - __uint_as_float(h3)));
+                        }
+                        tmem_wait_st();
+                    }
+                } else if (rows) {
+                    // ---- E4M3: base-2 scores t = s x score scale x the row's Q scale x the
+                    //      column's K scale, two columns per instruction, scaled before the maximum
+                    //      (any sign of the scales is handled).  P's factor per column: the V scale
+                    //      over the reference, which moves only when a larger scale appears (O is
+                    //      then rescaled with the maxima below); columns past nv get 0
+                    float2 vw[8];
+                    float vf = 1.f;
                     const float *ksm = reinterpret_cast<const float *>(smem + stage * L::kStageBytes + 2 * C::kTileBytes);
                     const float *vsm = ksm + kTile;
-                    float vmax = 0.f;
+                    const float2 qa = make_float2(qsc[0], qsc[0]), qb = make_float2(qsc[1], qsc[1]);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const int j = 8 * k + 2 * tig;
                         const float2 kk = *reinterpret_cast<const float2 *>(ksm + j);
-                        const float2 vv = *reinterpret_cast<const float2 *>(vsm + j);
-                        sv[k][0] *= kk.x;
-                        sv[k][1] *= kk.y;
-                        sv[k][2] *= kk.x;
-                        sv[k][3] *= kk.y;
-                        vw[k][0] = j < nv ? vv.x : 0.f;
-                        vw[k][1] = j + 1 < nv ? vv.y : 0.f;
-                        vmax = fmaxf(vmax, fmaxf(vw[k][0], vw[k][1]));
+                        vw[k] = *reinterpret_cast<const float2 *>(vsm + j);
+                        const float2 a = mul2(make_float2(sv[k][0], sv[k][1]), mul2(kk, qa));
+                        const float2 b = mul2(make_float2(sv[k][2], sv[k][3]), mul2(kk, qb));
+                        sv[k][0] = a.x, sv[k][1] = a.y, sv[k][2] = b.x, sv[k][3] = b.y;
                     }
+                    if (nv < kTile) {  // uniform over the CTA: the stage's valid-token count
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int j = 8 * k + 2 * tig;
+                            if (j >= nv) vw[k].x = 0.f;
+                            if (j + 1 >= nv) vw[k].y = 0.f;
+                        }
+                    }
+                    float vmax = fmaxf(vw[0].x, vw[0].y);
+#pragma unroll
+                    for (int k = 1; k < 8; ++k) vmax = max3f(vmax, vw[k].x, vw[k].y);
                     if (__any_sync(0xffffffffu, vmax > vref)) {  // the quad's four lanes cover the 64 columns
                         vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
                         vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
@@ -554,98 +655,73 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                             vinv = 1.f / vmax;
                         }
                     }
+                    const float2 vi = make_float2(vinv, vinv);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) vw[k] = mul2(vw[k], vi);
+                    // ---- columns a row may not see (slot >= nv, past its draft token's causal
+                    //      limit, or a row past R) are -inf: P = 2^-inf = 0 there, whatever the
+                    //      slot held
+                    const int tt = (dt0 + li) * kTile;
+                    const int vis0 = max(0, min(nv, lim[0] - tt)), vis1 = max(0, min(nv, lim[1] - tt));
+                    if (vis0 < kTile || vis1 < kTile) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int j = 8 * k + 2 * tig + (e & 1);
+                                if (j >= ((e >> 1) ? vis1 : vis0)) sv[k][e] = -INFINITY;
+                            }
+                    }
+                    // ---- running maximum of each row (three-input maxima, then the quad)
+                    float mx[2] = {fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[0][2], sv[0][3])};
+#pragma unroll
+                    for (int k = 1; k < 8; ++k) {
+                        mx[0] = max3f(mx[0], sv[k][0], sv[k][1]);
+                        mx[1] = max3f(mx[1], sv[k][2], sv[k][3]);
+                    }
+                    bool grow[2];
+                    float alpha[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+                        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+                        const float mnew = fmaxf(m[h], mx[h]);
+                        grow[h] = m[h] != -INFINITY && mnew > m[h] + 8.f;
+                        alpha[h] = grow[h] ? ex2(m[h] - mnew) : 1.f;
+                        if (grow[h] || m[h] == -INFINITY) m[h] = mnew;
+                    }
+                    // rows whose maximum grew, and all rows by the V reference's change
+                    if (__any_sync(0xffffffffu, grow[0] || grow[1] || vf != 1.f)) {
+                        if (!rescale_o(alpha[0] * vf, alpha[1] * vf)) {
+                            failed = true;
+                            break;
+                        }
+                        l[0] *= alpha[0];
+                        l[1] *= alpha[1];
+                    }
+                    // ---- P = 2^(t - m) x the column's V factor (<= 2^8) as f16, written over S
+                    //      in the buffer, tokens (2c, 2c + 1) packed in column c: the P.V's A
+                    //      operand.  A row that has seen nothing yet has m = -inf and only -inf
+                    //      scores: P = 0.
+                    const float n0 = m[0] == -INFINITY ? 0.f : -m[0], n1 = m[1] == -INFINITY ? 0.f : -m[1];
+                    const float2 nm0 = make_float2(n0, n0), nm1 = make_float2(n1, n1);
+                    float2 la = make_float2(0.f, 0.f), lb = la;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        vw[k][0] *= vinv;
-                        vw[k][1] *= vinv;
+                        float2 a = add2(make_float2(sv[k][0], sv[k][1]), nm0);
+                        float2 b = add2(make_float2(sv[k][2], sv[k][3]), nm1);
+                        a = make_float2(ex2(a.x), ex2(a.y));
+                        b = make_float2(ex2(b.x), ex2(b.y));
+                        la = add2(la, a);
+                        lb = add2(lb, b);
+                        a = mul2(a, vw[k]);
+                        b = mul2(b, vw[k]);
+                        tmem_st16x4(tmem + lane_base + 64 * buf + 4 * k, pack_f16x2(a.x, a.y), pack_f16x2(b.x, b.y));
                     }
+                    l[0] += la.x + la.y;
+                    l[1] += lb.x + lb.y;
+                    tmem_wait_st();
                 }
-                // ---- running maximum over each row's visible tokens (t < lim, slot < nv)
-                const int tt = (dt0 + li) * kTile;
-                const int vis[2] = {max(0, min(nv, lim[0] - tt)), max(0, min(nv, lim[1] - tt))};
-                const bool full = vis[0] == kTile && vis[1] == kTile;
-                float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int h = e >> 1, j = 8 * k + 2 * tig + (e & 1);
-                        mx[h] = fmaxf(mx[h], (full || j < vis[h]) ? sv[k][e] : -INFINITY);
-                    }
-                bool grow[2];
-                float alpha[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-                    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-                    const float mnew = fmaxf(m[h], mx[h] * (KV == 0 ? p.score_scale : qsc[h]));
-                    grow[h] = m[h] != -INFINITY && mnew > m[h] + 8.f;
-                    alpha[h] = grow[h] ? ex2(m[h] - mnew) : 1.f;
-                    if (grow[h] || m[h] == -INFINITY) m[h] = mnew;
-                }
-                if (__any_sync(0xffffffffu, grow[0] || grow[1] || (KV == 1 && vf != 1.f))) {
-                    // rows whose maximum grew: O_team *= 2^(m_old - m_new); E4M3: all rows also
-                    // by the V scale reference's change (after the previous P.V into O_team)
-                    if (!wait_prev_pv()) {
-                        failed = true;
-                        break;
-                    }
-                    tc_fence_after();
-#pragma unroll 1  // rare: kept small for the instruction cache
-                    for (int half = 0; half < 2; ++half) {
-                        float o[8][4];
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + o_col + 64 * half + 8 * k, o[k]);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            if constexpr (KV == 0) {
-                                o[k][0] *= alpha[0];
-                                o[k][1] *= alpha[0];
-                                o[k][2] *= alpha[1];
-                                o[k][3] *= alpha[1];
-                            } else {
-                                o[k][0] *= alpha[0] * vf;
-                                o[k][1] *= alpha[0] * vf;
-                                o[k][2] *= alpha[1] * vf;
-                                o[k][3] *= alpha[1] * vf;
-                            }
-                            tmem_st16x8(tmem + lane_base + o_col + 64 * half + 8 * k, o[k]);
-                        }
-                        tmem_wait_st();
-                    }
-                    l[0] *= alpha[0];
-                    l[1] *= alpha[1];
-                }
-                // ---- P = 2^(s * scale - m) (0 where not visible) as bf16 high part (the top 16
-                //      bits) and low part (the rest, rounded), written over S in the buffer: the
-                //      P.V's A operand, tokens (2c, 2c + 1) packed in column c (high part:
-                //      columns 0-31, low part: 32-63)
-                const float nm0 = -m[0], nm1 = -m[1];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    float pv[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int h = e >> 1, j = 8 * k + 2 * tig + (e & 1);
-                        const float q = ex2(fmaf(sv[k][e], KV == 0 ? p.score_scale : qsc[h], h ? nm1 : nm0));
-                        pv[e] = (full || j < vis[h]) ? q : 0.f;
-                    }
-                    l[0] += pv[0] + pv[1];
-                    l[1] += pv[2] + pv[3];
-                    if constexpr (KV == 0) {
-                        const uint32_t h0 = __float_as_uint(pv[0]) & 0xFFFF0000u, h1 = __float_as_uint(pv[1]) & 0xFFFF0000u;
-                        const uint32_t h2 = __float_as_uint(pv[2]) & 0xFFFF0000u, h3 = __float_as_uint(pv[3]) & 0xFFFF0000u;
-                        tmem_st16x4(tmem + lane_base + 64 * buf + 4 * k, prmt(h0, h1, 0x7632u), prmt(h2, h3, 0x7632u));
-                        tmem_st16x4(tmem + lane_base + 64 * buf + 32 + 4 * k,
-                                    pack_bf16x2(pv[0] - __uint_as_float(h0), pv[1] - __uint_as_float(h1)),
-                                    pack_bf16x2(pv[2] - __uint_as_float(h2), pv[3] - __uint_as_float(h3)));
-                    } else {  // E4M3: P x vs / vref <= 2^8 in f16, one product
-                        tmem_st16x4(tmem + lane_base + 64 * buf + 4 * k, pack_f16x2(pv[0] * vw[k][0], pv[1] * vw[k][1]),
-                                    pack_f16x2(pv[2] * vw[k][0], pv[3] * vw[k][1]));
-                    }
-                }
-                tmem_wait_st();
                 if constexpr (KV == 0) {
                     // ---- V rows past the request's length are zeroed (stale or NaN slots of the page)
                     if (nv < kTile) {

@@ -340,6 +340,18 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return r;
 }
 
+// Two-wide FP32 arithmetic (one instruction for both elements of a pair, each rounded
+// to nearest as the one-wide form).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+
+// max(a, b, c) in one instruction (the three-input form of max.f32).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Hardware base-2 exponential / logarithm (MUFU), flush-to-zero.
 __device__ __forceinline__ float ex2(float x) {
     float y;

@@ -73,6 +73,23 @@ def test_multi_vs_oracle(dsa, lens, q_len, hq, hkv, C, m, kv):
                 assert (out32[b, i] == 0).all() and torch.isneginf(lse[b, i]).all()
 
 
+@pytest.mark.parametrize("scale", [-0.3, 0.0])
+@pytest.mark.parametrize("q_len", [2, 6])
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_multi_any_finite_scale(dsa, scale, q_len, kv):
+    """The softmax scale may be any finite number (the header asks only that): a negative
+    scale turns the largest raw score into the smallest scaled one, and a zero scale gives
+    every visible token the same weight.  Both kernels must take the maximum over the
+    scaled scores and mask after scaling."""
+    inp = make([17, 300, 1500, 64], q_len, 64, 8, seed=21, kv=kv)
+    inp["sm_scale"] = scale
+    out16, out32, lse, tm, po, pl = run(dsa, inp, 40, 1)
+    ref, ref_lse = problem(inp).attention()
+    what = f"{kv} q_len {q_len} scale {scale}"
+    parity.check_outputs(out16.float().cpu().numpy(), out32.cpu().numpy(), ref, kv, what)
+    parity.assert_lse_close(lse.cpu().numpy(), ref_lse, what)
+
+
 @pytest.mark.parametrize("q_len", [2, 3, 6])
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 def test_multi_partials_each_descriptor(dsa, q_len, kv):
