@@ -516,8 +516,11 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                 vref = vinv = 0.f;
             }
             int pv_desc = 0, last_g = -1;
-            for (int li = 0; li < n; ++li, ++g) {
-                if ((g & 1) != team) continue;
+            // the team's tiles of this descriptor: every other one, from the first of parity team
+            const int g_first = g;
+            g += n;
+            for (int li = (team - g_first) & 1; li < n; li += 2) {
+                const int g = g_first + li;  // the tile's position in the CTA's stream
                 const int c = c_start + li, stage = c % STAGES, buf = g & 3;
                 if (!wait_phase(full_bar(stage), (c / STAGES) & 1, abort_flag, p.status) ||
                     !wait_phase(s_full(buf), (g >> 2) & 1, abort_flag, p.status)) {
