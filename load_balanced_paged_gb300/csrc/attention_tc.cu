@@ -590,27 +590,36 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                 if constexpr (KV == 0) {
                     if (rows) {
                         // ---- running maximum over each row's visible tokens (t < lim, slot < nv)
-                        //      of the raw scores, scaled once: the scale is non-negative here (the
-                        //      S warp negated Q for a negative one)
-                        const float sc = fabsf(p.score_scale);
+                        //      of the raw scores, scaled once: the scale is positive here (the S
+                        //      warp negated Q for a negative one; a zero scale is raised to the
+                        //      smallest normal float, which gives every visible token weight 1 as 0
+                        //      does).  Columns a row may not see are set to -inf first (a branch
+                        //      taken only by tiles with such a column), so P = 2^-inf = 0 there.
+                        const float sc = fmaxf(fabsf(p.score_scale), 1.17549435e-38f);
                         const int tt = (dt0 + li) * kTile;
-                        const int vis[2] = {max(0, min(nv, lim[0] - tt)), max(0, min(nv, lim[1] - tt))};
-                        const bool full = vis[0] == kTile && vis[1] == kTile;
-                        float mx[2] = {-INFINITY, -INFINITY};
+                        const int vis0 = max(0, min(nv, lim[0] - tt)), vis1 = max(0, min(nv, lim[1] - tt));
+                        if (vis0 < kTile || vis1 < kTile) {
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
+                            for (int k = 0; k < 8; ++k)
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int h = e >> 1, j = 8 * k + 2 * tig + (e & 1);
-                                mx[h] = fmaxf(mx[h], (full || j < vis[h]) ? sv[k][e] : -INFINITY);
-                            }
+                                for (int e = 0; e < 4; ++e) {
+                                    const int j = 8 * k + 2 * tig + (e & 1);
+                                    if (j >= ((e >> 1) ? vis1 : vis0)) sv[k][e] = -INFINITY;
+                                }
+                        }
+                        float mx[2] = {fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[0][2], sv[0][3])};
+#pragma unroll
+                        for (int k = 1; k < 8; ++k) {
+                            mx[0] = max3f(mx[0], sv[k][0], sv[k][1]);
+                            mx[1] = max3f(mx[1], sv[k][2], sv[k][3]);
+                        }
                         bool grow[2];
                         float alpha[2];
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
                             mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-                            const float mnew = fmaxf(m[h], mx[h] * sc);  // -inf x 0 = NaN is ignored
+                            const float mnew = fmaxf(m[h], mx[h] * sc);
                             grow[h] = m[h] != -INFINITY && mnew > m[h] + 8.f;
                             alpha[h] = grow[h] ? ex2(m[h] - mnew) : 1.f;
                             if (grow[h] || m[h] == -INFINITY) m[h] = mnew;
@@ -623,20 +632,17 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                             l[0] *= alpha[0];
                             l[1] *= alpha[1];
                         }
-                        // ---- P = 2^(s * scale - m) (0 where not visible) as bf16 high part (the top
-                        //      16 bits) and low part (the rest, rounded), written over S in the
-                        //      buffer: the P.V's A operand, tokens (2c, 2c + 1) packed in column c
-                        //      (high part: columns 0-31, low part: 32-63)
-                        const float nm0 = -m[0], nm1 = -m[1];
+                        // ---- P = 2^(s * scale - m) as bf16 high part (the top 16 bits) and low part
+                        //      (the rest, rounded), written over S in the buffer: the P.V's A
+                        //      operand, tokens (2c, 2c + 1) packed in column c (high part: columns
+                        //      0-31, low part: 32-63).  A row that has seen nothing yet has m = -inf
+                        //      and only -inf scores: P = 0.
+                        const float nm0 = m[0] == -INFINITY ? 0.f : -m[0], nm1 = m[1] == -INFINITY ? 0.f : -m[1];
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
                             float pv[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int h = e >> 1, j = 8 * k + 2 * tig + (e & 1);
-                                const float q = ex2(fmaf(sv[k][e], sc, h ? nm1 : nm0));
-                                pv[e] = (full || j < vis[h]) ? q : 0.f;
-                            }
+                            for (int e = 0; e < 4; ++e) pv[e] = ex2(fmaf(sv[k][e], sc, (e >> 1) ? nm1 : nm0));
                             l[0] += pv[0] + pv[1];
                             l[1] += pv[2] + pv[3];
                             const uint32_t h0 = __float_as_uint(pv[0]) & 0xFFFF0000u, h1 = __float_as_uint(pv[1]) & 0xFFFF0000u;
