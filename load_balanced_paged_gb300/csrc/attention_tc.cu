@@ -46,6 +46,33 @@ struct TcLayout {
     static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
 
+// 16 TMEM lanes x 64 columns over the warp in one load: v[k] holds columns 8 k .. 8 k + 7
+// as an m16n8 accumulator fragment (the layout of tmem_ld16x8, eight times side by side).
+__device__ __forceinline__ void tmem_ld16x64(uint32_t taddr, float (&v)[8][4]) {
+    uint32_t r[32];
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+                 "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                   "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+                   "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i >> 2][i & 3] = __uint_as_float(r[i]);
+}
+
+// 16 TMEM lanes x 32 columns over the warp in one store: w[2 k] and w[2 k + 1] go where
+// tmem_st16x4 at column 4 k puts its two words (eight of those side by side).
+__device__ __forceinline__ void tmem_st16x32(uint32_t taddr, const uint32_t (&w)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+                 "%13, %14, %15, %16};" ::"r"(taddr),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]),
+                 "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
+                 : "memory");
+}
+
 // The descriptor end of one softmax team.  It waits until the
 // team's products of the descriptor are done (its last tile's phase of o_done; that commit
 // covers every earlier product), reads O_team (o_tmem: the warp's lane quarter, O's first
@@ -531,8 +558,12 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                 tc_fence_after();
                 float sv[8][4];  // [column block k][(ra, 2tig), (ra, 2tig+1), (rb, 2tig), (rb, 2tig+1)]
                 if (nv > 0 && rows) {
+                    if constexpr (KV == 1) {
+                        tmem_ld16x64(tmem + lane_base + 64 * buf, sv);
+                    } else {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + 64 * buf + 8 * k, sv[k]);
+                        for (int k = 0; k < 8; ++k) tmem_ld16x8(tmem + lane_base + 64 * buf + 8 * k, sv[k]);
+                    }
                     tmem_wait_ld();
                 }
                 // this team's previous tile of the descriptor (-1: none; the first tile starts
@@ -745,6 +776,7 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                     const float n0 = m[0] == -INFINITY ? 0.f : -m[0], n1 = m[1] == -INFINITY ? 0.f : -m[1];
                     const float2 nm0 = make_float2(n0, n0), nm1 = make_float2(n1, n1);
                     float2 la = make_float2(0.f, 0.f), lb = la;
+                    uint32_t pw[16];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         float2 a = add2(make_float2(sv[k][0], sv[k][1]), nm0);
@@ -755,8 +787,9 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                         lb = add2(lb, b);
                         a = mul2(a, vw[k]);
                         b = mul2(b, vw[k]);
-                        tmem_st16x4(tmem + lane_base + 64 * buf + 4 * k, pack_f16x2(a.x, a.y), pack_f16x2(b.x, b.y));
+                        pw[2 * k] = pack_f16x2(a.x, a.y), pw[2 * k + 1] = pack_f16x2(b.x, b.y);
                     }
+                    tmem_st16x32(tmem + lane_base + 64 * buf, pw);
                     l[0] += la.x + la.y;
                     l[1] += lb.x + lb.y;
                     tmem_wait_st();
