@@ -73,6 +73,14 @@ __device__ __forceinline__ void tmem_st16x32(uint32_t taddr, const uint32_t (&w)
                  : "memory");
 }
 
+// Four E4M3 bytes (byte k -> element k) to two f16x2 words, exactly.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
+}
+
 // The descriptor end of one softmax team.  It waits until the
 // team's products of the descriptor are done (its last tile's phase of o_done; that commit
 // covers every earlier product), reads O_team (o_tmem: the warp's lane quarter, O's first
@@ -811,25 +819,30 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                     //      16-byte chunk c (dims 16 c .. 16 c + 15) of row t in, two chunks out
                     const uint8_t *vr = smem + stage * L::kStageBytes + C::kTileBytes;
                     uint8_t *vc = smem + stage * L::kStageBytes + L::kVcOff;
-#pragma unroll
-                    for (int it = 0; it < 4; ++it) {
-                        const int i = tid + 128 * it, t = i >> 3, c = i & 7;
-                        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-                        if (t < nv) {
-                            const uint4 x = *reinterpret_cast<const uint4 *>(vr + t * 128 + ((c ^ (t & 7)) << 4));
-                            lo = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(x.x & 0xFFFFu)),
-                                            e4m3x2_to_f16x2(static_cast<uint16_t>(x.x >> 16)),
-                                            e4m3x2_to_f16x2(static_cast<uint16_t>(x.y & 0xFFFFu)),
-                                            e4m3x2_to_f16x2(static_cast<uint16_t>(x.y >> 16)));
-                            hi = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(x.z & 0xFFFFu)),
-                                            e4m3x2_to_f16x2(static_cast<uint16_t>(x.z >> 16)),
-                                            e4m3x2_to_f16x2(static_cast<uint16_t>(x.w & 0xFFFFu)),
-                                            e4m3x2_to_f16x2(static_cast<uint16_t>(x.w >> 16)));
-                        }
+                    auto widen = [&](int t, int c, uint4 x) {
+                        uint4 lo, hi;
+                        e4m3x4_to_f16x4(x.x, lo.x, lo.y);
+                        e4m3x4_to_f16x4(x.y, lo.z, lo.w);
+                        e4m3x4_to_f16x4(x.z, hi.x, hi.y);
+                        e4m3x4_to_f16x4(x.w, hi.z, hi.w);
                         uint8_t *row = vc + (c >> 2) * 8192 + t * 128;  // half c / 4, chunks 2 (c % 4), + 1
                         const int cc = 2 * (c & 3);
                         *reinterpret_cast<uint4 *>(row + ((cc ^ (t & 7)) << 4)) = lo;
                         *reinterpret_cast<uint4 *>(row + (((cc + 1) ^ (t & 7)) << 4)) = hi;
+                    };
+                    if (nv == kTile) {  // uniform over the CTA: a full tile, no row to zero
+#pragma unroll
+                        for (int it = 0; it < 4; ++it) {
+                            const int i = tid + 128 * it, t = i >> 3, c = i & 7;
+                            widen(t, c, *reinterpret_cast<const uint4 *>(vr + t * 128 + ((c ^ (t & 7)) << 4)));
+                        }
+                    } else {
+#pragma unroll 1
+                        for (int it = 0; it < 4; ++it) {
+                            const int i = tid + 128 * it, t = i >> 3, c = i & 7;
+                            widen(t, c, t < nv ? *reinterpret_cast<const uint4 *>(vr + t * 128 + ((c ^ (t & 7)) << 4))
+                                               : make_uint4(0u, 0u, 0u, 0u));
+                        }
                     }
                 }
                 if (!wait_prev_pv()) {
