@@ -294,6 +294,16 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
             ++fetched[j];
         };
         auto land_q = [&](int j) { return wait_phase(qd_full(j), (fetched[j] - 1) & 1, abort_flag, p.status); };
+        // bf16: rows R .. 63 of both Q operand buffers are zero for the whole launch (R is fixed);
+        // the per-descriptor layout writes rows 0 .. R - 1 only
+        if constexpr (KV == 0) {
+            for (int i = lane; i < 2 * (kMaxRows - R) * 16; i += 32) {
+                const int b = i / ((kMaxRows - R) * 16), rem = i - b * ((kMaxRows - R) * 16);
+                const int r = R + (rem >> 4), kc = rem & 15;
+                *reinterpret_cast<uint4 *>(smem + L::kQcOff + b * kQcBuf + (kc >> 3) * 8192 + r * 128 +
+                                           (((kc & 7) ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
         int pf_slot = next_desc(d_begin - 1), pf_buf = 0;  // the descriptor whose Q is in flight
         if (pf_slot >= 0) fetch_q(pf_slot, 0);
         int g = 0, last_d = -1;
@@ -326,24 +336,28 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                 if constexpr (KV == 0) {
                 // 128-byte-swizzled K-major operand (as the TMA lays out K): dims 64 b .. 64 b + 63
                 // of row r at b * 8 KB + r * 128 B, 16-byte chunk c at (c ^ (r % 8)) * 16.  Each
-                // quarter-warp writes one 128-byte row: no bank conflicts either way.  A negative
-                // softmax scale is moved onto Q (its sign bits flipped, exact), so that the
-                // softmax sees S x |scale| and may take the maximum of the raw scores.
+                // quarter-warp writes one 128-byte row: no bank conflicts either way.  Rows R .. 63
+                // stay as zeroed at the start.  A negative softmax scale is moved onto Q (its sign
+                // bits flipped, exact), so that the softmax sees S x |scale| and may take the
+                // maximum of the raw scores.
                 const uint32_t qneg = p.score_scale < 0.f ? 0x80008000u : 0u;
 #pragma unroll
                 for (int rd = 0; rd < 4; ++rd) {
+                    if (16 * rd >= R) break;  // rows 16 rd .. are padding
                     uint4 v[8];
 #pragma unroll
                     for (int it = 0; it < 8; ++it) {  // chunk kc of row r
                         const int i = lane + 32 * (8 * rd + it), r = i >> 4, kc = i & 15;
-                        v[it] = r < R ? *reinterpret_cast<const uint4 *>(src + r * (kHeadDim * 2) + kc * 16)
-                                      : make_uint4(0u, 0u, 0u, 0u);
-                        v[it].x ^= qneg, v[it].y ^= qneg, v[it].z ^= qneg, v[it].w ^= qneg;
+                        if (r < R) {
+                            v[it] = *reinterpret_cast<const uint4 *>(src + r * (kHeadDim * 2) + kc * 16);
+                            v[it].x ^= qneg, v[it].y ^= qneg, v[it].z ^= qneg, v[it].w ^= qneg;
+                        }
                     }
 #pragma unroll
                     for (int it = 0; it < 8; ++it) {
                         const int i = lane + 32 * (8 * rd + it), r = i >> 4, kc = i & 15;
-                        *reinterpret_cast<uint4 *>(dst + (kc >> 3) * 8192 + r * 128 + (((kc & 7) ^ (r & 7)) << 4)) = v[it];
+                        if (r < R)
+                            *reinterpret_cast<uint4 *>(dst + (kc >> 3) * 8192 + r * 128 + (((kc & 7) ^ (r & 7)) << 4)) = v[it];
                     }
                 }
                 } else {
