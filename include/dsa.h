@@ -3,7 +3,7 @@
  * attention for GB300 (sm_103a), scheduled by a per-step task map.
  *
  * The operation (sources are web pages; section names as printed on them):
- *   HPC-Ops × SGLang blog (news.paixiangai.cn), "Attention：变长 decode 的负载均衡":
+ *   HPC-Ops × SGLang blog, "Attention：变长 decode 的负载均衡":
  *     decode attention work grows with each request's live KV length; a static
  *     split-KV grid over (KV head, request, chunk) either uses a fixed split
  *     count (long requests make heavy chunks and a tail) or a fixed chunk size
@@ -17,7 +17,7 @@
  *     covers one or more contiguous KV tiles of one (request, head) and yields a
  *     partial output with its log-sum-exp; a combine kernel merges the actual
  *     number of partials per (request, head) under the global softmax.
- *   Hy3 preview write-up (m.youleyou.com), 2.1.1 "Attention动态调度": the same
+ *   Hy3 preview write-up, 2.1.1 "Attention动态调度": the same
  *     scheme as uniform tiles, greedy bin packing, a task map generated before
  *     each step, and a combine kernel.
  *
@@ -206,7 +206,7 @@ dsa_status dsa_decode_fused(const void *q, dsa_dtype q_dtype, const float *q_sca
 /*
  * dsa_decode_multi -- dsa_decode for q_len query tokens per request (a multi-token
  * verify step: Hy3 preview write-up 2.5 "MTP与异步调度优化"; SGLang Low-Latency Mode:
- * Kernels and Runtime (paper-daily.com), section 1, a verify of 1 + 5 draft tokens
+ * Kernels and Runtime, section 1, a verify of 1 + 5 draft tokens
  * in one pass).  The task map, the scheduler and the KV
  * stream are those of dsa_decode: each KV tile is read once and serves all q_len * G
  * query rows of its unit.  Query token i of request b stands at position

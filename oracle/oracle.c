@@ -8,12 +8,12 @@
  *
  * Sources (web pages; section titles as printed on them):
  *   [HPC-Ops x SGLang blog]  "HPC-Ops × SGLang：腾讯混元开源高性能 Attention、
- *       Router GEMM 与 MoE 算子" (news.paixiangai.cn), sections
+ *       Router GEMM 与 MoE 算子", sections
  *       "Attention：变长 decode 的负载均衡" (static split-KV and its two forms),
  *       "围绕活跃 KV 工作进行调度" (assign kernel, budget, greedy bins,
  *       minimum-work floor, partial outputs with log-sum-exp, combine),
  *       "融合式 attention 前导" (FP8 Q with per-token/per-head scale).
- *   [Hy3 preview write-up]  m.youleyou.com/wenzhang/3105752.html, section
+ *   [Hy3 preview write-up]  section
  *       2.1.1 "Attention动态调度" (uniform tile granularity, greedy bin
  *       packing, task map built once per step, combine kernel).
  *
