@@ -75,6 +75,39 @@ def test_small_vs_oracle(dsa, lens, hq, hkv, kv, C, m):
     parity.assert_lse_close(lse.cpu().numpy(), ref_lse, "out lse")
 
 
+@pytest.mark.parametrize("scale", [-0.3, 0.0])
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_any_finite_scale(dsa, scale, kv):
+    """The softmax scale may be any finite number (the header asks only that): with a
+    negative scale the smallest raw score weighs most, with a zero scale every visible
+    token weighs the same.  The persistent decode (one and two CTAs per SM), the fused
+    decode + combine and the static split-KV path must all match the oracle."""
+    lens = [17, 300, 1500, 64, 1]
+    inp = make(lens, 16, 2, kv, seed=31)
+    inp["sm_scale"] = scale
+    h = workloads.host_view(inp)
+    ref, ref_lse = parity.problem_from_host(h, inp).attention()
+    for C in (7, "2x"):
+        out, lse, tm, po, pl = run_dynamic(dsa, inp, resolve_ctas(C), 1)
+        assert dsa.get_status(tm) == 0
+        out32 = dsa.combine(tm, po, pl, 16, out_dtype=torch.float32)
+        parity.check_outputs(out.float().cpu().numpy(), out32.cpu().numpy(), ref, kv, f"scale {scale}, C {C}")
+        parity.assert_lse_close(lse.cpu().numpy(), ref_lse, f"scale {scale}, C {C}")
+    kw = dict(q_scale=inp["q_scale"], k_scale=inp["k_scale"], v_scale=inp["v_scale"])
+    tm = dsa.plan(inp["seq_lens"], 2, 7, 1)
+    outf = dsa.decode_fused(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], inp["seq_lens"], tm,
+                            scale, out_dtype=torch.float32, **kw)
+    torch.cuda.synchronize()
+    assert dsa.get_status(tm) == 0
+    parity.assert_close(outf.cpu().numpy(), ref, kv, f"fused, scale {scale}", round_ref=False)
+    po, pl, S, status = dsa.static_splitkv(0, 16, max(lens), inp["q"], inp["k_pages"], inp["v_pages"],
+                                           inp["block_table"], inp["seq_lens"], 2, scale, **kw)
+    out32 = dsa.static_combine(S, po, pl, len(lens), 16, 2, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert dsa.read_status(status) == 0
+    parity.assert_close(out32.cpu().numpy(), ref, kv, f"static, scale {scale}", round_ref=False)
+
+
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 def test_partials_each_descriptor(dsa, kv):
     """Each GPU partial equals attention over its descriptor's tokens, and the oracle's
