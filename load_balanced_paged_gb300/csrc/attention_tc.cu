@@ -5,7 +5,8 @@
 // HPC-Ops × SGLang blog, "围绕活跃 KV 工作进行调度"); every KV tile serves all q_len x G query
 // rows of its unit.  Only the consumers differ: S = Q K^T and O = P V accumulate in tensor
 // memory (tcgen05.mma, M = 64), two teams of four softmax warps take alternate tiles, one
-// warp issues S (and lays Q out as its operand), one issues P.V.  Each team writes its own
+// warp issues S (and lays Q out as its operand; bf16 with at most 48 query rows: the fourth
+// warp of each team, whose rows are all padding, does that instead), one issues P.V.  Each team writes its own
 // partial at a descriptor end (two slots per descriptor).
 #include "engine.cuh"
 
@@ -37,7 +38,9 @@ struct TcLayout {
     static constexpr int kTcBars = 22;
     static constexpr int kNumBars = 2 * STAGES + 2 * kQSlots + kTcBars;
     static constexpr int kNValidOff = kBarOff + kNumBars * 8;
-    static constexpr int kAbortOff = kNValidOff + STAGES * 4;  // abort flag, then the TMEM base address
+    // abort flag, the TMEM base address, the slots of the descriptors in the two Q operand
+    // buffers (written by the Q helpers)
+    static constexpr int kAbortOff = kNValidOff + STAGES * 4;
     static constexpr int kInfoOff = round_up(kAbortOff + 16, 64);  // one DescInfo per Q slot
     static constexpr int kBytes = kInfoOff + kQSlots * kDescInfoBytes;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
@@ -177,6 +180,9 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G;
+    // bf16 with at most 48 query rows per unit: the fourth warp of each team holds only
+    // padding rows, and lays out Q for the S warp instead of joining the team's softmax
+    const bool helpers = KV == 0 && p.q_len * G <= 48;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -185,16 +191,16 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
         }
         for (int s = 0; s < kQSlots; ++s) {
             mbar_init(qfull_bar(s), 1);
-            mbar_init(qempty_bar(s), NCW + 2);  // every warp that reads the hand-off
+            mbar_init(qempty_bar(s), helpers ? NCW : NCW + 2);  // every warp that reads the hand-off (not the Q helpers)
         }
         for (int b = 0; b < 4; ++b) {
             mbar_init(s_full(b), 1);  // S warp
             mbar_init(s_free(b), 1);  // PV warp: the buffer's P has been read
-            mbar_init(p_full(b), 4);  // the owning softmax team
+            mbar_init(p_full(b), helpers ? 3 : 4);  // the owning softmax team
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(o_done(b), 1);
-            mbar_init(o_free(b), 4);
+            mbar_init(o_free(b), helpers ? 3 : 4);
             mbar_init(qc_full(b), 1);
             mbar_init(qc_free(b), 1);
             mbar_init(qd_full(b), 1);
@@ -253,7 +259,8 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
 
     if (warp == NCW + 1) {
         // ---- S warp: fetches each descriptor's Q rows one descriptor ahead (plain rows
-        //      into one of two buffers), lays them out as the A operand (zero past R), then
+        //      into one of two buffers), lays them out as the A operand (zero past R; bf16 with
+        //      at most 48 rows: waits for the Q helpers, which do both, instead), then
         //      issues S = Q K^T for its tiles as soon as a stage and an S buffer are ready
         //      (lane 0 issues, the warp waits together); its commit on the stage's empty
         //      barrier says the K half is no longer read
@@ -303,8 +310,10 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                 *reinterpret_cast<uint4 *>(smem + L::kQcOff + b * kQcBuf + (kc >> 3) * 8192 + r * 128 +
                                            (((kc & 7) ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
             }
+            fence_proxy_async_smem();
         }
-        int pf_slot = next_desc(d_begin - 1), pf_buf = 0;  // the descriptor whose Q is in flight
+        // the descriptor whose Q is in flight (none with helpers: they fetch it)
+        int pf_slot = helpers ? -1 : next_desc(d_begin - 1), pf_buf = 0;
         if (pf_slot >= 0) fetch_q(pf_slot, 0);
         int g = 0, last_d = -1;
         for (int d = 0;; ++d) {
@@ -315,7 +324,16 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
             }
             const DescInfo *inf = reinterpret_cast<const DescInfo *>(smem + L::kInfoOff) + qslot;
             const int end = inf->end, n = inf->n, c_start = inf->c_start, xs = inf->slot;
-            if (!end) {
+            if (!end && helpers) {
+                // laid out by the helper of team d % 2 in operand buffer d % 2, which follows the
+                // same descriptor sequence (a mismatch would be a map the two read differently)
+                if (!wait_phase(qc_full(d & 1), (d >> 1) & 1, abort_flag, p.status)) {
+                    failed = true;
+                    break;
+                }
+                if (lane == 0 && *reinterpret_cast<volatile int *>(smem + L::kAbortOff + 8 + 4 * (d & 1)) != xs)
+                    atomicOr(p.status, DSA_DEV_BAD_MAP);
+            } else if (!end) {
                 // this descriptor's Q: normally the prefetched one; otherwise fetched now
                 const int qb = pf_buf;
                 if (pf_slot != xs) {
@@ -490,6 +508,84 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                 __syncwarp();
             }
             if (failed) break;
+        }
+    } else if (helpers && (warp & 3) == 3) {
+        // ---- Q helper (bf16, at most 48 rows: the fourth warp of team t, whose 16 rows are
+        //      all padding).  The descriptors the producer hands over (valid, with tiles) come
+        //      in the order of the task map, the d-th of them being the S warp's descriptor d;
+        //      the helper walks the map itself (so it never holds up the hand-off ring) and
+        //      takes those with d % 2 == t: it fetches the descriptor's Q rows into plain
+        //      buffer t, lays them out as the A operand (rows 0 .. R - 1; the S warp zeroed the
+        //      rest) in operand buffer t once the S products of descriptor d - 2 have read it,
+        //      notes the descriptor's slot for the S warp to check, and signals it
+        const int team = warp >> 2;
+        const uint32_t qneg = p.score_scale < 0.f ? 0x80008000u : 0u;  // a negative scale moves onto Q
+        const uint8_t *src = smem + L::kQOff + team * L::kQSlot;
+        uint8_t *dst = smem + L::kQcOff + team * kQcBuf;
+        volatile int *laid_slot = reinterpret_cast<volatile int *>(smem + L::kAbortOff + 8) + team;
+        int fetched = 0;  // Q copies into plain buffer t, each one waited for
+        bool in_flight = false;
+        int d = -1;
+        for (int base = 0; base < d_count && !failed; base += 32) {
+            int wu = -1;  // lane j: the unit of descriptor base + j if it is handed over
+            if (base + lane < d_count) {
+                const int4 v = p.descs[d_begin + base + lane];
+                if (v.x >= 0 && v.x < p.num_units && v.y >= 0 && v.y < v.z && d_begin + base + lane < p.max_slots)
+                    wu = v.x;
+            }
+            for (uint32_t valid = __ballot_sync(0xffffffffu, wu >= 0); valid; valid &= valid - 1) {
+                const int j = __ffs(valid) - 1;
+                if (((++d) & 1) != team) continue;
+                const int u = __shfl_sync(0xffffffffu, wu, j), b = u / p.hkv, h = u - b * p.hkv;
+                if (lane == 0) {
+                    const uint32_t bytes = G * C::kQHeadBytes;
+                    mbar_arrive_expect_tx(qd_full(team), bytes * p.q_len);
+                    for (int i = 0; i < p.q_len; ++i)
+                        bulk_load(sbase + L::kQOff + team * L::kQSlot + i * bytes,
+                                  p.q + ((static_cast<int64_t>(b) * p.q_len + i) * p.hq + h * G) * C::kQHeadBytes,
+                                  bytes, qd_full(team));
+                }
+                ++fetched;
+                in_flight = true;
+                if (!wait_phase(qd_full(team), (fetched - 1) & 1, abort_flag, p.status)) {
+                    failed = true;
+                    break;
+                }
+                in_flight = false;
+                if (!wait_phase(qc_free(team), ((d >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                    failed = true;
+                    break;
+                }
+                if (lane == 0) *laid_slot = d_begin + base + j;
+                // the S warp's layout (128-byte swizzle, K-major), rows 0 .. R - 1
+#pragma unroll
+                for (int rd = 0; rd < 3; ++rd) {
+                    if (16 * rd >= R) break;
+                    uint4 v[8];
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int i = lane + 32 * (8 * rd + it), r = i >> 4, kc = i & 15;
+                        if (r < R) {
+                            v[it] = *reinterpret_cast<const uint4 *>(src + r * (kHeadDim * 2) + kc * 16);
+                            v[it].x ^= qneg, v[it].y ^= qneg, v[it].z ^= qneg, v[it].w ^= qneg;
+                        }
+                    }
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int i = lane + 32 * (8 * rd + it), r = i >> 4, kc = i & 15;
+                        if (r < R)
+                            *reinterpret_cast<uint4 *>(dst + (kc >> 3) * 8192 + r * 128 + (((kc & 7) ^ (r & 7)) << 4)) =
+                                v[it];
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qc_full(team));
+            }
+        }
+        if (in_flight) {  // a Q copy still in flight lands before the CTA leaves
+            const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+            drain_phase(qd_full(team), (fetched - 1) & 1, deadline);
         }
     } else {
         // ---- softmax warps: two teams of four (team t = warps 4t .. 4t + 3) take the tiles
@@ -820,7 +916,7 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
                     // ---- V rows past the request's length are zeroed (stale or NaN slots of the page)
                     if (nv < kTile) {
                         uint8_t *vt = smem + stage * L::kStageBytes + C::kTileBytes;
-                        for (int i = tid; i < (kTile - nv) * 16; i += 128) {
+                        for (int i = tid; i < (kTile - nv) * 16; i += helpers ? 96 : 128) {
                             const int row = nv + (i >> 4), ch = i & 15;
                             *reinterpret_cast<uint4 *>(vt + (ch >> 3) * (C::kTileBytes / 2) + row * 128 + (ch & 7) * 16) =
                                 make_uint4(0u, 0u, 0u, 0u);
