@@ -84,18 +84,18 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t &lo, uint32
         : "r"(x));
 }
 
-// The descriptor end of one softmax team.  It waits until the
-// team's products of the descriptor are done (its last tile's phase of o_done; that commit
-// covers every earlier product), reads O_team (o_tmem: the warp's lane quarter, O's first
-// column) into registers, releases it (o_free) and writes the team's partial for rows ra, rb
-// (< R): O / l (E4M3: times the V scale reference vref, by which O was divided) and
-// lse = ln 2 (m + log2 l), slot 2 x descriptor + team.
+// The descriptor end of one softmax team.  It waits until the team's products of the
+// descriptor are done (its last tile's phase of o_done; that commit covers every earlier
+// product), reads O_team (o_tmem: the warp's lane quarter, O's first column) into registers,
+// releases it (o_free) and writes the team's partial for rows ra, rb (< R): O / l (E4M3: times
+// the V scale reference vref, by which O was divided) and lse = ln 2 (m + log2 l), slot
+// 2 x descriptor + team.
 template <int KV>
 static __device__ __forceinline__ bool tc_team_epilogue(float *partial_o, float *partial_lse, int32_t *status,
-                                                     volatile int *abort_flag, uint32_t o_done_bar,
-                                                     uint32_t o_free_bar, uint32_t o_tmem, int R, int ra, int rb,
-                                                     int tig, int lane, int team, int slot, float m0, float m1,
-                                                     float l0, float l1, int pv_desc, int last_g, float vref) {
+                                                        volatile int *abort_flag, uint32_t o_done_bar,
+                                                        uint32_t o_free_bar, uint32_t o_tmem, int R, int ra, int rb,
+                                                        int tig, int lane, int team, int slot, float m0, float m1,
+                                                        float l0, float l1, int pv_desc, int last_g, float vref) {
     if (last_g >= 0) {
         if (!wait_phase(o_done_bar, (last_g >> 1) & 1, abort_flag, status)) return false;
         tc_fence_after();
