@@ -266,21 +266,22 @@ def combine(task_map: TaskMap, partial_o, partial_lse, num_q_heads: int, out=Non
 
 def decode_multi(q_len: int, q, k_pages, v_pages, block_table, seq_lens, task_map: TaskMap, sm_scale: float,
                  partial_o=None, partial_lse=None, q_scale=None, k_scale=None, v_scale=None, stream=None,
-                 kv_layout="HND"):
+                 kv_layout="HND", cta_times=None):
     """dsa_decode_multi: q [B, q_len, Hq, 128]; partials hold q_len * G rows per slot, two
-    slots per descriptor when q_len > 1."""
+    slots per descriptor when q_len > 1 (dsa_decode_ex for NHD pages or per-CTA timestamps,
+    cta_times uint64-sized [num_ctas, 2])."""
     R = q_len * (q.shape[-2] // task_map.num_kv_heads)
     if partial_o is None:
         spd = int(_lib.dsa_multi_slots_per_desc(q_len, q.shape[-2] // task_map.num_kv_heads))
         partial_o, partial_lse = partial_buffers(task_map.max_descs * spd, R, q.device)
     args = _attn_args(q, k_pages, v_pages, block_table, seq_lens, task_map.num_kv_heads, sm_scale,
                       q_scale, k_scale, v_scale, kv_layout)
-    if kv_layout == "HND":
+    if kv_layout == "HND" and cta_times is None:
         rc = _lib.dsa_decode_multi(q_len, *args, ctypes.byref(task_map.struct), _ptr(partial_o),
                                    _ptr(partial_lse), _stream(stream))
     else:
         rc = _lib.dsa_decode_ex(q_len, KV_LAYOUTS[kv_layout], *args, ctypes.byref(task_map.struct),
-                                _ptr(partial_o), _ptr(partial_lse), None, _stream(stream))
+                                _ptr(partial_o), _ptr(partial_lse), _ptr(cta_times), _stream(stream))
     _check(rc, "dsa_decode_multi")
     return partial_o, partial_lse
 

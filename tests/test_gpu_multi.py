@@ -175,6 +175,27 @@ def test_multi_one_token_is_decode(dsa):
     assert torch.equal(a32.reshape(out.shape), out) and torch.equal(alse.reshape(lse.shape), lse)
 
 
+@pytest.mark.parametrize("q_len,kv", [(2, "bf16"), (6, "bf16"), (6, "fp8")])
+def test_multi_cta_times_leave_results_unchanged(dsa, q_len, kv):
+    """dsa_decode_ex for q_len > 1 with a timestamp buffer: every CTA reports start <= end,
+    and the partials are bit-identical to a launch without timestamps."""
+    inp = make([1, 63, 700, 3000, 129], q_len, 64, 8, seed=11, kv=kv)
+    C = 7
+    tm = dsa.plan(inp["seq_lens"], 8, C, 1)
+    kw = dict(q_scale=inp.get("q_scale"), k_scale=inp.get("k_scale"), v_scale=inp.get("v_scale"))
+    po0, pl0 = dsa.decode_multi(q_len, inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"],
+                                inp["seq_lens"], tm, inp["sm_scale"], **kw)
+    times = torch.zeros(C, 2, dtype=torch.int64, device="cuda")
+    po1, pl1 = dsa.decode_multi(q_len, inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"],
+                                inp["seq_lens"], tm, inp["sm_scale"], cta_times=times, **kw)
+    torch.cuda.synchronize()
+    assert dsa.get_status(tm) == 0
+    assert torch.equal(po0, po1) and torch.equal(pl0, pl1)
+    t = times.cpu().numpy()
+    assert (t[:, 0] > 0).all() and (t[:, 1] >= t[:, 0]).all()
+    assert (t[:, 1] - t[:, 0]).max() < 10 ** 9  # under a second
+
+
 def test_multi_rejects_unsupported(dsa):
     inp = make([100, 200], 9, 64, 8)                   # 72 rows per unit
     tm = dsa.plan(inp["seq_lens"], 8, 4)
