@@ -23,9 +23,12 @@
 namespace dsa {
 namespace {
 
-constexpr int kProWarps = 8;      // warps per CTA
 constexpr int kProTokens = 8;     // tokens per warp (one per 4-lane group)
-constexpr int kProCtasPerSm = 2;  // resident CTAs per SM (128 registers per thread)
+// CTA shapes: warps per CTA and resident CTAs per SM.  Up to kProSmallTokens tokens, CTAs of
+// 4 warps, 3 per SM (up to 170 registers a thread, no spill); beyond, CTAs of 8 warps, 2 per
+// SM (128 registers, 16 warps per SM).  Measured on the 64 / 8-head chain: the small shape is
+// 0.3-2.5 us faster from 32 to 4096 tokens, the large one 3-5 us faster from 8192 on.
+constexpr int kProSmallTokens = 4096;
 constexpr float kE4m3Max = 448.0f;
 constexpr float kInvSqrtHeadDim = 0.08838834764831845f;  // 1 / sqrt(128)
 
@@ -252,14 +255,15 @@ __device__ __forceinline__ void encode_store(int l, float (&y)[4][8], float f, b
     }
 }
 
-__global__ void __launch_bounds__(kProWarps * 32, kProCtasPerSm) prologue_kernel(ProParams p) {
+template <int W, int CPS>
+__global__ void __launch_bounds__(W * 32, CPS) prologue_kernel(ProParams p) {
     grid_launch_dependents();
     grid_dependency_wait();
     const int lane = threadIdx.x & 31, grp = lane >> 2, l = lane & 3;
     const int H = p.hq + 2 * p.hkv;
     const int head_blocks = (H + p.heads_per_item - 1) / p.heads_per_item;
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * kProWarps;
-    for (int64_t it = static_cast<int64_t>(blockIdx.x) * kProWarps + (threadIdx.x >> 5); it < p.items; it += warps) {
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * W;
+    for (int64_t it = static_cast<int64_t>(blockIdx.x) * W + (threadIdx.x >> 5); it < p.items; it += warps) {
         const int item = static_cast<int>(it);
         const int tg = item / head_blocks, hb = item - tg * head_blocks;
         const int n_raw = tg * kProTokens + grp;
@@ -357,8 +361,10 @@ extern "C" dsa_status dsa_prologue(const void *qkv, int32_t n_tokens, int32_t nu
     const int64_t H = static_cast<int64_t>(num_q_heads) + 2 * num_kv_heads;
     const int64_t groups = (static_cast<int64_t>(n_tokens) + kProTokens - 1) / kProTokens;
     if (H * kHeadDim > INT32_MAX || groups * H > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+    const bool small = n_tokens <= kProSmallTokens;
+    const int W = small ? 4 : 8, CPS = small ? 3 : 2;
     const int sms = sm_count();
-    const int64_t warps_resident = static_cast<int64_t>(sms > 0 ? sms : 148) * kProCtasPerSm * kProWarps;
+    const int64_t warps_resident = static_cast<int64_t>(sms > 0 ? sms : 148) * CPS * W;
     // Heads per work item: blocks of 8 consecutive heads amortise the per-token loads; fewer
     // when that would leave the GPU's warps short of work (small decode batches).
     int hpi = 8;
@@ -398,8 +404,9 @@ extern "C" dsa_status dsa_prologue(const void *qkv, int32_t n_tokens, int32_t nu
     p.kv_fp8 = kv_dtype == DSA_FP8_E4M3;
     p.status = status;
 
-    const int64_t want = (p.items + kProWarps - 1) / kProWarps;
-    const int64_t cap = warps_resident / kProWarps;
+    const int64_t want = (p.items + W - 1) / W;
+    const int64_t cap = warps_resident / W;
     const int grid = static_cast<int>(want < cap ? want : cap);
-    return launch_pdl(prologue_kernel, dim3(grid), dim3(kProWarps * 32), 0, to_cuda(stream), p);
+    return small ? launch_pdl(prologue_kernel<4, 3>, dim3(grid), dim3(4 * 32), 0, to_cuda(stream), p)
+                 : launch_pdl(prologue_kernel<8, 2>, dim3(grid), dim3(8 * 32), 0, to_cuda(stream), p);
 }

@@ -147,12 +147,13 @@ def test_prologue_page_layouts(dsa, page, layout, kinds):
     check(inp, got, kinds[0], kinds[1], 128, "neox", True, True, f"P {page} {layout}")
 
 
+@pytest.mark.parametrize("n", [2048, 4097])
 @pytest.mark.parametrize("kinds", [("e4m3", "e4m3"), ("bf16", "bf16")])
-def test_prologue_prefill_size(dsa, kinds):
+def test_prologue_prefill_size(dsa, kinds, n):
     # 2048 tokens x 80 heads: enough work items for blocks of 8 heads per warp and several
-    # grid-stride passes
-    inp, got = run(dsa, 2048, 64, 8, kinds[0], kinds[1], 128, "neox", True, True, seed=11)
-    check(inp, got, kinds[0], kinds[1], 128, "neox", True, True, "prefill 2048")
+    # grid-stride passes; 4097 tokens: the CTA shape of large batches (above 4096 tokens)
+    inp, got = run(dsa, n, 64, 8, kinds[0], kinds[1], 128, "neox", True, True, seed=11)
+    check(inp, got, kinds[0], kinds[1], 128, "neox", True, True, f"prefill {n}")
 
 
 def test_bad_position_and_slot_set_status(dsa):
