@@ -306,7 +306,12 @@ dsa_status dsa_combine_multi(int32_t q_len, const dsa_task_map *map, const float
  * over unit u's slots [unit_partial_begin[u], + unit_num_partials[u]).
  * out: [B, Hq, 128] in out_dtype (DSA_BF16, round to nearest even, or DSA_FP32);
  * out_lse: [B, Hq] fp32, may be NULL.  A unit with no partials gives out = 0,
- * lse = -inf.
+ * lse = -inf.  The kernel reads the map's unit arrays before it waits for the preceding
+ * kernel in the stream (programmatic dependent launch).  That is safe after this library's
+ * decode calls (dsa_decode, dsa_decode_multi, dsa_decode_ex, dsa_decode_chained), which
+ * release the next kernel only after their own wait, when the plan that wrote the map has
+ * completed.  After any other kernel, the map must have been written by a kernel that
+ * completed before that one started.
  */
 dsa_status dsa_combine(const dsa_task_map *map, const float *partial_o, const float *partial_lse,
                        int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,

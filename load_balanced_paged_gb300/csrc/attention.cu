@@ -260,15 +260,12 @@ __global__ void __launch_bounds__(FUSE ? Layout<KV, STAGES, GROUPS, MSLOTS, QW>:
     }
     __syncthreads();
 
-    // Early KV gather (dsa_decode_chained): the producer warp waits for the preceding kernel
-    // later, after issuing the tiles it may load before that kernel completes.  The next kernel
-    // may start only once this one has waited, so that whatever it reads before its own wait
-    // comes from kernels that have completed.
-    if (p.early == 0) {
-        grid_launch_dependents();
+    // The next kernel may start only once this one has waited for its predecessor, so that
+    // whatever it reads before its own wait (the combine: the task map's unit arrays) comes from
+    // kernels that have completed.  Early KV gather (dsa_decode_chained): the producer warp
+    // waits later, after issuing the tiles it may load before the preceding kernel completes.
+    if (p.early == 0 || warp != NCW) {
         grid_dependency_wait();  // task map, lengths, pages and Q from earlier kernels
-    } else if (warp != NCW) {
-        grid_dependency_wait();
         grid_launch_dependents();
     }
     EndStamp end_stamp{nullptr};

@@ -210,8 +210,9 @@ __global__ void __launch_bounds__(TcLayout<KV, STAGES>::kThreads, 1)
     }
     __syncthreads();
 
-    grid_launch_dependents();
+    // released after the wait: the combine reads the task map before its own wait
     grid_dependency_wait();  // task map, lengths, pages and Q from earlier kernels
+    grid_launch_dependents();
     EndStamp end_stamp{nullptr};
     if (p.cta_times) {  // uniform over the CTA
         uint64_t *t = p.cta_times + 2 * blockIdx.x;

@@ -43,14 +43,16 @@ __global__ void __launch_bounds__(kMaxGroup * 32)
                    float *__restrict__ out_lse) {
     const int u = blockIdx.x;
     const int row = blockIdx.y * kMaxGroup + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    // spd partial slots per descriptor: the unit's slots are [spd * begin, spd * (begin + count)).
+    // The task map is read before the wait: the decode before this kernel releases it only after
+    // its own wait, when the plan that wrote the map has completed.
+    const int64_t beg = STATIC ? static_cast<int64_t>(u) * S : static_cast<int64_t>(unit_begin[u]) * spd;
+    const int n = STATIC ? S : unit_count[u] * spd;
     grid_launch_dependents();
     grid_dependency_wait();  // partials from the decode kernel
     const int R = q_len * G;  // partial rows per slot
     if (row >= R) return;
     const int b = u / hkv, h = u - b * hkv;
-    // spd partial slots per descriptor: the unit's slots are [spd * begin, spd * (begin + count))
-    const int64_t beg = STATIC ? static_cast<int64_t>(u) * S : static_cast<int64_t>(unit_begin[u]) * spd;
-    const int n = STATIC ? S : unit_count[u] * spd;
 
     // the first kPre partials' rows are loaded together with the LSEs, so the merge of a unit
     // with few partials waits for one round trip to memory after the lengths, not two
