@@ -784,27 +784,44 @@ def oracle_problem(inp, requests):
                           k_scale=pools["k_scale"], v_scale=pools["v_scale"]), lens
 
 
-def cpu_oracle_rate(inp, budget_s: float, rng_seed: int = 0, threads: int = 0):
+def oracle_seconds_per_token(inp, threads: int) -> float:
+    """Oracle time per token of one request (all its KV heads), measured on the request of
+    median length (the shortest would fold the per-call cost into every token)."""
+    lens = inp["seq_lens"].cpu().numpy()
+    b = int(np.argsort(lens)[len(lens) // 2])
+    prob, _ = oracle_problem(inp, [b])
+    t0 = time.perf_counter()
+    prob.attention(n_threads=threads)
+    return (time.perf_counter() - t0) / max(int(lens[b]), 1)
+
+
+def cpu_oracle_rate(inp, budget_s: float, rng_seed: int = 0, threads: int = 0, per_token: float | None = None,
+                    fit: bool = False):
     """Time the oracle (all host threads, or `threads`) on a bounded sample of requests;
-    returns (GB/s of KV processed, threads, description)."""
+    returns (GB/s of KV processed, threads, description).  Requests are taken in a seeded
+    random order until the estimated time fills the budget; with `fit`, a request that would
+    overrun it is skipped instead (at least one request: the shortest if none fits), so that
+    small budgets stay small."""
     import oracle
     lens = inp["seq_lens"].cpu().numpy()
     rng = np.random.default_rng(rng_seed)
     order = rng.permutation(len(lens))
-    # calibrate on the shortest request, then take requests until the estimated time fills the budget
     threads = threads or oracle.default_threads()
-    prob, _ = oracle_problem(inp, [int(np.argmin(lens))])
-    t0 = time.perf_counter()
-    prob.attention(n_threads=threads)
-    per_token = (time.perf_counter() - t0) / max(int(lens.min()), 1)
+    if per_token is None:
+        per_token = oracle_seconds_per_token(inp, threads)
     # the oracle runs one thread per (request, KV head) unit
     eff = min(threads, inp["num_kv_heads"] * len(lens))
     chosen, est = [], 0.0
     for b in order:
+        t = per_token * lens[b] * inp["num_kv_heads"] / eff
+        if fit and est + t > budget_s:
+            continue
         chosen.append(int(b))
-        est += per_token * lens[b] * inp["num_kv_heads"] / eff
+        est += t
         if est >= budget_s:
             break
+    if not chosen:
+        chosen = [int(np.argmin(lens))]
     prob, sl = oracle_problem(inp, chosen)
     t0 = time.perf_counter()
     prob.attention(n_threads=threads)
@@ -904,11 +921,13 @@ def bench_reference(args):
         sms, l2_note = 152, "no GPU visible"
     config = workload_config(w, int(inp["seq_lens"].shape[0]), w.num_ctas(sms), args.min_tiles, kv_bytes(inp),
                              l2_note, world)
-    per_step = max(0.5, 150.0 / (args.steps + args.warmup))
+    # about 150 s of oracle work over the whole run, whatever K and W are
+    per_step = 150.0 / (args.steps + args.warmup)
+    per_token = oracle_seconds_per_token(inp, oracle.default_threads())
     rates = []
     desc = ""
     for k in range(args.warmup + args.steps):
-        v, cores, desc = cpu_oracle_rate(inp, per_step, rng_seed=k)
+        v, cores, desc = cpu_oracle_rate(inp, per_step, rng_seed=k, per_token=per_token, fit=True)
         if k >= args.warmup:
             rates.append(v)
     v = float(np.mean(rates))
