@@ -51,3 +51,23 @@ def test_reference_arm_nonzero_rank_does_nothing(monkeypatch, capsys):
     monkeypatch.setattr("sys.argv", ["bench.py", "--impl", "reference", "--gpus", "2"])
     bench.main()
     assert capsys.readouterr().out == ""
+
+
+def test_reference_step_samples_stay_within_small_budgets():
+    """The reference arm sizes each step's oracle sample to its share of a fixed total: with a
+    budget no request fits, a step takes the shortest request alone; a larger budget takes
+    more requests, never one whose estimated time would overrun it."""
+    import bench
+    import workloads
+    inp = workloads.make_workload("tiny", device="cpu")
+    per_token = bench.oracle_seconds_per_token(inp, 2)
+    v, cores, desc = bench.cpu_oracle_rate(inp, 1e-9, rng_seed=0, threads=2, per_token=per_token, fit=True)
+    assert v > 0 and cores == 2
+    assert desc.startswith("1 of 4 requests (17 of ")  # the shortest length is 17
+    lens = inp["seq_lens"].numpy()
+    eff = min(2, inp["num_kv_heads"] * len(lens))
+    budget = per_token * (17 + 200) * inp["num_kv_heads"] / eff  # room for the two shortest
+    _, _, desc = bench.cpu_oracle_rate(inp, budget * 1.0001, rng_seed=3, threads=2, per_token=per_token, fit=True)
+    n = int(desc.split(" ")[0])
+    tokens = int(desc.split("(")[1].split(" ")[0])
+    assert 1 <= n <= 2 and tokens <= 17 + 200
